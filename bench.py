@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one chunkwise prefill over the batch B=4, H=16, T=4096,
+d_k=d_v=128 (bf16 q/k/v, fp32 gates and state, S0 = 0): every token of every
+head goes through the full path. Inputs are resident in HBM when the timed
+region starts and are larger than L2 (0.34 GB of inputs, 0.4 GB moved per
+step vs a 129 MB L2), so back-to-back steps read from HBM.
+
+Prints ONE JSON line (rank 0). Keys beyond the basic contract:
+  roofline      the prefill kernel against the measured HBM copy bandwidth
+                (algorithmic bytes per launch / mean launch time)
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample
+  e2e           the same metric through the public API with host buffers,
+                host<->device copies inside the timed region
+  decode        the decode step on 256 sequences x 32 heads (state GB/s)
+  clocks        SM clocks and throttle reasons sampled during the timed region
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torchrun (one process per GPU, independent batches:
+weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (% bf16 TC peak); decode step state GB/s (% HBM peak)"
+B, H, T, DK, DV, CHUNK = 4, 16, 4096, 128, 128, 64
+DEC_N, DEC_H = 256, 32
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def prefill_bytes(B, T, H, dk, dv, qkv_bytes=2, with_s0=False):
+    """Algorithmic HBM bytes of one prefill call: q, k, v, alpha, beta read
+    once, o written once, final state written once (and S0 read if given)."""
+    per_tok_head = 2 * dk * qkv_bytes + dv * qkv_bytes + dk * 4 + 4 + dv * qkv_bytes
+    state = B * H * dk * dv * 4
+    return B * T * H * per_tok_head + state * (2 if with_s0 else 1)
+
+
+def prefill_flops(B, T, H, dk, dv, C=CHUNK):
+    """Algorithmic flops per token-head of the chunked form: the three
+    d_k x d_v products (state read-outs X, Y and the state update), the
+    triangular halves of the intra-chunk products, the substitution."""
+    f = 6 * dk * dv + (C - 1) * (2 * dk + dv) + (C + 1) * (dk + dv) + C * C / 3
+    return B * T * H * f
+
+
+def decode_bytes(N, H, dk, dv, qkv_bytes=2):
+    return N * H * (2 * dk * dv * 4 + 2 * dk * qkv_bytes + dv * qkv_bytes + dk * 4 + 4 + dv * qkv_bytes)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "kda_gated_delta_chunkwise_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent.get("bytes_per_launch") if ent.get("source_sha") == sha else None
+
+
+def cpu_baseline_oracle(target_s: float = 12.0):
+    """Time the float64 oracle on a bounded sample of the prefill workload: all
+    B*H = 64 (sequence, head) pairs over the first Ts tokens, with Ts chosen so
+    the timed run takes about target_s seconds on the host cores."""
+    import oracle
+    from kda_gated_delta_chunkwise_gb300 import workloads as W
+
+    x = W.prefill_4x16x4096(T=4096)
+    cores = oracle.max_threads()
+    lib = oracle.load()
+
+    def run(Ts):
+        args = [t[:, :Ts] for t in x.tensors()]
+        t0 = time.perf_counter()
+        oracle.run(*args, lib=lib)
+        return time.perf_counter() - t0
+
+    Ts = 64
+    dt = run(Ts)
+    Ts = int(min(4096, max(64, Ts * target_s / max(dt, 1e-3))))
+    dt = run(Ts)
+    return {"value": B * Ts / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"B={B} x H={H} (all 64 sequence-head pairs) x first {Ts} of {T} tokens, "
+                      f"d={DK}, float64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the float64 oracle on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from kda_gated_delta_chunkwise_gb300 import workloads as W
+
+    x = W.prefill_4x16x4096(T=4096)
+    Ts = 128
+    sl = [t[:, :Ts] for t in x.tensors()]
+    lib = oracle.load()
+    cores = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.run(*sl, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(*sl, lib=lib)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    val = B * Ts / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"kda_prefill B={B} H={H} T={T} d_k={DK} d_v={DV} bf16 inputs",
+                       "sample": f"each step: all 64 sequence-head pairs, first {Ts} tokens"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"B={B} x H={H} x first {Ts} tokens per step"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    import kda_gated_delta_chunkwise_gb300 as kda
+    from kda_gated_delta_chunkwise_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    kda.load()
+    peaks, peak_src = load_peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- inputs (seeded; each rank its own batch) ----
+    x = W.prefill_4x16x4096(seed=rank)
+    q, k, v, a, b = (t.to(dev) for t in x.tensors())
+    o = torch.empty_like(v)
+    sT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.prefill(q, k, v, a, b, None, out=o, final_state=sT, algo=args.algo)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * B * T / (ms_per_step / 1e3)
+
+    algo_bytes = prefill_bytes(B, T, H, DK, DV)
+    algo_flops = prefill_flops(B, T, H, DK, DV)
+    achieved = algo_bytes / (launch_ms / 1e3) / 1e9
+    tflops = algo_flops / (launch_ms / 1e3) / 1e12
+    used_tc = args.algo == "tc" or (args.algo == "auto" and kda_uses_tc(kda, dev))
+    kfile = "kda_prefill_tc.cu" if used_tc else "kda_prefill_simt.cu"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": kernel_traffic(kfile, "prefill_tc" if used_tc else "prefill_simt"),
+                "peak_source": f"{peak_src} STREAM-style copy (hbm_gbs)",
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "kernel": "kda_prefill_tc" if used_tc else "kda_prefill_simt",
+                "tflops_algorithmic": tflops,
+                "tensor_frac": tflops / peaks["bf16_tflops"]}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, ha, hb = (t.pin_memory() for t in x.tensors())
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb))
+        d2h = o.numel() * o.element_size() + sT.numel() * 4
+        for _ in range(2):
+            kda.prefill(hq, hk, hv, ha, hb, None, algo=args.algo)
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            oh, sh = kda.prefill(hq, hk, hv, ha, hb, None, algo=args.algo)  # returns host tensors
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / n_e2e
+        if world > 1:
+            tt = torch.tensor([dt], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dt = float(tt.item())
+        e2e = {"value": world * B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+
+    # ---- decode step (secondary figure of the metric) ----
+    decode = None
+    if not args.no_decode:
+        del q, k, v, a, b, o, sT
+        xd = W.decode_256x32(seed=rank)
+        dq, dk_, dv_, da, db = (t.to(dev) for t in xd.tensors())
+        state = xd.initial_state.to(dev)
+        do = torch.empty_like(dv_)
+        for _ in range(args.warmup):
+            kda.decode_step(dq, dk_, dv_, da, db, state, out=do)
+        torch.cuda.synchronize()
+        evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            evd[i][0].record(stream)
+            kda.decode_step(dq, dk_, dv_, da, db, state, out=do)
+            evd[i][1].record(stream)
+        torch.cuda.synchronize()
+        dms = statistics.median(s.elapsed_time(e) for s, e in evd)
+        dbytes = decode_bytes(DEC_N, DEC_H, DK, DV)
+        gbs = dbytes / (dms / 1e3) / 1e9
+        decode = {"metric": "decode step state GB/s", "value": gbs, "unit": "GB/s",
+                  "ms_per_step": dms, "frac": gbs / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
+                  "algorithmic_bytes_per_step": dbytes,
+                  "traffic": kernel_traffic("kda_decode.cu", "decode"),
+                  "workload": f"{DEC_N} sequences x {DEC_H} heads, d={DK}, bf16 q/k/v, fp32 state in place"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"kda_prefill B={B} H={H} T={T} d_k={DK} d_v={DV} chunk={CHUNK}",
+                           "inputs": "bf16 q/k/v (q, k L2-normalised), fp32 alpha/beta, fp32 state, S0 = 0",
+                           "l2": "inputs larger than L2 (0.34 GB in, 0.41 GB moved per step; L2 129 MB)",
+                           "parallelism": f"{world} independent replica(s)"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+                "gpu_launches": args.steps, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def kda_uses_tc(kda, dev) -> bool:
+    """Whether the automatic choice takes the tensor-core kernel for this
+    workload: the library answers an explicit tensor-core request on an empty
+    batch with KDA_OK exactly when that kernel supports the shape and dtype."""
+    import ctypes
+    lib = kda.load()
+    p = ctypes.c_void_p(256)
+    return lib.kda_prefill_ex(p, p, p, 1, p, p, None, p, None, 0, T, H, DK, DV, 2, None) == 0
+
+
+if __name__ == "__main__":
+    main()

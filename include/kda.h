@@ -1,0 +1,148 @@
+/*
+ * kda.h - C ABI of the KDA (Kimi Delta Attention) library for GB300 (sm_103a).
+ *
+ * The method is the per-channel gated delta rule of the web page
+ * "研究KimiK3，我发现大模型正在学会“管理自己的计算”" (pwwt.cn/news/3763336),
+ * called "the K3 essay" below. Per sequence and head, for t = 1..T:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T   (§四)
+ *     o_t = S_t^T q_t                                                         (§二.1)
+ *
+ * with S a d_k x d_v float32 state, alpha_t in [0,1]^{d_k} a per-channel gate
+ * and beta_t a scalar write strength. Prefill evaluates it chunk by chunk in
+ * the WY form of §六 (chunks of 64 tokens: state passed between chunks, the
+ * tokens inside a chunk handled as a few dense products); decode applies one
+ * token in place.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte
+ *    aligned. The caller owns every buffer; the library allocates nothing, never
+ *    synchronises the stream, and launches all its work on `stream`.
+ *  - Layouts: q, k, alpha [.., T, H, d_k]; v, o [.., T, H, d_v]; beta [.., T, H];
+ *    states [N, H, d_k, d_v] with d_v fastest. alpha and beta are float32;
+ *    q, k, v and o share `qkv_dtype`; states are float32.
+ *  - Supported: d_k, d_v in {64, 128}. Other sizes return KDA_ERR_UNSUPPORTED.
+ *  - Gates: alpha is used as given (linear, not log); alpha = 0 is allowed and
+ *    erases the channel. beta may be any finite value.
+ *  - Errors: argument checks run before any launch and return a status with
+ *    nothing launched; the message is in kda_last_error() (per thread).
+ *    A failed launch returns KDA_ERR_CUDA. Device-side checks never trap: they
+ *    write a code to a caller-visible status word and skip the work.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer   */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d_k = 96)   */
+    KDA_ERR_CUDA = 3,          /* a CUDA call or launch failed                */
+    KDA_ERR_DEVICE_CHECK = 4,  /* a device-side check failed (status word)    */
+    KDA_ERR_WORKSPACE = 5      /* workspace missing or too small              */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Prefill implementation choice (kda_prefill picks KDA_ALGO_AUTO). */
+typedef enum {
+    KDA_ALGO_AUTO = 0,  /* tensor-core path for bf16 d=128, SIMT otherwise       */
+    KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunk kernel (any supported dtype/d)   */
+    KDA_ALGO_TC = 2     /* tcgen05/TMEM chunk kernel: bf16, d_k = d_v = 128 only */
+} kda_algo_t;
+
+/* Device-side status codes written to `device_status` by kda_varlen_prefill. */
+#define KDA_DEV_OK 0
+#define KDA_DEV_BAD_CU_SEQLENS 1   /* cu[0] != 0, decreasing, or cu[N] != T_total */
+
+/*
+ * kda_prefill - chunkwise prefill of B equal-length sequences (K3 essay §四
+ * update, evaluated with §六's chunking and WY form).
+ *
+ *   q, k         [B, T, H, d_k]  qkv_dtype          (read)
+ *   v            [B, T, H, d_v]  qkv_dtype          (read)
+ *   alpha        [B, T, H, d_k]  float32, in [0,1]  (read)
+ *   beta         [B, T, H]       float32            (read)
+ *   initial_state[B, H, d_k, d_v] float32 or NULL (zeros)            (read)
+ *   o            [B, T, H, d_v]  qkv_dtype: o_t = S_t^T q_t          (written)
+ *   final_state  [B, H, d_k, d_v] float32 or NULL (not written)      (written)
+ *
+ * final_state may equal initial_state (updated in place). T = 0 copies the
+ * initial state (or zeros) to final_state. Returns KDA_OK once the work is
+ * queued on `stream`.
+ */
+kda_status_t kda_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                         const float *alpha, const float *beta, const float *initial_state,
+                         void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
+                         kda_stream_t stream);
+
+/* kda_prefill with an explicit implementation choice (KDA_ALGO_TC on an
+ * unsupported dtype or size returns KDA_ERR_UNSUPPORTED). */
+kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                            const float *alpha, const float *beta, const float *initial_state,
+                            void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
+                            kda_algo_t algo, kda_stream_t stream);
+
+/*
+ * kda_varlen_prefill - prefill of N sequences packed along the token axis.
+ * Sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 and runs its own
+ * recurrence from its own initial state, with its own chunk grid starting at
+ * its first token; results are bitwise equal to kda_prefill on that sequence
+ * alone.
+ *
+ *   q, k, alpha  [T_total, H, d_k];  v, o [T_total, H, d_v];  beta [T_total, H]
+ *   cu_seqlens   [N + 1] int32, DEVICE memory; must start at 0, never decrease
+ *                and end at T_total (checked on the device).
+ *   initial_state / final_state  [N, H, d_k, d_v] float32, nullable as above.
+ *   workspace    device scratch of at least kda_varlen_workspace_bytes(N, H,
+ *                d_k, d_v) bytes, 256-byte aligned; its contents on entry do
+ *                not matter. Calls sharing a workspace must not overlap.
+ *   device_status DEVICE int32 or NULL: set to KDA_DEV_OK or a KDA_DEV_* code
+ *                when the call's kernels run; on a code, no o or state is
+ *                written by this call.
+ */
+kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                const float *alpha, const float *beta,
+                                const float *initial_state, void *o, float *final_state,
+                                const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
+                                int d_v, void *workspace, size_t workspace_bytes,
+                                int32_t *device_status, kda_stream_t stream);
+
+/* Workspace bytes kda_varlen_prefill needs for N sequences (0 < result). */
+size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
+
+/*
+ * kda_decode_step - one recurrent step per (sequence, head), in place
+ * (K3 essay §四 update for a single token, §二.1 read-out):
+ *     S' = Diag(alpha) S;  e = beta (v - S'^T k);  S <- S' + k e^T;  o = S^T q
+ *
+ *   q, k   [N, H, d_k] qkv_dtype;  v, o [N, H, d_v] qkv_dtype
+ *   alpha  [N, H, d_k] float32;    beta [N, H] float32
+ *   state  [N, H, d_k, d_v] float32, read and overwritten in place
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                             const float *alpha, const float *beta, float *state, void *o,
+                             int N, int H, int d_k, int d_v, kda_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *kda_last_error(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int kda_abi_version(void);
+
+#define KDA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,13 @@
+"""KDA (Kimi Delta Attention) gated-delta recurrence for GB300 (sm_103a).
+
+Per sequence and head, S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1}
++ beta_t k_t v_t^T and o_t = S_t^T q_t (the web page
+"研究KimiK3，我发现大模型正在学会“管理自己的计算”", pwwt.cn, §四 and §二.1).
+
+Entry points (thin ctypes binding over the C ABI in include/kda.h):
+``prefill``, ``varlen_prefill``, ``decode_step``. Build the CUDA library with
+``kda_gated_delta_chunkwise_gb300.build.build()`` first.
+"""
+from ._binding import (ALGOS, EXPORTS, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_OK, KdaError,  # noqa: F401
+                       decode_step, lib_path, load, prefill, varlen_prefill,
+                       varlen_workspace_bytes)

@@ -1,0 +1,237 @@
+"""ctypes binding of the KDA C ABI (include/kda.h).
+
+Argument marshalling only: shape and dtype checks, output allocation through
+PyTorch, the raw pointers and the current CUDA stream. Every step of the
+method runs in the library's CUDA kernels. There is no fallback: if the
+shared library is missing or fails to load, every call raises.
+
+Inputs on the host (CPU tensors) are accepted for end-to-end use: they are
+copied to the current CUDA device, the call runs there, and the outputs are
+copied back to the host.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_CHECK, KDA_ERR_WORKSPACE = range(6)
+KDA_F32, KDA_BF16 = 0, 1
+ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS = 0, 1
+
+EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_varlen_prefill", "kda_varlen_workspace_bytes",
+           "kda_decode_step", "kda_last_error", "kda_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"KDA error {status}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the shared library (it must have been built: ``build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"KDA CUDA library not built ({p}); run the package build first")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+        lib.kda_prefill_ex.restype = ctypes.c_int
+        lib.kda_prefill_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.kda_prefill.restype = ctypes.c_int
+        lib.kda_prefill.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.kda_varlen_prefill.restype = ctypes.c_int
+        lib.kda_varlen_prefill.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                           vp, ctypes.c_size_t, vp, vp]
+        lib.kda_varlen_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_varlen_workspace_bytes.argtypes = [i, i, i, i]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_abi_version.restype = ctypes.c_int
+        lib.kda_abi_version.argtypes = []
+        del f
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int):
+    if status != KDA_OK:
+        raise KdaError(status, lib.kda_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _host_call(fn, tensors: dict, **kw):
+    """Run ``fn`` on the CUDA device for host inputs; return host outputs."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    moved = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in tensors.items()}
+    out = fn(**moved, **kw)
+    if isinstance(out, tuple):
+        return tuple(None if x is None else x.to("cpu") for x in out)
+    return out.to("cpu")
+
+
+def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: bool = True,
+            algo: str = "auto", out=None, final_state=None, stream=None):
+    """Chunkwise KDA prefill of B equal-length sequences.
+
+    q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, same dtype);
+    alpha: [B, T, H, d_k] fp32; beta: [B, T, H] fp32;
+    initial_state: [B, H, d_k, d_v] fp32 or None (zeros).
+    Returns (o [B, T, H, d_v] in v's dtype, final_state [B, H, d_k, d_v] fp32 or None).
+    """
+    if q.device.type == "cpu":
+        return _host_call(prefill, dict(q=q, k=k, v=v, alpha=alpha, beta=beta,
+                                        initial_state=initial_state),
+                          output_final_state=output_final_state, algo=algo)
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(alpha, "alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or alpha.shape != q.shape or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch among q, k, v, alpha, beta")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev)
+        if initial_state.shape != (B, H, dk, dv):
+            raise ValueError(f"initial_state must be {(B, H, dk, dv)}")
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    if algo not in ALGOS:
+        raise ValueError(f"algo must be one of {sorted(ALGOS)}")
+    st = lib.kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
+                            _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
+                            ALGOS[algo], _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def varlen_workspace_bytes(N: int, H: int, dk: int = 128, dv: int = 128) -> int:
+    return int(load().kda_varlen_workspace_bytes(N, H, dk, dv))
+
+
+def varlen_prefill(q, k, v, alpha, beta, cu_seqlens, initial_state=None, *,
+                   output_final_state: bool = True, out=None, final_state=None, workspace=None,
+                   device_status=None, stream=None):
+    """KDA prefill of sequences packed along the token axis.
+
+    q, k, alpha: [T_total, H, d_k]; v: [T_total, H, d_v]; beta: [T_total, H];
+    cu_seqlens: int32 [N + 1]; initial_state: [N, H, d_k, d_v] fp32 or None.
+    Returns (o, final_state). ``device_status`` (int32 [1] on the device), when
+    given, receives the device-side check result.
+    """
+    if q.device.type == "cpu":
+        return _host_call(varlen_prefill, dict(q=q, k=k, v=v, alpha=alpha, beta=beta,
+                                               cu_seqlens=cu_seqlens, initial_state=initial_state),
+                          output_final_state=output_final_state)
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(alpha, "alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    Tt, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if k.shape != q.shape or v.shape != (Tt, H, dv) or alpha.shape != q.shape or beta.shape != (Tt, H):
+        raise ValueError("shape mismatch among q, k, v, alpha, beta")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev)
+        if initial_state.shape != (N, H, dk, dv):
+            raise ValueError(f"initial_state must be {(N, H, dk, dv)}")
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    nbytes = int(lib.kda_varlen_workspace_bytes(N, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib.kda_varlen_prefill(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
+                                _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(cu_seqlens),
+                                N, Tt, H, dk, dv, _ptr(workspace), workspace.numel(),
+                                _ptr(device_status), _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def decode_step(q, k, v, alpha, beta, state, *, out=None, stream=None):
+    """One recurrent KDA step per (sequence, head); ``state`` is updated in place.
+
+    q, k: [N, H, d_k]; v: [N, H, d_v]; alpha: [N, H, d_k] fp32; beta: [N, H] fp32;
+    state: [N, H, d_k, d_v] fp32. Returns o [N, H, d_v].
+    """
+    if q.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        st_dev = state.to(dev)
+        o = decode_step(q.to(dev), k.to(dev), v.to(dev), alpha.to(dev), beta.to(dev), st_dev)
+        state.copy_(st_dev.to("cpu"))
+        return o.to("cpu")
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(alpha, "alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(state, "state", torch.float32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (N, H, dv) or alpha.shape != q.shape or beta.shape != (N, H) \
+            or state.shape != (N, H, dk, dv):
+        raise ValueError("shape mismatch among q, k, v, alpha, beta, state")
+    if out is None:
+        out = torch.empty_like(v)
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
+                             _ptr(state), _ptr(out), N, H, dk, dv, _stream(stream))
+    _check(lib, st)
+    return out

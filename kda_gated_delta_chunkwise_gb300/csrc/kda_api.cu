@@ -1,0 +1,200 @@
+// Host side of the C ABI declared in include/kda.h: argument checks, kernel
+// choice and launches. Nothing here allocates, synchronises or reads device
+// memory; every check happens before the first launch of a call.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kda_status_t fail(kda_status_t st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kda_status_t ok() {
+    g_last_error.clear();
+    return KDA_OK;
+}
+
+kda_status_t cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return ok();
+    return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status_t check_dims(int H, int dk, int dv) {
+    if (H <= 0) return fail(KDA_ERR_INVALID_ARG, "H must be positive (got %d)", H);
+    if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARG, "d_k, d_v must be positive");
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128))
+        return fail(KDA_ERR_UNSUPPORTED, "d_k, d_v must be 64 or 128 (got %d, %d)", dk, dv);
+    return KDA_OK;
+}
+
+kda_status_t check_dtype(kda_dtype_t dt) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return fail(KDA_ERR_INVALID_ARG, "unknown qkv dtype %d", (int)dt);
+    return KDA_OK;
+}
+
+#define KDA_REQUIRE_PTR(p)                                                                  \
+    do {                                                                                    \
+        if (!(p)) return fail(KDA_ERR_INVALID_ARG, "%s must not be NULL", #p);              \
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p); \
+    } while (0)
+#define KDA_OPTIONAL_PTR(p)                                                                 \
+    do {                                                                                    \
+        if ((p) && !aligned16(p))                                                           \
+            return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);             \
+    } while (0)
+
+kda_status_t check_tensors(const void *q, const void *k, const void *v, const float *alpha,
+                           const float *beta, const void *o, const float *s0, const float *sT,
+                           bool any_tokens) {
+    if (any_tokens) {
+        KDA_REQUIRE_PTR(q);
+        KDA_REQUIRE_PTR(k);
+        KDA_REQUIRE_PTR(v);
+        KDA_REQUIRE_PTR(alpha);
+        if (!beta) return fail(KDA_ERR_INVALID_ARG, "beta must not be NULL");
+        if (reinterpret_cast<uintptr_t>(beta) & 3u) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
+        KDA_REQUIRE_PTR(o);
+    }
+    KDA_OPTIONAL_PTR(s0);
+    KDA_OPTIONAL_PTR(sT);
+    return KDA_OK;
+}
+
+kda_status_t run_prefill(const kda::PrefillArgs &a, kda_algo_t algo, cudaStream_t s) {
+    bool use_tc;
+    switch (algo) {
+        case KDA_ALGO_AUTO: use_tc = kda::prefill_tc_supported(a); break;
+        case KDA_ALGO_SIMT: use_tc = false; break;
+        case KDA_ALGO_TC:
+            if (!kda::prefill_tc_supported(a))
+                return fail(KDA_ERR_UNSUPPORTED,
+                            "the tensor-core prefill needs bf16 q/k/v and d_k = d_v = 128");
+            use_tc = true;
+            break;
+        default: return fail(KDA_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+    }
+    return cuda_status(use_tc ? kda::launch_prefill_tc(a, s) : kda::launch_prefill_simt(a, s),
+                       use_tc ? "tensor-core prefill launch" : "prefill launch");
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_last_error(void) { return g_last_error.c_str(); }
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                            const float *alpha, const float *beta, const float *initial_state,
+                            void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
+                            kda_algo_t algo, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
+    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state,
+                            (int64_t)B * T > 0)) != KDA_OK)
+        return st;
+    kda::PrefillArgs a{};
+    a.dt = qkv_dtype; a.dk = d_k; a.dv = d_v;
+    if (algo == KDA_ALGO_TC && !kda::prefill_tc_supported(a))
+        return fail(KDA_ERR_UNSUPPORTED, "the tensor-core prefill needs bf16 q/k/v and d_k = d_v = 128");
+    if (B == 0) return ok();
+    if (T == 0 && !final_state) return ok();
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = initial_state;
+    a.o = o; a.sT = final_state; a.cu_seqlens = nullptr;
+    a.N = B; a.T = T; a.H = H; a.dk = d_k; a.dv = d_v; a.dt = qkv_dtype;
+    a.order = nullptr; a.counter = nullptr; a.dev_status = nullptr;
+    return run_prefill(a, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                         const float *alpha, const float *beta, const float *initial_state,
+                         void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
+                         kda_stream_t stream) {
+    return kda_prefill_ex(q, k, v, qkv_dtype, alpha, beta, initial_state, o, final_state, B, T, H,
+                          d_k, d_v, KDA_ALGO_AUTO, stream);
+}
+
+size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v) {
+    (void)H; (void)d_k; (void)d_v;
+    const size_t n = N > 0 ? (size_t)N : 0;
+    return align_up(n * sizeof(int32_t)) + kAlign;  // order[N] | counter, status
+}
+
+kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                const float *alpha, const float *beta,
+                                const float *initial_state, void *o, float *final_state,
+                                const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
+                                int d_v, void *workspace, size_t workspace_bytes,
+                                int32_t *device_status, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (N < 0 || T_total < 0) return fail(KDA_ERR_INVALID_ARG, "N and T_total must be >= 0");
+    if (N == 0) return ok();
+    if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+    if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state, T_total > 0)) != KDA_OK)
+        return st;
+    const size_t need = kda_varlen_workspace_bytes(N, H, d_k, d_v);
+    if (!workspace || workspace_bytes < need)
+        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return fail(KDA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *order = reinterpret_cast<int32_t *>(ws);
+    int32_t *tail = reinterpret_cast<int32_t *>(ws + align_up((size_t)N * sizeof(int32_t)));
+    int32_t *counter = tail;
+    int32_t *status = device_status ? device_status : tail + 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    cudaError_t e = kda::launch_varlen_prep(cu_seqlens, N, T_total, order, counter, status, s);
+    if (e != cudaSuccess) return cuda_status(e, "varlen prep launch");
+
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = initial_state;
+    a.o = o; a.sT = final_state; a.cu_seqlens = cu_seqlens;
+    a.N = N; a.T = T_total; a.H = H; a.dk = d_k; a.dv = d_v; a.dt = qkv_dtype;
+    a.order = order; a.counter = counter; a.dev_status = status;
+    return run_prefill(a, KDA_ALGO_AUTO, s);
+}
+
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                             const float *alpha, const float *beta, float *state, void *o,
+                             int N, int H, int d_k, int d_v, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (N < 0) return fail(KDA_ERR_INVALID_ARG, "N must be >= 0");
+    if (N == 0) return ok();
+    if ((int64_t)N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N * H must fit in int32");
+    if ((st = check_tensors(q, k, v, alpha, beta, o, nullptr, nullptr, true)) != KDA_OK) return st;
+    KDA_REQUIRE_PTR(state);
+    return cuda_status(kda::launch_decode(q, k, v, qkv_dtype, alpha, beta, state, o, N, H, d_k, d_v,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                       "decode launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// Internal declarations shared by the host layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Element loads/stores for the two input dtypes.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_decode(const void *q, const void *k, const void *v, kda_dtype_t dt,
+                          const float *alpha, const float *beta, float *state, void *o,
+                          int N, int H, int dk, int dv, cudaStream_t s);
+
+// Prefill over sequences given by cu_seqlens (device) or, when cu_seqlens is
+// null, B equal sequences of T tokens. `order` (device, nullable) lists the
+// (sequence, head) work items to run, longest first; `counter` (device,
+// nullable) is a zeroed work counter for persistent scheduling.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *alpha, *beta, *s0;
+    void *o;
+    float *sT;
+    const int32_t *cu_seqlens;  // null: equal lengths
+    int N, T, H, dk, dv;        // T: tokens per sequence (equal) or T_total (packed)
+    kda_dtype_t dt;
+    const int32_t *order;       // nullable: sequence order (longest first)
+    int32_t *counter;           // nullable: persistent work counter
+    const int32_t *dev_status;  // nullable: skip all work when *dev_status != 0
+};
+
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+bool prefill_tc_supported(const PrefillArgs &a);
+
+// Varlen preparation: validates cu_seqlens, writes the status word, sorts the
+// sequences by length (longest first) into `order` and zeroes `counter`.
+cudaError_t launch_varlen_prep(const int32_t *cu_seqlens, int N, int T_total, int32_t *order,
+                               int32_t *counter, int32_t *status, cudaStream_t s);
+
+}  // namespace kda

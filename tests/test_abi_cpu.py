@@ -1,0 +1,114 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+function include/kda.h declares, and argument checks reject bad calls before
+any CUDA work (no kernel is launched by these tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kda_gated_delta_chunkwise_gb300 as kda
+from kda_gated_delta_chunkwise_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fname in os.listdir(os.path.join(ROOT, "include")):
+        if fname.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fname)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(kda_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kda.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kda_prefill", "kda_varlen_prefill", "kda_decode_step", "kda_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    for name in kda.EXPORTS:
+        assert hasattr(lib, name)
+
+
+def test_abi_version(lib):
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    ver = int(re.search(r"#define KDA_ABI_VERSION (\d+)", text).group(1))
+    assert lib.kda_abi_version() == ver
+
+
+def _prefill(lib, dk=128, dv=128, B=1, T=4, H=1, ptr=0x1000, algo=0, dtype=1, beta_ptr=None):
+    p = ctypes.c_void_p(ptr)
+    b = ctypes.c_void_p(ptr if beta_ptr is None else beta_ptr)
+    return lib.kda_prefill_ex(p, p, p, dtype, p, b, None, p, None, B, T, H, dk, dv, algo, None)
+
+
+def test_unsupported_head_size_is_rejected_before_launch(lib):
+    assert _prefill(lib, dk=96) == 2
+    assert b"64 or 128" in lib.kda_last_error()
+    assert _prefill(lib, dv=256) == 2
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    assert _prefill(lib, ptr=0) == 1
+    assert b"must not be NULL" in lib.kda_last_error()
+    assert _prefill(lib, ptr=0x1004) == 1
+    assert b"16-byte aligned" in lib.kda_last_error()
+    assert _prefill(lib, beta_ptr=0x1002) == 1
+
+
+def test_bad_sizes_and_enums(lib):
+    assert _prefill(lib, B=-1) == 1
+    assert _prefill(lib, H=0) == 1
+    assert _prefill(lib, dtype=7) == 1
+    assert _prefill(lib, algo=9) == 1
+
+
+def test_tensor_core_path_rejects_fp32(lib):
+    assert _prefill(lib, algo=2, dtype=0) == 2
+
+
+def test_empty_batches_are_no_ops(lib):
+    # B = 0 or T = 0 without a final state: nothing to do, nothing launched
+    assert _prefill(lib, B=0) == 0
+    assert _prefill(lib, T=0) == 0
+
+
+def test_varlen_argument_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    ws = lib.kda_varlen_workspace_bytes(64, 16, 128, 128)
+    assert ws >= 64 * 4 and ws % 256 == 0
+    # no workspace
+    st = lib.kda_varlen_prefill(p, p, p, 1, p, p, None, p, None, p, 64, 1000, 16, 128, 128,
+                                None, 0, None, None)
+    assert st == 5
+    # misaligned workspace
+    st = lib.kda_varlen_prefill(p, p, p, 1, p, p, None, p, None, p, 64, 1000, 16, 128, 128,
+                                ctypes.c_void_p(0x1010), ws, None, None)
+    assert st == 5
+    # missing cu_seqlens
+    st = lib.kda_varlen_prefill(p, p, p, 1, p, p, None, p, None, None, 64, 1000, 16, 128, 128,
+                                p, ws, None, None)
+    assert st == 1
+    # zero sequences: nothing to do
+    st = lib.kda_varlen_prefill(None, None, None, 1, None, None, None, None, None, None, 0, 0, 16,
+                                128, 128, None, 0, None, None)
+    assert st == 0
+
+
+def test_decode_argument_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    assert lib.kda_decode_step(p, p, p, 1, p, p, None, p, 4, 2, 128, 128, None) == 1
+    assert lib.kda_decode_step(p, p, p, 1, p, p, p, p, 4, 2, 80, 128, None) == 2
+    assert lib.kda_decode_step(p, p, p, 1, p, p, p, p, 0, 2, 128, 128, None) == 0

@@ -1,0 +1,146 @@
+"""GPU parity of kda_prefill against the float64 oracle.
+
+Small cases span several 64-token chunks and a ragged tail and are checked
+element by element on every output; the full-size workloads run in the
+launch configuration the benchmark uses and are checked on every output
+(4x16x4096) or on sampled heads (131k tokens), where the oracle evaluates
+the sampled (sequence, head) recurrences in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kda_gated_delta_chunkwise_gb300 import workloads as W
+from _parity import assert_close, tol_for
+
+pytestmark = pytest.mark.gpu
+ALGOS_BF16 = ["simt", "auto"]
+
+
+def _dev(x: W.Inputs):
+    d = torch.device("cuda")
+    s0 = None if x.initial_state is None else x.initial_state.to(d)
+    return [t.to(d) for t in x.tensors()] + [s0]
+
+
+def _check(kda, x: W.Inputs, algo="auto", heads=None):
+    q, k, v, a, b, s0 = _dev(x)
+    o, s = kda.prefill(q, k, v, a, b, s0, algo=algo)
+    torch.cuda.synchronize()
+    o, s = o.cpu(), s.cpu()
+    qc, kc, vc, ac, bc = x.tensors()
+    S0 = x.initial_state
+    if heads is not None:  # sampled (b, h) pairs, each run in full by the oracle
+        for (bi, h) in heads:
+            sl = (slice(bi, bi + 1), slice(None), slice(h, h + 1))
+            ro, rs = oracle.run(qc[sl], kc[sl], vc[sl], ac[sl], bc[sl],
+                                initial_state=None if S0 is None else S0[bi:bi + 1, h:h + 1])
+            tol = tol_for(x.q.dtype)
+            assert_close(f"o[{bi},:,{h}]", o[sl], ro, tol)
+            assert_close(f"S[{bi},{h}]", s[bi:bi + 1, h:h + 1], rs, tol)
+        return
+    ro, rs = oracle.run(qc, kc, vc, ac, bc, initial_state=S0)
+    tol = tol_for(x.q.dtype)
+    assert_close("o", o, ro, tol)
+    assert_close("final_state", s, rs, tol)
+
+
+def test_fwd_fp32_small(kda):
+    """B=1, H=1, T=256, d=64, fp32: rel-L2 <= 1e-4."""
+    _check(kda, W.fwd_fp32_small())
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_small_ragged_bf16(kda, algo):
+    x = W.batched(2, 1000, 3, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=11)
+    _check(kda, x, algo)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 130])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_ragged_lengths(kda, T, dtype):
+    x = W.batched(2, T, 2, 128, 128, dtype=dtype, alpha_scale=0.2, s0_std=0.05, seed=T)
+    _check(kda, x)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_head_sizes(kda, dk, dv):
+    x = W.batched(1, 200, 2, dk, dv, dtype="fp32", alpha_scale=0.1, s0_std=0.05, seed=dk * 3 + dv)
+    _check(kda, x)
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_prefill_4x16x4096_full(kda, algo):
+    """The benchmark workload: B=4, H=16, T=4096, d=128, bf16, every output."""
+    _check(kda, W.prefill_4x16x4096(), algo)
+
+
+@pytest.mark.slow
+def test_prefill_long_131k_sampled(kda):
+    """B=1, H=32, T=131072, d=128, split decay scales, S0 ~ N(0, 0.01^2);
+    four heads evaluated in full by the oracle."""
+    _check(kda, W.prefill_long_131k(), heads=[(0, 0), (0, 7), (0, 20), (0, 31)])
+
+
+def test_strong_decay_and_zero_gates(kda):
+    """Chunks whose gates decay past the factorised range (alpha = 0 tokens,
+    tiny alpha) take the exact token-by-token route; results still match."""
+    x = W.batched(1, 300, 2, 128, 128, dtype="fp32", alpha_scale=0.1, s0_std=0.05, seed=5)
+    x.alpha[0, 10, 0, :] = 0.0          # full erase of head 0 at token 10
+    x.alpha[0, 70:90, 1, 5] = 1e-3      # one channel of head 1 decays by e^-138
+    x.alpha[0, 200:264, 0, :64] = 0.2   # e^-103 over one chunk, half the channels
+    _check(kda, x)
+
+
+def test_beta_zero_is_pure_decay(kda):
+    x = W.batched(1, 100, 2, 64, 64, dtype="fp32", alpha_scale=0.1, s0_std=0.1, seed=6)
+    x.beta.zero_()
+    q, k, v, a, b, s0 = _dev(x)
+    _, s = kda.prefill(q, k, v, a, b, s0)
+    exp = torch.prod(x.alpha.double(), dim=1)[..., None] * x.initial_state.double()
+    np.testing.assert_allclose(s.cpu().double().numpy(), exp.numpy(), rtol=2e-5, atol=1e-9)
+
+
+def test_state_passing_split(kda):
+    """Chunk-aligned and unaligned splits: prefill(T1) then prefill(T2) from its
+    final state equals prefill(T1 + T2) (to rounding)."""
+    x = W.batched(2, 400, 2, 128, 128, dtype="fp32", alpha_scale=0.1, s0_std=0.05, seed=8)
+    q, k, v, a, b, s0 = _dev(x)
+    o, s = kda.prefill(q, k, v, a, b, s0)
+    for T1 in (128, 100):
+        o1, s1 = kda.prefill(q[:, :T1].contiguous(), k[:, :T1].contiguous(), v[:, :T1].contiguous(),
+                             a[:, :T1].contiguous(), b[:, :T1].contiguous(), s0)
+        o2, s2 = kda.prefill(q[:, T1:].contiguous(), k[:, T1:].contiguous(), v[:, T1:].contiguous(),
+                             a[:, T1:].contiguous(), b[:, T1:].contiguous(), s1)
+        assert_close("o", torch.cat([o1, o2], 1), o, dict(rel=1e-5, abs=None))
+        assert_close("S", s2, s, dict(rel=1e-5, abs=None))
+
+
+def test_in_place_state_and_optional_outputs(kda):
+    x = W.batched(2, 150, 2, 64, 64, dtype="fp32", alpha_scale=0.1, s0_std=0.05, seed=12)
+    q, k, v, a, b, s0 = _dev(x)
+    o_ref, s_ref = kda.prefill(q, k, v, a, b, s0)
+    st = s0.clone()
+    o2, s2 = kda.prefill(q, k, v, a, b, st, final_state=st)
+    assert s2.data_ptr() == st.data_ptr()
+    torch.testing.assert_close(st, s_ref, rtol=0, atol=0)
+    torch.testing.assert_close(o2, o_ref, rtol=0, atol=0)
+    o3, s3 = kda.prefill(q, k, v, a, b, s0, output_final_state=False)
+    assert s3 is None
+    torch.testing.assert_close(o3, o_ref, rtol=0, atol=0)
+    # zero initial state equals an explicit zero tensor
+    o4, s4 = kda.prefill(q, k, v, a, b, None)
+    o5, s5 = kda.prefill(q, k, v, a, b, torch.zeros_like(s0))
+    torch.testing.assert_close(o4, o5, rtol=0, atol=0)
+    torch.testing.assert_close(s4, s5, rtol=0, atol=0)
+
+
+def test_zero_length_copies_state(kda):
+    d = torch.device("cuda")
+    s0 = torch.randn(2, 3, 64, 64, device=d)
+    e = torch.empty(2, 0, 3, 64, device=d)
+    o, s = kda.prefill(e, e, e, e, torch.empty(2, 0, 3, device=d), s0)
+    torch.testing.assert_close(s, s0, rtol=0, atol=0)
+    _, s = kda.prefill(e, e, e, e, torch.empty(2, 0, 3, device=d), None)
+    assert torch.count_nonzero(s) == 0
