@@ -133,6 +133,15 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dt
                              const float *alpha, const float *beta, float *state, void *o,
                              int N, int H, int d_k, int d_v, kda_stream_t stream);
 
+/*
+ * kda_device_errors - diagnostic: reads the library's device-side error word
+ * (0 = none). A nonzero value means a kernel stopped early because one of its
+ * bounded waits ran out (its outputs are then invalid); the kernel returned
+ * instead of hanging. Synchronises with the device (a blocking copy of one
+ * int). reset != 0 clears the word after reading.
+ */
+kda_status_t kda_device_errors(int *errors, int reset);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char *kda_last_error(void);
 

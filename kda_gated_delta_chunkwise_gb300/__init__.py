@@ -9,5 +9,5 @@ Entry points (thin ctypes binding over the C ABI in include/kda.h):
 ``kda_gated_delta_chunkwise_gb300.build.build()`` first.
 """
 from ._binding import (ALGOS, EXPORTS, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_OK, KdaError,  # noqa: F401
-                       decode_step, lib_path, load, prefill, varlen_prefill,
+                       decode_step, device_errors, lib_path, load, prefill, varlen_prefill,
                        varlen_workspace_bytes)

@@ -25,7 +25,7 @@ ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS = 0, 1
 
 EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_varlen_prefill", "kda_varlen_workspace_bytes",
-           "kda_decode_step", "kda_last_error", "kda_abi_version")
+           "kda_decode_step", "kda_device_errors", "kda_last_error", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,10 +67,20 @@ def load(path: str | None = None):
         lib.kda_last_error.argtypes = []
         lib.kda_abi_version.restype = ctypes.c_int
         lib.kda_abi_version.argtypes = []
+        lib.kda_device_errors.restype = ctypes.c_int
+        lib.kda_device_errors.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         del f
         if path is None:
             _lib = lib
         return lib
+
+
+def device_errors(reset: bool = True) -> int:
+    """The device-side error word (nonzero: a kernel's bounded wait ran out)."""
+    lib = load()
+    v = ctypes.c_int(0)
+    _check(lib, lib.kda_device_errors(ctypes.byref(v), int(reset)))
+    return v.value
 
 
 def _check(lib, status: int):

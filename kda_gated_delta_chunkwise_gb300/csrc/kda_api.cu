@@ -102,6 +102,11 @@ const char *kda_last_error(void) { return g_last_error.c_str(); }
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
 
+kda_status_t kda_device_errors(int *errors, int reset) {
+    if (!errors) return fail(KDA_ERR_INVALID_ARG, "errors must not be NULL");
+    return cuda_status(kda::read_device_error(errors, reset != 0), "reading the device error word");
+}
+
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
                             const float *alpha, const float *beta, const float *initial_state,
                             void *o, float *final_state, int B, int T, int H, int d_k, int d_v,

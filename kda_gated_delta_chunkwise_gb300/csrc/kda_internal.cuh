@@ -43,6 +43,8 @@ struct PrefillArgs {
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
+// Reads (and optionally clears) the tensor-core kernel's error word.
+cudaError_t read_device_error(int *out, bool reset);
 
 // Varlen preparation: validates cu_seqlens, writes the status word, sorts the
 // sequences by length (longest first) into `order` and zeroes `counter`.

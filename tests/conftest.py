@@ -27,4 +27,16 @@ def kda():
         pytest.fail("GPU test collected on a machine without CUDA")
     import kda_gated_delta_chunkwise_gb300 as k
     k.load()  # raises if the shared library is missing
+    k.device_errors(reset=True)
     return k
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(request):
+    """Every GPU test must leave the device error word clear (no kernel gave
+    up on a bounded wait)."""
+    yield
+    if request.node.get_closest_marker("gpu") is not None:
+        import kda_gated_delta_chunkwise_gb300 as k
+        errs = k.device_errors(reset=True)
+        assert errs == 0, f"a kernel reported device error {errs}"

@@ -93,6 +93,28 @@ def test_strong_decay_and_zero_gates(kda):
     _check(kda, x)
 
 
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_strong_decay_and_zero_gates_bf16(kda, algo):
+    """Same gate edge cases on bf16 inputs (the tensor-core kernel runs such
+    chunks token by token)."""
+    x = W.batched(2, 300, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=15)
+    x.alpha[0, 10, 0, :] = 0.0
+    x.alpha[1, 70:90, 1, 5] = 1e-3
+    x.alpha[0, 200:264, 1, :64] = 0.2
+    _check(kda, x, algo)
+
+
+def test_tensor_core_and_cuda_core_paths_agree(kda):
+    """The tcgen05 kernel and the fp32 CUDA-core kernel evaluate the same
+    chunk algebra; on bf16 inputs they agree to bf16 operand rounding."""
+    x = W.batched(2, 777, 4, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=21)
+    q, k, v, a, b, s0 = _dev(x)
+    o_tc, s_tc = kda.prefill(q, k, v, a, b, s0, algo="tc")
+    o_si, s_si = kda.prefill(q, k, v, a, b, s0, algo="simt")
+    assert_close("o", o_tc, o_si, dict(rel=5e-3, abs=2e-2))
+    assert_close("S", s_tc, s_si, dict(rel=5e-3, abs=2e-2))
+
+
 def test_beta_zero_is_pure_decay(kda):
     x = W.batched(1, 100, 2, 64, 64, dtype="fp32", alpha_scale=0.1, s0_std=0.1, seed=6)
     x.beta.zero_()
