@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 
 namespace kda {
 
