@@ -121,6 +121,31 @@ kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda
 size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
 
 /*
+ * kda_varlen_prefill_noalloc - kda_varlen_prefill without a workspace, for
+ * callers that must not allocate device memory (engines whose device memory
+ * is planned up front and may not grow on the request path, plug-ins that
+ * are handed only the call's tensors, paths where an allocation would
+ * synchronise). The paper has no counterpart: this is an interface choice.
+ *
+ * Arguments, layouts and results are those of kda_varlen_prefill. The small
+ * scratch it needs (sequence order, work counter, status word) is a fixed
+ * array inside the library, present on every GPU that loads the library
+ * until the process exits; it holds at most KDA_NOALLOC_MAX_SEQS sequences,
+ * and larger N is rejected with KDA_ERR_UNSUPPORTED before anything runs.
+ * The first call on a device looks up that array's device address once
+ * (with the device current); make this first call before any stream capture.
+ * All calls share the one array and each call rewrites what it uses, so calls
+ * that overlap on the GPU (different streams, or different host threads on
+ * the same device) race and must be serialised by the caller.
+ */
+#define KDA_NOALLOC_MAX_SEQS 16384
+kda_status_t kda_varlen_prefill_noalloc(const void *q, const void *k, const void *v,
+                                        kda_dtype_t qkv_dtype, const float *alpha, const float *beta,
+                                        const float *initial_state, void *o, float *final_state,
+                                        const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
+                                        int d_v, int32_t *device_status, kda_stream_t stream);
+
+/*
  * kda_decode_step - one recurrent step per (sequence, head), in place
  * (K3 essay §四 update for a single token, §二.1 read-out):
  *     S' = Diag(alpha) S;  e = beta (v - S'^T k);  S <- S' + k e^T;  o = S^T q

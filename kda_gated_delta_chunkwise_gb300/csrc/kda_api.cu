@@ -96,6 +96,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 }  // namespace
 
+kda_status_t kda::set_error(kda_status_t st, const char *msg) { return fail(st, "%s", msg); }
+
 extern "C" {
 
 const char *kda_last_error(void) { return g_last_error.c_str(); }

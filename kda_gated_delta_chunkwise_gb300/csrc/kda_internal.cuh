@@ -51,4 +51,7 @@ cudaError_t read_device_error(int *out, bool reset);
 cudaError_t launch_varlen_prep(const int32_t *cu_seqlens, int N, int T_total, int32_t *order,
                                int32_t *counter, int32_t *status, cudaStream_t s);
 
+// Records `msg` as this thread's last error and returns `st`.
+kda_status_t set_error(kda_status_t st, const char *msg);
+
 }  // namespace kda
