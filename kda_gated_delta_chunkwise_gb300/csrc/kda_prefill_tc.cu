@@ -20,19 +20,25 @@
 // Every gated factor lies in [mu, 1/mu]; a chunk in which some channel decays
 // by more than e^-80 is run token by token instead (exact for alpha = 0).
 //
-// One CTA per (sequence, head, 64-wide slice of d_v); 512 threads, four
-// warpgroups with their own register budgets (setmaxnreg):
-//   warps 0-3   epilogue: the state chain (R, U, O, S) - one TMEM lane each  144 regs
-//   warps 4-7   gate: gate products, mu, the gated tables Kr, Qr, Kc        160 regs
-//   warps 8-11  solve: A/P read-out, T = (I + A)^-1, the [T; P] tile        128 regs
-//   warp 12     TMA producer (q, k, v tiles 2-deep; alpha 1-deep, freed early)
+// One cluster of two CTAs per (sequence, head). CTA `rank` owns value columns
+// 64 rank .. 64 rank + 63 of the state (its state chain) and, for the work
+// both halves share, key channels 64 rank .. 64 rank + 63 of the gated tables
+// and every other chunk's inverse (chunks n with n % 2 == rank). Each CTA
+// pushes what it computed into its peer's shared memory with bulk copies
+// (cp.async.bulk shared::cta -> shared::cluster) that complete on the peer's
+// mbarriers; the tensor-core issuers signal buffer releases to both CTAs with
+// multicast tcgen05.commit.
+//
+// 512 threads per CTA, four warpgroups with their own register budgets:
+//   warps 0-3   epilogue: the state chain (R, U, state), the outputs O
+//   warps 4-7   gate: products, mu, Kr / Qr / Kc for this CTA's key channels
+//   warps 8-11  solve (chunks of this CTA's parity): A/P read-out,
+//               T = (I + A)^{-1}, the [T; P] tile for both CTAs
+//   warp 12     TMA producer (this CTA's halves of q, k, alpha; its v slice)
 //   warp 13     MMA issuer of the state chain (one thread), TMEM owner
-//   warp 14     MMA issuer of the intra-chunk [A; P] products (one thread);
-//               tcgen05 commits track the issuing thread, so the two issuers
-//               never wait for each other; warp 15 idle                      80 regs
-// The three groups work on consecutive chunks at once: tables of chunk n+2,
-// inverse of chunk n+1, state chain of chunk n. All waits are bounded; on a
-// timeout the CTA records an error and winds down.
+//   warp 14     MMA issuer of [A; P] on this CTA's parity; warp 15 idle
+// The groups work on consecutive chunks at once. All waits are bounded; on a
+// timeout the CTA records an error, tells its peer and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,29 +53,35 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DV = 128;
-constexpr int VS = 64;
+constexpr int VS = 64;      // value columns per CTA
+constexpr int KH = 64;      // key channels per CTA in the gate
 constexpr int NSLICE = DV / VS;
+static_assert(NSLICE == 2, "one cluster of two CTAs per (sequence, head)");
 constexpr int NTHREADS = 512;
 // Register shares per warpgroup. Each SM sub-partition holds one warp of
 // every warpgroup, so the shares sum to 4 x 128 = the launch's allocation
 // (a larger sum would make setmaxnreg.inc wait forever).
-constexpr uint32_t REGS_EPI = 144, REGS_GATE = 160, REGS_SOLVE = 128, REGS_CTRL = 80;
+constexpr uint32_t REGS_EPI = 160, REGS_GATE = 112, REGS_SOLVE = 160, REGS_CTRL = 80;
 static_assert(REGS_EPI + REGS_GATE + REGS_SOLVE + REGS_CTRL == 4 * 128, "register split");
+// setmaxnreg.inc may only raise and .dec only lower a warp's count (from the
+// launch's 128); the wrong one is an illegal instruction.
+static_assert(REGS_EPI >= 128 && REGS_SOLVE >= 128 && REGS_GATE <= 128 && REGS_CTRL <= 128, "inc / dec");
 constexpr int EPI_THREADS = 128;
 constexpr int GATE_THREADS = 128;
 constexpr int SOLVE_THREADS = 128;
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
-constexpr int WARP_MMA0 = 14;
+constexpr int WARP_AUX = 14;
 constexpr float kMinGamma = 1.8e-35f;  // ~exp(-80)
 
-// TMEM columns (fp32 accumulators, 128 lanes each)
-constexpr uint32_t TM_AP0 = 0, TM_AP1 = 64, TM_XY = 128, TM_UO = 192, TM_D = 256, TM_COLS = 512;
+// TMEM columns (fp32 accumulators, 128 lanes each); AP, XY and UO are
+// double-buffered by chunk parity.
+constexpr uint32_t TM_AP = 0, TM_XY = 128, TM_UO = 256, TM_D = 384, TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t SM_A0 = 0;          // 2 x 32 KB: raw k|q (TMA, 128B swizzle) -> [Kr; Qr]
-constexpr uint32_t SM_B0 = 65536;      // 2 x 16 KB: Kc (K-major, 64 rows)
-constexpr uint32_t SM_AL = 98304;      // 32 KB: alpha (fp32 [64][128])
+constexpr uint32_t SM_A0 = 0;          // 2 x 32 KB: [Kr; Qr], two 16 KB key-channel halves (128B swizzle)
+constexpr uint32_t SM_B0 = 65536;      // 2 x 16 KB: Kc (K-major, 64 rows), two 8 KB halves
+constexpr uint32_t SM_AL = 98304;      // 2 x 16 KB: alpha of this CTA's key channels (fp32 [64][64])
 constexpr uint32_t SM_SOLVE = 131072;  // 32 KB: A and T (fp32 64x64 each, XOR-swizzled)
 constexpr uint32_t SM_V = 163840;      // 2 x 8 KB: v slice (128B swizzle)
 constexpr uint32_t SM_TP = 180224;     // 16 KB: [T; P] (K-major, 128 rows x 64)
@@ -77,22 +89,29 @@ constexpr uint32_t SM_ST = 196608;     // 16 KB: St (MN-major, 128 rows x 64)
 constexpr uint32_t SM_RU = 212992;     // 8 KB: R then U (MN-major, 64 rows x 64)
 constexpr uint32_t SM_MU = 221184;     // float[2][128]
 constexpr uint32_t SM_BETA = 222208;   // float[2][64]
-constexpr uint32_t SM_INFO = 222720;   // int[2][2]: valid rows, slow flag
-constexpr uint32_t SM_FLAGS = 222736;  // int[8]: [1] abort, [4 + b] slow vote of chunk parity b
-constexpr uint32_t SM_TMEM = 222768;   // uint32 TMEM base
-constexpr uint32_t SM_BAR = 222784;    // mbarriers
-constexpr uint32_t SM_RED = 223104;    // float[4][64] + float[64]: slow-path reductions
-constexpr uint32_t SM_MSCR = 224384;   // float[3][16*16]: mma.sync staging
-constexpr uint32_t SM_SCAN = 227456;   // float[4][128]: per-group gate products
-constexpr uint32_t SM_TOTAL = 229504;
+constexpr uint32_t SM_VOTE = 222720;   // int[2][8]: slow vote of key half 0 at [0], half 1 at [4]
+constexpr uint32_t SM_FLAGS = 222784;  // int[8]: [1] abort
+constexpr uint32_t SM_TMEM = 222816;   // uint32 TMEM base
+constexpr uint32_t SM_BAR = 222848;    // mbarriers (up to 40)
+constexpr uint32_t SM_RED = 223168;    // float[4][64] + float[64]: slow-path reductions
+constexpr uint32_t SM_MSCR = 224448;   // float[3][16*16]: mma.sync staging
+constexpr uint32_t SM_SCAN = 227520;   // float2[4][32]: per-group gate products
+constexpr uint32_t SM_TOTAL = 228544;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
+
+// Bytes one CTA pushes into its peer per chunk: its [Kr; Qr] half, its Kc
+// half, its half of mu and its slow vote.
+constexpr uint32_t PUSH_TAB = 16384 + 8192 + 256 + 16;
+constexpr uint32_t PUSH_TP = 16384;
+constexpr uint16_t BOTH = 3;  // CTA mask of the cluster
 
 enum Bar {
     B_QK_FULL = 0, B_QK_EMPTY = 2, B_AL_FULL = 4, B_AL_EMPTY = 6, B_V_FULL = 8, B_V_EMPTY = 10,
-    B_TAB_FULL = 12, B_AP_FULL = 14, B_B0_EMPTY = 16, B_TP_FULL = 18, B_TP_EMPTY = 19,
-    B_S_FULL = 20, B_XY_FULL = 21, B_R_FULL = 22, B_U_FULL = 23, B_UU_FULL = 24, B_D_FULL = 25,
-    B_DRAIN = 26, B_COUNT = 28  // B_DRAIN + 1: drain of the MMA0 issuer
+    B_TAB_FULL = 12, B_B0_EMPTY = 14, B_O_READ = 16, B_AP_FULL = 18, B_TP_FULL = 19, B_TP_EMPTY = 20,
+    B_S_FULL = 21, B_XY_FULL = 22, B_R_FULL = 23, B_U_FULL = 24, B_UU_FULL = 25, B_D_FULL = 26,
+    B_DRAIN = 27, B_DRAIN_AUX = 28, B_COUNT = 29
 };
+static_assert(B_COUNT <= 40, "mbarrier area");
 
 struct TcParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -161,124 +180,141 @@ __device__ __forceinline__ uint32_t row128_chunk(uint32_t row, uint32_t cc) {
 
 struct Smem {
     unsigned char *base;
+    uint32_t peer;  // cluster rank of the other CTA
     __device__ __forceinline__ uint64_t *bar(int i) const {
         return reinterpret_cast<uint64_t *>(base + SM_BAR) + i;
     }
     __device__ __forceinline__ volatile int *flags() const {
         return reinterpret_cast<volatile int *>(base + SM_FLAGS);
     }
-    __device__ __forceinline__ int *info(int b) const { return reinterpret_cast<int *>(base + SM_INFO) + 2 * b; }
     __device__ __forceinline__ float *mu(int b) const { return reinterpret_cast<float *>(base + SM_MU) + 128 * b; }
     __device__ __forceinline__ float *beta(int b) const { return reinterpret_cast<float *>(base + SM_BETA) + 64 * b; }
+    __device__ __forceinline__ int *vote(int b) const { return reinterpret_cast<int *>(base + SM_VOTE) + 8 * b; }
+    // A chunk runs token by token when either key half voted so.
+    __device__ __forceinline__ bool slow(int b) const {
+        const volatile int *v = vote(b);
+        return (v[0] | v[4]) != 0;
+    }
+    // Cluster address of this CTA's shared-memory location p in the peer.
+    __device__ __forceinline__ uint32_t remote(const void *p) const { return mapa(smem_u32(p), peer); }
 };
 
-__device__ __forceinline__ void report(const Smem &s, const TcParams &p, int code) {
-    s.flags()[1] = 1;  // abort
-    atomicOr(p.err ? p.err : &g_tc_error, code);
+// Out of line: it runs only after a wait timed out. Raises the abort flag
+// here and in the peer, and records the error code.
+__device__ __noinline__ void report(uint32_t flag_addr, uint32_t peer, int32_t *err, int code) {
+    asm volatile("st.shared.u32 [%0], 1;" ::"r"(flag_addr) : "memory");
+    st_cluster_u32(mapa(flag_addr, peer), 1u);
+    atomicOr(err ? err : &g_tc_error, code);
 }
-// Wait with the CTA-wide abort check; returns false when the CTA must stop.
+// Wait with the cluster-wide abort check; returns false when the CTA must stop.
 __device__ __forceinline__ bool wait_bar(const Smem &s, const TcParams &p, int i, uint32_t parity) {
     if (s.flags()[1]) return false;
     if (mbar_wait(s.bar(i), parity)) return true;
-    report(s, p, 2);
+    report(smem_u32(s.base + SM_FLAGS + 4), s.peer, p.err, 2);
     return false;
+}
+
+// Sum over the warp of eight per-lane values (one per column), reduced and
+// scattered in 9 shuffles: the result is the column ((lane >> 2) & 7) sum,
+// with column bits taken from lane bits 4, 3, 2 (high to low).
+__device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
+    const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0, u4 = (lane & 4) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float send = u16 ? v[e] : v[e + 4];
+        v[e] = (u16 ? v[e + 4] : v[e]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const float send = u8 ? v[e] : v[e + 2];
+        v[e] = (u8 ? v[e + 2] : v[e]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float x = (u4 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, u4 ? v[0] : v[1], 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
 }
 
 // Exact token-by-token update of one chunk (the K3 essay's §四 recurrence in
 // fp32), used for chunks whose gates decay past the factorised range. The
 // epilogue warpgroup holds the state slice in TMEM (lane = key channel,
-// 64 value columns); this reads it, runs the chunk's tokens and writes the
-// new state back. Rare; inlined (an out-of-line call costs the fast path
-// register spills around the call site).
+// 64 value columns) and updates it there, eight columns at a time; sums over
+// the key channels go through warp shuffles and four per-warp partials in
+// shared memory. Rare, so it is written for size rather than speed.
 __device__ __forceinline__ void slow_chunk(const float *__restrict__ alpha, const __nv_bfloat16 *__restrict__ kin,
                                         const __nv_bfloat16 *__restrict__ qin, const __nv_bfloat16 *__restrict__ vin,
                                         const float *__restrict__ beta, __nv_bfloat16 *__restrict__ o, float *red,
                                         uint32_t tm_d, int l, int warp, int lane, int64_t tok0, int L, int H, int h,
                                         int v0) {
-    float sreg[64];
-    uint32_t r32[32];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        tmem_ld32(tm_d + 32 * hf, r32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sreg[32 * hf + j] = __uint_as_float(r32[j]);
-    }
+    const int col = 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+    const bool writer = (lane & 3) == 0;
+#pragma unroll 1
     for (int r = 0; r < L; ++r) {
         const int64_t tk = (tok0 + r) * H + h;
         const float a = alpha[tk * DK + l];
         const float kf = __bfloat162float(kin[tk * DK + l]);
         const float qf = __bfloat162float(qin[tk * DK + l]);
-        float part[64];
+        // S' = Diag(alpha) S, and this warp's part of S'^T k
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t u[8];
+            float part[8];
+            tmem_ld8(tm_d + 8 * g, u);
+            tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            sreg[j] *= a;
-            part[j] = kf * sreg[j];
-        }
-        // butterfly reduce-scatter over the warp (64 -> 2 values per lane):
-        // the lane ends with the sums of columns 2*lane and 2*lane+1
-#pragma unroll
-        for (int nv = 64; nv >= 4; nv >>= 1) {
-            const int half = nv / 2, off = nv / 4;
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int j = 0; j < half; ++j) {
-                const float send = up ? part[j] : part[j + half];
-                const float keep = up ? part[j + half] : part[j];
-                part[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            for (int e = 0; e < 8; ++e) {
+                const float x = a * __uint_as_float(u[e]);
+                u[e] = __float_as_uint(x);
+                part[e] = kf * x;
             }
+            tmem_st8(tm_d + 8 * g, u);
+            const float sum = warp_sum8(part, lane);
+            if (writer) red[warp * 64 + 8 * g + col] = sum;
         }
-        red[warp * 64 + 2 * lane] = part[0];
-        red[warp * 64 + 2 * lane + 1] = part[1];
+        tmem_wait_st();
         named_bar(2, EPI_THREADS);
         if (l < 64) {
             const float vh = red[l] + red[64 + l] + red[128 + l] + red[192 + l];
-            const float vv = __bfloat162float(vin[tk * DV + v0 + l]);
-            red[256 + l] = beta[tk] * (vv - vh);
+            red[256 + l] = beta[tk] * (__bfloat162float(vin[tk * DV + v0 + l]) - vh);
         }
         named_bar(2, EPI_THREADS);
+        // S = S' + k e^T, and this warp's part of S^T q
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t u[8];
+            float part[8];
+            tmem_ld8(tm_d + 8 * g, u);
+            tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            sreg[j] += kf * red[256 + j];
-            part[j] = qf * sreg[j];
-        }
-        named_bar(2, EPI_THREADS);  // the error vector is read by all
-#pragma unroll
-        for (int nv = 64; nv >= 4; nv >>= 1) {
-            const int half = nv / 2, off = nv / 4;
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int j = 0; j < half; ++j) {
-                const float send = up ? part[j] : part[j + half];
-                const float keep = up ? part[j + half] : part[j];
-                part[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            for (int e = 0; e < 8; ++e) {
+                const float x = __uint_as_float(u[e]) + kf * red[256 + 8 * g + e];
+                u[e] = __float_as_uint(x);
+                part[e] = qf * x;
             }
+            tmem_st8(tm_d + 8 * g, u);
+            const float sum = warp_sum8(part, lane);
+            if (writer) red[warp * 64 + 8 * g + col] = sum;
         }
-        red[warp * 64 + 2 * lane] = part[0];
-        red[warp * 64 + 2 * lane + 1] = part[1];
+        tmem_wait_st();
         named_bar(2, EPI_THREADS);
         if (l < 64) o[tk * DV + v0 + l] = __float2bfloat16_rn(red[l] + red[64 + l] + red[128 + l] + red[192 + l]);
         named_bar(2, EPI_THREADS);
     }
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r32[j] = __float_as_uint(sreg[32 * hf + j]);
-        tmem_st32(tm_d + 32 * hf, r32);
-    }
-    tmem_wait_st();
 }
 
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ unsigned char smem_raw[];
-    Smem s{reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))};
+    const uint32_t rank = cluster_rank();  // value half and key half of this CTA (blockIdx.x % 2)
+    Smem s{reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)),
+           rank ^ 1u};
+    // Both CTAs of a cluster read the same status word and sequence: they
+    // leave here together or not at all.
     if (p.dev_status && *p.dev_status != 0) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slice = blockIdx.x % NSLICE;
     const int h = (blockIdx.x / NSLICE) % p.H;
     const int item = blockIdx.x / (NSLICE * p.H);
     const int seq = p.order ? p.order[item] : item;
@@ -291,7 +327,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         T = p.T;
     }
     const int H = p.H;
-    const int v0 = slice * VS;
+    const int v0 = (int)rank * VS;   // first value column of this CTA's state slice
+    const int c0 = (int)rank * KH;   // first key channel of this CTA's gate half
     const int64_t state_off = ((int64_t)seq * H + h) * DK * DV;
     const int NC = (int)((T + C - 1) / C);
 
@@ -307,25 +344,26 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(s.bar(B_QK_FULL + i), 1);
-            mbar_init(s.bar(B_QK_EMPTY + i), 2);  // both MMA issuers read the q/k tile
+            mbar_init(s.bar(B_QK_EMPTY + i), 2);  // MMA2 of both CTAs (multicast commits)
             mbar_init(s.bar(B_AL_FULL + i), 1);
             mbar_init(s.bar(B_AL_EMPTY + i), 1);
             mbar_init(s.bar(B_V_FULL + i), 1);
-            mbar_init(s.bar(B_V_EMPTY + i), EPI_THREADS);
-            mbar_init(s.bar(B_TAB_FULL + i), GATE_THREADS);
-            mbar_init(s.bar(B_AP_FULL + i), 1);
-            mbar_init(s.bar(B_B0_EMPTY + i), 1);
+            mbar_init(s.bar(B_V_EMPTY + i), 64);
+            mbar_init(s.bar(B_TAB_FULL + i), 1);  // own gate (expecting the peer's bytes) + the peer's copies
+            mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
+            mbar_init(s.bar(B_O_READ + i), 64);
         }
-        mbar_init(s.bar(B_TP_FULL), SOLVE_THREADS);
-        mbar_init(s.bar(B_TP_EMPTY), 1);
+        mbar_init(s.bar(B_AP_FULL), 1);
+        mbar_init(s.bar(B_TP_FULL), 1);   // the solving CTA: local arrive, or remote arrive + copy
+        mbar_init(s.bar(B_TP_EMPTY), 2);  // MMA4 of both CTAs
         mbar_init(s.bar(B_S_FULL), EPI_THREADS);
         mbar_init(s.bar(B_XY_FULL), 1);
-        mbar_init(s.bar(B_R_FULL), EPI_THREADS);
+        mbar_init(s.bar(B_R_FULL), 64);
         mbar_init(s.bar(B_U_FULL), 1);
-        mbar_init(s.bar(B_UU_FULL), EPI_THREADS);
+        mbar_init(s.bar(B_UU_FULL), 64);
         mbar_init(s.bar(B_D_FULL), 1);
         mbar_init(s.bar(B_DRAIN), 1);
-        mbar_init(s.bar(B_DRAIN + 1), 1);
+        mbar_init(s.bar(B_DRAIN_AUX), 1);
         for (int i = 0; i < 8; ++i) s.flags()[i] = 0;
         fence_mbar_init();
     }
@@ -334,7 +372,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive, copy or commit
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s.base + SM_TMEM);
 
@@ -348,38 +386,34 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_a);
             prefetch_tmap(&tm_v);
-            int issued = 0;
+            int nqk = 0, nal = 0, nv = 0;  // loads issued per stream
             for (int n = 0; n < NC; ++n) {
                 const int b = n & 1, kk = n >> 1;
                 const int z = (int)(t_begin + (int64_t)n * C);
+                // this CTA's key half of k and q (raw; the gate transforms them in place)
                 if (n >= 2 && !wait_bar(s, p, B_QK_EMPTY + b, (kk - 1) & 1)) break;
-                unsigned char *a0 = s.base + SM_A0 + b * 32768;
-                mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 32768);
-                tma_load_3d(a0 + 0, &tm_k, s.bar(B_QK_FULL + b), 0, h, z);
-                tma_load_3d(a0 + 8192, &tm_q, s.bar(B_QK_FULL + b), 0, h, z);
-                tma_load_3d(a0 + 16384, &tm_k, s.bar(B_QK_FULL + b), 64, h, z);
-                tma_load_3d(a0 + 24576, &tm_q, s.bar(B_QK_FULL + b), 64, h, z);
-                // alpha: one buffer, released by the gate group as soon as it
-                // holds the chunk's gates in registers
-                if (n >= 1 && !wait_bar(s, p, B_AL_EMPTY, (n - 1) & 1)) break;
-                mbar_arrive_expect_tx(s.bar(B_AL_FULL), 32768);
-                tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), 0, h, z);
+                unsigned char *a0 = s.base + SM_A0 + b * 32768 + rank * 16384;
+                mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 16384);
+                tma_load_3d(a0, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
+                tma_load_3d(a0 + 8192, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
+                nqk = n + 1;
+                if (n >= 2 && !wait_bar(s, p, B_AL_EMPTY + b, (kk - 1) & 1)) break;
+                mbar_arrive_expect_tx(s.bar(B_AL_FULL + b), 16384);
+                tma_load_3d(s.base + SM_AL + b * 16384, &tm_a, s.bar(B_AL_FULL + b), c0, h, z);
+                nal = n + 1;
                 if (n >= 2 && !wait_bar(s, p, B_V_EMPTY + b, (kk - 1) & 1)) break;
                 mbar_arrive_expect_tx(s.bar(B_V_FULL + b), 8192);
                 tma_load_3d(s.base + SM_V + b * 8192, &tm_v, s.bar(B_V_FULL + b), v0, h, z);
-                issued = n + 1;
+                nv = n + 1;
             }
             // never leave copies in flight: wait (bounded) for the last ones
-            for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n) {
-                const int b = n & 1, kk = n >> 1;
-                mbar_wait(s.bar(B_QK_FULL + b), kk & 1);
-                mbar_wait(s.bar(B_V_FULL + b), kk & 1);
-            }
-            if (issued > 0) mbar_wait(s.bar(B_AL_FULL), (issued - 1) & 1);
+            for (int n = nqk - 2 < 0 ? 0 : nqk - 2; n < nqk; ++n) mbar_wait(s.bar(B_QK_FULL + (n & 1)), (n >> 1) & 1);
+            for (int n = nal - 2 < 0 ? 0 : nal - 2; n < nal; ++n) mbar_wait(s.bar(B_AL_FULL + (n & 1)), (n >> 1) & 1);
+            for (int n = nv - 2 < 0 ? 0 : nv - 2; n < nv; ++n) mbar_wait(s.bar(B_V_FULL + (n & 1)), (n >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA
+        // ------------------------------------------------------------ MMA (state chain)
         if (lane == 0) {
             constexpr uint32_t I_KM_MN = idesc_bf16(128, 64, false, true);
             constexpr uint32_t I_MN_MN = idesc_bf16(128, 64, true, true);
@@ -388,29 +422,33 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                            ru = smem_u32(s.base + SM_RU);
             bool ok = true;
             for (int n = 0; ok && n < NC; ++n) {
-                const int b = n & 1;
-                if (!(ok = wait_bar(s, p, B_TAB_FULL + b, (n >> 1) & 1))) break;
-                const bool fast = !s.info(b)[1];
-                // MMA1: [X; Y] = [Kr; Qr] St
+                const int b = n & 1, kk = n >> 1;
+                if (!(ok = wait_bar(s, p, B_TAB_FULL + b, kk & 1))) break;
+                const bool fast = !s.slow(b);
+                const uint32_t xy = tmem + TM_XY + 64 * b, uo = tmem + TM_UO + 64 * b;
+                // MMA1: [X; Y] = [Kr; Qr] St, once the outputs of chunk n-2 left XY[b]
+                if (n >= 2 && !(ok = wait_bar(s, p, B_O_READ + b, (kk - 1) & 1))) break;
                 if (!(ok = wait_bar(s, p, B_S_FULL, n & 1))) break;
                 tc_fence_after();
                 if (fast) {
                     const uint32_t a0 = a0_base + b * 32768;
                     for (int ks = 0; ks < 8; ++ks)
-                        umma_bf16(tmem + TM_XY, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                        umma_bf16(xy, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(st + ks * 2048, 16384, 1024), I_KM_MN, ks > 0);
                 }
                 umma_commit(s.bar(B_XY_FULL));
-                umma_commit(s.bar(B_QK_EMPTY + b));  // with the MMA0 issuer's: 2 arrivals
                 // MMA2: U = T R (rows 0-63 of [T; P] R)
                 if (!(ok = wait_bar(s, p, B_R_FULL, n & 1))) break;
                 if (!(ok = wait_bar(s, p, B_TP_FULL, n & 1))) break;
                 tc_fence_after();
                 if (fast)
                     for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tmem + TM_UO, sdesc_sw128(tp + ks * 32, 16, 1024),
-                                  sdesc_sw128(ru + ks * 2048, 8192, 1024), I_KM_MN, ks > 0);
+                        umma_bf16(uo, sdesc_sw128(tp + ks * 32, 16, 1024), sdesc_sw128(ru + ks * 2048, 8192, 1024),
+                                  I_KM_MN, ks > 0);
                 umma_commit(s.bar(B_U_FULL));
+                // A0[b] is free in both CTAs once MMA2 of both completed (the
+                // [A; P] product of this chunk finished before [T; P] existed)
+                umma_commit_mc(s.bar(B_QK_EMPTY + b), BOTH);
                 // MMA3: D += Kc^T U (state update); MMA4: O2 = P U (rows 64-127)
                 if (!(ok = wait_bar(s, p, B_UU_FULL, n & 1))) break;
                 tc_fence_after();
@@ -420,48 +458,45 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                         umma_bf16(tmem + TM_D, sdesc_sw128(b0 + ks * 2048, 8192, 1024),
                                   sdesc_sw128(ru + ks * 2048, 8192, 1024), I_MN_MN, 1);
                     for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tmem + TM_UO, sdesc_sw128(tp + ks * 32, 16, 1024),
-                                  sdesc_sw128(ru + ks * 2048, 8192, 1024), I_KM_MN, ks > 0);
+                        umma_bf16(uo, sdesc_sw128(tp + ks * 32, 16, 1024), sdesc_sw128(ru + ks * 2048, 8192, 1024),
+                                  I_KM_MN, ks > 0);
                 }
                 umma_commit(s.bar(B_D_FULL));
-                umma_commit(s.bar(B_B0_EMPTY + b));
-                umma_commit(s.bar(B_TP_EMPTY));
+                umma_commit_mc(s.bar(B_B0_EMPTY + b), BOTH);
+                umma_commit_mc(s.bar(B_TP_EMPTY), BOTH);
             }
             // drain: every MMA issued has completed before TMEM is released
             umma_commit(s.bar(B_DRAIN));
             mbar_wait(s.bar(B_DRAIN), 0);
         }
         __syncwarp();
-    } else if (warp == WARP_MMA0) {
-        // ------------------------------------------------------------ MMA0 issuer
+    } else if (warp == WARP_AUX) {
+        // ------------------------------------------------------------ [A; P] issuer (this CTA's parity)
         if (lane == 0) {
             constexpr uint32_t I_AP = idesc_bf16(128, 64, false, false);
-            const uint32_t a0_base = smem_u32(s.base + SM_A0), b0_base = smem_u32(s.base + SM_B0);
-            for (int n = 0; n < NC; ++n) {
-                const int b = n & 1;
-                if (!wait_bar(s, p, B_TAB_FULL + b, (n >> 1) & 1)) break;
+            const uint32_t a0 = smem_u32(s.base + SM_A0) + rank * 32768, b0 = smem_u32(s.base + SM_B0) + rank * 16384;
+            for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
+                if (!wait_bar(s, p, B_TAB_FULL + (int)rank, i & 1)) break;  // chunk n uses buffer n & 1 = rank
                 tc_fence_after();
-                if (!s.info(b)[1]) {
-                    const uint32_t a0 = a0_base + b * 32768, b0 = b0_base + b * 16384;
-                    const uint32_t d = tmem + (b ? TM_AP1 : TM_AP0);
+                if (!s.slow((int)rank)) {
+                    const uint32_t d = tmem + TM_AP + 64 * (i & 1);
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(d, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(b0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), I_AP, ks > 0);
                 }
-                umma_commit(s.bar(B_AP_FULL + b));
-                umma_commit(s.bar(B_QK_EMPTY + b));
+                umma_commit(s.bar(B_AP_FULL));
             }
-            umma_commit(s.bar(B_DRAIN + 1));
-            mbar_wait(s.bar(B_DRAIN + 1), 0);
+            umma_commit(s.bar(B_DRAIN_AUX));
+            mbar_wait(s.bar(B_DRAIN_AUX), 0);
         }
         __syncwarp();
     } else if (warp >= 12) {
-        // idle warps of the control warpgroup
+        // idle warp of the control warpgroup
     } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue
         regs_inc<REGS_EPI>();
         // Group discipline (here and in the gate / solve groups): a failed
-        // wait never leaves the loop; the thread keeps passing the same named
+        // wait never leaves the loop; the thread keeps passing the same
         // barriers with its work switched off, and the next waits return at
         // once (abort flag). TMEM loads and stores are warp-collective, so the
         // conditions around them are warp-uniform.
@@ -470,12 +505,16 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         const uint32_t tm_d = tmem + lane_off + TM_D;
         uint32_t r32[32];
         bool ok = wait_bar(s, p, B_TAB_FULL, 0);
-        float mu_cur = ok ? s.mu(0)[l] : 1.f;
+        // The chunk's slow flag and mu are read once, as soon as its tables
+        // exist, and kept in registers: the gate of chunk n + 2 overwrites them.
+        bool slow_cur = ok && s.slow(0);
+        float mu_cur = (ok && !slow_cur) ? s.mu(0)[l] : 1.f;
+        bool slow_prev = false;
         // St_0 = Diag(mu_0) S0 -> TMEM (fp32 accumulator base) and the bf16 operand
         {
             const float *src = (ok && p.s0) ? p.s0 + state_off + (int64_t)l * DV + v0 : nullptr;
             unsigned char *st = s.base + SM_ST;
-#pragma unroll
+#pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 float x[32];
 #pragma unroll
@@ -499,112 +538,122 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             mbar_arrive(s.bar(B_S_FULL));
         }
 
-        for (int n = 0; n < NC; ++n) {
+        for (int n = 0; n <= NC; ++n) {
             const int b = n & 1, kk = n >> 1;
+            if (warp >= 2 && n >= 1) {
+                // Outputs of chunk n-1 (token rows 64-127 of XY and UO): O = Y + P U.
+                // Off the state chain: MMA1 of chunk n+1 waits for this read.
+                const int m = n - 1, bm = m & 1;
+                const int Lm = (int)((T - (int64_t)m * C) < C ? (T - (int64_t)m * C) : C);
+                const int r = l - 64;
+                if (__all_sync(0xffffffffu, ok && !slow_prev)) {
+                    __nv_bfloat16 *dst = p.o + ((t_begin + (int64_t)m * C + r) * H + h) * DV + v0;
+                    uint32_t y32[32];
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tmem_ld32(tmem + lane_off + TM_XY + 64 * bm + 32 * hf, y32);
+                        tmem_ld32(tmem + lane_off + TM_UO + 64 * bm + 32 * hf, r32);
+                        tmem_wait_ld();
+                        if (r < Lm) {
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = 8 * c4 + 2 * e;
+                                    w[e] = pack_bf16(__uint_as_float(y32[j]) + __uint_as_float(r32[j]),
+                                                     __uint_as_float(y32[j + 1]) + __uint_as_float(r32[j + 1]));
+                                }
+                                *reinterpret_cast<uint4 *>(dst + 32 * hf + 8 * c4) = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(s.bar(B_O_READ + bm));
+            }
+            if (n == NC) break;
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
             const int64_t tok0 = t_begin + (int64_t)n * C;
-            // E1: R = beta (V - X) for token rows 0-63
-            ok = wait_bar(s, p, B_XY_FULL, n & 1) && ok;
-            ok = wait_bar(s, p, B_V_FULL + b, kk & 1) && ok;
-            tc_fence_after();
-            const bool act = __all_sync(0xffffffffu, ok && s.info(b)[1] == 0);
-            if (act && l < 64) {
-                const float bt = s.beta(b)[l];
-                const unsigned char *vt = s.base + SM_V + b * 8192;
+            if (warp < 2) {
+                // E1: R = beta (V - X) for token rows 0-63
+                ok = wait_bar(s, p, B_XY_FULL, n & 1) && ok;
+                ok = wait_bar(s, p, B_V_FULL + b, kk & 1) && ok;
+                tc_fence_after();
+                const bool act = __all_sync(0xffffffffu, ok && !slow_cur);
                 unsigned char *ru = s.base + SM_RU;
-                uint4 vrow[8];  // the whole v row first: no load waits behind an R store
+                if (act) {
+                    const float bt = s.beta(b)[l];
+                    const unsigned char *vt = s.base + SM_V + b * 8192;
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint4 vrow[4];  // the v row first: no load waits behind an R store
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) vrow[cc] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, cc));
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    tmem_ld32(tmem + lane_off + TM_XY + 32 * hf, r32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int cc = 4 * hf + c4;
-                        const uint4 vv = vrow[cc];
-                        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-                        uint32_t ow[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 vf = unpack_bf16(vw[e]);
-                            const float x0 = __uint_as_float(r32[8 * c4 + 2 * e]);
-                            const float x1 = __uint_as_float(r32[8 * c4 + 2 * e + 1]);
-                            ow[e] = pack_bf16(bt * (vf.x - x0), bt * (vf.y - x1));
-                        }
-                        *reinterpret_cast<uint4 *>(ru + row128_chunk(l, cc)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                    }
-                }
-                fence_proxy_async();
-            }
-            tc_fence_before();
-            mbar_arrive(s.bar(B_R_FULL));
-            mbar_arrive(s.bar(B_V_EMPTY + b));
-            // E2: U -> bf16 operand (replaces R, which MMA2 has consumed)
-            ok = wait_bar(s, p, B_U_FULL, n & 1) && ok;
-            tc_fence_after();
-            if (__all_sync(0xffffffffu, act && ok) && l < 64) {
-                unsigned char *ru = s.base + SM_RU;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    tmem_ld32(tmem + lane_off + TM_UO + 32 * hf, r32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(r32[8 * c4 + 0]), __uint_as_float(r32[8 * c4 + 1]));
-                        w.y = pack_bf16(__uint_as_float(r32[8 * c4 + 2]), __uint_as_float(r32[8 * c4 + 3]));
-                        w.z = pack_bf16(__uint_as_float(r32[8 * c4 + 4]), __uint_as_float(r32[8 * c4 + 5]));
-                        w.w = pack_bf16(__uint_as_float(r32[8 * c4 + 6]), __uint_as_float(r32[8 * c4 + 7]));
-                        *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) = w;
-                    }
-                }
-                fence_proxy_async();
-            }
-            tc_fence_before();
-            mbar_arrive(s.bar(B_UU_FULL));
-            // E3: outputs, then the state S_{n+1} = mu_n D -> St_{n+1} = mu_{n+1} S_{n+1}
-            ok = wait_bar(s, p, B_D_FULL, n & 1) && ok;
-            tc_fence_after();
-            named_bar(2, EPI_THREADS);  // makes the slow-path decision group-uniform
-            const bool go = s.flags()[1] == 0;
-            const bool slow_g = go && s.info(b)[1] != 0;
-            if (!slow_g && l >= 64) {  // warps 2, 3: token rows of O = Y + P U
-                const int r = l - 64;
-                __nv_bfloat16 *dst = p.o + ((tok0 + r) * H + h) * DV + v0;
-                uint32_t y32[32];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    tmem_ld32(tmem + lane_off + TM_XY + 32 * hf, y32);
-                    tmem_ld32(tmem + lane_off + TM_UO + 32 * hf, r32);
-                    tmem_wait_ld();
-                    if (go && r < L) {
+                        for (int c4 = 0; c4 < 4; ++c4)
+                            vrow[c4] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 4 * hf + c4));
+                        tmem_ld32(tmem + lane_off + TM_XY + 64 * b + 32 * hf, r32);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
-                            uint32_t w[4];
+                            const uint32_t vw[4] = {vrow[c4].x, vrow[c4].y, vrow[c4].z, vrow[c4].w};
+                            uint32_t ow[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const int j = 8 * c4 + 2 * e;
-                                w[e] = pack_bf16(__uint_as_float(y32[j]) + __uint_as_float(r32[j]),
-                                                 __uint_as_float(y32[j + 1]) + __uint_as_float(r32[j + 1]));
+                                const float2 vf = unpack_bf16(vw[e]);
+                                ow[e] = pack_bf16(bt * (vf.x - __uint_as_float(r32[8 * c4 + 2 * e])),
+                                                  bt * (vf.y - __uint_as_float(r32[8 * c4 + 2 * e + 1])));
                             }
-                            *reinterpret_cast<uint4 *>(dst + 32 * hf + 8 * c4) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) =
+                                make_uint4(ow[0], ow[1], ow[2], ow[3]);
                         }
                     }
+                    fence_proxy_async();
                 }
+                tc_fence_before();
+                mbar_arrive(s.bar(B_R_FULL));
+                mbar_arrive(s.bar(B_V_EMPTY + b));
+                // E2: U -> bf16 operand (replaces R, which MMA2 has consumed)
+                ok = wait_bar(s, p, B_U_FULL, n & 1) && ok;
+                tc_fence_after();
+                if (__all_sync(0xffffffffu, act && ok)) {
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tmem_ld32(tmem + lane_off + TM_UO + 64 * b + 32 * hf, r32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(r32[8 * c4 + 0]), __uint_as_float(r32[8 * c4 + 1]));
+                            w.y = pack_bf16(__uint_as_float(r32[8 * c4 + 2]), __uint_as_float(r32[8 * c4 + 3]));
+                            w.z = pack_bf16(__uint_as_float(r32[8 * c4 + 4]), __uint_as_float(r32[8 * c4 + 5]));
+                            w.w = pack_bf16(__uint_as_float(r32[8 * c4 + 6]), __uint_as_float(r32[8 * c4 + 7]));
+                            *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) = w;
+                        }
+                    }
+                    fence_proxy_async();
+                }
+                tc_fence_before();
+                mbar_arrive(s.bar(B_UU_FULL));
             }
-            if (slow_g)  // TMEM holds S_n (mu_n = 1); leaves S_{n+1} there
+            // E3: the state S_{n+1} = mu_n D -> St_{n+1} = mu_{n+1} S_{n+1}
+            ok = wait_bar(s, p, B_D_FULL, n & 1) && ok;
+            tc_fence_after();
+            // one decision for the whole group (the slow path has group barriers)
+            const bool go = !named_bar_or(2, EPI_THREADS, s.flags()[1] != 0);
+            if (go && slow_cur)
                 slow_chunk(p.alpha, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d, l,
                            warp, lane, tok0, L, H, h, v0);
             const bool last = n == NC - 1;
             float mu_next = 1.f;
+            bool slow_next = false;
             if (!last) {
                 ok = wait_bar(s, p, B_TAB_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1) && ok;
-                if (ok) mu_next = s.mu((n + 1) & 1)[l];
+                slow_next = ok && s.slow((n + 1) & 1);
+                if (ok && !slow_next) mu_next = s.mu((n + 1) & 1)[l];
             }
             unsigned char *st = s.base + SM_ST;
             float *fin = p.sT ? p.sT + state_off + (int64_t)l * DV + v0 : nullptr;
-#pragma unroll
+#pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 tmem_ld32(tm_d + 32 * hf, r32);
                 tmem_wait_ld();
@@ -636,16 +685,20 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 tc_fence_before();
                 mbar_arrive(s.bar(B_S_FULL));
             }
+            slow_prev = slow_cur;
             mu_cur = mu_next;
+            slow_cur = slow_next;
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------ gate group (warps 4-7)
-        // Thread: value channels 4cq .. 4cq+3, token rows 16tg .. 16tg+15.
-        regs_inc<REGS_GATE>();
+        // Thread: key channels c0 + 2cp, c0 + 2cp + 1; token rows 16tg .. 16tg+15.
+        regs_dec<REGS_GATE>();  // below the launch's 128: a decrease
         const int pt = tid - 128;
-        const int cq = pt & 31, tg = pt >> 5;
-        float *scan = reinterpret_cast<float *>(s.base + SM_SCAN);
-        const float *al = reinterpret_cast<const float *>(s.base + SM_AL);
+        const int cp = pt & 31, tg = pt >> 5;
+        float2 *scan = reinterpret_cast<float2 *>(s.base + SM_SCAN);
+        // Byte offset of this thread's 4 bytes in row 16 tg + 8 i8 + j of a
+        // 128B-swizzled 64-column tile: rowbase(i8) + j * 128 + ((c8 ^ j) << 4) + sub.
+        const uint32_t c8 = (uint32_t)cp >> 2, sub = ((uint32_t)cp & 3u) * 4u;
         for (int n = 0; n < NC; ++n) {
             const int b = n & 1, kk = n >> 1;
             const int64_t tok0 = t_begin + (int64_t)n * C;
@@ -653,154 +706,128 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // beta of this chunk, loaded before the waits so its latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
             bool ok = wait_bar(s, p, B_QK_FULL + b, kk & 1);
-            ok = wait_bar(s, p, B_AL_FULL, n & 1) && ok;
-            if (pt == 0) s.flags()[4 + b] = 0;  // vote slot of this parity (last read two chunks ago)
-            float4 a[16];
-#pragma unroll
+            ok = wait_bar(s, p, B_AL_FULL + b, kk & 1) && ok;
+            const float *al = reinterpret_cast<const float *>(s.base + SM_AL + b * 16384) + 2 * cp;
+            // products of this thread's 16 rows, then the 4 group products
+            float2 g = make_float2(1.f, 1.f);
+#pragma unroll 4
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * tg + i;
-                a[i] = (ok && r < L) ? *reinterpret_cast<const float4 *>(al + r * 128 + 4 * cq)
-                                     : make_float4(1.f, 1.f, 1.f, 1.f);
+                if (r < L) {
+                    const float2 a = *reinterpret_cast<const float2 *>(al + r * KH);
+                    g.x *= a.x;
+                    g.y *= a.y;
+                }
             }
-            named_bar(1, GATE_THREADS);  // every gate is in registers: the buffer may refill
-            if (pt == 0) mbar_arrive(s.bar(B_AL_EMPTY));
-            float4 g = a[0];
-#pragma unroll
-            for (int i = 1; i < 16; ++i) {
-                g.x *= a[i].x; g.y *= a[i].y; g.z *= a[i].z; g.w *= a[i].w;
-            }
-            *reinterpret_cast<float4 *>(scan + tg * 128 + 4 * cq) = g;
+            scan[tg * 32 + cp] = g;
             named_bar(1, GATE_THREADS);
-            float4 before = make_float4(1.f, 1.f, 1.f, 1.f), after = before;
+            float2 before = make_float2(1.f, 1.f), after = before;
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
-                const float4 x = *reinterpret_cast<const float4 *>(scan + gi * 128 + 4 * cq);
-                if (gi < tg) { before.x *= x.x; before.y *= x.y; before.z *= x.z; before.w *= x.w; }
-                if (gi > tg) { after.x *= x.x; after.y *= x.y; after.z *= x.z; after.w *= x.w; }
+                const float2 x = scan[gi * 32 + cp];
+                if (gi < tg) { before.x *= x.x; before.y *= x.y; }
+                if (gi > tg) { after.x *= x.x; after.y *= x.y; }
             }
-            const float gam[4] = {before.x * g.x * after.x, before.y * g.y * after.y, before.z * g.z * after.z,
-                                  before.w * g.w * after.w};
-            bool bad = false;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) bad |= !(gam[c] >= kMinGamma);
-            if (bad) s.flags()[4 + b] = 1;
-            named_bar(1, GATE_THREADS);
-            const bool slow = s.flags()[4 + b] != 0;
-            float inv[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) inv[c] = slow ? 1.f : rsqrtf(gam[c]);
-            if (tg == 0)
-                *reinterpret_cast<float4 *>(s.mu(b) + 4 * cq) =
-                    slow ? make_float4(1.f, 1.f, 1.f, 1.f)
-                         : make_float4(gam[0] * inv[0], gam[1] * inv[1], gam[2] * inv[2], gam[3] * inv[3]);
+            const float gam0 = before.x * g.x * after.x, gam1 = before.y * g.y * after.y;
+            // vote of this key half (the barrier also keeps the scan slots
+            // from being overwritten while others still read them)
+            const bool slow = named_bar_or(1, GATE_THREADS, !(gam0 >= kMinGamma) || !(gam1 >= kMinGamma));
+            const float inv0 = slow ? 1.f : rsqrtf(gam0), inv1 = slow ? 1.f : rsqrtf(gam1);
+            const float mu0 = gam0 * inv0, mu1 = gam1 * inv1;
+            // Kc goes to B0[b] once MMA3 of chunk n-2 in both CTAs released it
+            if (n >= 2) ok = wait_bar(s, p, B_B0_EMPTY + b, (kk - 1) & 1) && ok;
+            unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
+            unsigned char *kch = s.base + SM_B0 + b * 16384 + rank * 8192;   // Kc rows of this key half
             if (ok && !slow) {
-                unsigned char *a0 = s.base + SM_A0 + b * 32768;
-                unsigned char *b0 = s.base + SM_B0 + b * 16384;
-                // This thread's rows r = 16 tg + i live at
-                //   row(i) = kp[i & 7] + (i >> 3) * 1024 + (i & 7) * 128      (k; q at +8192)
-                // in the 128B-swizzled tile: the swizzle term depends only on i & 7.
-                const uint32_t c8 = (uint32_t)cq >> 1;
-                const uint32_t abase = (c8 >> 3) * 16384u + 2u * (uint32_t)tg * 1024u + 8u * (cq & 1);
-                unsigned char *kp[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) kp[j] = a0 + abase + (((c8 & 7u) ^ (uint32_t)j) << 4);
-                // same position in the 64-row Kc tile
-                const ptrdiff_t kc_delta = (b0 - a0) - (ptrdiff_t)((c8 >> 3) * 8192u);
-                if (L < C) {  // ragged tail: zero the raw k, q rows past the sequence once
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (16 * tg + i >= L) {
-                            unsigned char *row = kp[i & 7] + (i >> 3) * 1024 + (i & 7) * 128;
-                            *reinterpret_cast<uint2 *>(row) = make_uint2(0u, 0u);
-                            *reinterpret_cast<uint2 *>(row + 8192) = make_uint2(0u, 0u);
-                        }
-                }
-                const uint64_t inv01 = f2_make(inv[0], inv[1]), inv23 = f2_make(inv[2], inv[3]);
-                const float mu[4] = {gam[0] * inv[0], gam[1] * inv[1], gam[2] * inv[2], gam[3] * inv[3]};
                 // One pass over the rows with the running product p_r:
-                //   Kr = k p / mu, Qr = q p / mu (in place), Kc = k (gamma / p) / mu = k mu / p
-                uint64_t pr01 = f2_make(before.x, before.y), pr23 = f2_make(before.z, before.w);
-                uint2 kcv[16];  // Kc rows, stored once MMA3 of chunk n-2 has released the buffer
-                // Batches of 8 rows: a batch's loads are issued before its in-place stores.
-#pragma unroll
-                for (int i0 = 0; i0 < 16; i0 += 8) {
-                    uint2 kw[8], qw[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int i = i0 + j;
-                        const unsigned char *row = kp[i & 7] + (i >> 3) * 1024 + (i & 7) * 128;
-                        kw[j] = *reinterpret_cast<const uint2 *>(row);
-                        qw[j] = *reinterpret_cast<const uint2 *>(row + 8192);
-                    }
+                //   Kr = k p / mu, Qr = q p / mu (in place), Kc = k mu / p  (= k (gamma / p) / mu)
+                // Rows past the sequence end read as k = q = 0, alpha = 1.
+                uint64_t pr = f2_make(before.x, before.y);
+                const uint64_t invv = f2_make(inv0, inv1);
+#pragma unroll 1
+                for (int i8 = 0; i8 < 2; ++i8) {
+                    const int rb = 16 * tg + 8 * i8;
+                    const uint32_t base = (uint32_t)(2 * tg + i8) * 1024u + sub;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int i = i0 + j;
-                        pr01 = f2_mul(pr01, f2_make(a[i].x, a[i].y));
-                        pr23 = f2_mul(pr23, f2_make(a[i].z, a[i].w));
-                        const uint64_t e2a = f2_mul(pr01, inv01), e2b = f2_mul(pr23, inv23);
-                        const uint64_t e3a = f2_make(__fdividef(mu[0], f2_lo(pr01)), __fdividef(mu[1], f2_hi(pr01)));
-                        const uint64_t e3b = f2_make(__fdividef(mu[2], f2_lo(pr23)), __fdividef(mu[3], f2_hi(pr23)));
-                        const uint64_t k01 = bf2_to_f2(kw[j].x), k23 = bf2_to_f2(kw[j].y);
-                        const uint64_t q01 = bf2_to_f2(qw[j].x), q23 = bf2_to_f2(qw[j].y);
-                        unsigned char *row = kp[i & 7] + (i >> 3) * 1024 + (i & 7) * 128;
-                        *reinterpret_cast<uint2 *>(row) = make_uint2(f2_to_bf2(f2_mul(k01, e2a)), f2_to_bf2(f2_mul(k23, e2b)));
-                        *reinterpret_cast<uint2 *>(row + 8192) =
-                            make_uint2(f2_to_bf2(f2_mul(q01, e2a)), f2_to_bf2(f2_mul(q23, e2b)));
-                        kcv[i] = make_uint2(f2_to_bf2(f2_mul(k01, e3a)), f2_to_bf2(f2_mul(k23, e3b)));
+                        const int r = rb + j;
+                        const uint32_t off = base + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
+                        const bool in = r < L;
+                        const float2 a = in ? *reinterpret_cast<const float2 *>(al + r * KH) : make_float2(1.f, 1.f);
+                        const uint32_t kw = in ? *reinterpret_cast<const uint32_t *>(ah + off) : 0u;
+                        const uint32_t qw = in ? *reinterpret_cast<const uint32_t *>(ah + 8192 + off) : 0u;
+                        pr = f2_mul(pr, f2_make(a.x, a.y));
+                        const uint64_t e2 = f2_mul(pr, invv);
+                        const uint64_t e3 = f2_make(__fdividef(mu0, f2_lo(pr)), __fdividef(mu1, f2_hi(pr)));
+                        const uint64_t k2 = bf2_to_f2(kw), q2 = bf2_to_f2(qw);
+                        *reinterpret_cast<uint32_t *>(ah + off) = f2_to_bf2(f2_mul(k2, e2));
+                        *reinterpret_cast<uint32_t *>(ah + 8192 + off) = f2_to_bf2(f2_mul(q2, e2));
+                        *reinterpret_cast<uint32_t *>(kch + off) = f2_to_bf2(f2_mul(k2, e3));
                     }
                 }
-                if (n >= 2) ok = wait_bar(s, p, B_B0_EMPTY + b, (kk - 1) & 1) && ok;
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    *reinterpret_cast<uint2 *>(kp[i & 7] + (i >> 3) * 1024 + (i & 7) * 128 + kc_delta) = kcv[i];
-            } else if (n >= 2) {
-                ok = wait_bar(s, p, B_B0_EMPTY + b, (kk - 1) & 1) && ok;  // keeps the phase order
             }
+            float *mu_b = s.mu(b) + c0;
+            if (tg == 0) *reinterpret_cast<float2 *>(mu_b + 2 * cp) = make_float2(mu0, mu1);
             if (pt < 64) s.beta(b)[pt] = beta_r;
-            if (pt == 0) {
-                s.info(b)[0] = L;
-                s.info(b)[1] = slow ? 1 : 0;
-            }
+            int *vslot = s.vote(b) + 4 * rank;
+            if (pt == 0) vslot[0] = slow ? 1 : 0;
             fence_proxy_async();
-            mbar_arrive(s.bar(B_TAB_FULL + b));
+            named_bar(1, GATE_THREADS);
+            if (pt == 0) {
+                mbar_arrive(s.bar(B_AL_EMPTY + b));  // alpha of this chunk is no longer read
+                // this key half into the peer (its A0[b] / B0[b] halves were
+                // released with B0_EMPTY and QK_EMPTY of chunk n-2, both CTAs)
+                const uint32_t rbar = s.remote(s.bar(B_TAB_FULL + b));
+                bulk_s2c(s.remote(ah), ah, 16384, rbar);
+                bulk_s2c(s.remote(kch), kch, 8192, rbar);
+                bulk_s2c(s.remote(mu_b), mu_b, 256, rbar);
+                bulk_s2c(s.remote(vslot), vslot, 16, rbar);
+                // own tables are written; the peer's arrive as copies
+                mbar_arrive_expect_tx(s.bar(B_TAB_FULL + b), PUSH_TAB);
+            }
         }
     } else {
         // ------------------------------------------------------------ solve group (warps 8-11)
+        // Chunks n = rank, rank + 2, ...: their tables sit in buffer rank.
         regs_inc<REGS_SOLVE>();
         const int qt = tid - 256;
         const int q4 = warp & 3;       // TMEM lane quarter = warp index in the group
         const int R = 32 * q4 + lane;  // row of [A; P]
-        float *asc = reinterpret_cast<float *>(s.base + SM_SOLVE);  // A (strictly lower, beta-scaled)
+        float *asc = reinterpret_cast<float *>(s.base + SM_SOLVE);  // A (beta-scaled; upper part unused)
         float *tsc = asc + 64 * 64;                                  // T
         const int g8 = lane >> 2, t4 = lane & 3;
-        for (int n = 0; n < NC; ++n) {
-            const int b = n & 1, kk = n >> 1;
-            bool ok = wait_bar(s, p, B_AP_FULL + b, kk & 1);
-            ok = wait_bar(s, p, B_TAB_FULL + b, kk & 1) && ok;  // the gate group's beta / info
+        const int b = (int)rank;
+        // T's blocks above the diagonal are never written by the solve: zero
+        // them once, so the tile write needs no mask (the diagonal blocks are
+        // written whole, zeros above their diagonal included)
+        for (int e = qt; e < 6 * 256; e += SOLVE_THREADS) {
+            const int blk = e >> 8, I = blk < 3 ? 0 : (blk < 5 ? 1 : 2), J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            tsc[swz(16 * I + ((e >> 4) & 15), 16 * J + (e & 15))] = 0.f;
+        }
+        named_bar(3, SOLVE_THREADS);
+        for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
+            const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
+            bool ok = wait_bar(s, p, B_AP_FULL, i & 1);
+            ok = wait_bar(s, p, B_TAB_FULL + b, i & 1) && ok;  // beta and the votes of this chunk
             tc_fence_after();
-            named_bar(3, SOLVE_THREADS);
-            const bool go = s.flags()[1] == 0;
-            const bool work = go && s.info(b)[1] == 0;  // group-uniform
-            const int L = s.info(b)[0];
+            // group-uniform decisions: step 2 and the TMEM loads are warp-collective
+            const bool go = !named_bar_or(3, SOLVE_THREADS, s.flags()[1] != 0);
+            const bool work = go && !s.slow(b);
             uint32_t pbuf[32];
             if (work) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t r32[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + (b ? TM_AP1 : TM_AP0) + 32 * hf, r32);
+                    tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1) + 32 * hf, r32);
                     tmem_wait_ld();
                     if (R < 64) {
+                        // A row: only the strictly lower part is read later
                         const float bt = s.beta(b)[R];
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            float w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = 32 * hf + 4 * j4 + e;
-                                w[e] = j < R ? bt * __uint_as_float(r32[4 * j4 + e]) : 0.f;
-                            }
-                            *reinterpret_cast<float4 *>(asc + swz(R, 32 * hf + 4 * j4)) = make_float4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            *reinterpret_cast<float4 *>(asc + swz(R, 32 * hf + 4 * j4)) =
+                                make_float4(bt * __uint_as_float(r32[4 * j4]), bt * __uint_as_float(r32[4 * j4 + 1]),
+                                            bt * __uint_as_float(r32[4 * j4 + 2]), bt * __uint_as_float(r32[4 * j4 + 3]));
                     } else {
                         const int r = R - 64;
 #pragma unroll
@@ -825,7 +852,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 const float *b0p = rowp + 16 * blk, *b1p = rowp + ((16 * blk) ^ 16);
                 float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = i == col ? 1.f : 0.f;
+                for (int i2 = 0; i2 < 16; ++i2) x[i2] = i2 == col ? 1.f : 0.f;
 #pragma unroll
                 for (int sidx = 0; sidx < 15; ++sidx) {
                     const float xs = x[sidx];
@@ -854,9 +881,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     for (int K = J; K < I; ++K) {
 #pragma unroll
                         for (int k8 = 0; k8 < 16; k8 += 8) {
-                            const int r0 = 16 * I + g8, c0 = 16 * K + k8 + t4;
-                            const uint32_t af[4] = {to_tf32(asc[swz(r0, c0)]), to_tf32(asc[swz(r0 + 8, c0)]),
-                                                    to_tf32(asc[swz(r0, c0 + 4)]), to_tf32(asc[swz(r0 + 8, c0 + 4)])};
+                            const int r0 = 16 * I + g8, cc0 = 16 * K + k8 + t4;
+                            const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
+                                                    to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
                             const int br = 16 * K + k8 + t4;
 #pragma unroll
                             for (int nt = 0; nt < 2; ++nt) {
@@ -880,9 +907,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                         for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
 #pragma unroll
                     for (int k8 = 0; k8 < 16; k8 += 8) {
-                        const int r0 = 16 * I + g8, c0 = 16 * I + k8 + t4;
-                        const uint32_t af[4] = {to_tf32(tsc[swz(r0, c0)]), to_tf32(tsc[swz(r0 + 8, c0)]),
-                                                to_tf32(tsc[swz(r0, c0 + 4)]), to_tf32(tsc[swz(r0 + 8, c0 + 4)])};
+                        const int r0 = 16 * I + g8, cc0 = 16 * I + k8 + t4;
+                        const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
+                                                to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt)
                             mma_tf32(t[nt], af, to_tf32(ms[(k8 + t4) * 16 + 8 * nt + g8]),
@@ -900,11 +927,14 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
             }
             named_bar(3, SOLVE_THREADS);
-            // [T; P] -> the bf16 operand tile, once MMA4 of the previous chunk is done
+            // [T; P] -> the bf16 operand tile of both CTAs, once MMA4 of the
+            // previous chunk completed in both
             if (n >= 1) ok = wait_bar(s, p, B_TP_EMPTY, (n - 1) & 1) && ok;
-            if (ok && work) {
+            const bool wr = __all_sync(0xffffffffu, ok && work);
+            if (wr) {
                 unsigned char *tpt = s.base + SM_TP;
-                const int r = qt >> 1, hc = qt & 1;  // T row r, columns 32hc .. 32hc+31
+                const int r = qt >> 1, hc = qt & 1;  // T row r, columns 32hc .. 32hc+31 (exact: unit
+                                                     // diagonal, zeros above)
                 float4 tv[8];  // loads before the tile stores
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
@@ -913,32 +943,35 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    const int c8 = 4 * hc + c4;
                     const float4 x0 = tv[2 * c4], x1 = tv[2 * c4 + 1];
-                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                    float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 8 * c8 + e;
-                        y[e] = j < r ? xv[e] : (j == r ? 1.f : 0.f);
-                    }
-                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, c8, 128)) =
-                        make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, 4 * hc + c4, 128)) =
+                        make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
+                                   pack_bf16(x1.z, x1.w));
                 }
                 if (R >= 64) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8)
-                        *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(R, c8, 128)) =
-                            make_uint4(pbuf[4 * c8], pbuf[4 * c8 + 1], pbuf[4 * c8 + 2], pbuf[4 * c8 + 3]);
+                    for (int cc8 = 0; cc8 < 8; ++cc8)
+                        *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(R, cc8, 128)) =
+                            make_uint4(pbuf[4 * cc8], pbuf[4 * cc8 + 1], pbuf[4 * cc8 + 2], pbuf[4 * cc8 + 3]);
                 }
                 fence_proxy_async();
             }
-            mbar_arrive(s.bar(B_TP_FULL));
+            const bool pushed = named_bar_or(3, SOLVE_THREADS, wr);
+            if (qt == 0) {
+                const uint32_t rbar = s.remote(s.bar(B_TP_FULL));
+                if (pushed) {
+                    mbar_arrive_remote_tx(rbar, PUSH_TP);
+                    bulk_s2c(s.remote(s.base + SM_TP), s.base + SM_TP, PUSH_TP, rbar);
+                } else {
+                    mbar_arrive_remote_tx(rbar, 0);
+                }
+                mbar_arrive(s.bar(B_TP_FULL));
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still write into it
     if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
@@ -999,7 +1032,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     const int64_t ext = tokens > 0 ? tokens : 1;
     if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, DK, a.H, ext, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, DK, a.H, ext, KH, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, DV, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     TcParams p;
@@ -1021,6 +1054,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // blocks is even: one cluster of NSLICE CTAs per (sequence, head)
     kda_prefill_tc_kernel<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(p, mk, mq, ma, mv);
     return cudaGetLastError();
 }
