@@ -61,7 +61,7 @@ constexpr int NTHREADS = 512;
 // Register shares per warpgroup. Each SM sub-partition holds one warp of
 // every warpgroup, so the shares sum to 4 x 128 = the launch's allocation
 // (a larger sum would make setmaxnreg.inc wait forever).
-constexpr uint32_t REGS_EPI = 160, REGS_GATE = 112, REGS_SOLVE = 160, REGS_CTRL = 80;
+constexpr uint32_t REGS_EPI = 168, REGS_GATE = 104, REGS_SOLVE = 160, REGS_CTRL = 80;
 static_assert(REGS_EPI + REGS_GATE + REGS_SOLVE + REGS_CTRL == 4 * 128, "register split");
 // setmaxnreg.inc may only raise and .dec only lower a warp's count (from the
 // launch's 128); the wrong one is an illegal instruction.
@@ -79,37 +79,44 @@ constexpr float kMinGamma = 1.8e-35f;  // ~exp(-80)
 constexpr uint32_t TM_AP = 0, TM_XY = 128, TM_UO = 256, TM_D = 384, TM_COLS = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
+// Buffers by lifetime: A0 ([Kr; Qr]) is read by the first products of its
+// chunk and cycles through 2 slots; Kc, mu, beta and the votes are read
+// until the state update of their chunk and cycle through 3 slots, so the
+// gate can run two chunks ahead of the state chain.
 constexpr uint32_t SM_A0 = 0;          // 2 x 32 KB: [Kr; Qr], two 16 KB key-channel halves (128B swizzle)
-constexpr uint32_t SM_B0 = 65536;      // 2 x 16 KB: Kc (K-major, 64 rows), two 8 KB halves
-constexpr uint32_t SM_AL = 98304;      // 2 x 16 KB: alpha of this CTA's key channels (fp32 [64][64])
+constexpr uint32_t SM_B0 = 65536;      // 3 x 16 KB: Kc (K-major, 64 rows), two 8 KB halves
+constexpr uint32_t SM_AL = 114688;     // 16 KB: alpha of this CTA's key channels (fp32 [64][64])
 constexpr uint32_t SM_SOLVE = 131072;  // 32 KB: A and T (fp32 64x64 each, XOR-swizzled)
-constexpr uint32_t SM_V = 163840;      // 2 x 8 KB: v slice (128B swizzle)
-constexpr uint32_t SM_TP = 180224;     // 16 KB: [T; P] (K-major, 128 rows x 64)
+constexpr uint32_t SM_V = 163840;      // 8 KB: v slice (128B swizzle)
+// T and the two P slots are 8 KB K-major tiles (64 rows x 64) laid out
+// back to back, so [T; P0] and [P_{b-1}; P_b] are 128-row operands: the
+// products U = T R and P_b U use rows 0-63 and rows 64-127 of them.
+constexpr uint32_t SM_TP = 172032;     // 24 KB: T | P0 | P1
 constexpr uint32_t SM_ST = 196608;     // 16 KB: St (MN-major, 128 rows x 64)
 constexpr uint32_t SM_RU = 212992;     // 8 KB: R then U (MN-major, 64 rows x 64)
-constexpr uint32_t SM_MU = 221184;     // float[2][128]
-constexpr uint32_t SM_BETA = 222208;   // float[2][64]
-constexpr uint32_t SM_VOTE = 222720;   // int[2][8]: slow vote of key half 0 at [0], half 1 at [4]
-constexpr uint32_t SM_FLAGS = 222784;  // int[8]: [1] abort
-constexpr uint32_t SM_TMEM = 222816;   // uint32 TMEM base
-constexpr uint32_t SM_BAR = 222848;    // mbarriers (up to 40)
-constexpr uint32_t SM_RED = 223168;    // float[4][64] + float[64]: slow-path reductions
-constexpr uint32_t SM_MSCR = 224448;   // float[3][16*16]: mma.sync staging
-constexpr uint32_t SM_SCAN = 227520;   // float2[4][32]: per-group gate products
-constexpr uint32_t SM_TOTAL = 228544;
+constexpr uint32_t SM_MU = 221184;     // float[3][128]
+constexpr uint32_t SM_BETA = 222720;   // float[3][64]
+constexpr uint32_t SM_VOTE = 223488;   // int[3][8]: slow vote of key half 0 at [0], half 1 at [4]
+constexpr uint32_t SM_FLAGS = 223584;  // int[8]: [1] abort
+constexpr uint32_t SM_TMEM = 223616;   // uint32 TMEM base
+constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
+constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
+constexpr uint32_t SM_MSCR = 225232;   // float[3][16*16]: mma.sync staging
+constexpr uint32_t SM_SCAN = 228304;   // float2[4][32]: per-group gate products
+constexpr uint32_t SM_TOTAL = 229328;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 
 // Bytes one CTA pushes into its peer per chunk: its [Kr; Qr] half, its Kc
 // half, its half of mu and its slow vote.
 constexpr uint32_t PUSH_TAB = 16384 + 8192 + 256 + 16;
-constexpr uint32_t PUSH_TP = 16384;
+constexpr uint32_t PUSH_TILE = 8192;  // T or P
 constexpr uint16_t BOTH = 3;  // CTA mask of the cluster
 
 enum Bar {
-    B_QK_FULL = 0, B_QK_EMPTY = 2, B_AL_FULL = 4, B_AL_EMPTY = 6, B_V_FULL = 8, B_V_EMPTY = 10,
-    B_TAB_FULL = 12, B_B0_EMPTY = 14, B_O_READ = 16, B_AP_FULL = 18, B_TP_FULL = 19, B_TP_EMPTY = 20,
-    B_S_FULL = 21, B_XY_FULL = 22, B_R_FULL = 23, B_U_FULL = 24, B_UU_FULL = 25, B_D_FULL = 26,
-    B_DRAIN = 27, B_DRAIN_AUX = 28, B_COUNT = 29
+    B_QK_FULL = 0, B_QK_EMPTY = 2, B_AL_FULL = 4, B_V_FULL = 6,
+    B_TAB_FULL = 8, B_B0_EMPTY = 10, B_O_READ = 13, B_AP_FULL = 15, B_T_FULL = 16, B_T_EMPTY = 17,
+    B_P_FULL = 18, B_P_EMPTY = 20, B_S_FULL = 22, B_XY_FULL = 23, B_R_FULL = 24, B_U_FULL = 25, B_UU_FULL = 26,
+    B_D_FULL = 27, B_DRAIN = 28, B_DRAIN_AUX = 29, B_COUNT = 30
 };
 static_assert(B_COUNT <= 40, "mbarrier area");
 
@@ -187,12 +194,13 @@ struct Smem {
     __device__ __forceinline__ volatile int *flags() const {
         return reinterpret_cast<volatile int *>(base + SM_FLAGS);
     }
-    __device__ __forceinline__ float *mu(int b) const { return reinterpret_cast<float *>(base + SM_MU) + 128 * b; }
-    __device__ __forceinline__ float *beta(int b) const { return reinterpret_cast<float *>(base + SM_BETA) + 64 * b; }
-    __device__ __forceinline__ int *vote(int b) const { return reinterpret_cast<int *>(base + SM_VOTE) + 8 * b; }
+    // slot b3 = chunk % 3
+    __device__ __forceinline__ float *mu(int b3) const { return reinterpret_cast<float *>(base + SM_MU) + 128 * b3; }
+    __device__ __forceinline__ float *beta(int b3) const { return reinterpret_cast<float *>(base + SM_BETA) + 64 * b3; }
+    __device__ __forceinline__ int *vote(int b3) const { return reinterpret_cast<int *>(base + SM_VOTE) + 8 * b3; }
     // A chunk runs token by token when either key half voted so.
-    __device__ __forceinline__ bool slow(int b) const {
-        const volatile int *v = vote(b);
+    __device__ __forceinline__ bool slow(int b3) const {
+        const volatile int *v = vote(b3);
         return (v[0] | v[4]) != 0;
     }
     // Cluster address of this CTA's shared-memory location p in the peer.
@@ -344,18 +352,27 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(s.bar(B_QK_FULL + i), 1);
-            mbar_init(s.bar(B_QK_EMPTY + i), 2);  // MMA2 of both CTAs (multicast commits)
-            mbar_init(s.bar(B_AL_FULL + i), 1);
-            mbar_init(s.bar(B_AL_EMPTY + i), 1);
-            mbar_init(s.bar(B_V_FULL + i), 1);
-            mbar_init(s.bar(B_V_EMPTY + i), 64);
+            // MMA1 of both CTAs and MMA0 of the solving CTA (multicast commits),
+            // and the solving CTA's solve group once it holds the chunk's
+            // barrier phases (so no waiter of TAB_FULL / AP_FULL can fall two
+            // phases behind)
+            mbar_init(s.bar(B_QK_EMPTY + i), 4);
             mbar_init(s.bar(B_TAB_FULL + i), 1);  // own gate (expecting the peer's bytes) + the peer's copies
-            mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
             mbar_init(s.bar(B_O_READ + i), 64);
         }
+        for (int i = 0; i < 3; ++i) mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
+        mbar_init(s.bar(B_AL_FULL), 1);  // alpha: loaded by the gate group for its next chunk
+        mbar_init(s.bar(B_V_FULL), 1);   // v: loaded by the epilogue for its next chunk
         mbar_init(s.bar(B_AP_FULL), 1);
-        mbar_init(s.bar(B_TP_FULL), 1);   // the solving CTA: local arrive, or remote arrive + copy
-        mbar_init(s.bar(B_TP_EMPTY), 2);  // MMA4 of both CTAs
+        // T and P of a chunk: the solving CTA arrives locally, the other CTA
+        // gets a remote arrive and the copy; released by MMA2 (T) / MMA4 (P)
+        // of both CTAs
+        mbar_init(s.bar(B_T_FULL), 1);
+        mbar_init(s.bar(B_T_EMPTY), 2);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s.bar(B_P_FULL + i), 1);
+            mbar_init(s.bar(B_P_EMPTY + i), 2);
+        }
         mbar_init(s.bar(B_S_FULL), EPI_THREADS);
         mbar_init(s.bar(B_XY_FULL), 1);
         mbar_init(s.bar(B_R_FULL), 64);
@@ -384,9 +401,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_a);
-            prefetch_tmap(&tm_v);
-            int nqk = 0, nal = 0, nv = 0;  // loads issued per stream
+            int nqk = 0;  // chunks whose q, k halves were issued
             for (int n = 0; n < NC; ++n) {
                 const int b = n & 1, kk = n >> 1;
                 const int z = (int)(t_begin + (int64_t)n * C);
@@ -397,19 +412,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 tma_load_3d(a0, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
                 tma_load_3d(a0 + 8192, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
                 nqk = n + 1;
-                if (n >= 2 && !wait_bar(s, p, B_AL_EMPTY + b, (kk - 1) & 1)) break;
-                mbar_arrive_expect_tx(s.bar(B_AL_FULL + b), 16384);
-                tma_load_3d(s.base + SM_AL + b * 16384, &tm_a, s.bar(B_AL_FULL + b), c0, h, z);
-                nal = n + 1;
-                if (n >= 2 && !wait_bar(s, p, B_V_EMPTY + b, (kk - 1) & 1)) break;
-                mbar_arrive_expect_tx(s.bar(B_V_FULL + b), 8192);
-                tma_load_3d(s.base + SM_V + b * 8192, &tm_v, s.bar(B_V_FULL + b), v0, h, z);
-                nv = n + 1;
             }
             // never leave copies in flight: wait (bounded) for the last ones
             for (int n = nqk - 2 < 0 ? 0 : nqk - 2; n < nqk; ++n) mbar_wait(s.bar(B_QK_FULL + (n & 1)), (n >> 1) & 1);
-            for (int n = nal - 2 < 0 ? 0 : nal - 2; n < nal; ++n) mbar_wait(s.bar(B_AL_FULL + (n & 1)), (n >> 1) & 1);
-            for (int n = nv - 2 < 0 ? 0 : nv - 2; n < nv; ++n) mbar_wait(s.bar(B_V_FULL + (n & 1)), (n >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -424,7 +429,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             for (int n = 0; ok && n < NC; ++n) {
                 const int b = n & 1, kk = n >> 1;
                 if (!(ok = wait_bar(s, p, B_TAB_FULL + b, kk & 1))) break;
-                const bool fast = !s.slow(b);
+                const int b3 = n % 3;
+                const bool fast = !s.slow(b3);
                 const uint32_t xy = tmem + TM_XY + 64 * b, uo = tmem + TM_UO + 64 * b;
                 // MMA1: [X; Y] = [Kr; Qr] St, once the outputs of chunk n-2 left XY[b]
                 if (n >= 2 && !(ok = wait_bar(s, p, B_O_READ + b, (kk - 1) & 1))) break;
@@ -432,38 +438,42 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 tc_fence_after();
                 if (fast) {
                     const uint32_t a0 = a0_base + b * 32768;
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(xy, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(st + ks * 2048, 16384, 1024), I_KM_MN, ks > 0);
                 }
                 umma_commit(s.bar(B_XY_FULL));
-                // MMA2: U = T R (rows 0-63 of [T; P] R)
+                umma_commit_mc(s.bar(B_QK_EMPTY + b), BOTH);  // A0[b] read
+                // MMA2: U = T R (rows 0-63 of [T; P0] R)
                 if (!(ok = wait_bar(s, p, B_R_FULL, n & 1))) break;
-                if (!(ok = wait_bar(s, p, B_TP_FULL, n & 1))) break;
-                tc_fence_after();
-                if (fast)
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(uo, sdesc_sw128(tp + ks * 32, 16, 1024), sdesc_sw128(ru + ks * 2048, 8192, 1024),
-                                  I_KM_MN, ks > 0);
-                umma_commit(s.bar(B_U_FULL));
-                // A0[b] is free in both CTAs once MMA2 of both completed (the
-                // [A; P] product of this chunk finished before [T; P] existed)
-                umma_commit_mc(s.bar(B_QK_EMPTY + b), BOTH);
-                // MMA3: D += Kc^T U (state update); MMA4: O2 = P U (rows 64-127)
-                if (!(ok = wait_bar(s, p, B_UU_FULL, n & 1))) break;
+                if (!(ok = wait_bar(s, p, B_T_FULL, n & 1))) break;
                 tc_fence_after();
                 if (fast) {
-                    const uint32_t b0 = b0_base + b * 16384;
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tmem + TM_D, sdesc_sw128(b0 + ks * 2048, 8192, 1024),
-                                  sdesc_sw128(ru + ks * 2048, 8192, 1024), I_MN_MN, 1);
+#pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
                         umma_bf16(uo, sdesc_sw128(tp + ks * 32, 16, 1024), sdesc_sw128(ru + ks * 2048, 8192, 1024),
                                   I_KM_MN, ks > 0);
                 }
+                umma_commit(s.bar(B_U_FULL));
+                umma_commit_mc(s.bar(B_T_EMPTY), BOTH);
+                // MMA3: D += Kc^T U (state update); MMA4: O2 = P U (rows 64-127 of [P_{b-1}; P_b] U)
+                if (!(ok = wait_bar(s, p, B_UU_FULL, n & 1))) break;
+                if (!(ok = wait_bar(s, p, B_P_FULL + b, kk & 1))) break;
+                tc_fence_after();
+                if (fast) {
+                    const uint32_t b0 = b0_base + b3 * 16384, pa = tp + 8192 * b;
+#pragma unroll 1
+                    for (int ks = 0; ks < 4; ++ks) {
+                        umma_bf16(tmem + TM_D, sdesc_sw128(b0 + ks * 2048, 8192, 1024),
+                                  sdesc_sw128(ru + ks * 2048, 8192, 1024), I_MN_MN, 1);
+                        umma_bf16(uo, sdesc_sw128(pa + ks * 32, 16, 1024), sdesc_sw128(ru + ks * 2048, 8192, 1024),
+                                  I_KM_MN, ks > 0);
+                    }
+                }
                 umma_commit(s.bar(B_D_FULL));
-                umma_commit_mc(s.bar(B_B0_EMPTY + b), BOTH);
-                umma_commit_mc(s.bar(B_TP_EMPTY), BOTH);
+                umma_commit_mc(s.bar(B_B0_EMPTY + b3), BOTH);
+                umma_commit_mc(s.bar(B_P_EMPTY + b), BOTH);
             }
             // drain: every MMA issued has completed before TMEM is released
             umma_commit(s.bar(B_DRAIN));
@@ -474,17 +484,19 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // ------------------------------------------------------------ [A; P] issuer (this CTA's parity)
         if (lane == 0) {
             constexpr uint32_t I_AP = idesc_bf16(128, 64, false, false);
-            const uint32_t a0 = smem_u32(s.base + SM_A0) + rank * 32768, b0 = smem_u32(s.base + SM_B0) + rank * 16384;
+            const uint32_t a0 = smem_u32(s.base + SM_A0) + rank * 32768;
             for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
-                if (!wait_bar(s, p, B_TAB_FULL + (int)rank, i & 1)) break;  // chunk n uses buffer n & 1 = rank
+                if (!wait_bar(s, p, B_TAB_FULL + (int)rank, i & 1)) break;  // chunk n uses A0 slot n & 1 = rank
                 tc_fence_after();
-                if (!s.slow((int)rank)) {
+                const uint32_t b0 = smem_u32(s.base + SM_B0) + (n % 3) * 16384;
+                if (!s.slow(n % 3)) {
                     const uint32_t d = tmem + TM_AP + 64 * (i & 1);
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(d, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(b0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), I_AP, ks > 0);
                 }
                 umma_commit(s.bar(B_AP_FULL));
+                umma_commit_mc(s.bar(B_QK_EMPTY + (int)rank), BOTH);  // A0[rank] read
             }
             umma_commit(s.bar(B_DRAIN_AUX));
             mbar_wait(s.bar(B_DRAIN_AUX), 0);
@@ -502,12 +514,18 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // conditions around them are warp-uniform.
         const int l = tid;  // TMEM lane: key channel (state) or token row
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // The v slice is single-buffered and refilled by this group as soon
+        // as E1 has read it (thread 0 issues the copy).
+        if (tid == 0) {
+            mbar_arrive_expect_tx(s.bar(B_V_FULL), 8192);
+            tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)t_begin);
+        }
         const uint32_t tm_d = tmem + lane_off + TM_D;
         uint32_t r32[32];
         bool ok = wait_bar(s, p, B_TAB_FULL, 0);
         // The chunk's slow flag and mu are read once, as soon as its tables
-        // exist, and kept in registers: the gate of chunk n + 2 overwrites them.
-        bool slow_cur = ok && s.slow(0);
+        // exist, and kept in registers: the gate of chunk n + 3 overwrites them.
+        bool slow_cur = s.slow(0);
         float mu_cur = (ok && !slow_cur) ? s.mu(0)[l] : 1.f;
         bool slow_prev = false;
         // St_0 = Diag(mu_0) S0 -> TMEM (fp32 accumulator base) and the bf16 operand
@@ -539,7 +557,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         }
 
         for (int n = 0; n <= NC; ++n) {
-            const int b = n & 1, kk = n >> 1;
+            const int b = n & 1;
             if (warp >= 2 && n >= 1) {
                 // Outputs of chunk n-1 (token rows 64-127 of XY and UO): O = Y + P U.
                 // Off the state chain: MMA1 of chunk n+1 waits for this read.
@@ -578,13 +596,13 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (warp < 2) {
                 // E1: R = beta (V - X) for token rows 0-63
                 ok = wait_bar(s, p, B_XY_FULL, n & 1) && ok;
-                ok = wait_bar(s, p, B_V_FULL + b, kk & 1) && ok;
+                ok = wait_bar(s, p, B_V_FULL, n & 1) && ok;
                 tc_fence_after();
                 const bool act = __all_sync(0xffffffffu, ok && !slow_cur);
                 unsigned char *ru = s.base + SM_RU;
                 if (act) {
-                    const float bt = s.beta(b)[l];
-                    const unsigned char *vt = s.base + SM_V + b * 8192;
+                    const float bt = s.beta(n % 3)[l];
+                    const unsigned char *vt = s.base + SM_V;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         uint4 vrow[4];  // the v row first: no load waits behind an R store
@@ -611,7 +629,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
                 tc_fence_before();
                 mbar_arrive(s.bar(B_R_FULL));
-                mbar_arrive(s.bar(B_V_EMPTY + b));
+                named_bar(4, 64);  // both E1 warps have read v: load the next chunk's
+                if (tid == 0 && n + 1 < NC) {
+                    mbar_arrive_expect_tx(s.bar(B_V_FULL), 8192);
+                    tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)(tok0 + C));
+                }
                 // E2: U -> bf16 operand (replaces R, which MMA2 has consumed)
                 ok = wait_bar(s, p, B_U_FULL, n & 1) && ok;
                 tc_fence_after();
@@ -636,20 +658,25 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 mbar_arrive(s.bar(B_UU_FULL));
             }
             // E3: the state S_{n+1} = mu_n D -> St_{n+1} = mu_{n+1} S_{n+1}
-            ok = wait_bar(s, p, B_D_FULL, n & 1) && ok;
-            tc_fence_after();
-            // one decision for the whole group (the slow path has group barriers)
-            const bool go = !named_bar_or(2, EPI_THREADS, s.flags()[1] != 0);
-            if (go && slow_cur)
-                slow_chunk(p.alpha, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d, l,
-                           warp, lane, tok0, L, H, h, v0);
             const bool last = n == NC - 1;
             float mu_next = 1.f;
             bool slow_next = false;
-            if (!last) {
+            if (!last) {  // the next chunk's tables exist long before D_FULL
                 ok = wait_bar(s, p, B_TAB_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1) && ok;
-                slow_next = ok && s.slow((n + 1) & 1);
-                if (ok && !slow_next) mu_next = s.mu((n + 1) & 1)[l];
+                // every thread reads the same slot: it changes only once the
+                // state update of chunk n+1 released it, or never after an abort
+                slow_next = s.slow((n + 1) % 3);
+                if (ok && !slow_next) mu_next = s.mu((n + 1) % 3)[l];
+            }
+            ok = wait_bar(s, p, B_D_FULL, n & 1) && ok;
+            tc_fence_after();
+            bool go = s.flags()[1] == 0;
+            if (slow_cur) {  // group-uniform (every thread read the same votes)
+                // one decision for the whole group: the slow path has group barriers
+                go = !named_bar_or(2, EPI_THREADS, !go);
+                if (go)
+                    slow_chunk(p.alpha, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d,
+                               l, warp, lane, tok0, L, H, h, v0);
             }
             unsigned char *st = s.base + SM_ST;
             float *fin = p.sT ? p.sT + state_off + (int64_t)l * DV + v0 : nullptr;
@@ -699,15 +726,23 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // Byte offset of this thread's 4 bytes in row 16 tg + 8 i8 + j of a
         // 128B-swizzled 64-column tile: rowbase(i8) + j * 128 + ((c8 ^ j) << 4) + sub.
         const uint32_t c8 = (uint32_t)cp >> 2, sub = ((uint32_t)cp & 3u) * 4u;
+        // alpha is single-buffered and refilled by this group once a chunk's
+        // pass is done (thread pt == 0 issues the copy)
+        if (pt == 0) {
+            prefetch_tmap(&tm_a);
+            mbar_arrive_expect_tx(s.bar(B_AL_FULL), 16384);
+            tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)t_begin);
+        }
         for (int n = 0; n < NC; ++n) {
             const int b = n & 1, kk = n >> 1;
             const int64_t tok0 = t_begin + (int64_t)n * C;
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
             // beta of this chunk, loaded before the waits so its latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
+            const int b3 = n % 3;
             bool ok = wait_bar(s, p, B_QK_FULL + b, kk & 1);
-            ok = wait_bar(s, p, B_AL_FULL + b, kk & 1) && ok;
-            const float *al = reinterpret_cast<const float *>(s.base + SM_AL + b * 16384) + 2 * cp;
+            ok = wait_bar(s, p, B_AL_FULL, n & 1) && ok;
+            const float *al = reinterpret_cast<const float *>(s.base + SM_AL) + 2 * cp;
             // products of this thread's 16 rows, then the 4 group products
             float2 g = make_float2(1.f, 1.f);
 #pragma unroll 4
@@ -734,10 +769,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             const bool slow = named_bar_or(1, GATE_THREADS, !(gam0 >= kMinGamma) || !(gam1 >= kMinGamma));
             const float inv0 = slow ? 1.f : rsqrtf(gam0), inv1 = slow ? 1.f : rsqrtf(gam1);
             const float mu0 = gam0 * inv0, mu1 = gam1 * inv1;
-            // Kc goes to B0[b] once MMA3 of chunk n-2 in both CTAs released it
-            if (n >= 2) ok = wait_bar(s, p, B_B0_EMPTY + b, (kk - 1) & 1) && ok;
+            // Kc, mu, beta and the votes go to slot n % 3 once the state update
+            // of chunk n-3 released it in both CTAs
+            if (n >= 3) ok = wait_bar(s, p, B_B0_EMPTY + b3, ((n / 3) - 1) & 1) && ok;
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
-            unsigned char *kch = s.base + SM_B0 + b * 16384 + rank * 8192;   // Kc rows of this key half
+            unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
             if (ok && !slow) {
                 // One pass over the rows with the running product p_r:
                 //   Kr = k p / mu, Qr = q p / mu (in place), Kc = k mu / p  (= k (gamma / p) / mu)
@@ -766,17 +802,23 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     }
                 }
             }
-            float *mu_b = s.mu(b) + c0;
-            if (tg == 0) *reinterpret_cast<float2 *>(mu_b + 2 * cp) = make_float2(mu0, mu1);
-            if (pt < 64) s.beta(b)[pt] = beta_r;
-            int *vslot = s.vote(b) + 4 * rank;
-            if (pt == 0) vslot[0] = slow ? 1 : 0;
+            // (after an abort nothing more is written: slots that others may
+            // still read stay as they are)
+            float *mu_b = s.mu(b3) + c0;
+            if (ok && tg == 0) *reinterpret_cast<float2 *>(mu_b + 2 * cp) = make_float2(mu0, mu1);
+            if (ok && pt < 64) s.beta(b3)[pt] = beta_r;
+            int *vslot = s.vote(b3) + 4 * rank;
+            if (ok && pt == 0) vslot[0] = slow ? 1 : 0;
             fence_proxy_async();
             named_bar(1, GATE_THREADS);
-            if (pt == 0) {
-                mbar_arrive(s.bar(B_AL_EMPTY + b));  // alpha of this chunk is no longer read
-                // this key half into the peer (its A0[b] / B0[b] halves were
-                // released with B0_EMPTY and QK_EMPTY of chunk n-2, both CTAs)
+            if (pt == 0 && n + 1 < NC) {  // alpha of this chunk is no longer read
+                mbar_arrive_expect_tx(s.bar(B_AL_FULL), 16384);
+                tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)(tok0 + C));
+            }
+            if (ok && pt == 0) {
+                // this key half into the peer (its A0 slot was released with
+                // QK_EMPTY of chunk n-2, its slot n % 3 with B0_EMPTY of chunk
+                // n-3, in both CTAs)
                 const uint32_t rbar = s.remote(s.bar(B_TAB_FULL + b));
                 bulk_s2c(s.remote(ah), ah, 16384, rbar);
                 bulk_s2c(s.remote(kch), kch, 8192, rbar);
@@ -788,7 +830,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         }
     } else {
         // ------------------------------------------------------------ solve group (warps 8-11)
-        // Chunks n = rank, rank + 2, ...: their tables sit in buffer rank.
+        // Chunks n = rank, rank + 2, ...: their [Kr; Qr] sit in A0 slot rank.
         regs_inc<REGS_SOLVE>();
         const int qt = tid - 256;
         const int q4 = warp & 3;       // TMEM lane quarter = warp index in the group
@@ -807,39 +849,73 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         named_bar(3, SOLVE_THREADS);
         for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
-            bool ok = wait_bar(s, p, B_AP_FULL, i & 1);
-            ok = wait_bar(s, p, B_TAB_FULL + b, i & 1) && ok;  // beta and the votes of this chunk
+            const int b3 = n % 3;
+            bool ok = wait_bar(s, p, B_TAB_FULL + b, i & 1);  // beta and the votes of this chunk
+            ok = wait_bar(s, p, B_AP_FULL, i & 1) && ok;
             tc_fence_after();
             // group-uniform decisions: step 2 and the TMEM loads are warp-collective
             const bool go = !named_bar_or(3, SOLVE_THREADS, s.flags()[1] != 0);
-            const bool work = go && !s.slow(b);
-            uint32_t pbuf[32];
+            // every thread of the group is past this chunk's TAB_FULL and
+            // AP_FULL phases: A0 slot b may be refilled in both CTAs
+            if (qt == 0) {
+                mbar_arrive(s.bar(B_QK_EMPTY + b));
+                mbar_arrive_remote_tx(s.remote(s.bar(B_QK_EMPTY + b)), 0);
+            }
+            const bool work = go && !s.slow(b3);
+            uint32_t r64[2][32];  // [A; P] row R: both halves in flight before one wait
             if (work) {
+                const uint32_t ta = tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1);
+                tmem_ld32(ta, r64[0]);
+                tmem_ld32(ta + 32, r64[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                if (R < 64) {
+                    // A row (beta-scaled; only the strictly lower part is read later)
+                    const float bt = s.beta(b3)[R];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t r32[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1) + 32 * hf, r32);
-                    tmem_wait_ld();
-                    if (R < 64) {
-                        // A row: only the strictly lower part is read later
-                        const float bt = s.beta(b)[R];
+                    for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4)
-                            *reinterpret_cast<float4 *>(asc + swz(R, 32 * hf + 4 * j4)) =
-                                make_float4(bt * __uint_as_float(r32[4 * j4]), bt * __uint_as_float(r32[4 * j4 + 1]),
-                                            bt * __uint_as_float(r32[4 * j4 + 2]), bt * __uint_as_float(r32[4 * j4 + 3]));
-                    } else {
-                        const int r = R - 64;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int j = 32 * hf + 2 * e;
-                            const float x0 = (j <= r && r < L) ? __uint_as_float(r32[2 * e]) : 0.f;
-                            const float x1 = (j + 1 <= r && r < L) ? __uint_as_float(r32[2 * e + 1]) : 0.f;
-                            pbuf[16 * hf + e] = pack_bf16(x0, x1);
-                        }
-                    }
+                            *reinterpret_cast<float4 *>(asc + swz(R, 32 * hf + 4 * j4)) = make_float4(
+                                bt * __uint_as_float(r64[hf][4 * j4]), bt * __uint_as_float(r64[hf][4 * j4 + 1]),
+                                bt * __uint_as_float(r64[hf][4 * j4 + 2]), bt * __uint_as_float(r64[hf][4 * j4 + 3]));
                 }
-                tc_fence_before();
+            }
+            if (q4 >= 2) {
+                // P row r (masked: j <= r, rows past the sequence end zero) into
+                // slot b of the P tiles once MMA4 of chunk n-2 released it in both
+                // CTAs, then to the peer
+                if (n >= 2) ok = wait_bar(s, p, B_P_EMPTY + b, ((n >> 1) - 1) & 1) && ok;
+                const bool wr = __all_sync(0xffffffffu, ok && work);
+                if (wr) {
+                    const int r = R - 64;
+                    unsigned char *pt = s.base + SM_TP + 8192 * (b + 1);
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 8 * c8 + 2 * e;
+                            const uint32_t u0 = r64[c8 >> 2][(8 * c8 + 2 * e) & 31], u1 = r64[c8 >> 2][(8 * c8 + 2 * e + 1) & 31];
+                            w[e] = pack_bf16((j <= r && r < L) ? __uint_as_float(u0) : 0.f,
+                                             (j + 1 <= r && r < L) ? __uint_as_float(u1) : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(pt + kmajor_chunk(r, c8, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async();
+                }
+                const bool pushed = named_bar_or(5, 64, wr);
+                if (qt == 64) {
+                    const uint32_t rbar = s.remote(s.bar(B_P_FULL + b));
+                    unsigned char *pt = s.base + SM_TP + 8192 * (b + 1);
+                    if (pushed) {
+                        mbar_arrive_remote_tx(rbar, PUSH_TILE);
+                        bulk_s2c(s.remote(pt), pt, PUSH_TILE, rbar);
+                    } else {
+                        mbar_arrive_remote_tx(rbar, 0);
+                    }
+                    mbar_arrive(s.bar(B_P_FULL + b));
+                }
             }
             named_bar(3, SOLVE_THREADS);
             if (work && q4 < 2) {
@@ -927,45 +1003,34 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
             }
             named_bar(3, SOLVE_THREADS);
-            // [T; P] -> the bf16 operand tile of both CTAs, once MMA4 of the
-            // previous chunk completed in both
-            if (n >= 1) ok = wait_bar(s, p, B_TP_EMPTY, (n - 1) & 1) && ok;
+            // T -> the bf16 operand tile of both CTAs, once MMA2 of the previous
+            // chunk completed in both
+            if (n >= 1) ok = wait_bar(s, p, B_T_EMPTY, (n - 1) & 1) && ok;
             const bool wr = __all_sync(0xffffffffu, ok && work);
             if (wr) {
                 unsigned char *tpt = s.base + SM_TP;
                 const int r = qt >> 1, hc = qt & 1;  // T row r, columns 32hc .. 32hc+31 (exact: unit
                                                      // diagonal, zeros above)
-                float4 tv[8];  // loads before the tile stores
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    tv[2 * c4] = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4)));
-                    tv[2 * c4 + 1] = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4) + 4));
-                }
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const float4 x0 = tv[2 * c4], x1 = tv[2 * c4 + 1];
-                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, 4 * hc + c4, 128)) =
+                    const float4 x0 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4)));
+                    const float4 x1 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4) + 4));
+                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, 4 * hc + c4, 64)) =
                         make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
                                    pack_bf16(x1.z, x1.w));
-                }
-                if (R >= 64) {
-#pragma unroll
-                    for (int cc8 = 0; cc8 < 8; ++cc8)
-                        *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(R, cc8, 128)) =
-                            make_uint4(pbuf[4 * cc8], pbuf[4 * cc8 + 1], pbuf[4 * cc8 + 2], pbuf[4 * cc8 + 3]);
                 }
                 fence_proxy_async();
             }
             const bool pushed = named_bar_or(3, SOLVE_THREADS, wr);
             if (qt == 0) {
-                const uint32_t rbar = s.remote(s.bar(B_TP_FULL));
+                const uint32_t rbar = s.remote(s.bar(B_T_FULL));
                 if (pushed) {
-                    mbar_arrive_remote_tx(rbar, PUSH_TP);
-                    bulk_s2c(s.remote(s.base + SM_TP), s.base + SM_TP, PUSH_TP, rbar);
+                    mbar_arrive_remote_tx(rbar, PUSH_TILE);
+                    bulk_s2c(s.remote(s.base + SM_TP), s.base + SM_TP, PUSH_TILE, rbar);
                 } else {
                     mbar_arrive_remote_tx(rbar, 0);
                 }
-                mbar_arrive(s.bar(B_TP_FULL));
+                mbar_arrive(s.bar(B_T_FULL));
             }
         }
     }
