@@ -119,6 +119,37 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def rank_env():
+    """(world, rank, local_rank) from the launcher's environment; (1, 0, 0)
+    when run alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_seed(rank: int) -> int:
+    """Seed of a rank's batch. Every rank draws its own independent batch of
+    (sequence, head) work: weak scaling, nothing is exchanged."""
+    return rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (the job's time). The only collective of the
+    benchmark besides its barriers; `device` is the tensor's device for the
+    process group's backend (cuda for nccl, cpu for gloo)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, seconds: float) -> float:
+    """Whole-job throughput: the tokens of all ranks over the slowest rank's time."""
+    return world * tokens_per_rank / seconds
+
+
 def kernel_traffic(kernel_file: str, key: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel (else None)."""
@@ -164,7 +195,7 @@ def cpu_baseline_oracle(target_s: float = 12.0):
 
 def run_reference(args):
     """The reference arm: the float64 oracle on the host cores (rank 0 only)."""
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return
     import oracle
@@ -215,9 +246,7 @@ def main():
     import kda_gated_delta_chunkwise_gb300 as kda
     from kda_gated_delta_chunkwise_gb300 import workloads as W
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -230,7 +259,7 @@ def main():
             dist.barrier()
 
     # ---- inputs (seeded; each rank its own batch) ----
-    x = W.prefill_4x16x4096(seed=rank)
+    x = W.prefill_4x16x4096(seed=shard_seed(rank))
     q, k, v, a, b = (t.to(dev) for t in x.tensors())
     o = torch.empty_like(v)
     sT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=dev)
@@ -262,12 +291,9 @@ def main():
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * B * T / (ms_per_step / 1e3)
+    value = job_tokens_per_s(world, B * T, ms_per_step / 1e3)
 
     algo_bytes = prefill_bytes(B, T, H, DK, DV)
     algo_flops = prefill_flops(B, T, H, DK, DV)
@@ -300,18 +326,15 @@ def main():
             oh, sh = kda.prefill(hq, hk, hv, ha, hb, None, algo=args.algo)  # returns host tensors
         torch.cuda.synchronize()
         dt = (time.perf_counter() - t0) / n_e2e
-        if world > 1:
-            tt = torch.tensor([dt], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            dt = float(tt.item())
-        e2e = {"value": world * B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        dt = max_over_ranks(dt, world, dev)
+        e2e = {"value": job_tokens_per_s(world, B * T, dt), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
 
     # ---- decode step (secondary figure of the metric) ----
     decode = None
     if not args.no_decode:
         del q, k, v, a, b, o, sT
-        xd = W.decode_256x32(seed=rank)
+        xd = W.decode_256x32(seed=shard_seed(rank))
         dq, dk_, dv_, da, db = (t.to(dev) for t in xd.tensors())
         state = xd.initial_state.to(dev)
         do = torch.empty_like(dv_)
