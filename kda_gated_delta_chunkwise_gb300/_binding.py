@@ -116,14 +116,27 @@ def _need(t, name, dtype=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _to_host(x: torch.Tensor) -> torch.Tensor:
+    """Device -> pinned host copy, queued on the current stream (pinned buffers
+    come from torch's caching host allocator, so repeated calls reuse them)."""
+    h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    h.copy_(x, non_blocking=True)
+    return h
+
+
 def _host_call(fn, tensors: dict, **kw):
-    """Run ``fn`` on the CUDA device for host inputs; return host outputs."""
+    """Run ``fn`` on the CUDA device for host inputs; return host outputs.
+    Inputs in pinned memory are copied asynchronously; outputs land in pinned
+    host memory and are complete when this returns."""
     dev = torch.device("cuda", torch.cuda.current_device())
     moved = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in tensors.items()}
     out = fn(**moved, **kw)
     if isinstance(out, tuple):
-        return tuple(None if x is None else x.to("cpu") for x in out)
-    return out.to("cpu")
+        res = tuple(None if x is None else _to_host(x) for x in out)
+    else:
+        res = _to_host(out)
+    torch.cuda.current_stream(dev).synchronize()
+    return res
 
 
 def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: bool = True,

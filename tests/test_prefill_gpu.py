@@ -166,3 +166,16 @@ def test_zero_length_copies_state(kda):
     torch.testing.assert_close(s, s0, rtol=0, atol=0)
     _, s = kda.prefill(e, e, e, e, torch.empty(2, 0, 3, device=d), None)
     assert torch.count_nonzero(s) == 0
+
+
+def test_host_buffers_round_trip(kda):
+    """Host (pinned) inputs go through the same kernels: outputs come back to
+    pinned host memory, bitwise equal to the device call."""
+    x = W.batched(2, 200, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=31)
+    q, k, v, a, b, s0 = _dev(x)
+    o_d, s_d = kda.prefill(q, k, v, a, b, s0)
+    host = [t.pin_memory() for t in x.tensors()]
+    o_h, s_h = kda.prefill(*host, x.initial_state.pin_memory())
+    assert o_h.device.type == "cpu" and o_h.is_pinned()
+    torch.testing.assert_close(o_h, o_d.cpu(), rtol=0, atol=0)
+    torch.testing.assert_close(s_h, s_d.cpu(), rtol=0, atol=0)
