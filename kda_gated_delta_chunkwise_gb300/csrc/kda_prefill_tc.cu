@@ -138,14 +138,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
-    return __bfloat1622float2(h);
-}
 // Two fp32 values packed in 64 bits, multiplied pairwise by one instruction.
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 __device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
@@ -579,8 +585,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const int j = 8 * c4 + 2 * e;
-                                    w[e] = pack_bf16(__uint_as_float(y32[j]) + __uint_as_float(r32[j]),
-                                                     __uint_as_float(y32[j + 1]) + __uint_as_float(r32[j + 1]));
+                                    w[e] = f2_to_bf2(f2_add((uint64_t)y32[j] | ((uint64_t)y32[j + 1] << 32),
+                                                            (uint64_t)r32[j] | ((uint64_t)r32[j + 1] << 32)));
                                 }
                                 *reinterpret_cast<uint4 *>(dst + 32 * hf + 8 * c4) = make_uint4(w[0], w[1], w[2], w[3]);
                             }
@@ -602,6 +608,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 unsigned char *ru = s.base + SM_RU;
                 if (act) {
                     const float bt = s.beta(n % 3)[l];
+                    const uint64_t bt2 = f2_make(bt, bt);
                     const unsigned char *vt = s.base + SM_V;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
@@ -617,9 +624,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                             uint32_t ow[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float2 vf = unpack_bf16(vw[e]);
-                                ow[e] = pack_bf16(bt * (vf.x - __uint_as_float(r32[8 * c4 + 2 * e])),
-                                                  bt * (vf.y - __uint_as_float(r32[8 * c4 + 2 * e + 1])));
+                                const uint64_t x2 = (uint64_t)r32[8 * c4 + 2 * e] | ((uint64_t)r32[8 * c4 + 2 * e + 1] << 32);
+                                ow[e] = f2_to_bf2(f2_mul(f2_sub(bf2_to_f2(vw[e]), x2), bt2));
                             }
                             *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -680,30 +686,35 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             }
             unsigned char *st = s.base + SM_ST;
             float *fin = p.sT ? p.sT + state_off + (int64_t)l * DV + v0 : nullptr;
+            // one scale per row: mu_n mu_{n+1} (the state) or mu_n (the final state)
+            const float sc = last ? mu_cur : mu_cur * mu_next;
+            const uint64_t sc2 = f2_make(sc, sc);
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 tmem_ld32(tm_d + 32 * hf, r32);
                 tmem_wait_ld();
-                float x[32];
+                uint64_t x2[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = mu_cur * __uint_as_float(r32[j]);
+                for (int j = 0; j < 16; ++j)
+                    x2[j] = f2_mul((uint64_t)r32[2 * j] | ((uint64_t)r32[2 * j + 1] << 32), sc2);
                 if (last) {
                     if (go && fin)
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(fin + 32 * hf + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                        for (int j = 0; j < 16; j += 2)
+                            *reinterpret_cast<float4 *>(fin + 32 * hf + 2 * j) =
+                                make_float4(f2_lo(x2[j]), f2_hi(x2[j]), f2_lo(x2[j + 1]), f2_hi(x2[j + 1]));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        x[j] *= mu_next;
-                        r32[j] = __float_as_uint(x[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        r32[2 * j] = (uint32_t)x2[j];
+                        r32[2 * j + 1] = (uint32_t)(x2[j] >> 32);
                     }
                     tmem_st32(tm_d + 32 * hf, r32);
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4)
                         *reinterpret_cast<uint4 *>(st + row128_chunk(l, 4 * hf + c4)) =
-                            make_uint4(pack_bf16(x[8 * c4], x[8 * c4 + 1]), pack_bf16(x[8 * c4 + 2], x[8 * c4 + 3]),
-                                       pack_bf16(x[8 * c4 + 4], x[8 * c4 + 5]), pack_bf16(x[8 * c4 + 6], x[8 * c4 + 7]));
+                            make_uint4(f2_to_bf2(x2[4 * c4]), f2_to_bf2(x2[4 * c4 + 1]), f2_to_bf2(x2[4 * c4 + 2]),
+                                       f2_to_bf2(x2[4 * c4 + 3]));
                 }
             }
             if (!last) {
