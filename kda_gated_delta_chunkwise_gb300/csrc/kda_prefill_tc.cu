@@ -61,7 +61,7 @@ constexpr int NTHREADS = 512;
 // Register shares per warpgroup. Each SM sub-partition holds one warp of
 // every warpgroup, so the shares sum to 4 x 128 = the launch's allocation
 // (a larger sum would make setmaxnreg.inc wait forever).
-constexpr uint32_t REGS_EPI = 168, REGS_GATE = 104, REGS_SOLVE = 160, REGS_CTRL = 80;
+constexpr uint32_t REGS_EPI = 168, REGS_GATE = 104, REGS_SOLVE = 152, REGS_CTRL = 88;
 static_assert(REGS_EPI + REGS_GATE + REGS_SOLVE + REGS_CTRL == 4 * 128, "register split");
 // setmaxnreg.inc may only raise and .dec only lower a warp's count (from the
 // launch's 128); the wrong one is an illegal instruction.
@@ -102,8 +102,8 @@ constexpr uint32_t SM_TMEM = 223616;   // uint32 TMEM base
 constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
 constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
 constexpr uint32_t SM_MSCR = 225232;   // float[3][16*16]: mma.sync staging
-constexpr uint32_t SM_SCAN = 228304;   // float2[4][32]: per-group gate products
-constexpr uint32_t SM_TOTAL = 229328;
+constexpr uint32_t SM_SCAN = 228304;   // float4[8][16]: per-group gate products
+constexpr uint32_t SM_TOTAL = 230352;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 
 // Bytes one CTA pushes into its peer per chunk: its [Kr; Qr] half, its Kc
@@ -729,14 +729,15 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------ gate group (warps 4-7)
-        // Thread: key channels c0 + 2cp, c0 + 2cp + 1; token rows 16tg .. 16tg+15.
+        // Thread: key channels c0 + 4cq .. c0 + 4cq + 3; token rows 8rg .. 8rg+7.
         regs_dec<REGS_GATE>();  // below the launch's 128: a decrease
         const int pt = tid - 128;
-        const int cp = pt & 31, tg = pt >> 5;
-        float2 *scan = reinterpret_cast<float2 *>(s.base + SM_SCAN);
-        // Byte offset of this thread's 4 bytes in row 16 tg + 8 i8 + j of a
-        // 128B-swizzled 64-column tile: rowbase(i8) + j * 128 + ((c8 ^ j) << 4) + sub.
-        const uint32_t c8 = (uint32_t)cp >> 2, sub = ((uint32_t)cp & 3u) * 4u;
+        const int cq = pt & 15, rg = pt >> 4;
+        float4 *scan = reinterpret_cast<float4 *>(s.base + SM_SCAN);
+        // Byte offset of this thread's 8 bytes in row 8 rg + j of a 128B-swizzled
+        // 64-column tile: rg * 1024 + j * 128 + ((c8 ^ j) << 4) + sub.
+        const uint32_t c8 = (uint32_t)cq >> 1, sub = ((uint32_t)cq & 1u) * 8u;
+        const uint32_t rowbase = (uint32_t)rg * 1024u + sub;
         // alpha is single-buffered and refilled by this group once a chunk's
         // pass is done (thread pt == 0 issues the copy)
         if (pt == 0) {
@@ -753,70 +754,88 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             const int b3 = n % 3;
             bool ok = wait_bar(s, p, B_QK_FULL + b, kk & 1);
             ok = wait_bar(s, p, B_AL_FULL, n & 1) && ok;
-            const float *al = reinterpret_cast<const float *>(s.base + SM_AL) + 2 * cp;
-            // products of this thread's 16 rows, then the 4 group products
-            float2 g = make_float2(1.f, 1.f);
-#pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const int r = 16 * tg + i;
-                if (r < L) {
-                    const float2 a = *reinterpret_cast<const float2 *>(al + r * KH);
-                    g.x *= a.x;
-                    g.y *= a.y;
-                }
-            }
-            scan[tg * 32 + cp] = g;
-            named_bar(1, GATE_THREADS);
-            float2 before = make_float2(1.f, 1.f), after = before;
+            // alpha row r of this thread's channels (1 past the sequence end)
+            const float4 *al = reinterpret_cast<const float4 *>(s.base + SM_AL) + cq;
+            auto alpha_row = [&](int r) {
+                return r < L ? al[r * (KH / 4)] : make_float4(1.f, 1.f, 1.f, 1.f);
+            };
+            // products of this thread's 8 rows, then the 8 group products
+            float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-                const float2 x = scan[gi * 32 + cp];
-                if (gi < tg) { before.x *= x.x; before.y *= x.y; }
-                if (gi > tg) { after.x *= x.x; after.y *= x.y; }
+            for (int j = 0; j < 8; ++j) {
+                const float4 a = alpha_row(8 * rg + j);
+                g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
             }
-            const float gam0 = before.x * g.x * after.x, gam1 = before.y * g.y * after.y;
+            scan[rg * 16 + cq] = g;
+            named_bar(1, GATE_THREADS);
+            float4 before = make_float4(1.f, 1.f, 1.f, 1.f), after = before;
+#pragma unroll
+            for (int gi = 0; gi < 8; ++gi) {
+                const float4 x = scan[gi * 16 + cq];
+                if (gi < rg) { before.x *= x.x; before.y *= x.y; before.z *= x.z; before.w *= x.w; }
+                if (gi > rg) { after.x *= x.x; after.y *= x.y; after.z *= x.z; after.w *= x.w; }
+            }
+            const float gm[4] = {before.x * g.x * after.x, before.y * g.y * after.y, before.z * g.z * after.z,
+                                 before.w * g.w * after.w};
+            bool bad = false;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) bad |= !(gm[c] >= kMinGamma);
             // vote of this key half (the barrier also keeps the scan slots
             // from being overwritten while others still read them)
-            const bool slow = named_bar_or(1, GATE_THREADS, !(gam0 >= kMinGamma) || !(gam1 >= kMinGamma));
-            const float inv0 = slow ? 1.f : rsqrtf(gam0), inv1 = slow ? 1.f : rsqrtf(gam1);
-            const float mu0 = gam0 * inv0, mu1 = gam1 * inv1;
+            const bool slow = named_bar_or(1, GATE_THREADS, bad);
+            float inv[4], mu[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                inv[c] = slow ? 1.f : rsqrtf(gm[c]);
+                mu[c] = gm[c] * inv[c];
+            }
             // Kc, mu, beta and the votes go to slot n % 3 once the state update
             // of chunk n-3 released it in both CTAs
             if (n >= 3) ok = wait_bar(s, p, B_B0_EMPTY + b3, ((n / 3) - 1) & 1) && ok;
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
             unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
             if (ok && !slow) {
-                // One pass over the rows with the running product p_r:
-                //   Kr = k p / mu, Qr = q p / mu (in place), Kc = k mu / p  (= k (gamma / p) / mu)
                 // Rows past the sequence end read as k = q = 0, alpha = 1.
-                uint64_t pr = f2_make(before.x, before.y);
-                const uint64_t invv = f2_make(inv0, inv1);
-#pragma unroll 1
-                for (int i8 = 0; i8 < 2; ++i8) {
-                    const int rb = 16 * tg + 8 * i8;
-                    const uint32_t base = (uint32_t)(2 * tg + i8) * 1024u + sub;
+                const uint64_t inv01 = f2_make(inv[0], inv[1]), inv23 = f2_make(inv[2], inv[3]);
+                // Backward over the rows with the suffix product s_r (gates after
+                // row r): Kc = k s / mu  (= k mu / p). It reads the raw k, so it
+                // runs before the forward pass overwrites k in place.
+                uint64_t sf01 = f2_make(after.x, after.y), sf23 = f2_make(after.z, after.w);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int r = rb + j;
-                        const uint32_t off = base + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
-                        const bool in = r < L;
-                        const float2 a = in ? *reinterpret_cast<const float2 *>(al + r * KH) : make_float2(1.f, 1.f);
-                        const uint32_t kw = in ? *reinterpret_cast<const uint32_t *>(ah + off) : 0u;
-                        const uint32_t qw = in ? *reinterpret_cast<const uint32_t *>(ah + 8192 + off) : 0u;
-                        pr = f2_mul(pr, f2_make(a.x, a.y));
-                        const uint64_t e2 = f2_mul(pr, invv);
-                        const uint64_t e3 = f2_make(__fdividef(mu0, f2_lo(pr)), __fdividef(mu1, f2_hi(pr)));
-                        const uint64_t k2 = bf2_to_f2(kw), q2 = bf2_to_f2(qw);
-                        *reinterpret_cast<uint32_t *>(ah + off) = f2_to_bf2(f2_mul(k2, e2));
-                        *reinterpret_cast<uint32_t *>(ah + 8192 + off) = f2_to_bf2(f2_mul(q2, e2));
-                        *reinterpret_cast<uint32_t *>(kch + off) = f2_to_bf2(f2_mul(k2, e3));
-                    }
+                for (int j = 7; j >= 0; --j) {
+                    const int r = 8 * rg + j;
+                    const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
+                    const uint2 kw = r < L ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
+                    const float4 a = alpha_row(r);
+                    const uint64_t e01 = f2_mul(sf01, inv01), e23 = f2_mul(sf23, inv23);
+                    *reinterpret_cast<uint2 *>(kch + off) =
+                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(kw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(kw.y), e23)));
+                    sf01 = f2_mul(sf01, f2_make(a.x, a.y));
+                    sf23 = f2_mul(sf23, f2_make(a.z, a.w));
+                }
+                // Forward with the running product p_r: Kr = k p / mu, Qr = q p / mu, in place.
+                uint64_t pr01 = f2_make(before.x, before.y), pr23 = f2_make(before.z, before.w);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = 8 * rg + j;
+                    const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
+                    const bool in = r < L;
+                    const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
+                    const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
+                    const float4 a = alpha_row(r);
+                    pr01 = f2_mul(pr01, f2_make(a.x, a.y));
+                    pr23 = f2_mul(pr23, f2_make(a.z, a.w));
+                    const uint64_t e01 = f2_mul(pr01, inv01), e23 = f2_mul(pr23, inv23);
+                    *reinterpret_cast<uint2 *>(ah + off) =
+                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(kw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(kw.y), e23)));
+                    *reinterpret_cast<uint2 *>(ah + 8192 + off) =
+                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(qw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(qw.y), e23)));
                 }
             }
             // (after an abort nothing more is written: slots that others may
             // still read stay as they are)
             float *mu_b = s.mu(b3) + c0;
-            if (ok && tg == 0) *reinterpret_cast<float2 *>(mu_b + 2 * cp) = make_float2(mu0, mu1);
+            if (ok && rg == 0) *reinterpret_cast<float4 *>(mu_b + 4 * cq) = make_float4(mu[0], mu[1], mu[2], mu[3]);
             if (ok && pt < 64) s.beta(b3)[pt] = beta_r;
             int *vslot = s.vote(b3) + 4 * rank;
             if (ok && pt == 0) vslot[0] = slow ? 1 : 0;
