@@ -61,7 +61,7 @@ constexpr int NTHREADS = 512;
 // Register shares per warpgroup. Each SM sub-partition holds one warp of
 // every warpgroup, so the shares sum to 4 x 128 = the launch's allocation
 // (a larger sum would make setmaxnreg.inc wait forever).
-constexpr uint32_t REGS_EPI = 168, REGS_GATE = 104, REGS_SOLVE = 152, REGS_CTRL = 88;
+constexpr uint32_t REGS_EPI = 176, REGS_GATE = 104, REGS_SOLVE = 144, REGS_CTRL = 88;
 static_assert(REGS_EPI + REGS_GATE + REGS_SOLVE + REGS_CTRL == 4 * 128, "register split");
 // setmaxnreg.inc may only raise and .dec only lower a warp's count (from the
 // launch's 128); the wrong one is an illegal instruction.
@@ -213,19 +213,25 @@ struct Smem {
     __device__ __forceinline__ uint32_t remote(const void *p) const { return mapa(smem_u32(p), peer); }
 };
 
-// Out of line: it runs only after a wait timed out. Raises the abort flag
-// here and in the peer, and records the error code.
-__device__ __noinline__ void report(uint32_t flag_addr, uint32_t peer, int32_t *err, int code) {
-    asm volatile("st.shared.u32 [%0], 1;" ::"r"(flag_addr) : "memory");
-    st_cluster_u32(mapa(flag_addr, peer), 1u);
-    atomicOr(err ? err : &g_tc_error, code);
-}
-// Wait with the cluster-wide abort check; returns false when the CTA must stop.
-__device__ __forceinline__ bool wait_bar(const Smem &s, const TcParams &p, int i, uint32_t parity) {
-    if (s.flags()[1]) return false;
-    if (mbar_wait(s.bar(i), parity)) return true;
-    report(smem_u32(s.base + SM_FLAGS + 4), s.peer, p.err, 2);
-    return false;
+// Bounded wait. try_wait suspends the thread for up to about a microsecond
+// while the phase is open, so the loop bound (kMaxWaitTries rounds) gives up
+// after about a second, or after tens of milliseconds should try_wait return
+// at once; both lie far beyond any wait of a working kernel. A timeout sets
+// the abort flag (bit 1: this CTA timed out; the error is reported once at
+// exit). After a failed wait the callers skip their remaining waits
+// (ok = ok && wait_bar(...)), so a CTA that gives up winds down after at most
+// one timeout per warp group.
+constexpr uint32_t kMaxWaitTries = 1u << 20;
+__device__ __forceinline__ bool wait_bar(const Smem &s, const TcParams &, int i, uint32_t parity) {
+    uint32_t it = 0;
+#pragma unroll 1
+    while (!mbar_try_wait(s.bar(i), parity)) {
+        if (++it > kMaxWaitTries) {
+            s.flags()[1] = 3;
+            return false;
+        }
+    }
+    return true;
 }
 
 // Sum over the warp of eight per-lane values (one per column), reduced and
@@ -599,10 +605,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (n == NC) break;
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
             const int64_t tok0 = t_begin + (int64_t)n * C;
+            ok = ok && s.flags()[1] == 0;  // stop waiting once the CTA gave up
             if (warp < 2) {
                 // E1: R = beta (V - X) for token rows 0-63
-                ok = wait_bar(s, p, B_XY_FULL, n & 1) && ok;
-                ok = wait_bar(s, p, B_V_FULL, n & 1) && ok;
+                ok = ok && wait_bar(s, p, B_XY_FULL, n & 1);
+                ok = ok && wait_bar(s, p, B_V_FULL, n & 1);
                 tc_fence_after();
                 const bool act = __all_sync(0xffffffffu, ok && !slow_cur);
                 unsigned char *ru = s.base + SM_RU;
@@ -641,7 +648,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)(tok0 + C));
                 }
                 // E2: U -> bf16 operand (replaces R, which MMA2 has consumed)
-                ok = wait_bar(s, p, B_U_FULL, n & 1) && ok;
+                ok = ok && wait_bar(s, p, B_U_FULL, n & 1);
                 tc_fence_after();
                 if (__all_sync(0xffffffffu, act && ok)) {
 #pragma unroll 1
@@ -668,13 +675,13 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             float mu_next = 1.f;
             bool slow_next = false;
             if (!last) {  // the next chunk's tables exist long before D_FULL
-                ok = wait_bar(s, p, B_TAB_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1) && ok;
+                ok = ok && wait_bar(s, p, B_TAB_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1);
                 // every thread reads the same slot: it changes only once the
                 // state update of chunk n+1 released it, or never after an abort
                 slow_next = s.slow((n + 1) % 3);
                 if (ok && !slow_next) mu_next = s.mu((n + 1) % 3)[l];
             }
-            ok = wait_bar(s, p, B_D_FULL, n & 1) && ok;
+            ok = ok && wait_bar(s, p, B_D_FULL, n & 1);
             tc_fence_after();
             bool go = s.flags()[1] == 0;
             if (slow_cur) {  // group-uniform (every thread read the same votes)
@@ -745,6 +752,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             mbar_arrive_expect_tx(s.bar(B_AL_FULL), 16384);
             tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)t_begin);
         }
+        bool alive = true;
         for (int n = 0; n < NC; ++n) {
             const int b = n & 1, kk = n >> 1;
             const int64_t tok0 = t_begin + (int64_t)n * C;
@@ -752,8 +760,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // beta of this chunk, loaded before the waits so its latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
             const int b3 = n % 3;
-            bool ok = wait_bar(s, p, B_QK_FULL + b, kk & 1);
-            ok = wait_bar(s, p, B_AL_FULL, n & 1) && ok;
+            alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
+            bool ok = alive && wait_bar(s, p, B_QK_FULL + b, kk & 1);
+            ok = ok && wait_bar(s, p, B_AL_FULL, n & 1);
             // alpha row r of this thread's channels (1 past the sequence end)
             const float4 *al = reinterpret_cast<const float4 *>(s.base + SM_AL) + cq;
             auto alpha_row = [&](int r) {
@@ -791,7 +800,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             }
             // Kc, mu, beta and the votes go to slot n % 3 once the state update
             // of chunk n-3 released it in both CTAs
-            if (n >= 3) ok = wait_bar(s, p, B_B0_EMPTY + b3, ((n / 3) - 1) & 1) && ok;
+            if (n >= 3) ok = ok && wait_bar(s, p, B_B0_EMPTY + b3, ((n / 3) - 1) & 1);
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
             unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
             if (ok && !slow) {
@@ -801,7 +810,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // row r): Kc = k s / mu  (= k mu / p). It reads the raw k, so it
                 // runs before the forward pass overwrites k in place.
                 uint64_t sf01 = f2_make(after.x, after.y), sf23 = f2_make(after.z, after.w);
-#pragma unroll
+#pragma unroll 1
                 for (int j = 7; j >= 0; --j) {
                     const int r = 8 * rg + j;
                     const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
@@ -815,7 +824,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
                 // Forward with the running product p_r: Kr = k p / mu, Qr = q p / mu, in place.
                 uint64_t pr01 = f2_make(before.x, before.y), pr23 = f2_make(before.z, before.w);
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < 8; ++j) {
                     const int r = 8 * rg + j;
                     const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
@@ -857,6 +866,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // own tables are written; the peer's arrive as copies
                 mbar_arrive_expect_tx(s.bar(B_TAB_FULL + b), PUSH_TAB);
             }
+            alive = ok;
         }
     } else {
         // ------------------------------------------------------------ solve group (warps 8-11)
@@ -877,11 +887,13 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             tsc[swz(16 * I + ((e >> 4) & 15), 16 * J + (e & 15))] = 0.f;
         }
         named_bar(3, SOLVE_THREADS);
+        bool alive = true;
         for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
             const int b3 = n % 3;
-            bool ok = wait_bar(s, p, B_TAB_FULL + b, i & 1);  // beta and the votes of this chunk
-            ok = wait_bar(s, p, B_AP_FULL, i & 1) && ok;
+            alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
+            bool ok = alive && wait_bar(s, p, B_TAB_FULL + b, i & 1);  // beta and the votes of this chunk
+            ok = ok && wait_bar(s, p, B_AP_FULL, i & 1);
             tc_fence_after();
             // group-uniform decisions: step 2 and the TMEM loads are warp-collective
             const bool go = !named_bar_or(3, SOLVE_THREADS, s.flags()[1] != 0);
@@ -915,7 +927,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // P row r (masked: j <= r, rows past the sequence end zero) into
                 // slot b of the P tiles once MMA4 of chunk n-2 released it in both
                 // CTAs, then to the peer
-                if (n >= 2) ok = wait_bar(s, p, B_P_EMPTY + b, ((n >> 1) - 1) & 1) && ok;
+                if (n >= 2) ok = ok && wait_bar(s, p, B_P_EMPTY + b, ((n >> 1) - 1) & 1);
                 const bool wr = __all_sync(0xffffffffu, ok && work);
                 if (wr) {
                     const int r = R - 64;
@@ -1035,7 +1047,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             named_bar(3, SOLVE_THREADS);
             // T -> the bf16 operand tile of both CTAs, once MMA2 of the previous
             // chunk completed in both
-            if (n >= 1) ok = wait_bar(s, p, B_T_EMPTY, (n - 1) & 1) && ok;
+            if (n >= 1) ok = ok && wait_bar(s, p, B_T_EMPTY, (n - 1) & 1);
             const bool wr = __all_sync(0xffffffffu, ok && work);
             if (wr) {
                 unsigned char *tpt = s.base + SM_TP;
@@ -1062,9 +1074,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 }
                 mbar_arrive(s.bar(B_T_FULL));
             }
+            alive = ok;
         }
     }
 
+    if (tid == 0 && (s.flags()[1] & 2)) atomicOr(p.err ? p.err : &g_tc_error, 2);  // a wait here timed out
     tc_fence_before();
     cluster_sync();  // neither CTA leaves while the other may still write into it
     if (warp == WARP_MMA) {
