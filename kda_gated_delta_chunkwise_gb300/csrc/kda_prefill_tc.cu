@@ -29,16 +29,22 @@
 // mbarriers; the tensor-core issuers signal buffer releases to both CTAs with
 // multicast tcgen05.commit.
 //
-// 512 threads per CTA, four warpgroups with their own register budgets:
-//   warps 0-3   epilogue: the state chain (R, U, state), the outputs O
-//   warps 4-7   gate: products, mu, Kr / Qr / Kc for this CTA's key channels
-//   warps 8-11  solve (chunks of this CTA's parity): A/P read-out,
-//               T = (I + A)^{-1}, the [T; P] tile for both CTAs
-//   warp 12     TMA producer (this CTA's halves of q, k, alpha; its v slice)
-//   warp 13     MMA issuer of the state chain (one thread), TMEM owner
-//   warp 14     MMA issuer of [A; P] on this CTA's parity; warp 15 idle
-// The groups work on consecutive chunks at once. All waits are bounded; on a
-// timeout the CTA records an error, tells its peer and winds down.
+// 512 threads per CTA. Roles are placed by SM sub-partition (warp id mod 4),
+// so that each sub-partition runs the code of only two busy roles (the
+// instruction caches thrash with more):
+//   warps 0-3        epilogue: the state chain (R, U, state), the outputs O
+//   warps 6,7,10,11  gate (sub-partitions 2, 3): products, mu, Kr / Qr / Kc
+//                    for this CTA's key channels; for chunks of this CTA's
+//                    parity also the P rows of [A; P] (TMEM lanes 64-127)
+//   warps 4,5,8,9    solve (sub-partitions 0, 1), chunks of this CTA's parity:
+//                    the A rows (TMEM lanes 0-63), T = (I + A)^{-1}, T tile
+//   warp 12          TMA producer of this CTA's q, k halves (the epilogue and
+//                    the gate refill v and alpha themselves)
+//   warp 13          MMA issuer of the state chain (one thread), TMEM owner
+//   warp 14          MMA issuer of [A; P] on this CTA's parity; warp 15 idle
+// Register budgets per warpgroup (setmaxnreg): epilogue 152, warps 4-11 128,
+// control 104. The groups work on consecutive chunks at once. All waits are
+// bounded; a CTA whose wait times out records an error and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -61,11 +67,11 @@ constexpr int NTHREADS = 512;
 // Register shares per warpgroup. Each SM sub-partition holds one warp of
 // every warpgroup, so the shares sum to 4 x 128 = the launch's allocation
 // (a larger sum would make setmaxnreg.inc wait forever).
-constexpr uint32_t REGS_EPI = 176, REGS_GATE = 104, REGS_SOLVE = 144, REGS_CTRL = 88;
-static_assert(REGS_EPI + REGS_GATE + REGS_SOLVE + REGS_CTRL == 4 * 128, "register split");
+constexpr uint32_t REGS_EPI = 152, REGS_PREP = 128, REGS_CTRL = 104;
+static_assert(REGS_EPI + 2 * REGS_PREP + REGS_CTRL == 4 * 128, "register split");
 // setmaxnreg.inc may only raise and .dec only lower a warp's count (from the
 // launch's 128); the wrong one is an illegal instruction.
-static_assert(REGS_EPI >= 128 && REGS_SOLVE >= 128 && REGS_GATE <= 128 && REGS_CTRL <= 128, "inc / dec");
+static_assert(REGS_EPI >= 128 && REGS_PREP == 128 && REGS_CTRL <= 128, "inc / dec (warpgroups 1, 2 keep 128)");
 constexpr int EPI_THREADS = 128;
 constexpr int GATE_THREADS = 128;
 constexpr int SOLVE_THREADS = 128;
@@ -101,7 +107,7 @@ constexpr uint32_t SM_FLAGS = 223584;  // int[8]: [1] abort
 constexpr uint32_t SM_TMEM = 223616;   // uint32 TMEM base
 constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
 constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
-constexpr uint32_t SM_MSCR = 225232;   // float[3][16*16]: mma.sync staging
+constexpr uint32_t SM_MSCR = 225232;   // float[4][16*8]: mma.sync staging (3 KB reserved)
 constexpr uint32_t SM_SCAN = 228304;   // float4[8][16]: per-group gate products
 constexpr uint32_t SM_TOTAL = 230352;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
@@ -734,11 +740,12 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             mu_cur = mu_next;
             slow_cur = slow_next;
         }
-    } else if (warp < 8) {
-        // ------------------------------------------------------------ gate group (warps 4-7)
+    } else if ((warp & 3) >= 2) {
+        // ------------------------------------------------------------ gate group (warps 6, 7, 10, 11)
         // Thread: key channels c0 + 4cq .. c0 + 4cq + 3; token rows 8rg .. 8rg+7.
-        regs_dec<REGS_GATE>();  // below the launch's 128: a decrease
-        const int pt = tid - 128;
+        // (SM sub-partitions 2 and 3; TMEM lanes 64-127, the P rows of [A; P])
+        const int gw = ((warp >> 3) << 1) | (warp & 1);  // 6, 7, 10, 11 -> 0..3
+        const int pt = 32 * gw + lane;
         const int cq = pt & 15, rg = pt >> 4;
         float4 *scan = reinterpret_cast<float4 *>(s.base + SM_SCAN);
         // Byte offset of this thread's 8 bytes in row 8 rg + j of a 128B-swizzled
@@ -753,7 +760,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)t_begin);
         }
         bool alive = true;
-        for (int n = 0; n < NC; ++n) {
+        for (int n = 0; n <= NC; ++n) {
+          if (n < NC) {
             const int b = n & 1, kk = n >> 1;
             const int64_t tok0 = t_begin + (int64_t)n * C;
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
@@ -867,14 +875,66 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 mbar_arrive_expect_tx(s.bar(B_TAB_FULL + b), PUSH_TAB);
             }
             alive = ok;
+          }
+            // ---- P read-out of chunk m = n - 1 when this CTA solves it: by now
+            // its [A; P] product has long completed (it waited only for the
+            // tables of m, which preceded the gate of n)
+            const int m = n - 1;
+            if (m < 0 || (m & 1) != (int)rank) continue;
+            const int bm = m & 1, im = m >> 1;
+            const int Lm = (int)((T - (int64_t)m * C) < C ? (T - (int64_t)m * C) : C);
+            bool okp = alive && wait_bar(s, p, B_AP_FULL, im & 1);
+            tc_fence_after();
+            const bool gop = !named_bar_or(1, GATE_THREADS, s.flags()[1] != 0);
+            const bool workp = gop && !s.slow(m % 3);
+            // P row r (masked: j <= r, rows past the sequence end zero), columns
+            // 32 hq .. 32 hq + 31, into slot bm of the P tiles once MMA4 of chunk
+            // m-2 released it in both CTAs, then to the peer
+            if (m >= 2) okp = okp && wait_bar(s, p, B_P_EMPTY + bm, ((m >> 1) - 1) & 1);
+            const bool wr = __all_sync(0xffffffffu, okp && workp);
+            unsigned char *ptile = s.base + SM_TP + 8192 * (bm + 1);
+            if (wr) {
+                const int hq = gw >> 1, r = 32 * ((warp & 3) - 2) + lane;
+                const int lim = r < Lm ? r : -1;  // last unmasked column
+                uint32_t r32[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TM_AP + 64 * (im & 1) + 32 * hq, r32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 32 * hq + 8 * c4 + 2 * e;
+                        w[e] = pack_bf16(j <= lim ? __uint_as_float(r32[8 * c4 + 2 * e]) : 0.f,
+                                         j + 1 <= lim ? __uint_as_float(r32[8 * c4 + 2 * e + 1]) : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(ptile + kmajor_chunk(r, 4 * hq + c4, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async();
+            }
+            tc_fence_before();
+            const bool pushed = named_bar_or(1, GATE_THREADS, wr);
+            if (pt == 0) {
+                const uint32_t rbar = s.remote(s.bar(B_P_FULL + bm));
+                if (pushed) {
+                    mbar_arrive_remote_tx(rbar, PUSH_TILE);
+                    bulk_s2c(s.remote(ptile), ptile, PUSH_TILE, rbar);
+                } else {
+                    mbar_arrive_remote_tx(rbar, 0);
+                }
+                mbar_arrive(s.bar(B_P_FULL + bm));
+            }
+            alive = okp;
         }
     } else {
-        // ------------------------------------------------------------ solve group (warps 8-11)
+        // ------------------------------------------------------------ solve group (warps 4, 5, 8, 9)
         // Chunks n = rank, rank + 2, ...: their [Kr; Qr] sit in A0 slot rank.
-        regs_inc<REGS_SOLVE>();
-        const int qt = tid - 256;
-        const int q4 = warp & 3;       // TMEM lane quarter = warp index in the group
-        const int R = 32 * q4 + lane;  // row of [A; P]
+        // (SM sub-partitions 0 and 1; TMEM lanes 0-63, the A rows of [A; P])
+        const int gw = ((warp >> 3) << 1) | (warp & 1);  // 4, 5, 8, 9 -> 0..3
+        const int qt = 32 * gw + lane;
+        const int q4 = warp & 3;           // TMEM lane quarter (0 or 1)
+        const int R = 32 * q4 + lane;      // row of A
+        const int hq = gw >> 1;            // column half of the A read-out
         float *asc = reinterpret_cast<float *>(s.base + SM_SOLVE);  // A (beta-scaled; upper part unused)
         float *tsc = asc + 64 * 64;                                  // T
         const int g8 = lane >> 2, t4 = lane & 3;
@@ -889,7 +949,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         named_bar(3, SOLVE_THREADS);
         bool alive = true;
         for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
-            const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
             const int b3 = n % 3;
             alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
             bool ok = alive && wait_bar(s, p, B_TAB_FULL + b, i & 1);  // beta and the votes of this chunk
@@ -904,68 +963,27 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 mbar_arrive_remote_tx(s.remote(s.bar(B_QK_EMPTY + b)), 0);
             }
             const bool work = go && !s.slow(b3);
-            uint32_t r64[2][32];  // [A; P] row R: both halves in flight before one wait
             if (work) {
-                const uint32_t ta = tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1);
-                tmem_ld32(ta, r64[0]);
-                tmem_ld32(ta + 32, r64[1]);
+                // A row R, columns 32 hq .. 32 hq + 31 (beta-scaled; only the
+                // strictly lower part is read later)
+                uint32_t r32[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1) + 32 * hq, r32);
                 tmem_wait_ld();
                 tc_fence_before();
-                if (R < 64) {
-                    // A row (beta-scaled; only the strictly lower part is read later)
-                    const float bt = s.beta(b3)[R];
+                const float bt = s.beta(b3)[R];
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4)
-                            *reinterpret_cast<float4 *>(asc + swz(R, 32 * hf + 4 * j4)) = make_float4(
-                                bt * __uint_as_float(r64[hf][4 * j4]), bt * __uint_as_float(r64[hf][4 * j4 + 1]),
-                                bt * __uint_as_float(r64[hf][4 * j4 + 2]), bt * __uint_as_float(r64[hf][4 * j4 + 3]));
-                }
-            }
-            if (q4 >= 2) {
-                // P row r (masked: j <= r, rows past the sequence end zero) into
-                // slot b of the P tiles once MMA4 of chunk n-2 released it in both
-                // CTAs, then to the peer
-                if (n >= 2) ok = ok && wait_bar(s, p, B_P_EMPTY + b, ((n >> 1) - 1) & 1);
-                const bool wr = __all_sync(0xffffffffu, ok && work);
-                if (wr) {
-                    const int r = R - 64;
-                    unsigned char *pt = s.base + SM_TP + 8192 * (b + 1);
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 8 * c8 + 2 * e;
-                            const uint32_t u0 = r64[c8 >> 2][(8 * c8 + 2 * e) & 31], u1 = r64[c8 >> 2][(8 * c8 + 2 * e + 1) & 31];
-                            w[e] = pack_bf16((j <= r && r < L) ? __uint_as_float(u0) : 0.f,
-                                             (j + 1 <= r && r < L) ? __uint_as_float(u1) : 0.f);
-                        }
-                        *reinterpret_cast<uint4 *>(pt + kmajor_chunk(r, c8, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    fence_proxy_async();
-                }
-                const bool pushed = named_bar_or(5, 64, wr);
-                if (qt == 64) {
-                    const uint32_t rbar = s.remote(s.bar(B_P_FULL + b));
-                    unsigned char *pt = s.base + SM_TP + 8192 * (b + 1);
-                    if (pushed) {
-                        mbar_arrive_remote_tx(rbar, PUSH_TILE);
-                        bulk_s2c(s.remote(pt), pt, PUSH_TILE, rbar);
-                    } else {
-                        mbar_arrive_remote_tx(rbar, 0);
-                    }
-                    mbar_arrive(s.bar(B_P_FULL + b));
-                }
+                for (int j4 = 0; j4 < 8; ++j4)
+                    *reinterpret_cast<float4 *>(asc + swz(R, 32 * hq + 4 * j4)) =
+                        make_float4(bt * __uint_as_float(r32[4 * j4]), bt * __uint_as_float(r32[4 * j4 + 1]),
+                                    bt * __uint_as_float(r32[4 * j4 + 2]), bt * __uint_as_float(r32[4 * j4 + 3]));
             }
             named_bar(3, SOLVE_THREADS);
-            if (work && q4 < 2) {
+            if (work && gw < 2) {
                 // T step 1: the four 16x16 diagonal blocks, one thread per column
                 // (x_r -= A[r][s] x_s for s < r); rows are compile-time so the A
                 // loads take immediate offsets from two base pointers (the
                 // swizzle flips bit 4 of the column for rows with r & 7 >= 4).
-                const int blk = 2 * q4 + (lane >> 4), col = lane & 15;
+                const int blk = 2 * gw + (lane >> 4), col = lane & 15;
                 const float *rowp = asc + (16 * blk) * 64;
                 const float *b0p = rowp + 16 * blk, *b1p = rowp + ((16 * blk) ^ 16);
                 float x[16];
@@ -985,63 +1003,90 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 for (int rl = 0; rl < 16; ++rl) tsc[swz(16 * blk + rl, 16 * blk + col)] = x[rl];
             }
             named_bar(3, SOLVE_THREADS);
-            if (work && q4 < 3) {
-                // T step 2 for block column J = q4, one warp, on mma.sync (tf32):
-                // T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ for I = J+1 .. 3
-                const int J = q4;
-                float *ms = reinterpret_cast<float *>(s.base + SM_MSCR) + J * 256;
-                for (int I = J + 1; I < 4; ++I) {
-                    float m[2][4];
+            // T step 2, two levels of 32-row blocks (tf32 mma.sync, all four warps):
+            //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (one 8-column half each)
+            //   T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32])
+            // (T's blocks above the diagonal are zero; the product A21 T1 is
+            // staged in A's unused upper-right quadrant).
+            if (work) {
+                // level A: warps gw 0, 1 -> T_10, gw 2, 3 -> T_32; 8-column half nt
+                const int I = gw < 2 ? 1 : 3, J = I - 1, nt = gw & 1;
+                float *ms = reinterpret_cast<float *>(s.base + SM_MSCR) + gw * 128;  // 16 x 8
+                float mq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int k8 = 0; k8 < 16; k8 += 8) {
+                    const int r0 = 16 * I + g8, cc0 = 16 * J + k8 + t4;
+                    const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
+                                            to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
+                    const int br = 16 * J + k8 + t4, bc = 16 * J + 8 * nt + g8;
+                    mma_tf32(mq, af, to_tf32(tsc[swz(br, bc)]), to_tf32(tsc[swz(br + 4, bc)]));
+                }
+                ms[g8 * 8 + 2 * t4] = mq[0];
+                ms[g8 * 8 + 2 * t4 + 1] = mq[1];
+                ms[(g8 + 8) * 8 + 2 * t4] = mq[2];
+                ms[(g8 + 8) * 8 + 2 * t4 + 1] = mq[3];
+                __syncwarp();
+                float tq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int k8 = 0; k8 < 16; k8 += 8) {
+                    const int r0 = 16 * I + g8, cc0 = 16 * I + k8 + t4;
+                    const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
+                                            to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
+                    mma_tf32(tq, af, to_tf32(ms[(k8 + t4) * 8 + g8]), to_tf32(ms[(k8 + t4 + 4) * 8 + g8]));
+                }
+                const int c = 16 * J + 8 * nt + 2 * t4;
+                tsc[swz(16 * I + g8, c)] = -tq[0];
+                tsc[swz(16 * I + g8, c + 1)] = -tq[1];
+                tsc[swz(16 * I + g8 + 8, c)] = -tq[2];
+                tsc[swz(16 * I + g8 + 8, c + 1)] = -tq[3];
+            }
+            named_bar(3, SOLVE_THREADS);
+            // levels B and C: warp gw owns rows 32 + 16 (gw >> 1) .. +15 and the
+            // 8-column tiles 2 (gw & 1), 2 (gw & 1) + 1 of a 32 x 32 result
+            const int mt = gw >> 1, ntb = 2 * (gw & 1);
+            if (work) {  // level B: M2 = A[32:64, 0:32] T[0:32, 0:32] -> asc[0:32, 32:64]
+                float mq[2][4] = {};
+#pragma unroll 1
+                for (int k8 = 0; k8 < 32; k8 += 8) {
+                    const int r0 = 32 + 16 * mt + g8, cc0 = k8 + t4;
+                    const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
+                                            to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) m[nt][e] = 0.f;
-                    for (int K = J; K < I; ++K) {
-#pragma unroll
-                        for (int k8 = 0; k8 < 16; k8 += 8) {
-                            const int r0 = 16 * I + g8, cc0 = 16 * K + k8 + t4;
-                            const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
-                                                    to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
-                            const int br = 16 * K + k8 + t4;
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const int bc = 16 * J + 8 * nt + g8;
-                                mma_tf32(m[nt], af, to_tf32(tsc[swz(br, bc)]), to_tf32(tsc[swz(br + 4, bc)]));
-                            }
-                        }
+                    for (int u = 0; u < 2; ++u) {
+                        const int bc = 8 * (ntb + u) + g8;
+                        mma_tf32(mq[u], af, to_tf32(tsc[swz(k8 + t4, bc)]), to_tf32(tsc[swz(k8 + t4 + 4, bc)]));
                     }
+                }
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        ms[g8 * 16 + 8 * nt + 2 * t4] = m[nt][0];
-                        ms[g8 * 16 + 8 * nt + 2 * t4 + 1] = m[nt][1];
-                        ms[(g8 + 8) * 16 + 8 * nt + 2 * t4] = m[nt][2];
-                        ms[(g8 + 8) * 16 + 8 * nt + 2 * t4 + 1] = m[nt][3];
+                for (int u = 0; u < 2; ++u) {
+                    const int r = 16 * mt + g8, c = 32 + 8 * (ntb + u) + 2 * t4;
+                    asc[swz(r, c)] = mq[u][0];
+                    asc[swz(r, c + 1)] = mq[u][1];
+                    asc[swz(r + 8, c)] = mq[u][2];
+                    asc[swz(r + 8, c + 1)] = mq[u][3];
+                }
+            }
+            named_bar(3, SOLVE_THREADS);
+            if (work) {  // level C: T[32:64, 0:32] = -T[32:64, 32:64] M2
+                float tq[2][4] = {};
+#pragma unroll 1
+                for (int k8 = 0; k8 < 32; k8 += 8) {
+                    const int r0 = 32 + 16 * mt + g8, cc0 = 32 + k8 + t4;
+                    const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
+                                            to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int bc = 32 + 8 * (ntb + u) + g8;
+                        mma_tf32(tq[u], af, to_tf32(asc[swz(k8 + t4, bc)]), to_tf32(asc[swz(k8 + t4 + 4, bc)]));
                     }
-                    __syncwarp();
-                    float t[2][4];
+                }
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
-#pragma unroll
-                    for (int k8 = 0; k8 < 16; k8 += 8) {
-                        const int r0 = 16 * I + g8, cc0 = 16 * I + k8 + t4;
-                        const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
-                                                to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-                            mma_tf32(t[nt], af, to_tf32(ms[(k8 + t4) * 16 + 8 * nt + g8]),
-                                     to_tf32(ms[(k8 + t4 + 4) * 16 + 8 * nt + g8]));
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int c = 16 * J + 8 * nt + 2 * t4;
-                        tsc[swz(16 * I + g8, c)] = -t[nt][0];
-                        tsc[swz(16 * I + g8, c + 1)] = -t[nt][1];
-                        tsc[swz(16 * I + g8 + 8, c)] = -t[nt][2];
-                        tsc[swz(16 * I + g8 + 8, c + 1)] = -t[nt][3];
-                    }
-                    __syncwarp();
+                for (int u = 0; u < 2; ++u) {
+                    const int r = 32 + 16 * mt + g8, c = 8 * (ntb + u) + 2 * t4;
+                    tsc[swz(r, c)] = -tq[u][0];
+                    tsc[swz(r, c + 1)] = -tq[u][1];
+                    tsc[swz(r + 8, c)] = -tq[u][2];
+                    tsc[swz(r + 8, c + 1)] = -tq[u][3];
                 }
             }
             named_bar(3, SOLVE_THREADS);
