@@ -266,8 +266,10 @@ __device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
 // epilogue warpgroup holds the state slice in TMEM (lane = key channel,
 // 64 value columns) and updates it there, eight columns at a time; sums over
 // the key channels go through warp shuffles and four per-warp partials in
-// shared memory. Rare, so it is written for size rather than speed.
-__device__ __forceinline__ void slow_chunk(const float *__restrict__ alpha, const __nv_bfloat16 *__restrict__ kin,
+// shared memory. Rare, so it is written for size rather than speed, and out
+// of line: the hot loop of the epilogue stays contiguous in the instruction
+// caches.
+__device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, const __nv_bfloat16 *__restrict__ kin,
                                         const __nv_bfloat16 *__restrict__ qin, const __nv_bfloat16 *__restrict__ vin,
                                         const float *__restrict__ beta, __nv_bfloat16 *__restrict__ o, float *red,
                                         uint32_t tm_d, int l, int warp, int lane, int64_t tok0, int L, int H, int h,
@@ -509,6 +511,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 const uint32_t b0 = smem_u32(s.base + SM_B0) + (n % 3) * 16384;
                 if (!s.slow(n % 3)) {
                     const uint32_t d = tmem + TM_AP + 64 * (i & 1);
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(d, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(b0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), I_AP, ks > 0);
