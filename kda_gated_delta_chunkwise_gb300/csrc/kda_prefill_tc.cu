@@ -219,10 +219,10 @@ struct Smem {
     __device__ __forceinline__ uint32_t remote(const void *p) const { return mapa(smem_u32(p), peer); }
 };
 
-// Bounded wait. try_wait suspends the thread for up to about a microsecond
-// while the phase is open, so the loop bound (kMaxWaitTries rounds) gives up
-// after about a second, or after tens of milliseconds should try_wait return
-// at once; both lie far beyond any wait of a working kernel. A timeout sets
+// Bounded wait. try_wait suspends the thread for at most about a microsecond
+// (kSuspendNs) while the phase is open, so the loop bound (kMaxWaitTries
+// rounds) gives up after about a second, or after tens of milliseconds should
+// try_wait return at once; both lie far beyond any wait of a working kernel. A timeout sets
 // the abort flag (bit 1: this CTA timed out; the error is reported once at
 // exit). After a failed wait the callers skip their remaining waits
 // (ok = ok && wait_bar(...)), so a CTA that gives up winds down after at most
@@ -336,8 +336,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                       const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t rank = cluster_rank();  // value half and key half of this CTA (blockIdx.x % 2)
-    Smem s{reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)),
-           rank ^ 1u};
+    // The 1024-byte alignment is an offset into smem_raw (not an integer
+    // round trip of its address), so the compiler keeps every access through
+    // s.base in the shared state space instead of falling back to generic
+    // loads and stores.
+    Smem s{smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u), rank ^ 1u};
     // Both CTAs of a cluster read the same status word and sequence: they
     // leave here together or not at all.
     if (p.dev_status && *p.dev_status != 0) return;

@@ -30,9 +30,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 // A thread whose phase is not complete is suspended (it issues nothing)
-// until the phase completes or about kSuspendNs pass, so waiting warps leave
-// the issue slots to the warps that work.
-constexpr uint32_t kSuspendNs = 100000;
+// until the phase completes or at most about kSuspendNs pass, so waiting warps
+// leave the issue slots to the warps that work. One microsecond keeps a bound
+// on the number of rounds a bound on the time as well.
+constexpr uint32_t kSuspendNs = 1000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
