@@ -38,8 +38,8 @@
 //                    parity also the P rows of [A; P] (TMEM lanes 64-127)
 //   warps 4,5,8,9    solve (sub-partitions 0, 1), chunks of this CTA's parity:
 //                    the A rows (TMEM lanes 0-63), T = (I + A)^{-1}, T tile
-//   warp 12          TMA producer of this CTA's q, k halves (the epilogue and
-//                    the gate refill v and alpha themselves)
+//   warp 12          TMA producer of this CTA's q, k halves (the epilogue
+//                    refills v itself; the gate reads alpha into registers)
 //   warp 13          MMA issuer of the state chain (one thread), TMEM owner
 //   warp 14          MMA issuer of [A; P] on this CTA's parity; warp 15 idle
 // Register budgets per warpgroup (setmaxnreg): epilogue 152, warps 4-11 128,
@@ -86,13 +86,14 @@ constexpr uint32_t TM_AP = 0, TM_XY = 128, TM_UO = 256, TM_D = 384, TM_COLS = 51
 
 // shared memory map (offsets from a 1024-byte aligned base)
 // Buffers by lifetime: A0 ([Kr; Qr]) is read by the first products of its
-// chunk and cycles through 2 slots; Kc, mu, beta and the votes are read
-// until the state update of their chunk and cycle through 3 slots, so the
-// gate can run two chunks ahead of the state chain.
-constexpr uint32_t SM_A0 = 0;          // 2 x 32 KB: [Kr; Qr], two 16 KB key-channel halves (128B swizzle)
-constexpr uint32_t SM_B0 = 65536;      // 3 x 16 KB: Kc (K-major, 64 rows), two 8 KB halves
-constexpr uint32_t SM_AL = 114688;     // 16 KB: alpha of this CTA's key channels (fp32 [64][64])
-constexpr uint32_t SM_SOLVE = 131072;  // 32 KB: A and T (fp32 64x64 each, XOR-swizzled)
+// chunk, Kc, mu, beta and the votes until the state update of their chunk;
+// both cycle through 3 slots (slot n % 3), so the q, k copies, the gate and
+// the inverse of chunk n + 3 may start as soon as the state chain has begun
+// chunk n.
+constexpr int NSLOT = 3;
+constexpr uint32_t SM_A0 = 0;          // 3 x 32 KB: [Kr; Qr], two 16 KB key-channel halves (128B swizzle)
+constexpr uint32_t SM_B0 = 98304;      // 3 x 16 KB: Kc (K-major, 64 rows), two 8 KB halves
+constexpr uint32_t SM_SOLVE = 147456;  // 16 KB: A, overwritten in place by T (fp32 64x64, XOR-swizzled)
 constexpr uint32_t SM_V = 163840;      // 8 KB: v slice (128B swizzle)
 // T and the two P slots are 8 KB K-major tiles (64 rows x 64) laid out
 // back to back, so [T; P0] and [P_{b-1}; P_b] are 128-row operands: the
@@ -118,11 +119,17 @@ constexpr uint32_t PUSH_TAB = 16384 + 8192 + 256 + 16;
 constexpr uint32_t PUSH_TILE = 8192;  // T or P
 constexpr uint16_t BOTH = 3;  // CTA mask of the cluster
 
+// A waiter of a parity wait must never fall two phases behind, nor run a
+// phase ahead, of the barrier it waits on. Every waiter below sees every
+// phase of its barriers: the tables of chunk n complete TAB_FULL[n % 6] (the
+// [A; P] issuer and the solve group, which take every other chunk, then see
+// every phase of the barriers of their parity), [A; P] of a CTA's i-th chunk
+// completes AP_FULL[i % 2], and MMA2 of chunk n completes T_EMPTY[n % 2].
+constexpr int NTAB = 2 * NSLOT;
 enum Bar {
-    B_QK_FULL = 0, B_QK_EMPTY = 2, B_AL_FULL = 4, B_V_FULL = 6,
-    B_TAB_FULL = 8, B_B0_EMPTY = 10, B_O_READ = 13, B_AP_FULL = 15, B_T_FULL = 16, B_T_EMPTY = 17,
-    B_P_FULL = 18, B_P_EMPTY = 20, B_S_FULL = 22, B_XY_FULL = 23, B_R_FULL = 24, B_U_FULL = 25, B_UU_FULL = 26,
-    B_D_FULL = 27, B_DRAIN = 28, B_DRAIN_AUX = 29, B_COUNT = 30
+    B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_TAB_FULL = 7, B_B0_EMPTY = 13, B_O_READ = 16,
+    B_AP_FULL = 18, B_T_FULL = 20, B_T_EMPTY = 21, B_P_FULL = 23, B_P_EMPTY = 25, B_S_FULL = 27, B_XY_FULL = 28,
+    B_R_FULL = 29, B_U_FULL = 30, B_UU_FULL = 31, B_D_FULL = 32, B_DRAIN = 33, B_DRAIN_AUX = 34, B_COUNT = 35
 };
 static_assert(B_COUNT <= 40, "mbarrier area");
 
@@ -173,6 +180,16 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t x) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(x >> 32)), "r"((uint32_t)x));
     return d;
+}
+// Hardware reciprocal (PTX rcp.approx): relative error far below the bf16
+// rounding its results go through.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -333,7 +350,7 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, const _
 // --------------------------------------------------------------------------
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_v) {
+                      const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t rank = cluster_rank();  // value half and key half of this CTA (blockIdx.x % 2)
     // The 1024-byte alignment is an offset into smem_raw (not an integer
@@ -373,25 +390,25 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
     }
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(s.bar(B_QK_FULL + i), 1);
             // MMA1 of both CTAs and MMA0 of the solving CTA (multicast commits),
             // and the solving CTA's solve group once it holds the chunk's
             // barrier phases (so no waiter of TAB_FULL / AP_FULL can fall two
             // phases behind)
             mbar_init(s.bar(B_QK_EMPTY + i), 4);
-            mbar_init(s.bar(B_TAB_FULL + i), 1);  // own gate (expecting the peer's bytes) + the peer's copies
-            mbar_init(s.bar(B_O_READ + i), 64);
+            mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
         }
-        for (int i = 0; i < 3; ++i) mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
-        mbar_init(s.bar(B_AL_FULL), 1);  // alpha: loaded by the gate group for its next chunk
+        // own gate (expecting the peer's bytes) + the peer's copies
+        for (int i = 0; i < NTAB; ++i) mbar_init(s.bar(B_TAB_FULL + i), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(s.bar(B_O_READ + i), 64);
         mbar_init(s.bar(B_V_FULL), 1);   // v: loaded by the epilogue for its next chunk
-        mbar_init(s.bar(B_AP_FULL), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(s.bar(B_AP_FULL + i), 1);
         // T and P of a chunk: the solving CTA arrives locally, the other CTA
         // gets a remote arrive and the copy; released by MMA2 (T) / MMA4 (P)
         // of both CTAs
         mbar_init(s.bar(B_T_FULL), 1);
-        mbar_init(s.bar(B_T_EMPTY), 2);
+        for (int i = 0; i < 2; ++i) mbar_init(s.bar(B_T_EMPTY + i), 2);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s.bar(B_P_FULL + i), 1);
             mbar_init(s.bar(B_P_EMPTY + i), 2);
@@ -426,10 +443,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             prefetch_tmap(&tm_q);
             int nqk = 0;  // chunks whose q, k halves were issued
             for (int n = 0; n < NC; ++n) {
-                const int b = n & 1, kk = n >> 1;
+                const int b = n % NSLOT, kk = n / NSLOT;
                 const int z = (int)(t_begin + (int64_t)n * C);
                 // this CTA's key half of k and q (raw; the gate transforms them in place)
-                if (n >= 2 && !wait_bar(s, p, B_QK_EMPTY + b, (kk - 1) & 1)) break;
+                if (n >= NSLOT && !wait_bar(s, p, B_QK_EMPTY + b, (kk - 1) & 1)) break;
                 unsigned char *a0 = s.base + SM_A0 + b * 32768 + rank * 16384;
                 mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 16384);
                 tma_load_3d(a0, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
@@ -437,7 +454,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 nqk = n + 1;
             }
             // never leave copies in flight: wait (bounded) for the last ones
-            for (int n = nqk - 2 < 0 ? 0 : nqk - 2; n < nqk; ++n) mbar_wait(s.bar(B_QK_FULL + (n & 1)), (n >> 1) & 1);
+            for (int n = nqk - NSLOT < 0 ? 0 : nqk - NSLOT; n < nqk; ++n)
+                mbar_wait(s.bar(B_QK_FULL + n % NSLOT), (n / NSLOT) & 1);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -450,9 +468,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                            ru = smem_u32(s.base + SM_RU);
             bool ok = true;
             for (int n = 0; ok && n < NC; ++n) {
-                const int b = n & 1, kk = n >> 1;
-                if (!(ok = wait_bar(s, p, B_TAB_FULL + b, kk & 1))) break;
-                const int b3 = n % 3;
+                const int b = n & 1, kk = n >> 1, b3 = n % NSLOT;
+                if (!(ok = wait_bar(s, p, B_TAB_FULL + n % NTAB, (n / NTAB) & 1))) break;
                 const bool fast = !s.slow(b3);
                 const uint32_t xy = tmem + TM_XY + 64 * b, uo = tmem + TM_UO + 64 * b;
                 // MMA1: [X; Y] = [Kr; Qr] St, once the outputs of chunk n-2 left XY[b]
@@ -460,14 +477,14 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 if (!(ok = wait_bar(s, p, B_S_FULL, n & 1))) break;
                 tc_fence_after();
                 if (fast) {
-                    const uint32_t a0 = a0_base + b * 32768;
+                    const uint32_t a0 = a0_base + b3 * 32768;
 #pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(xy, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(st + ks * 2048, 16384, 1024), I_KM_MN, ks > 0);
                 }
                 umma_commit(s.bar(B_XY_FULL));
-                umma_commit_mc(s.bar(B_QK_EMPTY + b), BOTH);  // A0[b] read
+                umma_commit_mc(s.bar(B_QK_EMPTY + b3), BOTH);  // A0[b3] read
                 // MMA2: U = T R (rows 0-63 of [T; P0] R)
                 if (!(ok = wait_bar(s, p, B_R_FULL, n & 1))) break;
                 if (!(ok = wait_bar(s, p, B_T_FULL, n & 1))) break;
@@ -479,7 +496,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                                   I_KM_MN, ks > 0);
                 }
                 umma_commit(s.bar(B_U_FULL));
-                umma_commit_mc(s.bar(B_T_EMPTY), BOTH);
+                umma_commit_mc(s.bar(B_T_EMPTY + b), BOTH);
                 // MMA3: D += Kc^T U (state update); MMA4: O2 = P U (rows 64-127 of [P_{b-1}; P_b] U)
                 if (!(ok = wait_bar(s, p, B_UU_FULL, n & 1))) break;
                 if (!(ok = wait_bar(s, p, B_P_FULL + b, kk & 1))) break;
@@ -507,20 +524,21 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // ------------------------------------------------------------ [A; P] issuer (this CTA's parity)
         if (lane == 0) {
             constexpr uint32_t I_AP = idesc_bf16(128, 64, false, false);
-            const uint32_t a0 = smem_u32(s.base + SM_A0) + rank * 32768;
             for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
-                if (!wait_bar(s, p, B_TAB_FULL + (int)rank, i & 1)) break;  // chunk n uses A0 slot n & 1 = rank
+                const int b3 = n % NSLOT;
+                if (!wait_bar(s, p, B_TAB_FULL + n % NTAB, (n / NTAB) & 1)) break;
                 tc_fence_after();
-                const uint32_t b0 = smem_u32(s.base + SM_B0) + (n % 3) * 16384;
-                if (!s.slow(n % 3)) {
+                const uint32_t a0 = smem_u32(s.base + SM_A0) + b3 * 32768;
+                const uint32_t b0 = smem_u32(s.base + SM_B0) + b3 * 16384;
+                if (!s.slow(b3)) {
                     const uint32_t d = tmem + TM_AP + 64 * (i & 1);
 #pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks)
                         umma_bf16(d, sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                   sdesc_sw128(b0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), I_AP, ks > 0);
                 }
-                umma_commit(s.bar(B_AP_FULL));
-                umma_commit_mc(s.bar(B_QK_EMPTY + (int)rank), BOTH);  // A0[rank] read
+                umma_commit(s.bar(B_AP_FULL + (i & 1)));
+                umma_commit_mc(s.bar(B_QK_EMPTY + b3), BOTH);  // A0[b3] read
             }
             umma_commit(s.bar(B_DRAIN_AUX));
             mbar_wait(s.bar(B_DRAIN_AUX), 0);
@@ -626,7 +644,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 const bool act = __all_sync(0xffffffffu, ok && !slow_cur);
                 unsigned char *ru = s.base + SM_RU;
                 if (act) {
-                    const float bt = s.beta(n % 3)[l];
+                    const float bt = s.beta(n % NSLOT)[l];
                     const uint64_t bt2 = f2_make(bt, bt);
                     const unsigned char *vt = s.base + SM_V;
 #pragma unroll 1
@@ -687,11 +705,11 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             float mu_next = 1.f;
             bool slow_next = false;
             if (!last) {  // the next chunk's tables exist long before D_FULL
-                ok = ok && wait_bar(s, p, B_TAB_FULL + ((n + 1) & 1), ((n + 1) >> 1) & 1);
+                ok = ok && wait_bar(s, p, B_TAB_FULL + (n + 1) % NTAB, ((n + 1) / NTAB) & 1);
                 // every thread reads the same slot: it changes only once the
                 // state update of chunk n+1 released it, or never after an abort
-                slow_next = s.slow((n + 1) % 3);
-                if (ok && !slow_next) mu_next = s.mu((n + 1) % 3)[l];
+                slow_next = s.slow((n + 1) % NSLOT);
+                if (ok && !slow_next) mu_next = s.mu((n + 1) % NSLOT)[l];
             }
             ok = ok && wait_bar(s, p, B_D_FULL, n & 1);
             tc_fence_after();
@@ -758,35 +776,38 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // 64-column tile: rg * 1024 + j * 128 + ((c8 ^ j) << 4) + sub.
         const uint32_t c8 = (uint32_t)cq >> 1, sub = ((uint32_t)cq & 1u) * 8u;
         const uint32_t rowbase = (uint32_t)rg * 1024u + sub;
-        // alpha is single-buffered and refilled by this group once a chunk's
-        // pass is done (thread pt == 0 issues the copy)
-        if (pt == 0) {
-            prefetch_tmap(&tm_a);
-            mbar_arrive_expect_tx(s.bar(B_AL_FULL), 16384);
-            tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)t_begin);
-        }
+        // alpha of this thread's channels in rows 8 rg .. 8 rg + 7 goes from
+        // global memory straight into registers: prefetched into L2 one chunk
+        // ahead, loaded before the chunk's waits (rows past the sequence end
+        // are not read)
+        auto alpha_src = [&](int n) {
+            return p.alpha + ((t_begin + (int64_t)n * C + 8 * rg) * H + h) * DK + c0 + 4 * cq;
+        };
         bool alive = true;
         for (int n = 0; n <= NC; ++n) {
           if (n < NC) {
-            const int b = n & 1, kk = n >> 1;
+            const int b = n % NSLOT, kk = n / NSLOT;
             const int64_t tok0 = t_begin + (int64_t)n * C;
             const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
-            // beta of this chunk, loaded before the waits so its latency is hidden
+            // beta and alpha of this chunk, loaded before the waits so their
+            // latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
-            const int b3 = n % 3;
+            float4 arow[8];
+            {
+                const float *src = alpha_src(n);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    arow[j] = 8 * rg + j < L ? __ldg(reinterpret_cast<const float4 *>(src + (int64_t)j * H * DK))
+                                             : make_float4(1.f, 1.f, 1.f, 1.f);
+            }
+            const int b3 = b;  // A0 and B0 slots go together
             alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
             bool ok = alive && wait_bar(s, p, B_QK_FULL + b, kk & 1);
-            ok = ok && wait_bar(s, p, B_AL_FULL, n & 1);
-            // alpha row r of this thread's channels (1 past the sequence end)
-            const float4 *al = reinterpret_cast<const float4 *>(s.base + SM_AL) + cq;
-            auto alpha_row = [&](int r) {
-                return r < L ? al[r * (KH / 4)] : make_float4(1.f, 1.f, 1.f, 1.f);
-            };
             // products of this thread's 8 rows, then the 8 group products
             float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float4 a = alpha_row(8 * rg + j);
+                const float4 a = arow[j];
                 g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
             }
             scan[rg * 16 + cq] = g;
@@ -814,45 +835,35 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             }
             // Kc, mu, beta and the votes go to slot n % 3 once the state update
             // of chunk n-3 released it in both CTAs
-            if (n >= 3) ok = ok && wait_bar(s, p, B_B0_EMPTY + b3, ((n / 3) - 1) & 1);
+            if (n >= NSLOT) ok = ok && wait_bar(s, p, B_B0_EMPTY + b3, (kk - 1) & 1);
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
             unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
             if (ok && !slow) {
-                // Rows past the sequence end read as k = q = 0, alpha = 1.
+                // One pass over the rows with the running product p_r:
+                // Kr = k p / mu and Qr = q p / mu in place, Kc = k mu / p (the
+                // gates after row r over mu). Rows past the sequence end read
+                // as k = q = 0, alpha = 1.
                 const uint64_t inv01 = f2_make(inv[0], inv[1]), inv23 = f2_make(inv[2], inv[3]);
-                // Backward over the rows with the suffix product s_r (gates after
-                // row r): Kc = k s / mu  (= k mu / p). It reads the raw k, so it
-                // runs before the forward pass overwrites k in place.
-                uint64_t sf01 = f2_make(after.x, after.y), sf23 = f2_make(after.z, after.w);
-#pragma unroll 1
-                for (int j = 7; j >= 0; --j) {
-                    const int r = 8 * rg + j;
-                    const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
-                    const uint2 kw = r < L ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
-                    const float4 a = alpha_row(r);
-                    const uint64_t e01 = f2_mul(sf01, inv01), e23 = f2_mul(sf23, inv23);
-                    *reinterpret_cast<uint2 *>(kch + off) =
-                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(kw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(kw.y), e23)));
-                    sf01 = f2_mul(sf01, f2_make(a.x, a.y));
-                    sf23 = f2_mul(sf23, f2_make(a.z, a.w));
-                }
-                // Forward with the running product p_r: Kr = k p / mu, Qr = q p / mu, in place.
+                const uint64_t mu01 = f2_make(mu[0], mu[1]), mu23 = f2_make(mu[2], mu[3]);
                 uint64_t pr01 = f2_make(before.x, before.y), pr23 = f2_make(before.z, before.w);
-#pragma unroll 1
+#pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int r = 8 * rg + j;
                     const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
-                    const bool in = r < L;
+                    const bool in = 8 * rg + j < L;
                     const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
                     const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
-                    const float4 a = alpha_row(r);
-                    pr01 = f2_mul(pr01, f2_make(a.x, a.y));
-                    pr23 = f2_mul(pr23, f2_make(a.z, a.w));
+                    pr01 = f2_mul(pr01, f2_make(arow[j].x, arow[j].y));
+                    pr23 = f2_mul(pr23, f2_make(arow[j].z, arow[j].w));
                     const uint64_t e01 = f2_mul(pr01, inv01), e23 = f2_mul(pr23, inv23);
+                    const uint64_t c01 = f2_mul(f2_make(rcp_approx(f2_lo(pr01)), rcp_approx(f2_hi(pr01))), mu01);
+                    const uint64_t c23 = f2_mul(f2_make(rcp_approx(f2_lo(pr23)), rcp_approx(f2_hi(pr23))), mu23);
+                    const uint64_t k01 = bf2_to_f2(kw.x), k23 = bf2_to_f2(kw.y);
                     *reinterpret_cast<uint2 *>(ah + off) =
-                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(kw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(kw.y), e23)));
+                        make_uint2(f2_to_bf2(f2_mul(k01, e01)), f2_to_bf2(f2_mul(k23, e23)));
                     *reinterpret_cast<uint2 *>(ah + 8192 + off) =
                         make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(qw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(qw.y), e23)));
+                    *reinterpret_cast<uint2 *>(kch + off) =
+                        make_uint2(f2_to_bf2(f2_mul(k01, c01)), f2_to_bf2(f2_mul(k23, c23)));
                 }
             }
             // (after an abort nothing more is written: slots that others may
@@ -864,21 +875,23 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (ok && pt == 0) vslot[0] = slow ? 1 : 0;
             fence_proxy_async();
             named_bar(1, GATE_THREADS);
-            if (pt == 0 && n + 1 < NC) {  // alpha of this chunk is no longer read
-                mbar_arrive_expect_tx(s.bar(B_AL_FULL), 16384);
-                tma_load_3d(s.base + SM_AL, &tm_a, s.bar(B_AL_FULL), c0, h, (int)(tok0 + C));
+            if (n + 1 < NC) {  // the next chunk's alpha rows into L2
+                const int Ln = (int)((T - (int64_t)(n + 1) * C) < C ? (T - (int64_t)(n + 1) * C) : C);
+                const float *src = alpha_src(n + 1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (8 * rg + j < Ln) prefetch_l2(src + (int64_t)j * H * DK);
             }
             if (ok && pt == 0) {
-                // this key half into the peer (its A0 slot was released with
-                // QK_EMPTY of chunk n-2, its slot n % 3 with B0_EMPTY of chunk
-                // n-3, in both CTAs)
-                const uint32_t rbar = s.remote(s.bar(B_TAB_FULL + b));
+                // this key half into the peer (its slot n % 3 was released with
+                // QK_EMPTY and B0_EMPTY of chunk n-3, in both CTAs)
+                const uint32_t rbar = s.remote(s.bar(B_TAB_FULL + n % NTAB));
                 bulk_s2c(s.remote(ah), ah, 16384, rbar);
                 bulk_s2c(s.remote(kch), kch, 8192, rbar);
                 bulk_s2c(s.remote(mu_b), mu_b, 256, rbar);
                 bulk_s2c(s.remote(vslot), vslot, 16, rbar);
                 // own tables are written; the peer's arrive as copies
-                mbar_arrive_expect_tx(s.bar(B_TAB_FULL + b), PUSH_TAB);
+                mbar_arrive_expect_tx(s.bar(B_TAB_FULL + n % NTAB), PUSH_TAB);
             }
             alive = ok;
           }
@@ -889,10 +902,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (m < 0 || (m & 1) != (int)rank) continue;
             const int bm = m & 1, im = m >> 1;
             const int Lm = (int)((T - (int64_t)m * C) < C ? (T - (int64_t)m * C) : C);
-            bool okp = alive && wait_bar(s, p, B_AP_FULL, im & 1);
+            bool okp = alive && wait_bar(s, p, B_AP_FULL + (im & 1), (im >> 1) & 1);
             tc_fence_after();
             const bool gop = !named_bar_or(1, GATE_THREADS, s.flags()[1] != 0);
-            const bool workp = gop && !s.slow(m % 3);
+            const bool workp = gop && !s.slow(m % NSLOT);
             // P row r (masked: j <= r, rows past the sequence end zero), columns
             // 32 hq .. 32 hq + 31, into slot bm of the P tiles once MMA4 of chunk
             // m-2 released it in both CTAs, then to the peer
@@ -934,54 +947,52 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         }
     } else {
         // ------------------------------------------------------------ solve group (warps 4, 5, 8, 9)
-        // Chunks n = rank, rank + 2, ...: their [Kr; Qr] sit in A0 slot rank.
+        // Chunks n = rank, rank + 2, ...
         // (SM sub-partitions 0 and 1; TMEM lanes 0-63, the A rows of [A; P])
         const int gw = ((warp >> 3) << 1) | (warp & 1);  // 4, 5, 8, 9 -> 0..3
         const int qt = 32 * gw + lane;
         const int q4 = warp & 3;           // TMEM lane quarter (0 or 1)
         const int R = 32 * q4 + lane;      // row of A
         const int hq = gw >> 1;            // column half of the A read-out
-        float *asc = reinterpret_cast<float *>(s.base + SM_SOLVE);  // A (beta-scaled; upper part unused)
-        float *tsc = asc + 64 * 64;                                  // T
+        // One fp32 64x64 scratch holds A and is overwritten by T block by block
+        // (16x16 blocks (I, J)): the read-out writes A's strictly lower blocks
+        // and zeros above the block diagonal; each step below writes a block
+        // of T only once the A block in its place has been read.
+        float *tsc = reinterpret_cast<float *>(s.base + SM_SOLVE);
         const int g8 = lane >> 2, t4 = lane & 3;
-        const int b = (int)rank;
-        // T's blocks above the diagonal are never written by the solve: zero
-        // them once, so the tile write needs no mask (the diagonal blocks are
-        // written whole, zeros above their diagonal included)
-        for (int e = qt; e < 6 * 256; e += SOLVE_THREADS) {
-            const int blk = e >> 8, I = blk < 3 ? 0 : (blk < 5 ? 1 : 2), J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            tsc[swz(16 * I + ((e >> 4) & 15), 16 * J + (e & 15))] = 0.f;
-        }
-        named_bar(3, SOLVE_THREADS);
         bool alive = true;
         for (int n = (int)rank, i = 0; n < NC; n += 2, ++i) {
-            const int b3 = n % 3;
+            const int b3 = n % NSLOT;
             alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
-            bool ok = alive && wait_bar(s, p, B_TAB_FULL + b, i & 1);  // beta and the votes of this chunk
-            ok = ok && wait_bar(s, p, B_AP_FULL, i & 1);
+            bool ok = alive && wait_bar(s, p, B_TAB_FULL + n % NTAB, (n / NTAB) & 1);  // beta and the votes
+            ok = ok && wait_bar(s, p, B_AP_FULL + (i & 1), (i >> 1) & 1);
             tc_fence_after();
             // group-uniform decisions: step 2 and the TMEM loads are warp-collective
             const bool go = !named_bar_or(3, SOLVE_THREADS, s.flags()[1] != 0);
             // every thread of the group is past this chunk's TAB_FULL and
-            // AP_FULL phases: A0 slot b may be refilled in both CTAs
+            // AP_FULL phases: A0 slot b3 may be refilled in both CTAs
             if (qt == 0) {
-                mbar_arrive(s.bar(B_QK_EMPTY + b));
-                mbar_arrive_remote_tx(s.remote(s.bar(B_QK_EMPTY + b)), 0);
+                mbar_arrive(s.bar(B_QK_EMPTY + b3));
+                mbar_arrive_remote_tx(s.remote(s.bar(B_QK_EMPTY + b3)), 0);
             }
             const bool work = go && !s.slow(b3);
             if (work) {
-                // A row R, columns 32 hq .. 32 hq + 31 (beta-scaled; only the
-                // strictly lower part is read later)
+                // A row R, columns 32 hq .. 32 hq + 31, beta-scaled, zero from
+                // the block after the diagonal block on (the diagonal block's
+                // upper part is never read)
                 uint32_t r32[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + TM_AP + 64 * (i & 1) + 32 * hq, r32);
                 tmem_wait_ld();
                 tc_fence_before();
                 const float bt = s.beta(b3)[R];
+                const int cend = 16 * (R >> 4) + 16 - 32 * hq;  // first zero column of this half
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)
-                    *reinterpret_cast<float4 *>(asc + swz(R, 32 * hq + 4 * j4)) =
-                        make_float4(bt * __uint_as_float(r32[4 * j4]), bt * __uint_as_float(r32[4 * j4 + 1]),
-                                    bt * __uint_as_float(r32[4 * j4 + 2]), bt * __uint_as_float(r32[4 * j4 + 3]));
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float f = 4 * j4 < cend ? bt : 0.f;
+                    *reinterpret_cast<float4 *>(tsc + swz(R, 32 * hq + 4 * j4)) =
+                        make_float4(f * __uint_as_float(r32[4 * j4]), f * __uint_as_float(r32[4 * j4 + 1]),
+                                    f * __uint_as_float(r32[4 * j4 + 2]), f * __uint_as_float(r32[4 * j4 + 3]));
+                }
             }
             named_bar(3, SOLVE_THREADS);
             if (work && gw < 2) {
@@ -990,7 +1001,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // loads take immediate offsets from two base pointers (the
                 // swizzle flips bit 4 of the column for rows with r & 7 >= 4).
                 const int blk = 2 * gw + (lane >> 4), col = lane & 15;
-                const float *rowp = asc + (16 * blk) * 64;
+                const float *rowp = tsc + (16 * blk) * 64;
                 const float *b0p = rowp + 16 * blk, *b1p = rowp + ((16 * blk) ^ 16);
                 float x[16];
 #pragma unroll
@@ -1005,6 +1016,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                         x[rl] -= av * xs;
                     }
                 }
+                __syncwarp();  // the block's A entries are read (its 16 columns are this warp's lanes)
 #pragma unroll
                 for (int rl = 0; rl < 16; ++rl) tsc[swz(16 * blk + rl, 16 * blk + col)] = x[rl];
             }
@@ -1012,8 +1024,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // T step 2, two levels of 32-row blocks (tf32 mma.sync, all four warps):
             //   T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (one 8-column half each)
             //   T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32])
-            // (T's blocks above the diagonal are zero; the product A21 T1 is
-            // staged in A's unused upper-right quadrant).
+            // (the scratch's blocks above the block diagonal are zero; the
+            // product A21 T1 is staged in its upper-right quadrant, which the
+            // T tile below writes as zeros).
             if (work) {
                 // level A: warps gw 0, 1 -> T_10, gw 2, 3 -> T_32; 8-column half nt
                 const int I = gw < 2 ? 1 : 3, J = I - 1, nt = gw & 1;
@@ -1022,8 +1035,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll 1
                 for (int k8 = 0; k8 < 16; k8 += 8) {
                     const int r0 = 16 * I + g8, cc0 = 16 * J + k8 + t4;
-                    const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
-                                            to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
+                    const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
+                                            to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
                     const int br = 16 * J + k8 + t4, bc = 16 * J + 8 * nt + g8;
                     mma_tf32(mq, af, to_tf32(tsc[swz(br, bc)]), to_tf32(tsc[swz(br + 4, bc)]));
                 }
@@ -1031,7 +1044,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 ms[g8 * 8 + 2 * t4 + 1] = mq[1];
                 ms[(g8 + 8) * 8 + 2 * t4] = mq[2];
                 ms[(g8 + 8) * 8 + 2 * t4 + 1] = mq[3];
-                __syncwarp();
+                named_bar(3, SOLVE_THREADS);  // A_10 and A_32 are read: T_10, T_32 go in their place
                 float tq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int k8 = 0; k8 < 16; k8 += 8) {
@@ -1050,13 +1063,13 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // levels B and C: warp gw owns rows 32 + 16 (gw >> 1) .. +15 and the
             // 8-column tiles 2 (gw & 1), 2 (gw & 1) + 1 of a 32 x 32 result
             const int mt = gw >> 1, ntb = 2 * (gw & 1);
-            if (work) {  // level B: M2 = A[32:64, 0:32] T[0:32, 0:32] -> asc[0:32, 32:64]
+            if (work) {  // level B: M2 = A[32:64, 0:32] T[0:32, 0:32] -> scratch [0:32, 32:64]
                 float mq[2][4] = {};
 #pragma unroll 1
                 for (int k8 = 0; k8 < 32; k8 += 8) {
                     const int r0 = 32 + 16 * mt + g8, cc0 = k8 + t4;
-                    const uint32_t af[4] = {to_tf32(asc[swz(r0, cc0)]), to_tf32(asc[swz(r0 + 8, cc0)]),
-                                            to_tf32(asc[swz(r0, cc0 + 4)]), to_tf32(asc[swz(r0 + 8, cc0 + 4)])};
+                    const uint32_t af[4] = {to_tf32(tsc[swz(r0, cc0)]), to_tf32(tsc[swz(r0 + 8, cc0)]),
+                                            to_tf32(tsc[swz(r0, cc0 + 4)]), to_tf32(tsc[swz(r0 + 8, cc0 + 4)])};
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int bc = 8 * (ntb + u) + g8;
@@ -1066,10 +1079,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int r = 16 * mt + g8, c = 32 + 8 * (ntb + u) + 2 * t4;
-                    asc[swz(r, c)] = mq[u][0];
-                    asc[swz(r, c + 1)] = mq[u][1];
-                    asc[swz(r + 8, c)] = mq[u][2];
-                    asc[swz(r + 8, c + 1)] = mq[u][3];
+                    tsc[swz(r, c)] = mq[u][0];
+                    tsc[swz(r, c + 1)] = mq[u][1];
+                    tsc[swz(r + 8, c)] = mq[u][2];
+                    tsc[swz(r + 8, c + 1)] = mq[u][3];
                 }
             }
             named_bar(3, SOLVE_THREADS);
@@ -1083,7 +1096,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int bc = 32 + 8 * (ntb + u) + g8;
-                        mma_tf32(tq[u], af, to_tf32(asc[swz(k8 + t4, bc)]), to_tf32(asc[swz(k8 + t4 + 4, bc)]));
+                        mma_tf32(tq[u], af, to_tf32(tsc[swz(k8 + t4, bc)]), to_tf32(tsc[swz(k8 + t4 + 4, bc)]));
                     }
                 }
 #pragma unroll
@@ -1098,19 +1111,23 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             named_bar(3, SOLVE_THREADS);
             // T -> the bf16 operand tile of both CTAs, once MMA2 of the previous
             // chunk completed in both
-            if (n >= 1) ok = ok && wait_bar(s, p, B_T_EMPTY, (n - 1) & 1);
+            if (n >= 1) ok = ok && wait_bar(s, p, B_T_EMPTY + ((n - 1) & 1), ((n - 1) >> 1) & 1);
             const bool wr = __all_sync(0xffffffffu, ok && work);
             if (wr) {
                 unsigned char *tpt = s.base + SM_TP;
                 const int r = qt >> 1, hc = qt & 1;  // T row r, columns 32hc .. 32hc+31 (exact: unit
                                                      // diagonal, zeros above)
+                const bool zero = r < 32 && hc == 1;  // T[0:32, 32:64] = 0 (the scratch holds M2 there)
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    const float4 x0 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4)));
-                    const float4 x1 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4) + 4));
-                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, 4 * hc + c4, 64)) =
-                        make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
-                                   pack_bf16(x1.z, x1.w));
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (!zero) {
+                        const float4 x0 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4)));
+                        const float4 x1 = *reinterpret_cast<const float4 *>(tsc + swz(r, 8 * (4 * hc + c4) + 4));
+                        w = make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
+                                       pack_bf16(x1.z, x1.w));
+                    }
+                    *reinterpret_cast<uint4 *>(tpt + kmajor_chunk(r, 4 * hc + c4, 64)) = w;
                 }
                 fence_proxy_async();
             }
@@ -1187,12 +1204,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     const int64_t tokens = a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T;
     const int64_t blocks = (int64_t)a.N * a.H * NSLICE;
     if (blocks == 0) return cudaSuccess;
-    CUtensorMap mk, mq, ma, mv;
+    CUtensorMap mk, mq, mv;
     // A map needs a non-empty extent; an empty token range never issues a copy.
     const int64_t ext = tokens > 0 ? tokens : 1;
     if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.alpha, DK, a.H, ext, KH, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, DV, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     TcParams p;
@@ -1215,7 +1231,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // blocks is even: one cluster of NSLICE CTAs per (sequence, head)
-    kda_prefill_tc_kernel<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(p, mk, mq, ma, mv);
+    kda_prefill_tc_kernel<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(p, mk, mq, mv);
     return cudaGetLastError();
 }
 
