@@ -60,9 +60,23 @@ typedef enum {
     KDA_ALGO_TC = 2     /* tcgen05/TMEM chunk kernel: bf16, d_k = d_v = 128 only */
 } kda_algo_t;
 
-/* Device-side status codes written to `device_status` by kda_varlen_prefill. */
+/*
+ * Gate kinds (the entry points ending in _gate / _slots take one). The K3
+ * essay's §四 places KDA's per-channel gate next to the scalar gate of Gated
+ * DeltaNet; with no gate the update is the plain delta rule of §三.
+ *   KDA_GATE_CHANNEL  alpha [.., H, d_k]: one gate per key channel (KDA)
+ *   KDA_GATE_SCALAR   alpha [.., H]: one gate per token and head, the same for
+ *                     every channel (Gated DeltaNet); 4-byte aligned suffices
+ *   KDA_GATE_NONE     alpha is not read and may be NULL: alpha = 1 (DeltaNet)
+ * Each kind computes exactly what KDA_GATE_CHANNEL computes with alpha
+ * broadcast over the channels (all ones for NONE).
+ */
+typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_SCALAR = 1, KDA_GATE_NONE = 2 } kda_gate_t;
+
+/* Device-side status codes written to `device_status`. */
 #define KDA_DEV_OK 0
 #define KDA_DEV_BAD_CU_SEQLENS 1   /* cu[0] != 0, decreasing, or cu[N] != T_total */
+#define KDA_DEV_BAD_SLOT 2         /* a state slot outside [0, pool_size)          */
 
 /*
  * kda_prefill - chunkwise prefill of B equal-length sequences (K3 essay §四
@@ -157,6 +171,62 @@ kda_status_t kda_varlen_prefill_noalloc(const void *q, const void *k, const void
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
                              const float *alpha, const float *beta, float *state, void *o,
                              int N, int H, int d_k, int d_v, kda_stream_t stream);
+
+/*
+ * kda_prefill_gate - kda_prefill_ex with a gate kind (see kda_gate_t): alpha is
+ * [B, T, H, d_k] (CHANNEL), [B, T, H] (SCALAR) or unused (NONE). Everything
+ * else as kda_prefill_ex.
+ */
+kda_status_t kda_prefill_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                              const float *alpha, kda_gate_t gate, const float *beta,
+                              const float *initial_state, void *o, float *final_state, int B, int T,
+                              int H, int d_k, int d_v, kda_algo_t algo, kda_stream_t stream);
+
+/*
+ * State slots for serving: a pool of recurrent states that outlives the calls
+ * (prefill, then any number of decode steps, or a long prompt prefilled in
+ * pieces), each request owning one slot. Both calls below read a sequence's
+ * state from its slot and write the new state back into the same slot.
+ *
+ *   state_pool  [pool_size, H, d_k, d_v] float32, DEVICE, read and written
+ *   slots       [N] int32, DEVICE: sequence n uses slot s = slots[n]; a value
+ *               -1 - s means "slot s, starting from the zero state" (a new
+ *               request). Two sequences of one call must not share a slot.
+ *   device_status  DEVICE int32 or NULL: set to KDA_DEV_OK, or to
+ *               KDA_DEV_BAD_SLOT when a slot lies outside [0, pool_size) (and
+ *               KDA_DEV_BAD_CU_SEQLENS as for kda_varlen_prefill).
+ *
+ * Prefilling a prompt in pieces, each piece continuing from the slot's state,
+ * gives the result of one prefill of the whole prompt (to rounding), because
+ * the state carries everything the recurrence knows (§六.1).
+ */
+
+/*
+ * kda_varlen_prefill_slots - kda_varlen_prefill whose initial and final states
+ * live in `state_pool` at `slots`, with a gate kind. On KDA_DEV_BAD_CU_SEQLENS
+ * or KDA_DEV_BAD_SLOT nothing is written (no o, no state). The workspace is
+ * the one of kda_varlen_prefill (kda_varlen_workspace_bytes).
+ */
+kda_status_t kda_varlen_prefill_slots(const void *q, const void *k, const void *v,
+                                      kda_dtype_t qkv_dtype, const float *alpha, kda_gate_t gate,
+                                      const float *beta, float *state_pool, const int32_t *slots,
+                                      int pool_size, void *o, const int32_t *cu_seqlens, int N,
+                                      int T_total, int H, int d_k, int d_v, void *workspace,
+                                      size_t workspace_bytes, int32_t *device_status,
+                                      kda_stream_t stream);
+
+/*
+ * kda_decode_step_slots - kda_decode_step on the states state_pool[slots[n]]
+ * (updated in place), with a gate kind: alpha [N, H, d_k] (CHANNEL), [N, H]
+ * (SCALAR) or unused (NONE). A sequence whose slot is out of range is skipped
+ * (its o is not written) and sets KDA_DEV_BAD_SLOT in `device_status`; the
+ * others run.
+ */
+kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                   const float *alpha, kda_gate_t gate, const float *beta,
+                                   float *state_pool, const int32_t *slots, int pool_size, void *o,
+                                   int N, int H, int d_k, int d_v, int32_t *device_status,
+                                   kda_stream_t stream);
 
 /*
  * kda_device_errors - diagnostic: reads the library's device-side error word

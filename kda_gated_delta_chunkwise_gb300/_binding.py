@@ -22,10 +22,13 @@ from . import build as _build
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_CHECK, KDA_ERR_WORKSPACE = range(6)
 KDA_F32, KDA_BF16 = 0, 1
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
-KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS = 0, 1
+# gate kinds: per-channel (KDA), one per token-head (Gated DeltaNet), none (delta rule)
+GATES = {"channel": 0, "scalar": 1, "none": 2}
+KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT = 0, 1, 2
 
-EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_varlen_prefill", "kda_varlen_workspace_bytes",
-           "kda_decode_step", "kda_device_errors", "kda_last_error", "kda_abi_version")
+EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_varlen_prefill", "kda_varlen_prefill_slots",
+           "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_decode_step", "kda_decode_step_slots",
+           "kda_device_errors", "kda_last_error", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +66,13 @@ def load(path: str | None = None):
         lib.kda_varlen_workspace_bytes.argtypes = [i, i, i, i]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.kda_prefill_gate.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.kda_prefill_gate.restype = i
+        lib.kda_varlen_prefill_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, vp, i, i, i, i, i,
+                                                 vp, ctypes.c_size_t, vp, vp]
+        lib.kda_varlen_prefill_slots.restype = i
+        lib.kda_decode_step_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, i, i, i, i, vp, vp]
+        lib.kda_decode_step_slots.restype = i
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
         lib.kda_abi_version.restype = ctypes.c_int
@@ -139,29 +149,43 @@ def _host_call(fn, tensors: dict, **kw):
     return res
 
 
+def _check_gate(gate: str, alpha, lead: tuple, dk: int, dev):
+    """alpha for a gate kind: [*lead, d_k] (channel), [*lead] (scalar), unused (none)."""
+    if gate not in GATES:
+        raise ValueError(f"gate must be one of {sorted(GATES)}")
+    if gate == "none":
+        return None
+    _need(alpha, "alpha", torch.float32, dev)
+    want = tuple(lead) + ((dk,) if gate == "channel" else ())
+    if tuple(alpha.shape) != want:
+        raise ValueError(f"alpha must be {want} for gate={gate!r}, got {tuple(alpha.shape)}")
+    return alpha
+
+
 def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: bool = True,
-            algo: str = "auto", out=None, final_state=None, stream=None):
+            algo: str = "auto", gate: str = "channel", out=None, final_state=None, stream=None):
     """Chunkwise KDA prefill of B equal-length sequences.
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, same dtype);
-    alpha: [B, T, H, d_k] fp32; beta: [B, T, H] fp32;
+    alpha: [B, T, H, d_k] fp32 (gate="channel"), [B, T, H] (gate="scalar",
+    Gated DeltaNet) or None (gate="none", the delta rule); beta: [B, T, H] fp32;
     initial_state: [B, H, d_k, d_v] fp32 or None (zeros).
     Returns (o [B, T, H, d_v] in v's dtype, final_state [B, H, d_k, d_v] fp32 or None).
     """
     if q.device.type == "cpu":
         return _host_call(prefill, dict(q=q, k=k, v=v, alpha=alpha, beta=beta,
                                         initial_state=initial_state),
-                          output_final_state=output_final_state, algo=algo)
+                          output_final_state=output_final_state, algo=algo, gate=gate)
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, q.dtype, dev)
-    _need(alpha, "alpha", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape != (B, T, H, dv) or alpha.shape != q.shape or beta.shape != (B, T, H):
-        raise ValueError("shape mismatch among q, k, v, alpha, beta")
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch among q, k, v, beta")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, dev)
     if initial_state is not None:
         _need(initial_state, "initial_state", torch.float32, dev)
         if initial_state.shape != (B, H, dk, dv):
@@ -172,9 +196,9 @@ def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: boo
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
     if algo not in ALGOS:
         raise ValueError(f"algo must be one of {sorted(ALGOS)}")
-    st = lib.kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
-                            _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
-                            ALGOS[algo], _stream(stream))
+    st = lib.kda_prefill_gate(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate], _ptr(beta),
+                              _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
+                              ALGOS[algo], _stream(stream))
     _check(lib, st)
     return out, final_state
 
@@ -256,5 +280,76 @@ def decode_step(q, k, v, alpha, beta, state, *, out=None, stream=None):
         out = torch.empty_like(v)
     st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
                              _ptr(state), _ptr(out), N, H, dk, dv, _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def varlen_prefill_slots(q, k, v, alpha, beta, cu_seqlens, state_pool, slots, *, gate: str = "channel",
+                         out=None, workspace=None, device_status=None, stream=None):
+    """Packed prefill whose states live in a pool: sequence n starts from
+    ``state_pool[slots[n]]`` (zeros when ``slots[n] = -1 - s``, a fresh request
+    in slot s) and its final state is written back into that slot.
+
+    q, k: [T_total, H, d_k]; v: [T_total, H, d_v]; alpha as for ``prefill``
+    with lead [T_total, H]; beta: [T_total, H]; cu_seqlens, slots: int32 [N + 1],
+    [N] on the device; state_pool: [P, H, d_k, d_v] fp32, updated in place.
+    Returns o. ``device_status`` (int32 [1]) receives KDA_DEV_OK or a KDA_DEV_* code.
+    """
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(slots, "slots", torch.int32, dev)
+    _need(state_pool, "state_pool", torch.float32, dev)
+    Tt, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if k.shape != q.shape or v.shape != (Tt, H, dv) or beta.shape != (Tt, H) or slots.shape != (N,) \
+            or state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError("shape mismatch among q, k, v, beta, slots, state_pool")
+    alpha = _check_gate(gate, alpha, (Tt, H), dk, dev)
+    if out is None:
+        out = torch.empty_like(v)
+    nbytes = int(lib.kda_varlen_workspace_bytes(N, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib.kda_varlen_prefill_slots(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate],
+                                      _ptr(beta), _ptr(state_pool), _ptr(slots), state_pool.shape[0], _ptr(out),
+                                      _ptr(cu_seqlens), N, Tt, H, dk, dv, _ptr(workspace), workspace.numel(),
+                                      _ptr(device_status), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def decode_step_slots(q, k, v, alpha, beta, state_pool, slots, *, gate: str = "channel", out=None,
+                      device_status=None, stream=None):
+    """One recurrent step per (sequence, head) on ``state_pool[slots[n]]``
+    (updated in place; ``-1 - s`` starts slot s from zeros).
+
+    q, k: [N, H, d_k]; v: [N, H, d_v]; alpha as for ``prefill`` with lead
+    [N, H]; beta: [N, H]; slots: int32 [N]; state_pool: [P, H, d_k, d_v] fp32.
+    Returns o [N, H, d_v]. A sequence with a slot outside [0, P) is skipped and
+    sets KDA_DEV_BAD_SLOT in ``device_status``.
+    """
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(slots, "slots", torch.int32, dev)
+    _need(state_pool, "state_pool", torch.float32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (N, H, dv) or beta.shape != (N, H) or slots.shape != (N,) \
+            or state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError("shape mismatch among q, k, v, beta, slots, state_pool")
+    alpha = _check_gate(gate, alpha, (N, H), dk, dev)
+    if out is None:
+        out = torch.empty_like(v)
+    st = lib.kda_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate],
+                                   _ptr(beta), _ptr(state_pool), _ptr(slots), state_pool.shape[0], _ptr(out),
+                                   N, H, dk, dv, _ptr(device_status), _stream(stream))
     _check(lib, st)
     return out

@@ -57,14 +57,25 @@ kda_status_t check_dtype(kda_dtype_t dt) {
             return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);             \
     } while (0)
 
+kda_status_t check_gate(int gate) {
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_SCALAR && gate != KDA_GATE_NONE)
+        return fail(KDA_ERR_INVALID_ARG, "unknown gate kind %d", gate);
+    return KDA_OK;
+}
+
 kda_status_t check_tensors(const void *q, const void *k, const void *v, const float *alpha,
                            const float *beta, const void *o, const float *s0, const float *sT,
-                           bool any_tokens) {
+                           bool any_tokens, int gate = KDA_GATE_CHANNEL) {
     if (any_tokens) {
         KDA_REQUIRE_PTR(q);
         KDA_REQUIRE_PTR(k);
         KDA_REQUIRE_PTR(v);
-        KDA_REQUIRE_PTR(alpha);
+        if (gate == KDA_GATE_CHANNEL) KDA_REQUIRE_PTR(alpha);
+        if (gate == KDA_GATE_SCALAR) {
+            if (!alpha) return fail(KDA_ERR_INVALID_ARG, "alpha must not be NULL");
+            if (reinterpret_cast<uintptr_t>(alpha) & 3u)
+                return fail(KDA_ERR_INVALID_ARG, "alpha must be 4-byte aligned");
+        }
         if (!beta) return fail(KDA_ERR_INVALID_ARG, "beta must not be NULL");
         if (reinterpret_cast<uintptr_t>(beta) & 3u) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
         KDA_REQUIRE_PTR(o);
@@ -109,17 +120,18 @@ kda_status_t kda_device_errors(int *errors, int reset) {
     return cuda_status(kda::read_device_error(errors, reset != 0), "reading the device error word");
 }
 
-kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                            const float *alpha, const float *beta, const float *initial_state,
-                            void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
-                            kda_algo_t algo, kda_stream_t stream) {
+kda_status_t kda_prefill_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                              const float *alpha, kda_gate_t gate, const float *beta,
+                              const float *initial_state, void *o, float *final_state, int B, int T,
+                              int H, int d_k, int d_v, kda_algo_t algo, kda_stream_t stream) {
     kda_status_t st;
     if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_gate(gate)) != KDA_OK) return st;
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
     if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
     if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
     if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state,
-                            (int64_t)B * T > 0)) != KDA_OK)
+                            (int64_t)B * T > 0, gate)) != KDA_OK)
         return st;
     kda::PrefillArgs a{};
     a.dt = qkv_dtype; a.dk = d_k; a.dv = d_v;
@@ -129,9 +141,18 @@ kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dty
     if (T == 0 && !final_state) return ok();
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = initial_state;
     a.o = o; a.sT = final_state; a.cu_seqlens = nullptr;
+    a.gate = gate; a.slots = nullptr;
     a.N = B; a.T = T; a.H = H; a.dk = d_k; a.dv = d_v; a.dt = qkv_dtype;
     a.order = nullptr; a.counter = nullptr; a.dev_status = nullptr;
     return run_prefill(a, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                            const float *alpha, const float *beta, const float *initial_state,
+                            void *o, float *final_state, int B, int T, int H, int d_k, int d_v,
+                            kda_algo_t algo, kda_stream_t stream) {
+    return kda_prefill_gate(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, initial_state, o, final_state, B,
+                            T, H, d_k, d_v, algo, stream);
 }
 
 kda_status_t kda_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
@@ -148,21 +169,26 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v) {
     return align_up(n * sizeof(int32_t)) + kAlign;  // order[N] | counter, status
 }
 
-kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                                const float *alpha, const float *beta,
-                                const float *initial_state, void *o, float *final_state,
-                                const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
-                                int d_v, void *workspace, size_t workspace_bytes,
-                                int32_t *device_status, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+kda_status_t varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                            const float *alpha, int gate, const float *beta, const float *initial_state,
+                            void *o, float *final_state, const int32_t *slots, int pool_size,
+                            const int32_t *cu_seqlens, int N, int T_total, int H, int d_k, int d_v,
+                            void *workspace, size_t workspace_bytes, int32_t *device_status,
+                            cudaStream_t s) {
     kda_status_t st;
     if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_gate(gate)) != KDA_OK) return st;
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
     if (N < 0 || T_total < 0) return fail(KDA_ERR_INVALID_ARG, "N and T_total must be >= 0");
     if (N == 0) return ok();
     if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
         return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
-    if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state, T_total > 0)) != KDA_OK)
+    if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state, T_total > 0, gate)) != KDA_OK)
         return st;
     const size_t need = kda_varlen_workspace_bytes(N, H, d_k, d_v);
     if (!workspace || workspace_bytes < need)
@@ -175,17 +201,50 @@ kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda
     int32_t *tail = reinterpret_cast<int32_t *>(ws + align_up((size_t)N * sizeof(int32_t)));
     int32_t *counter = tail;
     int32_t *status = device_status ? device_status : tail + 1;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    cudaError_t e = kda::launch_varlen_prep(cu_seqlens, N, T_total, order, counter, status, s);
+    cudaError_t e = kda::launch_varlen_prep(cu_seqlens, N, T_total, order, counter, status, slots, pool_size, s);
     if (e != cudaSuccess) return cuda_status(e, "varlen prep launch");
 
     kda::PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = initial_state;
     a.o = o; a.sT = final_state; a.cu_seqlens = cu_seqlens;
+    a.gate = gate; a.slots = slots;
     a.N = N; a.T = T_total; a.H = H; a.dk = d_k; a.dv = d_v; a.dt = qkv_dtype;
     a.order = order; a.counter = counter; a.dev_status = status;
     return run_prefill(a, KDA_ALGO_AUTO, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                const float *alpha, const float *beta,
+                                const float *initial_state, void *o, float *final_state,
+                                const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
+                                int d_v, void *workspace, size_t workspace_bytes,
+                                int32_t *device_status, kda_stream_t stream) {
+    return varlen_prefill(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, initial_state, o, final_state,
+                          nullptr, 0, cu_seqlens, N, T_total, H, d_k, d_v, workspace, workspace_bytes,
+                          device_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_varlen_prefill_slots(const void *q, const void *k, const void *v,
+                                      kda_dtype_t qkv_dtype, const float *alpha, kda_gate_t gate,
+                                      const float *beta, float *state_pool, const int32_t *slots,
+                                      int pool_size, void *o, const int32_t *cu_seqlens, int N,
+                                      int T_total, int H, int d_k, int d_v, void *workspace,
+                                      size_t workspace_bytes, int32_t *device_status,
+                                      kda_stream_t stream) {
+    if (N > 0) {
+        KDA_REQUIRE_PTR(state_pool);
+        if (!slots) return fail(KDA_ERR_INVALID_ARG, "slots must not be NULL");
+        if (reinterpret_cast<uintptr_t>(slots) & 3u) return fail(KDA_ERR_INVALID_ARG, "slots must be 4-byte aligned");
+        if (pool_size <= 0) return fail(KDA_ERR_INVALID_ARG, "pool_size must be positive");
+    }
+    return varlen_prefill(q, k, v, qkv_dtype, alpha, gate, beta, state_pool, o, state_pool, slots, pool_size,
+                          cu_seqlens, N, T_total, H, d_k, d_v, workspace, workspace_bytes, device_status,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
@@ -199,8 +258,38 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dt
     if ((int64_t)N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N * H must fit in int32");
     if ((st = check_tensors(q, k, v, alpha, beta, o, nullptr, nullptr, true)) != KDA_OK) return st;
     KDA_REQUIRE_PTR(state);
-    return cuda_status(kda::launch_decode(q, k, v, qkv_dtype, alpha, beta, state, o, N, H, d_k, d_v,
-                                          reinterpret_cast<cudaStream_t>(stream)),
+    return cuda_status(kda::launch_decode(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, state, nullptr, 0,
+                                          nullptr, o, N, H, d_k, d_v, reinterpret_cast<cudaStream_t>(stream)),
+                       "decode launch");
+}
+
+kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                   const float *alpha, kda_gate_t gate, const float *beta,
+                                   float *state_pool, const int32_t *slots, int pool_size, void *o,
+                                   int N, int H, int d_k, int d_v, int32_t *device_status,
+                                   kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_gate(gate)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (N < 0) return fail(KDA_ERR_INVALID_ARG, "N must be >= 0");
+    if (N == 0) return ok();
+    if ((int64_t)N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N * H must fit in int32");
+    if ((st = check_tensors(q, k, v, alpha, beta, o, nullptr, nullptr, true, gate)) != KDA_OK) return st;
+    KDA_REQUIRE_PTR(state_pool);
+    if (!slots) return fail(KDA_ERR_INVALID_ARG, "slots must not be NULL");
+    if (reinterpret_cast<uintptr_t>(slots) & 3u) return fail(KDA_ERR_INVALID_ARG, "slots must be 4-byte aligned");
+    if (pool_size <= 0) return fail(KDA_ERR_INVALID_ARG, "pool_size must be positive");
+    if ((int64_t)pool_size * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "pool_size * H must fit in int32");
+    if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+        return fail(KDA_ERR_INVALID_ARG, "device_status must be 4-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (device_status) {  // KDA_DEV_OK unless a head finds a bad slot
+        const cudaError_t e = cudaMemsetAsync(device_status, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_status(e, "status reset");
+    }
+    return cuda_status(kda::launch_decode(q, k, v, qkv_dtype, alpha, gate, beta, state_pool, slots, pool_size,
+                                          device_status, o, N, H, d_k, d_v, s),
                        "decode launch");
 }
 

@@ -14,6 +14,11 @@
 // loads). All of a thread's loads are issued before any arithmetic. The two
 // column reductions over key rows (S'^T k and S'^T q) go through shared
 // memory; the rank-1 write then needs only the reduced error vector.
+//
+// Gate kinds: the per-channel gate, one scalar gate per head (Gated DeltaNet)
+// or none (the delta rule). With a slot map the state of sequence n is the
+// pool entry slots[n] (zeros for a fresh slot); an out-of-range slot skips
+// its heads and reports KDA_DEV_BAD_SLOT.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -31,8 +36,9 @@ __device__ __forceinline__ void st_stream(float *p, float4 v) {
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
-                  const float *__restrict__ alpha, const float *__restrict__ beta,
-                  float *__restrict__ state, TIn *__restrict__ o) {
+                  const float *__restrict__ alpha, int gate, const float *__restrict__ beta,
+                  float *__restrict__ state, const int32_t *__restrict__ slots, int pool_size,
+                  int32_t *__restrict__ status, int H, TIn *__restrict__ o) {
     constexpr int TPR = DV / 4;                     // threads per state row
     constexpr int RPP = kDecodeThreads / TPR;       // rows per pass
     constexpr int PASSES = DK / RPP;                // rows per thread
@@ -48,17 +54,23 @@ kda_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
     const int tid = threadIdx.x;
     const int col = (tid % TPR) * 4;
     const int row0 = tid / TPR;
-    float *S = state + head * (int64_t)DK * DV;
+    bool fresh;
+    const int64_t slot = slot_of(slots, (int)(head / H), fresh);
+    if (slots && slot >= pool_size) {  // uniform over the CTA
+        if (tid == 0 && status) atomicOr(status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+    float *S = state + (slot * H + head % H) * (int64_t)DK * DV;
 
     // Issue the whole state tile first: PASSES independent 16-byte loads.
     float4 s[PASSES];
 #pragma unroll
     for (int p = 0; p < PASSES; ++p)
-        s[p] = ld_stream(S + (int64_t)(row0 + p * RPP) * DV + col);
+        s[p] = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_stream(S + (int64_t)(row0 + p * RPP) * DV + col);
 
     // Gate, gated key / query and the partial sums of q.k.
     if (tid < DK) {
-        const float a = alpha[head * DK + tid];
+        const float a = gate_at(alpha, gate, head, tid, DK);
         const float kk = to_f32(k[head * DK + tid]);
         const float qq = to_f32(q[head * DK + tid]);
         s_a[tid] = a;
@@ -115,27 +127,29 @@ kda_decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TI
 }
 
 template <int DK, int DV, typename TIn>
-cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const float *alpha,
-                            const float *beta, float *state, void *o, int N, int H,
-                            cudaStream_t s) {
+cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const float *alpha, int gate,
+                            const float *beta, float *state, const int32_t *slots, int pool_size,
+                            int32_t *status, void *o, int N, int H, cudaStream_t s) {
     const int64_t heads = (int64_t)N * H;
     if (heads == 0) return cudaSuccess;
     kda_decode_kernel<DK, DV, TIn><<<(unsigned)heads, kDecodeThreads, 0, s>>>(
-        (const TIn *)q, (const TIn *)k, (const TIn *)v, alpha, beta, state, (TIn *)o);
+        (const TIn *)q, (const TIn *)k, (const TIn *)v, alpha, gate, beta, state, slots, pool_size, status, H,
+        (TIn *)o);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, kda_dtype_t dt,
-                          const float *alpha, const float *beta, float *state, void *o,
+                          const float *alpha, int gate, const float *beta, float *state,
+                          const int32_t *slots, int pool_size, int32_t *status, void *o,
                           int N, int H, int dk, int dv, cudaStream_t s) {
-#define KDA_DECODE_CASE(DK_, DV_)                                                              \
-    if (dk == DK_ && dv == DV_) {                                                              \
-        return dt == KDA_BF16                                                                  \
-                   ? launch_decode_t<DK_, DV_, __nv_bfloat16>(q, k, v, alpha, beta, state, o, \
-                                                             N, H, s)                          \
-                   : launch_decode_t<DK_, DV_, float>(q, k, v, alpha, beta, state, o, N, H, s); \
+#define KDA_DECODE_CASE(DK_, DV_)                                                                     \
+    if (dk == DK_ && dv == DV_) {                                                                     \
+        return dt == KDA_BF16 ? launch_decode_t<DK_, DV_, __nv_bfloat16>(q, k, v, alpha, gate, beta, state, \
+                                                                        slots, pool_size, status, o, N, H, s) \
+                              : launch_decode_t<DK_, DV_, float>(q, k, v, alpha, gate, beta, state, slots,  \
+                                                                pool_size, status, o, N, H, s);            \
     }
     KDA_DECODE_CASE(128, 128)
     KDA_DECODE_CASE(64, 64)

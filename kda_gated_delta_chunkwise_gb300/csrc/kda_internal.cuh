@@ -18,9 +18,29 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
+// Gate of key channel c at token-head index th (= token * H + head): the
+// channel's own gate, the token-head's scalar gate for every channel, or 1.
+__device__ __forceinline__ float gate_at(const float *alpha, int gate, int64_t th, int c, int dk) {
+    return gate == KDA_GATE_CHANNEL ? alpha[th * dk + c] : gate == KDA_GATE_SCALAR ? alpha[th] : 1.f;
+}
+
+// State slot of sequence n: slots[n] >= 0 is a slot whose state is read and
+// written back, -1 - s is slot s starting from zeros (fresh = true). Without
+// a slot map the state of sequence n is entry n.
+__device__ __forceinline__ int64_t slot_of(const int32_t *slots, int n, bool &fresh) {
+    if (!slots) {
+        fresh = false;
+        return n;
+    }
+    const int32_t s = slots[n];
+    fresh = s < 0;
+    return fresh ? -1 - (int64_t)s : (int64_t)s;
+}
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_decode(const void *q, const void *k, const void *v, kda_dtype_t dt,
-                          const float *alpha, const float *beta, float *state, void *o,
+                          const float *alpha, int gate, const float *beta, float *state,
+                          const int32_t *slots, int pool_size, int32_t *status, void *o,
                           int N, int H, int dk, int dv, cudaStream_t s);
 
 // Prefill over sequences given by cu_seqlens (device) or, when cu_seqlens is
@@ -32,6 +52,8 @@ struct PrefillArgs {
     const float *alpha, *beta, *s0;
     void *o;
     float *sT;
+    int gate;                   // kda_gate_t: the layout of alpha
+    const int32_t *slots;       // nullable: state slot map (see slot_of); s0 and sT are then the pool
     const int32_t *cu_seqlens;  // null: equal lengths
     int N, T, H, dk, dv;        // T: tokens per sequence (equal) or T_total (packed)
     kda_dtype_t dt;
@@ -48,8 +70,10 @@ cudaError_t read_device_error(int *out, bool reset);
 
 // Varlen preparation: validates cu_seqlens, writes the status word, sorts the
 // sequences by length (longest first) into `order` and zeroes `counter`.
+// With a slot map it also checks that every slot lies in [0, pool_size).
 cudaError_t launch_varlen_prep(const int32_t *cu_seqlens, int N, int T_total, int32_t *order,
-                               int32_t *counter, int32_t *status, cudaStream_t s);
+                               int32_t *counter, int32_t *status, const int32_t *slots, int pool_size,
+                               cudaStream_t s);
 
 // Records `msg` as this thread's last error and returns `st`.
 kda_status_t set_error(kda_status_t st, const char *msg);

@@ -92,12 +92,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
     const TIn *k = (const TIn *)a.k;
     const TIn *v = (const TIn *)a.v;
     TIn *o = (TIn *)a.o;
-    const int64_t state_off = ((int64_t)n * H + h) * DK * DV;
+    bool fresh;
+    const int64_t state_off = (slot_of(a.slots, n, fresh) * H + h) * DK * DV;
 
     // ---- initial state slice ----
     for (int e = tid; e < DK * VS; e += NT) {
         const int c = e / VS, j = e % VS;
-        sm.S[e] = a.s0 ? a.s0[state_off + (int64_t)c * DV + v0 + j] : 0.f;
+        sm.S[e] = (a.s0 && !fresh) ? a.s0[state_off + (int64_t)c * DV + v0 + j] : 0.f;
     }
     __syncthreads();
 
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
 #pragma unroll
             for (int i = 0; i < TPS; ++i) {
                 const int r = seg * TPS + i;
-                al[i] = r < L ? a.alpha[((tok0 + r) * H + h) * DK + c] : 1.f;
+                al[i] = r < L ? gate_at(a.alpha, a.gate, (tok0 + r) * H + h, c, DK) : 1.f;
                 prod *= al[i];
             }
             sm.part[seg * DK + c] = prod;
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 const int j = tid % VS, part = tid / VS;  // 4 parts of the key rows
                 float vh = 0.f;
                 for (int c = part; c < DK; c += NT / VS)
-                    vh += a.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * sm.S[c * VS + j];
+                    vh += gate_at(a.alpha, a.gate, tk, c, DK) * ld_in(k, tk * DK + c) * sm.S[c * VS + j];
                 sm.R[part * VS + j] = vh;
                 __syncthreads();
                 if (tid < VS) {
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 __syncthreads();
                 float op = 0.f;
                 for (int c = part; c < DK; c += NT / VS) {
-                    const float sn = a.alpha[tk * DK + c] * sm.S[c * VS + j] +
+                    const float sn = gate_at(a.alpha, a.gate, tk, c, DK) * sm.S[c * VS + j] +
                                      ld_in(k, tk * DK + c) * sm.U[j];
                     sm.S[c * VS + j] = sn;
                     op += ld_in(q, tk * DK + c) * sn;

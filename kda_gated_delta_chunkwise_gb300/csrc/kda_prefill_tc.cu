@@ -142,6 +142,8 @@ struct TcParams {
     const int32_t *order;
     const int32_t *dev_status;
     int32_t *err;
+    const int32_t *slots;  // nullable: state slot map (s0 and sT are then the pool)
+    int gate;              // kda_gate_t
     int N, T, H;
 };
 
@@ -286,7 +288,7 @@ __device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
 // shared memory. Rare, so it is written for size rather than speed, and out
 // of line: the hot loop of the epilogue stays contiguous in the instruction
 // caches.
-__device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, const __nv_bfloat16 *__restrict__ kin,
+__device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gate, const __nv_bfloat16 *__restrict__ kin,
                                         const __nv_bfloat16 *__restrict__ qin, const __nv_bfloat16 *__restrict__ vin,
                                         const float *__restrict__ beta, __nv_bfloat16 *__restrict__ o, float *red,
                                         uint32_t tm_d, int l, int warp, int lane, int64_t tok0, int L, int H, int h,
@@ -296,7 +298,7 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, const _
 #pragma unroll 1
     for (int r = 0; r < L; ++r) {
         const int64_t tk = (tok0 + r) * H + h;
-        const float a = alpha[tk * DK + l];
+        const float a = gate_at(alpha, gate, tk, l, DK);
         const float kf = __bfloat162float(kin[tk * DK + l]);
         const float qf = __bfloat162float(qin[tk * DK + l]);
         // S' = Diag(alpha) S, and this warp's part of S'^T k
@@ -348,6 +350,9 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, const _
 }
 
 // --------------------------------------------------------------------------
+// GATE (a kda_gate_t) is a template parameter so that each gate kind keeps
+// the per-chunk code of the gate group as small as the per-channel one.
+template <int GATE>
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_v) {
@@ -377,14 +382,16 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
     const int H = p.H;
     const int v0 = (int)rank * VS;   // first value column of this CTA's state slice
     const int c0 = (int)rank * KH;   // first key channel of this CTA's gate half
-    const int64_t state_off = ((int64_t)seq * H + h) * DK * DV;
+    bool fresh;  // a fresh slot starts from the zero state
+    const int64_t state_off = (slot_of(p.slots, seq, fresh) * H + h) * DK * DV;
+    const float *s0 = fresh ? nullptr : p.s0;
     const int NC = (int)((T + C - 1) / C);
 
     if (NC == 0) {  // empty sequence: the final state is the initial one
         if (p.sT)
             for (int e = tid; e < DK * VS; e += NTHREADS) {
                 const int c = e / VS, j = e % VS;
-                p.sT[state_off + (int64_t)c * DV + v0 + j] = p.s0 ? p.s0[state_off + (int64_t)c * DV + v0 + j] : 0.f;
+                p.sT[state_off + (int64_t)c * DV + v0 + j] = s0 ? s0[state_off + (int64_t)c * DV + v0 + j] : 0.f;
             }
         return;
     }
@@ -572,7 +579,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         bool slow_prev = false;
         // St_0 = Diag(mu_0) S0 -> TMEM (fp32 accumulator base) and the bf16 operand
         {
-            const float *src = (ok && p.s0) ? p.s0 + state_off + (int64_t)l * DV + v0 : nullptr;
+            const float *src = (ok && s0) ? s0 + state_off + (int64_t)l * DV + v0 : nullptr;
             unsigned char *st = s.base + SM_ST;
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
@@ -718,7 +725,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // one decision for the whole group: the slow path has group barriers
                 go = !named_bar_or(2, EPI_THREADS, !go);
                 if (go)
-                    slow_chunk(p.alpha, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d,
+                    slow_chunk(p.alpha, p.gate, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d,
                                l, warp, lane, tok0, L, H, h, v0);
             }
             unsigned char *st = s.base + SM_ST;
@@ -780,9 +787,13 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // global memory straight into registers: prefetched into L2 one chunk
         // ahead, loaded before the chunk's waits (rows past the sequence end
         // are not read)
+        // (one gate per token-head, broadcast over the channels, for the
+        // scalar kind; none at all for the delta rule)
         auto alpha_src = [&](int n) {
-            return p.alpha + ((t_begin + (int64_t)n * C + 8 * rg) * H + h) * DK + c0 + 4 * cq;
+            const int64_t th = (t_begin + (int64_t)n * C + 8 * rg) * H + h;
+            return GATE == KDA_GATE_CHANNEL ? p.alpha + th * DK + c0 + 4 * cq : p.alpha + th;
         };
+        const int64_t astep = GATE == KDA_GATE_CHANNEL ? (int64_t)H * DK : (int64_t)H;  // one token
         bool alive = true;
         for (int n = 0; n <= NC; ++n) {
           if (n < NC) {
@@ -796,9 +807,18 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             {
                 const float *src = alpha_src(n);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    arow[j] = 8 * rg + j < L ? __ldg(reinterpret_cast<const float4 *>(src + (int64_t)j * H * DK))
-                                             : make_float4(1.f, 1.f, 1.f, 1.f);
+                for (int j = 0; j < 8; ++j) {
+                    float4 a = make_float4(1.f, 1.f, 1.f, 1.f);
+                    if (8 * rg + j < L) {
+                        if constexpr (GATE == KDA_GATE_CHANNEL) {
+                            a = __ldg(reinterpret_cast<const float4 *>(src + (int64_t)j * H * DK));
+                        } else if constexpr (GATE == KDA_GATE_SCALAR) {
+                            const float x = __ldg(src + (int64_t)j * H);
+                            a = make_float4(x, x, x, x);
+                        }
+                    }
+                    arow[j] = a;
+                }
             }
             const int b3 = b;  // A0 and B0 slots go together
             alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
@@ -880,7 +900,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 const float *src = alpha_src(n + 1);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (8 * rg + j < Ln) prefetch_l2(src + (int64_t)j * H * DK);
+                    if (GATE != KDA_GATE_NONE && 8 * rg + j < Ln) prefetch_l2(src + j * astep);
             }
             if (ok && pt == 0) {
                 // this key half into the peer (its slot n % 3 was released with
@@ -1224,14 +1244,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     p.order = a.order;
     p.dev_status = a.dev_status;
     p.err = nullptr;
+    p.slots = a.slots;
+    p.gate = a.gate;
     p.N = a.N;
     p.T = a.T;
     p.H = a.H;
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    auto kern = a.gate == KDA_GATE_SCALAR ? kda_prefill_tc_kernel<KDA_GATE_SCALAR>
+                : a.gate == KDA_GATE_NONE ? kda_prefill_tc_kernel<KDA_GATE_NONE>
+                                          : kda_prefill_tc_kernel<KDA_GATE_CHANNEL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // blocks is even: one cluster of NSLICE CTAs per (sequence, head)
-    kda_prefill_tc_kernel<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(p, mk, mq, mv);
+    kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(p, mk, mq, mv);
     return cudaGetLastError();
 }
 

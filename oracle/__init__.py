@@ -123,6 +123,32 @@ def run(q, k, v, alpha, beta, cu_seqlens=None, initial_state=None,
     return o, sT
 
 
+def expand_gate(alpha, gate: str, lead: tuple, dk: int) -> np.ndarray:
+    """The per-channel gate that a scalar gate or no gate stands for.
+
+    The K3 essay's §四 sets KDA's per-channel gate Diag(alpha_t) beside the
+    scalar gate alpha_t of Gated DeltaNet; without a gate the update is the
+    delta rule of §三 (alpha_t = 1). A scalar gate multiplies every channel by
+    the same alpha_t, so it is the per-channel gate with alpha_t repeated
+    over the d_k channels. Returns float64 ``[*lead, dk]``. (Input preparation
+    only: the recurrence itself is :func:`run`.)
+    """
+    lead = tuple(lead)
+    if gate == "channel":
+        a = _f64(alpha)
+        if a.shape != lead + (dk,):
+            raise ValueError(f"channel gate must be {lead + (dk,)}, got {a.shape}")
+        return a
+    if gate == "scalar":
+        a = _f64(alpha)
+        if a.shape != lead:
+            raise ValueError(f"scalar gate must be {lead}, got {a.shape}")
+        return np.repeat(a[..., None], dk, axis=-1)
+    if gate == "none":
+        return np.ones(lead + (dk,), dtype=np.float64)
+    raise ValueError(f"unknown gate {gate!r}")
+
+
 def max_threads(nthreads: int = 0) -> int:
     """Threads the oracle's OpenMP loop will use."""
     return int(load().kda_oracle_max_threads(int(nthreads)))

@@ -112,3 +112,37 @@ def test_decode_argument_checks(lib):
     assert lib.kda_decode_step(p, p, p, 1, p, p, None, p, 4, 2, 128, 128, None) == 1
     assert lib.kda_decode_step(p, p, p, 1, p, p, p, p, 4, 2, 80, 128, None) == 2
     assert lib.kda_decode_step(p, p, p, 1, p, p, p, p, 0, 2, 128, 128, None) == 0
+
+
+def test_gate_and_slot_argument_checks(lib):
+    """The gate-kind and slot entry points reject bad arguments before any
+    launch (no GPU is touched here)."""
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    ws = 4096
+    # unknown gate kind
+    assert lib.kda_prefill_gate(p, p, p, 1, p, 7, p, None, p, None, 1, 8, 2, 128, 128, 0, None) == 1
+    # per-channel gate needs a 16-byte aligned alpha; a scalar gate 4-byte; no gate none at all
+    assert lib.kda_prefill_gate(p, p, p, 1, odd, 0, p, None, p, None, 1, 8, 2, 128, 128, 0, None) == 1
+    assert lib.kda_prefill_gate(p, p, p, 1, ctypes.c_void_p(0x1001), 1, p, None, p, None, 1, 8, 2, 128, 128, 0,
+                                None) == 1
+    assert lib.kda_prefill_gate(p, p, p, 1, None, 1, p, None, p, None, 1, 8, 2, 128, 128, 0, None) == 1
+    # empty batch: nothing to do whatever the gate
+    assert lib.kda_prefill_gate(None, None, None, 1, None, 2, None, None, None, None, 0, 8, 2, 128, 128, 0,
+                                None) == 0
+    # slots: pool and slot map required, pool_size positive
+    assert lib.kda_varlen_prefill_slots(p, p, p, 1, p, 0, p, None, p, 4, p, p, 2, 100, 2, 128, 128, p, ws,
+                                        None, None) == 1
+    assert lib.kda_varlen_prefill_slots(p, p, p, 1, p, 0, p, p, None, 4, p, p, 2, 100, 2, 128, 128, p, ws,
+                                        None, None) == 1
+    assert lib.kda_varlen_prefill_slots(p, p, p, 1, p, 0, p, p, p, 0, p, p, 2, 100, 2, 128, 128, p, ws,
+                                        None, None) == 1
+    assert lib.kda_varlen_prefill_slots(p, p, p, 1, p, 9, p, p, p, 4, p, p, 2, 100, 2, 128, 128, p, ws,
+                                        None, None) == 1
+    assert lib.kda_varlen_prefill_slots(None, None, None, 1, None, 0, None, None, None, 0, None, None, 0, 0, 2,
+                                        128, 128, None, 0, None, None) == 0
+    assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, None, p, 4, p, 3, 2, 128, 128, None, None) == 1
+    assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, None, 4, p, 3, 2, 128, 128, None, None) == 1
+    assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 0, p, 3, 2, 128, 128, None, None) == 1
+    assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 4, p, 3, 2, 128, 128, odd, None) == 1
+    assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 4, p, 0, 2, 128, 128, None, None) == 0

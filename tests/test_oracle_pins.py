@@ -238,3 +238,62 @@ def test_thread_count_does_not_change_bits():
     o4, s4 = oracle.run(q, k, v, a, b, initial_state=S0, nthreads=4)
     np.testing.assert_array_equal(o1, o4)
     np.testing.assert_array_equal(s1, s4)
+
+
+def test_scalar_gate_expansion_is_gated_deltanet():
+    """The scalar gate of Gated DeltaNet (§四), given per token and head and
+    expanded by oracle.expand_gate, is the per-channel gate repeated over the
+    channels: the oracle then follows alpha_t (I - beta k k^T) S + beta k v^T
+    with a different alpha in every token and head."""
+    rng = np.random.default_rng(41)
+    B, T, H, dk, dv = 2, 9, 3, 5, 4
+    q, k, v, _, b, S0 = _rand_inputs(rng, B, T, H, dk, dv)
+    s = rng.uniform(0.1, 1.0, (B, T, H))
+    a = oracle.expand_gate(s, "scalar", (B, T, H), dk)
+    assert a.shape == (B, T, H, dk)
+    o, sT = oracle.run(q, k, v, a, b, initial_state=S0)
+    for bi in range(B):
+        for hi in range(H):
+            S = S0[bi, hi].copy()
+            for t in range(T):
+                kt = k[bi, t, hi]
+                S = s[bi, t, hi] * (np.eye(dk) - b[bi, t, hi] * np.outer(kt, kt)) @ S \
+                    + b[bi, t, hi] * np.outer(kt, v[bi, t, hi])
+                np.testing.assert_allclose(o[bi, t, hi], S.T @ q[bi, t, hi], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(sT[bi, hi], S, rtol=1e-12, atol=1e-12)
+
+
+def test_no_gate_is_the_delta_rule():
+    """Without a gate (§三) the update is S = (I - beta k k^T) S + beta k v^T;
+    writing two values under the same unit key with beta = 1 leaves only the
+    second one (the erase removes the first)."""
+    rng = np.random.default_rng(42)
+    B, T, H, dk, dv = 1, 12, 2, 6, 3
+    q, k, v, _, b, S0 = _rand_inputs(rng, B, T, H, dk, dv)
+    a = oracle.expand_gate(None, "none", (B, T, H), dk)
+    assert np.all(a == 1.0)
+    o, sT = oracle.run(q, k, v, a, b, initial_state=S0)
+    for hi in range(H):
+        S = S0[0, hi].copy()
+        for t in range(T):
+            kt = k[0, t, hi]
+            S = S - b[0, t, hi] * np.outer(kt, kt @ S) + b[0, t, hi] * np.outer(kt, v[0, t, hi])
+            np.testing.assert_allclose(o[0, t, hi], S.T @ q[0, t, hi], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(sT[0, hi], S, rtol=1e-12, atol=1e-12)
+    # overwrite: same unit key twice, beta = 1, read back with q = k
+    u = rng.standard_normal(dk)
+    u /= np.linalg.norm(u)
+    kk = np.broadcast_to(u, (1, 2, 1, dk)).copy()
+    vv = rng.standard_normal((1, 2, 1, dv))
+    bb = np.ones((1, 2, 1))
+    o2, _ = oracle.run(kk, kk, vv, oracle.expand_gate(None, "none", (1, 2, 1), dk), bb)
+    np.testing.assert_allclose(o2[0, 1, 0], vv[0, 1, 0], rtol=0, atol=1e-12)
+
+
+def test_expand_gate_rejects_wrong_shapes():
+    with pytest.raises(ValueError):
+        oracle.expand_gate(np.ones((2, 3)), "scalar", (2, 3, 1), 4)
+    with pytest.raises(ValueError):
+        oracle.expand_gate(np.ones((2, 3, 4)), "channel", (2, 3), 5)
+    with pytest.raises(ValueError):
+        oracle.expand_gate(None, "sigmoid", (1,), 2)
