@@ -50,10 +50,13 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def prefill_bytes(B, T, H, dk, dv, qkv_bytes=2, with_s0=False):
+def prefill_bytes(B, T, H, dk, dv, qkv_bytes=2, with_s0=False, gate="channel"):
     """Algorithmic HBM bytes of one prefill call: q, k, v, alpha, beta read
-    once, o written once, final state written once (and S0 read if given)."""
-    per_tok_head = 2 * dk * qkv_bytes + dv * qkv_bytes + dk * 4 + 4 + dv * qkv_bytes
+    once, o written once, final state written once (and S0 read if given).
+    alpha is d_k floats per token-head for the per-channel gate, one for the
+    scalar gate, none without a gate."""
+    alpha_bytes = {"channel": dk * 4, "scalar": 4, "none": 0}[gate]
+    per_tok_head = 2 * dk * qkv_bytes + dv * qkv_bytes + alpha_bytes + 4 + dv * qkv_bytes
     state = B * H * dk * dv * 4
     return B * T * H * per_tok_head + state * (2 if with_s0 else 1)
 
@@ -235,6 +238,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -330,6 +334,30 @@ def main():
         e2e = {"value": job_tokens_per_s(world, B * T, dt), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
 
+    # ---- the same workload with a scalar gate (Gated DeltaNet) and without a
+    #      gate (the delta rule): fewer gate bytes, same kernels ----
+    variants = None
+    if not args.no_variants:
+        variants = {}
+        for name, gate in (("gated_deltanet", "scalar"), ("deltanet", "none")):
+            av = a[..., 0].contiguous() if gate == "scalar" else None
+            for _ in range(args.warmup):
+                kda.prefill(q, k, v, av, b, None, out=o, final_state=sT, algo=args.algo, gate=gate)
+            torch.cuda.synchronize()
+            evv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for i in range(args.steps):
+                evv[i][0].record(stream)
+                kda.prefill(q, k, v, av, b, None, out=o, final_state=sT, algo=args.algo, gate=gate)
+                evv[i][1].record(stream)
+            torch.cuda.synchronize()
+            vms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in evv)
+            vbytes = prefill_bytes(B, T, H, DK, DV, gate=gate)
+            variants[name] = {"gate": gate, "value": B * T / (vms / 1e3), "unit": "tokens/s",
+                              "ms_per_step": vms, "algorithmic_bytes_per_launch": vbytes,
+                              "achieved_gbs": vbytes / (vms / 1e3) / 1e9,
+                              "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+
     # ---- decode step (secondary figure of the metric) ----
     decode = None
     if not args.no_decode:
@@ -371,6 +399,7 @@ def main():
                            "l2": "inputs larger than L2 (0.34 GB in, 0.41 GB moved per step; L2 129 MB)",
                            "parallelism": f"{world} independent replica(s)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+                "gate_variants": variants,
                 "gpu_launches": args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:
