@@ -134,6 +134,51 @@ def _to_host(x: torch.Tensor) -> torch.Tensor:
     return h
 
 
+_copy_streams: dict = {}
+
+
+def _streams(dev: torch.device, n: int):
+    """n CUDA streams of the device, created once and reused."""
+    with _lock:
+        pool = _copy_streams.setdefault(dev.index, [])
+        while len(pool) < n:
+            pool.append(torch.cuda.Stream(dev))
+        return pool[:n]
+
+
+def _host_prefill(q, k, v, alpha, beta, initial_state, *, output_final_state, algo, gate, groups: int = 4):
+    """``prefill`` on host tensors. The batch is split into groups of
+    sequences, each group on its own stream: copy in, run, copy out. The
+    sequences are independent, so the result is the same as one call; the
+    copies of one group overlap the kernels and the opposite-direction copies
+    of the others (host-to-device and device-to-host use separate engines)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B = q.shape[0]
+    G = max(1, min(groups, B))
+    bounds = [(B * g // G, B * (g + 1) // G) for g in range(G)]
+    o_h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    s_h = (torch.empty((B,) + tuple(q.shape[2:3]) + (q.shape[-1], v.shape[-1]), dtype=torch.float32,
+                       pin_memory=True) if output_final_state else None)
+    cur = torch.cuda.current_stream(dev)
+    streams = _streams(dev, G)
+    for (lo, hi), st in zip(bounds, streams):
+        if hi == lo:
+            continue
+        st.wait_stream(cur)  # after whatever the caller queued before
+        with torch.cuda.stream(st):
+            part = [None if t is None else t[lo:hi].to(dev, non_blocking=True)
+                    for t in (q, k, v, alpha, beta, initial_state)]
+            o_d, s_d = prefill(*part[:5], part[5], output_final_state=output_final_state, algo=algo,
+                               gate=gate, stream=st)
+            o_h[lo:hi].copy_(o_d, non_blocking=True)
+            if s_h is not None:
+                s_h[lo:hi].copy_(s_d, non_blocking=True)
+    for st in streams:
+        cur.wait_stream(st)
+    cur.synchronize()
+    return o_h, s_h
+
+
 def _host_call(fn, tensors: dict, **kw):
     """Run ``fn`` on the CUDA device for host inputs; return host outputs.
     Inputs in pinned memory are copied asynchronously; outputs land in pinned
@@ -173,9 +218,8 @@ def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: boo
     Returns (o [B, T, H, d_v] in v's dtype, final_state [B, H, d_k, d_v] fp32 or None).
     """
     if q.device.type == "cpu":
-        return _host_call(prefill, dict(q=q, k=k, v=v, alpha=alpha, beta=beta,
-                                        initial_state=initial_state),
-                          output_final_state=output_final_state, algo=algo, gate=gate)
+        return _host_prefill(q, k, v, alpha, beta, initial_state, output_final_state=output_final_state,
+                             algo=algo, gate=gate)
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

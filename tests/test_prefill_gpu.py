@@ -179,3 +179,18 @@ def test_host_buffers_round_trip(kda):
     assert o_h.device.type == "cpu" and o_h.is_pinned()
     torch.testing.assert_close(o_h, o_d.cpu(), rtol=0, atol=0)
     torch.testing.assert_close(s_h, s_d.cpu(), rtol=0, atol=0)
+
+
+def test_host_buffers_split_over_streams(kda):
+    """The host path splits the batch over several streams (copy in, run, copy
+    out per group): five sequences in four groups, a scalar gate and no final
+    state give the device call's bits."""
+    x = W.batched(5, 130, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=32)
+    a_s = x.alpha[..., 0].contiguous()
+    q, k, v, _, b, s0 = _dev(x)
+    o_d, _ = kda.prefill(q, k, v, a_s.cuda(), b, s0, gate="scalar", output_final_state=False)
+    o_h, s_h = kda.prefill(x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory(), a_s.pin_memory(),
+                           x.beta.pin_memory(), x.initial_state.pin_memory(), gate="scalar",
+                           output_final_state=False)
+    assert s_h is None and o_h.is_pinned()
+    torch.testing.assert_close(o_h, o_d.cpu(), rtol=0, atol=0)
