@@ -183,6 +183,26 @@ kda_status_t kda_prefill_gate(const void *q, const void *k, const void *v, kda_d
                               int H, int d_k, int d_v, kda_algo_t algo, kda_stream_t stream);
 
 /*
+ * kda_prefill_fp8 - kda_prefill_gate on FP8 inputs in the MX block format:
+ * q, k, v hold FP8 E4M3 codes and every 32 consecutive channels (values) of a
+ * token-head share one E8M0 scale byte t, the power of two 2^(t - 127):
+ *
+ *   q, k        [B, T, H, d_k] uint8 (E4M3)      q_scale, k_scale [B, T, H, d_k/32] uint8
+ *   v           [B, T, H, d_v] uint8 (E4M3)      v_scale          [B, T, H, d_v/32] uint8
+ *   o           [B, T, H, d_v] bfloat16 (written)
+ *
+ * The result is that of kda_prefill_gate with bf16 q, k, v holding the
+ * dequantised values (code x 2^(t-127), exactly representable in bf16 for
+ * t in [1, 254]); the inputs simply take half the bytes. Tensor-core kernel
+ * only: d_k = d_v = 128. Scale bytes 0 and 255 are not supported (their
+ * values are undefined); E4M3 NaN codes propagate.
+ */
+kda_status_t kda_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, const uint8_t *q_scale,
+                             const uint8_t *k_scale, const uint8_t *v_scale, const float *alpha,
+                             kda_gate_t gate, const float *beta, const float *initial_state, void *o,
+                             float *final_state, int B, int T, int H, int d_k, int d_v, kda_stream_t stream);
+
+/*
  * State slots for serving: a pool of recurrent states that outlives the calls
  * (prefill, then any number of decode steps, or a long prompt prefilled in
  * pieces), each request owning one slot. Both calls below read a sequence's

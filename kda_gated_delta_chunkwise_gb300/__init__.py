@@ -5,11 +5,12 @@ Per sequence and head, S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1}
 "研究KimiK3，我发现大模型正在学会“管理自己的计算”", pwwt.cn, §四 and §二.1).
 
 Entry points (thin ctypes binding over the C ABI in include/kda.h):
-``prefill`` (per-channel, scalar or no gate), ``varlen_prefill``,
+``prefill`` (per-channel, scalar or no gate), ``prefill_fp8`` (MX-style FP8
+q, k, v), ``varlen_prefill``,
 ``decode_step``, and for serving with a pool of states indexed by slot:
 ``varlen_prefill_slots``, ``decode_step_slots``. Build the CUDA library with
 ``kda_gated_delta_chunkwise_gb300.build.build()`` first.
 """
 from ._binding import (ALGOS, EXPORTS, GATES, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT,  # noqa: F401
                        KDA_DEV_OK, KdaError, decode_step, decode_step_slots, device_errors, lib_path, load,
-                       prefill, varlen_prefill, varlen_prefill_slots, varlen_workspace_bytes)
+                       prefill, prefill_fp8, varlen_prefill, varlen_prefill_slots, varlen_workspace_bytes)

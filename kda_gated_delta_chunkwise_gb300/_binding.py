@@ -26,7 +26,7 @@ ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 GATES = {"channel": 0, "scalar": 1, "none": 2}
 KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT = 0, 1, 2
 
-EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_varlen_prefill", "kda_varlen_prefill_slots",
+EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8", "kda_varlen_prefill", "kda_varlen_prefill_slots",
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_decode_step", "kda_decode_step_slots",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
@@ -68,6 +68,8 @@ def load(path: str | None = None):
         lib.kda_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, vp]
         lib.kda_prefill_gate.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.kda_prefill_gate.restype = i
+        lib.kda_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.kda_prefill_fp8.restype = i
         lib.kda_varlen_prefill_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, vp, i, i, i, i, i,
                                                  vp, ctypes.c_size_t, vp, vp]
         lib.kda_varlen_prefill_slots.restype = i
@@ -397,3 +399,35 @@ def decode_step_slots(q, k, v, alpha, beta, state_pool, slots, *, gate: str = "c
                                    N, H, dk, dv, _ptr(device_status), _stream(stream))
     _check(lib, st)
     return out
+
+
+def prefill_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, initial_state=None, *, gate: str = "channel",
+                output_final_state: bool = True, out=None, final_state=None, stream=None):
+    """``prefill`` on FP8 inputs in the MX block format: q, k, v are uint8
+    E4M3 codes [B, T, H, 128], each 32 channels of a token-head sharing one
+    E8M0 scale byte (q_scale, k_scale, v_scale: uint8 [B, T, H, 4]). The result
+    equals ``prefill`` on bf16 inputs holding the dequantised values; o is bf16.
+    """
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.uint8, dev)
+    _need(beta, "beta", torch.float32, dev)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H) \
+            or q_scale.shape != (B, T, H, dk // 32) or k_scale.shape != (B, T, H, dk // 32) \
+            or v_scale.shape != (B, T, H, dv // 32):
+        raise ValueError("shape mismatch among q, k, v, the scales and beta")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, dev)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    st = lib.kda_prefill_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), _ptr(alpha),
+                             GATES[gate], _ptr(beta), _ptr(initial_state), _ptr(out), _ptr(final_state),
+                             B, T, H, dk, dv, _stream(stream))
+    _check(lib, st)
+    return out, final_state

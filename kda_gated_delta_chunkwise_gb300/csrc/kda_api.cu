@@ -147,6 +147,38 @@ kda_status_t kda_prefill_gate(const void *q, const void *k, const void *v, kda_d
     return run_prefill(a, algo, reinterpret_cast<cudaStream_t>(stream));
 }
 
+kda_status_t kda_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, const uint8_t *q_scale,
+                             const uint8_t *k_scale, const uint8_t *v_scale, const float *alpha,
+                             kda_gate_t gate, const float *beta, const float *initial_state, void *o,
+                             float *final_state, int B, int T, int H, int d_k, int d_v, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_gate(gate)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (d_k != 128 || d_v != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "FP8 inputs need d_k = d_v = 128 (the tensor-core kernel)");
+    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
+    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state, (int64_t)B * T > 0, gate)) !=
+        KDA_OK)
+        return st;
+    if ((int64_t)B * T > 0) {
+        if (!q_scale || !k_scale || !v_scale) return fail(KDA_ERR_INVALID_ARG, "q_scale, k_scale, v_scale must not be NULL");
+        if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+             reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+            return fail(KDA_ERR_INVALID_ARG, "the scale arrays must be 4-byte aligned");
+    }
+    if (B == 0) return ok();
+    if (T == 0 && !final_state) return ok();
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = initial_state;
+    a.o = o; a.sT = final_state; a.cu_seqlens = nullptr;
+    a.gate = gate; a.slots = nullptr;
+    a.fp8 = true; a.qs = q_scale; a.ks = k_scale; a.vs = v_scale;
+    a.N = B; a.T = T; a.H = H; a.dk = d_k; a.dv = d_v; a.dt = KDA_BF16;
+    a.order = nullptr; a.counter = nullptr; a.dev_status = nullptr;
+    return cuda_status(kda::launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream)), "FP8 prefill launch");
+}
+
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
                             const float *alpha, const float *beta, const float *initial_state,
                             void *o, float *final_state, int B, int T, int H, int d_k, int d_v,

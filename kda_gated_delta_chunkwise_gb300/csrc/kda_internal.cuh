@@ -54,6 +54,8 @@ struct PrefillArgs {
     float *sT;
     int gate;                   // kda_gate_t: the layout of alpha
     const int32_t *slots;       // nullable: state slot map (see slot_of); s0 and sT are then the pool
+    bool fp8;                   // q, k, v are E4M3 codes with E8M0 scales qs, ks, vs (o is bf16)
+    const uint8_t *qs, *ks, *vs;
     const int32_t *cu_seqlens;  // null: equal lengths
     int N, T, H, dk, dv;        // T: tokens per sequence (equal) or T_total (packed)
     kda_dtype_t dt;

@@ -46,7 +46,10 @@
 // control 104. The groups work on consecutive chunks at once. All waits are
 // bounded; a CTA whose wait times out records an error and winds down.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "kda_internal.cuh"
 #include "kda_tc_ptx.cuh"
@@ -144,8 +147,31 @@ struct TcParams {
     int32_t *err;
     const int32_t *slots;  // nullable: state slot map (s0 and sT are then the pool)
     int gate;              // kda_gate_t
+    const uint8_t *qs, *ks, *vs;  // FP8 inputs: E8M0 scales, one per 32 channels (q, k, v are E4M3)
     int N, T, H;
 };
+
+// FP8 inputs (the MX block format): E4M3 codes, a power-of-two scale 2^(t-127)
+// per 32 channels. Four codes -> four floats, scaled (exact: the scale is a
+// power of two and the dequantised value fits fp32).
+__device__ __forceinline__ float e8m0(uint8_t t) { return __uint_as_float((uint32_t)t << 23); }
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float sc, float (&f)[4]) {
+    uint32_t h01, h23;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(w & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(w >> 16)));
+    const __half2 a = *reinterpret_cast<const __half2 *>(&h01), c = *reinterpret_cast<const __half2 *>(&h23);
+    f[0] = __low2float(a) * sc;
+    f[1] = __high2float(a) * sc;
+    f[2] = __low2float(c) * sc;
+    f[3] = __high2float(c) * sc;
+}
+// One FP8 input element (token-head th, channel c of a d-channel row).
+__device__ __forceinline__ float fp8_at(const uint8_t *x, const uint8_t *sc, int64_t th, int c, int d) {
+    const uint32_t w = x[th * d + c];
+    float f[4];
+    e4m3x4_to_f32(w, e8m0(sc[th * (d / 32) + c / 32]), f);
+    return f[0];
+}
 
 __device__ int g_tc_error = 0;
 
@@ -288,8 +314,10 @@ __device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
 // shared memory. Rare, so it is written for size rather than speed, and out
 // of line: the hot loop of the epilogue stays contiguous in the instruction
 // caches.
-__device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gate, const __nv_bfloat16 *__restrict__ kin,
-                                        const __nv_bfloat16 *__restrict__ qin, const __nv_bfloat16 *__restrict__ vin,
+__device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gate, const void *__restrict__ kin,
+                                        const void *__restrict__ qin, const void *__restrict__ vin,
+                                        const uint8_t *__restrict__ ks, const uint8_t *__restrict__ qs,
+                                        const uint8_t *__restrict__ vs,
                                         const float *__restrict__ beta, __nv_bfloat16 *__restrict__ o, float *red,
                                         uint32_t tm_d, int l, int warp, int lane, int64_t tok0, int L, int H, int h,
                                         int v0) {
@@ -299,8 +327,11 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gat
     for (int r = 0; r < L; ++r) {
         const int64_t tk = (tok0 + r) * H + h;
         const float a = gate_at(alpha, gate, tk, l, DK);
-        const float kf = __bfloat162float(kin[tk * DK + l]);
-        const float qf = __bfloat162float(qin[tk * DK + l]);
+        // (FP8 inputs when scales are given, else bf16)
+        const float kf = ks ? fp8_at((const uint8_t *)kin, ks, tk, l, DK)
+                            : __bfloat162float(((const __nv_bfloat16 *)kin)[tk * DK + l]);
+        const float qf = qs ? fp8_at((const uint8_t *)qin, qs, tk, l, DK)
+                            : __bfloat162float(((const __nv_bfloat16 *)qin)[tk * DK + l]);
         // S' = Diag(alpha) S, and this warp's part of S'^T k
 #pragma unroll 1
         for (int g = 0; g < 8; ++g) {
@@ -322,7 +353,9 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gat
         named_bar(2, EPI_THREADS);
         if (l < 64) {
             const float vh = red[l] + red[64 + l] + red[128 + l] + red[192 + l];
-            red[256 + l] = beta[tk] * (__bfloat162float(vin[tk * DV + v0 + l]) - vh);
+            const float vf = vs ? fp8_at((const uint8_t *)vin, vs, tk, v0 + l, DV)
+                                : __bfloat162float(((const __nv_bfloat16 *)vin)[tk * DV + v0 + l]);
+            red[256 + l] = beta[tk] * (vf - vh);
         }
         named_bar(2, EPI_THREADS);
         // S = S' + k e^T, and this warp's part of S^T q
@@ -351,8 +384,10 @@ __device__ __noinline__ void slow_chunk(const float *__restrict__ alpha, int gat
 
 // --------------------------------------------------------------------------
 // GATE (a kda_gate_t) is a template parameter so that each gate kind keeps
-// the per-chunk code of the gate group as small as the per-channel one.
-template <int GATE>
+// the per-chunk code of the gate group as small as the per-channel one; FP8
+// selects E4M3 q, k, v with block scales (TMA brings the codes, the gate and
+// E1 dequantise them).
+template <int GATE, bool FP8>
 __global__ void __cluster_dims__(NSLICE, 1, 1) __launch_bounds__(NTHREADS, 1)
 kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_v) {
@@ -455,9 +490,15 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // this CTA's key half of k and q (raw; the gate transforms them in place)
                 if (n >= NSLOT && !wait_bar(s, p, B_QK_EMPTY + b, (kk - 1) & 1)) break;
                 unsigned char *a0 = s.base + SM_A0 + b * 32768 + rank * 16384;
-                mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 16384);
-                tma_load_3d(a0, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
-                tma_load_3d(a0 + 8192, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
+                if constexpr (FP8) {  // codes into the Qr half (64-byte rows); the gate reads them first
+                    mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 8192);
+                    tma_load_3d(a0 + 8192, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
+                    tma_load_3d(a0 + 12288, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
+                } else {
+                    mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 16384);
+                    tma_load_3d(a0, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
+                    tma_load_3d(a0 + 8192, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
+                }
                 nqk = n + 1;
             }
             // never leave copies in flight: wait (bounded) for the last ones
@@ -566,7 +607,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         // The v slice is single-buffered and refilled by this group as soon
         // as E1 has read it (thread 0 issues the copy).
         if (tid == 0) {
-            mbar_arrive_expect_tx(s.bar(B_V_FULL), 8192);
+            mbar_arrive_expect_tx(s.bar(B_V_FULL), FP8 ? 4096 : 8192);
             tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)t_begin);
         }
         const uint32_t tm_d = tmem + lane_off + TM_D;
@@ -657,19 +698,38 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         uint4 vrow[4];  // the v row first: no load waits behind an R store
+                        float vsc = 1.f;
+                        if constexpr (FP8) {  // 32 E4M3 codes: 64-byte rows, no swizzle
+                            vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf);
+                            vrow[1] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf + 16);
+                            if (l < L) vsc = e8m0(p.vs[((tok0 + l) * H + h) * (DV / 32) + v0 / 32 + hf]);
+                        } else {
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4)
-                            vrow[c4] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 4 * hf + c4));
+                            for (int c4 = 0; c4 < 4; ++c4)
+                                vrow[c4] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 4 * hf + c4));
+                        }
                         tmem_ld32(tmem + lane_off + TM_XY + 64 * b + 32 * hf, r32);
                         tmem_wait_ld();
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
-                            const uint32_t vw[4] = {vrow[c4].x, vrow[c4].y, vrow[c4].z, vrow[c4].w};
+                            uint64_t vp[4];  // 8 values of v as 4 fp32 pairs
+                            if constexpr (FP8) {
+                                const uint4 w = vrow[c4 >> 1];
+                                float f[8];
+                                e4m3x4_to_f32((c4 & 1) ? w.z : w.x, vsc, *reinterpret_cast<float (*)[4]>(f));
+                                e4m3x4_to_f32((c4 & 1) ? w.w : w.y, vsc, *reinterpret_cast<float (*)[4]>(f + 4));
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) vp[e] = f2_make(f[2 * e], f[2 * e + 1]);
+                            } else {
+                                const uint32_t vw[4] = {vrow[c4].x, vrow[c4].y, vrow[c4].z, vrow[c4].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) vp[e] = bf2_to_f2(vw[e]);
+                            }
                             uint32_t ow[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const uint64_t x2 = (uint64_t)r32[8 * c4 + 2 * e] | ((uint64_t)r32[8 * c4 + 2 * e + 1] << 32);
-                                ow[e] = f2_to_bf2(f2_mul(f2_sub(bf2_to_f2(vw[e]), x2), bt2));
+                                ow[e] = f2_to_bf2(f2_mul(f2_sub(vp[e], x2), bt2));
                             }
                             *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -681,7 +741,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 mbar_arrive(s.bar(B_R_FULL));
                 named_bar(4, 64);  // both E1 warps have read v: load the next chunk's
                 if (tid == 0 && n + 1 < NC) {
-                    mbar_arrive_expect_tx(s.bar(B_V_FULL), 8192);
+                    mbar_arrive_expect_tx(s.bar(B_V_FULL), FP8 ? 4096 : 8192);
                     tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)(tok0 + C));
                 }
                 // E2: U -> bf16 operand (replaces R, which MMA2 has consumed)
@@ -725,7 +785,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // one decision for the whole group: the slow path has group barriers
                 go = !named_bar_or(2, EPI_THREADS, !go);
                 if (go)
-                    slow_chunk(p.alpha, p.gate, p.k, p.q, p.v, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d,
+                    slow_chunk(p.alpha, p.gate, p.k, p.q, p.v, FP8 ? p.ks : nullptr, FP8 ? p.qs : nullptr,
+                               FP8 ? p.vs : nullptr, p.beta, p.o, reinterpret_cast<float *>(s.base + SM_RED), tm_d,
                                l, warp, lane, tok0, L, H, h, v0);
             }
             unsigned char *st = s.base + SM_ST;
@@ -858,6 +919,21 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (n >= NSLOT) ok = ok && wait_bar(s, p, B_B0_EMPTY + b3, (kk - 1) & 1);
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
             unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
+            // FP8: this thread's codes of k and q (4 channels of each of its 8
+            // rows) leave the staging area in the Qr half before any Qr row is
+            // written there
+            uint32_t k8[8], q8[8];
+            if constexpr (FP8) {
+                if (ok && !slow) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t o8 = (uint32_t)(8 * rg + j) * 64u + 4u * (uint32_t)cq;
+                        k8[j] = *reinterpret_cast<const uint32_t *>(ah + 8192 + o8);
+                        q8[j] = *reinterpret_cast<const uint32_t *>(ah + 12288 + o8);
+                    }
+                }
+                named_bar(1, GATE_THREADS);
+            }
             if (ok && !slow) {
                 // One pass over the rows with the running product p_r:
                 // Kr = k p / mu and Qr = q p / mu in place, Kc = k mu / p (the
@@ -870,18 +946,31 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
                     const bool in = 8 * rg + j < L;
-                    const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
-                    const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
+                    uint64_t k01, k23, q01, q23;
+                    if constexpr (FP8) {
+                        float kf[4] = {0.f, 0.f, 0.f, 0.f}, qf[4] = {0.f, 0.f, 0.f, 0.f};
+                        if (in) {
+                            const int64_t sidx = ((tok0 + 8 * rg + j) * H + h) * (DK / 32) + (c0 + 4 * cq) / 32;
+                            e4m3x4_to_f32(k8[j], e8m0(p.ks[sidx]), kf);
+                            e4m3x4_to_f32(q8[j], e8m0(p.qs[sidx]), qf);
+                        }
+                        k01 = f2_make(kf[0], kf[1]); k23 = f2_make(kf[2], kf[3]);
+                        q01 = f2_make(qf[0], qf[1]); q23 = f2_make(qf[2], qf[3]);
+                    } else {
+                        const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
+                        const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
+                        k01 = bf2_to_f2(kw.x); k23 = bf2_to_f2(kw.y);
+                        q01 = bf2_to_f2(qw.x); q23 = bf2_to_f2(qw.y);
+                    }
                     pr01 = f2_mul(pr01, f2_make(arow[j].x, arow[j].y));
                     pr23 = f2_mul(pr23, f2_make(arow[j].z, arow[j].w));
                     const uint64_t e01 = f2_mul(pr01, inv01), e23 = f2_mul(pr23, inv23);
                     const uint64_t c01 = f2_mul(f2_make(rcp_approx(f2_lo(pr01)), rcp_approx(f2_hi(pr01))), mu01);
                     const uint64_t c23 = f2_mul(f2_make(rcp_approx(f2_lo(pr23)), rcp_approx(f2_hi(pr23))), mu23);
-                    const uint64_t k01 = bf2_to_f2(kw.x), k23 = bf2_to_f2(kw.y);
                     *reinterpret_cast<uint2 *>(ah + off) =
                         make_uint2(f2_to_bf2(f2_mul(k01, e01)), f2_to_bf2(f2_mul(k23, e23)));
                     *reinterpret_cast<uint2 *>(ah + 8192 + off) =
-                        make_uint2(f2_to_bf2(f2_mul(bf2_to_f2(qw.x), e01)), f2_to_bf2(f2_mul(bf2_to_f2(qw.y), e23)));
+                        make_uint2(f2_to_bf2(f2_mul(q01, e01)), f2_to_bf2(f2_mul(q23, e23)));
                     *reinterpret_cast<uint2 *>(kch + off) =
                         make_uint2(f2_to_bf2(f2_mul(k01, c01)), f2_to_bf2(f2_mul(k23, c23)));
                 }
@@ -1204,7 +1293,7 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ptr
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs &a) {
-    return a.dt == KDA_BF16 && a.dk == DK && a.dv == DV;
+    return (a.dt == KDA_BF16 || a.fp8) && a.dk == DK && a.dv == DV;
 }
 
 cudaError_t read_device_error(int *out, bool reset) {
@@ -1227,9 +1316,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     CUtensorMap mk, mq, mv;
     // A map needs a non-empty extent; an empty token range never issues a copy.
     const int64_t ext = tokens > 0 ? tokens : 1;
-    if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, DK, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, DV, a.H, ext, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    // bf16: 128-byte rows with the 128B swizzle the tensor core reads; FP8
+    // codes: 64-byte rows, unswizzled (the gate and E1 dequantise them)
+    const CUtensorMapDataType et = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int es = a.fp8 ? 1 : 2;
+    const CUtensorMapSwizzle sw = a.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map(&mk, et, es, a.k, DK, a.H, ext, 64, sw) || !make_map(&mq, et, es, a.q, DK, a.H, ext, 64, sw) ||
+        !make_map(&mv, et, es, a.v, DV, a.H, ext, 64, sw))
         return cudaErrorInvalidValue;
     TcParams p;
     p.q = (const __nv_bfloat16 *)a.q;
@@ -1246,12 +1339,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     p.err = nullptr;
     p.slots = a.slots;
     p.gate = a.gate;
+    p.qs = a.qs;
+    p.ks = a.ks;
+    p.vs = a.vs;
     p.N = a.N;
     p.T = a.T;
     p.H = a.H;
-    auto kern = a.gate == KDA_GATE_SCALAR ? kda_prefill_tc_kernel<KDA_GATE_SCALAR>
-                : a.gate == KDA_GATE_NONE ? kda_prefill_tc_kernel<KDA_GATE_NONE>
-                                          : kda_prefill_tc_kernel<KDA_GATE_CHANNEL>;
+    auto pick = [&](auto fp8) {
+        constexpr bool F = decltype(fp8)::value;
+        return a.gate == KDA_GATE_SCALAR ? kda_prefill_tc_kernel<KDA_GATE_SCALAR, F>
+               : a.gate == KDA_GATE_NONE ? kda_prefill_tc_kernel<KDA_GATE_NONE, F>
+                                         : kda_prefill_tc_kernel<KDA_GATE_CHANNEL, F>;
+    };
+    auto kern = a.fp8 ? pick(std::true_type{}) : pick(std::false_type{});
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // blocks is even: one cluster of NSLICE CTAs per (sequence, head)

@@ -26,6 +26,10 @@ Workloads (sizes as used by the tests and the benchmark):
 * ``varlen_64seq``:      64 packed sequences, lengths
   round(lognormal(8, 1)) clipped to [512, 32768] (306,055 tokens at seed 0),
   H=16, d=128, bf16, scale 0.1, per-sequence S0 ~ N(0, 0.01^2)
+
+``to_mxfp8`` quantises a tensor to FP8 E4M3 with one power-of-two scale per
+32 consecutive elements of the last axis (the MX block format) for the FP8
+input path; the kernels and the oracle then see the same dequantised values.
 """
 from __future__ import annotations
 
@@ -173,3 +177,27 @@ def varlen_64seq(seed=0, n_seqs=64, H=16, rescale_to=None) -> Inputs:
         L = np.clip(np.rint(L * (rescale_to / L.sum())), 512, 32768).astype(np.int64)
     return packed(L, H, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.01, rng=rng,
                   name=f"varlen_{n_seqs}seq")
+
+
+MX_BLOCK = 32
+
+
+def to_mxfp8(x: torch.Tensor):
+    """FP8 E4M3 codes and E8M0 block scales of ``x`` (last axis in blocks of
+    32): scale 2^e with e = ceil(log2(amax / 448)) per block, so no code
+    saturates; codes round to nearest even. Returns ``(codes uint8, scales
+    uint8 [..., d/32], values float32)`` where ``values`` are the exact
+    dequantised numbers (code value x 2^e) both sides consume."""
+    xf = x.float()
+    d = xf.shape[-1]
+    if d % MX_BLOCK:
+        raise ValueError("the last axis must be a multiple of 32")
+    blocks = xf.reshape(*xf.shape[:-1], d // MX_BLOCK, MX_BLOCK)
+    amax = blocks.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.ceil(torch.log2(amax / 448.0)), torch.zeros_like(amax))
+    e = e.clamp(-126, 127)
+    scaled = blocks / torch.exp2(e)[..., None]
+    codes = scaled.to(torch.float8_e4m3fn)
+    values = (codes.float() * torch.exp2(e)[..., None]).reshape(xf.shape)
+    scales = (e + 127).to(torch.uint8)
+    return codes.view(torch.uint8).reshape(xf.shape).contiguous(), scales.contiguous(), values.contiguous()

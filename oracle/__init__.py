@@ -149,6 +149,27 @@ def expand_gate(alpha, gate: str, lead: tuple, dk: int) -> np.ndarray:
     raise ValueError(f"unknown gate {gate!r}")
 
 
+def dequant_mxfp8(codes, scales, block: int = 32) -> np.ndarray:
+    """FP8 E4M3 codes with E8M0 block scales (one per ``block`` consecutive
+    elements of the last axis) -> float64 values, decoded from the bit fields:
+    sign s, exponent e (4 bits, bias 7), mantissa m (3 bits); e = 0 is
+    subnormal, m * 2^-9; otherwise (1 + m/8) * 2^(e-7); 0x7F / 0xFF are NaN.
+    The scale byte t stands for 2^(t - 127). (Input preparation for the FP8
+    path: the recurrence itself is :func:`run`.)"""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    t = np.asarray(scales, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    val = sign * mag
+    d = val.shape[-1]
+    if d % block or t.shape[-1] != d // block:
+        raise ValueError("scales must hold one byte per block of the last axis")
+    return val * np.repeat(np.exp2(t - 127.0), block, axis=-1)
+
+
 def max_threads(nthreads: int = 0) -> int:
     """Threads the oracle's OpenMP loop will use."""
     return int(load().kda_oracle_max_threads(int(nthreads)))

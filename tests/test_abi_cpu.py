@@ -146,3 +146,15 @@ def test_gate_and_slot_argument_checks(lib):
     assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 0, p, 3, 2, 128, 128, None, None) == 1
     assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 4, p, 3, 2, 128, 128, odd, None) == 1
     assert lib.kda_decode_step_slots(p, p, p, 1, p, 0, p, p, p, 4, p, 0, 2, 128, 128, None, None) == 0
+
+
+def test_fp8_argument_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    # scales required, d = 128 only, gate checked
+    assert lib.kda_prefill_fp8(p, p, p, None, p, p, p, 0, p, None, p, None, 1, 8, 2, 128, 128, None) == 1
+    assert lib.kda_prefill_fp8(p, p, p, p, p, p, p, 0, p, None, p, None, 1, 8, 2, 64, 64, None) == 2
+    assert lib.kda_prefill_fp8(p, p, p, p, p, p, p, 5, p, None, p, None, 1, 8, 2, 128, 128, None) == 1
+    assert lib.kda_prefill_fp8(p, p, p, ctypes.c_void_p(0x1001), p, p, p, 0, p, None, p, None, 1, 8, 2, 128, 128,
+                               None) == 1
+    assert lib.kda_prefill_fp8(None, None, None, None, None, None, None, 0, None, None, None, None, 0, 8, 2, 128,
+                               128, None) == 0

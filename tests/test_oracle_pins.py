@@ -297,3 +297,30 @@ def test_expand_gate_rejects_wrong_shapes():
         oracle.expand_gate(np.ones((2, 3, 4)), "channel", (2, 3), 5)
     with pytest.raises(ValueError):
         oracle.expand_gate(None, "sigmoid", (1,), 2)
+
+
+def test_mxfp8_decoding_fixed_codes():
+    """E4M3 code points fixed by the format: 0x38 = 1, 0x40 = 2, 0x7E = 448
+    (largest), 0x01 = 2^-9 (smallest subnormal), 0x08 = 2^-6 (smallest
+    normal), 0xB8 = -1; 0x7F is NaN; a scale byte t multiplies by 2^(t-127)."""
+    codes = np.array([[0x38, 0x40, 0x7E, 0x01, 0x08, 0xB8, 0x00, 0x3C] * 4], dtype=np.uint8)
+    v = oracle.dequant_mxfp8(codes, np.array([[127]], dtype=np.uint8))
+    np.testing.assert_array_equal(v[0, :8], [1.0, 2.0, 448.0, 2.0 ** -9, 2.0 ** -6, -1.0, 0.0, 1.5])
+    v2 = oracle.dequant_mxfp8(codes, np.array([[130]], dtype=np.uint8))
+    np.testing.assert_array_equal(v2, v * 8.0)
+    assert np.isnan(oracle.dequant_mxfp8(np.full((1, 32), 0x7F, np.uint8), np.array([[127]], np.uint8))).all()
+
+
+def test_mxfp8_round_trip_of_the_input_generator():
+    """The inputs' quantiser and the oracle's decoder agree on every element:
+    the dequantised values the generator hands to the kernels are exactly
+    the oracle's decoding of its codes and scales, and within half an E4M3
+    step of the original numbers."""
+    from kda_gated_delta_chunkwise_gb300 import workloads as W
+    import torch
+    x = torch.randn(7, 3, 128, generator=torch.Generator().manual_seed(5)) * 3.0
+    codes, scales, values = W.to_mxfp8(x)
+    dec = oracle.dequant_mxfp8(codes.numpy(), scales.numpy())
+    np.testing.assert_array_equal(dec, values.double().numpy())
+    blk = np.repeat(np.exp2(scales.numpy().astype(np.float64) - 127.0), 32, axis=-1)
+    assert np.all(np.abs(dec - x.double().numpy()) <= 2.0 ** -4 * np.maximum(np.abs(x.double().numpy()), 2.0 ** -6 * blk) + 1e-300)
