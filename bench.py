@@ -357,6 +357,29 @@ def main():
                               "ms_per_step": vms, "algorithmic_bytes_per_launch": vbytes,
                               "achieved_gbs": vbytes / (vms / 1e3) / 1e9,
                               "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        # FP8 inputs (MX block format: E4M3 codes, one scale byte per 32 channels)
+        cq, sq, _ = W.to_mxfp8(q)
+        ck, sk, _ = W.to_mxfp8(k)
+        cv, sv, _ = W.to_mxfp8(v)
+        for _ in range(args.warmup):
+            kda.prefill_fp8(cq, ck, cv, sq, sk, sv, a, b, None, out=o, final_state=sT)
+        torch.cuda.synchronize()
+        evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            evf[i][0].record(stream)
+            kda.prefill_fp8(cq, ck, cv, sq, sk, sv, a, b, None, out=o, final_state=sT)
+            evf[i][1].record(stream)
+        torch.cuda.synchronize()
+        fms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in evf)
+        # q, k, v: one byte per element instead of two, plus a scale byte per 32
+        fbytes = prefill_bytes(B, T, H, DK, DV) - B * T * H * (2 * DK + DV) + B * T * H * (2 * DK + DV) // 32
+        variants["fp8_inputs"] = {"inputs": "E4M3 q, k, v with E8M0 scales per 32 channels; bf16 o",
+                                  "value": B * T / (fms / 1e3), "unit": "tokens/s", "ms_per_step": fms,
+                                  "algorithmic_bytes_per_launch": fbytes,
+                                  "achieved_gbs": fbytes / (fms / 1e3) / 1e9,
+                                  "frac": fbytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        del cq, ck, cv, sq, sk, sv
 
     # ---- decode step (secondary figure of the metric) ----
     decode = None
