@@ -42,6 +42,10 @@
 //                    refills v itself; the gate reads alpha into registers)
 //   warp 13          MMA issuer of the state chain (one thread), TMEM owner
 //   warp 14          MMA issuer of [A; P] on this CTA's parity; warp 15 idle
+// FP8 inputs (E4M3 codes, one power-of-two scale per 32 channels): the TMA
+// warp loads the codes into the Qr half of the slot, the gate dequantises k
+// and q while it builds the tables, E1 dequantises v; everything after that
+// is the bf16 path.
 // Register budgets per warpgroup (setmaxnreg): epilogue 152, warps 4-11 128,
 // control 104. The groups work on consecutive chunks at once. All waits are
 // bounded; a CTA whose wait times out records an error and winds down.
