@@ -690,6 +690,14 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             ok = ok && s.flags()[1] == 0;  // stop waiting once the CTA gave up
             if (warp < 2) {
                 // E1: R = beta (V - X) for token rows 0-63
+                float vsc2[2] = {1.f, 1.f};  // FP8: this row's two block scales, loaded before the waits
+                if constexpr (FP8) {
+                    if (l < L) {
+                        const uint8_t *vsr = p.vs + ((tok0 + l) * H + h) * (DV / 32) + v0 / 32;
+                        vsc2[0] = e8m0(__ldg(vsr));
+                        vsc2[1] = e8m0(__ldg(vsr + 1));
+                    }
+                }
                 ok = ok && wait_bar(s, p, B_XY_FULL, n & 1);
                 ok = ok && wait_bar(s, p, B_V_FULL, n & 1);
                 tc_fence_after();
@@ -702,11 +710,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         uint4 vrow[4];  // the v row first: no load waits behind an R store
-                        float vsc = 1.f;
+                        const float vsc = hf ? vsc2[1] : vsc2[0];
                         if constexpr (FP8) {  // 32 E4M3 codes: 64-byte rows, no swizzle
                             vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf);
                             vrow[1] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf + 16);
-                            if (l < L) vsc = e8m0(p.vs[((tok0 + l) * H + h) * (DV / 32) + v0 / 32 + hf]);
                         } else {
 #pragma unroll
                             for (int c4 = 0; c4 < 4; ++c4)
@@ -868,6 +875,18 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // beta and alpha of this chunk, loaded before the waits so their
             // latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
+            // FP8: the block scales of this thread's k and q rows, packed four
+            // to a register (loaded here so their latency passes in the waits)
+            uint32_t ksc[2] = {0u, 0u}, qsc[2] = {0u, 0u};
+            if constexpr (FP8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (8 * rg + j < L) {
+                        const int64_t sidx = ((tok0 + 8 * rg + j) * H + h) * (DK / 32) + (c0 + 4 * cq) / 32;
+                        ksc[j >> 2] |= (uint32_t)__ldg(p.ks + sidx) << (8 * (j & 3));
+                        qsc[j >> 2] |= (uint32_t)__ldg(p.qs + sidx) << (8 * (j & 3));
+                    }
+            }
             float4 arow[8];
             {
                 const float *src = alpha_src(n);
@@ -954,9 +973,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     if constexpr (FP8) {
                         float kf[4] = {0.f, 0.f, 0.f, 0.f}, qf[4] = {0.f, 0.f, 0.f, 0.f};
                         if (in) {
-                            const int64_t sidx = ((tok0 + 8 * rg + j) * H + h) * (DK / 32) + (c0 + 4 * cq) / 32;
-                            e4m3x4_to_f32(k8[j], e8m0(p.ks[sidx]), kf);
-                            e4m3x4_to_f32(q8[j], e8m0(p.qs[sidx]), qf);
+                            e4m3x4_to_f32(k8[j], e8m0((uint8_t)(ksc[j >> 2] >> (8 * (j & 3)))), kf);
+                            e4m3x4_to_f32(q8[j], e8m0((uint8_t)(qsc[j >> 2] >> (8 * (j & 3)))), qf);
                         }
                         k01 = f2_make(kf[0], kf[1]); k23 = f2_make(kf[2], kf[3]);
                         q01 = f2_make(qf[0], qf[1]); q23 = f2_make(qf[2], qf[3]);
