@@ -196,6 +196,14 @@ def cpu_baseline_oracle(target_s: float = 12.0):
                       f"d={DK}, float64, {dt:.1f} s"}
 
 
+def bench_config(world: int) -> dict:
+    """The workload description both arms report."""
+    return {"workload": f"kda_prefill B={B} H={H} T={T} d_k={DK} d_v={DV} chunk={CHUNK}",
+            "inputs": "bf16 q/k/v (q, k L2-normalised), fp32 alpha/beta, fp32 state, S0 = 0",
+            "l2": "inputs larger than L2 (0.34 GB in, 0.41 GB moved per step; L2 129 MB)",
+            "parallelism": f"{world} independent replica(s)"}
+
+
 def run_reference(args):
     """The reference arm: the float64 oracle on the host cores (rank 0 only)."""
     _, rank, _ = rank_env()
@@ -220,8 +228,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"kda_prefill B={B} H={H} T={T} d_k={DK} d_v={DV} bf16 inputs",
-                       "sample": f"each step: all 64 sequence-head pairs, first {Ts} tokens"},
+            "config": dict(bench_config(args.gpus), sample=f"each step: all 64 sequence-head pairs, first {Ts} tokens"),
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"B={B} x H={H} x first {Ts} tokens per step"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -417,10 +424,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": f"kda_prefill B={B} H={H} T={T} d_k={DK} d_v={DV} chunk={CHUNK}",
-                           "inputs": "bf16 q/k/v (q, k L2-normalised), fp32 alpha/beta, fp32 state, S0 = 0",
-                           "l2": "inputs larger than L2 (0.34 GB in, 0.41 GB moved per step; L2 129 MB)",
-                           "parallelism": f"{world} independent replica(s)"},
+                "config": bench_config(world),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
                 "gate_variants": variants,
                 "gpu_launches": args.steps, "clocks": clk}
