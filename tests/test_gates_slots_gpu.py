@@ -207,3 +207,47 @@ def test_serving_loop_prefill_then_decode(kda):
     tol = tol_for(torch.bfloat16)
     assert_close("o", o_all, ro[0], tol)
     assert_close("state", pool[1], rs[0], tol)
+
+
+def test_slots_identity_map_is_the_packed_prefill_bit_for_bit(kda):
+    """The 64-sequence packed workload through the slot entry point with slot
+    n for sequence n (the pool holding the initial states) gives the bits of
+    kda_varlen_prefill."""
+    x = W.varlen_64seq()
+    q, k, v, a, b = (t.to(DEV) for t in x.tensors())
+    cu = x.cu_seqlens.to(DEV)
+    s0 = x.initial_state.to(DEV)
+    o_ref, s_ref = kda.varlen_prefill(q, k, v, a, b, cu, s0)
+    pool = s0.clone()
+    slots = torch.arange(x.num_seqs, dtype=torch.int32, device=DEV)
+    status = torch.full((1,), -7, dtype=torch.int32, device=DEV)
+    o = kda.varlen_prefill_slots(q, k, v, a, b, cu, pool, slots, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kda.KDA_DEV_OK
+    assert torch.equal(o, o_ref)
+    assert torch.equal(pool, s_ref)
+
+
+def test_long_prompt_prefilled_in_pieces(kda):
+    """The 131,072-token workload (32 heads) prefilled through a slot in four
+    pieces equals one prefill of the whole sequence to rounding (the state
+    carries everything between the pieces)."""
+    x = W.prefill_long_131k()
+    q, k, v, a, b = (t.to(DEV) for t in x.tensors())
+    s0 = x.initial_state.to(DEV)
+    o_ref, s_ref = kda.prefill(q, k, v, a, b, s0)
+    pool = torch.zeros(2, 32, 128, 128, device=DEV)
+    pool[1] = s0[0]
+    T = q.shape[1]
+    outs = []
+    for lo in range(0, T, T // 4):
+        hi = lo + T // 4
+        cu = torch.tensor([0, hi - lo], dtype=torch.int32, device=DEV)
+        outs.append(kda.varlen_prefill_slots(q[0, lo:hi].contiguous(), k[0, lo:hi].contiguous(),
+                                             v[0, lo:hi].contiguous(), a[0, lo:hi].contiguous(),
+                                             b[0, lo:hi].contiguous(), cu, pool,
+                                             torch.tensor([1], dtype=torch.int32, device=DEV)))
+    o = torch.cat(outs)[None]
+    tol = tol_for(torch.bfloat16)
+    assert_close("o", o, o_ref, tol)
+    assert_close("state", pool[1:2], s_ref, tol)
