@@ -117,7 +117,8 @@ constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
 constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
 constexpr uint32_t SM_MSCR = 225232;   // float[4][16*8]: mma.sync staging (3 KB reserved)
 constexpr uint32_t SM_SCAN = 228304;   // float4[8][16]: per-group gate products
-constexpr uint32_t SM_TOTAL = 230352;
+constexpr uint32_t SM_FSC = 230352;    // uint32[2][64]: FP8 block scales of the chunk's k and q rows
+constexpr uint32_t SM_TOTAL = 230864;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 
 // Bytes one CTA pushes into its peer per chunk: its [Kr; Qr] half, its Kc
@@ -693,9 +694,9 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 float vsc2[2] = {1.f, 1.f};  // FP8: this row's two block scales, loaded before the waits
                 if constexpr (FP8) {
                     if (l < L) {
-                        const uint8_t *vsr = p.vs + ((tok0 + l) * H + h) * (DV / 32) + v0 / 32;
-                        vsc2[0] = e8m0(__ldg(vsr));
-                        vsc2[1] = e8m0(__ldg(vsr + 1));
+                        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(p.vs) + (tok0 + l) * H + h);
+                        vsc2[0] = e8m0((uint8_t)(w >> (8 * (v0 / 32))));
+                        vsc2[1] = e8m0((uint8_t)(w >> (8 * (v0 / 32 + 1))));
                     }
                 }
                 ok = ok && wait_bar(s, p, B_XY_FULL, n & 1);
@@ -711,9 +712,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     for (int hf = 0; hf < 2; ++hf) {
                         uint4 vrow[4];  // the v row first: no load waits behind an R store
                         const float vsc = hf ? vsc2[1] : vsc2[0];
-                        if constexpr (FP8) {  // 32 E4M3 codes: 64-byte rows, no swizzle
-                            vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf);
-                            vrow[1] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 32 * hf + 16);
+                        if constexpr (FP8) {  // 32 E4M3 codes: 64-byte rows, 64B swizzle
+                            const int sw = (l >> 1) & 3;
+                            vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 16 * ((2 * hf) ^ sw));
+                            vrow[1] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 16 * ((2 * hf + 1) ^ sw));
                         } else {
 #pragma unroll
                             for (int c4 = 0; c4 < 4; ++c4)
@@ -875,17 +877,15 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // beta and alpha of this chunk, loaded before the waits so their
             // latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
-            // FP8: the block scales of this thread's k and q rows, packed four
-            // to a register (loaded here so their latency passes in the waits)
-            uint32_t ksc[2] = {0u, 0u}, qsc[2] = {0u, 0u};
+            // FP8: the four block scales of token row pt of k and of q (one
+            // word each), loaded here so their latency passes in the waits, and
+            // shared through SM_FSC before the table pass
+            uint32_t ksw = 0x7f7f7f7fu, qsw = 0x7f7f7f7fu;
             if constexpr (FP8) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (8 * rg + j < L) {
-                        const int64_t sidx = ((tok0 + 8 * rg + j) * H + h) * (DK / 32) + (c0 + 4 * cq) / 32;
-                        ksc[j >> 2] |= (uint32_t)__ldg(p.ks + sidx) << (8 * (j & 3));
-                        qsc[j >> 2] |= (uint32_t)__ldg(p.qs + sidx) << (8 * (j & 3));
-                    }
+                if (pt < L) {
+                    ksw = __ldg(reinterpret_cast<const uint32_t *>(p.ks) + (tok0 + pt) * H + h);
+                    qsw = __ldg(reinterpret_cast<const uint32_t *>(p.qs) + (tok0 + pt) * H + h);
+                }
             }
             float4 arow[8];
             {
@@ -915,6 +915,12 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
             }
             scan[rg * 16 + cq] = g;
+            if constexpr (FP8) {
+                if (pt < 64) {
+                    reinterpret_cast<uint32_t *>(s.base + SM_FSC)[pt] = ksw;
+                    reinterpret_cast<uint32_t *>(s.base + SM_FSC)[64 + pt] = qsw;
+                }
+            }
             named_bar(1, GATE_THREADS);
             float4 before = make_float4(1.f, 1.f, 1.f, 1.f), after = before;
 #pragma unroll
@@ -973,8 +979,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     if constexpr (FP8) {
                         float kf[4] = {0.f, 0.f, 0.f, 0.f}, qf[4] = {0.f, 0.f, 0.f, 0.f};
                         if (in) {
-                            e4m3x4_to_f32(k8[j], e8m0((uint8_t)(ksc[j >> 2] >> (8 * (j & 3)))), kf);
-                            e4m3x4_to_f32(q8[j], e8m0((uint8_t)(qsc[j >> 2] >> (8 * (j & 3)))), qf);
+                            const uint32_t *fsc = reinterpret_cast<const uint32_t *>(s.base + SM_FSC);
+                            const int sh = 8 * (((int)rank * KH + 4 * cq) / 32);  // this thread's block
+                            e4m3x4_to_f32(k8[j], e8m0((uint8_t)(fsc[8 * rg + j] >> sh)), kf);
+                            e4m3x4_to_f32(q8[j], e8m0((uint8_t)(fsc[64 + 8 * rg + j] >> sh)), qf);
                         }
                         k01 = f2_make(kf[0], kf[1]); k23 = f2_make(kf[2], kf[3]);
                         q01 = f2_make(qf[0], qf[1]); q23 = f2_make(qf[2], qf[3]);
@@ -1339,12 +1347,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     // A map needs a non-empty extent; an empty token range never issues a copy.
     const int64_t ext = tokens > 0 ? tokens : 1;
     // bf16: 128-byte rows with the 128B swizzle the tensor core reads; FP8
-    // codes: 64-byte rows, unswizzled (the gate and E1 dequantise them)
+    // codes: 64-byte rows (the gate and E1 dequantise them)
     const CUtensorMapDataType et = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int es = a.fp8 ? 1 : 2;
+    // (v codes: 64B swizzle, so that E1's row-per-thread reads hit distinct banks)
     const CUtensorMapSwizzle sw = a.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle swv = a.fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     if (!make_map(&mk, et, es, a.k, DK, a.H, ext, 64, sw) || !make_map(&mq, et, es, a.q, DK, a.H, ext, 64, sw) ||
-        !make_map(&mv, et, es, a.v, DV, a.H, ext, 64, sw))
+        !make_map(&mv, et, es, a.v, DV, a.H, ext, 64, swv))
         return cudaErrorInvalidValue;
     TcParams p;
     p.q = (const __nv_bfloat16 *)a.q;
