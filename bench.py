@@ -339,7 +339,9 @@ def main():
         dt = (time.perf_counter() - t0) / n_e2e
         dt = max_over_ranks(dt, world, dev)
         e2e = {"value": job_tokens_per_s(world, B * T, dt), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+               "path": "kda_prefill_host: page-locked host tensors, copied in pieces along T (about 32 MiB "
+                       "of input each) with copy-in, kernels and copy-out overlapped on three streams"}
 
     # ---- the same workload with a scalar gate (Gated DeltaNet) and without a
     #      gate (the delta rule): fewer gate bytes, same kernels ----

@@ -16,8 +16,10 @@
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte
- *    aligned. The caller owns every buffer; the library allocates nothing, never
- *    synchronises the stream, and launches all its work on `stream`.
+ *    aligned (kda_prefill_host alone takes host buffers). The caller owns every
+ *    buffer; the library allocates nothing, never synchronises the stream, and
+ *    launches all its work on `stream` (kda_prefill_host also uses two copy
+ *    streams of its own, joined back into `stream`).
  *  - Layouts: q, k, alpha [.., T, H, d_k]; v, o [.., T, H, d_v]; beta [.., T, H];
  *    states [N, H, d_k, d_v] with d_v fastest. alpha and beta are float32;
  *    q, k, v and o share `qkv_dtype`; states are float32.
@@ -158,6 +160,48 @@ kda_status_t kda_varlen_prefill_noalloc(const void *q, const void *k, const void
                                         const float *initial_state, void *o, float *final_state,
                                         const int32_t *cu_seqlens, int N, int T_total, int H, int d_k,
                                         int d_v, int32_t *device_status, kda_stream_t stream);
+
+/*
+ * kda_prefill_host - kda_prefill_gate on HOST buffers: q, k, v, alpha, beta,
+ * initial_state (nullable), o and final_state (nullable) are host pointers in
+ * the layouts of kda_prefill_gate (no alignment needed); `workspace` is device
+ * memory of at least kda_prefill_host_workspace_bytes(...) bytes, 16-byte
+ * aligned, owned by the caller.
+ *
+ * The tokens go to the device in pieces of `piece_tokens` tokens along T (0:
+ * the library picks about 32 MiB of input per piece; otherwise a positive
+ * multiple of 64), each piece is one kda_prefill_gate launch on `stream` that
+ * continues from the state the previous piece left in the workspace (the
+ * chunk-to-chunk state passing of the K3 essay §六.1), and each piece's o
+ * returns while later pieces are still in flight. The result is bit for bit
+ * that of kda_prefill_gate run piece by piece on the device with the state
+ * passed between the pieces; against one kda_prefill_gate call over all T
+ * tokens it differs only by rounding at the piece boundaries (one piece, i.e.
+ * piece_tokens >= T, gives the bits of the single call).
+ *
+ * Ordering: everything is queued after the work already on `stream`, and work
+ * queued on `stream` afterwards starts once o and final_state are in host
+ * memory; synchronise `stream` before reading them. The call returns once all
+ * copies are queued (sooner than that only if host memory is pageable: the
+ * driver then copies synchronously, which is correct but does not overlap).
+ * Page-locked host memory gives the overlap. The first call on a device
+ * creates two copy streams and a few events that live until the process
+ * exits; calls are serialised by a lock while they queue their work.
+ *
+ * Errors: as kda_prefill_gate; a device pointer where a host buffer is
+ * expected returns KDA_ERR_INVALID_ARG, a missing or short workspace
+ * KDA_ERR_WORKSPACE, both before anything is queued.
+ */
+kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                              const float *alpha, kda_gate_t gate, const float *beta,
+                              const float *initial_state, void *o, float *final_state, int B, int T,
+                              int H, int d_k, int d_v, kda_algo_t algo, int piece_tokens, void *workspace,
+                              size_t workspace_bytes, kda_stream_t stream);
+
+/* Device workspace bytes kda_prefill_host needs for these sizes (0 for invalid
+ * arguments): three piece buffers of every tensor and one set of states. */
+size_t kda_prefill_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,
+                                        kda_gate_t gate, int piece_tokens);
 
 /*
  * kda_decode_step - one recurrent step per (sequence, head), in place

@@ -26,7 +26,8 @@ ALGOS = {"auto": 0, "simt": 1, "tc": 2}
 GATES = {"channel": 0, "scalar": 1, "none": 2}
 KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT = 0, 1, 2
 
-EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8", "kda_varlen_prefill", "kda_varlen_prefill_slots",
+EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8", "kda_prefill_host",
+           "kda_prefill_host_workspace_bytes", "kda_varlen_prefill", "kda_varlen_prefill_slots",
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_decode_step", "kda_decode_step_slots",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
@@ -70,6 +71,11 @@ def load(path: str | None = None):
         lib.kda_prefill_gate.restype = i
         lib.kda_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp]
         lib.kda_prefill_fp8.restype = i
+        lib.kda_prefill_host.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, i, i, i, i, i, i, i, vp,
+                                         ctypes.c_size_t, vp]
+        lib.kda_prefill_host.restype = i
+        lib.kda_prefill_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.kda_prefill_host_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_varlen_prefill_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, vp, i, i, i, i, i,
                                                  vp, ctypes.c_size_t, vp, vp]
         lib.kda_varlen_prefill_slots.restype = i
@@ -136,48 +142,38 @@ def _to_host(x: torch.Tensor) -> torch.Tensor:
     return h
 
 
-_copy_streams: dict = {}
-
-
-def _streams(dev: torch.device, n: int):
-    """n CUDA streams of the device, created once and reused."""
-    with _lock:
-        pool = _copy_streams.setdefault(dev.index, [])
-        while len(pool) < n:
-            pool.append(torch.cuda.Stream(dev))
-        return pool[:n]
-
-
-def _host_prefill(q, k, v, alpha, beta, initial_state, *, output_final_state, algo, gate, groups: int = 4):
-    """``prefill`` on host tensors. The batch is split into groups of
-    sequences, each group on its own stream: copy in, run, copy out. The
-    sequences are independent, so the result is the same as one call; the
-    copies of one group overlap the kernels and the opposite-direction copies
-    of the others (host-to-device and device-to-host use separate engines)."""
+def _host_prefill(q, k, v, alpha, beta, initial_state, *, output_final_state, algo, gate, piece_tokens):
+    """``prefill`` on host tensors through kda_prefill_host: the library moves
+    the tokens to the device in pieces along T and the outputs back, overlapped
+    with the kernels, on the current CUDA stream. Outputs land in page-locked
+    host tensors and are complete when this returns."""
+    lib = load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    B = q.shape[0]
-    G = max(1, min(groups, B))
-    bounds = [(B * g // G, B * (g + 1) // G) for g in range(G)]
+    cpu = torch.device("cpu")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, cpu)
+    _need(beta, "beta", torch.float32, cpu)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch among q, k, v, beta")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, cpu)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, cpu)
+        if initial_state.shape != (B, H, dk, dv):
+            raise ValueError(f"initial_state must be {(B, H, dk, dv)}")
+    if algo not in ALGOS:
+        raise ValueError(f"algo must be one of {sorted(ALGOS)}")
     o_h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-    s_h = (torch.empty((B,) + tuple(q.shape[2:3]) + (q.shape[-1], v.shape[-1]), dtype=torch.float32,
-                       pin_memory=True) if output_final_state else None)
-    cur = torch.cuda.current_stream(dev)
-    streams = _streams(dev, G)
-    for (lo, hi), st in zip(bounds, streams):
-        if hi == lo:
-            continue
-        st.wait_stream(cur)  # after whatever the caller queued before
-        with torch.cuda.stream(st):
-            part = [None if t is None else t[lo:hi].to(dev, non_blocking=True)
-                    for t in (q, k, v, alpha, beta, initial_state)]
-            o_d, s_d = prefill(*part[:5], part[5], output_final_state=output_final_state, algo=algo,
-                               gate=gate, stream=st)
-            o_h[lo:hi].copy_(o_d, non_blocking=True)
-            if s_h is not None:
-                s_h[lo:hi].copy_(s_d, non_blocking=True)
-    for st in streams:
-        cur.wait_stream(st)
-    cur.synchronize()
+    s_h = torch.empty((B, H, dk, dv), dtype=torch.float32, pin_memory=True) if output_final_state else None
+    nbytes = lib.kda_prefill_host_workspace_bytes(B, T, H, dk, dv, _dtype_code(q), GATES[gate], piece_tokens)
+    ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = lib.kda_prefill_host(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate], _ptr(beta),
+                              _ptr(initial_state), _ptr(o_h), _ptr(s_h), B, T, H, dk, dv, ALGOS[algo],
+                              int(piece_tokens), _ptr(ws), ws.numel(), _stream(stream))
+    _check(lib, st)
+    stream.synchronize()
     return o_h, s_h
 
 
@@ -210,7 +206,8 @@ def _check_gate(gate: str, alpha, lead: tuple, dk: int, dev):
 
 
 def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: bool = True,
-            algo: str = "auto", gate: str = "channel", out=None, final_state=None, stream=None):
+            algo: str = "auto", gate: str = "channel", out=None, final_state=None, stream=None,
+            piece_tokens: int = 0):
     """Chunkwise KDA prefill of B equal-length sequences.
 
     q, k: [B, T, H, d_k]; v: [B, T, H, d_v] (bf16 or fp32, same dtype);
@@ -218,10 +215,17 @@ def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: boo
     Gated DeltaNet) or None (gate="none", the delta rule); beta: [B, T, H] fp32;
     initial_state: [B, H, d_k, d_v] fp32 or None (zeros).
     Returns (o [B, T, H, d_v] in v's dtype, final_state [B, H, d_k, d_v] fp32 or None).
+
+    Host (CPU) tensors go through kda_prefill_host: pieces of ``piece_tokens``
+    tokens (0: the library's choice) travel to the GPU and back overlapped with
+    the kernels; the outputs are page-locked host tensors. Page-locked inputs
+    (``tensor.pin_memory()``) let the copies overlap.
     """
     if q.device.type == "cpu":
+        if out is not None or final_state is not None or stream is not None:
+            raise ValueError("out, final_state and stream apply to device tensors only")
         return _host_prefill(q, k, v, alpha, beta, initial_state, output_final_state=output_final_state,
-                             algo=algo, gate=gate)
+                             algo=algo, gate=gate, piece_tokens=piece_tokens)
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

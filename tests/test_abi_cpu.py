@@ -158,3 +158,45 @@ def test_fp8_argument_checks(lib):
                                None) == 1
     assert lib.kda_prefill_fp8(None, None, None, None, None, None, None, 0, None, None, None, None, 0, 8, 2, 128,
                                128, None) == 0
+
+
+def test_host_prefill_argument_checks(lib):
+    """kda_prefill_host checks its arguments and workspace before any CUDA call."""
+    p = ctypes.c_void_p(0x1000)
+
+    def call(dtype=1, gate=0, B=1, T=64, H=1, dk=64, dv=64, algo=0, piece=0, ws=p, nbytes=1 << 30, q=p, a=p):
+        return lib.kda_prefill_host(q, p, p, dtype, a, gate, p, None, p, None, B, T, H, dk, dv, algo, piece,
+                                    ws, nbytes, None)
+
+    assert call(dtype=5) == 1
+    assert call(gate=3) == 1
+    assert call(algo=7) == 1
+    assert call(dk=96) == 2
+    assert call(piece=100) == 1 and b"multiple of 64" in lib.kda_last_error()
+    assert call(piece=-64) == 1
+    assert call(q=None) == 1
+    assert call(a=None) == 1                # the channel gate needs alpha
+    assert call(ws=None) == 5               # no workspace
+    assert call(nbytes=16) == 5             # too small
+    assert call(ws=ctypes.c_void_p(0x1008)) == 1  # misaligned workspace
+    assert call(B=0) == 0                   # nothing to do
+    assert call(T=0) == 0                   # no tokens and no final state
+
+
+def test_host_prefill_workspace_size(lib):
+    """Three piece buffers of q, k, v, alpha, beta and o (each rounded up to
+    256 bytes) plus one set of states."""
+    f = lib.kda_prefill_host_workspace_bytes
+    # B=1, T=64, H=1, d=64, fp32, channel gate, pieces of 64 tokens:
+    # q, k, v, alpha, o 64*64*4 = 16384 bytes each, beta 256; state 16384
+    assert f(1, 64, 1, 64, 64, 0, 0, 64) == 3 * (5 * 16384 + 256) + 16384
+    # no gate: no alpha buffer; a piece longer than T holds T tokens
+    assert f(1, 64, 1, 64, 64, 0, 2, 512) == 3 * (4 * 16384 + 256) + 16384
+    # invalid arguments give 0
+    assert f(1, 64, 1, 96, 64, 0, 0, 0) == 0
+    assert f(1, 64, 1, 64, 64, 0, 0, 65) == 0
+    # the library's own piece size stays within about 32 MiB of input per piece
+    B, T, H = 4, 4096, 16
+    full_in = B * T * H * (3 * 128 * 2 + 128 * 4 + 4)
+    ws = f(B, T, H, 128, 128, 1, 0, 0)
+    assert 0 < ws < full_in

@@ -181,10 +181,9 @@ def test_host_buffers_round_trip(kda):
     torch.testing.assert_close(s_h, s_d.cpu(), rtol=0, atol=0)
 
 
-def test_host_buffers_split_over_streams(kda):
-    """The host path splits the batch over several streams (copy in, run, copy
-    out per group): five sequences in four groups, a scalar gate and no final
-    state give the device call's bits."""
+def test_host_buffers_scalar_gate_without_final_state(kda):
+    """Host inputs with a scalar gate and no final state (five sequences, one
+    piece): the device call's bits."""
     x = W.batched(5, 130, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=32)
     a_s = x.alpha[..., 0].contiguous()
     q, k, v, _, b, s0 = _dev(x)
