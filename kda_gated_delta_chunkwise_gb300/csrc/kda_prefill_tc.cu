@@ -41,11 +41,12 @@
 //   warp 12          TMA producer of this CTA's q, k halves (the epilogue
 //                    refills v itself; the gate reads alpha into registers)
 //   warp 13          MMA issuer of the state chain (one thread), TMEM owner
-//   warp 14          MMA issuer of [A; P] on this CTA's parity; warp 15 idle
+//   warp 14          MMA issuer of [A; P] on this CTA's parity
+//   warp 15          FP8 inputs only: k and q codes -> bf16 tiles (idle otherwise)
 // FP8 inputs (E4M3 codes, one power-of-two scale per 32 channels): the TMA
-// warp loads the codes into the Qr half of the slot, the gate dequantises k
-// and q while it builds the tables, E1 dequantises v; everything after that
-// is the bf16 path.
+// warp loads the codes into the Qr half of the slot, warp 15 turns them into
+// the bf16 k and q tiles in place, so the gate runs the bf16 code; E1
+// dequantises v; everything after that is the bf16 path.
 // Register budgets per warpgroup (setmaxnreg): epilogue 152, warps 4-11 128,
 // control 104. The groups work on consecutive chunks at once. All waits are
 // bounded; a CTA whose wait times out records an error and winds down.
@@ -85,6 +86,7 @@ constexpr int SOLVE_THREADS = 128;
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
 constexpr int WARP_AUX = 14;
+constexpr int WARP_DQ = 15;
 constexpr float kMinGamma = 1.8e-35f;  // ~exp(-80)
 
 // TMEM columns (fp32 accumulators, 128 lanes each); AP, XY and UO are
@@ -117,8 +119,7 @@ constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
 constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
 constexpr uint32_t SM_MSCR = 225232;   // float[4][16*8]: mma.sync staging (3 KB reserved)
 constexpr uint32_t SM_SCAN = 228304;   // float4[8][16]: per-group gate products
-constexpr uint32_t SM_FSC = 230352;    // uint32[2][64]: FP8 block scales of the chunk's k and q rows
-constexpr uint32_t SM_TOTAL = 230864;
+constexpr uint32_t SM_TOTAL = 230352;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 
 // Bytes one CTA pushes into its peer per chunk: its [Kr; Qr] half, its Kc
@@ -137,7 +138,8 @@ constexpr int NTAB = 2 * NSLOT;
 enum Bar {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_TAB_FULL = 7, B_B0_EMPTY = 13, B_O_READ = 16,
     B_AP_FULL = 18, B_T_FULL = 20, B_T_EMPTY = 21, B_P_FULL = 23, B_P_EMPTY = 25, B_S_FULL = 27, B_XY_FULL = 28,
-    B_R_FULL = 29, B_U_FULL = 30, B_UU_FULL = 31, B_D_FULL = 32, B_DRAIN = 33, B_DRAIN_AUX = 34, B_COUNT = 35
+    B_R_FULL = 29, B_U_FULL = 30, B_UU_FULL = 31, B_D_FULL = 32, B_DRAIN = 33, B_DRAIN_AUX = 34, B_DQ_FULL = 35,
+    B_COUNT = 38
 };
 static_assert(B_COUNT <= 40, "mbarrier area");
 
@@ -445,6 +447,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // phases behind)
             mbar_init(s.bar(B_QK_EMPTY + i), 4);
             mbar_init(s.bar(B_B0_EMPTY + i), 2);  // MMA3 of both CTAs
+            mbar_init(s.bar(B_DQ_FULL + i), 1);   // FP8: the bf16 k, q tiles of the slot (warp 15)
         }
         // own gate (expecting the peer's bytes) + the peer's copies
         for (int i = 0; i < NTAB; ++i) mbar_init(s.bar(B_TAB_FULL + i), 1);
@@ -597,6 +600,66 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             mbar_wait(s.bar(B_DRAIN_AUX), 0);
         }
         __syncwarp();
+    } else if (warp == WARP_DQ) {
+        // ------------------------------------------------------------ FP8: k, q codes -> bf16 tiles
+        // Lane: token rows lane and lane + 32 of this CTA's key half. The codes
+        // (64-byte rows: k at +8192, q at +12288 of the half) become the tiles
+        // the TMA writes for bf16 inputs (128-byte rows, 16-byte chunks swizzled
+        // by the row's low three bits): k over the Kr half, q over the Qr half.
+        // Four passes (k rows 0-31, 32-63, q rows 0-31, 32-63); in each, every
+        // lane reads its row's codes before any lane writes. A pass writes over
+        // codes only of rows already converted or of its own pass (q rows 0-31
+        // land on k's codes, q rows 32-63 on q's codes of rows 0-63).
+        if constexpr (FP8) {
+            bool alive = true;
+            for (int n = 0; n < NC; ++n) {
+                const int b = n % NSLOT, kk = n / NSLOT;
+                const int64_t tok0 = t_begin + (int64_t)n * C;
+                const int L = (int)((T - (int64_t)n * C) < C ? (T - (int64_t)n * C) : C);
+                uint32_t ksw[2], qsw[2];  // the rows' scale words, loaded before the wait
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int r = lane + 32 * u;
+                    ksw[u] = qsw[u] = 0x7f7f7f7fu;
+                    if (r < L) {
+                        ksw[u] = __ldg(reinterpret_cast<const uint32_t *>(p.ks) + (tok0 + r) * H + h);
+                        qsw[u] = __ldg(reinterpret_cast<const uint32_t *>(p.qs) + (tok0 + r) * H + h);
+                    }
+                }
+                alive = alive && s.flags()[1] == 0;
+                const bool ok = __all_sync(0xffffffffu, alive && wait_bar(s, p, B_QK_FULL + b, kk & 1));
+                unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;
+                if (ok) {
+#pragma unroll 1
+                    for (int tu = 0; tu < 4; ++tu) {  // k rows lane, lane + 32, then q rows lane, lane + 32
+                        const int t = tu >> 1, r = lane + 32 * (tu & 1);
+                        const uint32_t sw = t ? ((tu & 1) ? qsw[1] : qsw[0]) : ((tu & 1) ? ksw[1] : ksw[0]);
+                        uint4 w[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            w[c] = *reinterpret_cast<const uint4 *>(ah + 8192 + 4096 * t + r * 64 + 16 * c);
+                        __syncwarp();  // q rows 32-63 land on codes other lanes read in this pass
+                        unsigned char *dst = ah + 8192 * t + r * 128;
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {  // 8 channels: codes 8 c8 .. 8 c8 + 7
+                            const uint4 cw = w[c8 >> 1];
+                            const float sc = e8m0((uint8_t)(sw >> (8 * (2 * (int)rank + (c8 >> 2)))));
+                            float f[4], g[4];
+                            e4m3x4_to_f32((c8 & 1) ? cw.z : cw.x, sc, f);
+                            e4m3x4_to_f32((c8 & 1) ? cw.w : cw.y, sc, g);
+                            *reinterpret_cast<uint4 *>(dst + ((c8 ^ (r & 7)) << 4)) =
+                                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(g[0], g[1]),
+                                           pack_bf16(g[2], g[3]));
+                        }
+                        __syncwarp();
+                    }
+                    fence_proxy_async();  // before the slot returns to the copy engine
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s.bar(B_DQ_FULL + b));
+                alive = ok;
+            }
+        }
     } else if (warp >= 12) {
         // idle warp of the control warpgroup
     } else if (warp < 4) {
@@ -877,16 +940,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             // beta and alpha of this chunk, loaded before the waits so their
             // latency is hidden
             const float beta_r = pt < L ? p.beta[(tok0 + pt) * H + h] : 0.f;
-            // FP8: the four block scales of token row pt of k and of q (one
-            // word each), loaded here so their latency passes in the waits, and
-            // shared through SM_FSC before the table pass
-            uint32_t ksw = 0x7f7f7f7fu, qsw = 0x7f7f7f7fu;
-            if constexpr (FP8) {
-                if (pt < L) {
-                    ksw = __ldg(reinterpret_cast<const uint32_t *>(p.ks) + (tok0 + pt) * H + h);
-                    qsw = __ldg(reinterpret_cast<const uint32_t *>(p.qs) + (tok0 + pt) * H + h);
-                }
-            }
             float4 arow[8];
             {
                 const float *src = alpha_src(n);
@@ -906,7 +959,8 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             }
             const int b3 = b;  // A0 and B0 slots go together
             alive = alive && s.flags()[1] == 0;  // stop waiting once the CTA gave up
-            bool ok = alive && wait_bar(s, p, B_QK_FULL + b, kk & 1);
+            // (FP8: the bf16 tiles warp 15 made from the codes)
+            bool ok = alive && wait_bar(s, p, (FP8 ? B_DQ_FULL : B_QK_FULL) + b, kk & 1);
             // products of this thread's 8 rows, then the 8 group products
             float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
@@ -915,12 +969,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
             }
             scan[rg * 16 + cq] = g;
-            if constexpr (FP8) {
-                if (pt < 64) {
-                    reinterpret_cast<uint32_t *>(s.base + SM_FSC)[pt] = ksw;
-                    reinterpret_cast<uint32_t *>(s.base + SM_FSC)[64 + pt] = qsw;
-                }
-            }
             named_bar(1, GATE_THREADS);
             float4 before = make_float4(1.f, 1.f, 1.f, 1.f), after = before;
 #pragma unroll
@@ -948,21 +996,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (n >= NSLOT) ok = ok && wait_bar(s, p, B_B0_EMPTY + b3, (kk - 1) & 1);
             unsigned char *ah = s.base + SM_A0 + b * 32768 + rank * 16384;  // [k; q] rows of this key half
             unsigned char *kch = s.base + SM_B0 + b3 * 16384 + rank * 8192;  // Kc rows of this key half
-            // FP8: this thread's codes of k and q (4 channels of each of its 8
-            // rows) leave the staging area in the Qr half before any Qr row is
-            // written there
-            uint32_t k8[8], q8[8];
-            if constexpr (FP8) {
-                if (ok && !slow) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t o8 = (uint32_t)(8 * rg + j) * 64u + 4u * (uint32_t)cq;
-                        k8[j] = *reinterpret_cast<const uint32_t *>(ah + 8192 + o8);
-                        q8[j] = *reinterpret_cast<const uint32_t *>(ah + 12288 + o8);
-                    }
-                }
-                named_bar(1, GATE_THREADS);
-            }
             if (ok && !slow) {
                 // One pass over the rows with the running product p_r:
                 // Kr = k p / mu and Qr = q p / mu in place, Kc = k mu / p (the
@@ -975,23 +1008,10 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t off = rowbase + (uint32_t)j * 128u + ((c8 ^ (uint32_t)j) << 4);
                     const bool in = 8 * rg + j < L;
-                    uint64_t k01, k23, q01, q23;
-                    if constexpr (FP8) {
-                        float kf[4] = {0.f, 0.f, 0.f, 0.f}, qf[4] = {0.f, 0.f, 0.f, 0.f};
-                        if (in) {
-                            const uint32_t *fsc = reinterpret_cast<const uint32_t *>(s.base + SM_FSC);
-                            const int sh = 8 * (((int)rank * KH + 4 * cq) / 32);  // this thread's block
-                            e4m3x4_to_f32(k8[j], e8m0((uint8_t)(fsc[8 * rg + j] >> sh)), kf);
-                            e4m3x4_to_f32(q8[j], e8m0((uint8_t)(fsc[64 + 8 * rg + j] >> sh)), qf);
-                        }
-                        k01 = f2_make(kf[0], kf[1]); k23 = f2_make(kf[2], kf[3]);
-                        q01 = f2_make(qf[0], qf[1]); q23 = f2_make(qf[2], qf[3]);
-                    } else {
-                        const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
-                        const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
-                        k01 = bf2_to_f2(kw.x); k23 = bf2_to_f2(kw.y);
-                        q01 = bf2_to_f2(qw.x); q23 = bf2_to_f2(qw.y);
-                    }
+                    const uint2 kw = in ? *reinterpret_cast<const uint2 *>(ah + off) : make_uint2(0u, 0u);
+                    const uint2 qw = in ? *reinterpret_cast<const uint2 *>(ah + 8192 + off) : make_uint2(0u, 0u);
+                    const uint64_t k01 = bf2_to_f2(kw.x), k23 = bf2_to_f2(kw.y);
+                    const uint64_t q01 = bf2_to_f2(qw.x), q23 = bf2_to_f2(qw.y);
                     pr01 = f2_mul(pr01, f2_make(arow[j].x, arow[j].y));
                     pr23 = f2_mul(pr23, f2_make(arow[j].z, arow[j].w));
                     const uint64_t e01 = f2_mul(pr01, inv01), e23 = f2_mul(pr23, inv23);
