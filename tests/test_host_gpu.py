@@ -147,3 +147,58 @@ def test_full_size_workload_through_host_buffers(kda):
     tol = tol_for(torch.bfloat16)
     assert_close("o", o_a, o_1.cpu(), tol)
     assert_close("final_state", s_a, s_1.cpu(), tol)
+
+
+def test_back_to_back_calls_share_a_workspace_on_one_stream(kda):
+    """Two kda_prefill_host calls queued on one stream with one workspace and
+    no synchronisation between them: the second call's copies wait for the
+    first call's work, so both results are the single calls' bits."""
+    from kda_gated_delta_chunkwise_gb300 import _binding
+    lib = kda.load()
+    xs = [W.batched(2, 300, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=s) for s in (51, 52)]
+    ref = [_host(kda, x, "channel", 128) for x in xs]
+    d = torch.device("cuda")
+    nbytes = lib.kda_prefill_host_workspace_bytes(2, 300, 2, 128, 128, 1, 0, 128)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=d)
+    stream = torch.cuda.Stream()
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    outs = []
+    for x in xs:
+        h = [t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta, x.initial_state)]
+        o = torch.empty(x.v.shape, dtype=x.v.dtype, pin_memory=True)
+        s = torch.empty(x.initial_state.shape, pin_memory=True)
+        st = lib.kda_prefill_host(p(h[0]), p(h[1]), p(h[2]), 1, p(h[3]), 0, p(h[4]), p(h[5]), p(o), p(s),
+                                  2, 300, 2, 128, 128, 0, 128, p(ws), nbytes, ctypes.c_void_p(stream.cuda_stream))
+        assert st == _binding.KDA_OK, lib.kda_last_error()
+        outs.append((o, s, h))
+    stream.synchronize()
+    for (o, s, _), (o_r, s_r) in zip(outs, ref):
+        assert torch.equal(o, o_r) and torch.equal(s, s_r)
+
+
+def test_concurrent_host_calls_from_two_threads(kda):
+    """Host threads each running prefill on host buffers on their own stream
+    (the library serialises the queueing, the copies share its streams): every
+    result is the bits of the same call made alone."""
+    import threading
+    xs = [W.batched(2, 260, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=s) for s in (61, 62, 63)]
+    ref = [_host(kda, x, "channel", 64) for x in xs]
+    got = [None] * len(xs)
+    errors = []
+
+    def work(i):
+        try:
+            with torch.cuda.stream(torch.cuda.Stream()):
+                for _ in range(3):
+                    got[i] = _host(kda, xs[i], "channel", 64)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(xs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (o, s), (o_r, s_r) in zip(got, ref):
+        assert torch.equal(o, o_r) and torch.equal(s, s_r)
