@@ -392,6 +392,26 @@ def main():
                                   "algorithmic_bytes_per_launch": fbytes,
                                   "achieved_gbs": fbytes / (fms / 1e3) / 1e9,
                                   "frac": fbytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        if not args.no_e2e:
+            # end to end from page-locked host memory (kda_prefill_fp8_host):
+            # the host link carries one byte per q, k, v element
+            fh = [t.cpu().pin_memory() for t in (cq, ck, cv, sq, sk, sv)]
+            ah, bh = a.cpu().pin_memory(), b.cpu().pin_memory()
+            oh = sh = None
+            for _ in range(3):
+                oh, sh = kda.prefill_fp8(*fh, ah, bh, None)
+            torch.cuda.synchronize()
+            n_e2e = max(3, min(args.steps, 10))
+            t0 = time.perf_counter()
+            for _ in range(n_e2e):
+                oh, sh = kda.prefill_fp8(*fh, ah, bh, None)
+            torch.cuda.synchronize()
+            fdt = (time.perf_counter() - t0) / n_e2e
+            variants["fp8_inputs"]["e2e"] = {
+                "value": B * T / fdt, "unit": "tokens/s", "ms_per_step": fdt * 1e3,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in fh + [ah, bh]),
+                "d2h_bytes_per_step": oh.numel() * oh.element_size() + sh.numel() * 4}
+            del fh, ah, bh, oh, sh
         del cq, ck, cv, sq, sk, sv
 
     # ---- decode step (secondary figure of the metric) ----

@@ -16,10 +16,11 @@
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte
- *    aligned (kda_prefill_host alone takes host buffers). The caller owns every
- *    buffer; the library allocates nothing, never synchronises the stream, and
- *    launches all its work on `stream` (kda_prefill_host also uses two copy
- *    streams of its own, joined back into `stream`).
+ *    aligned (kda_prefill_host and kda_prefill_fp8_host alone take host
+ *    buffers). The caller owns every buffer; the library allocates nothing,
+ *    never synchronises the stream, and launches all its work on `stream`
+ *    (the two host-buffer calls also use two copy streams of their own,
+ *    joined back into `stream`).
  *  - Layouts: q, k, alpha [.., T, H, d_k]; v, o [.., T, H, d_v]; beta [.., T, H];
  *    states [N, H, d_k, d_v] with d_v fastest. alpha and beta are float32;
  *    q, k, v and o share `qkv_dtype`; states are float32.
@@ -202,6 +203,28 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_d
  * arguments): three piece buffers of every tensor and one set of states. */
 size_t kda_prefill_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,
                                         kda_gate_t gate, int piece_tokens);
+
+/*
+ * kda_prefill_fp8_host - kda_prefill_fp8 on HOST buffers, through the piece
+ * pipeline of kda_prefill_host: q, k, v (E4M3 codes), q_scale, k_scale,
+ * v_scale (E8M0), alpha, beta, initial_state (nullable), o (bf16) and
+ * final_state (nullable) are host pointers in the layouts of kda_prefill_fp8;
+ * `workspace` is device memory of at least kda_prefill_fp8_host_workspace_bytes
+ * bytes, 16-byte aligned. The host link carries 1 byte per q, k, v element
+ * instead of 2, which is where the FP8 format pays off: the end-to-end call is
+ * bound by that link. Result, ordering, piece size and errors as for
+ * kda_prefill_host (bit for bit kda_prefill_fp8 run piece by piece on the
+ * device with the state passed between the pieces). d_k = d_v = 128 only.
+ */
+kda_status_t kda_prefill_fp8_host(const uint8_t *q, const uint8_t *k, const uint8_t *v, const uint8_t *q_scale,
+                                  const uint8_t *k_scale, const uint8_t *v_scale, const float *alpha,
+                                  kda_gate_t gate, const float *beta, const float *initial_state, void *o,
+                                  float *final_state, int B, int T, int H, int d_k, int d_v, int piece_tokens,
+                                  void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Device workspace bytes kda_prefill_fp8_host needs (0 for invalid arguments). */
+size_t kda_prefill_fp8_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_gate_t gate,
+                                            int piece_tokens);
 
 /*
  * kda_decode_step - one recurrent step per (sequence, head), in place

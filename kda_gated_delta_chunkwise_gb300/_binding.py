@@ -27,7 +27,8 @@ GATES = {"channel": 0, "scalar": 1, "none": 2}
 KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT = 0, 1, 2
 
 EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8", "kda_prefill_host",
-           "kda_prefill_host_workspace_bytes", "kda_varlen_prefill", "kda_varlen_prefill_slots",
+           "kda_prefill_host_workspace_bytes", "kda_prefill_fp8_host", "kda_prefill_fp8_host_workspace_bytes",
+           "kda_varlen_prefill", "kda_varlen_prefill_slots",
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_decode_step", "kda_decode_step_slots",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
@@ -76,6 +77,11 @@ def load(path: str | None = None):
         lib.kda_prefill_host.restype = i
         lib.kda_prefill_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         lib.kda_prefill_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_prefill_fp8_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, i, vp,
+                                             ctypes.c_size_t, vp]
+        lib.kda_prefill_fp8_host.restype = i
+        lib.kda_prefill_fp8_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kda_prefill_fp8_host_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_varlen_prefill_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, vp, i, i, i, i, i,
                                                  vp, ctypes.c_size_t, vp, vp]
         lib.kda_varlen_prefill_slots.restype = i
@@ -172,6 +178,39 @@ def _host_prefill(q, k, v, alpha, beta, initial_state, *, output_final_state, al
     st = lib.kda_prefill_host(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate], _ptr(beta),
                               _ptr(initial_state), _ptr(o_h), _ptr(s_h), B, T, H, dk, dv, ALGOS[algo],
                               int(piece_tokens), _ptr(ws), ws.numel(), _stream(stream))
+    _check(lib, st)
+    stream.synchronize()
+    return o_h, s_h
+
+
+def _host_prefill_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, initial_state, *, output_final_state,
+                      gate, piece_tokens):
+    """``prefill_fp8`` on host tensors through kda_prefill_fp8_host."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cpu = torch.device("cpu")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.uint8, cpu)
+    _need(beta, "beta", torch.float32, cpu)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H) \
+            or q_scale.shape != (B, T, H, dk // 32) or k_scale.shape != (B, T, H, dk // 32) \
+            or v_scale.shape != (B, T, H, dv // 32):
+        raise ValueError("shape mismatch among q, k, v, the scales and beta")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, cpu)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, cpu)
+        if initial_state.shape != (B, H, dk, dv):
+            raise ValueError(f"initial_state must be {(B, H, dk, dv)}")
+    o_h = torch.empty((B, T, H, dv), dtype=torch.bfloat16, pin_memory=True)
+    s_h = torch.empty((B, H, dk, dv), dtype=torch.float32, pin_memory=True) if output_final_state else None
+    nbytes = lib.kda_prefill_fp8_host_workspace_bytes(B, T, H, dk, dv, GATES[gate], piece_tokens)
+    ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = lib.kda_prefill_fp8_host(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                  _ptr(alpha), GATES[gate], _ptr(beta), _ptr(initial_state), _ptr(o_h), _ptr(s_h),
+                                  B, T, H, dk, dv, int(piece_tokens), _ptr(ws), ws.numel(), _stream(stream))
     _check(lib, st)
     stream.synchronize()
     return o_h, s_h
@@ -406,12 +445,19 @@ def decode_step_slots(q, k, v, alpha, beta, state_pool, slots, *, gate: str = "c
 
 
 def prefill_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, initial_state=None, *, gate: str = "channel",
-                output_final_state: bool = True, out=None, final_state=None, stream=None):
+                output_final_state: bool = True, out=None, final_state=None, stream=None, piece_tokens: int = 0):
     """``prefill`` on FP8 inputs in the MX block format: q, k, v are uint8
     E4M3 codes [B, T, H, 128], each 32 channels of a token-head sharing one
     E8M0 scale byte (q_scale, k_scale, v_scale: uint8 [B, T, H, 4]). The result
     equals ``prefill`` on bf16 inputs holding the dequantised values; o is bf16.
+    Host (CPU) tensors go through kda_prefill_fp8_host (pieces of
+    ``piece_tokens`` tokens, 0: the library's choice), like ``prefill``.
     """
+    if q.device.type == "cpu":
+        if out is not None or final_state is not None or stream is not None:
+            raise ValueError("out, final_state and stream apply to device tensors only")
+        return _host_prefill_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, initial_state,
+                                 output_final_state=output_final_state, gate=gate, piece_tokens=piece_tokens)
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):

@@ -1,9 +1,9 @@
-// Prefill on host buffers (kda_prefill_host): the tokens travel to the GPU in
-// pieces along T and the outputs come back piece by piece, so the host link,
-// the kernels and the copies back overlap. The state between pieces stays on
-// the device; each piece is one kda_prefill_gate call that starts from the
-// state the previous piece left (the chunk-to-chunk passing of the K3 essay
-// §六.1, carried across calls).
+// Prefill on host buffers (kda_prefill_host, kda_prefill_fp8_host): the tokens
+// travel to the GPU in pieces along T and the outputs come back piece by
+// piece, so the host link, the kernels and the copies back overlap. The state
+// between pieces stays on the device; each piece is one device prefill call
+// that starts from the state the previous piece left (the chunk-to-chunk
+// passing of the K3 essay §六.1, carried across calls).
 //
 // Streams: the kernels run on the caller's stream; the copies to the device run
 // on one internal stream and the copies back on another (created once per
@@ -14,17 +14,17 @@
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
-#include <string>
 
 #include "kda_internal.cuh"
 
 namespace {
 
-constexpr int kRing = 3;                      // piece buffers in flight
+constexpr int kRing = 3;                       // piece buffers in flight
 constexpr size_t kAlign = 256;
-constexpr int64_t kPieceBytes = 32ll << 20;   // input bytes per piece when the caller leaves it open
+constexpr int64_t kPieceBytes = 32ll << 20;    // input bytes per piece when the caller leaves it open
 constexpr size_t kMaxPitch = size_t(1) << 30;  // larger row pitches are copied row by row
 constexpr int kMaxDevices = 64;
+constexpr int kMaxInputs = 8;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -42,52 +42,56 @@ kda_status_t cuda_fail(cudaError_t e, const char *what) {
     return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Bytes of one token row (all heads) of each tensor.
-struct Rows {
-    size_t qk, v, a, b, o;
+// One host-to-device stream of token rows: the caller's host tensor and the
+// bytes of one token row (all heads). A tensor the call does not use has
+// row = 0 (no buffer, no copy).
+struct In {
+    const void *src;
+    size_t row;
 };
 
-Rows row_bytes(int H, int dk, int dv, kda_dtype_t dt, kda_gate_t gate) {
-    const size_t es = dt == KDA_BF16 ? 2 : 4;
-    Rows r;
-    r.qk = (size_t)H * dk * es;
-    r.v = (size_t)H * dv * es;
-    r.a = gate == KDA_GATE_CHANNEL ? (size_t)H * dk * 4 : gate == KDA_GATE_SCALAR ? (size_t)H * 4 : 0;
-    r.b = (size_t)H * 4;
-    r.o = (size_t)H * dv * es;
-    return r;
-}
+// The tensors of one call: inputs in the order the launcher expects them,
+// the output row (o), the state size.
+struct Plan {
+    In in[kMaxInputs];
+    int nin;
+    size_t orow, state_bytes;
+};
 
 // Tokens per piece: the caller's choice, else about kPieceBytes of input per
 // piece, in whole chunks.
-int64_t piece_tokens_for(int B, int T, const Rows &r, int piece_tokens) {
+int64_t piece_tokens_for(const Plan &pl, int B, int T, int piece_tokens) {
     if (T <= 0) return 0;
     int64_t pt = piece_tokens;
     if (pt == 0) {
-        const int64_t per_tok = (int64_t)B * (int64_t)(2 * r.qk + r.v + r.a + r.b);
-        const int64_t pieces = (T * per_tok + kPieceBytes - 1) / kPieceBytes;
-        const int64_t len = (T + (pieces > 0 ? pieces : 1) - 1) / (pieces > 0 ? pieces : 1);
+        size_t row = 0;
+        for (int i = 0; i < pl.nin; ++i) row += pl.in[i].row;
+        const int64_t per_tok = (int64_t)B * (int64_t)row;
+        int64_t pieces = (T * per_tok + kPieceBytes - 1) / kPieceBytes;
+        if (pieces < 1) pieces = 1;
+        const int64_t len = (T + pieces - 1) / pieces;
         pt = (len + 63) / 64 * 64;
     }
     return pt < T ? pt : T;  // buffers hold at most T tokens
 }
 
+// Workspace: kRing slots of [inputs..., o], then the state.
 struct Layout {
-    size_t q, k, v, a, b, o, slot, state, total;
+    size_t in[kMaxInputs], o, slot, state, total;
 };
 
-Layout layout(int B, int64_t cap, int H, int dk, int dv, const Rows &r) {
+Layout layout(const Plan &pl, int B, int64_t cap) {
     Layout l;
     const size_t n = (size_t)B * (size_t)cap;
-    l.q = 0;
-    l.k = l.q + align_up(n * r.qk);
-    l.v = l.k + align_up(n * r.qk);
-    l.a = l.v + align_up(n * r.v);
-    l.b = l.a + align_up(n * r.a);
-    l.o = l.b + align_up(n * r.b);
-    l.slot = l.o + align_up(n * r.o);
+    size_t off = 0;
+    for (int i = 0; i < pl.nin; ++i) {
+        l.in[i] = off;
+        off += align_up(n * pl.in[i].row);
+    }
+    l.o = off;
+    l.slot = off + align_up(n * pl.orow);
     l.state = kRing * l.slot;
-    l.total = l.state + align_up((size_t)B * H * dk * dv * sizeof(float));
+    l.total = l.state + align_up(pl.state_bytes);
     return l;
 }
 
@@ -141,64 +145,32 @@ kda_status_t need_host(const void *p, const char *name) {
     return KDA_OK;
 }
 
-bool valid_args(kda_dtype_t dt, kda_gate_t gate, int B, int T, int H, int dk, int dv, int piece_tokens) {
-    return (dt == KDA_F32 || dt == KDA_BF16) &&
-           (gate == KDA_GATE_CHANNEL || gate == KDA_GATE_SCALAR || gate == KDA_GATE_NONE) && B >= 0 && T >= 0 &&
-           H > 0 && (dk == 64 || dk == 128) && (dv == 64 || dv == 128) && piece_tokens >= 0 &&
-           piece_tokens % 64 == 0 && (int64_t)B * T <= INT32_MAX;
-}
+// Launch of one piece: device buffers of the inputs (in Plan order), the
+// piece's tokens, the state to start from (NULL: zeros) and the state buffer
+// to write, on the caller's stream.
+struct Launcher {
+    virtual kda_status_t operator()(char *const in[], void *o, int len, const float *s0, float *state,
+                                    kda_stream_t s) const = 0;
+};
 
-}  // namespace
-
-extern "C" {
-
-size_t kda_prefill_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,
-                                        kda_gate_t gate, int piece_tokens) {
-    if (!valid_args(qkv_dtype, gate, B, T, H, d_k, d_v, piece_tokens)) return 0;
-    const Rows r = row_bytes(H, d_k, d_v, qkv_dtype, gate);
-    return layout(B, piece_tokens_for(B, T, r, piece_tokens), H, d_k, d_v, r).total;
-}
-
-kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                              const float *alpha, kda_gate_t gate, const float *beta,
-                              const float *initial_state, void *o, float *final_state, int B, int T,
-                              int H, int d_k, int d_v, kda_algo_t algo, int piece_tokens, void *workspace,
-                              size_t workspace_bytes, kda_stream_t stream) {
-    // ---- argument checks, before any CUDA call
-    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16)
-        return fail(KDA_ERR_INVALID_ARG, "unknown qkv dtype %d", (int)qkv_dtype);
-    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_SCALAR && gate != KDA_GATE_NONE)
-        return fail(KDA_ERR_INVALID_ARG, "unknown gate kind %d", (int)gate);
-    if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SIMT && algo != KDA_ALGO_TC)
-        return fail(KDA_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
-    if (H <= 0 || d_k <= 0 || d_v <= 0) return fail(KDA_ERR_INVALID_ARG, "H, d_k, d_v must be positive");
-    if ((d_k != 64 && d_k != 128) || (d_v != 64 && d_v != 128))
-        return fail(KDA_ERR_UNSUPPORTED, "d_k, d_v must be 64 or 128 (got %d, %d)", d_k, d_v);
-    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
-    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
-    if (piece_tokens < 0 || piece_tokens % 64 != 0)
-        return fail(KDA_ERR_INVALID_ARG, "piece_tokens must be 0 or a positive multiple of 64 (got %d)",
-                    piece_tokens);
-    const bool any = (int64_t)B * T > 0;
-    if (any) {
-        if (!q || !k || !v || !beta || !o) return fail(KDA_ERR_INVALID_ARG, "q, k, v, beta and o must not be NULL");
-        if (gate != KDA_GATE_NONE && !alpha) return fail(KDA_ERR_INVALID_ARG, "alpha must not be NULL");
-    }
-    if (B == 0 || (T == 0 && !final_state)) return KDA_OK;
-    const Rows r = row_bytes(H, d_k, d_v, qkv_dtype, gate);
-    const int64_t piece = piece_tokens_for(B, T, r, piece_tokens);
-    const Layout L = layout(B, piece, H, d_k, d_v, r);
+// The pipeline shared by the host entry points; arguments already checked
+// except the workspace and the memory kinds.
+kda_status_t run_host(const Plan &pl, const char *const *names, const float *initial_state, void *o,
+                      float *final_state, int B, int T, int piece_tokens, void *workspace, size_t workspace_bytes,
+                      kda_stream_t stream, const Launcher &launch) {
+    const int64_t piece = piece_tokens_for(pl, B, T, piece_tokens);
+    const Layout L = layout(pl, B, piece);
     if (!workspace || workspace_bytes < L.total)
-        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes needed (kda_prefill_host_workspace_bytes)", L.total);
+        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes needed (the call's workspace_bytes function)", L.total);
     if (reinterpret_cast<uintptr_t>(workspace) & 15u)
         return fail(KDA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
 
-    // ---- buffers: host inputs and outputs, device workspace
     kda_status_t st;
-    const void *hosts[] = {q, k, v, alpha, beta, initial_state, o, final_state};
-    const char *names[] = {"q", "k", "v", "alpha", "beta", "initial_state", "o", "final_state"};
-    for (int i = 0; i < 8; ++i)
-        if ((st = need_host(hosts[i], names[i])) != KDA_OK) return st;
+    for (int i = 0; i < pl.nin; ++i)
+        if ((st = need_host(pl.in[i].src, names[i])) != KDA_OK) return st;
+    if ((st = need_host(initial_state, "initial_state")) != KDA_OK) return st;
+    if ((st = need_host(o, "o")) != KDA_OK) return st;
+    if ((st = need_host(final_state, "final_state")) != KDA_OK) return st;
     cudaPointerAttributes wat;
     cudaError_t e = cudaPointerGetAttributes(&wat, workspace);
     if (e != cudaSuccess) return cuda_fail(e, "pointer query");
@@ -214,7 +186,6 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_d
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     float *state = reinterpret_cast<float *>(ws + L.state);
-    const size_t state_bytes = (size_t)B * H * d_k * d_v * sizeof(float);
 
     // every queued step below is checked; on a failure the caller's stream
     // still waits for what was queued, so the workspace stays owned until then
@@ -225,7 +196,7 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_d
     };
     if (q_ok(cudaEventRecord(p.start, s), "event record") && q_ok(cudaStreamWaitEvent(p.in, p.start, 0), "wait") &&
         q_ok(cudaStreamWaitEvent(p.out, p.start, 0), "wait") && initial_state)
-        q_ok(cudaMemcpyAsync(state, initial_state, state_bytes, cudaMemcpyDefault, p.in), "initial state copy");
+        q_ok(cudaMemcpyAsync(state, initial_state, pl.state_bytes, cudaMemcpyDefault, p.in), "initial state copy");
     const int64_t npieces = T > 0 ? (T + piece - 1) / piece : 1;
     for (int64_t i = 0; i < npieces && st == KDA_OK; ++i) {
         const int slot = (int)(i % kRing);
@@ -235,35 +206,32 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_d
         // inputs of piece i into ring slot i % kRing, once the kernel that read
         // that slot before (piece i - kRing) is done
         if (i >= kRing && !q_ok(cudaStreamWaitEvent(p.in, p.ran[slot], 0), "wait")) break;
-        const struct {
-            size_t off;
-            const void *src;
-            size_t row;
-        } ins[] = {{L.q, q, r.qk}, {L.k, k, r.qk}, {L.v, v, r.v}, {L.a, alpha, r.a}, {L.b, beta, r.b}};
-        for (const auto &x : ins)
-            if (x.src && x.row && !q_ok(copy_rows(b + x.off, (size_t)len * x.row,
-                                                  static_cast<const char *>(x.src) + t0 * x.row, (size_t)T * x.row,
-                                                  (size_t)len * x.row, B, p.in),
-                                        "host-to-device copy"))
+        char *bufs[kMaxInputs];
+        for (int j = 0; j < pl.nin; ++j) {
+            const In &x = pl.in[j];
+            bufs[j] = x.row ? b + L.in[j] : nullptr;
+            if (x.src && x.row &&
+                !q_ok(copy_rows(bufs[j], (size_t)len * x.row, static_cast<const char *>(x.src) + t0 * x.row,
+                                (size_t)T * x.row, (size_t)len * x.row, B, p.in),
+                      "host-to-device copy"))
                 break;
+        }
         if (!q_ok(cudaEventRecord(p.copied[slot], p.in), "event record")) break;
         // the kernel of piece i: from the state the previous piece left (or the
         // caller's initial state), into the same state buffer
         if (!q_ok(cudaStreamWaitEvent(s, p.copied[slot], 0), "wait")) break;
         if (i >= kRing && !q_ok(cudaStreamWaitEvent(s, p.sent[slot], 0), "wait")) break;
         const float *s0 = (i == 0 && !initial_state) ? nullptr : state;
-        st = kda_prefill_gate(b + L.q, b + L.k, b + L.v, qkv_dtype, gate == KDA_GATE_NONE ? nullptr : (const float *)(b + L.a),
-                              gate, (const float *)(b + L.b), s0, b + L.o, state, B, len, H, d_k, d_v, algo, stream);
-        if (st != KDA_OK) break;
+        if ((st = launch(bufs, b + L.o, len, s0, state, stream)) != KDA_OK) break;
         if (!q_ok(cudaEventRecord(p.ran[slot], s), "event record")) break;
         // outputs of piece i back to the host
         if (!q_ok(cudaStreamWaitEvent(p.out, p.ran[slot], 0), "wait")) break;
-        if (!q_ok(copy_rows(static_cast<char *>(o) + t0 * r.o, (size_t)T * r.o, b + L.o, (size_t)len * r.o,
-                            (size_t)len * r.o, B, p.out),
+        if (!q_ok(copy_rows(static_cast<char *>(o) + t0 * pl.orow, (size_t)T * pl.orow, b + L.o,
+                            (size_t)len * pl.orow, (size_t)len * pl.orow, B, p.out),
                   "device-to-host copy"))
             break;
         if (i == npieces - 1 && final_state &&
-            !q_ok(cudaMemcpyAsync(final_state, state, state_bytes, cudaMemcpyDefault, p.out), "final state copy"))
+            !q_ok(cudaMemcpyAsync(final_state, state, pl.state_bytes, cudaMemcpyDefault, p.out), "final state copy"))
             break;
         if (!q_ok(cudaEventRecord(p.sent[slot], p.out), "event record")) break;
     }
@@ -273,6 +241,165 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_d
     if (st != KDA_OK) return st;
     if (e2 != cudaSuccess) return cuda_fail(e2, "joining the copy streams");
     return KDA_OK;
+}
+
+bool valid_gate(int gate) { return gate == KDA_GATE_CHANNEL || gate == KDA_GATE_SCALAR || gate == KDA_GATE_NONE; }
+
+size_t alpha_row(kda_gate_t gate, int H, int dk) {
+    return gate == KDA_GATE_CHANNEL ? (size_t)H * dk * 4 : gate == KDA_GATE_SCALAR ? (size_t)H * 4 : 0;
+}
+
+// ---- kda_prefill_host: q, k, v in qkv_dtype
+Plan plan_plain(const void *q, const void *k, const void *v, kda_dtype_t dt, const float *alpha, kda_gate_t gate,
+                const float *beta, int B, int H, int dk, int dv) {
+    const size_t es = dt == KDA_BF16 ? 2 : 4;
+    Plan pl{};
+    pl.nin = 5;
+    pl.in[0] = {q, (size_t)H * dk * es};
+    pl.in[1] = {k, (size_t)H * dk * es};
+    pl.in[2] = {v, (size_t)H * dv * es};
+    pl.in[3] = {alpha, alpha_row(gate, H, dk)};
+    pl.in[4] = {beta, (size_t)H * 4};
+    pl.orow = (size_t)H * dv * es;
+    pl.state_bytes = (size_t)B * H * dk * dv * sizeof(float);
+    return pl;
+}
+const char *const kPlainNames[] = {"q", "k", "v", "alpha", "beta"};
+
+struct PlainLauncher : Launcher {
+    kda_dtype_t dt;
+    kda_gate_t gate;
+    kda_algo_t algo;
+    int B, H, dk, dv;
+    kda_status_t operator()(char *const in[], void *o, int len, const float *s0, float *state,
+                            kda_stream_t s) const override {
+        return kda_prefill_gate(in[0], in[1], in[2], dt, reinterpret_cast<const float *>(in[3]), gate,
+                                reinterpret_cast<const float *>(in[4]), s0, o, state, B, len, H, dk, dv, algo, s);
+    }
+};
+
+bool valid_plain(kda_dtype_t dt, kda_gate_t gate, int B, int T, int H, int dk, int dv, int piece_tokens) {
+    return (dt == KDA_F32 || dt == KDA_BF16) && valid_gate(gate) && B >= 0 && T >= 0 && H > 0 &&
+           (dk == 64 || dk == 128) && (dv == 64 || dv == 128) && piece_tokens >= 0 && piece_tokens % 64 == 0 &&
+           (int64_t)B * T <= INT32_MAX;
+}
+
+// ---- kda_prefill_fp8_host: E4M3 codes and E8M0 block scales
+Plan plan_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, const uint8_t *qs, const uint8_t *ks,
+              const uint8_t *vs, const float *alpha, kda_gate_t gate, const float *beta, int B, int H, int dk,
+              int dv) {
+    Plan pl{};
+    pl.nin = 8;
+    pl.in[0] = {q, (size_t)H * dk};
+    pl.in[1] = {k, (size_t)H * dk};
+    pl.in[2] = {v, (size_t)H * dv};
+    pl.in[3] = {qs, (size_t)H * (dk / 32)};
+    pl.in[4] = {ks, (size_t)H * (dk / 32)};
+    pl.in[5] = {vs, (size_t)H * (dv / 32)};
+    pl.in[6] = {alpha, alpha_row(gate, H, dk)};
+    pl.in[7] = {beta, (size_t)H * 4};
+    pl.orow = (size_t)H * dv * 2;  // o is bf16
+    pl.state_bytes = (size_t)B * H * dk * dv * sizeof(float);
+    return pl;
+}
+const char *const kFp8Names[] = {"q", "k", "v", "q_scale", "k_scale", "v_scale", "alpha", "beta"};
+
+struct Fp8Launcher : Launcher {
+    kda_gate_t gate;
+    int B, H, dk, dv;
+    kda_status_t operator()(char *const in[], void *o, int len, const float *s0, float *state,
+                            kda_stream_t s) const override {
+        auto u8 = [&](int i) { return reinterpret_cast<const uint8_t *>(in[i]); };
+        return kda_prefill_fp8(u8(0), u8(1), u8(2), u8(3), u8(4), u8(5), reinterpret_cast<const float *>(in[6]),
+                               gate, reinterpret_cast<const float *>(in[7]), s0, o, state, B, len, H, dk, dv, s);
+    }
+};
+
+bool valid_fp8(kda_gate_t gate, int B, int T, int H, int dk, int dv, int piece_tokens) {
+    return valid_gate(gate) && B >= 0 && T >= 0 && H > 0 && dk == 128 && dv == 128 && piece_tokens >= 0 &&
+           piece_tokens % 64 == 0 && (int64_t)B * T <= INT32_MAX;
+}
+
+kda_status_t check_common(kda_gate_t gate, int B, int T, int H, int d_k, int d_v, int piece_tokens) {
+    if (!valid_gate(gate)) return fail(KDA_ERR_INVALID_ARG, "unknown gate kind %d", (int)gate);
+    if (H <= 0 || d_k <= 0 || d_v <= 0) return fail(KDA_ERR_INVALID_ARG, "H, d_k, d_v must be positive");
+    if ((d_k != 64 && d_k != 128) || (d_v != 64 && d_v != 128))
+        return fail(KDA_ERR_UNSUPPORTED, "d_k, d_v must be 64 or 128 (got %d, %d)", d_k, d_v);
+    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
+    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    if (piece_tokens < 0 || piece_tokens % 64 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "piece_tokens must be 0 or a positive multiple of 64 (got %d)",
+                    piece_tokens);
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,
+                                        kda_gate_t gate, int piece_tokens) {
+    if (!valid_plain(qkv_dtype, gate, B, T, H, d_k, d_v, piece_tokens)) return 0;
+    const Plan pl = plan_plain(nullptr, nullptr, nullptr, qkv_dtype, nullptr, gate, nullptr, B, H, d_k, d_v);
+    return layout(pl, B, piece_tokens_for(pl, B, T, piece_tokens)).total;
+}
+
+kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                              const float *alpha, kda_gate_t gate, const float *beta,
+                              const float *initial_state, void *o, float *final_state, int B, int T,
+                              int H, int d_k, int d_v, kda_algo_t algo, int piece_tokens, void *workspace,
+                              size_t workspace_bytes, kda_stream_t stream) {
+    // ---- argument checks, before any CUDA call
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16)
+        return fail(KDA_ERR_INVALID_ARG, "unknown qkv dtype %d", (int)qkv_dtype);
+    if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SIMT && algo != KDA_ALGO_TC)
+        return fail(KDA_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+    kda_status_t st;
+    if ((st = check_common(gate, B, T, H, d_k, d_v, piece_tokens)) != KDA_OK) return st;
+    if ((int64_t)B * T > 0) {
+        if (!q || !k || !v || !beta || !o) return fail(KDA_ERR_INVALID_ARG, "q, k, v, beta and o must not be NULL");
+        if (gate != KDA_GATE_NONE && !alpha) return fail(KDA_ERR_INVALID_ARG, "alpha must not be NULL");
+    }
+    if (B == 0 || (T == 0 && !final_state)) return KDA_OK;
+    const Plan pl = plan_plain(q, k, v, qkv_dtype, gate == KDA_GATE_NONE ? nullptr : alpha, gate, beta, B, H, d_k,
+                               d_v);
+    PlainLauncher launch;
+    launch.dt = qkv_dtype; launch.gate = gate; launch.algo = algo;
+    launch.B = B; launch.H = H; launch.dk = d_k; launch.dv = d_v;
+    return run_host(pl, kPlainNames, initial_state, o, final_state, B, T, piece_tokens, workspace, workspace_bytes,
+                    stream, launch);
+}
+
+size_t kda_prefill_fp8_host_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_gate_t gate,
+                                            int piece_tokens) {
+    if (!valid_fp8(gate, B, T, H, d_k, d_v, piece_tokens)) return 0;
+    const Plan pl = plan_fp8(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, gate, nullptr, B, H,
+                             d_k, d_v);
+    return layout(pl, B, piece_tokens_for(pl, B, T, piece_tokens)).total;
+}
+
+kda_status_t kda_prefill_fp8_host(const uint8_t *q, const uint8_t *k, const uint8_t *v, const uint8_t *q_scale,
+                                  const uint8_t *k_scale, const uint8_t *v_scale, const float *alpha,
+                                  kda_gate_t gate, const float *beta, const float *initial_state, void *o,
+                                  float *final_state, int B, int T, int H, int d_k, int d_v, int piece_tokens,
+                                  void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_common(gate, B, T, H, d_k, d_v, piece_tokens)) != KDA_OK) return st;
+    if (d_k != 128 || d_v != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "FP8 inputs need d_k = d_v = 128 (the tensor-core kernel)");
+    if ((int64_t)B * T > 0) {
+        if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !beta || !o)
+            return fail(KDA_ERR_INVALID_ARG, "q, k, v, their scales, beta and o must not be NULL");
+        if (gate != KDA_GATE_NONE && !alpha) return fail(KDA_ERR_INVALID_ARG, "alpha must not be NULL");
+    }
+    if (B == 0 || (T == 0 && !final_state)) return KDA_OK;
+    const Plan pl = plan_fp8(q, k, v, q_scale, k_scale, v_scale, gate == KDA_GATE_NONE ? nullptr : alpha, gate, beta,
+                             B, H, d_k, d_v);
+    Fp8Launcher launch;
+    launch.gate = gate;
+    launch.B = B; launch.H = H; launch.dk = d_k; launch.dv = d_v;
+    return run_host(pl, kFp8Names, initial_state, o, final_state, B, T, piece_tokens, workspace, workspace_bytes,
+                    stream, launch);
 }
 
 }  // extern "C"

@@ -200,3 +200,25 @@ def test_host_prefill_workspace_size(lib):
     full_in = B * T * H * (3 * 128 * 2 + 128 * 4 + 4)
     ws = f(B, T, H, 128, 128, 1, 0, 0)
     assert 0 < ws < full_in
+
+
+def test_fp8_host_prefill_argument_checks(lib):
+    """kda_prefill_fp8_host checks its arguments and workspace before any CUDA call."""
+    p = ctypes.c_void_p(0x1000)
+
+    def call(gate=0, B=1, T=64, H=1, dk=128, dv=128, piece=0, ws=p, nbytes=1 << 30, qs=p):
+        return lib.kda_prefill_fp8_host(p, p, p, qs, p, p, p, gate, p, None, p, None, B, T, H, dk, dv, piece,
+                                        ws, nbytes, None)
+
+    assert call(gate=5) == 1
+    assert call(dk=64) == 2 and b"128" in lib.kda_last_error()
+    assert call(piece=96) == 1
+    assert call(qs=None) == 1
+    assert call(ws=None) == 5
+    assert call(B=0) == 0
+    f = lib.kda_prefill_fp8_host_workspace_bytes
+    # B=1, T=64, H=1, d=128, channel gate, pieces of 64: q, k, v 64*128 = 8192 B
+    # each; scales 64*4 = 256 each; alpha 64*512 = 32768; beta 256; o (bf16)
+    # 16384; state 65536
+    assert f(1, 64, 1, 128, 128, 0, 64) == 3 * (3 * 8192 + 3 * 256 + 32768 + 256 + 16384) + 65536
+    assert f(1, 64, 1, 64, 128, 0, 64) == 0

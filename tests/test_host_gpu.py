@@ -202,3 +202,41 @@ def test_concurrent_host_calls_from_two_threads(kda):
     assert not errors, errors
     for (o, s), (o_r, s_r) in zip(got, ref):
         assert torch.equal(o, o_r) and torch.equal(s, s_r)
+
+
+def _fp8(x, d):
+    out = []
+    for t in (x.q, x.k, x.v):
+        c, sc, _ = W.to_mxfp8(t)
+        out += [c.to(d), sc.to(d)]
+    return out  # cq, sq, ck, sk, cv, sv
+
+
+@pytest.mark.parametrize("gate", ["channel", "none"])
+def test_fp8_pieces_are_the_device_piece_loop_bit_for_bit(kda, gate):
+    """FP8 inputs from host memory in pieces of 128 tokens over T = 300: the
+    bits of kda_prefill_fp8 run piece by piece on the device."""
+    x = W.batched(2, 300, 2, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=71)
+    cq, sq, ck, sk, cv, sv = _fp8(x, torch.device("cpu"))
+    a = _alpha(x, gate)
+    pin = lambda t: None if t is None else t.pin_memory()  # noqa: E731
+    o_h, s_h = kda.prefill_fp8(pin(cq), pin(ck), pin(cv), pin(sq), pin(sk), pin(sv), pin(a), pin(x.beta),
+                               pin(x.initial_state), gate=gate, piece_tokens=128)
+    assert o_h.is_pinned() and s_h.is_pinned()
+    d = torch.device("cuda")
+    s = x.initial_state.to(d)
+    outs = []
+    for t0 in range(0, 300, 128):
+        sl = slice(t0, min(300, t0 + 128))
+        part = [t[:, sl].contiguous().to(d) for t in (cq, ck, cv, sq, sk, sv)]
+        ap = None if a is None else a[:, sl].contiguous().to(d)
+        o, s = kda.prefill_fp8(*part, ap, x.beta[:, sl].contiguous().to(d), s, gate=gate)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, torch.cat(outs, 1).cpu()) and torch.equal(s_h, s.cpu())
+    # one piece: the single device call
+    o1, s1 = kda.prefill_fp8(pin(cq), pin(ck), pin(cv), pin(sq), pin(sk), pin(sv), pin(a), pin(x.beta),
+                             pin(x.initial_state), gate=gate, piece_tokens=0)
+    part = [t.to(d) for t in (cq, ck, cv, sq, sk, sv)]
+    o_d, s_d = kda.prefill_fp8(*part, None if a is None else a.to(d), x.beta.to(d), x.initial_state.to(d), gate=gate)
+    assert torch.equal(o1, o_d.cpu()) and torch.equal(s1, s_d.cpu())
