@@ -183,9 +183,10 @@ kda_status_t kda_varlen_prefill_noalloc(const void *q, const void *k, const void
  * Ordering: everything is queued after the work already on `stream`, and work
  * queued on `stream` afterwards starts once o and final_state are in host
  * memory; synchronise `stream` before reading them. The call returns once all
- * copies are queued (sooner than that only if host memory is pageable: the
- * driver then copies synchronously, which is correct but does not overlap).
- * Page-locked host memory gives the overlap. The first call on a device
+ * copies are queued. With pageable host memory the driver copies
+ * synchronously, so the call returns only after those copies, and nothing
+ * overlaps; the result is the same. Page-locked host memory gives the
+ * overlap. The first call on a device
  * creates two copy streams and a few events that live until the process
  * exits; calls are serialised by a lock while they queue their work.
  *
