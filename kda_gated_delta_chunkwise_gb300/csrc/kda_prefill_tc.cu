@@ -498,7 +498,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 // this CTA's key half of k and q (raw; the gate transforms them in place)
                 if (n >= NSLOT && !wait_bar(s, p, B_QK_EMPTY + b, (kk - 1) & 1)) break;
                 unsigned char *a0 = s.base + SM_A0 + b * 32768 + rank * 16384;
-                if constexpr (FP8) {  // codes into the Qr half (64-byte rows); the gate reads them first
+                if constexpr (FP8) {  // codes into the Qr half (64-byte rows); warp 15 makes the bf16 tiles
                     mbar_arrive_expect_tx(s.bar(B_QK_FULL + b), 8192);
                     tma_load_3d(a0 + 8192, &tm_k, s.bar(B_QK_FULL + b), c0, h, z);
                     tma_load_3d(a0 + 12288, &tm_q, s.bar(B_QK_FULL + b), c0, h, z);
@@ -660,8 +660,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 alive = ok;
             }
         }
-    } else if (warp >= 12) {
-        // idle warp of the control warpgroup
     } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue
         regs_inc<REGS_EPI>();
