@@ -142,7 +142,7 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * callers that must not allocate device memory (engines whose device memory
  * is planned up front and may not grow on the request path, plug-ins that
  * are handed only the call's tensors, paths where an allocation would
- * synchronise). The paper has no counterpart: this is an interface choice.
+ * synchronise). The method has no counterpart: this is an interface choice.
  *
  * Arguments, layouts and results are those of kda_varlen_prefill. The small
  * scratch it needs (sequence order, work counter, status word) is a fixed
