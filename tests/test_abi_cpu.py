@@ -222,3 +222,17 @@ def test_fp8_host_prefill_argument_checks(lib):
     # 16384; state 65536
     assert f(1, 64, 1, 128, 128, 0, 64) == 3 * (3 * 8192 + 3 * 256 + 32768 + 256 + 16384) + 65536
     assert f(1, 64, 1, 64, 128, 0, 64) == 0
+
+
+def test_host_prefill_picks_pieces_of_about_32_mib(lib):
+    """The library's own piece size on the benchmark shape (4 x 16 x 4096,
+    bf16, per-channel gate): 20,544 input bytes per token row, so eleven
+    pieces of at most 32 MiB, each 384 tokens (whole chunks); the workspace is
+    that of explicit 384-token pieces."""
+    f = lib.kda_prefill_host_workspace_bytes
+    assert f(4, 4096, 16, 128, 128, 1, 0, 0) == f(4, 4096, 16, 128, 128, 1, 0, 384)
+    assert f(4, 4096, 16, 128, 128, 1, 0, 0) != f(4, 4096, 16, 128, 128, 1, 0, 448)
+    row = 4 * (3 * 16 * 128 * 2 + 16 * 128 * 4 + 16 * 4)
+    assert 384 * row <= 32 << 20 < 448 * row
+    # a small input is one piece: the workspace holds T tokens
+    assert f(1, 300, 2, 128, 128, 1, 0, 0) == f(1, 300, 2, 128, 128, 1, 0, 320)
