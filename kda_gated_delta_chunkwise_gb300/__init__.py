@@ -7,9 +7,9 @@ Per sequence and head, S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1}
 Entry points (thin ctypes binding over the C ABI in include/kda.h):
 ``prefill`` (per-channel, scalar or no gate), ``prefill_fp8`` (MX-style FP8
 q, k, v), ``varlen_prefill``,
-``decode_step``; host (CPU) tensors given to ``prefill`` go through the
-native host-buffer pipeline (kda_prefill_host); and for serving with a pool
-of states indexed by slot:
+``decode_step``; host (CPU) tensors given to ``prefill`` or ``prefill_fp8``
+go through the native host-buffer pipeline (kda_prefill_host,
+kda_prefill_fp8_host); and for serving with a pool of states indexed by slot:
 ``varlen_prefill_slots``, ``decode_step_slots``. Build the CUDA library with
 ``kda_gated_delta_chunkwise_gb300.build.build()`` first.
 """
