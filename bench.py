@@ -14,7 +14,13 @@ Prints ONE JSON line (rank 0). Keys beyond the basic contract:
   e2e           the same metric through the public API with host buffers,
                 host<->device copies inside the timed region
   decode        the decode step on 256 sequences x 32 heads (state GB/s)
+  long_context  prefill of one 131,072-token sequence with 32 heads
+  varlen        packed prefill of 64 lognormal-length sequences (306,055
+                tokens, 16 heads), and varlen_1m: the same lengths scaled to
+                2^20 tokens
+  gate_variants the benchmark workload with a scalar gate, no gate, FP8 inputs
   clocks        SM clocks and throttle reasons sampled during the timed region
+                (and during about a second of the same steps just before it)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torchrun (one process per GPU, independent batches:
@@ -189,11 +195,123 @@ def cpu_baseline_oracle(target_s: float = 12.0):
 
     Ts = 64
     dt = run(Ts)
-    Ts = int(min(4096, max(64, Ts * target_s / max(dt, 1e-3))))
-    dt = run(Ts)
+    Ts = int(min(T, max(64, Ts * target_s / max(dt, 1e-3))))
+    reps, total = 0, 0.0
+    while reps == 0 or total < 0.5 * target_s:  # the whole workload is shorter: repeat it
+        total += run(Ts)
+        reps += 1
+    dt = total / reps
     return {"value": B * Ts / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"B={B} x H={H} (all 64 sequence-head pairs) x first {Ts} of {T} tokens, "
-                      f"d={DK}, float64, {dt:.1f} s"}
+                      f"d={DK}, float64, {reps} run(s), {total:.1f} s in all"}
+
+
+def time_events(fn, steps: int, warmup: int, stream) -> float:
+    """Mean CUDA-event time (ms) of ``fn`` over ``steps`` launches after
+    ``warmup`` untimed ones, events recorded on ``stream`` (the launching
+    stream)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s_, e_ in ev:
+        s_.record(stream)
+        fn()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(s_.elapsed_time(e_) for s_, e_ in ev)
+
+
+def oracle_tokens_per_s(x, n_tokens_of, sample: str, target_s: float = 4.0, lib=None):
+    """The float64 oracle on a bounded sample of a workload: ``n_tokens_of(Ts)``
+    gives the oracle inputs (and token count) for the first Ts tokens of every
+    sequence; Ts is chosen so the run takes about ``target_s`` seconds."""
+    import oracle
+    lib = lib or oracle.load()
+
+    def run(Ts):
+        args, kw, ntok = n_tokens_of(Ts)
+        t0 = time.perf_counter()
+        oracle.run(*args, **kw, lib=lib)
+        return time.perf_counter() - t0, ntok
+
+    Ts = 64
+    dt, _ = run(Ts)
+    Ts = max(64, int(Ts * target_s / max(dt, 1e-3)) // 64 * 64)
+    dt, ntok = run(Ts)
+    return {"value": ntok / dt, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": sample.format(Ts=Ts) + f", float64, {dt:.1f} s"}
+
+
+def bench_long_context(kda, W, dev, stream, peaks, steps, warmup, with_cpu):
+    """One 131,072-token sequence with 32 heads (split decay scales, S0 given):
+    the case where a sequence is far longer than the batch is wide, so the
+    per-chunk state chain of each head sets the time."""
+    x = W.prefill_long_131k()
+    q, k, v, a, b, s0 = (t.to(dev) for t in (*x.tensors(), x.initial_state))
+    Bl, Tl, Hl = 1, x.q.shape[1], x.q.shape[2]
+    o = torch_empty_like(v)
+    sT = torch_empty_like(s0)
+    ms = time_events(lambda: kda.prefill(q, k, v, a, b, s0, out=o, final_state=sT), steps, warmup, stream)
+    nbytes = prefill_bytes(Bl, Tl, Hl, DK, DV, with_s0=True)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": f"kda_prefill B=1 H={Hl} T={Tl} d_k={DK} d_v={DV} chunk={CHUNK}, bf16 q/k/v, "
+                       "alpha scales 1e-4 / 0.2 per half of the key channels, S0 ~ N(0, 0.01^2)",
+           "value": Bl * Tl / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+           "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+           "kernel": "kda_prefill_tc", "clusters": Bl * Hl}
+    del q, k, v, a, b, o, sT
+    if with_cpu:
+        res["cpu_baseline"] = oracle_tokens_per_s(
+            x, lambda Ts: ([t[:, :Ts] for t in x.tensors()], {"initial_state": x.initial_state}, Ts),
+            "all 32 heads x first {Ts} of 131072 tokens")
+    return res
+
+
+def bench_varlen(kda, W, x, dev, stream, peaks, steps, warmup, with_cpu, label):
+    """Packed prefill (kda_varlen_prefill) of the lognormal 64-sequence batch."""
+    (q, k, v, a, b), cu, s0 = [t.to(dev) for t in x.tensors()], x.cu_seqlens.to(dev), x.initial_state.to(dev)
+    N, Tt, Hv = x.num_seqs, x.q.shape[0], x.q.shape[1]
+    o = torch_empty_like(v)
+    sT = torch_empty_like(s0)
+    ws = torch_empty_bytes(kda.varlen_workspace_bytes(N, Hv), dev)
+    ms = time_events(lambda: kda.varlen_prefill(q, k, v, a, b, cu, s0, out=o, final_state=sT, workspace=ws),
+                     steps, warmup, stream)
+    # every token-head's inputs and o, plus each sequence's S0 read and final state written
+    nbytes = prefill_bytes(1, Tt, Hv, DK, DV) - Hv * DK * DV * 4 + 2 * N * Hv * DK * DV * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    L = (x.cu_seqlens[1:] - x.cu_seqlens[:-1]).tolist()
+    res = {"workload": f"kda_varlen_prefill N={N} T_total={Tt} H={Hv} d_k={DK} d_v={DV}, {label}, "
+                       f"lengths {min(L)}..{max(L)}, bf16 q/k/v, per-sequence S0 ~ N(0, 0.01^2)",
+           "value": Tt / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+           "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+           "kernel": "kda_prefill_tc (+ kda_varlen_prep)", "clusters": N * Hv}
+    del q, k, v, a, b, o, sT, cu, s0, ws
+    if with_cpu:
+        cuh = x.cu_seqlens.tolist()
+
+        def first(Ts):
+            # the first Ts tokens of every sequence, packed
+            idx = [(cuh[n], min(cuh[n + 1], cuh[n] + Ts)) for n in range(N)]
+            cut = [0]
+            for lo, hi in idx:
+                cut.append(cut[-1] + hi - lo)
+            import torch
+            args = [torch.cat([t[lo:hi] for lo, hi in idx]) for t in x.tensors()]
+            return args, {"cu_seqlens": cut, "initial_state": x.initial_state}, cut[-1]
+        res["cpu_baseline"] = oracle_tokens_per_s(x, first, "all 64 sequences x 16 heads, first {Ts} tokens of each")
+    return res
+
+
+def torch_empty_like(t):
+    import torch
+    return torch.empty_like(t)
+
+
+def torch_empty_bytes(n, dev):
+    import torch
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=dev)
 
 
 def bench_config(world: int) -> dict:
@@ -213,10 +331,16 @@ def run_reference(args):
     from kda_gated_delta_chunkwise_gb300 import workloads as W
 
     x = W.prefill_4x16x4096(T=4096)
-    Ts = 128
-    sl = [t[:, :Ts] for t in x.tensors()]
     lib = oracle.load()
     cores = oracle.max_threads()
+    # tokens per step: the whole sequence length when a step of it takes at
+    # most about 2 s on these cores (so K + W steps end within minutes),
+    # else the first Ts tokens of every sequence
+    t0 = time.perf_counter()
+    oracle.run(*[t[:, :256] for t in x.tensors()], lib=lib)
+    per_tok = (time.perf_counter() - t0) / 256
+    Ts = int(min(T, max(64, 2.0 / max(per_tok, 1e-9) // 64 * 64)))
+    sl = [t[:, :Ts] for t in x.tensors()]
     for _ in range(args.warmup):
         oracle.run(*sl, lib=lib)
     t0 = time.perf_counter()
@@ -228,7 +352,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(bench_config(args.gpus), sample=f"each step: all 64 sequence-head pairs, first {Ts} tokens"),
+            "config": dict(bench_config(args.gpus),
+                           sample=f"each step: all 64 sequence-head pairs, first {Ts} of {T} tokens"),
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"B={B} x H={H} x first {Ts} tokens per step"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -246,6 +371,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the long-context and packed-batch legs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -285,6 +411,13 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
+    # about a second of the same steps (untimed) right before the timed
+    # region, so that the clock samples (every 200 ms) cover this load
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
@@ -300,6 +433,8 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
+    if clk:
+        clk["window"] = "about 1 s of the same steps, untimed, then the timed region"
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
     total_ms = max_over_ranks(total_ms, world, dev)
@@ -420,29 +555,56 @@ def main():
         del q, k, v, a, b, o, sT
         xd = W.decode_256x32(seed=shard_seed(rank))
         dq, dk_, dv_, da, db = (t.to(dev) for t in xd.tensors())
-        state = xd.initial_state.to(dev)
+        # two state batches used in turn (1 GiB together, 8x the L2): a step
+        # never finds its state, or the previous step's dirty lines of it, in L2
+        states = [xd.initial_state.to(dev), xd.initial_state.to(dev)]
         do = torch.empty_like(dv_)
+        it = [0]
+
+        def dstep():
+            kda.decode_step(dq, dk_, dv_, da, db, states[it[0] & 1], out=do)
+            it[0] += 1
         for _ in range(args.warmup):
-            kda.decode_step(dq, dk_, dv_, da, db, state, out=do)
+            dstep()
         torch.cuda.synchronize()
         evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         for i in range(args.steps):
             evd[i][0].record(stream)
-            kda.decode_step(dq, dk_, dv_, da, db, state, out=do)
+            dstep()
             evd[i][1].record(stream)
         torch.cuda.synchronize()
         dms = statistics.median(s.elapsed_time(e) for s, e in evd)
         dbytes = decode_bytes(DEC_N, DEC_H, DK, DV)
         gbs = dbytes / (dms / 1e3) / 1e9
+        dtraffic = kernel_traffic("kda_decode.cu", "decode")
         decode = {"metric": "decode step state GB/s", "value": gbs, "unit": "GB/s",
                   "ms_per_step": dms, "frac": gbs / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
                   "algorithmic_bytes_per_step": dbytes,
-                  "traffic": kernel_traffic("kda_decode.cu", "decode"),
-                  "workload": f"{DEC_N} sequences x {DEC_H} heads, d={DK}, bf16 q/k/v, fp32 state in place"}
+                  "traffic": dtraffic,
+                  "dram_gbs_from_traffic": None if dtraffic is None else dtraffic / (dms / 1e3) / 1e9,
+                  "note": "the peak is a plain copy; this kernel streams half the bytes of that copy "
+                          "per launch and can sit a hair above it",
+                  "workload": f"{DEC_N} sequences x {DEC_H} heads, d={DK}, bf16 q/k/v, fp32 state in place, "
+                              "two state batches in turn"}
+        del states, dq, dk_, dv_, da, db, do
+
+    long_ctx = varlen = varlen_1m = None
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if not args.no_long:
+        torch.cuda.empty_cache()
+        long_ctx = bench_long_context(kda, W, dev, stream, peaks, args.steps, args.warmup, with_cpu)
+        torch.cuda.empty_cache()
+        varlen = bench_varlen(kda, W, W.varlen_64seq(seed=shard_seed(rank)), dev, stream, peaks, args.steps,
+                              args.warmup, with_cpu, "lengths round(lognormal(8, 1)) clipped to [512, 32768]")
+        torch.cuda.empty_cache()
+        varlen_1m = bench_varlen(kda, W, W.varlen_64seq_1m(seed=shard_seed(rank)), dev, stream, peaks,
+                                 max(3, args.steps // 2), args.warmup, with_cpu,
+                                 "the same lengths scaled to 2^20 tokens and re-clipped")
+        torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if with_cpu:
         cpu = cpu_baseline_oracle()
 
     if rank == 0:
@@ -452,6 +614,7 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": bench_config(world),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+                "long_context": long_ctx, "varlen": varlen, "varlen_1m": varlen_1m,
                 "gate_variants": variants,
                 "gpu_launches": args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)

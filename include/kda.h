@@ -134,6 +134,13 @@ kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda
                                 int d_v, void *workspace, size_t workspace_bytes,
                                 int32_t *device_status, kda_stream_t stream);
 
+/* Workspace bytes kda_prefill, kda_prefill_ex, kda_prefill_gate and
+ * kda_prefill_fp8 need: always 0. Equal-length sequences need no scratch (the
+ * state of every chunk stays on chip), so those calls take no workspace
+ * argument; the function exists so that callers that size workspaces
+ * generically can treat every prefill alike. */
+size_t kda_prefill_workspace_bytes(int B, int T, int H, int d_k, int d_v);
+
 /* Workspace bytes kda_varlen_prefill needs for N sequences (0 < result). */
 size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
 
@@ -151,6 +158,8 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * and larger N is rejected with KDA_ERR_UNSUPPORTED before anything runs.
  * The first call on a device looks up that array's device address once
  * (with the device current); make this first call before any stream capture.
+ * The address is kept until the process exits, so do not use this entry
+ * point on a device after cudaDeviceReset.
  * All calls share the one array and each call rewrites what it uses, so calls
  * that overlap on the GPU (different streams, or different host threads on
  * the same device) race and must be serialised by the caller.
@@ -324,6 +333,23 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
  * int). reset != 0 clears the word after reading.
  */
 kda_status_t kda_device_errors(int *errors, int reset);
+
+/*
+ * kda_selftest_bounded_wait - diagnostic with no counterpart in the method:
+ * runs the tensor-core prefill on one bf16 sequence of one head (B = H = 1,
+ * d_k = d_v = 128, T tokens, zero initial state; tensors as for kda_prefill)
+ * with its state chain made to wait, at chunk `stall_chunk`, on a barrier
+ * that nothing ever completes. Every wait of the kernel is bounded: this one
+ * gives up after about a second, the kernel's other groups give up on the
+ * waits that depended on it, the kernel records a nonzero device error word
+ * (see kda_device_errors) and returns. Its o and final_state are then
+ * invalid. It exists so that a test can show that a stuck wait ends in an
+ * error status, with the GPU context still usable, instead of a hang.
+ * stall_chunk must lie in [0, ceil(T / 64)); KDA_ERR_INVALID_ARG otherwise.
+ */
+kda_status_t kda_selftest_bounded_wait(const void *q, const void *k, const void *v, const float *alpha,
+                                       const float *beta, void *o, float *final_state, int T, int stall_chunk,
+                                       kda_stream_t stream);
 
 /* Message of the last failing call on this thread ("" if none). */
 const char *kda_last_error(void);

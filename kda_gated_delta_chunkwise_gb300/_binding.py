@@ -29,7 +29,8 @@ KDA_DEV_OK, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT = 0, 1, 2
 EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8", "kda_prefill_host",
            "kda_prefill_host_workspace_bytes", "kda_prefill_fp8_host", "kda_prefill_fp8_host_workspace_bytes",
            "kda_varlen_prefill", "kda_varlen_prefill_slots",
-           "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_decode_step", "kda_decode_step_slots",
+           "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_prefill_workspace_bytes",
+           "kda_decode_step", "kda_decode_step_slots", "kda_selftest_bounded_wait",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
 _lock = threading.Lock()
@@ -87,6 +88,10 @@ def load(path: str | None = None):
         lib.kda_varlen_prefill_slots.restype = i
         lib.kda_decode_step_slots.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, i, vp, i, i, i, i, vp, vp]
         lib.kda_decode_step_slots.restype = i
+        lib.kda_prefill_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_prefill_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.kda_selftest_bounded_wait.restype = i
+        lib.kda_selftest_bounded_wait.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, vp]
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
         lib.kda_abi_version.restype = ctypes.c_int
@@ -105,6 +110,34 @@ def device_errors(reset: bool = True) -> int:
     v = ctypes.c_int(0)
     _check(lib, lib.kda_device_errors(ctypes.byref(v), int(reset)))
     return v.value
+
+
+def selftest_bounded_wait(q, k, v, alpha, beta, stall_chunk: int, *, stream=None):
+    """Diagnostic: the tensor-core prefill of one bf16 sequence of one head
+    (q, k, v [T, 128], alpha [T, 128], beta [T]) with its state chain stalled
+    at chunk ``stall_chunk`` on a wait that never completes. The kernel gives
+    up after about a second and returns; read the outcome with
+    :func:`device_errors`. Returns the (invalid) o and final state."""
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(alpha, "alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    T = q.shape[0]
+    if q.shape != (T, 128) or k.shape != q.shape or v.shape != q.shape or alpha.shape != q.shape \
+            or beta.shape != (T,):
+        raise ValueError("q, k, v, alpha must be [T, 128] and beta [T]")
+    o = torch.empty_like(v)
+    s = torch.empty((128, 128), dtype=torch.float32, device=dev)
+    _check(lib, lib.kda_selftest_bounded_wait(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o), _ptr(s),
+                                              T, int(stall_chunk), _stream(stream)))
+    return o, s
+
+
+def prefill_workspace_bytes(B: int, T: int, H: int, dk: int = 128, dv: int = 128) -> int:
+    """Device scratch the equal-length prefill needs: always 0."""
+    return int(load().kda_prefill_workspace_bytes(B, T, H, dk, dv))
 
 
 def _check(lib, status: int):

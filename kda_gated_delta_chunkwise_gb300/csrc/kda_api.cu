@@ -57,6 +57,15 @@ kda_status_t check_dtype(kda_dtype_t dt) {
             return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);             \
     } while (0)
 
+// Every prefill kernel launches one CTA per (sequence, head, value slice),
+// at most two slices of 64 columns for d_v = 128: the grid must stay within
+// the 2^31 - 1 blocks of one launch.
+kda_status_t check_grid(int64_t n_seqs, int H) {
+    if (n_seqs * H * 2 > INT32_MAX)
+        return fail(KDA_ERR_UNSUPPORTED, "N * H * 2 must fit in int32 (got N = %lld, H = %d)", (long long)n_seqs, H);
+    return KDA_OK;
+}
+
 kda_status_t check_gate(int gate) {
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_SCALAR && gate != KDA_GATE_NONE)
         return fail(KDA_ERR_INVALID_ARG, "unknown gate kind %d", gate);
@@ -130,6 +139,7 @@ kda_status_t kda_prefill_gate(const void *q, const void *k, const void *v, kda_d
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
     if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
     if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    if ((st = check_grid(B, H)) != KDA_OK) return st;
     if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state,
                             (int64_t)B * T > 0, gate)) != KDA_OK)
         return st;
@@ -158,6 +168,7 @@ kda_status_t kda_prefill_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *
         return fail(KDA_ERR_UNSUPPORTED, "FP8 inputs need d_k = d_v = 128 (the tensor-core kernel)");
     if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
     if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    if ((st = check_grid(B, H)) != KDA_OK) return st;
     if ((st = check_tensors(q, k, v, alpha, beta, o, initial_state, final_state, (int64_t)B * T > 0, gate)) !=
         KDA_OK)
         return st;
@@ -195,6 +206,11 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, kda_dtype_
                           d_k, d_v, KDA_ALGO_AUTO, stream);
 }
 
+size_t kda_prefill_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
+    (void)B; (void)T; (void)H; (void)d_k; (void)d_v;
+    return 0;  // the equal-length prefill keeps everything on chip
+}
+
 size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v) {
     (void)H; (void)d_k; (void)d_v;
     const size_t n = N > 0 ? (size_t)N : 0;
@@ -217,6 +233,7 @@ kda_status_t varlen_prefill(const void *q, const void *k, const void *v, kda_dty
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
     if (N < 0 || T_total < 0) return fail(KDA_ERR_INVALID_ARG, "N and T_total must be >= 0");
     if (N == 0) return ok();
+    if ((st = check_grid(N, H)) != KDA_OK) return st;
     if (!cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
         return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
@@ -277,6 +294,24 @@ kda_status_t kda_varlen_prefill_slots(const void *q, const void *k, const void *
     return varlen_prefill(q, k, v, qkv_dtype, alpha, gate, beta, state_pool, o, state_pool, slots, pool_size,
                           cu_seqlens, N, T_total, H, d_k, d_v, workspace, workspace_bytes, device_status,
                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_selftest_bounded_wait(const void *q, const void *k, const void *v, const float *alpha,
+                                       const float *beta, void *o, float *final_state, int T, int stall_chunk,
+                                       kda_stream_t stream) {
+    kda_status_t st;
+    if (T <= 0) return fail(KDA_ERR_INVALID_ARG, "T must be positive (got %d)", T);
+    if (stall_chunk < 0 || (int64_t)stall_chunk * 64 >= T)
+        return fail(KDA_ERR_INVALID_ARG, "stall_chunk must name one of the %d chunks", (T + 63) / 64);
+    if ((st = check_tensors(q, k, v, alpha, beta, o, nullptr, final_state, true)) != KDA_OK) return st;
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.s0 = nullptr;
+    a.o = o; a.sT = final_state; a.cu_seqlens = nullptr;
+    a.gate = KDA_GATE_CHANNEL; a.slots = nullptr;
+    a.N = 1; a.T = T; a.H = 1; a.dk = 128; a.dv = 128; a.dt = KDA_BF16;
+    a.order = nullptr; a.counter = nullptr; a.dev_status = nullptr;
+    a.stall1 = stall_chunk + 1;
+    return cuda_status(kda::launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream)), "self-test launch");
 }
 
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,

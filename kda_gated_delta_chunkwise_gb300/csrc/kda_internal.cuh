@@ -62,6 +62,8 @@ struct PrefillArgs {
     const int32_t *order;       // nullable: sequence order (longest first)
     int32_t *counter;           // nullable: persistent work counter
     const int32_t *dev_status;  // nullable: skip all work when *dev_status != 0
+    int stall1;                 // self-test of the tensor-core kernel's bounded waits: 1 + the
+                                // chunk at which its state chain stops (0, the default: never)
 };
 
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);

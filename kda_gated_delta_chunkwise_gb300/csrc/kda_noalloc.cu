@@ -33,7 +33,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does it).
+// per device (the first call on a device does it) and kept for the life of
+// the process. cudaDeviceReset destroys the context that address belongs to,
+// so this entry point must not be used on a device after it was reset.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -405,6 +405,7 @@ template <int DK, typename TIn>
 cudaError_t launch_simt_t(const PrefillArgs &a, cudaStream_t s) {
     const int64_t blocks = (int64_t)a.N * a.H * (a.dv / VS);
     if (blocks == 0) return cudaSuccess;
+    if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(SimtSmem<DK>);
     auto kern = kda_prefill_simt_kernel<DK, TIn>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -113,7 +113,7 @@ constexpr uint32_t SM_RU = 212992;     // 8 KB: R then U (MN-major, 64 rows x 64
 constexpr uint32_t SM_MU = 221184;     // float[3][128]
 constexpr uint32_t SM_BETA = 222720;   // float[3][64]
 constexpr uint32_t SM_VOTE = 223488;   // int[3][8]: slow vote of key half 0 at [0], half 1 at [4]
-constexpr uint32_t SM_FLAGS = 223584;  // int[8]: [1] abort
+constexpr uint32_t SM_FLAGS = 223584;  // int[8]: [1] abort, [2] the peer's abort flag at exit
 constexpr uint32_t SM_TMEM = 223616;   // uint32 TMEM base
 constexpr uint32_t SM_BAR = 223632;    // mbarriers (up to 40)
 constexpr uint32_t SM_RED = 223952;    // float[4][64] + float[64]: slow-path reductions
@@ -139,7 +139,8 @@ enum Bar {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_TAB_FULL = 7, B_B0_EMPTY = 13, B_O_READ = 16,
     B_AP_FULL = 18, B_T_FULL = 20, B_T_EMPTY = 21, B_P_FULL = 23, B_P_EMPTY = 25, B_S_FULL = 27, B_XY_FULL = 28,
     B_R_FULL = 29, B_U_FULL = 30, B_UU_FULL = 31, B_D_FULL = 32, B_DRAIN = 33, B_DRAIN_AUX = 34, B_DQ_FULL = 35,
-    B_COUNT = 38
+    B_STALL = 38,  // self-test only: nothing ever arrives on it
+    B_COUNT = 39
 };
 static_assert(B_COUNT <= 40, "mbarrier area");
 
@@ -156,6 +157,8 @@ struct TcParams {
     int gate;              // kda_gate_t
     const uint8_t *qs, *ks, *vs;  // FP8 inputs: E8M0 scales, one per 32 channels (q, k, v are E4M3)
     int N, T, H;
+    int stall1;  // self-test of the bounded waits: 1 + the chunk at which the state-chain
+                 // issuer waits on B_STALL (0: never)
 };
 
 // FP8 inputs (the MX block format): E4M3 codes, a power-of-two scale 2^(t-127)
@@ -471,6 +474,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         mbar_init(s.bar(B_D_FULL), 1);
         mbar_init(s.bar(B_DRAIN), 1);
         mbar_init(s.bar(B_DRAIN_AUX), 1);
+        mbar_init(s.bar(B_STALL), 1);
         for (int i = 0; i < 8; ++i) s.flags()[i] = 0;
         fence_mbar_init();
     }
@@ -525,6 +529,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             bool ok = true;
             for (int n = 0; ok && n < NC; ++n) {
                 const int b = n & 1, kk = n >> 1, b3 = n % NSLOT;
+                if (n + 1 == p.stall1 && !(ok = wait_bar(s, p, B_STALL, 0))) break;
                 if (!(ok = wait_bar(s, p, B_TAB_FULL + n % NTAB, (n / NTAB) & 1))) break;
                 const bool fast = !s.slow(b3);
                 const uint32_t xy = tmem + TM_XY + 64 * b, uo = tmem + TM_UO + 64 * b;
@@ -814,7 +819,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                 tc_fence_before();
                 mbar_arrive(s.bar(B_R_FULL));
                 named_bar(4, 64);  // both E1 warps have read v: load the next chunk's
-                if (tid == 0 && n + 1 < NC) {
+                if (tid == 0 && n + 1 < NC && ok) {  // (no new copies once this thread gave up)
                     mbar_arrive_expect_tx(s.bar(B_V_FULL), FP8 ? 4096 : 8192);
                     tma_load_3d(s.base + SM_V, &tm_v, s.bar(B_V_FULL), v0, h, (int)(tok0 + C));
                 }
@@ -1304,8 +1309,21 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
     }
 
     if (tid == 0 && (s.flags()[1] & 2)) atomicOr(p.err ? p.err : &g_tc_error, 2);  // a wait here timed out
+    __syncthreads();  // every thread of this CTA is done: its abort flag is final
+    if (tid == 0) st_cluster_u32(s.remote(s.base + SM_FLAGS + 8), (uint32_t)s.flags()[1]);  // the peer's flags[2]
     tc_fence_before();
     cluster_sync();  // neither CTA leaves while the other may still write into it
+    // After a timeout some groups skipped the waits that would have seen their
+    // last copies land (bulk copies into the peer, a v refill). Every thread of
+    // both CTAs is past its last copy here, so a pause of some 50 us, far
+    // longer than any such copy takes, lets them land before either CTA
+    // leaves. Both CTAs take the same decision (either one's abort flag).
+    if ((s.flags()[1] | s.flags()[2]) != 0) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 100000) {
+        }
+        cluster_sync();
+    }
     if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
@@ -1361,6 +1379,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     const int64_t tokens = a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T;
     const int64_t blocks = (int64_t)a.N * a.H * NSLICE;
     if (blocks == 0) return cudaSuccess;
+    if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
     CUtensorMap mk, mq, mv;
     // A map needs a non-empty extent; an empty token range never issues a copy.
     const int64_t ext = tokens > 0 ? tokens : 1;
@@ -1395,6 +1414,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     p.N = a.N;
     p.T = a.T;
     p.H = a.H;
+    p.stall1 = a.stall1;
     auto pick = [&](auto fp8) {
         constexpr bool F = decltype(fp8)::value;
         return a.gate == KDA_GATE_SCALAR ? kda_prefill_tc_kernel<KDA_GATE_SCALAR, F>

@@ -9,6 +9,11 @@ CASE is one of:
                       and with FP8 q, k, v (one launch of each per rep)
   decode_256x32       the decode workload (256 sequences x 32 heads, d=128)
   decode_64x32        a quarter of it, for full ncu captures
+  long_131k           one 131,072-token sequence with 32 heads (d=128, bf16)
+  varlen_64seq        the packed batch of 64 lognormal-length sequences
+  varlen_64seq_1m     the same lengths scaled to 2^20 tokens
+  hostlink            no kernel: the host link's copy rates (page-locked host
+                      memory to the device, back, and both at once), printed
 
 Each case draws its seeded inputs, runs the kernel --reps times (default 3)
 and synchronises; it prints one line and exits 0 on success.
@@ -62,12 +67,88 @@ def _decode(N: int, reps: int):
     torch.cuda.synchronize()
 
 
+def _long(reps: int):
+    dev = torch.device("cuda")
+    x = W.prefill_long_131k()
+    q, k, v, a, b, s0 = (t.to(dev) for t in (*x.tensors(), x.initial_state))
+    o = torch.empty_like(v)
+    s = torch.empty_like(s0)
+    for _ in range(reps):
+        kda.prefill(q, k, v, a, b, s0, out=o, final_state=s)
+    torch.cuda.synchronize()
+
+
+def _varlen(x, reps: int):
+    dev = torch.device("cuda")
+    (q, k, v, a, b), cu, s0 = [t.to(dev) for t in x.tensors()], x.cu_seqlens.to(dev), x.initial_state.to(dev)
+    o = torch.empty_like(v)
+    s = torch.empty_like(s0)
+    for _ in range(reps):
+        kda.varlen_prefill(q, k, v, a, b, cu, s0, out=o, final_state=s)
+    torch.cuda.synchronize()
+
+
+def _hostlink(reps: int):
+    """Copy rates between page-locked host memory and the device: 256 MiB
+    buffers, each direction alone on its own stream, then both directions
+    at once on two streams; CUDA events, best of ``reps`` (at least 5)."""
+    dev = torch.device("cuda")
+    n = 256 << 20
+    h_in = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(n, dtype=torch.uint8, device=dev)
+    d_out = torch.ones(n, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        best = None
+        for _ in range(max(reps, 5)):
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            s1.wait_event(t0)
+            s2.wait_event(t0)
+            fn()
+            e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+            e1.record(s1)
+            e2.record(s2)
+            torch.cuda.current_stream().wait_event(e1)
+            torch.cuda.current_stream().wait_event(e2)
+            t1.record()
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    for name, fn, nbytes in (("host-to-device", h2d, n), ("device-to-host", d2h, n), ("both at once", both, 2 * n)):
+        ms = timed(fn)
+        print(f"hostlink {name}: {nbytes / (ms / 1e3) / 1e9:.1f} GB/s ({nbytes >> 20} MiB in {ms:.3f} ms, best of "
+              f"{max(reps, 5)})")
+
+
 CASES = {
     "prefill_4x16x4096": lambda r: _prefill(4, r),
     "prefill_1x16x4096": lambda r: _prefill(1, r),
     "variants_4x16x4096": _variants,
     "decode_256x32": lambda r: _decode(256, r),
     "decode_64x32": lambda r: _decode(64, r),
+    "long_131k": _long,
+    "varlen_64seq": lambda r: _varlen(W.varlen_64seq(), r),
+    "varlen_64seq_1m": lambda r: _varlen(W.varlen_64seq_1m(), r),
+    "hostlink": _hostlink,
 }
 
 

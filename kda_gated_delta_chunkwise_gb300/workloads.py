@@ -26,6 +26,8 @@ Workloads (sizes as used by the tests and the benchmark):
 * ``varlen_64seq``:      64 packed sequences, lengths
   round(lognormal(8, 1)) clipped to [512, 32768] (306,055 tokens at seed 0),
   H=16, d=128, bf16, scale 0.1, per-sequence S0 ~ N(0, 0.01^2)
+* ``varlen_64seq_1m``:   the same lengths scaled to about 2^20 tokens in all
+  and re-clipped, each sequence drawn from its own generator
 
 ``to_mxfp8`` quantises a tensor to FP8 E4M3 with one power-of-two scale per
 32 consecutive elements of the last axis (the MX block format) for the FP8
@@ -177,6 +179,76 @@ def varlen_64seq(seed=0, n_seqs=64, H=16, rescale_to=None) -> Inputs:
         L = np.clip(np.rint(L * (rescale_to / L.sum())), 512, 32768).astype(np.int64)
     return packed(L, H, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.01, rng=rng,
                   name=f"varlen_{n_seqs}seq")
+
+
+def packed_per_sequence(lengths, H: int, dk: int = 128, dv: int = 128, *, dtype="bf16",
+                        alpha_scale=0.1, s0_std=0.01, seed=0, name="packed", threads=16) -> Inputs:
+    """Sequences of the given lengths packed along the token axis, each drawn
+    from its own generator ``default_rng([seed, n])`` (q, k, v, beta logits,
+    alpha logits, S0 of that sequence, in that order) and rounded to the
+    kernel dtype sequence by sequence. No full-size fp32 temporary of q, k or
+    v ever exists, and the sequences are drawn on ``threads`` host threads, so
+    batches of millions of tokens stay cheap to make. (A different random
+    stream from :func:`packed`, which draws every tensor for the whole batch
+    at once.)"""
+    import concurrent.futures as cf
+
+    lengths = np.asarray(lengths, dtype=np.int64)
+    N = int(lengths.size)
+    cu = np.zeros(N + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lengths)
+    Tt = int(cu[-1])
+    tdt = DTYPES[dtype]
+    q = torch.empty((Tt, H, dk), dtype=tdt)
+    k = torch.empty((Tt, H, dk), dtype=tdt)
+    v = torch.empty((Tt, H, dv), dtype=tdt)
+    alpha = torch.empty((Tt, H, dk), dtype=torch.float32)
+    beta = torch.empty((Tt, H), dtype=torch.float32)
+    s0 = torch.empty((N, H, dk, dv), dtype=torch.float32) if s0_std is not None else None
+
+    def one(n):
+        lo, hi = int(cu[n]), int(cu[n + 1])
+        qn, kn, vn, an, bn, sn = draw((hi - lo,), H, dk, dv, dtype=dtype, alpha_scale=alpha_scale,
+                                      s0_std=s0_std, n_states=1, rng=np.random.default_rng([seed, n]))
+        q[lo:hi], k[lo:hi], v[lo:hi], alpha[lo:hi], beta[lo:hi] = qn, kn, vn, an, bn
+        if s0 is not None:
+            s0[n] = sn[0]
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+        list(ex.map(one, range(N)))
+    return Inputs(name, q, k, v, alpha, beta, s0, torch.from_numpy(cu.astype(np.int32)),
+                  dict(N=N, T_total=Tt, H=H, dk=dk, dv=dv, dtype=dtype))
+
+
+def varlen_lengths_rescaled(n_seqs=64, total=1 << 20, seed=0, lo=512, hi=32768) -> np.ndarray:
+    """The lengths of ``varlen_64seq`` scaled by one common factor so that,
+    rounded and re-clipped to [lo, hi], they total as close to ``total`` as
+    that factor can bring them (bisection on the factor: the clip at ``hi``
+    takes tokens away, so the plain ratio total / sum falls short). The second
+    reading of the packed workload's "about a million tokens"."""
+    L = varlen_lengths(n_seqs, np.random.default_rng(seed))
+
+    def lengths(f):
+        return np.clip(np.rint(L * f), lo, hi).astype(np.int64)
+
+    a, b = 0.0, 2.0 * hi / max(1, int(L.min()))
+    for _ in range(100):
+        m = 0.5 * (a + b)
+        if lengths(m).sum() < total:
+            a = m
+        else:
+            b = m
+    la, lb = lengths(a), lengths(b)
+    return la if abs(int(la.sum()) - total) <= abs(int(lb.sum()) - total) else lb
+
+
+def varlen_64seq_1m(seed=0, n_seqs=64, H=16, total=1 << 20) -> Inputs:
+    """The packed lognormal workload at about a million tokens: the lengths of
+    ``varlen_64seq`` rescaled (:func:`varlen_lengths_rescaled`), every
+    sequence drawn on its own (:func:`packed_per_sequence`)."""
+    L = varlen_lengths_rescaled(n_seqs, total, seed)
+    return packed_per_sequence(L, H, 128, 128, dtype="bf16", alpha_scale=0.1, s0_std=0.01, seed=seed,
+                               name=f"varlen_{n_seqs}seq_{int(L.sum())}tok")
 
 
 MX_BLOCK = 32

@@ -43,3 +43,35 @@ def assert_close(name, x, ref, tol):
         ma = max_abs(x64, r64)
         assert ma <= tol["abs"], f"{name}: max-abs {ma:.3e} > {tol['abs']:.1e}"
     return rl
+
+
+class ErrAccum:
+    """Whole-tensor rel-L2 and max-abs built up piece by piece (pieces of one
+    tensor, e.g. groups of heads or sequences that the oracle runs one at a
+    time): sum of squared differences, sum of squared references, largest
+    absolute difference."""
+
+    def __init__(self, name):
+        self.name, self.d2, self.r2, self.mx, self.n = name, 0.0, 0.0, 0.0, 0
+
+    def add(self, x, ref):
+        x64, r64 = to64(x), to64(ref)
+        assert x64.shape == r64.shape, f"{self.name}: shape {x64.shape} vs {r64.shape}"
+        assert np.all(np.isfinite(x64)), f"{self.name}: non-finite values"
+        d = x64 - r64
+        self.d2 += float(np.sum(d * d))
+        self.r2 += float(np.sum(r64 * r64))
+        if d.size:
+            self.mx = max(self.mx, float(np.abs(d).max()))
+        self.n += d.size
+
+    def rel(self) -> float:
+        return (self.d2 ** 0.5) / (self.r2 ** 0.5 if self.r2 > 0 else 1.0)
+
+    def check(self, tol):
+        rl = self.rel()
+        assert rl <= tol["rel"], f"{self.name}: rel-L2 {rl:.3e} > {tol['rel']:.1e} over {self.n} elements"
+        if tol.get("abs") is not None:
+            assert self.mx <= tol["abs"], f"{self.name}: max-abs {self.mx:.3e} > {tol['abs']:.1e}"
+        print(f"{self.name}: rel-L2 {rl:.3e}, max-abs {self.mx:.3e} over {self.n} elements")
+        return rl

@@ -236,3 +236,33 @@ def test_host_prefill_picks_pieces_of_about_32_mib(lib):
     assert 384 * row <= 32 << 20 < 448 * row
     # a small input is one piece: the workspace holds T tokens
     assert f(1, 300, 2, 128, 128, 1, 0, 0) == f(1, 300, 2, 128, 128, 1, 0, 320)
+
+
+def test_grid_size_limit_is_checked_before_launch(lib):
+    """One CTA per (sequence, head, value half): N * H * 2 beyond 2^31 - 1
+    blocks is rejected as unsupported on every prefill entry point."""
+    p = ctypes.c_void_p(0x1000)
+    big_h = 1 << 20  # B * H * 2 = 2^31 with B = 1024
+    assert lib.kda_prefill_ex(p, p, p, 1, p, p, None, p, None, 1024, 1, big_h, 128, 128, 0, None) == 2
+    assert b"N * H * 2" in lib.kda_last_error()
+    assert lib.kda_prefill_fp8(p, p, p, p, p, p, p, 0, p, None, p, None, 1024, 1, big_h, 128, 128, None) == 2
+    ws = lib.kda_varlen_workspace_bytes(1024, big_h, 128, 128)
+    st = lib.kda_varlen_prefill(p, p, p, 1, p, p, None, p, None, p, 1024, 1024, big_h, 128, 128,
+                                ctypes.c_void_p(0x100000), ws, None, None)
+    assert st == 2
+    # just below the limit passes the check (and fails later on the pointers)
+    assert lib.kda_prefill_ex(None, p, p, 1, p, p, None, p, None, 1023, 1, big_h, 128, 128, 0, None) == 1
+
+
+def test_equal_length_prefill_needs_no_workspace(lib):
+    assert lib.kda_prefill_workspace_bytes(4, 4096, 16, 128, 128) == 0
+    assert kda.prefill_workspace_bytes(1, 1 << 20, 32) == 0
+
+
+def test_selftest_argument_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    assert lib.kda_selftest_bounded_wait(p, p, p, p, p, p, None, 0, 0, None) == 1      # T = 0
+    assert lib.kda_selftest_bounded_wait(p, p, p, p, p, p, None, 256, 4, None) == 1    # chunk 4 of 4
+    assert b"stall_chunk" in lib.kda_last_error()
+    assert lib.kda_selftest_bounded_wait(p, p, p, p, p, p, None, 256, -1, None) == 1
+    assert lib.kda_selftest_bounded_wait(None, p, p, p, p, p, None, 256, 0, None) == 1

@@ -3,8 +3,7 @@
 Small cases span several 64-token chunks and a ragged tail and are checked
 element by element on every output; the full-size workloads run in the
 launch configuration the benchmark uses and are checked on every output
-(4x16x4096) or on sampled heads (131k tokens), where the oracle evaluates
-the sampled (sequence, head) recurrences in full.
+(4x16x4096 and the 32-head 131k-token sequence) against the oracle.
 """
 import numpy as np
 import pytest
@@ -12,7 +11,7 @@ import torch
 
 import oracle
 from kda_gated_delta_chunkwise_gb300 import workloads as W
-from _parity import assert_close, tol_for
+from _parity import ErrAccum, assert_close, tol_for
 
 pytestmark = pytest.mark.gpu
 ALGOS_BF16 = ["simt", "auto"]
@@ -24,22 +23,13 @@ def _dev(x: W.Inputs):
     return [t.to(d) for t in x.tensors()] + [s0]
 
 
-def _check(kda, x: W.Inputs, algo="auto", heads=None):
+def _check(kda, x: W.Inputs, algo="auto"):
     q, k, v, a, b, s0 = _dev(x)
     o, s = kda.prefill(q, k, v, a, b, s0, algo=algo)
     torch.cuda.synchronize()
     o, s = o.cpu(), s.cpu()
     qc, kc, vc, ac, bc = x.tensors()
     S0 = x.initial_state
-    if heads is not None:  # sampled (b, h) pairs, each run in full by the oracle
-        for (bi, h) in heads:
-            sl = (slice(bi, bi + 1), slice(None), slice(h, h + 1))
-            ro, rs = oracle.run(qc[sl], kc[sl], vc[sl], ac[sl], bc[sl],
-                                initial_state=None if S0 is None else S0[bi:bi + 1, h:h + 1])
-            tol = tol_for(x.q.dtype)
-            assert_close(f"o[{bi},:,{h}]", o[sl], ro, tol)
-            assert_close(f"S[{bi},{h}]", s[bi:bi + 1, h:h + 1], rs, tol)
-        return
     ro, rs = oracle.run(qc, kc, vc, ac, bc, initial_state=S0)
     tol = tol_for(x.q.dtype)
     assert_close("o", o, ro, tol)
@@ -77,10 +67,29 @@ def test_prefill_4x16x4096_full(kda, algo):
 
 
 @pytest.mark.slow
-def test_prefill_long_131k_sampled(kda):
-    """B=1, H=32, T=131072, d=128, split decay scales, S0 ~ N(0, 0.01^2);
-    four heads evaluated in full by the oracle."""
-    _check(kda, W.prefill_long_131k(), heads=[(0, 0), (0, 7), (0, 20), (0, 31)])
+def test_prefill_long_131k_full(kda):
+    """B=1, H=32, T=131072, d=128, split decay scales (1e-4 / 0.2 per half of
+    the key channels), S0 ~ N(0, 0.01^2), in the benchmark's launch (all 32
+    heads in one call): every output against the oracle, which runs 16 heads
+    at a time; rel-L2 and max-abs over the whole o and the whole final
+    state."""
+    x = W.prefill_long_131k()
+    q, k, v, a, b, s0 = _dev(x)
+    o, s = kda.prefill(q, k, v, a, b, s0)
+    torch.cuda.synchronize()
+    del q, k, v, a, b
+    o, s = o.cpu(), s.cpu()
+    eo, es = ErrAccum("o"), ErrAccum("final_state")
+    qc, kc, vc, ac, bc = x.tensors()
+    for h0 in range(0, x.q.shape[2], 16):
+        hs = slice(h0, h0 + 16)
+        ro, rs = oracle.run(qc[:, :, hs], kc[:, :, hs], vc[:, :, hs], ac[:, :, hs], bc[:, :, hs],
+                            initial_state=x.initial_state[:, hs])
+        eo.add(o[:, :, hs], ro)
+        es.add(s[:, hs], rs)
+        del ro, rs
+    eo.check(tol_for(x.q.dtype))
+    es.check(tol_for(x.q.dtype))
 
 
 def test_strong_decay_and_zero_gates(kda):
