@@ -12,6 +12,10 @@ Two independent evaluations of the method live here:
   evaluated token by token in float64 in its rank-1 expanded form.
 * :mod:`oracle.brute` - explicit d_k x d_k transition matrices multiplied out
   (same page, §五), for tiny inputs only; it pins the C oracle.
+* :func:`backward` - the C gradient oracle (``kda_oracle_bwd.c``): the chain
+  rule applied to that token-by-token update in reverse time, in float64,
+  with the states replayed from checkpoints. The pages give no gradients;
+  central finite differences of :func:`run` pin it.
 
 Every input is upcast exactly to float64 before the call, so the oracle sees
 precisely the values (fp32 or bf16) that a device kernel receives.
@@ -29,8 +33,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libkda_oracle.so")
+_BWD_SRC = os.path.join(_HERE, "kda_oracle_bwd.c")
+_BWD_LIB_PATH = os.path.join(_OUT_DIR, "libkda_oracle_bwd.so")
 _lock = threading.Lock()
 _lib = None
+_bwd_lib = None
 
 # -ffp-contract=off keeps every multiply and add separately rounded, so the
 # x86 build and the aarch64 build return the same bits.
@@ -47,6 +54,32 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
     subprocess.run(["gcc", *GCC_FLAGS, src, "-o", tmp], check=True)
     os.replace(tmp, out)
     return out
+
+
+def build_all(force: bool = False):
+    """Compile both oracle libraries (forward and gradients)."""
+    build(force)
+    build(force, src=_BWD_SRC, out=_BWD_LIB_PATH)
+
+
+def load_backward(path: str | None = None):
+    """Load (building first if needed) the gradient oracle library."""
+    global _bwd_lib
+    with _lock:
+        if path is not None:
+            return _bind_backward(ctypes.CDLL(path))
+        if _bwd_lib is None:
+            _bwd_lib = _bind_backward(ctypes.CDLL(build(src=_BWD_SRC, out=_BWD_LIB_PATH)))
+        return _bwd_lib
+
+
+def _bind_backward(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.kda_oracle_backward.restype = ctypes.c_int
+    lib.kda_oracle_backward.argtypes = [dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int32),
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+    return lib
 
 
 def load(path: str | None = None):
@@ -121,6 +154,48 @@ def run(q, k, v, alpha, beta, cu_seqlens=None, initial_state=None,
     if rc != 0:
         raise ValueError(f"kda_oracle_run failed with code {rc}")
     return o, sT
+
+
+def backward(q, k, v, alpha, beta, d_o, d_final_state=None, cu_seqlens=None, initial_state=None,
+             nthreads: int = 0, lib=None):
+    """Gradients of L = sum <d_o, o> + <d_final_state, S_T> in float64.
+
+    Inputs as for :func:`run`; ``d_o`` has o's shape, ``d_final_state`` the
+    final state's (None: zero). Returns a dict with ``dq``, ``dk``, ``dv``,
+    ``dalpha``, ``dbeta`` (shaped like their inputs) and ``d_initial_state``
+    ``[N, H, dk, dv]``.
+    """
+    q, k, v, alpha, beta, d_o = (_f64(x) for x in (q, k, v, alpha, beta, d_o))
+    lead = v.shape[:-2]
+    H, dk = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    if d_o.shape != v.shape:
+        raise ValueError(f"d_o must be {v.shape}, got {d_o.shape}")
+    if cu_seqlens is None:
+        if len(lead) != 2:
+            raise ValueError("batched inputs must be [B, T, H, d]")
+        B, T = lead
+        cu = np.arange(B + 1, dtype=np.int32) * T
+    else:
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    s0 = None if initial_state is None else _f64(initial_state)
+    dsT = None if d_final_state is None else _f64(d_final_state)
+    for name, x in (("initial_state", s0), ("d_final_state", dsT)):
+        if x is not None and x.shape != (N, H, dk, dv):
+            raise ValueError(f"{name} must be {(N, H, dk, dv)}, got {x.shape}")
+    out = {"dq": np.zeros(q.shape), "dk": np.zeros(k.shape), "dv": np.zeros(v.shape),
+           "dalpha": np.zeros(alpha.shape), "dbeta": np.zeros(beta.shape),
+           "d_initial_state": np.zeros((N, H, dk, dv))}
+    lib = lib or load_backward()
+    rc = lib.kda_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                 cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), N, H, dk, dv,
+                                 _ptr(s0), _ptr(d_o), _ptr(dsT), _ptr(out["dq"]), _ptr(out["dk"]),
+                                 _ptr(out["dv"]), _ptr(out["dalpha"]), _ptr(out["dbeta"]),
+                                 _ptr(out["d_initial_state"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_backward failed with code {rc}")
+    return out
 
 
 def expand_gate(alpha, gate: str, lead: tuple, dk: int) -> np.ndarray:
