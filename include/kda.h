@@ -335,6 +335,42 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
 kda_status_t kda_device_errors(int *errors, int reset);
 
 /*
+ * kda_prefill_backward - gradients of the prefill (training). The pages give
+ * no gradients; they follow from the chain rule applied to the K3 essay's
+ * §四 update and §二.1 read-out, evaluated with §六's chunks in reverse. For
+ * L = sum_t <d_o_t, o_t> + <d_final_state, S_T> it returns dL/dq, dL/dk,
+ * dL/dv, dL/dalpha, dL/dbeta and dL/dS_0 of kda_prefill on the same inputs
+ * (equal-length batches, per-channel gate).
+ *
+ *   q, k, v, alpha, beta, initial_state  as for kda_prefill (read)
+ *   d_o            [B, T, H, d_v] qkv_dtype: gradient of o (read)
+ *   d_final_state  [B, H, d_k, d_v] float32 or NULL (zero) (read)
+ *   dq, dk, dalpha [B, T, H, d_k] float32 (written)
+ *   dv             [B, T, H, d_v] float32 (written)
+ *   dbeta          [B, T, H] float32 (written; 4-byte aligned suffices)
+ *   d_initial_state[B, H, d_k, d_v] float32 or NULL (not written)
+ *   workspace      device scratch of kda_prefill_backward_workspace_bytes(...)
+ *                  bytes, 16-byte aligned, owned by the caller: the state
+ *                  before every 64-token chunk and the state gradient after
+ *                  it (2 x 4 d_k d_v bytes per chunk of every sequence and
+ *                  head). Calls sharing a workspace must not overlap.
+ *
+ * Every gradient is float32 whatever qkv_dtype is (fp32 arithmetic on CUDA
+ * cores throughout). The result does not depend on the call's timing: where
+ * two value halves (d_v = 128) both contribute to an element, it is the sum of
+ * exactly two terms. Errors as for kda_prefill; a missing or short workspace
+ * returns KDA_ERR_WORKSPACE before anything runs.
+ */
+kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                  const float *alpha, const float *beta, const float *initial_state,
+                                  const void *d_o, const float *d_final_state, float *dq, float *dk, float *dv,
+                                  float *dalpha, float *dbeta, float *d_initial_state, int B, int T, int H,
+                                  int d_k, int d_v, void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Workspace bytes kda_prefill_backward needs (0 for invalid arguments). */
+size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_v);
+
+/*
  * kda_selftest_bounded_wait - diagnostic with no counterpart in the method:
  * runs the tensor-core prefill on one bf16 sequence of one head (B = H = 1,
  * d_k = d_v = 128, T tokens, zero initial state; tensors as for kda_prefill)

@@ -10,10 +10,11 @@ q, k, v), ``varlen_prefill``,
 ``decode_step``; host (CPU) tensors given to ``prefill`` or ``prefill_fp8``
 go through the native host-buffer pipeline (kda_prefill_host,
 kda_prefill_fp8_host); and for serving with a pool of states indexed by slot:
-``varlen_prefill_slots``, ``decode_step_slots``. Build the CUDA library with
+``varlen_prefill_slots``, ``decode_step_slots``; for training,
+``prefill_backward`` (the gradients of ``prefill``). Build the CUDA library with
 ``kda_gated_delta_chunkwise_gb300.build.build()`` first.
 """
 from ._binding import (ALGOS, EXPORTS, GATES, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT,  # noqa: F401
                        KDA_DEV_OK, KdaError, decode_step, decode_step_slots, device_errors, lib_path, load,
-                       prefill, prefill_fp8, prefill_workspace_bytes, selftest_bounded_wait, varlen_prefill,
+                       prefill, prefill_backward, prefill_fp8, prefill_workspace_bytes, selftest_bounded_wait, varlen_prefill,
                        varlen_prefill_slots, varlen_workspace_bytes)

@@ -296,6 +296,51 @@ kda_status_t kda_varlen_prefill_slots(const void *q, const void *k, const void *
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
+    if (B < 0 || T < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return 0;
+    return kda::backward_workspace_bytes(B, T, H, d_k, d_v);
+}
+
+kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                  const float *alpha, const float *beta, const float *initial_state,
+                                  const void *d_o, const float *d_final_state, float *dq, float *dk, float *dv,
+                                  float *dalpha, float *dbeta, float *d_initial_state, int B, int T, int H,
+                                  int d_k, int d_v, void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_status_t st;
+    if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
+    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
+    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
+    const int64_t nc = ((int64_t)T + 63) / 64;
+    if ((int64_t)B * H * (nc > 0 ? nc : 1) * 2 > INT32_MAX)
+        return fail(KDA_ERR_UNSUPPORTED, "B * H * ceil(T / 64) * 2 must fit in int32");
+    const bool any = (int64_t)B * T > 0;
+    if ((st = check_tensors(q, k, v, alpha, beta, d_o, initial_state, d_final_state, any)) != KDA_OK) return st;
+    if (any) {
+        KDA_REQUIRE_PTR(dq);
+        KDA_REQUIRE_PTR(dk);
+        KDA_REQUIRE_PTR(dv);
+        KDA_REQUIRE_PTR(dalpha);
+        if (!dbeta) return fail(KDA_ERR_INVALID_ARG, "dbeta must not be NULL");
+        if (reinterpret_cast<uintptr_t>(dbeta) & 3u) return fail(KDA_ERR_INVALID_ARG, "dbeta must be 4-byte aligned");
+    }
+    KDA_OPTIONAL_PTR(d_initial_state);
+    if (B == 0) return ok();
+    const size_t need = kda::backward_workspace_bytes(B, T, H, d_k, d_v);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
+    if (need && !aligned16(workspace)) return fail(KDA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    kda::BackwardArgs b{};
+    b.q = q; b.k = k; b.v = v; b.d_o = d_o; b.dt = qkv_dtype;
+    b.alpha = alpha; b.beta = beta; b.s0 = initial_state; b.dsT = d_final_state;
+    b.dq = dq; b.dk = dk; b.dvv = dv; b.dalpha = dalpha; b.dbeta = dbeta; b.ds0 = d_initial_state;
+    float *ws = static_cast<float *>(workspace);
+    b.states = ws;
+    b.gnext = ws ? ws + need / sizeof(float) / 2 : nullptr;
+    b.N = B; b.T = T; b.H = H; b.d_k = d_k; b.d_v = d_v;
+    return cuda_status(kda::launch_backward(b, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
+}
+
 kda_status_t kda_selftest_bounded_wait(const void *q, const void *k, const void *v, const float *alpha,
                                        const float *beta, void *o, float *final_state, int T, int stall_chunk,
                                        kda_stream_t stream) {

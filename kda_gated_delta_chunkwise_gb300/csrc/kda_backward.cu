@@ -1,0 +1,628 @@
+// KDA chunkwise backward on CUDA cores (fp32 arithmetic): the gradients of
+// L = sum_t <do_t, o_t> + <dS_T, S_T> with respect to q, k, v, alpha, beta
+// and the initial state, for equal-length batches.
+//
+// Source of the map: the web page "研究KimiK3，我发现大模型正在学会“管理自己的计算”"
+// (pwwt.cn), the K3 essay: §四 (the KDA update), §二.1 (the read-out o = S^T q),
+// §六.1 (chunks: recursion between chunks) and §六.2 (the WY form). The pages
+// give no gradients; the chain rule applied to the chunk algebra below does.
+//
+// Chunk algebra (as in the forward; C = 64 rows r, j; key channels c; value
+// columns v; St = Diag(mu) S the centred start state; tables from
+// kda_chunk_simt.cuh):
+//   X = Kr St,  R = Diag(beta) (V - X),  U = T R,  O = Qr St + P U,
+//   S_next = Diag(mu) (St + Kc^T U).
+// Reverse, with G = dL/dS_next and Gt = Diag(mu) G:
+//   dU  = Kc Gt + P^T dO           dR = T^T dU        dX = -Diag(beta) dR
+//   dV  = Diag(beta) dR            dbeta_r = sum_v dR (V - X) + sum_j dA Kr Kc^T
+//   dSt = Gt + Qr^T dO + Kr^T dX   dS = Diag(mu) dSt  (the state chain)
+//   dP  = lower(dO U^T)            dT = dU R^T        dA = strict-lower(-T^T dT T^T)
+//   dQr = dO St^T + dP Kc          dKr = dX St^T + Diag(beta) dA Kc
+//   dKc = U Gt^T + (Diag(beta) dA)^T Kr + dP^T Qr
+//   dq = dQr (.) p/mu,  dk = dKr (.) p/mu + dKc (.) mu/p
+// and the gates through logs: d log p_r = dKr Kr + dQr Qr - dKc Kc (per
+// channel), d log mu = 2 sum_v Gt St + sum_r [Qr (dO St^T) + Kr (dX St^T) +
+// Kc (U Gt^T)] - sum_r d log p_r, d log p_{L-1} += d log mu / 2 (gamma is the
+// last row's product), d log alpha_m = sum_{r>=m} d log p_r and
+// dalpha = d log alpha / alpha. Chunks that the forward runs token by token
+// (a channel decays past e^-80) take the token-level reverse steps instead:
+//   G += q do^T; w = G^T k; dv = beta w; dbeta = w.e; dk = beta (G e - S' w);
+//   dS' = G - beta k w^T; dalpha = rowsum(dS' (.) S_{t-1}); G = Diag(alpha) dS'
+// with S_{t-1} replayed from the chunk's start state.
+//
+// Three launches after the forward (the fp32 chunk kernel, which also writes
+// the state before every chunk into the workspace):
+//   chain  one CTA per (sequence, head, 64-column value slice), chunks in
+//          reverse: writes dL/dS after every chunk into the workspace and the
+//          initial state's gradient;
+//   local  one CTA per (sequence, head, chunk, value slice), all chunks at
+//          once: dv of its slice, and its slice's share of dq, dk, dalpha,
+//          dbeta, added with atomicAdd onto zeroed outputs (at most two slices,
+//          so every sum is a + b: the same bits in either order).
+#include "kda_chunk_simt.cuh"
+
+namespace kda {
+namespace {
+
+using simt::C;
+using simt::ld_in;
+using simt::NT;
+using simt::VS;
+
+constexpr int LDC = C + 4;
+
+struct BwdParams {
+    const void *q, *k, *v, *d_o;
+    const float *alpha, *beta, *dsT;
+    float *dq, *dk, *dv, *dalpha, *dbeta, *ds0;
+    const float *states;  // [N, H, NC, DK, DV]: the state before every chunk
+    float *gnext;         // [N, H, NC, DK, DV]: dL/dS after every chunk
+    int N, T, H, DV, NC;
+};
+
+// acc[i][jj] += sum_{m < K} a(ty + 16 i, m) * b(m, 4 tx + jj)
+template <int K, typename FA, typename FB>
+__device__ __forceinline__ void mm(float (&acc)[4][4], FA a, FB b) {
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+#pragma unroll 2
+    for (int m = 0; m < K; ++m) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = a(ty + 16 * i, m);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) bv[jj] = b(m, 4 * tx + jj);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[i][jj] += av[i] * bv[jj];
+    }
+}
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
+}
+
+// Sum over the 16 lanes that share a thread row (tx = lane % 16).
+__device__ __forceinline__ float sum16(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    return x;
+}
+
+// ---------------------------------------------------------------- chain
+template <int DK> struct ChainSmem {
+    float G[DK * VS];
+    simt::Tables<DK> tb;
+    float dO[C * VS];
+    float red[4 * VS];
+};
+
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ChainSmem<DK> &sm = *reinterpret_cast<ChainSmem<DK> *>(smem_raw);
+    simt::Tables<DK> &tb = sm.tb;
+    constexpr int LDK = simt::Tables<DK>::LDK;
+    constexpr int RB = DK / 64;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int nslices = p.DV / VS;
+    const int slice = blockIdx.x % nslices;
+    const int h = (blockIdx.x / nslices) % p.H;
+    const int n = blockIdx.x / (nslices * p.H);
+    const int H = p.H, DV = p.DV, v0 = slice * VS;
+    const int64_t T = p.T, t_begin = (int64_t)n * p.T;
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *dO = (const TIn *)p.d_o;
+    const int64_t sh = (int64_t)n * H + h;
+    float *gn = p.gnext + sh * p.NC * DK * DV;
+
+    for (int e = tid; e < DK * VS; e += NT)
+        sm.G[e] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    __syncthreads();
+
+    for (int ci = p.NC - 1; ci >= 0; --ci) {
+        const int64_t t0 = (int64_t)ci * C;
+        const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
+        const int64_t tok0 = t_begin + t0;
+        for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
+            gn[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[e];
+        simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, q, k, p.beta, tok0, L, H, h);
+        for (int e = tid; e < C * VS; e += NT) {
+            const int r = e / VS;
+            sm.dO[e] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
+        }
+        if (tb.slow) {
+            __syncthreads();
+            // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
+            const int j = tid % VS, part = tid / VS;
+            for (int r = L - 1; r >= 0; --r) {
+                const int64_t tk = (tok0 + r) * H + h;
+                const float dj = sm.dO[r * VS + j];
+                float wp = 0.f;
+                for (int c = part; c < DK; c += NT / VS) {
+                    const float g = sm.G[c * VS + j] + ld_in(q, tk * DK + c) * dj;
+                    sm.G[c * VS + j] = g;
+                    wp += ld_in(k, tk * DK + c) * g;
+                }
+                sm.red[part * VS + j] = wp;
+                __syncthreads();
+                float w = 0.f;
+#pragma unroll
+                for (int p2 = 0; p2 < NT / VS; ++p2) w += sm.red[p2 * VS + j];
+                const float bt = p.beta[tk];
+                for (int c = part; c < DK; c += NT / VS)
+                    sm.G[c * VS + j] = p.alpha[tk * DK + c] * (sm.G[c * VS + j] - bt * ld_in(k, tk * DK + c) * w);
+                __syncthreads();
+            }
+            continue;
+        }
+        simt::wy_tables<DK>(tb);  // (ends with a barrier: dO is staged too)
+        float *dU = tb.A;         // free once T exists
+        float acc[4][4];
+        // dU = Kc Gt + P^T dO
+        zero(acc);
+        mm<DK>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
+               [&](int c, int j) { return tb.mu[c] * sm.G[c * VS + j]; });
+        mm<C>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * VS + j]; });
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) dU[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+        __syncthreads();
+        // dX = -Diag(beta) T^T dU (into dU's place)
+        zero(acc);
+        mm<C>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; });
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                dU[(ty + 16 * i) * LDC + 4 * tx + jj] = -tb.beta[ty + 16 * i] * acc[i][jj];
+        __syncthreads();
+        // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX); tile rows 64 b2 + 4 ty + i, columns 4 tx + jj
+        float acc2[RB][4][4];
+#pragma unroll
+        for (int b2 = 0; b2 < RB; ++b2) zero(acc2[b2]);
+        for (int r = 0; r < C; ++r) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dO[r * VS + 4 * tx]);
+            const float4 x4 = *reinterpret_cast<const float4 *>(&dU[r * LDC + 4 * tx]);
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w}, xv4[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int b2 = 0; b2 < RB; ++b2) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(&tb.Qr[r * LDK + 64 * b2 + 4 * ty]);
+                const float4 k4 = *reinterpret_cast<const float4 *>(&tb.Kr[r * LDK + 64 * b2 + 4 * ty]);
+                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) acc2[b2][i][jj] += qv[i] * dv4[jj] + kv[i] * xv4[jj];
+            }
+        }
+#pragma unroll
+        for (int b2 = 0; b2 < RB; ++b2)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = 64 * b2 + 4 * ty + i;
+                const float m = tb.mu[c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float &g = sm.G[c * VS + 4 * tx + jj];
+                    g = m * (m * g + acc2[b2][i][jj]);
+                }
+            }
+        __syncthreads();
+    }
+    if (p.ds0)
+        for (int e = tid; e < DK * VS; e += NT)
+            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[e];
+}
+
+// ---------------------------------------------------------------- local
+template <int DK> struct LocalSmem {
+    simt::Tables<DK> tb;
+    float W[3][C * LDC];  // work tiles; tb.A is the fourth
+    float red[16 * DK];   // per-thread-row partial sums over columns
+};
+
+template <int DK, typename TIn>
+__device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, const float *Sg, const float *Gg,
+                                        int64_t tok0, int L, int h, int v0) {
+    // Token-level reverse steps; the state before token r is replayed from the
+    // chunk's start state for every r (the chunk is rare: this is written for
+    // size). Buffers: Sb (state) in Kr, G in Qr, vectors in W.
+    constexpr int NP = NT / VS;     // key-row parts of the column mapping
+    constexpr int NH = NT / DK;     // column parts of the row mapping
+    const int H = p.H, DV = p.DV, tid = threadIdx.x;
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
+    float *Sb = sm.tb.Kr, *G = sm.tb.Qr;
+    float *redv = sm.W[0], *redw = sm.W[0] + NP * VS, *ev = sm.W[0] + 2 * NP * VS, *wv = ev + VS;
+    float *redc = sm.W[1];  // [NH][4][DK]
+    const int j = tid % VS, part = tid / VS;
+    for (int e = tid; e < DK * VS; e += NT) G[e] = Gg[(int64_t)(e / VS) * DV + v0 + e % VS];
+    for (int r = L - 1; r >= 0; --r) {
+        // Sb = S_{r-1}
+        for (int e = tid; e < DK * VS; e += NT) Sb[e] = Sg[(int64_t)(e / VS) * DV + v0 + e % VS];
+        __syncthreads();
+        for (int m = 0; m < r; ++m) {
+            const int64_t tk = (tok0 + m) * H + h;
+            float vp = 0.f;
+            for (int c = part; c < DK; c += NP) vp += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * Sb[c * VS + j];
+            redv[part * VS + j] = vp;
+            __syncthreads();
+            float vh = 0.f;
+#pragma unroll
+            for (int p2 = 0; p2 < NP; ++p2) vh += redv[p2 * VS + j];
+            const float e = ld_in(v, tk * DV + v0 + j) - vh, be = p.beta[tk] * e;
+            for (int c = part; c < DK; c += NP)
+                Sb[c * VS + j] = p.alpha[tk * DK + c] * Sb[c * VS + j] + ld_in(k, tk * DK + c) * be;
+            __syncthreads();
+        }
+        // reverse step of token r
+        const int64_t tk = (tok0 + r) * H + h;
+        const float bt = p.beta[tk];
+        {
+            const float dj = ld_in(dO, tk * DV + v0 + j);
+            float vp = 0.f, wp = 0.f;
+            for (int c = part; c < DK; c += NP) {
+                const float kc = ld_in(k, tk * DK + c);
+                const float g = G[c * VS + j] + ld_in(q, tk * DK + c) * dj;
+                G[c * VS + j] = g;
+                vp += p.alpha[tk * DK + c] * kc * Sb[c * VS + j];
+                wp += kc * g;
+            }
+            redv[part * VS + j] = vp;
+            redw[part * VS + j] = wp;
+            __syncthreads();
+            if (part == 0) {
+                float vh = 0.f, w = 0.f;
+#pragma unroll
+                for (int p2 = 0; p2 < NP; ++p2) {
+                    vh += redv[p2 * VS + j];
+                    w += redw[p2 * VS + j];
+                }
+                ev[j] = ld_in(v, tk * DV + v0 + j) - vh;
+                wv[j] = w;
+                p.dv[tk * DV + v0 + j] = bt * w;
+            }
+            __syncthreads();
+        }
+        {
+            // row mapping: channel c, columns of part hp
+            const int c = tid % DK, hp = tid / DK;
+            const float ac = p.alpha[tk * DK + c], kc = ld_in(k, tk * DK + c);
+            float dq = 0.f, ge = 0.f, sw = 0.f, da = 0.f;
+            for (int jj = hp * (VS / NH); jj < (hp + 1) * (VS / NH); ++jj) {
+                const float s = Sb[c * VS + jj], g = G[c * VS + jj], e = ev[jj], w = wv[jj];
+                dq += (ac * s + bt * kc * e) * ld_in(dO, tk * DV + v0 + jj);
+                ge += g * e;
+                sw += ac * s * w;
+                da += (g - bt * kc * w) * s;
+            }
+            redc[(hp * 4 + 0) * DK + c] = dq;
+            redc[(hp * 4 + 1) * DK + c] = ge;
+            redc[(hp * 4 + 2) * DK + c] = sw;
+            redc[(hp * 4 + 3) * DK + c] = da;
+            __syncthreads();
+            if (tid < DK) {
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int h2 = 0; h2 < NH; ++h2)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) s4[u] += redc[(h2 * 4 + u) * DK + tid];
+                atomicAdd(&p.dq[tk * DK + tid], s4[0]);
+                atomicAdd(&p.dk[tk * DK + tid], bt * (s4[1] - s4[2]));
+                atomicAdd(&p.dalpha[tk * DK + tid], s4[3]);
+            }
+            if (tid == 0) {
+                float db = 0.f;
+                for (int jj = 0; jj < VS; ++jj) db += wv[jj] * ev[jj];
+                atomicAdd(&p.dbeta[tk], db);
+            }
+        }
+        // G = Diag(alpha)(G - beta k w^T)
+        for (int c = part; c < DK; c += NP)
+            G[c * VS + j] = p.alpha[tk * DK + c] * (G[c * VS + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
+        __syncthreads();
+    }
+}
+
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    LocalSmem<DK> &sm = *reinterpret_cast<LocalSmem<DK> *>(smem_raw);
+    simt::Tables<DK> &tb = sm.tb;
+    constexpr int LDK = simt::Tables<DK>::LDK;
+    constexpr int RB = DK / 64;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int nslices = p.DV / VS;
+    const int slice = blockIdx.x % nslices;
+    int64_t rest = blockIdx.x / nslices;
+    const int ci = (int)(rest % p.NC);
+    rest /= p.NC;
+    const int h = (int)(rest % p.H);
+    const int n = (int)(rest / p.H);
+    const int H = p.H, DV = p.DV, v0 = slice * VS;
+    const int64_t t0 = (int64_t)ci * C;
+    const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
+    const int64_t tok0 = (int64_t)n * p.T + t0;
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
+    const int64_t off = (((int64_t)n * H + h) * p.NC + ci) * DK * DV;
+    const float *Sg = p.states + off, *Gg = p.gnext + off;
+
+    simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, q, k, p.beta, tok0, L, H, h);
+    if (tb.slow) {
+        local_slow<DK, TIn>(sm, p, Sg, Gg, tok0, L, h, v0);
+        return;
+    }
+    simt::wy_tables<DK>(tb);
+    float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
+    auto S_ = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };  // St
+    auto G_ = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };  // Gt
+    float acc[4][4];
+
+    // dO -> WD; V - Kr St -> WB
+    for (int e = tid; e < C * VS; e += NT) {
+        const int r = e / VS;
+        WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
+    }
+    zero(acc);
+    mm<DK>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, S_);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = ty + 16 * i;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj) : 0.f;
+            WB[r * LDC + 4 * tx + jj] = vv - acc[i][jj];
+        }
+    }
+    __syncthreads();
+    // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
+    zero(acc);
+    mm<C>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; });
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) WC[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+    zero(acc);
+    mm<DK>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, G_);
+    mm<C>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; });
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) WA[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+    __syncthreads();
+    // dT = dU R^T (registers); dR = T^T dU: dV, the first part of dbeta, dX
+    float dT[4][4], dR[4][4];
+    zero(dT);
+    mm<VS>(dT, [&](int r, int j) { return WA[r * LDC + j]; }, [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; });
+    zero(dR);
+    mm<C>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; });
+    float dbeta_r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = ty + 16 * i;
+        float s = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            s += dR[i][jj] * WB[r * LDC + 4 * tx + jj];
+            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj] = tb.beta[r] * dR[i][jj];
+        }
+        dbeta_r[i] = sum16(s);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = ty + 16 * i;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            WB[r * LDC + 4 * tx + jj] = -tb.beta[r] * dR[i][jj];  // dX
+            WA[r * LDC + 4 * tx + jj] = dT[i][jj];
+        }
+    }
+    __syncthreads();
+    // dP = lower(dO U^T) (registers); dKc = U Gt^T
+    float dP[4][4];
+    zero(dP);
+    mm<VS>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; });
+    float dKc[RB][4][4], dQr[RB][4][4], dKr[RB][4][4], s123[RB][4];
+#pragma unroll
+    for (int b2 = 0; b2 < RB; ++b2) {
+        zero(dKc[b2]);
+        mm<VS>(dKc[b2], [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return G_(c + 64 * b2, j); });
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s += tb.Kc[(ty + 16 * i) * LDK + 64 * b2 + 4 * tx + jj] * dKc[b2][i][jj];
+            s123[b2][jj] = s;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int r = ty + 16 * i, m = 4 * tx + jj;
+            WC[r * LDC + m] = m <= r ? dP[i][jj] : 0.f;
+        }
+    __syncthreads();
+    // dQr = dO St^T, dKr = dX St^T (the parts that meet St), then the rest
+#pragma unroll
+    for (int b2 = 0; b2 < RB; ++b2) {
+        zero(dQr[b2]);
+        zero(dKr[b2]);
+        mm<VS>(dQr[b2], [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return S_(c + 64 * b2, j); });
+        mm<VS>(dKr[b2], [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return S_(c + 64 * b2, j); });
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rc = (ty + 16 * i) * LDK + 64 * b2 + 4 * tx + jj;
+                s += tb.Qr[rc] * dQr[b2][i][jj] + tb.Kr[rc] * dKr[b2][i][jj];
+            }
+            s123[b2][jj] += s;
+        }
+        // dQr += dP Kc;  dKc += dP^T Qr
+        mm<C>(dQr[b2], [&](int r, int m) { return WC[r * LDC + m]; },
+              [&](int m, int c) { return tb.Kc[m * LDK + c + 64 * b2]; });
+        mm<C>(dKc[b2], [&](int r, int m) { return WC[m * LDC + r]; },
+              [&](int m, int c) { return tb.Qr[m * LDK + c + 64 * b2]; });
+    }
+    // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
+    zero(acc);
+    mm<C>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; });
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) WD[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+    __syncthreads();
+    zero(acc);
+    mm<C>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; });
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int r = ty + 16 * i, m = 4 * tx + jj;
+            WA[r * LDC + m] = m < r ? -acc[i][jj] : 0.f;
+        }
+    __syncthreads();
+    // dKr += Diag(beta) dA Kc (and dbeta's second part Kr . (dA Kc));  dKc += (Diag(beta) dA)^T Kr
+#pragma unroll
+    for (int b2 = 0; b2 < RB; ++b2) {
+        float t[4][4];
+        zero(t);
+        mm<C>(t, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c + 64 * b2]; });
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = ty + 16 * i;
+            float s = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                s += tb.Kr[r * LDK + 64 * b2 + 4 * tx + jj] * t[i][jj];
+                dKr[b2][i][jj] += tb.beta[r] * t[i][jj];
+            }
+            dbeta_r[i] += sum16(s);
+        }
+        mm<C>(dKc[b2], [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
+              [&](int m, int c) { return tb.Kr[m * LDK + c + 64 * b2]; });
+    }
+    if (tx == 0)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = ty + 16 * i;
+            if (r < L) atomicAdd(&p.dbeta[(tok0 + r) * H + h], dbeta_r[i]);
+        }
+    // dq, dk with this thread's p (running gate products over the chunk's rows),
+    // and d log p into Qr's place
+    float dlogp[RB][4][4];
+#pragma unroll
+    for (int b2 = 0; b2 < RB; ++b2) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int c = 64 * b2 + 4 * tx + jj;
+            const float mu = tb.mu[c];
+            float pr = 1.f;
+            int m = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = ty + 16 * i, rc = r * LDK + c;
+                for (; m <= r; ++m)
+                    if (m < L) pr *= p.alpha[((tok0 + m) * H + h) * DK + c];
+                const float e2 = pr / mu, e3 = mu / pr;
+                if (r < L) {
+                    const int64_t th = (tok0 + r) * H + h;
+                    atomicAdd(&p.dq[th * DK + c], dQr[b2][i][jj] * e2);
+                    atomicAdd(&p.dk[th * DK + c], dKr[b2][i][jj] * e2 + dKc[b2][i][jj] * e3);
+                }
+                dlogp[b2][i][jj] = dKr[b2][i][jj] * tb.Kr[rc] + dQr[b2][i][jj] * tb.Qr[rc] - dKc[b2][i][jj] * tb.Kc[rc];
+            }
+        }
+    }
+    __syncthreads();  // every read of Qr is done
+#pragma unroll
+    for (int b2 = 0; b2 < RB; ++b2)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int c = 64 * b2 + 4 * tx + jj;
+            sm.red[ty * DK + c] = s123[b2][jj];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tb.Qr[(ty + 16 * i) * LDK + c] = dlogp[b2][i][jj];
+        }
+    __syncthreads();
+    // per channel: d log mu, then d log alpha by a reverse running sum over the rows
+    if (tid < DK) {
+        const int c = tid;
+        float s0 = 0.f;
+        for (int j = 0; j < VS; ++j) s0 += S_(c, j) * G_(c, j);
+        float s123c = 0.f;
+        for (int t2 = 0; t2 < 16; ++t2) s123c += sm.red[t2 * DK + c];
+        float colsum = 0.f;
+        for (int r = 0; r < L; ++r) colsum += tb.Qr[r * LDK + c];
+        const float dlogmu = 2.f * s0 + s123c - colsum;
+        float run = 0.5f * dlogmu;
+        for (int r = L - 1; r >= 0; --r) {
+            run += tb.Qr[r * LDK + c];
+            const int64_t th = (tok0 + r) * H + h;
+            atomicAdd(&p.dalpha[th * DK + c], run / p.alpha[th * DK + c]);
+        }
+    }
+}
+
+template <int DK, typename TIn>
+cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
+    const int NC = (b.T + C - 1) / C;
+    const int nslices = b.d_v / VS;
+    // 1. forward on CUDA cores, keeping the state before every chunk
+    PrefillArgs a{};
+    a.q = b.q; a.k = b.k; a.v = b.v; a.alpha = b.alpha; a.beta = b.beta; a.s0 = b.s0;
+    a.o = nullptr; a.sT = nullptr; a.gate = KDA_GATE_CHANNEL; a.slots = nullptr; a.cu_seqlens = nullptr;
+    a.N = b.N; a.T = b.T; a.H = b.H; a.dk = DK; a.dv = b.d_v; a.dt = b.dt;
+    a.chunk_states = b.states;
+    cudaError_t e = launch_prefill_simt(a, s);
+    if (e != cudaSuccess) return e;
+    BwdParams p;
+    p.q = b.q; p.k = b.k; p.v = b.v; p.d_o = b.d_o; p.alpha = b.alpha; p.beta = b.beta; p.dsT = b.dsT;
+    p.dq = b.dq; p.dk = b.dk; p.dv = b.dvv; p.dalpha = b.dalpha; p.dbeta = b.dbeta; p.ds0 = b.ds0;
+    p.states = b.states; p.gnext = b.gnext;
+    p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC;
+    // 2. the reverse state chain
+    auto chain = kda_bwd_chain_kernel<DK, TIn>;
+    const size_t sc = sizeof(ChainSmem<DK>);
+    if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc)) != cudaSuccess) return e;
+    chain<<<(unsigned)((int64_t)b.N * b.H * nslices), NT, sc, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 3. the per-chunk gradients, added onto zeroed dq, dk, dalpha, dbeta
+    const size_t tok = (size_t)b.N * b.T * b.H;
+    if ((e = cudaMemsetAsync(b.dq, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(b.dk, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(b.dalpha, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(b.dbeta, 0, tok * sizeof(float), s)) != cudaSuccess) return e;
+    if (NC == 0) return cudaSuccess;
+    auto local = kda_bwd_local_kernel<DK, TIn>;
+    const size_t sl = sizeof(LocalSmem<DK>);
+    if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
+    local<<<(unsigned)((int64_t)b.N * b.H * NC * nslices), NT, sl, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv) {
+    const size_t NC = ((size_t)T + C - 1) / C;
+    return 2 * (size_t)N * H * NC * dk * dv * sizeof(float);
+}
+
+cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s) {
+    if (b.d_v % VS) return cudaErrorInvalidValue;
+    if (b.d_k == 128) return b.dt == KDA_BF16 ? launch_t<128, __nv_bfloat16>(b, s) : launch_t<128, float>(b, s);
+    if (b.d_k == 64) return b.dt == KDA_BF16 ? launch_t<64, __nv_bfloat16>(b, s) : launch_t<64, float>(b, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

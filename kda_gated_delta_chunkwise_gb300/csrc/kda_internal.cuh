@@ -64,6 +64,8 @@ struct PrefillArgs {
     const int32_t *dev_status;  // nullable: skip all work when *dev_status != 0
     int stall1;                 // self-test of the tensor-core kernel's bounded waits: 1 + the
                                 // chunk at which its state chain stops (0, the default: never)
+    float *chunk_states;        // CUDA-core kernel, equal lengths only (nullable): the state
+                                // before every chunk, [N, H, ceil(T / 64), dk, dv]
 };
 
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
@@ -71,6 +73,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
 // Reads (and optionally clears) the tensor-core kernel's error word.
 cudaError_t read_device_error(int *out, bool reset);
+
+// Backward of the prefill (equal-length batches, per-channel gate). Every
+// gradient is float32; d_o has the dtype of q, k, v.
+struct BackwardArgs {
+    const void *q, *k, *v, *d_o;
+    kda_dtype_t dt;
+    const float *alpha, *beta, *s0, *dsT;  // s0, dsT nullable (zeros)
+    float *dq, *dk, *dvv, *dalpha, *dbeta;
+    float *ds0;                            // nullable
+    float *states, *gnext;                 // workspace: backward_workspace_bytes
+    int N, T, H, d_k, d_v;
+};
+size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv);
+cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s);
 
 // Varlen preparation: validates cu_seqlens, writes the status word, sorts the
 // sequences by length (longest first) into `order` and zeroes `counter`.

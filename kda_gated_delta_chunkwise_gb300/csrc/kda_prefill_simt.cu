@@ -32,43 +32,30 @@
 //
 // Work split: one CTA of 256 threads per (sequence, head, 64-column slice of
 // d_v). The state slice lives in shared memory for the whole sequence.
-#include "kda_internal.cuh"
+#include "kda_chunk_simt.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int C = 64;          // chunk length
-constexpr int VS = 64;         // value columns per CTA
-constexpr int NT = 256;        // threads per CTA
-constexpr float kMinGamma = 1.8e-35f;  // ~exp(-80): chunk decay limit of the WY form
+using simt::C;
+using simt::NT;
+using simt::VS;
+using simt::ld_in;
 
 template <int DK> struct SimtSmem {
-    static constexpr int LDK = DK + 4;  // padded row of a [C][DK] table
-    static constexpr int LDC = C + 4;   // padded row of a [C][C] table
     float S[DK * VS];
-    float Kr[C * LDK];
-    float Qr[C * LDK];
-    float Kc[C * LDK];
-    float T[C * LDC];
-    float P[C * LDC];
-    float A[C * LDC];   // strictly lower A (only during the substitution)
+    simt::Tables<DK> tb;
     float R[C * VS];
     float U[C * VS];
-    float mu[DK];
-    float beta[C];
-    float part[4 * DK];
-    int slow;
 };
-
-template <typename TIn>
-__device__ __forceinline__ float ld_in(const TIn *p, int64_t i) { return to_f32(p[i]); }
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
-    constexpr int LDK = SimtSmem<DK>::LDK;
-    constexpr int LDC = SimtSmem<DK>::LDC;
+    simt::Tables<DK> &tb = sm.tb;
+    constexpr int LDK = simt::Tables<DK>::LDK;
+    constexpr int LDC = simt::Tables<DK>::LDC;
 
     if (a.dev_status && *a.dev_status != 0) return;
 
@@ -91,9 +78,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
     const TIn *q = (const TIn *)a.q;
     const TIn *k = (const TIn *)a.k;
     const TIn *v = (const TIn *)a.v;
-    TIn *o = (TIn *)a.o;
+    TIn *o = (TIn *)a.o;  // may be null when only the chunk states are wanted
     bool fresh;
     const int64_t state_off = (slot_of(a.slots, n, fresh) * H + h) * DK * DV;
+    // chunk states (equal-length batches only): the state before chunk i of
+    // (sequence n, head h) at chunk_states + ((n H + h) NC + i) DK DV
+    const int64_t NCs = ((int64_t)a.T + C - 1) / C;
+    float *cst = a.chunk_states ? a.chunk_states + ((int64_t)n * H + h) * NCs * DK * DV : nullptr;
 
     // ---- initial state slice ----
     for (int e = tid; e < DK * VS; e += NT) {
@@ -109,63 +100,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         const int64_t tok0 = t_begin + t0;
 
-        // ---- gate products, factors and the gated tables (one thread per
-        //      channel and token segment) ----
-        {
-            constexpr int SEG = NT / DK;       // token segments per channel
-            constexpr int TPS = C / SEG;       // tokens per segment
-            const int c = tid % DK, seg = tid / DK;
-            float al[TPS];
-            float prod = 1.f;
-#pragma unroll
-            for (int i = 0; i < TPS; ++i) {
-                const int r = seg * TPS + i;
-                al[i] = r < L ? gate_at(a.alpha, a.gate, (tok0 + r) * H + h, c, DK) : 1.f;
-                prod *= al[i];
-            }
-            sm.part[seg * DK + c] = prod;
-            if (tid == 0) sm.slow = 0;
-            __syncthreads();
-            float before = 1.f, after = 1.f, gamma = 1.f;
-#pragma unroll
-            for (int s2 = 0; s2 < SEG; ++s2) {
-                const float pt = sm.part[s2 * DK + c];
-                if (s2 < seg) before *= pt;
-                if (s2 > seg) after *= pt;
-                gamma *= pt;
-            }
-            if (gamma < kMinGamma) sm.slow = 1;
-            const float mu = sqrtf(gamma);
-            const float inv_mu = 1.f / mu;
-            if (seg == 0) sm.mu[c] = mu;
-            // prefix (inclusive) and suffix (exclusive) products in this segment
-            float pre = before;
-            float suf[TPS];
-            float s_acc = after;
-#pragma unroll
-            for (int i = TPS - 1; i >= 0; --i) {
-                suf[i] = s_acc;
-                s_acc *= al[i];
-            }
-#pragma unroll
-            for (int i = 0; i < TPS; ++i) {
-                const int r = seg * TPS + i;
-                pre *= al[i];
-                float kk = 0.f, qq = 0.f;
-                if (r < L) {
-                    kk = ld_in(k, ((tok0 + r) * H + h) * DK + c);
-                    qq = ld_in(q, ((tok0 + r) * H + h) * DK + c);
-                }
-                const float e2 = pre * inv_mu, e3 = suf[i] * inv_mu;
-                sm.Kr[r * LDK + c] = kk * e2;
-                sm.Qr[r * LDK + c] = qq * e2;
-                sm.Kc[r * LDK + c] = kk * e3;
-            }
-            if (tid < C) sm.beta[tid] = tid < L ? a.beta[(tok0 + tid) * H + h] : 0.f;
-        }
-        __syncthreads();
+        if (cst)  // the state this chunk starts from
+            for (int e = tid; e < DK * VS; e += NT)
+                cst[(t0 / C) * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[e];
 
-        if (sm.slow) {
+        // ---- gate products, factors and the gated tables ----
+        simt::gate_tables<DK, TIn>(tb, a.alpha, a.gate, q, k, a.beta, tok0, L, H, h);
+
+        if (tb.slow) {
             // ---- exact token-by-token fallback for strongly decaying chunks ----
             for (int r = 0; r < L; ++r) {
                 const int64_t tk = (tok0 + r) * H + h;
@@ -190,7 +132,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 }
                 sm.R[part * VS + j] = op;
                 __syncthreads();
-                if (tid < VS) {
+                if (tid < VS && o) {
                     float s = 0.f;
                     for (int p2 = 0; p2 < NT / VS; ++p2) s += sm.R[p2 * VS + tid];
                     o[tk * DV + v0 + tid] = from_f32<TIn>(s);
@@ -200,56 +142,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
             continue;
         }
 
-        // ---- A = beta (Kr Kc^T) strictly lower, P = Qr Kc^T lower incl. diag ----
-        {
-            float accA[4][4], accP[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) accA[i][jj] = accP[i][jj] = 0.f;
-            for (int c = 0; c < DK; c += 4) {
-                float4 kr[4], qr[4], kc[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    kr[i] = *reinterpret_cast<const float4 *>(&sm.Kr[(ty + 16 * i) * LDK + c]);
-                    qr[i] = *reinterpret_cast<const float4 *>(&sm.Qr[(ty + 16 * i) * LDK + c]);
-                    kc[i] = *reinterpret_cast<const float4 *>(&sm.Kc[(tx + 16 * i) * LDK + c]);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        accA[i][jj] += kr[i].x * kc[jj].x + kr[i].y * kc[jj].y +
-                                       kr[i].z * kc[jj].z + kr[i].w * kc[jj].w;
-                        accP[i][jj] += qr[i].x * kc[jj].x + qr[i].y * kc[jj].y +
-                                       qr[i].z * kc[jj].z + qr[i].w * kc[jj].w;
-                    }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int r = ty + 16 * i, j = tx + 16 * jj;
-                    sm.A[r * LDC + j] = j < r ? sm.beta[r] * accA[i][jj] : 0.f;
-                    sm.P[r * LDC + j] = j <= r ? accP[i][jj] : 0.f;
-                }
-        }
-        __syncthreads();
-
-        // ---- T = (I + A)^{-1}, one row at a time (forward substitution) ----
-        {
-            const int j = tid / 4, part = tid % 4;  // column j, 4-way split of the sum
-            for (int r = 0; r < C; ++r) {
-                float s = 0.f;
-                if (j < r)
-                    for (int sidx = j + part; sidx < r; sidx += 4)
-                        s += sm.A[r * LDC + sidx] * sm.T[sidx * LDC + j];
-                s += __shfl_xor_sync(0xffffffffu, s, 1);
-                s += __shfl_xor_sync(0xffffffffu, s, 2);
-                if (part == 0) sm.T[r * LDC + j] = j < r ? -s : (j == r ? 1.f : 0.f);
-                __syncthreads();
-            }
-        }
+        // ---- A = beta (Kr Kc^T) strictly lower, P = Qr Kc^T, T = (I + A)^{-1} ----
+        simt::wy_tables<DK>(tb);
 
         // ---- X = Kr St, Y = Qr St (St = Diag(mu) S0), R = beta (V - X) ----
         float y[4][4];
@@ -263,12 +157,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 float4 kr[4], qr[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    kr[i] = *reinterpret_cast<const float4 *>(&sm.Kr[(ty + 16 * i) * LDK + c]);
-                    qr[i] = *reinterpret_cast<const float4 *>(&sm.Qr[(ty + 16 * i) * LDK + c]);
+                    kr[i] = *reinterpret_cast<const float4 *>(&tb.Kr[(ty + 16 * i) * LDK + c]);
+                    qr[i] = *reinterpret_cast<const float4 *>(&tb.Qr[(ty + 16 * i) * LDK + c]);
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const float m = sm.mu[c + cc];
+                    const float m = tb.mu[c + cc];
                     float4 s4 = *reinterpret_cast<const float4 *>(&sm.S[(c + cc) * VS + 4 * tx]);
                     s4.x *= m; s4.y *= m; s4.z *= m; s4.w *= m;
 #pragma unroll
@@ -283,7 +177,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = ty + 16 * i;
-                const float b = sm.beta[r];
+                const float b = tb.beta[r];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj) : 0.f;
@@ -304,7 +198,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 float4 t4[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    t4[i] = *reinterpret_cast<const float4 *>(&sm.T[(ty + 16 * i) * LDC + j]);
+                    t4[i] = *reinterpret_cast<const float4 *>(&tb.T[(ty + 16 * i) * LDC + j]);
 #pragma unroll
                 for (int jj2 = 0; jj2 < 4; ++jj2) {
                     const float4 r4 = *reinterpret_cast<const float4 *>(&sm.R[(j + jj2) * VS + 4 * tx]);
@@ -328,7 +222,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 float4 p4[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    p4[i] = *reinterpret_cast<const float4 *>(&sm.P[(ty + 16 * i) * LDC + j]);
+                    p4[i] = *reinterpret_cast<const float4 *>(&tb.P[(ty + 16 * i) * LDC + j]);
 #pragma unroll
                 for (int jj2 = 0; jj2 < 4; ++jj2) {
                     const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[(j + jj2) * VS + 4 * tx]);
@@ -342,7 +236,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = ty + 16 * i;
-                if (r < L) {
+                if (r < L && o) {
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         o[((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj] = from_f32<TIn>(y[i][jj]);
@@ -365,7 +259,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[j * VS + 4 * tx]);
 #pragma unroll
                 for (int b2 = 0; b2 < RB; ++b2) {
-                    const float4 k4 = *reinterpret_cast<const float4 *>(&sm.Kc[j * LDK + 64 * b2 + 4 * ty]);
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&tb.Kc[j * LDK + 64 * b2 + 4 * ty]);
                     const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -380,7 +274,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = 64 * b2 + 4 * ty + i;
-                    const float m = sm.mu[c];
+                    const float m = tb.mu[c];
                     float4 s4 = *reinterpret_cast<float4 *>(&sm.S[c * VS + 4 * tx]);
                     s4.x = m * (m * s4.x + acc[b2][i][0]);
                     s4.y = m * (m * s4.y + acc[b2][i][1]);

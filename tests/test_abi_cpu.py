@@ -266,3 +266,22 @@ def test_selftest_argument_checks(lib):
     assert b"stall_chunk" in lib.kda_last_error()
     assert lib.kda_selftest_bounded_wait(p, p, p, p, p, p, None, 256, -1, None) == 1
     assert lib.kda_selftest_bounded_wait(None, p, p, p, p, p, None, 256, 0, None) == 1
+
+
+def test_backward_argument_checks(lib):
+    p = ctypes.c_void_p(0x1000)
+    ws = lib.kda_prefill_backward_workspace_bytes(2, 130, 3, 128, 128)
+    assert ws == 2 * 2 * 3 * 3 * 128 * 128 * 4  # state and state gradient per chunk
+    args = [p, p, p, 1, p, p, None, p, None, p, p, p, p, p, None, 2, 130, 3, 128, 128]
+    assert lib.kda_prefill_backward(*args, None, 0, None) == 5           # no workspace
+    assert lib.kda_prefill_backward(*args, ctypes.c_void_p(0x1008), ws, None) == 5  # misaligned
+    bad = list(args)
+    bad[9] = None                                                        # dq
+    assert lib.kda_prefill_backward(*bad, p, ws, None) == 1
+    bad = list(args)
+    bad[18] = 96                                                         # d_k
+    assert lib.kda_prefill_backward(*bad, p, ws, None) == 2
+    # nothing to do for B = 0
+    z = list(args)
+    z[15] = 0
+    assert lib.kda_prefill_backward(*z, None, 0, None) == 0
