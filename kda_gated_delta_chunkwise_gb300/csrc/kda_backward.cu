@@ -102,6 +102,10 @@ template <int DK> struct ChainSmem {
     float red[4 * VS];
 };
 
+static_assert(offsetof(ChainSmem<128>, dO) % 16 == 0 && offsetof(ChainSmem<64>, dO) % 16 == 0 &&
+                  offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, tb) % 16 == 0,
+              "float4 accesses need 16-byte offsets");
+
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -227,6 +231,9 @@ template <int DK> struct LocalSmem {
     float W[3][C * LDC];  // work tiles; tb.A is the fourth
     float red[16 * DK];   // per-thread-row partial sums over columns
 };
+
+static_assert(offsetof(LocalSmem<128>, W) % 16 == 0 && offsetof(LocalSmem<64>, W) % 16 == 0,
+              "float4 accesses need 16-byte offsets");
 
 template <int DK, typename TIn>
 __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, const float *Sg, const float *Gg,

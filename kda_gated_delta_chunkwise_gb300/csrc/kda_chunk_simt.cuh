@@ -16,6 +16,8 @@
 // Rows past the end of the sequence read as k = q = 0, alpha = 1, beta = 0.
 #pragma once
 
+#include <cstddef>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -26,7 +28,9 @@ constexpr int VS = 64;         // value columns per CTA
 constexpr int NT = 256;        // threads per CTA
 constexpr float kMinGamma = 1.8e-35f;  // ~exp(-80): chunk decay limit of the WY form
 
-template <int DK> struct Tables {
+// 16-byte aligned (and so sized in multiples of 16 bytes): the kernels read
+// these tables, and the shared-memory arrays placed after them, as float4.
+template <int DK> struct alignas(16) Tables {
     static constexpr int LDK = DK + 4;  // padded row of a [C][DK] table
     static constexpr int LDC = C + 4;   // padded row of a [C][C] table
     float Kr[C * LDK];
@@ -40,6 +44,12 @@ template <int DK> struct Tables {
     float part[4 * DK];
     int slow;
 };
+
+static_assert(sizeof(Tables<64>) % 16 == 0 && sizeof(Tables<128>) % 16 == 0, "float4 alignment");
+static_assert(offsetof(Tables<128>, Qr) % 16 == 0 && offsetof(Tables<128>, Kc) % 16 == 0 &&
+                  offsetof(Tables<128>, T) % 16 == 0 && offsetof(Tables<128>, P) % 16 == 0 &&
+                  offsetof(Tables<128>, A) % 16 == 0 && offsetof(Tables<64>, T) % 16 == 0,
+              "float4 alignment");
 
 template <typename TIn>
 __device__ __forceinline__ float ld_in(const TIn *p, int64_t i) { return to_f32(p[i]); }

@@ -49,6 +49,11 @@ template <int DK> struct SimtSmem {
     float U[C * VS];
 };
 
+static_assert(offsetof(SimtSmem<64>, R) % 16 == 0 && offsetof(SimtSmem<128>, R) % 16 == 0 &&
+                  offsetof(SimtSmem<64>, U) % 16 == 0 && offsetof(SimtSmem<128>, U) % 16 == 0 &&
+                  offsetof(SimtSmem<128>, tb) % 16 == 0,
+              "float4 accesses need 16-byte offsets");
+
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
