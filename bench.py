@@ -18,6 +18,7 @@ Prints ONE JSON line (rank 0). Keys beyond the basic contract:
   varlen        packed prefill of 64 lognormal-length sequences (306,055
                 tokens, 16 heads), and varlen_1m: the same lengths scaled to
                 2^20 tokens
+  backward      gradients of the benchmark workload (kda_prefill_backward)
   gate_variants the benchmark workload with a scalar gate, no gate, FP8 inputs
   clocks        SM clocks and throttle reasons sampled during the timed region
                 (and during about a second of the same steps just before it)
@@ -304,6 +305,34 @@ def bench_varlen(kda, W, x, dev, stream, peaks, steps, warmup, with_cpu, label):
     return res
 
 
+def backward_bytes(B, T, H, dk, dv, qkv_bytes=2):
+    """Algorithmic HBM bytes of one backward call: q, k, v, alpha, beta and
+    d_o read once, the fp32 gradients dq, dk, dalpha, dv, dbeta written once,
+    and the initial state's gradient written once."""
+    per_tok_head = (2 * dk + 2 * dv) * qkv_bytes + dk * 4 + 4 + (3 * dk + dv) * 4 + 4
+    return B * T * H * per_tok_head + B * H * dk * dv * 4
+
+
+def bench_backward(kda, W, dev, stream, peaks, steps, warmup):
+    """Gradients of the 4x16x4096 prefill (kda_prefill_backward) for a random d_o."""
+    import torch
+    x = W.prefill_4x16x4096()
+    q, k, v, a, b = (t.to(dev) for t in x.tensors())
+    d_o = torch.randn(v.shape, generator=torch.Generator(device=dev).manual_seed(7), device=dev).to(v.dtype)
+    Bb, Tb, Hb = q.shape[0], q.shape[1], q.shape[2]
+    ws = torch_empty_bytes(kda.load().kda_prefill_backward_workspace_bytes(Bb, Tb, Hb, DK, DV), dev)
+    ms = time_events(lambda: kda.prefill_backward(q, k, v, a, b, d_o, workspace=ws), steps, warmup, stream)
+    nbytes = backward_bytes(Bb, Tb, Hb, DK, DV)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": f"kda_prefill_backward B={Bb} H={Hb} T={Tb} d_k={DK} d_v={DV}, bf16 q/k/v/d_o, fp32 gradients",
+           "value": Bb * Tb / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+           "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+           "kernels": "kda_prefill_simt (chunk states) + kda_bwd_chain + kda_bwd_local, fp32 on CUDA cores",
+           "workspace_bytes": ws.numel()}
+    del q, k, v, a, b, d_o, ws
+    return res
+
+
 def torch_empty_like(t):
     import torch
     return torch.empty_like(t)
@@ -372,6 +401,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the long-context and packed-batch legs")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -589,6 +619,10 @@ def main():
                               "two state batches in turn"}
         del states, dq, dk_, dv_, da, db, do
 
+    backward = None
+    if not args.no_backward:
+        torch.cuda.empty_cache()
+        backward = bench_backward(kda, W, dev, stream, peaks, args.steps, args.warmup)
     long_ctx = varlen = varlen_1m = None
     with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if not args.no_long:
@@ -614,7 +648,7 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": bench_config(world),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
-                "long_context": long_ctx, "varlen": varlen, "varlen_1m": varlen_1m,
+                "long_context": long_ctx, "varlen": varlen, "varlen_1m": varlen_1m, "backward": backward,
                 "gate_variants": variants,
                 "gpu_launches": args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)

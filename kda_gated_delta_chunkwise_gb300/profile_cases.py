@@ -12,6 +12,8 @@ CASE is one of:
   long_131k           one 131,072-token sequence with 32 heads (d=128, bf16)
   varlen_64seq        the packed batch of 64 lognormal-length sequences
   varlen_64seq_1m     the same lengths scaled to 2^20 tokens
+  backward_4x16x4096  the gradients of the benchmark workload (kda_prefill_backward)
+  backward_1x16x1024  a small case of it, for full ncu captures
   hostlink            no kernel: the host link's copy rates (page-locked host
                       memory to the device, back, and both at once), printed
 
@@ -88,6 +90,16 @@ def _varlen(x, reps: int):
     torch.cuda.synchronize()
 
 
+def _backward(B: int, T: int, reps: int):
+    dev = torch.device("cuda")
+    x = W.prefill_4x16x4096(B=B, T=T)
+    q, k, v, a, b = (t.to(dev) for t in x.tensors())
+    d_o = torch.randn(v.shape, generator=torch.Generator(device=dev).manual_seed(7), device=dev).to(v.dtype)
+    for _ in range(reps):
+        kda.prefill_backward(q, k, v, a, b, d_o)
+    torch.cuda.synchronize()
+
+
 def _hostlink(reps: int):
     """Copy rates between page-locked host memory and the device: 256 MiB
     buffers, each direction alone on its own stream, then both directions
@@ -149,6 +161,8 @@ CASES = {
     "varlen_64seq": lambda r: _varlen(W.varlen_64seq(), r),
     "varlen_64seq_1m": lambda r: _varlen(W.varlen_64seq_1m(), r),
     "hostlink": _hostlink,
+    "backward_4x16x4096": lambda r: _backward(4, 4096, r),
+    "backward_1x16x1024": lambda r: _backward(1, 1024, r),
 }
 
 
