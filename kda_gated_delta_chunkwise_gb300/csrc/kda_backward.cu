@@ -60,21 +60,61 @@ struct BwdParams {
     int N, T, H, DV, NC;
 };
 
-// acc[i][jj] += sum_{m < K} a(ty + 16 i, m) * b(m, 4 tx + jj)
-template <int K, typename FA, typename FB>
-__device__ __forceinline__ void mm(float (&acc)[4][4], FA a, FB b) {
+// acc[i][jj] += sum_{m < K} a(ty + 16 i, m) * b(m, 4 tx + jj), with 16-byte
+// loads, K in steps of 4, operands given by pointer and leading dimension
+// (shared or global memory):
+//   MM_NN: a(r, m) = A[r lda + m], b(m, c) = B[m ldb + c]
+//   MM_NT: a(r, m) = A[r lda + m], b(m, c) = B[c ldb + m]
+//   MM_TN: a(r, m) = A[m lda + r], b(m, c) = B[m ldb + c]
+// ks (nullable) scales the terms of index m. A, B, lda, ldb keep 16-byte
+// alignment of the rows read as float4.
+enum Mode { MM_NN, MM_NT, MM_TN };
+template <int K, Mode MODE>
+__device__ __forceinline__ void mm4(float (&acc)[4][4], const float *__restrict__ A, int lda,
+                                    const float *__restrict__ B, int ldb, const float *__restrict__ ks = nullptr) {
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
 #pragma unroll 2
-    for (int m = 0; m < K; ++m) {
-        float av[4], bv[4];
+    for (int m = 0; m < K; m += 4) {
+        float a[4][4], b[4][4];  // a[i][u] = a(ty + 16 i, m + u), b[u][jj] = b(m + u, 4 tx + jj)
+        if (MODE == MM_TN) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = a(ty + 16 * i, m);
+            for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) bv[jj] = b(m, 4 * tx + jj);
+                for (int i = 0; i < 4; ++i) a[i][u] = A[(m + u) * lda + ty + 16 * i];
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 4; ++i) {
+                const float4 f = *reinterpret_cast<const float4 *>(A + (ty + 16 * i) * lda + m);
+                a[i][0] = f.x; a[i][1] = f.y; a[i][2] = f.z; a[i][3] = f.w;
+            }
+        }
+        if (MODE == MM_NT) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) acc[i][jj] += av[i] * bv[jj];
+            for (int jj = 0; jj < 4; ++jj) {
+                const float4 f = *reinterpret_cast<const float4 *>(B + (4 * tx + jj) * ldb + m);
+                b[0][jj] = f.x; b[1][jj] = f.y; b[2][jj] = f.z; b[3][jj] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 f = *reinterpret_cast<const float4 *>(B + (m + u) * ldb + 4 * tx);
+                b[u][0] = f.x; b[u][1] = f.y; b[u][2] = f.z; b[u][3] = f.w;
+            }
+        }
+        if (ks) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float sc = ks[m + u];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) b[u][jj] *= sc;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[i][jj] += a[i][u] * b[u][jj];
     }
 }
 
@@ -169,9 +209,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         float acc[4][4];
         // dU = Kc Gt + P^T dO
         zero(acc);
-        mm<DK>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
-               [&](int c, int j) { return tb.mu[c] * sm.G[c * VS + j]; });
-        mm<C>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * VS + j]; });
+        mm4<DK, MM_NN>(acc, tb.Kc, LDK, sm.G, VS, tb.mu);
+        mm4<C, MM_TN>(acc, tb.P, LDC, sm.dO, VS);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -179,7 +218,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         __syncthreads();
         // dX = -Diag(beta) T^T dU (into dU's place)
         zero(acc);
-        mm<C>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; });
+        mm4<C, MM_TN>(acc, tb.T, LDC, dU, LDC);
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -376,7 +415,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
     }
     zero(acc);
-    mm<DK>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, S_);
+    mm4<DK, MM_NN>(acc, tb.Kr, LDK, Sg + v0, DV, tb.mu);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = ty + 16 * i;
@@ -389,14 +428,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     __syncthreads();
     // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
     zero(acc);
-    mm<C>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; });
+    mm4<C, MM_NN>(acc, tb.T, LDC, WB, LDC, tb.beta);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) WC[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
     zero(acc);
-    mm<DK>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, G_);
-    mm<C>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; });
+    mm4<DK, MM_NN>(acc, tb.Kc, LDK, Gg + v0, DV, tb.mu);
+    mm4<C, MM_TN>(acc, tb.P, LDC, WD, LDC);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -405,9 +444,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // dT = dU R^T (registers); dR = T^T dU: dV, the first part of dbeta, dX
     float dT[4][4], dR[4][4];
     zero(dT);
-    mm<VS>(dT, [&](int r, int j) { return WA[r * LDC + j]; }, [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; });
+    mm4<VS, MM_NT>(dT, WA, LDC, WB, LDC);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) dT[i][jj] *= tb.beta[4 * tx + jj];
     zero(dR);
-    mm<C>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; });
+    mm4<C, MM_TN>(dR, tb.T, LDC, WA, LDC);
     float dbeta_r[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -434,12 +477,16 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // dP = lower(dO U^T) (registers); dKc = U Gt^T
     float dP[4][4];
     zero(dP);
-    mm<VS>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; });
+    mm4<VS, MM_NT>(dP, WD, LDC, WC, LDC);
     float dKc[RB][4][4], dQr[RB][4][4], dKr[RB][4][4], s123[RB][4];
 #pragma unroll
     for (int b2 = 0; b2 < RB; ++b2) {
         zero(dKc[b2]);
-        mm<VS>(dKc[b2], [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return G_(c + 64 * b2, j); });
+        mm4<VS, MM_NT>(dKc[b2], WC, LDC, Gg + (int64_t)64 * b2 * DV + v0, DV);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) dKc[b2][i][jj] *= tb.mu[64 * b2 + 4 * tx + jj];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             float s = 0.f;
@@ -462,8 +509,16 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     for (int b2 = 0; b2 < RB; ++b2) {
         zero(dQr[b2]);
         zero(dKr[b2]);
-        mm<VS>(dQr[b2], [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return S_(c + 64 * b2, j); });
-        mm<VS>(dKr[b2], [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return S_(c + 64 * b2, j); });
+        mm4<VS, MM_NT>(dQr[b2], WD, LDC, Sg + (int64_t)64 * b2 * DV + v0, DV);
+        mm4<VS, MM_NT>(dKr[b2], WB, LDC, Sg + (int64_t)64 * b2 * DV + v0, DV);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float m = tb.mu[64 * b2 + 4 * tx + jj];
+                dQr[b2][i][jj] *= m;
+                dKr[b2][i][jj] *= m;
+            }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             float s = 0.f;
@@ -475,14 +530,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             s123[b2][jj] += s;
         }
         // dQr += dP Kc;  dKc += dP^T Qr
-        mm<C>(dQr[b2], [&](int r, int m) { return WC[r * LDC + m]; },
-              [&](int m, int c) { return tb.Kc[m * LDK + c + 64 * b2]; });
-        mm<C>(dKc[b2], [&](int r, int m) { return WC[m * LDC + r]; },
-              [&](int m, int c) { return tb.Qr[m * LDK + c + 64 * b2]; });
+        mm4<C, MM_NN>(dQr[b2], WC, LDC, tb.Kc + 64 * b2, LDK);
+        mm4<C, MM_TN>(dKc[b2], WC, LDC, tb.Qr + 64 * b2, LDK);
     }
     // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
     zero(acc);
-    mm<C>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; });
+    mm4<C, MM_NT>(acc, WA, LDC, tb.T, LDC);
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -490,7 +543,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int jj = 0; jj < 4; ++jj) WD[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
     __syncthreads();
     zero(acc);
-    mm<C>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; });
+    mm4<C, MM_TN>(acc, tb.T, LDC, WD, LDC);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -504,7 +557,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     for (int b2 = 0; b2 < RB; ++b2) {
         float t[4][4];
         zero(t);
-        mm<C>(t, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c + 64 * b2]; });
+        mm4<C, MM_NN>(t, WA, LDC, tb.Kc + 64 * b2, LDK);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = ty + 16 * i;
@@ -516,8 +569,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             }
             dbeta_r[i] += sum16(s);
         }
-        mm<C>(dKc[b2], [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
-              [&](int m, int c) { return tb.Kr[m * LDK + c + 64 * b2]; });
+        mm4<C, MM_TN>(dKc[b2], WA, LDC, tb.Kr + 64 * b2, LDK, tb.beta);
     }
     if (tx == 0)
 #pragma unroll
