@@ -577,23 +577,21 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             const int r = ty + 16 * i;
             if (r < L) atomicAdd(&p.dbeta[(tok0 + r) * H + h], dbeta_r[i]);
         }
-    // dq, dk with this thread's p (running gate products over the chunk's rows),
-    // and d log p into Qr's place
+    // the chunk's gate factors p / mu (as in the forward tables) into the free
+    // work tiles; dq, dk, and d log p into Qr's place
+    float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
+    static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
+    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, KDA_GATE_CHANNEL, tok0, L, H, h);
     float dlogp[RB][4][4];
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2) {
+    for (int b2 = 0; b2 < RB; ++b2)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int c = 64 * b2 + 4 * tx + jj;
-            const float mu = tb.mu[c];
-            float pr = 1.f;
-            int m = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = ty + 16 * i, rc = r * LDK + c;
-                for (; m <= r; ++m)
-                    if (m < L) pr *= p.alpha[((tok0 + m) * H + h) * DK + c];
-                const float e2 = pr / mu, e3 = mu / pr;
+                const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
                 if (r < L) {
                     const int64_t th = (tok0 + r) * H + h;
                     atomicAdd(&p.dq[th * DK + c], dQr[b2][i][jj] * e2);
@@ -602,6 +600,18 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
                 dlogp[b2][i][jj] = dKr[b2][i][jj] * tb.Kr[rc] + dQr[b2][i][jj] * tb.Qr[rc] - dKc[b2][i][jj] * tb.Kc[rc];
             }
         }
+    // sum_v St Gt per channel: channel c, value columns of part hp (16-byte loads)
+    {
+        constexpr int NH = NT / DK, CW = VS / NH;
+        const int c = tid % DK, hp = tid / DK;
+        const float *sr = Sg + (int64_t)c * DV + v0 + hp * CW, *gr = Gg + (int64_t)c * DV + v0 + hp * CW;
+        float s0 = 0.f;
+#pragma unroll
+        for (int j = 0; j < CW; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(sr + j), g4 = *reinterpret_cast<const float4 *>(gr + j);
+            s0 += a4.x * g4.x + a4.y * g4.y + a4.z * g4.z + a4.w * g4.w;
+        }
+        tb.part[hp * DK + c] = tb.mu[c] * tb.mu[c] * s0;
     }
     __syncthreads();  // every read of Qr is done
 #pragma unroll
@@ -618,13 +628,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     if (tid < DK) {
         const int c = tid;
         float s0 = 0.f;
-        for (int j = 0; j < VS; ++j) s0 += S_(c, j) * G_(c, j);
+        for (int hp = 0; hp < NT / DK; ++hp) s0 += tb.part[hp * DK + c];
         float s123c = 0.f;
         for (int t2 = 0; t2 < 16; ++t2) s123c += sm.red[t2 * DK + c];
         float colsum = 0.f;
         for (int r = 0; r < L; ++r) colsum += tb.Qr[r * LDK + c];
         const float dlogmu = 2.f * s0 + s123c - colsum;
         float run = 0.5f * dlogmu;
+#pragma unroll 8
         for (int r = L - 1; r >= 0; --r) {
             run += tb.Qr[r * LDK + c];
             const int64_t th = (tok0 + r) * H + h;
