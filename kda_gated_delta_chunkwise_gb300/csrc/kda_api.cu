@@ -334,9 +334,7 @@ kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, k
     b.q = q; b.k = k; b.v = v; b.d_o = d_o; b.dt = qkv_dtype;
     b.alpha = alpha; b.beta = beta; b.s0 = initial_state; b.dsT = d_final_state;
     b.dq = dq; b.dk = dk; b.dvv = dv; b.dalpha = dalpha; b.dbeta = dbeta; b.ds0 = d_initial_state;
-    float *ws = static_cast<float *>(workspace);
-    b.states = ws;
-    b.gnext = ws ? ws + need / sizeof(float) / 2 : nullptr;
+    b.workspace = workspace;
     b.N = B; b.T = T; b.H = H; b.d_k = d_k; b.d_v = d_v;
     return cuda_status(kda::launch_backward(b, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
 }

@@ -30,8 +30,12 @@
 //   dS' = G - beta k w^T; dalpha = rowsum(dS' (.) S_{t-1}); G = Diag(alpha) dS'
 // with S_{t-1} replayed from the chunk's start state.
 //
-// Three launches after the forward (the fp32 chunk kernel, which also writes
-// the state before every chunk into the workspace):
+// Four launches:
+//   tables one CTA per (sequence, head, chunk), all chunks at once: the
+//          chunk's gate products and WY tables (Kr, Qr, Kc, T, P, mu, beta)
+//          into the workspace, so no serial pass rebuilds them;
+//   states one CTA per (sequence, head, 64-column value slice): the forward
+//          state chain, writing the state before every chunk;
 //   chain  one CTA per (sequence, head, 64-column value slice), chunks in
 //          reverse: writes dL/dS after every chunk into the workspace and the
 //          initial state's gradient;
@@ -55,10 +59,78 @@ struct BwdParams {
     const void *q, *k, *v, *d_o;
     const float *alpha, *beta, *dsT;
     float *dq, *dk, *dv, *dalpha, *dbeta, *ds0;
-    const float *states;  // [N, H, NC, DK, DV]: the state before every chunk
+    float *states;        // [N, H, NC, DK, DV]: the state before every chunk
     float *gnext;         // [N, H, NC, DK, DV]: dL/dS after every chunk
+    float *tabs;          // [N, H, NC, TabLayout<DK>::FLOATS]: every chunk's tables
     int N, T, H, DV, NC;
 };
+
+// Every chunk's tables, computed once by kda_bwd_tables_kernel (all chunks at
+// once) and read by the three passes that follow, so the serial chains do
+// not rebuild them: Kr, Qr, Kc [C][DK], T, P [C][C], mu [DK], beta [C], the
+// slow flag (its bits in a float), unpadded, in fp32.
+template <int DK> struct TabLayout {
+    static constexpr int KR = 0, QR = C * DK, KC = 2 * C * DK, T = 3 * C * DK, P = T + C * C, MU = P + C * C,
+                         BETA = MU + DK, SLOW = BETA + C, FLOATS = SLOW + 4;
+};
+enum TabPart : unsigned { TAB_KR = 1, TAB_QR = 2, TAB_KC = 4, TAB_T = 8, TAB_P = 16, TAB_ALL = 31 };
+
+template <int DK> __device__ void store_tables(const simt::Tables<DK> &tb, float *dst) {
+    using L = TabLayout<DK>;
+    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, Q4 = DK / 4, C4 = C / 4;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < C * Q4; e += NT) {
+        const int r = e / Q4, c = 4 * (e % Q4);
+        *reinterpret_cast<float4 *>(dst + L::KR + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Kr[r * LDK + c]);
+        *reinterpret_cast<float4 *>(dst + L::QR + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Qr[r * LDK + c]);
+        *reinterpret_cast<float4 *>(dst + L::KC + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Kc[r * LDK + c]);
+    }
+    if (!tb.slow)
+        for (int e = tid; e < C * C4; e += NT) {
+            const int r = e / C4, c = 4 * (e % C4);
+            *reinterpret_cast<float4 *>(dst + L::T + r * C + c) = *reinterpret_cast<const float4 *>(&tb.T[r * LDC + c]);
+            *reinterpret_cast<float4 *>(dst + L::P + r * C + c) = *reinterpret_cast<const float4 *>(&tb.P[r * LDC + c]);
+        }
+    for (int e = tid; e < DK; e += NT) dst[L::MU + e] = tb.mu[e];
+    for (int e = tid; e < C; e += NT) dst[L::BETA + e] = tb.beta[e];
+    if (tid == 0) dst[L::SLOW] = __int_as_float(tb.slow);
+}
+
+// Loads the parts `which` (TAB_*) of a chunk's tables, plus mu, beta and the
+// slow flag; T and P only when the chunk is not slow. Ends with a barrier.
+template <int DK> __device__ void load_tables(simt::Tables<DK> &tb, const float *src, unsigned which) {
+    using L = TabLayout<DK>;
+    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, Q4 = DK / 4, C4 = C / 4;
+    const int tid = threadIdx.x;
+    const int slow = __float_as_int(src[L::SLOW]);
+    for (int e = tid; e < C * Q4; e += NT) {
+        const int r = e / Q4, c = 4 * (e % Q4);
+        if (which & TAB_KR)
+            *reinterpret_cast<float4 *>(&tb.Kr[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::KR + r * DK + c);
+        if (which & TAB_QR)
+            *reinterpret_cast<float4 *>(&tb.Qr[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::QR + r * DK + c);
+        if (which & TAB_KC)
+            *reinterpret_cast<float4 *>(&tb.Kc[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::KC + r * DK + c);
+    }
+    if (!slow)
+        for (int e = tid; e < C * C4; e += NT) {
+            const int r = e / C4, c = 4 * (e % C4);
+            if (which & TAB_T)
+                *reinterpret_cast<float4 *>(&tb.T[r * LDC + c]) = *reinterpret_cast<const float4 *>(src + L::T + r * C + c);
+            if (which & TAB_P)
+                *reinterpret_cast<float4 *>(&tb.P[r * LDC + c]) = *reinterpret_cast<const float4 *>(src + L::P + r * C + c);
+        }
+    for (int e = tid; e < DK; e += NT) tb.mu[e] = src[L::MU + e];
+    for (int e = tid; e < C; e += NT) tb.beta[e] = src[L::BETA + e];
+    if (tid == 0) tb.slow = slow;
+    __syncthreads();
+}
+
+// Pulls a chunk's tables into L2 ahead of their use (128-byte lines).
+template <int DK> __device__ __forceinline__ void prefetch_tables(const float *src) {
+    constexpr int LINES = (TabLayout<DK>::FLOATS * 4 + 127) / 128;
+    for (int l = threadIdx.x; l < LINES; l += NT) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 32 * l));
+}
 
 // acc[i][jj] += sum_{m < K} a(ty + 16 i, m) * b(m, 4 tx + jj), with 16-byte
 // loads, K in steps of 4, operands given by pointer and leading dimension
@@ -134,6 +206,139 @@ __device__ __forceinline__ float sum16(float x) {
     return x;
 }
 
+// ---------------------------------------------------------------- tables
+// One CTA per (sequence, head, chunk): the chunk's tables into the workspace.
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    simt::Tables<DK> &tb = *reinterpret_cast<simt::Tables<DK> *>(smem_raw);
+    const int64_t idx = blockIdx.x;  // (n H + h) NC + ci
+    const int ci = (int)(idx % p.NC), h = (int)((idx / p.NC) % p.H), n = (int)(idx / ((int64_t)p.NC * p.H));
+    const int64_t t0 = (int64_t)ci * C;
+    const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
+    const int64_t tok0 = (int64_t)n * p.T + t0;
+    simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
+                               p.H, h);
+    if (!tb.slow) simt::wy_tables<DK>(tb);
+    store_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS);
+}
+
+// ---------------------------------------------------------------- states
+// The forward chain only: one CTA per (sequence, head, value slice) writes the
+// state before every chunk (S_{n+1} = Diag(mu) (Diag(mu) S_n + Kc^T U), U =
+// T Diag(beta) (V - Kr Diag(mu) S_n)), reading the chunk's tables; slow
+// chunks go token by token (the §四 update).
+template <int DK> struct StatesSmem {
+    float S[DK * VS];
+    simt::Tables<DK> tb;
+    float R[C * VS];
+    float U[C * VS];
+};
+static_assert(offsetof(StatesSmem<128>, R) % 16 == 0 && offsetof(StatesSmem<64>, R) % 16 == 0 &&
+                  offsetof(StatesSmem<128>, U) % 16 == 0 && offsetof(StatesSmem<64>, U) % 16 == 0 &&
+                  offsetof(StatesSmem<128>, tb) % 16 == 0 && offsetof(StatesSmem<64>, tb) % 16 == 0,
+              "float4 accesses need 16-byte offsets");
+
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, const float *s0) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    StatesSmem<DK> &sm = *reinterpret_cast<StatesSmem<DK> *>(smem_raw);
+    simt::Tables<DK> &tb = sm.tb;
+    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, RB = DK / 64;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int nslices = p.DV / VS;
+    const int slice = blockIdx.x % nslices;
+    const int h = (blockIdx.x / nslices) % p.H;
+    const int n = blockIdx.x / (nslices * p.H);
+    const int H = p.H, DV = p.DV, v0 = slice * VS;
+    const int64_t T = p.T, t_begin = (int64_t)n * p.T, sh = (int64_t)n * H + h;
+    const TIn *k = (const TIn *)p.k, *v = (const TIn *)p.v;
+    float *st = p.states + sh * p.NC * DK * DV;
+    const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
+    for (int e = tid; e < DK * VS; e += NT)
+        sm.S[e] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    __syncthreads();
+    for (int ci = 0; ci < p.NC; ++ci) {
+        const int64_t t0 = (int64_t)ci * C, tok0 = t_begin + t0;
+        const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
+        for (int e = tid; e < DK * VS; e += NT)
+            st[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[e];
+        load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
+        if (ci + 1 < p.NC) prefetch_tables<DK>(tabs + (int64_t)(ci + 1) * TabLayout<DK>::FLOATS);
+        if (tb.slow) {
+            const int j = tid % VS, part = tid / VS;
+            for (int r = 0; r < L; ++r) {
+                const int64_t tk = (tok0 + r) * H + h;
+                float vh = 0.f;
+                for (int c = part; c < DK; c += NT / VS) vh += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * sm.S[c * VS + j];
+                sm.R[part * VS + j] = vh;
+                __syncthreads();
+                float vs = 0.f;
+#pragma unroll
+                for (int p2 = 0; p2 < NT / VS; ++p2) vs += sm.R[p2 * VS + j];
+                const float be = p.beta[tk] * (ld_in(v, tk * DV + v0 + j) - vs);
+                __syncthreads();
+                for (int c = part; c < DK; c += NT / VS)
+                    sm.S[c * VS + j] = p.alpha[tk * DK + c] * sm.S[c * VS + j] + ld_in(k, tk * DK + c) * be;
+                __syncthreads();
+            }
+            continue;
+        }
+        float acc[4][4];
+        // R = Diag(beta) (V - Kr St)
+        zero(acc);
+        mm4<DK, MM_NN>(acc, tb.Kr, LDK, sm.S, VS, tb.mu);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = ty + 16 * i;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj) : 0.f;
+                sm.R[r * VS + 4 * tx + jj] = tb.beta[r] * (vv - acc[i][jj]);
+            }
+        }
+        __syncthreads();
+        // U = T R
+        zero(acc);
+        mm4<C, MM_NN>(acc, tb.T, LDC, sm.R, VS);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4 *>(&sm.U[(ty + 16 * i) * VS + 4 * tx]) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        __syncthreads();
+        // S <- Diag(mu) (Diag(mu) S + Kc^T U); tile rows 64 b2 + 4 ty + i, columns 4 tx + jj
+        float acc2[RB][4][4];
+#pragma unroll
+        for (int b2 = 0; b2 < RB; ++b2) zero(acc2[b2]);
+        for (int r = 0; r < C; ++r) {
+            const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[r * VS + 4 * tx]);
+            const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int b2 = 0; b2 < RB; ++b2) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(&tb.Kc[r * LDK + 64 * b2 + 4 * ty]);
+                const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) acc2[b2][i][jj] += kv[i] * uv[jj];
+            }
+        }
+#pragma unroll
+        for (int b2 = 0; b2 < RB; ++b2)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = 64 * b2 + 4 * ty + i;
+                const float m = tb.mu[c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float &sv = sm.S[c * VS + 4 * tx + jj];
+                    sv = m * (m * sv + acc2[b2][i][jj]);
+                }
+            }
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- chain
 template <int DK> struct ChainSmem {
     float G[DK * VS];
@@ -163,6 +368,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *dO = (const TIn *)p.d_o;
     const int64_t sh = (int64_t)n * H + h;
     float *gn = p.gnext + sh * p.NC * DK * DV;
+    const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
 
     for (int e = tid; e < DK * VS; e += NT)
         sm.G[e] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
@@ -174,13 +380,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         const int64_t tok0 = t_begin + t0;
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
             gn[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[e];
-        simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, q, k, p.beta, tok0, L, H, h);
         for (int e = tid; e < C * VS; e += NT) {
             const int r = e / VS;
             sm.dO[e] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
         }
+        load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
+        if (ci > 0) prefetch_tables<DK>(tabs + (int64_t)(ci - 1) * TabLayout<DK>::FLOATS);
         if (tb.slow) {
-            __syncthreads();
             // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
             const int j = tid % VS, part = tid / VS;
             for (int r = L - 1; r >= 0; --r) {
@@ -204,8 +410,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
             }
             continue;
         }
-        simt::wy_tables<DK>(tb);  // (ends with a barrier: dO is staged too)
-        float *dU = tb.A;         // free once T exists
+        float *dU = tb.A;  // a work tile here
         float acc[4][4];
         // dU = Kc Gt + P^T dO
         zero(acc);
@@ -394,16 +599,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     const int64_t t0 = (int64_t)ci * C;
     const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
     const int64_t tok0 = (int64_t)n * p.T + t0;
-    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
+    const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
     const int64_t off = (((int64_t)n * H + h) * p.NC + ci) * DK * DV;
     const float *Sg = p.states + off, *Gg = p.gnext + off;
 
-    simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, q, k, p.beta, tok0, L, H, h);
+    load_tables<DK>(tb, p.tabs + ((((int64_t)n * H + h) * p.NC + ci) * TabLayout<DK>::FLOATS), TAB_ALL);
     if (tb.slow) {
         local_slow<DK, TIn>(sm, p, Sg, Gg, tok0, L, h, v0);
         return;
     }
-    simt::wy_tables<DK>(tb);
     float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
     auto S_ = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };  // St
     auto G_ = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };  // Gt
@@ -648,44 +852,58 @@ template <int DK, typename TIn>
 cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     const int NC = (b.T + C - 1) / C;
     const int nslices = b.d_v / VS;
-    // 1. forward on CUDA cores, keeping the state before every chunk
-    PrefillArgs a{};
-    a.q = b.q; a.k = b.k; a.v = b.v; a.alpha = b.alpha; a.beta = b.beta; a.s0 = b.s0;
-    a.o = nullptr; a.sT = nullptr; a.gate = KDA_GATE_CHANNEL; a.slots = nullptr; a.cu_seqlens = nullptr;
-    a.N = b.N; a.T = b.T; a.H = b.H; a.dk = DK; a.dv = b.d_v; a.dt = b.dt;
-    a.chunk_states = b.states;
-    cudaError_t e = launch_prefill_simt(a, s);
-    if (e != cudaSuccess) return e;
+    const int64_t chunks = (int64_t)b.N * b.H * NC;
     BwdParams p;
     p.q = b.q; p.k = b.k; p.v = b.v; p.d_o = b.d_o; p.alpha = b.alpha; p.beta = b.beta; p.dsT = b.dsT;
     p.dq = b.dq; p.dk = b.dk; p.dv = b.dvv; p.dalpha = b.dalpha; p.dbeta = b.dbeta; p.ds0 = b.ds0;
-    p.states = b.states; p.gnext = b.gnext;
+    float *ws = static_cast<float *>(b.workspace);
+    p.states = ws;
+    p.gnext = ws + chunks * DK * b.d_v;
+    p.tabs = ws + 2 * chunks * DK * b.d_v;
     p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC;
-    // 2. the reverse state chain
+    cudaError_t e;
+    const unsigned heads = (unsigned)((int64_t)b.N * b.H * nslices);
+    if (chunks > 0) {  // 1. every chunk's tables, all chunks at once
+        auto tabk = kda_bwd_tables_kernel<DK, TIn>;
+        const size_t st = sizeof(simt::Tables<DK>);
+        if ((e = cudaFuncSetAttribute(tabk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st)) != cudaSuccess)
+            return e;
+        tabk<<<(unsigned)chunks, NT, st, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // 2. the state before every chunk
+        auto stk = kda_bwd_states_kernel<DK, TIn>;
+        const size_t ss = sizeof(StatesSmem<DK>);
+        if ((e = cudaFuncSetAttribute(stk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss)) != cudaSuccess)
+            return e;
+        stk<<<heads, NT, ss, s>>>(p, b.s0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 3. the reverse state-gradient chain (also for T = 0: dS_0 = dS_T)
     auto chain = kda_bwd_chain_kernel<DK, TIn>;
     const size_t sc = sizeof(ChainSmem<DK>);
     if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc)) != cudaSuccess) return e;
-    chain<<<(unsigned)((int64_t)b.N * b.H * nslices), NT, sc, s>>>(p);
+    chain<<<heads, NT, sc, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 3. the per-chunk gradients, added onto zeroed dq, dk, dalpha, dbeta
+    if (chunks == 0) return cudaSuccess;
+    // 4. the per-chunk gradients, added onto zeroed dq, dk, dalpha, dbeta
     const size_t tok = (size_t)b.N * b.T * b.H;
     if ((e = cudaMemsetAsync(b.dq, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(b.dk, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(b.dalpha, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(b.dbeta, 0, tok * sizeof(float), s)) != cudaSuccess) return e;
-    if (NC == 0) return cudaSuccess;
     auto local = kda_bwd_local_kernel<DK, TIn>;
     const size_t sl = sizeof(LocalSmem<DK>);
     if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
-    local<<<(unsigned)((int64_t)b.N * b.H * NC * nslices), NT, sl, s>>>(p);
+    local<<<(unsigned)(chunks * nslices), NT, sl, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv) {
-    const size_t NC = ((size_t)T + C - 1) / C;
-    return 2 * (size_t)N * H * NC * dk * dv * sizeof(float);
+    const size_t chunks = (size_t)N * H * (((size_t)T + C - 1) / C);
+    const size_t tab = dk == 128 ? TabLayout<128>::FLOATS : TabLayout<64>::FLOATS;
+    return (2 * chunks * dk * dv + chunks * tab) * sizeof(float);
 }
 
 cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s) {

@@ -82,7 +82,7 @@ struct BackwardArgs {
     const float *alpha, *beta, *s0, *dsT;  // s0, dsT nullable (zeros)
     float *dq, *dk, *dvv, *dalpha, *dbeta;
     float *ds0;                            // nullable
-    float *states, *gnext;                 // workspace: backward_workspace_bytes
+    void *workspace;                       // backward_workspace_bytes, 16-byte aligned
     int N, T, H, d_k, d_v;
 };
 size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv);
