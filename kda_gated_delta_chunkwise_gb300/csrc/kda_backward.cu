@@ -197,15 +197,6 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
         for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
 }
 
-// Sum over the 16 lanes that share a thread row (tx = lane % 16).
-__device__ __forceinline__ float sum16(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    return x;
-}
-
 // ---------------------------------------------------------------- tables
 // One CTA per (sequence, head, chunk): the chunk's tables into the workspace.
 template <int DK, typename TIn>
@@ -472,8 +463,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
 // ---------------------------------------------------------------- local
 template <int DK> struct LocalSmem {
     simt::Tables<DK> tb;
-    float W[3][C * LDC];  // work tiles; tb.A is the fourth
-    float red[16 * DK];   // per-thread-row partial sums over columns
+    float W[3][C * LDC];       // work tiles; tb.A is the fourth
+    float red[8 * DK + 2 * C];  // column sums by row block; dbeta row sums by column half
 };
 
 static_assert(offsetof(LocalSmem<128>, W) % 16 == 0 && offsetof(LocalSmem<64>, W) % 16 == 0,
@@ -580,14 +571,70 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
     }
 }
 
+// ---- warp-level products on the tensor cores (mma.sync, m16n8k8, tf32) with
+// fp32 accuracy: every operand x is split into hi = tf32(x) and lo =
+// tf32(x - hi), and a b = a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term is
+// below fp32 rounding). Fragment layout (lane = 4 g + t): A rows g, g + 8 and
+// columns t, t + 4; B rows t, t + 4 and column g; C rows g, g + 8 and columns
+// 2 t, 2 t + 1 of each 16 x 8 tile.
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_bits(x);
+    lo = tf32_bits(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc[nt] (the 16 x 8 tile at rows r0.., columns c0 + 8 nt ..) += sum_{k < K} a(r, k) b(k, c)
+template <int K, int NT8, typename FA, typename FB>
+__device__ __forceinline__ void wmm(float (&acc)[NT8][4], FA a, FB b, int r0, int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+    for (int k = 0; k < K; k += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(a(r0 + g, k + t), ah[0], al[0]);
+        split_tf32(a(r0 + g + 8, k + t), ah[1], al[1]);
+        split_tf32(a(r0 + g, k + t + 4), ah[2], al[2]);
+        split_tf32(a(r0 + g + 8, k + t + 4), ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(b(k + t, c0 + 8 * nt + g), bh0, bl0);
+            split_tf32(b(k + t + 4, c0 + 8 * nt + g), bh1, bl1);
+            mma8(acc[nt], al, bh0, bh1);
+            mma8(acc[nt], ah, bl0, bl1);
+            mma8(acc[nt], ah, bh0, bh1);
+        }
+    }
+}
+template <int NT8> __device__ __forceinline__ void fzero(float (&acc)[NT8][4]) {
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+}
+// f(r, c, value&) for each accumulator element of the tile at (r0, c0)
+template <int NT8, typename F> __device__ __forceinline__ void ffor(float (&acc)[NT8][4], int r0, int c0, F f) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f(r0 + g + 8 * (e >> 1), c0 + 8 * nt + 2 * t + (e & 1), acc[nt][e]);
+}
+
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LocalSmem<DK> &sm = *reinterpret_cast<LocalSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
     constexpr int LDK = simt::Tables<DK>::LDK;
-    constexpr int RB = DK / 64;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2;
     const int nslices = p.DV / VS;
     const int slice = blockIdx.x % nslices;
     int64_t rest = blockIdx.x / nslices;
@@ -609,201 +656,168 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         return;
     }
     float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
-    auto S_ = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };  // St
-    auto G_ = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };  // Gt
+    // warp tile: rows R0 .. R0 + 15; columns C0 .. C0 + 31 of a 64-wide product,
+    // CK .. CK + DK/2 - 1 of a DK-wide one
+    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2), CK = (DK / 2) * (warp >> 2);
+    auto St = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };
+    auto Gt = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };
+    auto store = [&](float (&acc)[4][4], float *W) { ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { W[r * LDC + c] = x; }); };
+    float *dbr = sm.red + 8 * DK;  // [2][C] row sums of dbeta by column half
     float acc[4][4];
 
-    // dO -> WD; V - Kr St -> WB
+    // dO -> WD
     for (int e = tid; e < C * VS; e += NT) {
         const int r = e / VS;
         WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
     }
-    zero(acc);
-    mm4<DK, MM_NN>(acc, tb.Kr, LDK, Sg + v0, DV, tb.mu);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = ty + 16 * i;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj) : 0.f;
-            WB[r * LDC + 4 * tx + jj] = vv - acc[i][jj];
-        }
-    }
+    // V - Kr St -> WB
+    fzero<4>(acc);
+    wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
+    ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
+        const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
+        WB[r * LDC + c] = vv - x;
+    });
     __syncthreads();
     // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
-    zero(acc);
-    mm4<C, MM_NN>(acc, tb.T, LDC, WB, LDC, tb.beta);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) WC[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
-    zero(acc);
-    mm4<DK, MM_NN>(acc, tb.Kc, LDK, Gg + v0, DV, tb.mu);
-    mm4<C, MM_TN>(acc, tb.P, LDC, WD, LDC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) WA[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+    fzero<4>(acc);
+    wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; },
+              R0, C0);
+    store(acc, WC);
+    fzero<4>(acc);
+    wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
+    wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0, C0);
+    store(acc, WA);
     __syncthreads();
-    // dT = dU R^T (registers); dR = T^T dU: dV, the first part of dbeta, dX
+    // dT = dU R^T; dR = T^T dU: dV, dbeta's first part, dX
     float dT[4][4], dR[4][4];
-    zero(dT);
-    mm4<VS, MM_NT>(dT, WA, LDC, WB, LDC);
+    fzero<4>(dT);
+    wmm<VS, 4>(dT, [&](int r, int j) { return WA[r * LDC + j]; }, [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; },
+               R0, C0);
+    fzero<4>(dR);
+    wmm<C, 4>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0, C0);
+    float db[2] = {0.f, 0.f};  // rows R0 + g, R0 + g + 8
+    {
+        const int t = lane & 3;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) dT[i][jj] *= tb.beta[4 * tx + jj];
-    zero(dR);
-    mm4<C, MM_TN>(dR, tb.T, LDC, WA, LDC);
-    float dbeta_r[4];
+            for (int e = 0; e < 4; ++e) {
+                const int r = R0 + g + 8 * (e >> 1), c = C0 + 8 * nt + 2 * t + (e & 1);
+                db[e >> 1] += dR[nt][e] * WB[r * LDC + c];
+                if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = tb.beta[r] * dR[nt][e];
+            }
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = ty + 16 * i;
-        float s = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            s += dR[i][jj] * WB[r * LDC + 4 * tx + jj];
-            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj] = tb.beta[r] * dR[i][jj];
-        }
-        dbeta_r[i] = sum16(s);
+    for (int u = 0; u < 2; ++u) {
+        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 1);
+        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 2);
     }
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = ty + 16 * i;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            WB[r * LDC + 4 * tx + jj] = -tb.beta[r] * dR[i][jj];  // dX
-            WA[r * LDC + 4 * tx + jj] = dT[i][jj];
-        }
-    }
+    ffor<4>(dR, R0, C0, [&](int r, int c, float &x) { WB[r * LDC + c] = -tb.beta[r] * x; });  // dX
+    store(dT, WA);
     __syncthreads();
     // dP = lower(dO U^T) (registers); dKc = U Gt^T
     float dP[4][4];
-    zero(dP);
-    mm4<VS, MM_NT>(dP, WD, LDC, WC, LDC);
-    float dKc[RB][4][4], dQr[RB][4][4], dKr[RB][4][4], s123[RB][4];
+    fzero<4>(dP);
+    wmm<VS, 4>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0, C0);
+    float dKc[NK][4], dQr[NK][4], dKr[NK][4];
+    float s123[NK][2];  // per column 2t, 2t + 1 of each tile: sums over this thread's two rows
+    fzero<NK>(dKc);
+    wmm<VS, NK>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
+    {
+        const int t = lane & 3;
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2) {
-        zero(dKc[b2]);
-        mm4<VS, MM_NT>(dKc[b2], WC, LDC, Gg + (int64_t)64 * b2 * DV + v0, DV);
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) dKc[b2][i][jj] *= tb.mu[64 * b2 + 4 * tx + jj];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s += tb.Kc[(ty + 16 * i) * LDK + 64 * b2 + 4 * tx + jj] * dKc[b2][i][jj];
-            s123[b2][jj] = s;
-        }
+            for (int u = 0; u < 2; ++u) {
+                const int c = CK + 8 * nt + 2 * t + u;
+                s123[nt][u] = tb.Kc[(R0 + g) * LDK + c] * dKc[nt][u] + tb.Kc[(R0 + g + 8) * LDK + c] * dKc[nt][2 + u];
+            }
     }
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int r = ty + 16 * i, m = 4 * tx + jj;
-            WC[r * LDC + m] = m <= r ? dP[i][jj] : 0.f;
-        }
+    ffor<4>(dP, R0, C0, [&](int r, int c, float &x) { WC[r * LDC + c] = c <= r ? x : 0.f; });
     __syncthreads();
     // dQr = dO St^T, dKr = dX St^T (the parts that meet St), then the rest
+    fzero<NK>(dQr);
+    fzero<NK>(dKr);
+    wmm<VS, NK>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+    wmm<VS, NK>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+    {
+        const int t = lane & 3;
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2) {
-        zero(dQr[b2]);
-        zero(dKr[b2]);
-        mm4<VS, MM_NT>(dQr[b2], WD, LDC, Sg + (int64_t)64 * b2 * DV + v0, DV);
-        mm4<VS, MM_NT>(dKr[b2], WB, LDC, Sg + (int64_t)64 * b2 * DV + v0, DV);
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float m = tb.mu[64 * b2 + 4 * tx + jj];
-                dQr[b2][i][jj] *= m;
-                dKr[b2][i][jj] *= m;
+            for (int u = 0; u < 2; ++u) {
+                const int c = CK + 8 * nt + 2 * t + u, a0 = (R0 + g) * LDK + c, a1 = (R0 + g + 8) * LDK + c;
+                s123[nt][u] += tb.Qr[a0] * dQr[nt][u] + tb.Qr[a1] * dQr[nt][2 + u] + tb.Kr[a0] * dKr[nt][u] +
+                               tb.Kr[a1] * dKr[nt][2 + u];
             }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int rc = (ty + 16 * i) * LDK + 64 * b2 + 4 * tx + jj;
-                s += tb.Qr[rc] * dQr[b2][i][jj] + tb.Kr[rc] * dKr[b2][i][jj];
-            }
-            s123[b2][jj] += s;
-        }
-        // dQr += dP Kc;  dKc += dP^T Qr
-        mm4<C, MM_NN>(dQr[b2], WC, LDC, tb.Kc + 64 * b2, LDK);
-        mm4<C, MM_TN>(dKc[b2], WC, LDC, tb.Qr + 64 * b2, LDK);
     }
+    wmm<C, NK>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0, CK);
+    wmm<C, NK>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int c) { return tb.Qr[m * LDK + c]; }, R0, CK);
     // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
-    zero(acc);
-    mm4<C, MM_NT>(acc, WA, LDC, tb.T, LDC);
+    fzero<4>(acc);
+    wmm<C, 4>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; }, R0, C0);
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) WD[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+    store(acc, WD);
     __syncthreads();
-    zero(acc);
-    mm4<C, MM_TN>(acc, tb.T, LDC, WD, LDC);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int r = ty + 16 * i, m = 4 * tx + jj;
-            WA[r * LDC + m] = m < r ? -acc[i][jj] : 0.f;
-        }
+    fzero<4>(acc);
+    wmm<C, 4>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; }, R0, C0);
+    ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { WA[r * LDC + c] = c < r ? -x : 0.f; });
     __syncthreads();
     // dKr += Diag(beta) dA Kc (and dbeta's second part Kr . (dA Kc));  dKc += (Diag(beta) dA)^T Kr
+    {
+        float tmp[NK][4];
+        fzero<NK>(tmp);
+        wmm<C, NK>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0,
+                   CK);
+        float d2[2] = {0.f, 0.f};
+        const int t = lane & 3;
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2) {
-        float t[4][4];
-        zero(t);
-        mm4<C, MM_NN>(t, WA, LDC, tb.Kc + 64 * b2, LDK);
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = ty + 16 * i;
-            float s = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                s += tb.Kr[r * LDK + 64 * b2 + 4 * tx + jj] * t[i][jj];
-                dKr[b2][i][jj] += tb.beta[r] * t[i][jj];
+            for (int e = 0; e < 4; ++e) {
+                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t + (e & 1);
+                d2[e >> 1] += tb.Kr[r * LDK + c] * tmp[nt][e];
+                dKr[nt][e] += tb.beta[r] * tmp[nt][e];
             }
-            dbeta_r[i] += sum16(s);
-        }
-        mm4<C, MM_TN>(dKc[b2], WA, LDC, tb.Kr + 64 * b2, LDK, tb.beta);
-    }
-    if (tx == 0)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = ty + 16 * i;
-            if (r < L) atomicAdd(&p.dbeta[(tok0 + r) * H + h], dbeta_r[i]);
+        for (int u = 0; u < 2; ++u) {
+            d2[u] += __shfl_xor_sync(0xffffffffu, d2[u], 1);
+            d2[u] += __shfl_xor_sync(0xffffffffu, d2[u], 2);
+            db[u] += d2[u];
         }
+    }
+    wmm<C, NK>(dKc, [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
+               [&](int m, int c) { return tb.Kr[m * LDK + c]; }, R0, CK);
+    // dbeta: the two column halves of each row, added in a fixed order
+    if ((lane & 3) == 0) {
+        dbr[(warp >> 2) * C + R0 + g] = db[0];
+        dbr[(warp >> 2) * C + R0 + g + 8] = db[1];
+    }
     // the chunk's gate factors p / mu (as in the forward tables) into the free
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
     simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, KDA_GATE_CHANNEL, tok0, L, H, h);
-    float dlogp[RB][4][4];
+    if (tid < C && tid < L) atomicAdd(&p.dbeta[(tok0 + tid) * H + h], dbr[tid] + dbr[C + tid]);
+    float dlogp[NK][4];
+    {
+        const int t = lane & 3;
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int c = 64 * b2 + 4 * tx + jj;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = ty + 16 * i, rc = r * LDK + c;
+            for (int e = 0; e < 4; ++e) {
+                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t + (e & 1), rc = r * LDK + c;
                 const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
                 if (r < L) {
                     const int64_t th = (tok0 + r) * H + h;
-                    atomicAdd(&p.dq[th * DK + c], dQr[b2][i][jj] * e2);
-                    atomicAdd(&p.dk[th * DK + c], dKr[b2][i][jj] * e2 + dKc[b2][i][jj] * e3);
+                    atomicAdd(&p.dq[th * DK + c], dQr[nt][e] * e2);
+                    atomicAdd(&p.dk[th * DK + c], dKr[nt][e] * e2 + dKc[nt][e] * e3);
                 }
-                dlogp[b2][i][jj] = dKr[b2][i][jj] * tb.Kr[rc] + dQr[b2][i][jj] * tb.Qr[rc] - dKc[b2][i][jj] * tb.Kc[rc];
+                dlogp[nt][e] = dKr[nt][e] * tb.Kr[rc] + dQr[nt][e] * tb.Qr[rc] - dKc[nt][e] * tb.Kc[rc];
             }
-        }
+    }
     // sum_v St Gt per channel: channel c, value columns of part hp (16-byte loads)
     {
         constexpr int NH = NT / DK, CW = VS / NH;
@@ -817,16 +831,26 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         }
         tb.part[hp * DK + c] = tb.mu[c] * tb.mu[c] * s0;
     }
-    __syncthreads();  // every read of Qr is done
+    // s123: sums over the 16 rows of this warp (lanes with the same t), then by warp row block
 #pragma unroll
-    for (int b2 = 0; b2 < RB; ++b2)
+    for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int c = 64 * b2 + 4 * tx + jj;
-            sm.red[ty * DK + c] = s123[b2][jj];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tb.Qr[(ty + 16 * i) * LDK + c] = dlogp[b2][i][jj];
+        for (int u = 0; u < 2; ++u) {
+            float x = s123[nt][u];
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            s123[nt][u] = x;
         }
+    __syncthreads();  // every read of Qr is done
+    if (g == 0) {
+        const int t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) sm.red[(warp & 3) * DK + CK + 8 * nt + 2 * t + u] = s123[nt][u];
+    }
+    ffor<NK>(dlogp, R0, CK, [&](int r, int c, float &x) { tb.Qr[r * LDK + c] = x; });
     __syncthreads();
     // per channel: d log mu, then d log alpha by a reverse running sum over the rows
     if (tid < DK) {
@@ -834,7 +858,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         float s0 = 0.f;
         for (int hp = 0; hp < NT / DK; ++hp) s0 += tb.part[hp * DK + c];
         float s123c = 0.f;
-        for (int t2 = 0; t2 < 16; ++t2) s123c += sm.red[t2 * DK + c];
+        for (int t2 = 0; t2 < 4; ++t2) s123c += sm.red[t2 * DK + c];
         float colsum = 0.f;
         for (int r = 0; r < L; ++r) colsum += tb.Qr[r * LDK + c];
         const float dlogmu = 2.f * s0 + s123c - colsum;
