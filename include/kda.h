@@ -350,16 +350,18 @@ kda_status_t kda_device_errors(int *errors, int reset);
  *   dbeta          [B, T, H] float32 (written; 4-byte aligned suffices)
  *   d_initial_state[B, H, d_k, d_v] float32 or NULL (not written)
  *   workspace      device scratch of kda_prefill_backward_workspace_bytes(...)
- *                  bytes, 16-byte aligned, owned by the caller: the state
- *                  before every 64-token chunk and the state gradient after
- *                  it (2 x 4 d_k d_v bytes per chunk of every sequence and
- *                  head). Calls sharing a workspace must not overlap.
+ *                  bytes, 16-byte aligned, owned by the caller: for every
+ *                  64-token chunk of every sequence and head, the state before
+ *                  it, the state gradient after it (4 d_k d_v bytes each) and
+ *                  its chunk tables (about 129 KB for d_k = 128). Calls sharing
+ *                  a workspace must not overlap.
  *
- * Every gradient is float32 whatever qkv_dtype is (fp32 arithmetic on CUDA
- * cores throughout). The result does not depend on the call's timing: where
- * two value halves (d_v = 128) both contribute to an element, it is the sum of
- * exactly two terms. Errors as for kda_prefill; a missing or short workspace
- * returns KDA_ERR_WORKSPACE before anything runs.
+ * Every gradient is float32 whatever qkv_dtype is, and computed with fp32
+ * accuracy (CUDA cores, and tensor-core products with every operand split
+ * into two tf32 parts). Each gradient element is written once by one thread,
+ * so two calls on the same inputs give the same bits. Errors as for
+ * kda_prefill; a missing or short workspace returns KDA_ERR_WORKSPACE before
+ * anything runs.
  */
 kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
                                   const float *alpha, const float *beta, const float *initial_state,

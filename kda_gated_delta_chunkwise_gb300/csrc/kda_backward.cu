@@ -39,10 +39,12 @@
 //   chain  one CTA per (sequence, head, 64-column value slice), chunks in
 //          reverse: writes dL/dS after every chunk into the workspace and the
 //          initial state's gradient;
-//   local  one CTA per (sequence, head, chunk, value slice), all chunks at
-//          once: dv of its slice, and its slice's share of dq, dk, dalpha,
-//          dbeta, added with atomicAdd onto zeroed outputs (at most two slices,
-//          so every sum is a + b: the same bits in either order).
+//   local  one CTA per (sequence, head, chunk), all chunks at once, the
+//          products on the tensor cores (mma.sync tf32 with a hi/lo split:
+//          fp32 accuracy): dv, dq, dk, dalpha, dbeta of the chunk's tokens,
+//          each written once (the value columns are taken 64 at a time and
+//          the sums over them accumulate in registers), so the result is
+//          deterministic.
 #include "kda_chunk_simt.cuh"
 
 namespace kda {
@@ -472,77 +474,76 @@ static_assert(offsetof(LocalSmem<128>, W) % 16 == 0 && offsetof(LocalSmem<64>, W
 
 template <int DK, typename TIn>
 __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, const float *Sg, const float *Gg,
-                                        int64_t tok0, int L, int h, int v0) {
-    // Token-level reverse steps; the state before token r is replayed from the
-    // chunk's start state for every r (the chunk is rare: this is written for
-    // size). Buffers: Sb (state) in Kr, G in Qr, vectors in W.
-    constexpr int NP = NT / VS;     // key-row parts of the column mapping
-    constexpr int NH = NT / DK;     // column parts of the row mapping
+                                        int64_t tok0, int L, int h) {
+    // Token-level reverse steps over every value column; the state before
+    // token r is replayed from the chunk's start state for every r (the chunk
+    // is rare: this is written for size). Buffers: the state in Kr..Qr, G in
+    // Kc..P, vectors in W.
     const int H = p.H, DV = p.DV, tid = threadIdx.x;
+    const int NP = NT / DV;      // key-row parts of the column mapping
+    constexpr int NH = NT / DK;  // column parts of the row mapping
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
-    float *Sb = sm.tb.Kr, *G = sm.tb.Qr;
-    float *redv = sm.W[0], *redw = sm.W[0] + NP * VS, *ev = sm.W[0] + 2 * NP * VS, *wv = ev + VS;
+    float *Sb = sm.tb.Kr, *G = sm.tb.Kc;
+    float *redv = sm.W[0], *redw = sm.W[0] + NP * DV, *ev = sm.W[0] + 2 * NP * DV, *wv = ev + DV;
     float *redc = sm.W[1];  // [NH][4][DK]
-    const int j = tid % VS, part = tid / VS;
-    for (int e = tid; e < DK * VS; e += NT) G[e] = Gg[(int64_t)(e / VS) * DV + v0 + e % VS];
+    const int j = tid % DV, part = tid / DV;
+    for (int e = tid; e < DK * DV; e += NT) G[e] = Gg[e];
     for (int r = L - 1; r >= 0; --r) {
         // Sb = S_{r-1}
-        for (int e = tid; e < DK * VS; e += NT) Sb[e] = Sg[(int64_t)(e / VS) * DV + v0 + e % VS];
+        for (int e = tid; e < DK * DV; e += NT) Sb[e] = Sg[e];
         __syncthreads();
         for (int m = 0; m < r; ++m) {
             const int64_t tk = (tok0 + m) * H + h;
             float vp = 0.f;
-            for (int c = part; c < DK; c += NP) vp += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * Sb[c * VS + j];
-            redv[part * VS + j] = vp;
+            for (int c = part; c < DK; c += NP) vp += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * Sb[c * DV + j];
+            redv[part * DV + j] = vp;
             __syncthreads();
             float vh = 0.f;
-#pragma unroll
-            for (int p2 = 0; p2 < NP; ++p2) vh += redv[p2 * VS + j];
-            const float e = ld_in(v, tk * DV + v0 + j) - vh, be = p.beta[tk] * e;
+            for (int p2 = 0; p2 < NP; ++p2) vh += redv[p2 * DV + j];
+            const float be = p.beta[tk] * (ld_in(v, tk * DV + j) - vh);
             for (int c = part; c < DK; c += NP)
-                Sb[c * VS + j] = p.alpha[tk * DK + c] * Sb[c * VS + j] + ld_in(k, tk * DK + c) * be;
+                Sb[c * DV + j] = p.alpha[tk * DK + c] * Sb[c * DV + j] + ld_in(k, tk * DK + c) * be;
             __syncthreads();
         }
         // reverse step of token r
         const int64_t tk = (tok0 + r) * H + h;
         const float bt = p.beta[tk];
         {
-            const float dj = ld_in(dO, tk * DV + v0 + j);
+            const float dj = ld_in(dO, tk * DV + j);
             float vp = 0.f, wp = 0.f;
             for (int c = part; c < DK; c += NP) {
                 const float kc = ld_in(k, tk * DK + c);
-                const float g = G[c * VS + j] + ld_in(q, tk * DK + c) * dj;
-                G[c * VS + j] = g;
-                vp += p.alpha[tk * DK + c] * kc * Sb[c * VS + j];
+                const float g = G[c * DV + j] + ld_in(q, tk * DK + c) * dj;
+                G[c * DV + j] = g;
+                vp += p.alpha[tk * DK + c] * kc * Sb[c * DV + j];
                 wp += kc * g;
             }
-            redv[part * VS + j] = vp;
-            redw[part * VS + j] = wp;
+            redv[part * DV + j] = vp;
+            redw[part * DV + j] = wp;
             __syncthreads();
             if (part == 0) {
                 float vh = 0.f, w = 0.f;
-#pragma unroll
                 for (int p2 = 0; p2 < NP; ++p2) {
-                    vh += redv[p2 * VS + j];
-                    w += redw[p2 * VS + j];
+                    vh += redv[p2 * DV + j];
+                    w += redw[p2 * DV + j];
                 }
-                ev[j] = ld_in(v, tk * DV + v0 + j) - vh;
+                ev[j] = ld_in(v, tk * DV + j) - vh;
                 wv[j] = w;
-                p.dv[tk * DV + v0 + j] = bt * w;
+                p.dv[tk * DV + j] = bt * w;
             }
             __syncthreads();
         }
         {
-            // row mapping: channel c, columns of part hp
-            const int c = tid % DK, hp = tid / DK;
+            // row mapping: channel c, value columns of part hp
+            const int c = tid % DK, hp = tid / DK, cw = DV / NH;
             const float ac = p.alpha[tk * DK + c], kc = ld_in(k, tk * DK + c);
             float dq = 0.f, ge = 0.f, sw = 0.f, da = 0.f;
-            for (int jj = hp * (VS / NH); jj < (hp + 1) * (VS / NH); ++jj) {
-                const float s = Sb[c * VS + jj], g = G[c * VS + jj], e = ev[jj], w = wv[jj];
-                dq += (ac * s + bt * kc * e) * ld_in(dO, tk * DV + v0 + jj);
+            for (int jj = hp * cw; jj < (hp + 1) * cw; ++jj) {
+                const float sv = Sb[c * DV + jj], g = G[c * DV + jj], e = ev[jj], w = wv[jj];
+                dq += (ac * sv + bt * kc * e) * ld_in(dO, tk * DV + jj);
                 ge += g * e;
-                sw += ac * s * w;
-                da += (g - bt * kc * w) * s;
+                sw += ac * sv * w;
+                da += (g - bt * kc * w) * sv;
             }
             redc[(hp * 4 + 0) * DK + c] = dq;
             redc[(hp * 4 + 1) * DK + c] = ge;
@@ -554,19 +555,19 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                 for (int h2 = 0; h2 < NH; ++h2)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) s4[u] += redc[(h2 * 4 + u) * DK + tid];
-                atomicAdd(&p.dq[tk * DK + tid], s4[0]);
-                atomicAdd(&p.dk[tk * DK + tid], bt * (s4[1] - s4[2]));
-                atomicAdd(&p.dalpha[tk * DK + tid], s4[3]);
+                p.dq[tk * DK + tid] = s4[0];
+                p.dk[tk * DK + tid] = bt * (s4[1] - s4[2]);
+                p.dalpha[tk * DK + tid] = s4[3];
             }
             if (tid == 0) {
                 float db = 0.f;
-                for (int jj = 0; jj < VS; ++jj) db += wv[jj] * ev[jj];
-                atomicAdd(&p.dbeta[tk], db);
+                for (int jj = 0; jj < DV; ++jj) db += wv[jj] * ev[jj];
+                p.dbeta[tk] = db;
             }
         }
         // G = Diag(alpha)(G - beta k w^T)
         for (int c = part; c < DK; c += NP)
-            G[c * VS + j] = p.alpha[tk * DK + c] * (G[c * VS + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
+            G[c * DV + j] = p.alpha[tk * DK + c] * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
         __syncthreads();
     }
 }
@@ -634,135 +635,125 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     simt::Tables<DK> &tb = sm.tb;
     constexpr int LDK = simt::Tables<DK>::LDK;
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2;
-    const int nslices = p.DV / VS;
-    const int slice = blockIdx.x % nslices;
-    int64_t rest = blockIdx.x / nslices;
-    const int ci = (int)(rest % p.NC);
-    rest /= p.NC;
-    const int h = (int)(rest % p.H);
-    const int n = (int)(rest / p.H);
-    const int H = p.H, DV = p.DV, v0 = slice * VS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int64_t idx = blockIdx.x;  // (n H + h) NC + ci
+    const int ci = (int)(idx % p.NC), h = (int)((idx / p.NC) % p.H), n = (int)(idx / ((int64_t)p.NC * p.H));
+    const int H = p.H, DV = p.DV;
     const int64_t t0 = (int64_t)ci * C;
     const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
     const int64_t tok0 = (int64_t)n * p.T + t0;
     const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
-    const int64_t off = (((int64_t)n * H + h) * p.NC + ci) * DK * DV;
-    const float *Sg = p.states + off, *Gg = p.gnext + off;
+    const float *Sg = p.states + idx * DK * DV, *Gg = p.gnext + idx * DK * DV;
 
-    load_tables<DK>(tb, p.tabs + ((((int64_t)n * H + h) * p.NC + ci) * TabLayout<DK>::FLOATS), TAB_ALL);
+    load_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS, TAB_ALL);
     if (tb.slow) {
-        local_slow<DK, TIn>(sm, p, Sg, Gg, tok0, L, h, v0);
+        local_slow<DK, TIn>(sm, p, Sg, Gg, tok0, L, h);
         return;
     }
     float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
     // warp tile: rows R0 .. R0 + 15; columns C0 .. C0 + 31 of a 64-wide product,
     // CK .. CK + DK/2 - 1 of a DK-wide one
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2), CK = (DK / 2) * (warp >> 2);
-    auto St = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };
-    auto Gt = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };
     auto store = [&](float (&acc)[4][4], float *W) { ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { W[r * LDC + c] = x; }); };
     float *dbr = sm.red + 8 * DK;  // [2][C] row sums of dbeta by column half
     float acc[4][4];
-
-    // dO -> WD
-    for (int e = tid; e < C * VS; e += NT) {
-        const int r = e / VS;
-        WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
-    }
-    // V - Kr St -> WB
-    fzero<4>(acc);
-    wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
-    ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-        const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
-        WB[r * LDC + c] = vv - x;
-    });
-    __syncthreads();
-    // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
-    fzero<4>(acc);
-    wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; },
-              R0, C0);
-    store(acc, WC);
-    fzero<4>(acc);
-    wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
-    wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0, C0);
-    store(acc, WA);
-    __syncthreads();
-    // dT = dU R^T; dR = T^T dU: dV, dbeta's first part, dX
-    float dT[4][4], dR[4][4];
+    // Accumulated over the value slices (every one of these is a sum over value columns):
+    float dT[4][4], dP[4][4];                      // dU R^T, dO U^T
+    float dKc[NK][4], dQr[NK][4], dKr[NK][4];      // U Gt^T, dO St^T, dX St^T so far
+    float db[2] = {0.f, 0.f};                      // sum_v dR (V - X) of rows R0 + g, R0 + g + 8
+    float s0 = 0.f;                                // sum_v St Gt of channel tid % DK (part tid / DK)
     fzero<4>(dT);
-    wmm<VS, 4>(dT, [&](int r, int j) { return WA[r * LDC + j]; }, [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; },
-               R0, C0);
-    fzero<4>(dR);
-    wmm<C, 4>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0, C0);
-    float db[2] = {0.f, 0.f};  // rows R0 + g, R0 + g + 8
-    {
-        const int t = lane & 3;
+    fzero<4>(dP);
+    fzero<NK>(dKc);
+    fzero<NK>(dQr);
+    fzero<NK>(dKr);
+
+    for (int v0 = 0; v0 < DV; v0 += VS) {
+        auto St = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };
+        auto Gt = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };
+        // dO -> WD; V - Kr St -> WB
+        for (int e = tid; e < C * VS; e += NT) {
+            const int r = e / VS;
+            WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
+        }
+        fzero<4>(acc);
+        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
+            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
+            WB[r * LDC + c] = vv - x;
+        });
+        {
+            constexpr int NH = NT / DK, CW = VS / NH;
+            const int c = tid % DK, hp = tid / DK;
+            const float *sr = Sg + (int64_t)c * DV + v0 + hp * CW, *gr = Gg + (int64_t)c * DV + v0 + hp * CW;
+#pragma unroll
+            for (int j = 0; j < CW; j += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(sr + j), g4 = *reinterpret_cast<const float4 *>(gr + j);
+                s0 += a4.x * g4.x + a4.y * g4.y + a4.z * g4.z + a4.w * g4.w;
+            }
+        }
+        __syncthreads();
+        // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
+        fzero<4>(acc);
+        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; },
+                  [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
+        store(acc, WC);
+        fzero<4>(acc);
+        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
+        wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0,
+                  C0);
+        store(acc, WA);
+        __syncthreads();
+        // dT += dU R^T; dR = T^T dU: dV, dbeta's first part, then dX
+        wmm<VS, 4>(dT, [&](int r, int j) { return WA[r * LDC + j]; },
+                   [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
+        float dR[4][4];
+        fzero<4>(dR);
+        wmm<C, 4>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0,
+                  C0);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), c = C0 + 8 * nt + 2 * t + (e & 1);
+                const int r = R0 + g + 8 * (e >> 1), c = C0 + 8 * nt + 2 * t4 + (e & 1);
                 db[e >> 1] += dR[nt][e] * WB[r * LDC + c];
                 if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = tb.beta[r] * dR[nt][e];
             }
+        __syncthreads();
+        ffor<4>(dR, R0, C0, [&](int r, int c, float &x) { WB[r * LDC + c] = -tb.beta[r] * x; });  // dX
+        __syncthreads();
+        // dP += dO U^T; dKc += U Gt^T; dQr += dO St^T; dKr += dX St^T
+        wmm<VS, 4>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0,
+                   C0);
+        wmm<VS, NK>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
+        wmm<VS, NK>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+        wmm<VS, NK>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+        __syncthreads();  // the work tiles are reused by the next slice
     }
+    // the first parts of d log mu's column sums: Kc (U Gt^T), Qr (dO St^T), Kr (dX St^T)
+    float s123[NK][2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 1);
-        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 2);
-    }
-    __syncthreads();
-    ffor<4>(dR, R0, C0, [&](int r, int c, float &x) { WB[r * LDC + c] = -tb.beta[r] * x; });  // dX
+    for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c = CK + 8 * nt + 2 * t4 + u, a0 = (R0 + g) * LDK + c, a1 = (R0 + g + 8) * LDK + c;
+            s123[nt][u] = tb.Kc[a0] * dKc[nt][u] + tb.Kc[a1] * dKc[nt][2 + u] + tb.Qr[a0] * dQr[nt][u] +
+                          tb.Qr[a1] * dQr[nt][2 + u] + tb.Kr[a0] * dKr[nt][u] + tb.Kr[a1] * dKr[nt][2 + u];
+        }
+    ffor<4>(dP, R0, C0, [&](int r, int c, float &x) { WC[r * LDC + c] = c <= r ? x : 0.f; });  // lower(dP)
     store(dT, WA);
     __syncthreads();
-    // dP = lower(dO U^T) (registers); dKc = U Gt^T
-    float dP[4][4];
-    fzero<4>(dP);
-    wmm<VS, 4>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0, C0);
-    float dKc[NK][4], dQr[NK][4], dKr[NK][4];
-    float s123[NK][2];  // per column 2t, 2t + 1 of each tile: sums over this thread's two rows
-    fzero<NK>(dKc);
-    wmm<VS, NK>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
-    {
-        const int t = lane & 3;
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int c = CK + 8 * nt + 2 * t + u;
-                s123[nt][u] = tb.Kc[(R0 + g) * LDK + c] * dKc[nt][u] + tb.Kc[(R0 + g + 8) * LDK + c] * dKc[nt][2 + u];
-            }
-    }
-    __syncthreads();
-    ffor<4>(dP, R0, C0, [&](int r, int c, float &x) { WC[r * LDC + c] = c <= r ? x : 0.f; });
-    __syncthreads();
-    // dQr = dO St^T, dKr = dX St^T (the parts that meet St), then the rest
-    fzero<NK>(dQr);
-    fzero<NK>(dKr);
-    wmm<VS, NK>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
-    wmm<VS, NK>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
-    {
-        const int t = lane & 3;
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int c = CK + 8 * nt + 2 * t + u, a0 = (R0 + g) * LDK + c, a1 = (R0 + g + 8) * LDK + c;
-                s123[nt][u] += tb.Qr[a0] * dQr[nt][u] + tb.Qr[a1] * dQr[nt][2 + u] + tb.Kr[a0] * dKr[nt][u] +
-                               tb.Kr[a1] * dKr[nt][2 + u];
-            }
-    }
+    // dQr += dP Kc;  dKc += dP^T Qr
     wmm<C, NK>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0, CK);
     wmm<C, NK>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int c) { return tb.Qr[m * LDK + c]; }, R0, CK);
     // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
     fzero<4>(acc);
     wmm<C, 4>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; }, R0, C0);
-    __syncthreads();
     store(acc, WD);
     __syncthreads();
     fzero<4>(acc);
     wmm<C, 4>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; }, R0, C0);
+    __syncthreads();  // every read of dT in WA is done
     ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { WA[r * LDC + c] = c < r ? -x : 0.f; });
     __syncthreads();
     // dKr += Diag(beta) dA Kc (and dbeta's second part Kr . (dA Kc));  dKc += (Diag(beta) dA)^T Kr
@@ -772,26 +763,27 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         wmm<C, NK>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0,
                    CK);
         float d2[2] = {0.f, 0.f};
-        const int t = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t + (e & 1);
+                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t4 + (e & 1);
                 d2[e >> 1] += tb.Kr[r * LDK + c] * tmp[nt][e];
                 dKr[nt][e] += tb.beta[r] * tmp[nt][e];
             }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            d2[u] += __shfl_xor_sync(0xffffffffu, d2[u], 1);
-            d2[u] += __shfl_xor_sync(0xffffffffu, d2[u], 2);
-            db[u] += d2[u];
-        }
+        for (int u = 0; u < 2; ++u) db[u] += d2[u];
     }
     wmm<C, NK>(dKc, [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
                [&](int m, int c) { return tb.Kr[m * LDK + c]; }, R0, CK);
-    // dbeta: the two column halves of each row, added in a fixed order
-    if ((lane & 3) == 0) {
+    // dbeta: sums over this warp's columns (the 4 lanes of a row), then the two
+    // column halves of each row in a fixed order
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 1);
+        db[u] += __shfl_xor_sync(0xffffffffu, db[u], 2);
+    }
+    if (t4 == 0) {
         dbr[(warp >> 2) * C + R0 + g] = db[0];
         dbr[(warp >> 2) * C + R0 + g + 8] = db[1];
     }
@@ -800,37 +792,22 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
     simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, KDA_GATE_CHANNEL, tok0, L, H, h);
-    if (tid < C && tid < L) atomicAdd(&p.dbeta[(tok0 + tid) * H + h], dbr[tid] + dbr[C + tid]);
+    tb.part[(tid / DK) * DK + tid % DK] = tb.mu[tid % DK] * tb.mu[tid % DK] * s0;
+    if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid];
     float dlogp[NK][4];
-    {
-        const int t = lane & 3;
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
+    for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t + (e & 1), rc = r * LDK + c;
-                const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
-                if (r < L) {
-                    const int64_t th = (tok0 + r) * H + h;
-                    atomicAdd(&p.dq[th * DK + c], dQr[nt][e] * e2);
-                    atomicAdd(&p.dk[th * DK + c], dKr[nt][e] * e2 + dKc[nt][e] * e3);
-                }
-                dlogp[nt][e] = dKr[nt][e] * tb.Kr[rc] + dQr[nt][e] * tb.Qr[rc] - dKc[nt][e] * tb.Kc[rc];
+        for (int e = 0; e < 4; ++e) {
+            const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t4 + (e & 1), rc = r * LDK + c;
+            const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
+            if (r < L) {
+                const int64_t th = (tok0 + r) * H + h;
+                p.dq[th * DK + c] = dQr[nt][e] * e2;
+                p.dk[th * DK + c] = dKr[nt][e] * e2 + dKc[nt][e] * e3;
             }
-    }
-    // sum_v St Gt per channel: channel c, value columns of part hp (16-byte loads)
-    {
-        constexpr int NH = NT / DK, CW = VS / NH;
-        const int c = tid % DK, hp = tid / DK;
-        const float *sr = Sg + (int64_t)c * DV + v0 + hp * CW, *gr = Gg + (int64_t)c * DV + v0 + hp * CW;
-        float s0 = 0.f;
-#pragma unroll
-        for (int j = 0; j < CW; j += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(sr + j), g4 = *reinterpret_cast<const float4 *>(gr + j);
-            s0 += a4.x * g4.x + a4.y * g4.y + a4.z * g4.z + a4.w * g4.w;
+            dlogp[nt][e] = dKr[nt][e] * tb.Kr[rc] + dQr[nt][e] * tb.Qr[rc] - dKc[nt][e] * tb.Kc[rc];
         }
-        tb.part[hp * DK + c] = tb.mu[c] * tb.mu[c] * s0;
-    }
     // s123: sums over the 16 rows of this warp (lanes with the same t), then by warp row block
 #pragma unroll
     for (int nt = 0; nt < NK; ++nt)
@@ -843,31 +820,29 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             s123[nt][u] = x;
         }
     __syncthreads();  // every read of Qr is done
-    if (g == 0) {
-        const int t = lane & 3;
+    if (g == 0)
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) sm.red[(warp & 3) * DK + CK + 8 * nt + 2 * t + u] = s123[nt][u];
-    }
+            for (int u = 0; u < 2; ++u) sm.red[(warp & 3) * DK + CK + 8 * nt + 2 * t4 + u] = s123[nt][u];
     ffor<NK>(dlogp, R0, CK, [&](int r, int c, float &x) { tb.Qr[r * LDK + c] = x; });
     __syncthreads();
     // per channel: d log mu, then d log alpha by a reverse running sum over the rows
     if (tid < DK) {
         const int c = tid;
-        float s0 = 0.f;
-        for (int hp = 0; hp < NT / DK; ++hp) s0 += tb.part[hp * DK + c];
+        float s0c = 0.f;
+        for (int hp = 0; hp < NT / DK; ++hp) s0c += tb.part[hp * DK + c];
         float s123c = 0.f;
         for (int t2 = 0; t2 < 4; ++t2) s123c += sm.red[t2 * DK + c];
         float colsum = 0.f;
         for (int r = 0; r < L; ++r) colsum += tb.Qr[r * LDK + c];
-        const float dlogmu = 2.f * s0 + s123c - colsum;
+        const float dlogmu = 2.f * s0c + s123c - colsum;
         float run = 0.5f * dlogmu;
 #pragma unroll 8
         for (int r = L - 1; r >= 0; --r) {
             run += tb.Qr[r * LDK + c];
             const int64_t th = (tok0 + r) * H + h;
-            atomicAdd(&p.dalpha[th * DK + c], run / p.alpha[th * DK + c]);
+            p.dalpha[th * DK + c] = run / p.alpha[th * DK + c];
         }
     }
 }
@@ -909,16 +884,11 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     chain<<<heads, NT, sc, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (chunks == 0) return cudaSuccess;
-    // 4. the per-chunk gradients, added onto zeroed dq, dk, dalpha, dbeta
-    const size_t tok = (size_t)b.N * b.T * b.H;
-    if ((e = cudaMemsetAsync(b.dq, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(b.dk, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(b.dalpha, 0, tok * DK * sizeof(float), s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(b.dbeta, 0, tok * sizeof(float), s)) != cudaSuccess) return e;
+    // 4. every chunk's gradients
     auto local = kda_bwd_local_kernel<DK, TIn>;
     const size_t sl = sizeof(LocalSmem<DK>);
     if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
-    local<<<(unsigned)(chunks * nslices), NT, sl, s>>>(p);
+    local<<<(unsigned)chunks, NT, sl, s>>>(p);
     return cudaGetLastError();
 }
 
