@@ -134,69 +134,60 @@ template <int DK> __device__ __forceinline__ void prefetch_tables(const float *s
     for (int l = threadIdx.x; l < LINES; l += NT) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 32 * l));
 }
 
-// acc[i][jj] += sum_{m < K} a(ty + 16 i, m) * b(m, 4 tx + jj), with 16-byte
-// loads, K in steps of 4, operands given by pointer and leading dimension
-// (shared or global memory):
-//   MM_NN: a(r, m) = A[r lda + m], b(m, c) = B[m ldb + c]
-//   MM_NT: a(r, m) = A[r lda + m], b(m, c) = B[c ldb + m]
-//   MM_TN: a(r, m) = A[m lda + r], b(m, c) = B[m ldb + c]
-// ks (nullable) scales the terms of index m. A, B, lda, ldb keep 16-byte
-// alignment of the rows read as float4.
-enum Mode { MM_NN, MM_NT, MM_TN };
-template <int K, Mode MODE>
-__device__ __forceinline__ void mm4(float (&acc)[4][4], const float *__restrict__ A, int lda,
-                                    const float *__restrict__ B, int ldb, const float *__restrict__ ks = nullptr) {
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+// ---- warp-level products on the tensor cores (mma.sync, m16n8k8, tf32) with
+// fp32 accuracy: every operand x is split into hi = tf32(x) and lo =
+// tf32(x - hi), and a b = a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term is
+// below fp32 rounding). Fragment layout (lane = 4 g + t): A rows g, g + 8 and
+// columns t, t + 4; B rows t, t + 4 and column g; C rows g, g + 8 and columns
+// 2 t, 2 t + 1 of each 16 x 8 tile.
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_bits(x);
+    lo = tf32_bits(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc[nt] (the 16 x 8 tile at rows r0.., columns c0 + 8 nt ..) += sum_{k < K} a(r, k) b(k, c)
+template <int K, int NT8, typename FA, typename FB>
+__device__ __forceinline__ void wmm(float (&acc)[NT8][4], FA a, FB b, int r0, int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll 2
-    for (int m = 0; m < K; m += 4) {
-        float a[4][4], b[4][4];  // a[i][u] = a(ty + 16 i, m + u), b[u][jj] = b(m + u, 4 tx + jj)
-        if (MODE == MM_TN) {
+    for (int k = 0; k < K; k += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(a(r0 + g, k + t), ah[0], al[0]);
+        split_tf32(a(r0 + g + 8, k + t), ah[1], al[1]);
+        split_tf32(a(r0 + g, k + t + 4), ah[2], al[2]);
+        split_tf32(a(r0 + g + 8, k + t + 4), ah[3], al[3]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) a[i][u] = A[(m + u) * lda + ty + 16 * i];
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 f = *reinterpret_cast<const float4 *>(A + (ty + 16 * i) * lda + m);
-                a[i][0] = f.x; a[i][1] = f.y; a[i][2] = f.z; a[i][3] = f.w;
-            }
+        for (int nt = 0; nt < NT8; ++nt) {
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(b(k + t, c0 + 8 * nt + g), bh0, bl0);
+            split_tf32(b(k + t + 4, c0 + 8 * nt + g), bh1, bl1);
+            mma8(acc[nt], al, bh0, bh1);
+            mma8(acc[nt], ah, bl0, bl1);
+            mma8(acc[nt], ah, bh0, bh1);
         }
-        if (MODE == MM_NT) {
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float4 f = *reinterpret_cast<const float4 *>(B + (4 * tx + jj) * ldb + m);
-                b[0][jj] = f.x; b[1][jj] = f.y; b[2][jj] = f.z; b[3][jj] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 f = *reinterpret_cast<const float4 *>(B + (m + u) * ldb + 4 * tx);
-                b[u][0] = f.x; b[u][1] = f.y; b[u][2] = f.z; b[u][3] = f.w;
-            }
-        }
-        if (ks) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float sc = ks[m + u];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) b[u][jj] *= sc;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) acc[i][jj] += a[i][u] * b[u][jj];
     }
 }
-
-__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+template <int NT8> __device__ __forceinline__ void fzero(float (&acc)[NT8][4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+}
+// f(r, c, value&) for each accumulator element of the tile at (r0, c0)
+template <int NT8, typename F> __device__ __forceinline__ void ffor(float (&acc)[NT8][4], int r0, int c0, F f) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f(r0 + g + 8 * (e >> 1), c0 + 8 * nt + 2 * t + (e & 1), acc[nt][e]);
 }
 
 // ---------------------------------------------------------------- tables
@@ -220,25 +211,33 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
 // The forward chain only: one CTA per (sequence, head, value slice) writes the
 // state before every chunk (S_{n+1} = Diag(mu) (Diag(mu) S_n + Kc^T U), U =
 // T Diag(beta) (V - Kr Diag(mu) S_n)), reading the chunk's tables; slow
-// chunks go token by token (the §四 update).
+// chunks go token by token (the §四 update). Products on the tensor cores
+// (wmm: fp32 accuracy).
 template <int DK> struct StatesSmem {
-    float S[DK * VS];
+    float S[DK * LDC];  // the state slice, rows of LDC
     simt::Tables<DK> tb;
-    float R[C * VS];
-    float U[C * VS];
+    float R[C * LDC];
+    float U[C * LDC];
 };
-static_assert(offsetof(StatesSmem<128>, R) % 16 == 0 && offsetof(StatesSmem<64>, R) % 16 == 0 &&
-                  offsetof(StatesSmem<128>, U) % 16 == 0 && offsetof(StatesSmem<64>, U) % 16 == 0 &&
-                  offsetof(StatesSmem<128>, tb) % 16 == 0 && offsetof(StatesSmem<64>, tb) % 16 == 0,
-              "float4 accesses need 16-byte offsets");
+static_assert(offsetof(StatesSmem<128>, tb) % 16 == 0 && offsetof(StatesSmem<64>, tb) % 16 == 0,
+              "16-byte offsets");
+
+// Warp tiles of a DK x 64 product (the state slice): DK = 128 gives each warp
+// 16 rows and all 64 columns, DK = 64 16 rows and 32 columns.
+template <int DK> struct StateTile {
+    static constexpr int N8 = DK == 128 ? 8 : 4;
+    __device__ static int r0(int warp) { return 16 * (DK == 128 ? warp : (warp & 3)); }
+    __device__ static int c0(int warp) { return DK == 128 ? 0 : 32 * (warp >> 2); }
+};
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, const float *s0) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     StatesSmem<DK> &sm = *reinterpret_cast<StatesSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
-    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, RB = DK / 64;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    constexpr int LDK = simt::Tables<DK>::LDK;
+    using ST = StateTile<DK>;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int nslices = p.DV / VS;
     const int slice = blockIdx.x % nslices;
     const int h = (blockIdx.x / nslices) % p.H;
@@ -248,14 +247,16 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     const TIn *k = (const TIn *)p.k, *v = (const TIn *)p.v;
     float *st = p.states + sh * p.NC * DK * DV;
     const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
+    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
+    const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
     for (int e = tid; e < DK * VS; e += NT)
-        sm.S[e] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+        sm.S[(e / VS) * LDC + e % VS] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
     __syncthreads();
     for (int ci = 0; ci < p.NC; ++ci) {
         const int64_t t0 = (int64_t)ci * C, tok0 = t_begin + t0;
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         for (int e = tid; e < DK * VS; e += NT)
-            st[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[e];
+            st[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
         load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
         if (ci + 1 < p.NC) prefetch_tables<DK>(tabs + (int64_t)(ci + 1) * TabLayout<DK>::FLOATS);
         if (tb.slow) {
@@ -263,86 +264,59 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
             for (int r = 0; r < L; ++r) {
                 const int64_t tk = (tok0 + r) * H + h;
                 float vh = 0.f;
-                for (int c = part; c < DK; c += NT / VS) vh += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * sm.S[c * VS + j];
-                sm.R[part * VS + j] = vh;
+                for (int c = part; c < DK; c += NT / VS)
+                    vh += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * sm.S[c * LDC + j];
+                sm.R[part * LDC + j] = vh;
                 __syncthreads();
                 float vs = 0.f;
 #pragma unroll
-                for (int p2 = 0; p2 < NT / VS; ++p2) vs += sm.R[p2 * VS + j];
+                for (int p2 = 0; p2 < NT / VS; ++p2) vs += sm.R[p2 * LDC + j];
                 const float be = p.beta[tk] * (ld_in(v, tk * DV + v0 + j) - vs);
                 __syncthreads();
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.S[c * VS + j] = p.alpha[tk * DK + c] * sm.S[c * VS + j] + ld_in(k, tk * DK + c) * be;
+                    sm.S[c * LDC + j] = p.alpha[tk * DK + c] * sm.S[c * LDC + j] + ld_in(k, tk * DK + c) * be;
                 __syncthreads();
             }
             continue;
         }
         float acc[4][4];
         // R = Diag(beta) (V - Kr St)
-        zero(acc);
-        mm4<DK, MM_NN>(acc, tb.Kr, LDK, sm.S, VS, tb.mu);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = ty + 16 * i;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj) : 0.f;
-                sm.R[r * VS + 4 * tx + jj] = tb.beta[r] * (vv - acc[i][jj]);
-            }
-        }
+        fzero<4>(acc);
+        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
+                   [&](int c, int j) { return tb.mu[c] * sm.S[c * LDC + j]; }, R0, C0);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
+            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
+            sm.R[r * LDC + c] = tb.beta[r] * (vv - x);
+        });
         __syncthreads();
         // U = T R
-        zero(acc);
-        mm4<C, MM_NN>(acc, tb.T, LDC, sm.R, VS);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float4 *>(&sm.U[(ty + 16 * i) * VS + 4 * tx]) =
-                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        fzero<4>(acc);
+        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return sm.R[m * LDC + j]; }, R0,
+                  C0);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { sm.U[r * LDC + c] = x; });
         __syncthreads();
-        // S <- Diag(mu) (Diag(mu) S + Kc^T U); tile rows 64 b2 + 4 ty + i, columns 4 tx + jj
-        float acc2[RB][4][4];
-#pragma unroll
-        for (int b2 = 0; b2 < RB; ++b2) zero(acc2[b2]);
-        for (int r = 0; r < C; ++r) {
-            const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[r * VS + 4 * tx]);
-            const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-            for (int b2 = 0; b2 < RB; ++b2) {
-                const float4 k4 = *reinterpret_cast<const float4 *>(&tb.Kc[r * LDK + 64 * b2 + 4 * ty]);
-                const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) acc2[b2][i][jj] += kv[i] * uv[jj];
-            }
-        }
-#pragma unroll
-        for (int b2 = 0; b2 < RB; ++b2)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = 64 * b2 + 4 * ty + i;
-                const float m = tb.mu[c];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    float &sv = sm.S[c * VS + 4 * tx + jj];
-                    sv = m * (m * sv + acc2[b2][i][jj]);
-                }
-            }
+        // S <- Diag(mu) (Diag(mu) S + Kc^T U)
+        float acc2[ST::N8][4];
+        fzero<ST::N8>(acc2);
+        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Kc[r * LDK + c]; }, [&](int r, int j) { return sm.U[r * LDC + j]; },
+                       SR0, SC0);
+        ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
+            const float m = tb.mu[c];
+            float &sv = sm.S[c * LDC + j];
+            sv = m * (m * sv + x);
+        });
         __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------- chain
 template <int DK> struct ChainSmem {
-    float G[DK * VS];
+    float G[DK * LDC];  // dL/dS slice, rows of LDC
     simt::Tables<DK> tb;
-    float dO[C * VS];
+    float dO[C * LDC];
     float red[4 * VS];
 };
-
-static_assert(offsetof(ChainSmem<128>, dO) % 16 == 0 && offsetof(ChainSmem<64>, dO) % 16 == 0 &&
-                  offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, tb) % 16 == 0,
-              "float4 accesses need 16-byte offsets");
+static_assert(offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, tb) % 16 == 0, "16-byte offsets");
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
@@ -350,8 +324,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     ChainSmem<DK> &sm = *reinterpret_cast<ChainSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
     constexpr int LDK = simt::Tables<DK>::LDK;
-    constexpr int RB = DK / 64;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    using ST = StateTile<DK>;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int nslices = p.DV / VS;
     const int slice = blockIdx.x % nslices;
     const int h = (blockIdx.x / nslices) % p.H;
@@ -362,9 +336,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     const int64_t sh = (int64_t)n * H + h;
     float *gn = p.gnext + sh * p.NC * DK * DV;
     const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
+    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
+    const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
 
     for (int e = tid; e < DK * VS; e += NT)
-        sm.G[e] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+        sm.G[(e / VS) * LDC + e % VS] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
     __syncthreads();
 
     for (int ci = p.NC - 1; ci >= 0; --ci) {
@@ -372,10 +348,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         const int64_t tok0 = t_begin + t0;
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
-            gn[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[e];
+            gn[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
         for (int e = tid; e < C * VS; e += NT) {
             const int r = e / VS;
-            sm.dO[e] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
+            sm.dO[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
         }
         load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
         if (ci > 0) prefetch_tables<DK>(tabs + (int64_t)(ci - 1) * TabLayout<DK>::FLOATS);
@@ -384,11 +360,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
             const int j = tid % VS, part = tid / VS;
             for (int r = L - 1; r >= 0; --r) {
                 const int64_t tk = (tok0 + r) * H + h;
-                const float dj = sm.dO[r * VS + j];
+                const float dj = sm.dO[r * LDC + j];
                 float wp = 0.f;
                 for (int c = part; c < DK; c += NT / VS) {
-                    const float g = sm.G[c * VS + j] + ld_in(q, tk * DK + c) * dj;
-                    sm.G[c * VS + j] = g;
+                    const float g = sm.G[c * LDC + j] + ld_in(q, tk * DK + c) * dj;
+                    sm.G[c * LDC + j] = g;
                     wp += ld_in(k, tk * DK + c) * g;
                 }
                 sm.red[part * VS + j] = wp;
@@ -398,7 +374,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
                 for (int p2 = 0; p2 < NT / VS; ++p2) w += sm.red[p2 * VS + j];
                 const float bt = p.beta[tk];
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.G[c * VS + j] = p.alpha[tk * DK + c] * (sm.G[c * VS + j] - bt * ld_in(k, tk * DK + c) * w);
+                    sm.G[c * LDC + j] = p.alpha[tk * DK + c] * (sm.G[c * LDC + j] - bt * ld_in(k, tk * DK + c) * w);
                 __syncthreads();
             }
             continue;
@@ -406,60 +382,36 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         float *dU = tb.A;  // a work tile here
         float acc[4][4];
         // dU = Kc Gt + P^T dO
-        zero(acc);
-        mm4<DK, MM_NN>(acc, tb.Kc, LDK, sm.G, VS, tb.mu);
-        mm4<C, MM_TN>(acc, tb.P, LDC, sm.dO, VS);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) dU[(ty + 16 * i) * LDC + 4 * tx + jj] = acc[i][jj];
+        fzero<4>(acc);
+        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
+                   [&](int c, int j) { return tb.mu[c] * sm.G[c * LDC + j]; }, R0, C0);
+        wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * LDC + j]; }, R0,
+                  C0);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = x; });
         __syncthreads();
         // dX = -Diag(beta) T^T dU (into dU's place)
-        zero(acc);
-        mm4<C, MM_TN>(acc, tb.T, LDC, dU, LDC);
+        fzero<4>(acc);
+        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; }, R0, C0);
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                dU[(ty + 16 * i) * LDC + 4 * tx + jj] = -tb.beta[ty + 16 * i] * acc[i][jj];
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = -tb.beta[r] * x; });
         __syncthreads();
-        // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX); tile rows 64 b2 + 4 ty + i, columns 4 tx + jj
-        float acc2[RB][4][4];
-#pragma unroll
-        for (int b2 = 0; b2 < RB; ++b2) zero(acc2[b2]);
-        for (int r = 0; r < C; ++r) {
-            const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dO[r * VS + 4 * tx]);
-            const float4 x4 = *reinterpret_cast<const float4 *>(&dU[r * LDC + 4 * tx]);
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w}, xv4[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-            for (int b2 = 0; b2 < RB; ++b2) {
-                const float4 q4 = *reinterpret_cast<const float4 *>(&tb.Qr[r * LDK + 64 * b2 + 4 * ty]);
-                const float4 k4 = *reinterpret_cast<const float4 *>(&tb.Kr[r * LDK + 64 * b2 + 4 * ty]);
-                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) acc2[b2][i][jj] += qv[i] * dv4[jj] + kv[i] * xv4[jj];
-            }
-        }
-#pragma unroll
-        for (int b2 = 0; b2 < RB; ++b2)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = 64 * b2 + 4 * ty + i;
-                const float m = tb.mu[c];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    float &g = sm.G[c * VS + 4 * tx + jj];
-                    g = m * (m * g + acc2[b2][i][jj]);
-                }
-            }
+        // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX)
+        float acc2[ST::N8][4];
+        fzero<ST::N8>(acc2);
+        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Qr[r * LDK + c]; },
+                       [&](int r, int j) { return sm.dO[r * LDC + j]; }, SR0, SC0);
+        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Kr[r * LDK + c]; }, [&](int r, int j) { return dU[r * LDC + j]; },
+                       SR0, SC0);
+        ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
+            const float m = tb.mu[c];
+            float &gv = sm.G[c * LDC + j];
+            gv = m * (m * gv + x);
+        });
         __syncthreads();
     }
     if (p.ds0)
         for (int e = tid; e < DK * VS; e += NT)
-            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[e];
+            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
 }
 
 // ---------------------------------------------------------------- local
@@ -570,62 +522,6 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
             G[c * DV + j] = p.alpha[tk * DK + c] * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
         __syncthreads();
     }
-}
-
-// ---- warp-level products on the tensor cores (mma.sync, m16n8k8, tf32) with
-// fp32 accuracy: every operand x is split into hi = tf32(x) and lo =
-// tf32(x - hi), and a b = a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term is
-// below fp32 rounding). Fragment layout (lane = 4 g + t): A rows g, g + 8 and
-// columns t, t + 4; B rows t, t + 4 and column g; C rows g, g + 8 and columns
-// 2 t, 2 t + 1 of each 16 x 8 tile.
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_bits(x);
-    lo = tf32_bits(x - __uint_as_float(hi));
-}
-__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// acc[nt] (the 16 x 8 tile at rows r0.., columns c0 + 8 nt ..) += sum_{k < K} a(r, k) b(k, c)
-template <int K, int NT8, typename FA, typename FB>
-__device__ __forceinline__ void wmm(float (&acc)[NT8][4], FA a, FB b, int r0, int c0) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
-    for (int k = 0; k < K; k += 8) {
-        uint32_t ah[4], al[4];
-        split_tf32(a(r0 + g, k + t), ah[0], al[0]);
-        split_tf32(a(r0 + g + 8, k + t), ah[1], al[1]);
-        split_tf32(a(r0 + g, k + t + 4), ah[2], al[2]);
-        split_tf32(a(r0 + g + 8, k + t + 4), ah[3], al[3]);
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) {
-            uint32_t bh0, bl0, bh1, bl1;
-            split_tf32(b(k + t, c0 + 8 * nt + g), bh0, bl0);
-            split_tf32(b(k + t + 4, c0 + 8 * nt + g), bh1, bl1);
-            mma8(acc[nt], al, bh0, bh1);
-            mma8(acc[nt], ah, bl0, bl1);
-            mma8(acc[nt], ah, bh0, bh1);
-        }
-    }
-}
-template <int NT8> __device__ __forceinline__ void fzero(float (&acc)[NT8][4]) {
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-}
-// f(r, c, value&) for each accumulator element of the tile at (r0, c0)
-template <int NT8, typename F> __device__ __forceinline__ void ffor(float (&acc)[NT8][4], int r0, int c0, F f) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) f(r0 + g + 8 * (e >> 1), c0 + 8 * nt + 2 * t + (e & 1), acc[nt][e]);
 }
 
 template <int DK, typename TIn>
@@ -846,6 +742,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         }
     }
 }
+
+constexpr size_t kMaxSmem = 232448;  // dynamic shared memory one CTA may have
+static_assert(sizeof(StatesSmem<128>) <= kMaxSmem && sizeof(ChainSmem<128>) <= kMaxSmem &&
+                  sizeof(LocalSmem<128>) <= kMaxSmem && sizeof(simt::Tables<128>) <= kMaxSmem,
+              "shared memory per CTA");
 
 template <int DK, typename TIn>
 cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
