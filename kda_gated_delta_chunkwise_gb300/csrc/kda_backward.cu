@@ -98,6 +98,13 @@ template <int DK> __device__ void store_tables(const simt::Tables<DK> &tb, float
     if (tid == 0) dst[L::SLOW] = __int_as_float(tb.slow);
 }
 
+// 16 bytes global -> shared without a register round trip (cp.async), so
+// that every thread has all its loads of a table in flight at once.
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+
 // Loads the parts `which` (TAB_*) of a chunk's tables, plus mu, beta and the
 // slow flag; T and P only when the chunk is not slow. Ends with a barrier.
 template <int DK> __device__ void load_tables(simt::Tables<DK> &tb, const float *src, unsigned which) {
@@ -107,23 +114,19 @@ template <int DK> __device__ void load_tables(simt::Tables<DK> &tb, const float 
     const int slow = __float_as_int(src[L::SLOW]);
     for (int e = tid; e < C * Q4; e += NT) {
         const int r = e / Q4, c = 4 * (e % Q4);
-        if (which & TAB_KR)
-            *reinterpret_cast<float4 *>(&tb.Kr[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::KR + r * DK + c);
-        if (which & TAB_QR)
-            *reinterpret_cast<float4 *>(&tb.Qr[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::QR + r * DK + c);
-        if (which & TAB_KC)
-            *reinterpret_cast<float4 *>(&tb.Kc[r * LDK + c]) = *reinterpret_cast<const float4 *>(src + L::KC + r * DK + c);
+        if (which & TAB_KR) cp16(&tb.Kr[r * LDK + c], src + L::KR + r * DK + c);
+        if (which & TAB_QR) cp16(&tb.Qr[r * LDK + c], src + L::QR + r * DK + c);
+        if (which & TAB_KC) cp16(&tb.Kc[r * LDK + c], src + L::KC + r * DK + c);
     }
     if (!slow)
         for (int e = tid; e < C * C4; e += NT) {
             const int r = e / C4, c = 4 * (e % C4);
-            if (which & TAB_T)
-                *reinterpret_cast<float4 *>(&tb.T[r * LDC + c]) = *reinterpret_cast<const float4 *>(src + L::T + r * C + c);
-            if (which & TAB_P)
-                *reinterpret_cast<float4 *>(&tb.P[r * LDC + c]) = *reinterpret_cast<const float4 *>(src + L::P + r * C + c);
+            if (which & TAB_T) cp16(&tb.T[r * LDC + c], src + L::T + r * C + c);
+            if (which & TAB_P) cp16(&tb.P[r * LDC + c], src + L::P + r * C + c);
         }
-    for (int e = tid; e < DK; e += NT) tb.mu[e] = src[L::MU + e];
-    for (int e = tid; e < C; e += NT) tb.beta[e] = src[L::BETA + e];
+    for (int e = tid; e < DK / 4; e += NT) cp16(&tb.mu[4 * e], src + L::MU + 4 * e);
+    for (int e = tid; e < C / 4; e += NT) cp16(&tb.beta[4 * e], src + L::BETA + 4 * e);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     if (tid == 0) tb.slow = slow;
     __syncthreads();
 }
