@@ -226,9 +226,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -924,16 +921,15 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
         const uint32_t c8 = (uint32_t)cq >> 1, sub = ((uint32_t)cq & 1u) * 8u;
         const uint32_t rowbase = (uint32_t)rg * 1024u + sub;
         // alpha of this thread's channels in rows 8 rg .. 8 rg + 7 goes from
-        // global memory straight into registers: prefetched into L2 one chunk
-        // ahead, loaded before the chunk's waits (rows past the sequence end
-        // are not read)
+        // global memory straight into registers, loaded before the chunk's
+        // waits (rows past the sequence end are not read). (An L2 prefetch
+        // one chunk ahead gained nothing and cost 1.4 KB of hot code.)
         // (one gate per token-head, broadcast over the channels, for the
         // scalar kind; none at all for the delta rule)
         auto alpha_src = [&](int n) {
             const int64_t th = (t_begin + (int64_t)n * C + 8 * rg) * H + h;
             return GATE == KDA_GATE_CHANNEL ? p.alpha + th * DK + c0 + 4 * cq : p.alpha + th;
         };
-        const int64_t astep = GATE == KDA_GATE_CHANNEL ? (int64_t)H * DK : (int64_t)H;  // one token
         bool alive = true;
         for (int n = 0; n <= NC; ++n) {
           if (n < NC) {
@@ -1037,13 +1033,6 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
             if (ok && pt == 0) vslot[0] = slow ? 1 : 0;
             fence_proxy_async();
             named_bar(1, GATE_THREADS);
-            if (n + 1 < NC) {  // the next chunk's alpha rows into L2
-                const int Ln = (int)((T - (int64_t)(n + 1) * C) < C ? (T - (int64_t)(n + 1) * C) : C);
-                const float *src = alpha_src(n + 1);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (GATE != KDA_GATE_NONE && 8 * rg + j < Ln) prefetch_l2(src + j * astep);
-            }
             if (ok && pt == 0) {
                 // this key half into the peer (its slot n % 3 was released with
                 // QK_EMPTY and B0_EMPTY of chunk n-3, in both CTAs)
