@@ -369,6 +369,20 @@ kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, k
                                   float *dalpha, float *dbeta, float *d_initial_state, int B, int T, int H,
                                   int d_k, int d_v, void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_prefill_backward_gate - kda_prefill_backward with a gate kind (see
+ * kda_gate_t): alpha and dalpha are [B, T, H, d_k] (CHANNEL), [B, T, H]
+ * (SCALAR: the gradient of the one gate a token-head has, i.e. the sum over
+ * the channels of the per-channel gradient) or unused and NULL-able (NONE).
+ * Everything else as kda_prefill_backward (same workspace).
+ */
+kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                       const float *alpha, kda_gate_t gate, const float *beta,
+                                       const float *initial_state, const void *d_o, const float *d_final_state,
+                                       float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                                       float *d_initial_state, int B, int T, int H, int d_k, int d_v,
+                                       void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
 /* Workspace bytes kda_prefill_backward needs (0 for invalid arguments). */
 size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 

@@ -31,7 +31,7 @@ EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8
            "kda_varlen_prefill", "kda_varlen_prefill_slots",
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_prefill_workspace_bytes",
            "kda_decode_step", "kda_decode_step_slots", "kda_selftest_bounded_wait",
-           "kda_prefill_backward", "kda_prefill_backward_workspace_bytes",
+           "kda_prefill_backward", "kda_prefill_backward_gate", "kda_prefill_backward_workspace_bytes",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
 _lock = threading.Lock()
@@ -96,6 +96,9 @@ def load(path: str | None = None):
         lib.kda_prefill_backward.restype = i
         lib.kda_prefill_backward.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                              i, i, i, i, i, vp, ctypes.c_size_t, vp]
+        lib.kda_prefill_backward_gate.restype = i
+        lib.kda_prefill_backward_gate.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                  i, i, i, i, i, vp, ctypes.c_size_t, vp]
         lib.kda_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.kda_last_error.restype = ctypes.c_char_p
@@ -523,25 +526,25 @@ def prefill_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, initial_state=N
 
 
 def prefill_backward(q, k, v, alpha, beta, d_o, initial_state=None, d_final_state=None, *,
-                     want_initial_state_grad: bool = True, workspace=None, stream=None):
-    """Gradients of ``prefill`` (per-channel gate, equal-length batches) for
+                     gate: str = "channel", want_initial_state_grad: bool = True, workspace=None, stream=None):
+    """Gradients of ``prefill`` (equal-length batches) for
     L = sum <d_o, o> + <d_final_state, S_T>.
 
-    q, k, v, alpha, beta, initial_state as for ``prefill``; d_o: o's shape and
-    dtype; d_final_state: [B, H, d_k, d_v] fp32 or None (zero). Returns a dict
-    of float32 tensors: ``dq``, ``dk``, ``dv``, ``dalpha``, ``dbeta`` and
-    ``d_initial_state`` (None when not wanted)."""
+    q, k, v, alpha, beta, initial_state, gate as for ``prefill``; d_o: o's
+    shape and dtype; d_final_state: [B, H, d_k, d_v] fp32 or None (zero).
+    Returns a dict of float32 tensors: ``dq``, ``dk``, ``dv``, ``dalpha``
+    (alpha's shape; None without a gate), ``dbeta`` and ``d_initial_state``
+    (None when not wanted)."""
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_o, "d_o")):
         _need(t, n, q.dtype, dev)
-    _need(alpha, "alpha", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape != (B, T, H, dv) or alpha.shape != q.shape or beta.shape != (B, T, H) \
-            or d_o.shape != v.shape:
-        raise ValueError("shape mismatch among q, k, v, alpha, beta, d_o")
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H) or d_o.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, beta, d_o")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, dev)
     for t, n in ((initial_state, "initial_state"), (d_final_state, "d_final_state")):
         if t is not None:
             _need(t, n, torch.float32, dev)
@@ -549,15 +552,16 @@ def prefill_backward(q, k, v, alpha, beta, d_o, initial_state=None, d_final_stat
                 raise ValueError(f"{n} must be {(B, H, dk, dv)}")
     f32 = dict(dtype=torch.float32, device=dev)
     out = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(k.shape, **f32), "dv": torch.empty(v.shape, **f32),
-           "dalpha": torch.empty(alpha.shape, **f32), "dbeta": torch.empty(beta.shape, **f32),
+           "dalpha": None if alpha is None else torch.empty(alpha.shape, **f32),
+           "dbeta": torch.empty(beta.shape, **f32),
            "d_initial_state": torch.empty((B, H, dk, dv), **f32) if want_initial_state_grad else None}
     nbytes = int(lib.kda_prefill_backward_workspace_bytes(B, T, H, dk, dv))
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    st = lib.kda_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
-                                  _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(out["dq"]),
-                                  _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dalpha"]), _ptr(out["dbeta"]),
-                                  _ptr(out["d_initial_state"]), B, T, H, dk, dv, _ptr(workspace), workspace.numel(),
-                                  _stream(stream))
+    st = lib.kda_prefill_backward_gate(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate],
+                                       _ptr(beta), _ptr(initial_state), _ptr(d_o), _ptr(d_final_state),
+                                       _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dalpha"]),
+                                       _ptr(out["dbeta"]), _ptr(out["d_initial_state"]), B, T, H, dk, dv,
+                                       _ptr(workspace), workspace.numel(), _stream(stream))
     _check(lib, st)
     return out

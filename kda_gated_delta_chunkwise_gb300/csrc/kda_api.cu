@@ -301,13 +301,15 @@ size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_
     return kda::backward_workspace_bytes(B, T, H, d_k, d_v);
 }
 
-kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                                  const float *alpha, const float *beta, const float *initial_state,
-                                  const void *d_o, const float *d_final_state, float *dq, float *dk, float *dv,
-                                  float *dalpha, float *dbeta, float *d_initial_state, int B, int T, int H,
-                                  int d_k, int d_v, void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                       const float *alpha, kda_gate_t gate, const float *beta,
+                                       const float *initial_state, const void *d_o, const float *d_final_state,
+                                       float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                                       float *d_initial_state, int B, int T, int H, int d_k, int d_v,
+                                       void *workspace, size_t workspace_bytes, kda_stream_t stream) {
     kda_status_t st;
     if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
+    if ((st = check_gate(gate)) != KDA_OK) return st;
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
     if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
     if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
@@ -315,12 +317,17 @@ kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, k
     if ((int64_t)B * H * (nc > 0 ? nc : 1) * 2 > INT32_MAX)
         return fail(KDA_ERR_UNSUPPORTED, "B * H * ceil(T / 64) * 2 must fit in int32");
     const bool any = (int64_t)B * T > 0;
-    if ((st = check_tensors(q, k, v, alpha, beta, d_o, initial_state, d_final_state, any)) != KDA_OK) return st;
+    if ((st = check_tensors(q, k, v, alpha, beta, d_o, initial_state, d_final_state, any, gate)) != KDA_OK) return st;
     if (any) {
         KDA_REQUIRE_PTR(dq);
         KDA_REQUIRE_PTR(dk);
         KDA_REQUIRE_PTR(dv);
-        KDA_REQUIRE_PTR(dalpha);
+        if (gate == KDA_GATE_CHANNEL) KDA_REQUIRE_PTR(dalpha);
+        if (gate == KDA_GATE_SCALAR) {
+            if (!dalpha) return fail(KDA_ERR_INVALID_ARG, "dalpha must not be NULL");
+            if (reinterpret_cast<uintptr_t>(dalpha) & 3u)
+                return fail(KDA_ERR_INVALID_ARG, "dalpha must be 4-byte aligned");
+        }
         if (!dbeta) return fail(KDA_ERR_INVALID_ARG, "dbeta must not be NULL");
         if (reinterpret_cast<uintptr_t>(dbeta) & 3u) return fail(KDA_ERR_INVALID_ARG, "dbeta must be 4-byte aligned");
     }
@@ -335,8 +342,19 @@ kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, k
     b.alpha = alpha; b.beta = beta; b.s0 = initial_state; b.dsT = d_final_state;
     b.dq = dq; b.dk = dk; b.dvv = dv; b.dalpha = dalpha; b.dbeta = dbeta; b.ds0 = d_initial_state;
     b.workspace = workspace;
+    b.gate = gate;
     b.N = B; b.T = T; b.H = H; b.d_k = d_k; b.d_v = d_v;
     return cuda_status(kda::launch_backward(b, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
+}
+
+kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                  const float *alpha, const float *beta, const float *initial_state,
+                                  const void *d_o, const float *d_final_state, float *dq, float *dk, float *dv,
+                                  float *dalpha, float *dbeta, float *d_initial_state, int B, int T, int H,
+                                  int d_k, int d_v, void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return kda_prefill_backward_gate(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, initial_state, d_o,
+                                     d_final_state, dq, dk, dv, dalpha, dbeta, d_initial_state, B, T, H, d_k, d_v,
+                                     workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_selftest_bounded_wait(const void *q, const void *k, const void *v, const float *alpha,

@@ -64,6 +64,7 @@ struct BwdParams {
     float *states;        // [N, H, NC, DK, DV]: the state before every chunk
     float *gnext;         // [N, H, NC, DK, DV]: dL/dS after every chunk
     float *tabs;          // [N, H, NC, TabLayout<DK>::FLOATS]: every chunk's tables
+    int gate;             // kda_gate_t: dalpha per channel, per token-head, or none
     int N, T, H, DV, NC;
 };
 
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
     const int64_t t0 = (int64_t)ci * C;
     const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
     const int64_t tok0 = (int64_t)n * p.T + t0;
-    simt::gate_tables<DK, TIn>(tb, p.alpha, KDA_GATE_CHANNEL, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
+    simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
                                p.H, h);
     if (!tb.slow) simt::wy_tables<DK>(tb);
     store_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS);
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
                 const int64_t tk = (tok0 + r) * H + h;
                 float vh = 0.f;
                 for (int c = part; c < DK; c += NT / VS)
-                    vh += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * sm.S[c * LDC + j];
+                    vh += gate_at(p.alpha, p.gate, tk, c, DK) * ld_in(k, tk * DK + c) * sm.S[c * LDC + j];
                 sm.R[part * LDC + j] = vh;
                 __syncthreads();
                 float vs = 0.f;
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
                 const float be = p.beta[tk] * (ld_in(v, tk * DV + v0 + j) - vs);
                 __syncthreads();
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.S[c * LDC + j] = p.alpha[tk * DK + c] * sm.S[c * LDC + j] + ld_in(k, tk * DK + c) * be;
+                    sm.S[c * LDC + j] = gate_at(p.alpha, p.gate, tk, c, DK) * sm.S[c * LDC + j] + ld_in(k, tk * DK + c) * be;
                 __syncthreads();
             }
             continue;
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
                 for (int p2 = 0; p2 < NT / VS; ++p2) w += sm.red[p2 * VS + j];
                 const float bt = p.beta[tk];
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.G[c * LDC + j] = p.alpha[tk * DK + c] * (sm.G[c * LDC + j] - bt * ld_in(k, tk * DK + c) * w);
+                    sm.G[c * LDC + j] = gate_at(p.alpha, p.gate, tk, c, DK) * (sm.G[c * LDC + j] - bt * ld_in(k, tk * DK + c) * w);
                 __syncthreads();
             }
             continue;
@@ -440,7 +441,8 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
     float *Sb = sm.tb.Kr, *G = sm.tb.Kc;
     float *redv = sm.W[0], *redw = sm.W[0] + NP * DV, *ev = sm.W[0] + 2 * NP * DV, *wv = ev + DV;
-    float *redc = sm.W[1];  // [NH][4][DK]
+    float *redc = sm.W[1];                    // [NH][4][DK]
+    float *das = sm.W[1] + 4 * NH * DK;       // [DK]: a token's dalpha by channel
     const int j = tid % DV, part = tid / DV;
     for (int e = tid; e < DK * DV; e += NT) G[e] = Gg[e];
     for (int r = L - 1; r >= 0; --r) {
@@ -450,14 +452,14 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
         for (int m = 0; m < r; ++m) {
             const int64_t tk = (tok0 + m) * H + h;
             float vp = 0.f;
-            for (int c = part; c < DK; c += NP) vp += p.alpha[tk * DK + c] * ld_in(k, tk * DK + c) * Sb[c * DV + j];
+            for (int c = part; c < DK; c += NP) vp += gate_at(p.alpha, p.gate, tk, c, DK) * ld_in(k, tk * DK + c) * Sb[c * DV + j];
             redv[part * DV + j] = vp;
             __syncthreads();
             float vh = 0.f;
             for (int p2 = 0; p2 < NP; ++p2) vh += redv[p2 * DV + j];
             const float be = p.beta[tk] * (ld_in(v, tk * DV + j) - vh);
             for (int c = part; c < DK; c += NP)
-                Sb[c * DV + j] = p.alpha[tk * DK + c] * Sb[c * DV + j] + ld_in(k, tk * DK + c) * be;
+                Sb[c * DV + j] = gate_at(p.alpha, p.gate, tk, c, DK) * Sb[c * DV + j] + ld_in(k, tk * DK + c) * be;
             __syncthreads();
         }
         // reverse step of token r
@@ -470,7 +472,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                 const float kc = ld_in(k, tk * DK + c);
                 const float g = G[c * DV + j] + ld_in(q, tk * DK + c) * dj;
                 G[c * DV + j] = g;
-                vp += p.alpha[tk * DK + c] * kc * Sb[c * DV + j];
+                vp += gate_at(p.alpha, p.gate, tk, c, DK) * kc * Sb[c * DV + j];
                 wp += kc * g;
             }
             redv[part * DV + j] = vp;
@@ -491,7 +493,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
         {
             // row mapping: channel c, value columns of part hp
             const int c = tid % DK, hp = tid / DK, cw = DV / NH;
-            const float ac = p.alpha[tk * DK + c], kc = ld_in(k, tk * DK + c);
+            const float ac = gate_at(p.alpha, p.gate, tk, c, DK), kc = ld_in(k, tk * DK + c);
             float dq = 0.f, ge = 0.f, sw = 0.f, da = 0.f;
             for (int jj = hp * cw; jj < (hp + 1) * cw; ++jj) {
                 const float sv = Sb[c * DV + jj], g = G[c * DV + jj], e = ev[jj], w = wv[jj];
@@ -512,17 +514,24 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                     for (int u = 0; u < 4; ++u) s4[u] += redc[(h2 * 4 + u) * DK + tid];
                 p.dq[tk * DK + tid] = s4[0];
                 p.dk[tk * DK + tid] = bt * (s4[1] - s4[2]);
-                p.dalpha[tk * DK + tid] = s4[3];
+                if (p.gate == KDA_GATE_CHANNEL) p.dalpha[tk * DK + tid] = s4[3];
+                das[tid] = s4[3];
             }
             if (tid == 0) {
                 float db = 0.f;
                 for (int jj = 0; jj < DV; ++jj) db += wv[jj] * ev[jj];
                 p.dbeta[tk] = db;
             }
+            __syncthreads();
+            if (tid == 0 && p.gate == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them
+                float da = 0.f;
+                for (int c = 0; c < DK; ++c) da += das[c];
+                p.dalpha[tk] = da;
+            }
         }
         // G = Diag(alpha)(G - beta k w^T)
         for (int c = part; c < DK; c += NP)
-            G[c * DV + j] = p.alpha[tk * DK + c] * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
+            G[c * DV + j] = gate_at(p.alpha, p.gate, tk, c, DK) * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
         __syncthreads();
     }
 }
@@ -690,7 +699,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
-    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, KDA_GATE_CHANNEL, tok0, L, H, h);
+    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, p.gate, tok0, L, H, h);
     tb.part[(tid / DK) * DK + tid % DK] = tb.mu[tid % DK] * tb.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid];
     float dlogp[NK][4];
@@ -741,7 +750,17 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int r = L - 1; r >= 0; --r) {
             run += tb.Qr[r * LDK + c];
             const int64_t th = (tok0 + r) * H + h;
-            p.dalpha[th * DK + c] = run / p.alpha[th * DK + c];
+            const float da = run / gate_at(p.alpha, p.gate, th, c, DK);
+            if (p.gate == KDA_GATE_CHANNEL) p.dalpha[th * DK + c] = da;
+            tb.Qr[r * LDK + c] = da;  // (this thread's own column, read only by itself above)
+        }
+    }
+    if (p.gate == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
+        __syncthreads();
+        if (tid < L) {
+            float da = 0.f;
+            for (int c = 0; c < DK; ++c) da += tb.Qr[tid * LDK + c];
+            p.dalpha[(tok0 + tid) * H + h] = da;
         }
     }
 }
@@ -763,7 +782,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     p.states = ws;
     p.gnext = ws + chunks * DK * b.d_v;
     p.tabs = ws + 2 * chunks * DK * b.d_v;
-    p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC;
+    p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC; p.gate = b.gate;
     cudaError_t e;
     const unsigned heads = (unsigned)((int64_t)b.N * b.H * nslices);
     if (chunks > 0) {  // 1. every chunk's tables, all chunks at once

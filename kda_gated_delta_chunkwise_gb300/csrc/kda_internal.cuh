@@ -83,6 +83,7 @@ struct BackwardArgs {
     float *dq, *dk, *dvv, *dalpha, *dbeta;
     float *ds0;                            // nullable
     void *workspace;                       // backward_workspace_bytes, 16-byte aligned
+    int gate;                              // kda_gate_t (layout of alpha and dalpha)
     int N, T, H, d_k, d_v;
 };
 size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv);

@@ -112,3 +112,34 @@ def test_backward_zero_length(kda):
     g = kda.prefill_backward(e, e, e, e, torch.empty(2, 0, 3, device=d), e, d_final_state=dsT)
     torch.cuda.synchronize()
     torch.testing.assert_close(g["d_initial_state"], dsT, rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "none"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_backward_gate_kinds(kda, gate, dtype):
+    """Scalar gate (Gated DeltaNet) and no gate (the delta rule): the oracle
+    runs the per-channel gate expanded from them (alpha repeated over the
+    channels, or all ones); the scalar gate's gradient is the sum over the
+    channels of the per-channel one. Includes a chunk decaying past e^-80 (a
+    token-level chunk) for the scalar gate."""
+    x = W.batched(2, 200, 2, 128, 128, dtype=dtype, alpha_scale=0.1, s0_std=0.05, seed=40)
+    B, T, H, dk = x.q.shape
+    a_s = x.alpha[..., 0].contiguous()
+    if gate == "scalar":
+        a_s[0, 70:134, 1] = 0.2  # e^-103 over one chunk of head 1
+    d_o, dsT = _upstream(x, 41)
+    d = torch.device("cuda")
+    g = kda.prefill_backward(x.q.to(d), x.k.to(d), x.v.to(d), None if gate == "none" else a_s.to(d), x.beta.to(d),
+                             d_o.to(d), initial_state=x.initial_state.to(d), d_final_state=dsT.to(d), gate=gate)
+    torch.cuda.synchronize()
+    full = oracle.expand_gate(a_s.numpy(), gate, (B, T, H), dk)
+    ref = oracle.backward(x.q, x.k, x.v, full, x.beta, d_o, dsT, initial_state=x.initial_state)
+    rel = 1e-4 if dtype == "fp32" else 5e-3
+    for key in ("dq", "dk", "dv", "dbeta", "d_initial_state"):
+        r = ref[key]
+        assert_close(key, g[key].cpu(), r, dict(rel=rel, abs=max(1e-6, rel * 4 * float(np.abs(r).max()))))
+    if gate == "none":
+        assert g["dalpha"] is None
+    else:
+        r = ref["dalpha"].sum(axis=-1)
+        assert_close("dalpha", g["dalpha"].cpu(), r, dict(rel=rel, abs=max(1e-6, rel * 4 * float(np.abs(r).max()))))
