@@ -387,6 +387,30 @@ kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void 
 size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 
 /*
+ * kda_varlen_prefill_backward - the gradients of kda_varlen_prefill (N
+ * sequences packed along the token axis by cu_seqlens, each with its own
+ * initial state and chunk grid), with a gate kind as in
+ * kda_prefill_backward_gate. Layouts as kda_varlen_prefill; the gradients
+ * have the layouts of their inputs ([T_total, H, ...]; d_initial_state
+ * [N, H, d_k, d_v]). Every sequence's gradients are those of
+ * kda_prefill_backward_gate on that sequence alone, bit for bit.
+ * cu_seqlens (DEVICE) is checked on the device: on a bad one device_status
+ * (DEVICE int32, nullable) receives KDA_DEV_BAD_CU_SEQLENS and nothing is
+ * written; otherwise KDA_DEV_OK. workspace: kda_varlen_prefill_backward_
+ * workspace_bytes(N, T_total, H, d_k, d_v) bytes, 16-byte aligned.
+ */
+kda_status_t kda_varlen_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                         const float *alpha, kda_gate_t gate, const float *beta,
+                                         const float *initial_state, const void *d_o, const float *d_final_state,
+                                         float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                                         float *d_initial_state, const int32_t *cu_seqlens, int N, int T_total,
+                                         int H, int d_k, int d_v, void *workspace, size_t workspace_bytes,
+                                         int32_t *device_status, kda_stream_t stream);
+
+/* Workspace bytes kda_varlen_prefill_backward needs (0 for invalid arguments). */
+size_t kda_varlen_prefill_backward_workspace_bytes(int N, int T_total, int H, int d_k, int d_v);
+
+/*
  * kda_selftest_bounded_wait - diagnostic with no counterpart in the method:
  * runs the tensor-core prefill on one bf16 sequence of one head (B = H = 1,
  * d_k = d_v = 128, T tokens, zero initial state; tensors as for kda_prefill)

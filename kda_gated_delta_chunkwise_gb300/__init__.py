@@ -17,4 +17,5 @@ kda_prefill_fp8_host); and for serving with a pool of states indexed by slot:
 from ._binding import (ALGOS, EXPORTS, GATES, KDA_DEV_BAD_CU_SEQLENS, KDA_DEV_BAD_SLOT,  # noqa: F401
                        KDA_DEV_OK, KdaError, decode_step, decode_step_slots, device_errors, lib_path, load,
                        prefill, prefill_backward, prefill_fp8, prefill_workspace_bytes, selftest_bounded_wait, varlen_prefill,
+                       varlen_prefill_backward,
                        varlen_prefill_slots, varlen_workspace_bytes)

@@ -32,6 +32,7 @@ EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_prefill_workspace_bytes",
            "kda_decode_step", "kda_decode_step_slots", "kda_selftest_bounded_wait",
            "kda_prefill_backward", "kda_prefill_backward_gate", "kda_prefill_backward_workspace_bytes",
+           "kda_varlen_prefill_backward", "kda_varlen_prefill_backward_workspace_bytes",
            "kda_device_errors", "kda_last_error", "kda_abi_version")
 
 _lock = threading.Lock()
@@ -99,6 +100,11 @@ def load(path: str | None = None):
         lib.kda_prefill_backward_gate.restype = i
         lib.kda_prefill_backward_gate.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                   i, i, i, i, i, vp, ctypes.c_size_t, vp]
+        lib.kda_varlen_prefill_backward.restype = i
+        lib.kda_varlen_prefill_backward.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                    vp, i, i, i, i, i, vp, ctypes.c_size_t, vp, vp]
+        lib.kda_varlen_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_varlen_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.kda_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.kda_last_error.restype = ctypes.c_char_p
@@ -563,5 +569,46 @@ def prefill_backward(q, k, v, alpha, beta, d_o, initial_state=None, d_final_stat
                                        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dalpha"]),
                                        _ptr(out["dbeta"]), _ptr(out["d_initial_state"]), B, T, H, dk, dv,
                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def varlen_prefill_backward(q, k, v, alpha, beta, d_o, cu_seqlens, initial_state=None, d_final_state=None, *,
+                            gate: str = "channel", workspace=None, device_status=None, stream=None):
+    """Gradients of ``varlen_prefill`` (sequences packed by ``cu_seqlens``):
+    q, k: [T_total, H, d_k]; v, d_o: [T_total, H, d_v]; alpha per ``gate``
+    with lead [T_total, H]; beta: [T_total, H]; cu_seqlens: int32 [N + 1] on
+    the device; initial_state, d_final_state: [N, H, d_k, d_v] fp32 or None.
+    Returns the dict of ``prefill_backward``."""
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_o, "d_o")):
+        _need(t, n, q.dtype, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    Tt, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if k.shape != q.shape or v.shape != (Tt, H, dv) or beta.shape != (Tt, H) or d_o.shape != v.shape:
+        raise ValueError("shape mismatch among q, k, v, beta, d_o")
+    alpha = _check_gate(gate, alpha, (Tt, H), dk, dev)
+    for t, n in ((initial_state, "initial_state"), (d_final_state, "d_final_state")):
+        if t is not None:
+            _need(t, n, torch.float32, dev)
+            if t.shape != (N, H, dk, dv):
+                raise ValueError(f"{n} must be {(N, H, dk, dv)}")
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(k.shape, **f32), "dv": torch.empty(v.shape, **f32),
+           "dalpha": None if alpha is None else torch.empty(alpha.shape, **f32),
+           "dbeta": torch.empty(beta.shape, **f32), "d_initial_state": torch.empty((N, H, dk, dv), **f32)}
+    nbytes = int(lib.kda_varlen_prefill_backward_workspace_bytes(N, Tt, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    st = lib.kda_varlen_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate],
+                                         _ptr(beta), _ptr(initial_state), _ptr(d_o), _ptr(d_final_state),
+                                         _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dalpha"]),
+                                         _ptr(out["dbeta"]), _ptr(out["d_initial_state"]), _ptr(cu_seqlens), N, Tt,
+                                         H, dk, dv, _ptr(workspace), workspace.numel(), _ptr(device_status),
+                                         _stream(stream))
     _check(lib, st)
     return out

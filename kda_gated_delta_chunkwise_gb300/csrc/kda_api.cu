@@ -298,25 +298,38 @@ kda_status_t kda_varlen_prefill_slots(const void *q, const void *k, const void *
 
 size_t kda_prefill_backward_workspace_bytes(int B, int T, int H, int d_k, int d_v) {
     if (B < 0 || T < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return 0;
-    return kda::backward_workspace_bytes(B, T, H, d_k, d_v);
+    return kda::backward_workspace_bytes(B, T, H, d_k, d_v, false);
 }
 
-kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                                       const float *alpha, kda_gate_t gate, const float *beta,
-                                       const float *initial_state, const void *d_o, const float *d_final_state,
-                                       float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
-                                       float *d_initial_state, int B, int T, int H, int d_k, int d_v,
-                                       void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+size_t kda_varlen_prefill_backward_workspace_bytes(int N, int T_total, int H, int d_k, int d_v) {
+    if (N < 0 || T_total < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return 0;
+    return kda::backward_workspace_bytes(N, T_total, H, d_k, d_v, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The checks and the launch shared by the equal-length and the packed backward
+// (cu_seqlens == NULL: B sequences of T tokens; else N = B packed sequences of
+// T = T_total tokens in all).
+kda_status_t backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype, const float *alpha,
+                      kda_gate_t gate, const float *beta, const float *initial_state, const void *d_o,
+                      const float *d_final_state, float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                      float *d_initial_state, const int32_t *cu_seqlens, int B, int T, int H, int d_k, int d_v,
+                      void *workspace, size_t workspace_bytes, int32_t *device_status, kda_stream_t stream) {
     kda_status_t st;
+    const bool packed = cu_seqlens != nullptr;
     if ((st = check_dtype(qkv_dtype)) != KDA_OK) return st;
     if ((st = check_gate(gate)) != KDA_OK) return st;
     if ((st = check_dims(H, d_k, d_v)) != KDA_OK) return st;
-    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B and T must be >= 0 (got %d, %d)", B, T);
-    if ((int64_t)B * T > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "B * T must fit in int32");
-    const int64_t nc = ((int64_t)T + 63) / 64;
-    if ((int64_t)B * H * (nc > 0 ? nc : 1) * 2 > INT32_MAX)
-        return fail(KDA_ERR_UNSUPPORTED, "B * H * ceil(T / 64) * 2 must fit in int32");
-    const bool any = (int64_t)B * T > 0;
+    if (B < 0 || T < 0) return fail(KDA_ERR_INVALID_ARG, "B (N) and T (T_total) must be >= 0 (got %d, %d)", B, T);
+    const int64_t tokens = packed ? (int64_t)T : (int64_t)B * T;
+    if (tokens > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "the token count must fit in int32");
+    const int64_t chunks = packed ? ((int64_t)T + 63) / 64 + B : (int64_t)B * (((int64_t)T + 63) / 64);
+    if ((chunks > 0 ? chunks : 1) * H * 2 > INT32_MAX)
+        return fail(KDA_ERR_UNSUPPORTED, "the chunks of all sequences times H times 2 must fit in int32");
+    const bool any = tokens > 0;
     if ((st = check_tensors(q, k, v, alpha, beta, d_o, initial_state, d_final_state, any, gate)) != KDA_OK) return st;
     if (any) {
         KDA_REQUIRE_PTR(dq);
@@ -332,8 +345,14 @@ kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void 
         if (reinterpret_cast<uintptr_t>(dbeta) & 3u) return fail(KDA_ERR_INVALID_ARG, "dbeta must be 4-byte aligned");
     }
     KDA_OPTIONAL_PTR(d_initial_state);
+    if (packed) {
+        if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+        if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+            return fail(KDA_ERR_INVALID_ARG, "device_status must be 4-byte aligned");
+    }
     if (B == 0) return ok();
-    const size_t need = kda::backward_workspace_bytes(B, T, H, d_k, d_v);
+    const size_t need = kda::backward_workspace_bytes(B, T, H, d_k, d_v, packed);
     if (need && (!workspace || workspace_bytes < need))
         return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
     if (need && !aligned16(workspace)) return fail(KDA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
@@ -344,7 +363,23 @@ kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void 
     b.workspace = workspace;
     b.gate = gate;
     b.N = B; b.T = T; b.H = H; b.d_k = d_k; b.d_v = d_v;
+    b.cu_seqlens = cu_seqlens;
+    b.dev_status = device_status;
     return cuda_status(kda::launch_backward(b, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_prefill_backward_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                       const float *alpha, kda_gate_t gate, const float *beta,
+                                       const float *initial_state, const void *d_o, const float *d_final_state,
+                                       float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                                       float *d_initial_state, int B, int T, int H, int d_k, int d_v,
+                                       void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return backward(q, k, v, qkv_dtype, alpha, gate, beta, initial_state, d_o, d_final_state, dq, dk, dv, dalpha,
+                    dbeta, d_initial_state, nullptr, B, T, H, d_k, d_v, workspace, workspace_bytes, nullptr, stream);
 }
 
 kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
@@ -355,6 +390,20 @@ kda_status_t kda_prefill_backward(const void *q, const void *k, const void *v, k
     return kda_prefill_backward_gate(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, initial_state, d_o,
                                      d_final_state, dq, dk, dv, dalpha, dbeta, d_initial_state, B, T, H, d_k, d_v,
                                      workspace, workspace_bytes, stream);
+}
+
+kda_status_t kda_varlen_prefill_backward(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                         const float *alpha, kda_gate_t gate, const float *beta,
+                                         const float *initial_state, const void *d_o, const float *d_final_state,
+                                         float *dq, float *dk, float *dv, float *dalpha, float *dbeta,
+                                         float *d_initial_state, const int32_t *cu_seqlens, int N, int T_total,
+                                         int H, int d_k, int d_v, void *workspace, size_t workspace_bytes,
+                                         int32_t *device_status, kda_stream_t stream) {
+    if (N > 0 && !cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    if (N == 0) return ok();
+    return backward(q, k, v, qkv_dtype, alpha, gate, beta, initial_state, d_o, d_final_state, dq, dk, dv, dalpha,
+                    dbeta, d_initial_state, cu_seqlens, N, T_total, H, d_k, d_v, workspace, workspace_bytes,
+                    device_status, stream);
 }
 
 kda_status_t kda_selftest_bounded_wait(const void *q, const void *k, const void *v, const float *alpha,

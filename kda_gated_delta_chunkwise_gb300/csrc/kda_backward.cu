@@ -65,8 +65,47 @@ struct BwdParams {
     float *gnext;         // [N, H, NC, DK, DV]: dL/dS after every chunk
     float *tabs;          // [N, H, NC, TabLayout<DK>::FLOATS]: every chunk's tables
     int gate;             // kda_gate_t: dalpha per channel, per token-head, or none
-    int N, T, H, DV, NC;
+    int N, T, H, DV, NC;  // T, NC: tokens and chunks of every sequence (equal lengths)
+    const int32_t *cu;    // nullable: sequences packed by cu_seqlens [N + 1] (T is then T_total)
+    const int32_t *coff;  // packed: first chunk of every sequence [N + 1]
+    const int32_t *status;  // packed: nonzero = bad cu_seqlens, nothing runs
 };
+
+// Sequence n: first token, length and first chunk. The workspace holds every
+// chunk of every sequence at (chunk * H + head).
+__device__ __forceinline__ void seq_of(const BwdParams &p, int n, int64_t &t_begin, int64_t &T, int64_t &cbase) {
+    if (p.cu) {
+        t_begin = p.cu[n];
+        T = (int64_t)p.cu[n + 1] - t_begin;
+        cbase = p.coff[n];
+    } else {
+        t_begin = (int64_t)n * p.T;
+        T = p.T;
+        cbase = (int64_t)n * p.NC;
+    }
+}
+// Flat chunk c: its sequence, first token and length; false past the last
+// chunk (packed launches are sized by an upper bound).
+__device__ __forceinline__ bool chunk_of(const BwdParams &p, int64_t c, int &n, int64_t &tok0, int &L) {
+    if (p.cu) {
+        if (c >= p.coff[p.N]) return false;
+        int lo = 0, hi = p.N - 1;  // the last n with coff[n] <= c (empty sequences own no chunk)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.coff[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        n = lo;
+    } else {
+        n = (int)(c / p.NC);
+    }
+    int64_t t_begin, T, cbase;
+    seq_of(p, n, t_begin, T, cbase);
+    const int64_t t0 = (c - cbase) * C;
+    tok0 = t_begin + t0;
+    L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
+    return true;
+}
 
 // Every chunk's tables, computed once by kda_bwd_tables_kernel (all chunks at
 // once) and read by the three passes that follow, so the serial chains do
@@ -200,11 +239,11 @@ template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     simt::Tables<DK> &tb = *reinterpret_cast<simt::Tables<DK> *>(smem_raw);
-    const int64_t idx = blockIdx.x;  // (n H + h) NC + ci
-    const int ci = (int)(idx % p.NC), h = (int)((idx / p.NC) % p.H), n = (int)(idx / ((int64_t)p.NC * p.H));
-    const int64_t t0 = (int64_t)ci * C;
-    const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
-    const int64_t tok0 = (int64_t)n * p.T + t0;
+    const int64_t idx = blockIdx.x;  // chunk * H + head
+    const int h = (int)(idx % p.H);
+    int n, L;
+    int64_t tok0;
+    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
     simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
                                p.H, h);
     if (!tb.slow) simt::wy_tables<DK>(tb);
@@ -247,22 +286,26 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     const int h = (blockIdx.x / nslices) % p.H;
     const int n = blockIdx.x / (nslices * p.H);
     const int H = p.H, DV = p.DV, v0 = slice * VS;
-    const int64_t T = p.T, t_begin = (int64_t)n * p.T, sh = (int64_t)n * H + h;
+    if (p.status && *p.status) return;
+    int64_t t_begin, T, cbase;
+    seq_of(p, n, t_begin, T, cbase);
+    const int NC = (int)((T + C - 1) / C);
+    const int64_t sh = (int64_t)n * H + h;
     const TIn *k = (const TIn *)p.k, *v = (const TIn *)p.v;
-    float *st = p.states + sh * p.NC * DK * DV;
-    const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
+    float *st = p.states + (cbase * H + h) * DK * DV;                   // chunk i at i H DK DV
+    const float *tabs = p.tabs + (cbase * H + h) * TabLayout<DK>::FLOATS;  // chunk i at i H FLOATS
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
     for (int e = tid; e < DK * VS; e += NT)
         sm.S[(e / VS) * LDC + e % VS] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
     __syncthreads();
-    for (int ci = 0; ci < p.NC; ++ci) {
+    for (int ci = 0; ci < NC; ++ci) {
         const int64_t t0 = (int64_t)ci * C, tok0 = t_begin + t0;
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         for (int e = tid; e < DK * VS; e += NT)
-            st[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
-        load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
-        if (ci + 1 < p.NC) prefetch_tables<DK>(tabs + (int64_t)(ci + 1) * TabLayout<DK>::FLOATS);
+            st[(int64_t)ci * H * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
+        load_tables<DK>(tb, tabs + (int64_t)ci * H * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
+        if (ci + 1 < NC) prefetch_tables<DK>(tabs + (int64_t)(ci + 1) * H * TabLayout<DK>::FLOATS);
         if (tb.slow) {
             const int j = tid % VS, part = tid / VS;
             for (int r = 0; r < L; ++r) {
@@ -335,11 +378,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     const int h = (blockIdx.x / nslices) % p.H;
     const int n = blockIdx.x / (nslices * p.H);
     const int H = p.H, DV = p.DV, v0 = slice * VS;
-    const int64_t T = p.T, t_begin = (int64_t)n * p.T;
+    if (p.status && *p.status) return;
+    int64_t t_begin, T, cbase;
+    seq_of(p, n, t_begin, T, cbase);
+    const int NC = (int)((T + C - 1) / C);
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *dO = (const TIn *)p.d_o;
     const int64_t sh = (int64_t)n * H + h;
-    float *gn = p.gnext + sh * p.NC * DK * DV;
-    const float *tabs = p.tabs + sh * p.NC * TabLayout<DK>::FLOATS;
+    float *gn = p.gnext + (cbase * H + h) * DK * DV;                    // chunk i at i H DK DV
+    const float *tabs = p.tabs + (cbase * H + h) * TabLayout<DK>::FLOATS;  // chunk i at i H FLOATS
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
 
@@ -347,18 +393,18 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         sm.G[(e / VS) * LDC + e % VS] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
     __syncthreads();
 
-    for (int ci = p.NC - 1; ci >= 0; --ci) {
+    for (int ci = NC - 1; ci >= 0; --ci) {
         const int64_t t0 = (int64_t)ci * C;
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         const int64_t tok0 = t_begin + t0;
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
-            gn[(int64_t)ci * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
+            gn[(int64_t)ci * H * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
         for (int e = tid; e < C * VS; e += NT) {
             const int r = e / VS;
             sm.dO[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
         }
-        load_tables<DK>(tb, tabs + (int64_t)ci * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
-        if (ci > 0) prefetch_tables<DK>(tabs + (int64_t)(ci - 1) * TabLayout<DK>::FLOATS);
+        load_tables<DK>(tb, tabs + (int64_t)ci * H * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
+        if (ci > 0) prefetch_tables<DK>(tabs + (int64_t)(ci - 1) * H * TabLayout<DK>::FLOATS);
         if (tb.slow) {
             // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
             const int j = tid % VS, part = tid / VS;
@@ -544,12 +590,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     constexpr int LDK = simt::Tables<DK>::LDK;
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int64_t idx = blockIdx.x;  // (n H + h) NC + ci
-    const int ci = (int)(idx % p.NC), h = (int)((idx / p.NC) % p.H), n = (int)(idx / ((int64_t)p.NC * p.H));
+    const int64_t idx = blockIdx.x;  // chunk * H + head
+    const int h = (int)(idx % p.H);
     const int H = p.H, DV = p.DV;
-    const int64_t t0 = (int64_t)ci * C;
-    const int L = (int)(((int64_t)p.T - t0) < C ? ((int64_t)p.T - t0) : (int64_t)C);
-    const int64_t tok0 = (int64_t)n * p.T + t0;
+    int n, L;
+    int64_t tok0;
+    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
     const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
     const float *Sg = p.states + idx * DK * DV, *Gg = p.gnext + idx * DK * DV;
 
@@ -770,27 +816,94 @@ static_assert(sizeof(StatesSmem<128>) <= kMaxSmem && sizeof(ChainSmem<128>) <= k
                   sizeof(LocalSmem<128>) <= kMaxSmem && sizeof(simt::Tables<128>) <= kMaxSmem,
               "shared memory per CTA");
 
+// Packed batches: checks cu_seqlens (starts at 0, never decreases, ends at
+// T_total) and lists the first chunk of every sequence (coff, an exclusive
+// sum of ceil(L_n / 64)); on a bad cu_seqlens it writes the status and an
+// empty chunk list, and every later kernel skips its work.
+constexpr int kPrepThreads = 1024;
+__global__ void __launch_bounds__(kPrepThreads) kda_bwd_varlen_prep_kernel(const int32_t *__restrict__ cu, int N,
+                                                                          int T_total, int32_t *__restrict__ coff,
+                                                                          int32_t *__restrict__ status) {
+    __shared__ int bad;
+    __shared__ int32_t part[kPrepThreads];
+    __shared__ int32_t total;
+    const int tid = threadIdx.x;
+    if (tid == 0) bad = (cu[0] != 0 || cu[N] != T_total) ? 1 : 0;
+    __syncthreads();
+    const int per = (N + kPrepThreads - 1) / kPrepThreads, lo = tid * per, hi = lo + per < N ? lo + per : N;
+    int32_t local = 0;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t L = cu[i + 1] - cu[i];
+        if (L < 0) atomicOr(&bad, 1);
+        else local += (L + C - 1) / C;
+    }
+    part[tid] = local;
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int t = 0; t < kPrepThreads; ++t) {
+            const int32_t x = part[t];
+            part[t] = run;
+            run += x;
+        }
+        total = run;
+    }
+    __syncthreads();
+    int32_t run = part[tid];
+    for (int i = lo; i < hi; ++i) {
+        coff[i] = run;
+        const int32_t L = cu[i + 1] - cu[i];
+        run += L > 0 ? (L + C - 1) / C : 0;
+    }
+    if (tid == 0) {
+        coff[N] = bad ? 0 : total;
+        *status = bad ? KDA_DEV_BAD_CU_SEQLENS : KDA_DEV_OK;
+    }
+}
+
+// Chunks the workspace must hold: every chunk of equal-length sequences, or
+// for a packed batch an upper bound (each sequence adds at most one partial
+// chunk to ceil(T_total / 64)).
+int64_t chunk_bound(bool packed, int N, int T) {
+    return packed ? ((int64_t)T + C - 1) / C + N : (int64_t)N * ((T + C - 1) / C);
+}
+
 template <int DK, typename TIn>
 cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
-    const int NC = (b.T + C - 1) / C;
+    const bool packed = b.cu_seqlens != nullptr;
+    const int NC = packed ? 0 : (b.T + C - 1) / C;
     const int nslices = b.d_v / VS;
-    const int64_t chunks = (int64_t)b.N * b.H * NC;
+    const int64_t chunks = chunk_bound(packed, b.N, b.T);
     BwdParams p;
     p.q = b.q; p.k = b.k; p.v = b.v; p.d_o = b.d_o; p.alpha = b.alpha; p.beta = b.beta; p.dsT = b.dsT;
     p.dq = b.dq; p.dk = b.dk; p.dv = b.dvv; p.dalpha = b.dalpha; p.dbeta = b.dbeta; p.ds0 = b.ds0;
     float *ws = static_cast<float *>(b.workspace);
+    const int64_t slab = chunks * b.H * DK * b.d_v;
     p.states = ws;
-    p.gnext = ws + chunks * DK * b.d_v;
-    p.tabs = ws + 2 * chunks * DK * b.d_v;
+    p.gnext = ws + slab;
+    p.tabs = ws + 2 * slab;
     p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC; p.gate = b.gate;
+    p.cu = b.cu_seqlens;
+    p.coff = nullptr;
+    p.status = nullptr;
     cudaError_t e;
+    if (packed) {
+        int32_t *tail = reinterpret_cast<int32_t *>(p.tabs + chunks * b.H * TabLayout<DK>::FLOATS);
+        int32_t *coff = tail + 4;  // tail[0]: the status word when the caller gives none
+        int32_t *status = b.dev_status ? b.dev_status : tail;
+        kda_bwd_varlen_prep_kernel<<<1, kPrepThreads, 0, s>>>(b.cu_seqlens, b.N, b.T, coff, status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        p.coff = coff;
+        p.status = status;
+    }
     const unsigned heads = (unsigned)((int64_t)b.N * b.H * nslices);
+    const unsigned chunk_ctas = (unsigned)(chunks * b.H);
     if (chunks > 0) {  // 1. every chunk's tables, all chunks at once
         auto tabk = kda_bwd_tables_kernel<DK, TIn>;
         const size_t st = sizeof(simt::Tables<DK>);
         if ((e = cudaFuncSetAttribute(tabk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st)) != cudaSuccess)
             return e;
-        tabk<<<(unsigned)chunks, NT, st, s>>>(p);
+        tabk<<<chunk_ctas, NT, st, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // 2. the state before every chunk
         auto stk = kda_bwd_states_kernel<DK, TIn>;
@@ -800,7 +913,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
         stk<<<heads, NT, ss, s>>>(p, b.s0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // 3. the reverse state-gradient chain (also for T = 0: dS_0 = dS_T)
+    // 3. the reverse state-gradient chain (also for empty sequences: dS_0 = dS_T)
     auto chain = kda_bwd_chain_kernel<DK, TIn>;
     const size_t sc = sizeof(ChainSmem<DK>);
     if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc)) != cudaSuccess) return e;
@@ -811,16 +924,17 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     auto local = kda_bwd_local_kernel<DK, TIn>;
     const size_t sl = sizeof(LocalSmem<DK>);
     if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
-    local<<<(unsigned)chunks, NT, sl, s>>>(p);
+    local<<<chunk_ctas, NT, sl, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv) {
-    const size_t chunks = (size_t)N * H * (((size_t)T + C - 1) / C);
+size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv, bool packed) {
+    const size_t chunks = (size_t)chunk_bound(packed, N, T) * H;
     const size_t tab = dk == 128 ? TabLayout<128>::FLOATS : TabLayout<64>::FLOATS;
-    return (2 * chunks * dk * dv + chunks * tab) * sizeof(float);
+    const size_t tail = packed ? (4 + (size_t)N + 1) * sizeof(int32_t) : 0;  // status, chunk offsets
+    return (2 * chunks * dk * dv + chunks * tab) * sizeof(float) + tail;
 }
 
 cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s) {

@@ -84,9 +84,11 @@ struct BackwardArgs {
     float *ds0;                            // nullable
     void *workspace;                       // backward_workspace_bytes, 16-byte aligned
     int gate;                              // kda_gate_t (layout of alpha and dalpha)
-    int N, T, H, d_k, d_v;
+    int N, T, H, d_k, d_v;                 // packed: T is T_total
+    const int32_t *cu_seqlens;             // nullable: packed sequences
+    int32_t *dev_status;                   // packed, nullable: the device status word
 };
-size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv);
+size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv, bool packed);
 cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s);
 
 // Varlen preparation: validates cu_seqlens, writes the status word, sorts the

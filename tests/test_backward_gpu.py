@@ -143,3 +143,54 @@ def test_backward_gate_kinds(kda, gate, dtype):
     else:
         r = ref["dalpha"].sum(axis=-1)
         assert_close("dalpha", g["dalpha"].cpu(), r, dict(rel=rel, abs=max(1e-6, rel * 4 * float(np.abs(r).max()))))
+
+
+def _packed_upstream(x, seed):
+    r = np.random.default_rng(seed)
+    d_o = torch.from_numpy(r.standard_normal(x.v.shape, dtype=np.float32)).to(x.v.dtype)
+    N, H, dk, dv = x.num_seqs, x.q.shape[1], x.q.shape[2], x.v.shape[-1]
+    dsT = torch.from_numpy(r.standard_normal((N, H, dk, dv), dtype=np.float32))
+    return d_o, dsT
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_varlen_backward_bitexact_and_oracle(kda, dtype):
+    """Packed sequences (lengths 130, 1, 64, 0, 257, 63, 65): every sequence's
+    gradients are bitwise those of the equal-length backward on it alone, and
+    the whole packed result matches the oracle."""
+    x = W.packed([130, 1, 64, 0, 257, 63, 65], 3, 128, 128, dtype=dtype, s0_std=0.05, seed=50)
+    d_o, dsT = _packed_upstream(x, 51)
+    d = torch.device("cuda")
+    q, k, v, a, b = (t.to(d) for t in x.tensors())
+    cu, s0, do_d, dsT_d = x.cu_seqlens.to(d), x.initial_state.to(d), d_o.to(d), dsT.to(d)
+    status = torch.full((1,), -1, dtype=torch.int32, device=d)
+    g = kda.varlen_prefill_backward(q, k, v, a, b, do_d, cu, s0, dsT_d, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kda.KDA_DEV_OK
+    cuh = x.cu_seqlens.tolist()
+    for n in range(len(cuh) - 1):
+        lo, hi = cuh[n], cuh[n + 1]
+        gn = kda.prefill_backward(q[None, lo:hi], k[None, lo:hi], v[None, lo:hi], a[None, lo:hi], b[None, lo:hi],
+                                  do_d[None, lo:hi], s0[n:n + 1], dsT_d[n:n + 1])
+        for key in ("dq", "dk", "dv", "dalpha", "dbeta"):
+            assert torch.equal(g[key][lo:hi], gn[key][0]), f"sequence {n}: {key} differs from its own backward"
+        assert torch.equal(g["d_initial_state"][n], gn["d_initial_state"][0]), f"sequence {n}: dS0 differs"
+    ref = oracle.backward(*x.tensors(), d_o, dsT, cu_seqlens=x.cu_seqlens, initial_state=x.initial_state)
+    rel = 1e-4 if dtype == "fp32" else 5e-3
+    for key in KEYS:
+        r = ref[key]
+        assert_close(key, g[key].cpu(), r, dict(rel=rel, abs=max(1e-6, rel * 4 * float(np.abs(r).max()))))
+
+
+def test_varlen_backward_bad_cu_seqlens_sets_status(kda):
+    x = W.packed([40, 50, 60], 2, 64, 64, dtype="fp32", s0_std=0.05, seed=52)
+    d_o, dsT = _packed_upstream(x, 53)
+    d = torch.device("cuda")
+    q, k, v, a, b = (t.to(d) for t in x.tensors())
+    cu = x.cu_seqlens.to(d).clone()
+    cu[1] = 100  # decreasing
+    status = torch.full((1,), -1, dtype=torch.int32, device=d)
+    kda.varlen_prefill_backward(q, k, v, a, b, d_o.to(d), cu, x.initial_state.to(d), dsT.to(d),
+                                device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kda.KDA_DEV_BAD_CU_SEQLENS
