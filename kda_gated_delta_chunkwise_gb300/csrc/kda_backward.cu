@@ -239,14 +239,11 @@ template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     simt::Tables<DK> &tb = *reinterpret_cast<simt::Tables<DK> *>(smem_raw);
-    // launch order: head-major (consecutive CTAs take consecutive chunks of
-    // one head); workspace order: chunk * H + head
-    const int64_t nct = gridDim.x / p.H, c = blockIdx.x % nct;
-    const int h = (int)(blockIdx.x / nct);
-    const int64_t idx = c * p.H + h;
+    const int64_t idx = blockIdx.x;  // chunk * H + head
+    const int h = (int)(idx % p.H);
     int n, L;
     int64_t tok0;
-    if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
+    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
     simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
                                p.H, h);
     if (!tb.slow) simt::wy_tables<DK>(tb);
@@ -593,15 +590,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     constexpr int LDK = simt::Tables<DK>::LDK;
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    // launch order: head-major (consecutive CTAs take consecutive chunks of
-    // one head); workspace order: chunk * H + head
-    const int64_t nct = gridDim.x / p.H, c = blockIdx.x % nct;
-    const int h = (int)(blockIdx.x / nct);
-    const int64_t idx = c * p.H + h;
+    const int64_t idx = blockIdx.x;  // chunk * H + head
+    const int h = (int)(idx % p.H);
     const int H = p.H, DV = p.DV;
     int n, L;
     int64_t tok0;
-    if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
+    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
     const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
     const float *Sg = p.states + idx * DK * DV, *Gg = p.gnext + idx * DK * DV;
 
