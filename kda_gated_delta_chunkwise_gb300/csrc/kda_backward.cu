@@ -84,6 +84,31 @@ __device__ __forceinline__ void seq_of(const BwdParams &p, int n, int64_t &t_beg
         cbase = (int64_t)n * p.NC;
     }
 }
+// The workspace slot of a sequence's chunks: slot(ci) = base + ci * stride.
+// Equal lengths keep each (sequence, head)'s chunks together ((n H + h) NC +
+// ci); packed batches go by chunk, then head (c H + h).
+__device__ __forceinline__ void slots_of(const BwdParams &p, int n, int h, int64_t cbase, int64_t &base,
+                                         int64_t &stride) {
+    if (p.cu) {
+        base = cbase * p.H + h;
+        stride = p.H;
+    } else {
+        base = ((int64_t)n * p.H + h) * p.NC;
+        stride = 1;
+    }
+}
+// The chunk and head of a CTA of the chunk-parallel passes, in the order of
+// the workspace slots (its index is the slot).
+__device__ __forceinline__ void cta_chunk(const BwdParams &p, int64_t bid, int64_t &c, int &h) {
+    if (p.cu) {
+        c = bid / p.H;
+        h = (int)(bid % p.H);
+    } else {
+        const int64_t nh = bid / p.NC;
+        h = (int)(nh % p.H);
+        c = (nh / p.H) * p.NC + bid % p.NC;
+    }
+}
 // Flat chunk c: its sequence, first token and length; false past the last
 // chunk (packed launches are sized by an upper bound).
 __device__ __forceinline__ bool chunk_of(const BwdParams &p, int64_t c, int &n, int64_t &tok0, int &L) {
@@ -239,11 +264,12 @@ template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     simt::Tables<DK> &tb = *reinterpret_cast<simt::Tables<DK> *>(smem_raw);
-    const int64_t idx = blockIdx.x;  // chunk * H + head
-    const int h = (int)(idx % p.H);
-    int n, L;
+    const int64_t idx = blockIdx.x;  // the chunk's workspace slot
+    int64_t c;
+    int h, n, L;
     int64_t tok0;
-    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
+    cta_chunk(p, idx, c, h);
+    if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
     simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
                                p.H, h);
     if (!tb.slow) simt::wy_tables<DK>(tb);
@@ -292,8 +318,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     const int NC = (int)((T + C - 1) / C);
     const int64_t sh = (int64_t)n * H + h;
     const TIn *k = (const TIn *)p.k, *v = (const TIn *)p.v;
-    float *st = p.states + (cbase * H + h) * DK * DV;                   // chunk i at i H DK DV
-    const float *tabs = p.tabs + (cbase * H + h) * TabLayout<DK>::FLOATS;  // chunk i at i H FLOATS
+    int64_t wbase, wstride;
+    slots_of(p, n, h, cbase, wbase, wstride);
+    float *st = p.states + wbase * DK * DV;                    // chunk i at slot wbase + i wstride
+    const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
     for (int e = tid; e < DK * VS; e += NT)
@@ -303,9 +331,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         const int64_t t0 = (int64_t)ci * C, tok0 = t_begin + t0;
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         for (int e = tid; e < DK * VS; e += NT)
-            st[(int64_t)ci * H * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
-        load_tables<DK>(tb, tabs + (int64_t)ci * H * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
-        if (ci + 1 < NC) prefetch_tables<DK>(tabs + (int64_t)(ci + 1) * H * TabLayout<DK>::FLOATS);
+            st[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
+        load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
+        if (ci + 1 < NC) prefetch_tables<DK>(tabs + (ci + 1) * wstride * TabLayout<DK>::FLOATS);
         if (tb.slow) {
             const int j = tid % VS, part = tid / VS;
             for (int r = 0; r < L; ++r) {
@@ -384,8 +412,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     const int NC = (int)((T + C - 1) / C);
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *dO = (const TIn *)p.d_o;
     const int64_t sh = (int64_t)n * H + h;
-    float *gn = p.gnext + (cbase * H + h) * DK * DV;                    // chunk i at i H DK DV
-    const float *tabs = p.tabs + (cbase * H + h) * TabLayout<DK>::FLOATS;  // chunk i at i H FLOATS
+    int64_t wbase, wstride;
+    slots_of(p, n, h, cbase, wbase, wstride);
+    float *gn = p.gnext + wbase * DK * DV;                     // chunk i at slot wbase + i wstride
+    const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
 
@@ -398,13 +428,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         const int64_t tok0 = t_begin + t0;
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
-            gn[(int64_t)ci * H * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
+            gn[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
         for (int e = tid; e < C * VS; e += NT) {
             const int r = e / VS;
             sm.dO[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
         }
-        load_tables<DK>(tb, tabs + (int64_t)ci * H * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
-        if (ci > 0) prefetch_tables<DK>(tabs + (int64_t)(ci - 1) * H * TabLayout<DK>::FLOATS);
+        load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
+        if (ci > 0) prefetch_tables<DK>(tabs + (ci - 1) * wstride * TabLayout<DK>::FLOATS);
         if (tb.slow) {
             // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
             const int j = tid % VS, part = tid / VS;
@@ -590,12 +620,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     constexpr int LDK = simt::Tables<DK>::LDK;
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int64_t idx = blockIdx.x;  // chunk * H + head
-    const int h = (int)(idx % p.H);
-    const int H = p.H, DV = p.DV;
-    int n, L;
+    const int64_t idx = blockIdx.x;  // the chunk's workspace slot
+    int64_t c;
+    int h, n, L;
     int64_t tok0;
-    if ((p.status && *p.status) || !chunk_of(p, idx / p.H, n, tok0, L)) return;
+    cta_chunk(p, idx, c, h);
+    const int H = p.H, DV = p.DV;
+    if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
     const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
     const float *Sg = p.states + idx * DK * DV, *Gg = p.gnext + idx * DK * DV;
 
@@ -798,7 +829,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             const int64_t th = (tok0 + r) * H + h;
             const float da = run / gate_at(p.alpha, p.gate, th, c, DK);
             if (p.gate == KDA_GATE_CHANNEL) p.dalpha[th * DK + c] = da;
-            tb.Qr[r * LDK + c] = da;  // (this thread's own column, read only by itself above)
+            else tb.Qr[r * LDK + c] = da;  // (this thread's own column, read only by itself above)
         }
     }
     if (p.gate == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
