@@ -504,7 +504,7 @@ template <int DK> struct LocalSmem {
 static_assert(offsetof(LocalSmem<128>, W) % 16 == 0 && offsetof(LocalSmem<64>, W) % 16 == 0,
               "float4 accesses need 16-byte offsets");
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, int GATE>
 __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, const float *Sg, const float *Gg,
                                         int64_t tok0, int L, int h) {
     // Token-level reverse steps over every value column; the state before
@@ -528,14 +528,14 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
         for (int m = 0; m < r; ++m) {
             const int64_t tk = (tok0 + m) * H + h;
             float vp = 0.f;
-            for (int c = part; c < DK; c += NP) vp += gate_at(p.alpha, p.gate, tk, c, DK) * ld_in(k, tk * DK + c) * Sb[c * DV + j];
+            for (int c = part; c < DK; c += NP) vp += gate_at(p.alpha, GATE, tk, c, DK) * ld_in(k, tk * DK + c) * Sb[c * DV + j];
             redv[part * DV + j] = vp;
             __syncthreads();
             float vh = 0.f;
             for (int p2 = 0; p2 < NP; ++p2) vh += redv[p2 * DV + j];
             const float be = p.beta[tk] * (ld_in(v, tk * DV + j) - vh);
             for (int c = part; c < DK; c += NP)
-                Sb[c * DV + j] = gate_at(p.alpha, p.gate, tk, c, DK) * Sb[c * DV + j] + ld_in(k, tk * DK + c) * be;
+                Sb[c * DV + j] = gate_at(p.alpha, GATE, tk, c, DK) * Sb[c * DV + j] + ld_in(k, tk * DK + c) * be;
             __syncthreads();
         }
         // reverse step of token r
@@ -548,7 +548,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                 const float kc = ld_in(k, tk * DK + c);
                 const float g = G[c * DV + j] + ld_in(q, tk * DK + c) * dj;
                 G[c * DV + j] = g;
-                vp += gate_at(p.alpha, p.gate, tk, c, DK) * kc * Sb[c * DV + j];
+                vp += gate_at(p.alpha, GATE, tk, c, DK) * kc * Sb[c * DV + j];
                 wp += kc * g;
             }
             redv[part * DV + j] = vp;
@@ -569,7 +569,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
         {
             // row mapping: channel c, value columns of part hp
             const int c = tid % DK, hp = tid / DK, cw = DV / NH;
-            const float ac = gate_at(p.alpha, p.gate, tk, c, DK), kc = ld_in(k, tk * DK + c);
+            const float ac = gate_at(p.alpha, GATE, tk, c, DK), kc = ld_in(k, tk * DK + c);
             float dq = 0.f, ge = 0.f, sw = 0.f, da = 0.f;
             for (int jj = hp * cw; jj < (hp + 1) * cw; ++jj) {
                 const float sv = Sb[c * DV + jj], g = G[c * DV + jj], e = ev[jj], w = wv[jj];
@@ -590,7 +590,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                     for (int u = 0; u < 4; ++u) s4[u] += redc[(h2 * 4 + u) * DK + tid];
                 p.dq[tk * DK + tid] = s4[0];
                 p.dk[tk * DK + tid] = bt * (s4[1] - s4[2]);
-                if (p.gate == KDA_GATE_CHANNEL) p.dalpha[tk * DK + tid] = s4[3];
+                if (GATE == KDA_GATE_CHANNEL) p.dalpha[tk * DK + tid] = s4[3];
                 das[tid] = s4[3];
             }
             if (tid == 0) {
@@ -599,7 +599,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
                 p.dbeta[tk] = db;
             }
             __syncthreads();
-            if (tid == 0 && p.gate == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them
+            if (tid == 0 && GATE == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them
                 float da = 0.f;
                 for (int c = 0; c < DK; ++c) da += das[c];
                 p.dalpha[tk] = da;
@@ -607,12 +607,12 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
         }
         // G = Diag(alpha)(G - beta k w^T)
         for (int c = part; c < DK; c += NP)
-            G[c * DV + j] = gate_at(p.alpha, p.gate, tk, c, DK) * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
+            G[c * DV + j] = gate_at(p.alpha, GATE, tk, c, DK) * (G[c * DV + j] - bt * ld_in(k, tk * DK + c) * wv[j]);
         __syncthreads();
     }
 }
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, int GATE>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LocalSmem<DK> &sm = *reinterpret_cast<LocalSmem<DK> *>(smem_raw);
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 
     load_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS, TAB_ALL);
     if (tb.slow) {
-        local_slow<DK, TIn>(sm, p, Sg, Gg, tok0, L, h);
+        local_slow<DK, TIn, GATE>(sm, p, Sg, Gg, tok0, L, h);
         return;
     }
     float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
-    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, p.gate, tok0, L, H, h);
+    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, GATE, tok0, L, H, h);
     tb.part[(tid / DK) * DK + tid % DK] = tb.mu[tid % DK] * tb.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid];
     float dlogp[NK][4];
@@ -827,12 +827,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int r = L - 1; r >= 0; --r) {
             run += tb.Qr[r * LDK + c];
             const int64_t th = (tok0 + r) * H + h;
-            const float da = run / gate_at(p.alpha, p.gate, th, c, DK);
-            if (p.gate == KDA_GATE_CHANNEL) p.dalpha[th * DK + c] = da;
+            const float da = run / gate_at(p.alpha, GATE, th, c, DK);
+            if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + c] = da;
             else tb.Qr[r * LDK + c] = da;  // (this thread's own column, read only by itself above)
         }
     }
-    if (p.gate == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
+    if (GATE == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
         __syncthreads();
         if (tid < L) {
             float da = 0.f;
@@ -952,7 +952,11 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (chunks == 0) return cudaSuccess;
     // 4. every chunk's gradients
-    auto local = kda_bwd_local_kernel<DK, TIn>;
+    // (the gate kind is a template parameter here: this pass runs at the
+    // register limit, where run-time branches on it cost 7 %)
+    auto local = b.gate == KDA_GATE_SCALAR ? kda_bwd_local_kernel<DK, TIn, KDA_GATE_SCALAR>
+                 : b.gate == KDA_GATE_NONE ? kda_bwd_local_kernel<DK, TIn, KDA_GATE_NONE>
+                                           : kda_bwd_local_kernel<DK, TIn, KDA_GATE_CHANNEL>;
     const size_t sl = sizeof(LocalSmem<DK>);
     if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
     local<<<chunk_ctas, NT, sl, s>>>(p);
