@@ -64,8 +64,6 @@ struct PrefillArgs {
     const int32_t *dev_status;  // nullable: skip all work when *dev_status != 0
     int stall1;                 // self-test of the tensor-core kernel's bounded waits: 1 + the
                                 // chunk at which its state chain stops (0, the default: never)
-    float *chunk_states;        // CUDA-core kernel, equal lengths only (nullable): the state
-                                // before every chunk, [N, H, ceil(T / 64), dk, dv]
 };
 
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);

@@ -83,13 +83,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
     const TIn *q = (const TIn *)a.q;
     const TIn *k = (const TIn *)a.k;
     const TIn *v = (const TIn *)a.v;
-    TIn *o = (TIn *)a.o;  // may be null when only the chunk states are wanted
+    TIn *o = (TIn *)a.o;
     bool fresh;
     const int64_t state_off = (slot_of(a.slots, n, fresh) * H + h) * DK * DV;
-    // chunk states (equal-length batches only): the state before chunk i of
-    // (sequence n, head h) at chunk_states + ((n H + h) NC + i) DK DV
-    const int64_t NCs = ((int64_t)a.T + C - 1) / C;
-    float *cst = a.chunk_states ? a.chunk_states + ((int64_t)n * H + h) * NCs * DK * DV : nullptr;
 
     // ---- initial state slice ----
     for (int e = tid; e < DK * VS; e += NT) {
@@ -104,10 +100,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
     for (int64_t t0 = 0; t0 < T; t0 += C) {
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         const int64_t tok0 = t_begin + t0;
-
-        if (cst)  // the state this chunk starts from
-            for (int e = tid; e < DK * VS; e += NT)
-                cst[(t0 / C) * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[e];
 
         // ---- gate products, factors and the gated tables ----
         simt::gate_tables<DK, TIn>(tb, a.alpha, a.gate, q, k, a.beta, tok0, L, H, h);
@@ -137,7 +129,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
                 }
                 sm.R[part * VS + j] = op;
                 __syncthreads();
-                if (tid < VS && o) {
+                if (tid < VS) {
                     float s = 0.f;
                     for (int p2 = 0; p2 < NT / VS; ++p2) s += sm.R[p2 * VS + tid];
                     o[tk * DV + v0 + tid] = from_f32<TIn>(s);
@@ -241,7 +233,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_simt_kernel(PrefillArgs a) 
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = ty + 16 * i;
-                if (r < L && o) {
+                if (r < L) {
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         o[((tok0 + r) * H + h) * DV + v0 + 4 * tx + jj] = from_f32<TIn>(y[i][jj]);
