@@ -45,6 +45,8 @@
 //          each written once (the value columns are taken 64 at a time and
 //          the sums over them accumulate in registers), so the result is
 //          deterministic.
+#include <type_traits>
+
 #include "kda_chunk_simt.cuh"
 
 namespace kda {
@@ -224,24 +226,33 @@ __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 // acc[nt] (the 16 x 8 tile at rows r0.., columns c0 + 8 nt ..) += sum_{k < K} a(r, k) b(k, c)
-template <int K, int NT8, typename FA, typename FB>
+// SPLIT = false takes one tf32 product per product (for bf16 inputs, whose
+// tolerance is that of bf16: about 1e-3 relative instead of fp32's 1e-7).
+template <int K, int NT8, bool SPLIT = true, typename FA, typename FB>
 __device__ __forceinline__ void wmm(float (&acc)[NT8][4], FA a, FB b, int r0, int c0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll 2
     for (int k = 0; k < K; k += 8) {
         uint32_t ah[4], al[4];
-        split_tf32(a(r0 + g, k + t), ah[0], al[0]);
-        split_tf32(a(r0 + g + 8, k + t), ah[1], al[1]);
-        split_tf32(a(r0 + g, k + t + 4), ah[2], al[2]);
-        split_tf32(a(r0 + g + 8, k + t + 4), ah[3], al[3]);
+        const float av[4] = {a(r0 + g, k + t), a(r0 + g + 8, k + t), a(r0 + g, k + t + 4), a(r0 + g + 8, k + t + 4)};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (SPLIT) split_tf32(av[u], ah[u], al[u]);
+            else ah[u] = tf32_bits(av[u]);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT8; ++nt) {
-            uint32_t bh0, bl0, bh1, bl1;
-            split_tf32(b(k + t, c0 + 8 * nt + g), bh0, bl0);
-            split_tf32(b(k + t + 4, c0 + 8 * nt + g), bh1, bl1);
-            mma8(acc[nt], al, bh0, bh1);
-            mma8(acc[nt], ah, bl0, bl1);
-            mma8(acc[nt], ah, bh0, bh1);
+            const float b0 = b(k + t, c0 + 8 * nt + g), b1 = b(k + t + 4, c0 + 8 * nt + g);
+            if (SPLIT) {
+                uint32_t bh0, bl0, bh1, bl1;
+                split_tf32(b0, bh0, bl0);
+                split_tf32(b1, bh1, bl1);
+                mma8(acc[nt], al, bh0, bh1);
+                mma8(acc[nt], ah, bl0, bl1);
+                mma8(acc[nt], ah, bh0, bh1);
+            } else {
+                mma8(acc[nt], ah, tf32_bits(b0), tf32_bits(b1));
+            }
         }
     }
 }
@@ -301,6 +312,7 @@ template <int DK> struct StateTile {
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, const float *s0) {
+    constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
     extern __shared__ __align__(16) unsigned char smem_raw[];
     StatesSmem<DK> &sm = *reinterpret_cast<StatesSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         float acc[4][4];
         // R = Diag(beta) (V - Kr St)
         fzero<4>(acc);
-        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
+        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.S[c * LDC + j]; }, R0, C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
             const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
@@ -366,14 +378,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         __syncthreads();
         // U = T R
         fzero<4>(acc);
-        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return sm.R[m * LDC + j]; }, R0,
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return sm.R[m * LDC + j]; }, R0,
                   C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { sm.U[r * LDC + c] = x; });
         __syncthreads();
         // S <- Diag(mu) (Diag(mu) S + Kc^T U)
         float acc2[ST::N8][4];
         fzero<ST::N8>(acc2);
-        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Kc[r * LDK + c]; }, [&](int r, int j) { return sm.U[r * LDC + j]; },
+        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Kc[r * LDK + c]; }, [&](int r, int j) { return sm.U[r * LDC + j]; },
                        SR0, SC0);
         ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
             const float m = tb.mu[c];
@@ -395,6 +407,7 @@ static_assert(offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, 
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
+    constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ChainSmem<DK> &sm = *reinterpret_cast<ChainSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
@@ -463,24 +476,24 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         float acc[4][4];
         // dU = Kc Gt + P^T dO
         fzero<4>(acc);
-        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
+        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.G[c * LDC + j]; }, R0, C0);
-        wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * LDC + j]; }, R0,
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * LDC + j]; }, R0,
                   C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = x; });
         __syncthreads();
         // dX = -Diag(beta) T^T dU (into dU's place)
         fzero<4>(acc);
-        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; }, R0, C0);
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; }, R0, C0);
         __syncthreads();
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = -tb.beta[r] * x; });
         __syncthreads();
         // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX)
         float acc2[ST::N8][4];
         fzero<ST::N8>(acc2);
-        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Qr[r * LDK + c]; },
+        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Qr[r * LDK + c]; },
                        [&](int r, int j) { return sm.dO[r * LDC + j]; }, SR0, SC0);
-        wmm<C, ST::N8>(acc2, [&](int c, int r) { return tb.Kr[r * LDK + c]; }, [&](int r, int j) { return dU[r * LDC + j]; },
+        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Kr[r * LDK + c]; }, [&](int r, int j) { return dU[r * LDC + j]; },
                        SR0, SC0);
         ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
             const float m = tb.mu[c];
@@ -614,6 +627,7 @@ __device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, c
 
 template <int DK, typename TIn, int GATE>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
+    constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LocalSmem<DK> &sm = *reinterpret_cast<LocalSmem<DK> *>(smem_raw);
     simt::Tables<DK> &tb = sm.tb;
@@ -662,7 +676,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
         }
         fzero<4>(acc);
-        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
+        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
             const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
             WB[r * LDC + c] = vv - x;
@@ -680,21 +694,21 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         __syncthreads();
         // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
         fzero<4>(acc);
-        wmm<C, 4>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; },
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; },
                   [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
         store(acc, WC);
         fzero<4>(acc);
-        wmm<DK, 4>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
-        wmm<C, 4>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0,
+        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0,
                   C0);
         store(acc, WA);
         __syncthreads();
         // dT += dU R^T; dR = T^T dU: dV, dbeta's first part, then dX
-        wmm<VS, 4>(dT, [&](int r, int j) { return WA[r * LDC + j]; },
+        wmm<VS, 4, SPLIT>(dT, [&](int r, int j) { return WA[r * LDC + j]; },
                    [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
         float dR[4][4];
         fzero<4>(dR);
-        wmm<C, 4>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0,
+        wmm<C, 4, SPLIT>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0,
                   C0);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -708,11 +722,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         ffor<4>(dR, R0, C0, [&](int r, int c, float &x) { WB[r * LDC + c] = -tb.beta[r] * x; });  // dX
         __syncthreads();
         // dP += dO U^T; dKc += U Gt^T; dQr += dO St^T; dKr += dX St^T
-        wmm<VS, 4>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0,
+        wmm<VS, 4, SPLIT>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0,
                    C0);
-        wmm<VS, NK>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
-        wmm<VS, NK>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
-        wmm<VS, NK>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+        wmm<VS, NK, SPLIT>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
+        wmm<VS, NK, SPLIT>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
+        wmm<VS, NK, SPLIT>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
         __syncthreads();  // the work tiles are reused by the next slice
     }
     // the first parts of d log mu's column sums: Kc (U Gt^T), Qr (dO St^T), Kr (dX St^T)
@@ -729,15 +743,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     store(dT, WA);
     __syncthreads();
     // dQr += dP Kc;  dKc += dP^T Qr
-    wmm<C, NK>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0, CK);
-    wmm<C, NK>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int c) { return tb.Qr[m * LDK + c]; }, R0, CK);
+    wmm<C, NK, SPLIT>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0, CK);
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int c) { return tb.Qr[m * LDK + c]; }, R0, CK);
     // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
     fzero<4>(acc);
-    wmm<C, 4>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; }, R0, C0);
+    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; }, R0, C0);
     store(acc, WD);
     __syncthreads();
     fzero<4>(acc);
-    wmm<C, 4>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; }, R0, C0);
+    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; }, R0, C0);
     __syncthreads();  // every read of dT in WA is done
     ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { WA[r * LDC + c] = c < r ? -x : 0.f; });
     __syncthreads();
@@ -745,7 +759,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     {
         float tmp[NK][4];
         fzero<NK>(tmp);
-        wmm<C, NK>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0,
+        wmm<C, NK, SPLIT>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0,
                    CK);
         float d2[2] = {0.f, 0.f};
 #pragma unroll
@@ -759,7 +773,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) db[u] += d2[u];
     }
-    wmm<C, NK>(dKc, [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
                [&](int m, int c) { return tb.Kr[m * LDK + c]; }, R0, CK);
     // dbeta: sums over this warp's columns (the 4 lanes of a row), then the two
     // column halves of each row in a fixed order
