@@ -356,10 +356,12 @@ kda_status_t kda_device_errors(int *errors, int reset);
  *                  its chunk tables (about 129 KB for d_k = 128). Calls sharing
  *                  a workspace must not overlap.
  *
- * Every gradient is float32 whatever qkv_dtype is, and computed with fp32
- * accuracy (CUDA cores, and tensor-core products with every operand split
- * into two tf32 parts). Each gradient element is written once by one thread,
- * so two calls on the same inputs give the same bits. Errors as for
+ * Every gradient is float32 whatever qkv_dtype is. With float32 inputs the
+ * arithmetic has fp32 accuracy (CUDA cores, and tensor-core products with
+ * every operand split into two tf32 parts); with bfloat16 inputs the
+ * tensor-core products are single tf32 products (about 1e-3 relative, well
+ * inside the bf16 tolerance). Each gradient element is written once by one
+ * thread, so two calls on the same inputs give the same bits. Errors as for
  * kda_prefill; a missing or short workspace returns KDA_ERR_WORKSPACE before
  * anything runs.
  */
