@@ -152,8 +152,8 @@ __device__ void gate_factor_table(Tables<DK> &tb, float *E2, int ld, const float
 }
 
 // A = beta (Kr Kc^T) strictly lower, P = Qr Kc^T lower incl. diagonal, then
-// T = (I + A)^{-1} one row at a time (forward substitution). Ends with a
-// barrier.
+// T = (I + A)^{-1} (forward substitution on 16 x 16 blocks, then block
+// products). Leaves A's upper triangle overwritten. Ends with a barrier.
 template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
     constexpr int LDK = Tables<DK>::LDK, LDC = Tables<DK>::LDC;
     const int tid = threadIdx.x;
@@ -190,17 +190,67 @@ template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
             }
     }
     __syncthreads();
+    // T = (I + A)^{-1} by blocks of 16 (A strictly lower, so T is unit lower):
+    //   the four diagonal blocks by forward substitution, one thread per column;
+    //   then T_{b+1,b} = -T_{b+1,b+1} A_{b+1,b} T_{b,b} for the pairs (0,1), (2,3);
+    //   then T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]).
+    // The products in between sit in A's upper triangle, which is zero and
+    // unread: A[0:16, 16:32] and A[32:48, 48:64] for the pairs, A[0:32, 32:64]
+    // for the 32 x 32 block.
+    for (int e = tid; e < C * C; e += NT) tb.T[(e / C) * LDC + e % C] = 0.f;
+    __syncthreads();
+    if (tid < C) {
+        const int bk = tid >> 4, col = tid & 15, o = 16 * bk;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = i == col ? 1.f : 0.f;
+#pragma unroll
+        for (int sidx = 0; sidx < 15; ++sidx)
+#pragma unroll
+            for (int r = sidx + 1; r < 16; ++r) x[r] -= tb.A[(o + r) * LDC + o + sidx] * x[sidx];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tb.T[(o + r) * LDC + o + col] = x[r];
+    }
+    __syncthreads();
     {
-        const int j = tid / 4, part = tid % 4;  // column j, 4-way split of the sum
-        for (int r = 0; r < C; ++r) {
-            float s = 0.f;
-            if (j < r)
-                for (int sidx = j + part; sidx < r; sidx += 4) s += tb.A[r * LDC + sidx] * tb.T[sidx * LDC + j];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (part == 0) tb.T[r * LDC + j] = j < r ? -s : (j == r ? 1.f : 0.f);
-            __syncthreads();
+        // M = A_{b+1,b} T_{b,b} for both pairs: 2 x 256 entries, two per thread
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + NT * u, pr = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * pr;
+            float m = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) m += tb.A[(o + 16 + r) * LDC + o + kk] * tb.T[(o + kk) * LDC + o + c];
+            tb.A[(o + r) * LDC + o + 16 + c] = m;
         }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + NT * u, pr = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * pr;
+            float m = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) m += tb.T[(o + 16 + r) * LDC + o + 16 + kk] * tb.A[(o + kk) * LDC + o + 16 + c];
+            tb.T[(o + 16 + r) * LDC + o + c] = -m;
+        }
+        __syncthreads();
+        // M2 = A[32:64, 0:32] T[0:32, 0:32]: 1024 entries, four per thread
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + NT * u, r = e >> 5, c = e & 31;
+            float m = 0.f;
+#pragma unroll 8
+            for (int kk = 0; kk < 32; ++kk) m += tb.A[(32 + r) * LDC + kk] * tb.T[kk * LDC + c];
+            tb.A[r * LDC + 32 + c] = m;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + NT * u, r = e >> 5, c = e & 31;
+            float m = 0.f;
+#pragma unroll 8
+            for (int kk = 0; kk < 32; ++kk) m += tb.T[(32 + r) * LDC + 32 + kk] * tb.A[kk * LDC + 32 + c];
+            tb.T[(32 + r) * LDC + c] = -m;
+        }
+        __syncthreads();
     }
 }
 
