@@ -327,8 +327,8 @@ def bench_backward(kda, W, dev, stream, peaks, steps, warmup):
     res = {"workload": f"kda_prefill_backward B={Bb} H={Hb} T={Tb} d_k={DK} d_v={DV}, bf16 q/k/v/d_o, fp32 gradients",
            "value": Bb * Tb / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
            "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
-           "kernels": "kda_bwd_tables + kda_bwd_states + kda_bwd_chain + kda_bwd_local (fp32 accuracy; "
-                      "products on the tensor cores as split tf32)",
+           "kernels": "kda_bwd_tables + kda_bwd_states + kda_bwd_chain + kda_bwd_local (fp32 arithmetic; "
+                      "products on the tensor cores as single tf32 products for bf16 inputs)",
            "workspace_bytes": ws.numel()}
     del q, k, v, a, b, d_o, ws
     return res

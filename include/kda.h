@@ -352,8 +352,9 @@ kda_status_t kda_device_errors(int *errors, int reset);
  *   workspace      device scratch of kda_prefill_backward_workspace_bytes(...)
  *                  bytes, 16-byte aligned, owned by the caller: for every
  *                  64-token chunk of every sequence and head, the state before
- *                  it, the state gradient after it (4 d_k d_v bytes each) and
- *                  its chunk tables (about 129 KB for d_k = 128). Calls sharing
+ *                  it, the state gradient after it (4 d_k d_v bytes each), its
+ *                  chunk tables (about 129 KB for d_k = 128) and four 64 x d_v
+ *                  fp32 work tiles (1 KB per value column). Calls sharing
  *                  a workspace must not overlap.
  *
  * Every gradient is float32 whatever qkv_dtype is. With float32 inputs the

@@ -35,16 +35,20 @@
 //          chunk's gate products and WY tables (Kr, Qr, Kc, T, P, mu, beta)
 //          into the workspace, so no serial pass rebuilds them;
 //   states one CTA per (sequence, head, 64-column value slice): the forward
-//          state chain, writing the state before every chunk;
+//          state chain, writing the state before every chunk and the chunk's
+//          U and V - X;
 //   chain  one CTA per (sequence, head, 64-column value slice), chunks in
-//          reverse: writes dL/dS after every chunk into the workspace and the
-//          initial state's gradient;
-//   local  one CTA per (sequence, head, chunk), all chunks at once, the
-//          products on the tensor cores (mma.sync tf32 with a hi/lo split:
-//          fp32 accuracy): dv, dq, dk, dalpha, dbeta of the chunk's tokens,
-//          each written once (the value columns are taken 64 at a time and
-//          the sums over them accumulate in registers), so the result is
+//          reverse: writes dL/dS after every chunk, the chunk's dU and dR,
+//          dv, and the initial state's gradient (it needs no forward state,
+//          so it does not wait for the states pass's results);
+//   local  one CTA per (sequence, head, chunk), all chunks at once: dq, dk,
+//          dalpha, dbeta of the chunk's tokens from the chunk's tables, its
+//          states and the four work tiles, each written once (the value
+//          columns are taken 32 at a time, double-buffered in shared memory,
+//          and the sums over them accumulate in registers), so the result is
 //          deterministic.
+// The products run on the tensor cores (mma.sync tf32; with a hi/lo split of
+// every operand for fp32 inputs: fp32 accuracy).
 #include <type_traits>
 
 #include "kda_chunk_simt.cuh"
@@ -66,6 +70,7 @@ struct BwdParams {
     float *states;        // [N, H, NC, DK, DV]: the state before every chunk
     float *gnext;         // [N, H, NC, DK, DV]: dL/dS after every chunk
     float *tabs;          // [N, H, NC, TabLayout<DK>::FLOATS]: every chunk's tables
+    float *work;          // [N, H, NC, 4, C, DV]: U and V - X (states pass), dU and dR (chain pass)
     int gate;             // kda_gate_t: dalpha per channel, per token-head, or none
     int N, T, H, DV, NC;  // T, NC: tokens and chunks of every sequence (equal lengths)
     const int32_t *cu;    // nullable: sequences packed by cu_seqlens [N + 1] (T is then T_total)
@@ -268,6 +273,18 @@ template <int NT8, typename F> __device__ __forceinline__ void ffor(float (&acc)
 #pragma unroll
         for (int e = 0; e < 4; ++e) f(r0 + g + 8 * (e >> 1), c0 + 8 * nt + 2 * t + (e & 1), acc[nt][e]);
 }
+// The tile at (r0, c0) into row-major global memory of row stride ld, two
+// columns per store.
+template <int NT8>
+__device__ __forceinline__ void gstore(const float (&acc)[NT8][4], int r0, int c0, float *dst, int64_t ld) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+        const int c = c0 + 8 * nt + 2 * t;
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + g) * ld + c) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + g + 8) * ld + c) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+}
 
 // ---------------------------------------------------------------- tables
 // One CTA per (sequence, head, chunk): the chunk's tables into the workspace.
@@ -290,9 +307,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
 // ---------------------------------------------------------------- states
 // The forward chain only: one CTA per (sequence, head, value slice) writes the
 // state before every chunk (S_{n+1} = Diag(mu) (Diag(mu) S_n + Kc^T U), U =
-// T Diag(beta) (V - Kr Diag(mu) S_n)), reading the chunk's tables; slow
-// chunks go token by token (the §四 update). Products on the tensor cores
-// (wmm: fp32 accuracy).
+// T Diag(beta) (V - Kr Diag(mu) S_n)) and the chunk's U and V - X, reading the
+// chunk's tables; slow chunks go token by token (the §四 update) and write no
+// U or V - X. Products on the tensor cores (wmm).
 template <int DK> struct StatesSmem {
     float S[DK * LDC];  // the state slice, rows of LDC
     simt::Tables<DK> tb;
@@ -333,6 +350,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     int64_t wbase, wstride;
     slots_of(p, n, h, cbase, wbase, wstride);
     float *st = p.states + wbase * DK * DV;                    // chunk i at slot wbase + i wstride
+    float *wkb = p.work + wbase * 4 * C * DV;
     const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
@@ -366,21 +384,25 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
             }
             continue;
         }
+        float *wk = wkb + ci * wstride * 4 * C * DV + v0;  // this chunk's U, V - X (the slice's columns)
         float acc[4][4];
-        // R = Diag(beta) (V - Kr St)
+        // R = Diag(beta) (V - Kr St); V - X into the workspace
         fzero<4>(acc);
         wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.S[c * LDC + j]; }, R0, C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
             const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
-            sm.R[r * LDC + c] = tb.beta[r] * (vv - x);
+            x = vv - x;
+            sm.R[r * LDC + c] = tb.beta[r] * x;
         });
+        gstore<4>(acc, R0, C0, wk + C * DV, DV);
         __syncthreads();
-        // U = T R
+        // U = T R, also into the workspace
         fzero<4>(acc);
         wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return sm.R[m * LDC + j]; }, R0,
                   C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { sm.U[r * LDC + c] = x; });
+        gstore<4>(acc, R0, C0, wk, DV);
         __syncthreads();
         // S <- Diag(mu) (Diag(mu) S + Kc^T U)
         float acc2[ST::N8][4];
@@ -428,6 +450,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     int64_t wbase, wstride;
     slots_of(p, n, h, cbase, wbase, wstride);
     float *gn = p.gnext + wbase * DK * DV;                     // chunk i at slot wbase + i wstride
+    float *wkb = p.work + wbase * 4 * C * DV;
     const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
@@ -473,20 +496,26 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
             continue;
         }
         float *dU = tb.A;  // a work tile here
+        float *wk = wkb + ci * wstride * 4 * C * DV + v0;  // this chunk's dU, dR (the slice's columns)
         float acc[4][4];
-        // dU = Kc Gt + P^T dO
+        // dU = Kc Gt + P^T dO, also into the workspace
         fzero<4>(acc);
         wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.G[c * LDC + j]; }, R0, C0);
         wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * LDC + j]; }, R0,
                   C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = x; });
+        gstore<4>(acc, R0, C0, wk + 2 * C * DV, DV);
         __syncthreads();
-        // dX = -Diag(beta) T^T dU (into dU's place)
+        // dR = T^T dU into the workspace; dv = Diag(beta) dR; dX = -Diag(beta) dR (into dU's place)
         fzero<4>(acc);
         wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; }, R0, C0);
+        gstore<4>(acc, R0, C0, wk + 3 * C * DV, DV);
         __syncthreads();
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = -tb.beta[r] * x; });
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
+            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = tb.beta[r] * x;
+            dU[r * LDC + c] = -tb.beta[r] * x;
+        });
         __syncthreads();
         // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX)
         float acc2[ST::N8][4];
@@ -508,30 +537,117 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- local
-template <int DK> struct LocalSmem {
-    simt::Tables<DK> tb;
-    float W[3][C * LDC];       // work tiles; tb.A is the fourth
-    float red[8 * DK + 2 * C];  // column sums by row block; dbeta row sums by column half
+constexpr int VP = 32;       // value columns per piece of the local pass
+constexpr int LDP = VP + 4;  // padded row of a piece tile (fp32): conflict-free fragments
+// padded row of the dO tile (elements): 16-byte rows, conflict-free fragments
+template <typename TIn> struct DoRow { static constexpr int LD = sizeof(TIn) == 4 ? LDP : VP + 8; };
+
+// One piece of value columns [v0, v0 + VP) of everything the local pass sums
+// over the value columns.
+template <int DK, typename TIn> struct LocalPiece {
+    float S[DK * LDP];  // the state before the chunk (rows: key channels)
+    float G[DK * LDP];  // dL/dS after the chunk
+    float U[C * LDP];
+    float VmX[C * LDP];  // V - X
+    float dU[C * LDP];
+    float dR[C * LDP];
+    TIn dO[C * DoRow<TIn>::LD];
+};
+// What the last part of the local pass reads, in the pieces' place.
+template <int DK> struct LocalFinal {
+    float Kr[C * (DK + 4)];
+    float Qr[C * (DK + 4)];
+    float W[4][C * LDC];  // work tiles
+};
+// The token path's buffers (local_slow), in the pieces' place.
+template <int DK> constexpr int slow_floats() { return 2 * DK * 128 + 2 * NT + 2 * 128 + 4 * NT + DK; }
+
+template <int DK, typename TIn> struct LocalSmem {
+    union Front {
+        LocalPiece<DK, TIn> piece[2];  // double-buffered pieces
+        LocalFinal<DK> fin;
+        float slow[slow_floats<DK>()];
+    } u;
+    float Kc[C * (DK + 4)];
+    float T[C * LDC];
+    float mu[DK];
+    float beta[C];
+    float part[(NT / DK) * DK];
+    float red[8 * DK + 3 * C];  // column sums by row block; dbeta parts by row
 };
 
-static_assert(offsetof(LocalSmem<128>, W) % 16 == 0 && offsetof(LocalSmem<64>, W) % 16 == 0,
-              "float4 accesses need 16-byte offsets");
+// 16-byte tiles and offsets (cp.async and float4 accesses)
+template <int DK, typename TIn> constexpr bool local_layout_ok() {
+    using P = LocalPiece<DK, TIn>;
+    using S = LocalSmem<DK, TIn>;
+    return sizeof(P) % 16 == 0 && offsetof(P, dO) % 16 == 0 && offsetof(P, U) % 16 == 0 && offsetof(S, Kc) % 16 == 0 &&
+           offsetof(S, T) % 16 == 0 && offsetof(S, mu) % 16 == 0 && offsetof(S, beta) % 16 == 0 &&
+           offsetof(LocalFinal<DK>, Qr) % 16 == 0 && offsetof(LocalFinal<DK>, W) % 16 == 0;
+}
+static_assert(local_layout_ok<128, float>() && local_layout_ok<128, __nv_bfloat16>() && local_layout_ok<64, float>() &&
+                  local_layout_ok<64, __nv_bfloat16>(),
+              "16-byte tiles and offsets");
 
+// 16 bytes global -> shared, or 16 zero bytes when n = 0 (src is then not read).
+__device__ __forceinline__ void cp16z(void *dst, const void *src, uint32_t n) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
+                 "r"(n)
+                 : "memory");
+}
+
+// tf32 operands of one m16n8k8 step (hi, and lo when split).
+struct BFrag {
+    uint32_t h0, h1, l0, l1;
+};
+template <bool SPLIT> __device__ __forceinline__ BFrag bfrag(float b0, float b1) {
+    BFrag f;
+    if (SPLIT) {
+        split_tf32(b0, f.h0, f.l0);
+        split_tf32(b1, f.h1, f.l1);
+    } else {
+        f.h0 = tf32_bits(b0);
+        f.h1 = tf32_bits(b1);
+        f.l0 = f.l1 = 0u;
+    }
+    return f;
+}
+// A fragment of the 16 x 8 block at rows r0.., columns k.. of a row-major tile.
+template <bool SPLIT, typename TS>
+__device__ __forceinline__ void afrag(const TS *x, int ld, int r0, int k, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float v[4] = {to_f32(x[(r0 + g) * ld + k + t]), to_f32(x[(r0 + g + 8) * ld + k + t]),
+                        to_f32(x[(r0 + g) * ld + k + t + 4]), to_f32(x[(r0 + g + 8) * ld + k + t + 4])};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (SPLIT) split_tf32(v[u], hi[u], lo[u]);
+        else hi[u] = tf32_bits(v[u]), lo[u] = 0u;
+    }
+}
+template <bool SPLIT>
+__device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const BFrag &b) {
+    if (SPLIT) {
+        mma8(d, al, b.h0, b.h1);
+        mma8(d, ah, b.l0, b.l1);
+    }
+    mma8(d, ah, b.h0, b.h1);
+}
+
+// The local pass of a chunk that the forward runs token by token (a channel
+// decays past e^-80), in `buf` (slow_floats<DK>() floats of shared memory).
 template <int DK, typename TIn, int GATE>
-__device__ __noinline__ void local_slow(LocalSmem<DK> &sm, const BwdParams &p, const float *Sg, const float *Gg,
-                                        int64_t tok0, int L, int h) {
+__device__ __noinline__ void local_slow(float *buf, const BwdParams &p, const float *Sg, const float *Gg, int64_t tok0,
+                                        int L, int h) {
     // Token-level reverse steps over every value column; the state before
     // token r is replayed from the chunk's start state for every r (the chunk
-    // is rare: this is written for size). Buffers: the state in Kr..Qr, G in
-    // Kc..P, vectors in W.
+    // is rare: this is written for size).
     const int H = p.H, DV = p.DV, tid = threadIdx.x;
     const int NP = NT / DV;      // key-row parts of the column mapping
     constexpr int NH = NT / DK;  // column parts of the row mapping
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
-    float *Sb = sm.tb.Kr, *G = sm.tb.Kc;
-    float *redv = sm.W[0], *redw = sm.W[0] + NP * DV, *ev = sm.W[0] + 2 * NP * DV, *wv = ev + DV;
-    float *redc = sm.W[1];                    // [NH][4][DK]
-    float *das = sm.W[1] + 4 * NH * DK;       // [DK]: a token's dalpha by channel
+    float *Sb = buf, *G = buf + DK * DV;
+    float *redv = G + DK * DV, *redw = redv + NP * DV, *ev = redw + NP * DV, *wv = ev + DV;
+    float *redc = wv + DV;          // [NH][4][DK]
+    float *das = redc + 4 * NH * DK;  // [DK]: a token's dalpha by channel
     const int j = tid % DV, part = tid / DV;
     for (int e = tid; e < DK * DV; e += NT) G[e] = Gg[e];
     for (int r = L - 1; r >= 0; --r) {
@@ -629,10 +745,11 @@ template <int DK, typename TIn, int GATE>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    LocalSmem<DK> &sm = *reinterpret_cast<LocalSmem<DK> *>(smem_raw);
-    simt::Tables<DK> &tb = sm.tb;
-    constexpr int LDK = simt::Tables<DK>::LDK;
+    LocalSmem<DK, TIn> &sm = *reinterpret_cast<LocalSmem<DK, TIn> *>(smem_raw);
+    using TL = TabLayout<DK>;
+    constexpr int LDK = DK + 4;
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
+    constexpr int DLD = DoRow<TIn>::LD;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const int64_t idx = blockIdx.x;  // the chunk's workspace slot
     int64_t c;
@@ -641,142 +758,205 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     cta_chunk(p, idx, c, h);
     const int H = p.H, DV = p.DV;
     if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
-    const TIn *v = (const TIn *)p.v, *dO = (const TIn *)p.d_o;
+    const TIn *dO = (const TIn *)p.d_o;
     const float *Sg = p.states + idx * DK * DV, *Gg = p.gnext + idx * DK * DV;
-
-    load_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS, TAB_ALL);
-    if (tb.slow) {
-        local_slow<DK, TIn, GATE>(sm, p, Sg, Gg, tok0, L, h);
+    const float *tab = p.tabs + idx * TL::FLOATS;
+    const float *wk = p.work + idx * 4 * C * DV;  // U, V - X, dU, dR: [4][C][DV]
+    if (__float_as_int(tab[TL::SLOW])) {
+        local_slow<DK, TIn, GATE>(sm.u.slow, p, Sg, Gg, tok0, L, h);
         return;
     }
-    float *WA = tb.A, *WB = sm.W[0], *WC = sm.W[1], *WD = sm.W[2];
+    // Kr and Qr are read last, into the pieces' place: pull them into L2 now
+    for (int l = tid; l < 2 * C * DK / 32; l += NT) asm volatile("prefetch.global.L2 [%0];" ::"l"(tab + TL::KR + 32 * l));
+    // Kc, T, mu, beta, then the first piece
+    for (int e = tid; e < C * DK / 4; e += NT) {
+        const int r = e / (DK / 4), cc = 4 * (e % (DK / 4));
+        cp16(&sm.Kc[r * LDK + cc], tab + TL::KC + r * DK + cc);
+    }
+    for (int e = tid; e < C * C / 4; e += NT) {
+        const int r = e / (C / 4), cc = 4 * (e % (C / 4));
+        cp16(&sm.T[r * LDC + cc], tab + TL::T + r * C + cc);
+    }
+    for (int e = tid; e < DK / 4; e += NT) cp16(&sm.mu[4 * e], tab + TL::MU + 4 * e);
+    for (int e = tid; e < C / 4; e += NT) cp16(&sm.beta[4 * e], tab + TL::BETA + 4 * e);
+    auto load_piece = [&](int v0, LocalPiece<DK, TIn> &P) {
+        constexpr int Q = VP / 4;  // 16-byte pieces of a fp32 row
+        for (int e = tid; e < DK * Q; e += NT) {
+            const int r = e / Q, cc = 4 * (e % Q);
+            cp16(&P.S[r * LDP + cc], Sg + (int64_t)r * DV + v0 + cc);
+            cp16(&P.G[r * LDP + cc], Gg + (int64_t)r * DV + v0 + cc);
+        }
+        for (int e = tid; e < C * Q; e += NT) {
+            const int r = e / Q, cc = 4 * (e % Q);
+            const float *src = wk + (int64_t)r * DV + v0 + cc;
+            cp16(&P.U[r * LDP + cc], src);
+            cp16(&P.VmX[r * LDP + cc], src + C * DV);
+            cp16(&P.dU[r * LDP + cc], src + 2 * C * DV);
+            cp16(&P.dR[r * LDP + cc], src + 3 * C * DV);
+        }
+        constexpr int EO = 16 / (int)sizeof(TIn), QO = VP / EO;  // elements per 16 bytes; 16-byte pieces of a row
+        for (int e = tid; e < C * QO; e += NT) {
+            const int r = e / QO, cc = EO * (e % QO);
+            const TIn *src = dO + ((tok0 + (r < L ? r : 0)) * H + h) * DV + v0 + cc;
+            cp16z(&P.dO[r * DLD + cc], src, r < L ? 16u : 0u);  // rows past the sequence: zeros
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_piece(0, sm.u.piece[0]);
+
     // warp tile: rows R0 .. R0 + 15; columns C0 .. C0 + 31 of a 64-wide product,
     // CK .. CK + DK/2 - 1 of a DK-wide one
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2), CK = (DK / 2) * (warp >> 2);
-    auto store = [&](float (&acc)[4][4], float *W) { ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { W[r * LDC + c] = x; }); };
-    float *dbr = sm.red + 8 * DK;  // [2][C] row sums of dbeta by column half
-    float acc[4][4];
-    // Accumulated over the value slices (every one of these is a sum over value columns):
-    float dT[4][4], dP[4][4];                      // dU R^T, dO U^T
-    float dKc[NK][4], dQr[NK][4], dKr[NK][4];      // U Gt^T, dO St^T, dX St^T so far
-    float db[2] = {0.f, 0.f};                      // sum_v dR (V - X) of rows R0 + g, R0 + g + 8
-    float s0 = 0.f;                                // sum_v St Gt of channel tid % DK (part tid / DK)
+    // Sums over the value columns, accumulated piece by piece (the diagonal
+    // factors that do not depend on the column are applied after the loop):
+    float dT[4][4], dP[4][4];                  // dU (V - X)^T, dO U^T
+    float dKc[NK][4], dQr[NK][4], dKr[NK][4];  // U G^T, dO S^T, dR S^T
+    float db1 = 0.f;                           // sum_v dR (V - X) of row tid / 4 (a quarter of the columns)
+    float s0 = 0.f;                            // sum_v S G of channel tid % DK (part tid / DK)
     fzero<4>(dT);
     fzero<4>(dP);
     fzero<NK>(dKc);
     fzero<NK>(dQr);
     fzero<NK>(dKr);
-
-    for (int v0 = 0; v0 < DV; v0 += VS) {
-        auto St = [&](int c, int j) { return tb.mu[c] * Sg[(int64_t)c * DV + v0 + j]; };
-        auto Gt = [&](int c, int j) { return tb.mu[c] * Gg[(int64_t)c * DV + v0 + j]; };
-        // dO -> WD; V - Kr St -> WB
-        for (int e = tid; e < C * VS; e += NT) {
-            const int r = e / VS;
-            WD[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
+    const int npieces = DV / VP;
+    for (int it = 0; it < npieces; ++it) {
+        if (it + 1 < npieces) {
+            load_piece((it + 1) * VP, sm.u.piece[(it + 1) & 1]);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
-        fzero<4>(acc);
-        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; }, St, R0, C0);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
-            WB[r * LDC + c] = vv - x;
-        });
+        __syncthreads();
+        const LocalPiece<DK, TIn> &P = sm.u.piece[it & 1];
+#pragma unroll 1
+        for (int k = 0; k < VP; k += 8) {
+            uint32_t oh[4], ol[4], rh[4], rl[4], uh[4], ul[4], dh[4], dl[4];
+            afrag<SPLIT>(P.dO, DLD, R0, k, oh, ol);
+            afrag<SPLIT>(P.dR, LDP, R0, k, rh, rl);
+            afrag<SPLIT>(P.U, LDP, R0, k, uh, ul);
+            afrag<SPLIT>(P.dU, LDP, R0, k, dh, dl);
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt) {
+                const int o = (CK + 8 * nt + g) * LDP + k + t4;
+                const BFrag bs = bfrag<SPLIT>(P.S[o], P.S[o + 4]);
+                const BFrag bg = bfrag<SPLIT>(P.G[o], P.G[o + 4]);
+                mma_f<SPLIT>(dQr[nt], oh, ol, bs);
+                mma_f<SPLIT>(dKr[nt], rh, rl, bs);
+                mma_f<SPLIT>(dKc[nt], uh, ul, bg);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int o = (C0 + 8 * nt + g) * LDP + k + t4;
+                const BFrag bu = bfrag<SPLIT>(P.U[o], P.U[o + 4]);
+                const BFrag bv = bfrag<SPLIT>(P.VmX[o], P.VmX[o + 4]);
+                mma_f<SPLIT>(dP[nt], oh, ol, bu);
+                mma_f<SPLIT>(dT[nt], dh, dl, bv);
+            }
+        }
         {
-            constexpr int NH = NT / DK, CW = VS / NH;
-            const int c = tid % DK, hp = tid / DK;
-            const float *sr = Sg + (int64_t)c * DV + v0 + hp * CW, *gr = Gg + (int64_t)c * DV + v0 + hp * CW;
+            constexpr int NH = NT / DK, CW = VP / NH;
+            const int cc = tid % DK, hp = tid / DK;
 #pragma unroll
             for (int j = 0; j < CW; j += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(sr + j), g4 = *reinterpret_cast<const float4 *>(gr + j);
+                const float4 a4 = *reinterpret_cast<const float4 *>(&P.S[cc * LDP + hp * CW + j]);
+                const float4 g4 = *reinterpret_cast<const float4 *>(&P.G[cc * LDP + hp * CW + j]);
                 s0 += a4.x * g4.x + a4.y * g4.y + a4.z * g4.z + a4.w * g4.w;
             }
-        }
-        __syncthreads();
-        // U = T Diag(beta) (V - X) -> WC;  dU = Kc Gt + P^T dO -> WA
-        fzero<4>(acc);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; },
-                  [&](int m, int j) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
-        store(acc, WC);
-        fzero<4>(acc);
-        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; }, Gt, R0, C0);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return WD[m * LDC + j]; }, R0,
-                  C0);
-        store(acc, WA);
-        __syncthreads();
-        // dT += dU R^T; dR = T^T dU: dV, dbeta's first part, then dX
-        wmm<VS, 4, SPLIT>(dT, [&](int r, int j) { return WA[r * LDC + j]; },
-                   [&](int j, int m) { return tb.beta[m] * WB[m * LDC + j]; }, R0, C0);
-        float dR[4][4];
-        fzero<4>(dR);
-        wmm<C, 4, SPLIT>(dR, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return WA[m * LDC + j]; }, R0,
-                  C0);
+            const int r = tid >> 2, j0 = (VP / 4) * (tid & 3);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), c = C0 + 8 * nt + 2 * t4 + (e & 1);
-                db[e >> 1] += dR[nt][e] * WB[r * LDC + c];
-                if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = tb.beta[r] * dR[nt][e];
+            for (int j = 0; j < VP / 4; j += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&P.dR[r * LDP + j0 + j]);
+                const float4 e4 = *reinterpret_cast<const float4 *>(&P.VmX[r * LDP + j0 + j]);
+                db1 += a4.x * e4.x + a4.y * e4.y + a4.z * e4.z + a4.w * e4.w;
             }
-        __syncthreads();
-        ffor<4>(dR, R0, C0, [&](int r, int c, float &x) { WB[r * LDC + c] = -tb.beta[r] * x; });  // dX
-        __syncthreads();
-        // dP += dO U^T; dKc += U Gt^T; dQr += dO St^T; dKr += dX St^T
-        wmm<VS, 4, SPLIT>(dP, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int m) { return WC[m * LDC + j]; }, R0,
-                   C0);
-        wmm<VS, NK, SPLIT>(dKc, [&](int r, int j) { return WC[r * LDC + j]; }, [&](int j, int c) { return Gt(c, j); }, R0, CK);
-        wmm<VS, NK, SPLIT>(dQr, [&](int r, int j) { return WD[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
-        wmm<VS, NK, SPLIT>(dKr, [&](int r, int j) { return WB[r * LDC + j]; }, [&](int j, int c) { return St(c, j); }, R0, CK);
-        __syncthreads();  // the work tiles are reused by the next slice
+        }
+        __syncthreads();  // this piece's buffer is refilled two pieces on
     }
+    // Kr, Qr into the pieces' place; meanwhile the column and row factors:
+    // dQr = dO St^T, dKr = dX St^T (dX = -Diag(beta) dR), dKc = U Gt^T with
+    // St = Diag(mu) S, Gt = Diag(mu) G; dT = dU R^T with R = Diag(beta) (V - X)
+    LocalFinal<DK> &F = sm.u.fin;
+    for (int e = tid; e < C * DK / 4; e += NT) {
+        const int r = e / (DK / 4), cc = 4 * (e % (DK / 4));
+        cp16(&F.Kr[r * LDK + cc], tab + TL::KR + r * DK + cc);
+        cp16(&F.Qr[r * LDK + cc], tab + TL::QR + r * DK + cc);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll
+    for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1);
+            const float m = sm.mu[cc];
+            dQr[nt][e] *= m;
+            dKc[nt][e] *= m;
+            dKr[nt][e] *= -sm.beta[r] * m;
+        }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dT[nt][e] *= sm.beta[C0 + 8 * nt + 2 * t4 + (e & 1)];
+    db1 += __shfl_xor_sync(0xffffffffu, db1, 1);
+    db1 += __shfl_xor_sync(0xffffffffu, db1, 2);
+    float *dbr = sm.red + 8 * DK;  // [3][C]: dbeta's second part by column half, its first part
+    if ((tid & 3) == 0) dbr[2 * C + (tid >> 2)] = db1;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    float *WA = F.W[0], *WC = F.W[2], *WD = F.W[3];
+    auto store = [&](float (&acc)[4][4], float *W) { ffor<4>(acc, R0, C0, [&](int r, int cc, float &x) { W[r * LDC + cc] = x; }); };
+    float acc[4][4];
+    float db[2] = {0.f, 0.f};  // dbeta's second part, rows R0 + g, R0 + g + 8
     // the first parts of d log mu's column sums: Kc (U Gt^T), Qr (dO St^T), Kr (dX St^T)
     float s123[NK][2];
 #pragma unroll
     for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int c = CK + 8 * nt + 2 * t4 + u, a0 = (R0 + g) * LDK + c, a1 = (R0 + g + 8) * LDK + c;
-            s123[nt][u] = tb.Kc[a0] * dKc[nt][u] + tb.Kc[a1] * dKc[nt][2 + u] + tb.Qr[a0] * dQr[nt][u] +
-                          tb.Qr[a1] * dQr[nt][2 + u] + tb.Kr[a0] * dKr[nt][u] + tb.Kr[a1] * dKr[nt][2 + u];
+            const int cc = CK + 8 * nt + 2 * t4 + u, a0 = (R0 + g) * LDK + cc, a1 = (R0 + g + 8) * LDK + cc;
+            s123[nt][u] = sm.Kc[a0] * dKc[nt][u] + sm.Kc[a1] * dKc[nt][2 + u] + F.Qr[a0] * dQr[nt][u] +
+                          F.Qr[a1] * dQr[nt][2 + u] + F.Kr[a0] * dKr[nt][u] + F.Kr[a1] * dKr[nt][2 + u];
         }
-    ffor<4>(dP, R0, C0, [&](int r, int c, float &x) { WC[r * LDC + c] = c <= r ? x : 0.f; });  // lower(dP)
+    ffor<4>(dP, R0, C0, [&](int r, int cc, float &x) { WC[r * LDC + cc] = cc <= r ? x : 0.f; });  // lower(dP)
     store(dT, WA);
     __syncthreads();
     // dQr += dP Kc;  dKc += dP^T Qr
-    wmm<C, NK, SPLIT>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0, CK);
-    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int c) { return tb.Qr[m * LDK + c]; }, R0, CK);
+    wmm<C, NK, SPLIT>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int cc) { return sm.Kc[m * LDK + cc]; }, R0,
+                      CK);
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int cc) { return F.Qr[m * LDK + cc]; }, R0,
+                      CK);
     // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
     fzero<4>(acc);
-    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.T[c * LDC + m]; }, R0, C0);
+    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int cc) { return sm.T[cc * LDC + m]; }, R0,
+                     C0);
     store(acc, WD);
     __syncthreads();
     fzero<4>(acc);
-    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int c) { return WD[m * LDC + c]; }, R0, C0);
+    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return sm.T[m * LDC + r]; }, [&](int m, int cc) { return WD[m * LDC + cc]; }, R0,
+                     C0);
     __syncthreads();  // every read of dT in WA is done
-    ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { WA[r * LDC + c] = c < r ? -x : 0.f; });
+    ffor<4>(acc, R0, C0, [&](int r, int cc, float &x) { WA[r * LDC + cc] = cc < r ? -x : 0.f; });
     __syncthreads();
     // dKr += Diag(beta) dA Kc (and dbeta's second part Kr . (dA Kc));  dKc += (Diag(beta) dA)^T Kr
     {
         float tmp[NK][4];
         fzero<NK>(tmp);
-        wmm<C, NK, SPLIT>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int c) { return tb.Kc[m * LDK + c]; }, R0,
-                   CK);
-        float d2[2] = {0.f, 0.f};
+        wmm<C, NK, SPLIT>(tmp, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int cc) { return sm.Kc[m * LDK + cc]; },
+                          R0, CK);
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t4 + (e & 1);
-                d2[e >> 1] += tb.Kr[r * LDK + c] * tmp[nt][e];
-                dKr[nt][e] += tb.beta[r] * tmp[nt][e];
+                const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1);
+                db[e >> 1] += F.Kr[r * LDK + cc] * tmp[nt][e];
+                dKr[nt][e] += sm.beta[r] * tmp[nt][e];
             }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) db[u] += d2[u];
     }
-    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return tb.beta[m] * WA[m * LDC + r]; },
-               [&](int m, int c) { return tb.Kr[m * LDK + c]; }, R0, CK);
-    // dbeta: sums over this warp's columns (the 4 lanes of a row), then the two
-    // column halves of each row in a fixed order
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return sm.beta[m] * WA[m * LDC + r]; },
+                      [&](int m, int cc) { return F.Kr[m * LDK + cc]; }, R0, CK);
+    // dbeta's second part: sums over this warp's columns (the 4 lanes of a
+    // row), then the two column halves of each row and the first part, in a
+    // fixed order
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         db[u] += __shfl_xor_sync(0xffffffffu, db[u], 1);
@@ -788,24 +968,24 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     }
     // the chunk's gate factors p / mu (as in the forward tables) into the free
     // work tiles; dq, dk, and d log p into Qr's place
-    float *E2 = sm.W[0];  // [C][LDK]: spans W[0] and W[1]
+    float *E2 = F.W[1];  // [C][LDK]: spans W[1] and W[2]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
-    simt::gate_factor_table<DK>(tb, E2, LDK, p.alpha, GATE, tok0, L, H, h);
-    tb.part[(tid / DK) * DK + tid % DK] = tb.mu[tid % DK] * tb.mu[tid % DK] * s0;
-    if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid];
+    simt::gate_factor_table<DK>(sm.part, sm.mu, E2, LDK, p.alpha, GATE, tok0, L, H, h);
+    sm.part[(tid / DK) * DK + tid % DK] = sm.mu[tid % DK] * sm.mu[tid % DK] * s0;
+    if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid] + dbr[2 * C + tid];
     float dlogp[NK][4];
 #pragma unroll
     for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int r = R0 + g + 8 * (e >> 1), c = CK + 8 * nt + 2 * t4 + (e & 1), rc = r * LDK + c;
+            const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1), rc = r * LDK + cc;
             const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
             if (r < L) {
                 const int64_t th = (tok0 + r) * H + h;
-                p.dq[th * DK + c] = dQr[nt][e] * e2;
-                p.dk[th * DK + c] = dKr[nt][e] * e2 + dKc[nt][e] * e3;
+                p.dq[th * DK + cc] = dQr[nt][e] * e2;
+                p.dk[th * DK + cc] = dKr[nt][e] * e2 + dKc[nt][e] * e3;
             }
-            dlogp[nt][e] = dKr[nt][e] * tb.Kr[rc] + dQr[nt][e] * tb.Qr[rc] - dKc[nt][e] * tb.Kc[rc];
+            dlogp[nt][e] = dKr[nt][e] * F.Kr[rc] + dQr[nt][e] * F.Qr[rc] - dKc[nt][e] * sm.Kc[rc];
         }
     // s123: sums over the 16 rows of this warp (lanes with the same t), then by warp row block
 #pragma unroll
@@ -824,33 +1004,33 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int u = 0; u < 2; ++u) sm.red[(warp & 3) * DK + CK + 8 * nt + 2 * t4 + u] = s123[nt][u];
-    ffor<NK>(dlogp, R0, CK, [&](int r, int c, float &x) { tb.Qr[r * LDK + c] = x; });
+    ffor<NK>(dlogp, R0, CK, [&](int r, int cc, float &x) { F.Qr[r * LDK + cc] = x; });
     __syncthreads();
     // per channel: d log mu, then d log alpha by a reverse running sum over the rows
     if (tid < DK) {
-        const int c = tid;
+        const int cc = tid;
         float s0c = 0.f;
-        for (int hp = 0; hp < NT / DK; ++hp) s0c += tb.part[hp * DK + c];
+        for (int hp = 0; hp < NT / DK; ++hp) s0c += sm.part[hp * DK + cc];
         float s123c = 0.f;
-        for (int t2 = 0; t2 < 4; ++t2) s123c += sm.red[t2 * DK + c];
+        for (int t2 = 0; t2 < 4; ++t2) s123c += sm.red[t2 * DK + cc];
         float colsum = 0.f;
-        for (int r = 0; r < L; ++r) colsum += tb.Qr[r * LDK + c];
+        for (int r = 0; r < L; ++r) colsum += F.Qr[r * LDK + cc];
         const float dlogmu = 2.f * s0c + s123c - colsum;
         float run = 0.5f * dlogmu;
 #pragma unroll 8
         for (int r = L - 1; r >= 0; --r) {
-            run += tb.Qr[r * LDK + c];
+            run += F.Qr[r * LDK + cc];
             const int64_t th = (tok0 + r) * H + h;
-            const float da = run / gate_at(p.alpha, GATE, th, c, DK);
-            if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + c] = da;
-            else tb.Qr[r * LDK + c] = da;  // (this thread's own column, read only by itself above)
+            const float da = run / gate_at(p.alpha, GATE, th, cc, DK);
+            if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + cc] = da;
+            else F.Qr[r * LDK + cc] = da;  // (this thread's own column, read only by itself above)
         }
     }
     if (GATE == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
         __syncthreads();
         if (tid < L) {
             float da = 0.f;
-            for (int c = 0; c < DK; ++c) da += tb.Qr[tid * LDK + c];
+            for (int cc = 0; cc < DK; ++cc) da += F.Qr[tid * LDK + cc];
             p.dalpha[(tok0 + tid) * H + h] = da;
         }
     }
@@ -858,7 +1038,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 
 constexpr size_t kMaxSmem = 232448;  // dynamic shared memory one CTA may have
 static_assert(sizeof(StatesSmem<128>) <= kMaxSmem && sizeof(ChainSmem<128>) <= kMaxSmem &&
-                  sizeof(LocalSmem<128>) <= kMaxSmem && sizeof(simt::Tables<128>) <= kMaxSmem,
+                  sizeof(LocalSmem<128, float>) <= kMaxSmem && sizeof(LocalSmem<128, __nv_bfloat16>) <= kMaxSmem &&
+                  sizeof(simt::Tables<128>) <= kMaxSmem,
               "shared memory per CTA");
 
 // Packed batches: checks cu_seqlens (starts at 0, never decreases, ends at
@@ -927,13 +1108,14 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     p.states = ws;
     p.gnext = ws + slab;
     p.tabs = ws + 2 * slab;
+    p.work = p.tabs + chunks * b.H * TabLayout<DK>::FLOATS;
     p.N = b.N; p.T = b.T; p.H = b.H; p.DV = b.d_v; p.NC = NC; p.gate = b.gate;
     p.cu = b.cu_seqlens;
     p.coff = nullptr;
     p.status = nullptr;
     cudaError_t e;
     if (packed) {
-        int32_t *tail = reinterpret_cast<int32_t *>(p.tabs + chunks * b.H * TabLayout<DK>::FLOATS);
+        int32_t *tail = reinterpret_cast<int32_t *>(p.work + chunks * b.H * 4 * C * b.d_v);
         int32_t *coff = tail + 4;  // tail[0]: the status word when the caller gives none
         int32_t *status = b.dev_status ? b.dev_status : tail;
         kda_bwd_varlen_prep_kernel<<<1, kPrepThreads, 0, s>>>(b.cu_seqlens, b.N, b.T, coff, status);
@@ -971,7 +1153,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     auto local = b.gate == KDA_GATE_SCALAR ? kda_bwd_local_kernel<DK, TIn, KDA_GATE_SCALAR>
                  : b.gate == KDA_GATE_NONE ? kda_bwd_local_kernel<DK, TIn, KDA_GATE_NONE>
                                            : kda_bwd_local_kernel<DK, TIn, KDA_GATE_CHANNEL>;
-    const size_t sl = sizeof(LocalSmem<DK>);
+    const size_t sl = sizeof(LocalSmem<DK, TIn>);
     if ((e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl)) != cudaSuccess) return e;
     local<<<chunk_ctas, NT, sl, s>>>(p);
     return cudaGetLastError();
@@ -983,7 +1165,7 @@ size_t backward_workspace_bytes(int N, int T, int H, int dk, int dv, bool packed
     const size_t chunks = (size_t)chunk_bound(packed, N, T) * H;
     const size_t tab = dk == 128 ? TabLayout<128>::FLOATS : TabLayout<64>::FLOATS;
     const size_t tail = packed ? (4 + (size_t)N + 1) * sizeof(int32_t) : 0;  // status, chunk offsets
-    return (2 * chunks * dk * dv + chunks * tab) * sizeof(float) + tail;
+    return (2 * chunks * dk * dv + chunks * tab + chunks * 4 * C * dv) * sizeof(float) + tail;
 }
 
 cudaError_t launch_backward(const BackwardArgs &b, cudaStream_t s) {

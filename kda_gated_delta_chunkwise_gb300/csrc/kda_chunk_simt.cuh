@@ -117,11 +117,11 @@ __device__ void gate_tables(Tables<DK> &tb, const float *alpha, int gate, const 
 
 // The gate factor p / mu of every row and channel of the chunk (the factor
 // that made Kr and Qr) into E2 ([C][ld] floats), with the same arithmetic as
-// gate_tables, so the same bits. Needs tb.mu of the chunk; uses tb.part as
-// scratch. Ends with a barrier.
+// gate_tables, so the same bits. Needs the chunk's mu ([DK], shared memory);
+// uses part ([NT / DK][DK], shared memory) as scratch. Ends with a barrier.
 template <int DK>
-__device__ void gate_factor_table(Tables<DK> &tb, float *E2, int ld, const float *alpha, int gate, int64_t tok0, int L,
-                                  int H, int h) {
+__device__ void gate_factor_table(float *part, const float *mu, float *E2, int ld, const float *alpha, int gate,
+                                  int64_t tok0, int L, int H, int h) {
     constexpr int SEG = NT / DK;
     constexpr int TPS = C / SEG;
     const int tid = threadIdx.x;
@@ -134,14 +134,14 @@ __device__ void gate_factor_table(Tables<DK> &tb, float *E2, int ld, const float
         al[i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, c, DK) : 1.f;
         prod *= al[i];
     }
-    __syncthreads();  // earlier readers of tb.part are done
-    tb.part[seg * DK + c] = prod;
+    __syncthreads();  // earlier readers of part are done
+    part[seg * DK + c] = prod;
     __syncthreads();
     float before = 1.f;
 #pragma unroll
     for (int s2 = 0; s2 < SEG; ++s2)
-        if (s2 < seg) before *= tb.part[s2 * DK + c];
-    const float inv_mu = 1.f / tb.mu[c];
+        if (s2 < seg) before *= part[s2 * DK + c];
+    const float inv_mu = 1.f / mu[c];
     float pre = before;
 #pragma unroll
     for (int i = 0; i < TPS; ++i) {

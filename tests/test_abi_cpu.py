@@ -272,9 +272,9 @@ def test_backward_argument_checks(lib):
     p = ctypes.c_void_p(0x1000)
     ws = lib.kda_prefill_backward_workspace_bytes(2, 130, 3, 128, 128)
     chunks = 2 * 3 * 3
-    # per chunk: the state, the state gradient, and the chunk tables (Kr, Qr,
-    # Kc, T, P, mu, beta and a flag)
-    assert ws == chunks * (2 * 128 * 128 + 3 * 64 * 128 + 2 * 64 * 64 + 128 + 64 + 4) * 4
+    # per chunk: the state, the state gradient, the chunk tables (Kr, Qr, Kc,
+    # T, P, mu, beta and a flag) and four 64 x d_v work tiles (U, V - X, dU, dR)
+    assert ws == chunks * (2 * 128 * 128 + 3 * 64 * 128 + 2 * 64 * 64 + 128 + 64 + 4 + 4 * 64 * 128) * 4
     args = [p, p, p, 1, p, p, None, p, None, p, p, p, p, p, None, 2, 130, 3, 128, 128]
     assert lib.kda_prefill_backward(*args, None, 0, None) == 5           # no workspace
     assert lib.kda_prefill_backward(*args, ctypes.c_void_p(0x1008), ws, None) == 5  # misaligned
