@@ -177,6 +177,33 @@ __device__ __forceinline__ void cp16(void *dst, const void *src) {
                  : "memory");
 }
 
+// 16 bytes global -> shared, or 16 zero bytes when n = 0 (src is then not read).
+__device__ __forceinline__ void cp16z(void *dst, const void *src, uint32_t n) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
+                 "r"(n)
+                 : "memory");
+}
+// A [C][VS] tile of per-token rows (v or dO of value columns v0 ..) into
+// shared memory (rows of ld elements), rows past the sequence as zeros;
+// cp.async, not committed.
+template <typename TIn>
+__device__ __forceinline__ void load_rows(TIn *dst, int ld, const TIn *src, int64_t tok0, int L, int H, int h, int DV,
+                                          int v0) {
+    constexpr int E = 16 / (int)sizeof(TIn), Q = VS / E;  // elements per 16 bytes; 16-byte pieces of a row
+    for (int e = threadIdx.x; e < C * Q; e += NT) {
+        const int r = e / Q, cc = E * (e % Q);
+        cp16z(dst + r * ld + cc, src + ((tok0 + (r < L ? r : 0)) * H + h) * DV + v0 + cc, r < L ? 16u : 0u);
+    }
+}
+// Pulls the rows of such a tile into L2 ahead of their use.
+template <typename TIn>
+__device__ __forceinline__ void prefetch_rows(const TIn *src, int64_t tok0, int L, int H, int h, int DV, int v0) {
+    if ((int)threadIdx.x < L)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + ((tok0 + threadIdx.x) * H + h) * DV + v0));
+}
+// The padded row of such a tile (elements): 16-byte rows, conflict-free reads.
+template <typename TIn> struct RowTile { static constexpr int LD = sizeof(TIn) == 4 ? VS + 4 : VS + 8; };
+
 // Loads the parts `which` (TAB_*) of a chunk's tables, plus mu, beta and the
 // slow flag; T and P only when the chunk is not slow. Ends with a barrier.
 template <int DK> __device__ void load_tables(simt::Tables<DK> &tb, const float *src, unsigned which) {
@@ -352,6 +379,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     float *st = p.states + wbase * DK * DV;                    // chunk i at slot wbase + i wstride
     float *wkb = p.work + wbase * 4 * C * DV;
     const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
+    TIn *Vt = reinterpret_cast<TIn *>(tb.Qr);  // the chunk's v (Qr is not loaded here)
+    constexpr int LDV = RowTile<TIn>::LD;
+    static_assert(C * LDV * sizeof(TIn) <= sizeof(tb.Qr), "the v tile fits in Qr's place");
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
     for (int e = tid; e < DK * VS; e += NT)
@@ -362,8 +392,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
         for (int e = tid; e < DK * VS; e += NT)
             st[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
+        load_rows<TIn>(Vt, LDV, v, tok0, L, H, h, DV, v0);  // completes with the tables
         load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
-        if (ci + 1 < NC) prefetch_tables<DK>(tabs + (ci + 1) * wstride * TabLayout<DK>::FLOATS);
+        if (ci + 1 < NC) {
+            prefetch_tables<DK>(tabs + (ci + 1) * wstride * TabLayout<DK>::FLOATS);
+            const int64_t tn = t0 + C;
+            prefetch_rows<TIn>(v, tok0 + C, (int)((T - tn) < C ? (T - tn) : (int64_t)C), H, h, DV, v0);
+        }
         if (tb.slow) {
             const int j = tid % VS, part = tid / VS;
             for (int r = 0; r < L; ++r) {
@@ -391,8 +426,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.S[c * LDC + j]; }, R0, C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-            const float vv = r < L ? ld_in(v, ((tok0 + r) * H + h) * DV + v0 + c) : 0.f;
-            x = vv - x;
+            x = to_f32(Vt[r * LDV + c]) - x;
             sm.R[r * LDC + c] = tb.beta[r] * x;
         });
         gstore<4>(acc, R0, C0, wk + C * DV, DV);
@@ -422,7 +456,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
 template <int DK> struct ChainSmem {
     float G[DK * LDC];  // dL/dS slice, rows of LDC
     simt::Tables<DK> tb;
-    float dO[C * LDC];
+    float dO[C * LDC];  // holds the chunk's dO tile (qkv type, rows of RowTile::LD)
     float red[4 * VS];
 };
 static_assert(offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, tb) % 16 == 0, "16-byte offsets");
@@ -452,6 +486,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     float *gn = p.gnext + wbase * DK * DV;                     // chunk i at slot wbase + i wstride
     float *wkb = p.work + wbase * 4 * C * DV;
     const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
+    TIn *dOt = reinterpret_cast<TIn *>(sm.dO);  // the chunk's dO, rows of LDD elements
+    constexpr int LDD = RowTile<TIn>::LD;
+    static_assert(C * LDD * sizeof(TIn) <= sizeof(sm.dO), "the dO tile fits");
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
 
@@ -465,18 +502,18 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         const int64_t tok0 = t_begin + t0;
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
             gn[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
-        for (int e = tid; e < C * VS; e += NT) {
-            const int r = e / VS;
-            sm.dO[r * LDC + e % VS] = r < L ? ld_in(dO, ((tok0 + r) * H + h) * DV + v0 + e % VS) : 0.f;
-        }
+        load_rows<TIn>(dOt, LDD, dO, tok0, L, H, h, DV, v0);  // completes with the tables
         load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
-        if (ci > 0) prefetch_tables<DK>(tabs + (ci - 1) * wstride * TabLayout<DK>::FLOATS);
+        if (ci > 0) {
+            prefetch_tables<DK>(tabs + (ci - 1) * wstride * TabLayout<DK>::FLOATS);
+            prefetch_rows<TIn>(dO, tok0 - C, C, H, h, DV, v0);
+        }
         if (tb.slow) {
             // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
             const int j = tid % VS, part = tid / VS;
             for (int r = L - 1; r >= 0; --r) {
                 const int64_t tk = (tok0 + r) * H + h;
-                const float dj = sm.dO[r * LDC + j];
+                const float dj = to_f32(dOt[r * LDD + j]);
                 float wp = 0.f;
                 for (int c = part; c < DK; c += NT / VS) {
                     const float g = sm.G[c * LDC + j] + ld_in(q, tk * DK + c) * dj;
@@ -502,8 +539,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         fzero<4>(acc);
         wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
                    [&](int c, int j) { return tb.mu[c] * sm.G[c * LDC + j]; }, R0, C0);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; }, [&](int m, int j) { return sm.dO[m * LDC + j]; }, R0,
-                  C0);
+        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; },
+                         [&](int m, int j) { return to_f32(dOt[m * LDD + j]); }, R0, C0);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = x; });
         gstore<4>(acc, R0, C0, wk + 2 * C * DV, DV);
         __syncthreads();
@@ -521,7 +558,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         float acc2[ST::N8][4];
         fzero<ST::N8>(acc2);
         wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Qr[r * LDK + c]; },
-                       [&](int r, int j) { return sm.dO[r * LDC + j]; }, SR0, SC0);
+                       [&](int r, int j) { return to_f32(dOt[r * LDD + j]); }, SR0, SC0);
         wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Kr[r * LDK + c]; }, [&](int r, int j) { return dU[r * LDC + j]; },
                        SR0, SC0);
         ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
@@ -587,13 +624,6 @@ template <int DK, typename TIn> constexpr bool local_layout_ok() {
 static_assert(local_layout_ok<128, float>() && local_layout_ok<128, __nv_bfloat16>() && local_layout_ok<64, float>() &&
                   local_layout_ok<64, __nv_bfloat16>(),
               "16-byte tiles and offsets");
-
-// 16 bytes global -> shared, or 16 zero bytes when n = 0 (src is then not read).
-__device__ __forceinline__ void cp16z(void *dst, const void *src, uint32_t n) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
-                 "r"(n)
-                 : "memory");
-}
 
 // tf32 operands of one m16n8k8 step (hi, and lo when split).
 struct BFrag {

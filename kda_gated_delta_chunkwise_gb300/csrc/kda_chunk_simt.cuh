@@ -65,14 +65,19 @@ __device__ void gate_tables(Tables<DK> &tb, const float *alpha, int gate, const 
     constexpr int TPS = C / SEG;       // tokens per segment
     const int tid = threadIdx.x;
     const int c = tid % DK, seg = tid / DK;
-    float al[TPS];
-    float prod = 1.f;
+    float al[TPS], kk[TPS], qq[TPS];  // every load of the thread in flight at once
 #pragma unroll
     for (int i = 0; i < TPS; ++i) {
         const int r = seg * TPS + i;
-        al[i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, c, DK) : 1.f;
-        prod *= al[i];
+        const int64_t th = (tok0 + r) * H + h;
+        const bool in = r < L;
+        al[i] = in ? gate_at(alpha, gate, th, c, DK) : 1.f;
+        kk[i] = in ? ld_in(k, th * DK + c) : 0.f;
+        qq[i] = in ? ld_in(q, th * DK + c) : 0.f;
     }
+    float prod = 1.f;
+#pragma unroll
+    for (int i = 0; i < TPS; ++i) prod *= al[i];
     tb.part[seg * DK + c] = prod;
     if (tid == 0) tb.slow = 0;
     __syncthreads();
@@ -101,15 +106,10 @@ __device__ void gate_tables(Tables<DK> &tb, const float *alpha, int gate, const 
     for (int i = 0; i < TPS; ++i) {
         const int r = seg * TPS + i;
         pre *= al[i];
-        float kk = 0.f, qq = 0.f;
-        if (r < L) {
-            kk = ld_in(k, ((tok0 + r) * H + h) * DK + c);
-            qq = ld_in(q, ((tok0 + r) * H + h) * DK + c);
-        }
         const float e2 = pre * inv_mu, e3 = suf[i] * inv_mu;
-        tb.Kr[r * LDK + c] = kk * e2;
-        tb.Qr[r * LDK + c] = qq * e2;
-        tb.Kc[r * LDK + c] = kk * e3;
+        tb.Kr[r * LDK + c] = kk[i] * e2;
+        tb.Qr[r * LDK + c] = qq[i] * e2;
+        tb.Kc[r * LDK + c] = kk[i] * e3;
     }
     if (tid < C) tb.beta[tid] = tid < L ? beta[(tok0 + tid) * H + h] : 0.f;
     __syncthreads();
