@@ -313,7 +313,72 @@ __device__ __forceinline__ void gstore(const float (&acc)[NT8][4], int r0, int c
     }
 }
 
+// tf32 operands of one m16n8k8 step (hi, and lo when split).
+struct BFrag {
+    uint32_t h0, h1, l0, l1;
+};
+template <bool SPLIT> __device__ __forceinline__ BFrag bfrag(float b0, float b1) {
+    BFrag f;
+    if (SPLIT) {
+        split_tf32(b0, f.h0, f.l0);
+        split_tf32(b1, f.h1, f.l1);
+    } else {
+        f.h0 = tf32_bits(b0);
+        f.h1 = tf32_bits(b1);
+        f.l0 = f.l1 = 0u;
+    }
+    return f;
+}
+// A fragment of the 16 x 8 block at rows r0.., columns k.. of a row-major tile.
+template <bool SPLIT, typename TS>
+__device__ __forceinline__ void afrag(const TS *x, int ld, int r0, int k, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float v[4] = {to_f32(x[(r0 + g) * ld + k + t]), to_f32(x[(r0 + g + 8) * ld + k + t]),
+                        to_f32(x[(r0 + g) * ld + k + t + 4]), to_f32(x[(r0 + g + 8) * ld + k + t + 4])};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (SPLIT) split_tf32(v[u], hi[u], lo[u]);
+        else hi[u] = tf32_bits(v[u]), lo[u] = 0u;
+    }
+}
+template <bool SPLIT>
+__device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const BFrag &b) {
+    if (SPLIT) {
+        mma8(d, al, b.h0, b.h1);
+        mma8(d, ah, b.l0, b.l1);
+    }
+    mma8(d, ah, b.h0, b.h1);
+}
+
 // ---------------------------------------------------------------- tables
+// A = beta (Kr Kc^T) strictly lower and P = Qr Kc^T lower incl. diagonal on
+// the tensor cores (the two products share the Kc fragments). Ends with a
+// barrier.
+template <int DK, bool SPLIT> __device__ void ap_products(simt::Tables<DK> &tb) {
+    constexpr int LDK = simt::Tables<DK>::LDK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
+    float accA[4][4], accP[4][4];
+    fzero<4>(accA);
+    fzero<4>(accP);
+#pragma unroll 2
+    for (int k = 0; k < DK; k += 8) {
+        uint32_t kh[4], kl[4], qh[4], ql[4];
+        afrag<SPLIT>(tb.Kr, LDK, R0, k, kh, kl);
+        afrag<SPLIT>(tb.Qr, LDK, R0, k, qh, ql);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int o = (C0 + 8 * nt + g) * LDK + k + t4;
+            const BFrag b = bfrag<SPLIT>(tb.Kc[o], tb.Kc[o + 4]);
+            mma_f<SPLIT>(accA[nt], kh, kl, b);
+            mma_f<SPLIT>(accP[nt], qh, ql, b);
+        }
+    }
+    ffor<4>(accA, R0, C0, [&](int r, int j, float &x) { tb.A[r * LDC + j] = j < r ? tb.beta[r] * x : 0.f; });
+    ffor<4>(accP, R0, C0, [&](int r, int j, float &x) { tb.P[r * LDC + j] = j <= r ? x : 0.f; });
+    __syncthreads();
+}
+
 // One CTA per (sequence, head, chunk): the chunk's tables into the workspace.
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
@@ -327,7 +392,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
     if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
     simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
                                p.H, h);
-    if (!tb.slow) simt::wy_tables<DK>(tb);
+    if (!tb.slow) {
+        ap_products<DK, std::is_same<TIn, float>::value>(tb);  // fp32 inputs: split tf32, fp32 accuracy
+        simt::invert_a<DK>(tb);
+    }
     store_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS);
 }
 
@@ -624,43 +692,6 @@ template <int DK, typename TIn> constexpr bool local_layout_ok() {
 static_assert(local_layout_ok<128, float>() && local_layout_ok<128, __nv_bfloat16>() && local_layout_ok<64, float>() &&
                   local_layout_ok<64, __nv_bfloat16>(),
               "16-byte tiles and offsets");
-
-// tf32 operands of one m16n8k8 step (hi, and lo when split).
-struct BFrag {
-    uint32_t h0, h1, l0, l1;
-};
-template <bool SPLIT> __device__ __forceinline__ BFrag bfrag(float b0, float b1) {
-    BFrag f;
-    if (SPLIT) {
-        split_tf32(b0, f.h0, f.l0);
-        split_tf32(b1, f.h1, f.l1);
-    } else {
-        f.h0 = tf32_bits(b0);
-        f.h1 = tf32_bits(b1);
-        f.l0 = f.l1 = 0u;
-    }
-    return f;
-}
-// A fragment of the 16 x 8 block at rows r0.., columns k.. of a row-major tile.
-template <bool SPLIT, typename TS>
-__device__ __forceinline__ void afrag(const TS *x, int ld, int r0, int k, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const float v[4] = {to_f32(x[(r0 + g) * ld + k + t]), to_f32(x[(r0 + g + 8) * ld + k + t]),
-                        to_f32(x[(r0 + g) * ld + k + t + 4]), to_f32(x[(r0 + g + 8) * ld + k + t + 4])};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        if (SPLIT) split_tf32(v[u], hi[u], lo[u]);
-        else hi[u] = tf32_bits(v[u]), lo[u] = 0u;
-    }
-}
-template <bool SPLIT>
-__device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const BFrag &b) {
-    if (SPLIT) {
-        mma8(d, al, b.h0, b.h1);
-        mma8(d, ah, b.l0, b.l1);
-    }
-    mma8(d, ah, b.h0, b.h1);
-}
 
 // The local pass of a chunk that the forward runs token by token (a channel
 // decays past e^-80), in `buf` (slow_floats<DK>() floats of shared memory).

@@ -151,10 +151,9 @@ __device__ void gate_factor_table(float *part, const float *mu, float *E2, int l
     __syncthreads();
 }
 
-// A = beta (Kr Kc^T) strictly lower, P = Qr Kc^T lower incl. diagonal, then
-// T = (I + A)^{-1} (forward substitution on 16 x 16 blocks, then block
-// products). Leaves A's upper triangle overwritten. Ends with a barrier.
-template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
+// A = beta (Kr Kc^T) strictly lower and P = Qr Kc^T lower incl. diagonal, in
+// fp32 on CUDA cores. Ends with a barrier.
+template <int DK> __device__ void wy_products(Tables<DK> &tb) {
     constexpr int LDK = Tables<DK>::LDK, LDC = Tables<DK>::LDC;
     const int tid = threadIdx.x;
     const int tx = tid % 16, ty = tid / 16;
@@ -190,6 +189,14 @@ template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
             }
     }
     __syncthreads();
+}
+
+// T = (I + A)^{-1} for the strictly lower A in tb.A (forward substitution on
+// 16 x 16 blocks, then block products). Leaves A's upper triangle
+// overwritten. Ends with a barrier.
+template <int DK> __device__ void invert_a(Tables<DK> &tb) {
+    constexpr int LDC = Tables<DK>::LDC;
+    const int tid = threadIdx.x;
     // T = (I + A)^{-1} by blocks of 16 (A strictly lower, so T is unit lower):
     //   the four diagonal blocks by forward substitution, one thread per column;
     //   then T_{b+1,b} = -T_{b+1,b+1} A_{b+1,b} T_{b,b} for the pairs (0,1), (2,3);
@@ -252,6 +259,12 @@ template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
         }
         __syncthreads();
     }
+}
+
+// The WY tables of a chunk whose gated tables are in tb: A, P, then T.
+template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
+    wy_products<DK>(tb);
+    invert_a<DK>(tb);
 }
 
 }  // namespace simt
