@@ -149,27 +149,6 @@ template <int DK> struct TabLayout {
 };
 enum TabPart : unsigned { TAB_KR = 1, TAB_QR = 2, TAB_KC = 4, TAB_T = 8, TAB_P = 16, TAB_ALL = 31 };
 
-template <int DK> __device__ void store_tables(const simt::Tables<DK> &tb, float *dst) {
-    using L = TabLayout<DK>;
-    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, Q4 = DK / 4, C4 = C / 4;
-    const int tid = threadIdx.x;
-    for (int e = tid; e < C * Q4; e += NT) {
-        const int r = e / Q4, c = 4 * (e % Q4);
-        *reinterpret_cast<float4 *>(dst + L::KR + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Kr[r * LDK + c]);
-        *reinterpret_cast<float4 *>(dst + L::QR + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Qr[r * LDK + c]);
-        *reinterpret_cast<float4 *>(dst + L::KC + r * DK + c) = *reinterpret_cast<const float4 *>(&tb.Kc[r * LDK + c]);
-    }
-    if (!tb.slow)
-        for (int e = tid; e < C * C4; e += NT) {
-            const int r = e / C4, c = 4 * (e % C4);
-            *reinterpret_cast<float4 *>(dst + L::T + r * C + c) = *reinterpret_cast<const float4 *>(&tb.T[r * LDC + c]);
-            *reinterpret_cast<float4 *>(dst + L::P + r * C + c) = *reinterpret_cast<const float4 *>(&tb.P[r * LDC + c]);
-        }
-    for (int e = tid; e < DK; e += NT) dst[L::MU + e] = tb.mu[e];
-    for (int e = tid; e < C; e += NT) dst[L::BETA + e] = tb.beta[e];
-    if (tid == 0) dst[L::SLOW] = __int_as_float(tb.slow);
-}
-
 // 16 bytes global -> shared without a register round trip (cp.async), so
 // that every thread has all its loads of a table in flight at once.
 __device__ __forceinline__ void cp16(void *dst, const void *src) {
@@ -351,52 +330,174 @@ __device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&ah)[4], co
 }
 
 // ---------------------------------------------------------------- tables
-// A = beta (Kr Kc^T) strictly lower and P = Qr Kc^T lower incl. diagonal on
-// the tensor cores (the two products share the Kc fragments). Ends with a
-// barrier.
-template <int DK, bool SPLIT> __device__ void ap_products(simt::Tables<DK> &tb) {
-    constexpr int LDK = simt::Tables<DK>::LDK;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
-    float accA[4][4], accP[4][4];
-    fzero<4>(accA);
-    fzero<4>(accP);
-#pragma unroll 2
-    for (int k = 0; k < DK; k += 8) {
-        uint32_t kh[4], kl[4], qh[4], ql[4];
-        afrag<SPLIT>(tb.Kr, LDK, R0, k, kh, kl);
-        afrag<SPLIT>(tb.Qr, LDK, R0, k, qh, ql);
+// The key channels are taken in two halves of CH = DK / 2, so that the
+// shared memory of a CTA (one half of Kr, Qr, Kc, plus A and T: about 88 KB
+// for d_k = 128) lets two CTAs share an SM and hide each other's loads. Per
+// half, thread (channel cl, segment seg) owns TPS consecutive tokens of one
+// channel.
+template <int DK> struct GateSplit {
+    static constexpr int CH = DK / 2, SEG = NT / CH, TPS = C / SEG, LDH = CH + 4;
+};
+
+template <int DK> struct TabSmem {
+    float Kr[C * GateSplit<DK>::LDH];  // one half of the channels
+    float Qr[C * GateSplit<DK>::LDH];
+    float Kc[C * GateSplit<DK>::LDH];
+    float A[C * LDC];
+    float T[C * LDC];
+    float beta[C];
+    float part[NT];  // segment products
+    int slow;
+};
+
+// The gate factor p / mu of every row and channel of the chunk (the factor
+// that made Kr and Qr) into E2 ([C][ld] floats), with the arithmetic of the
+// tables pass, so the same bits. Needs the chunk's mu ([DK], shared memory);
+// uses part ([NT], shared memory) as scratch. Ends with a barrier.
+template <int DK>
+__device__ void gate_factor_table(float *part, const float *mu, float *E2, int ld, const float *alpha, int gate,
+                                  int64_t tok0, int L, int H, int h) {
+    using GS = GateSplit<DK>;
+    const int tid = threadIdx.x, cl = tid % GS::CH, seg = tid / GS::CH;
+    for (int half = 0; half < 2; ++half) {
+        const int c = half * GS::CH + cl;
+        float al[GS::TPS];
+        float prod = 1.f;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int o = (C0 + 8 * nt + g) * LDK + k + t4;
-            const BFrag b = bfrag<SPLIT>(tb.Kc[o], tb.Kc[o + 4]);
-            mma_f<SPLIT>(accA[nt], kh, kl, b);
-            mma_f<SPLIT>(accP[nt], qh, ql, b);
+        for (int i = 0; i < GS::TPS; ++i) {
+            const int r = seg * GS::TPS + i;
+            al[i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, c, DK) : 1.f;
+            prod *= al[i];
+        }
+        __syncthreads();  // earlier readers of part are done
+        part[seg * GS::CH + cl] = prod;
+        __syncthreads();
+        float before = 1.f;
+#pragma unroll
+        for (int s2 = 0; s2 < GS::SEG; ++s2)
+            if (s2 < seg) before *= part[s2 * GS::CH + cl];
+        const float inv_mu = 1.f / mu[c];
+        float pre = before;
+#pragma unroll
+        for (int i = 0; i < GS::TPS; ++i) {
+            pre *= al[i];
+            E2[(seg * GS::TPS + i) * ld + c] = pre * inv_mu;
         }
     }
-    ffor<4>(accA, R0, C0, [&](int r, int j, float &x) { tb.A[r * LDC + j] = j < r ? tb.beta[r] * x : 0.f; });
-    ffor<4>(accP, R0, C0, [&](int r, int j, float &x) { tb.P[r * LDC + j] = j <= r ? x : 0.f; });
     __syncthreads();
 }
 
 // One CTA per (sequence, head, chunk): the chunk's tables into the workspace.
+// Per half of the channels: the gate products (p_r running products, gamma,
+// mu = sqrt(gamma), the slow flag), Kr = k p / mu, Qr = q p / mu, Kc = k
+// (gamma / p) / mu written straight to the workspace and kept in shared
+// memory for the half's share of A = Diag(beta) Kr Kc^T and P = Qr Kc^T (tensor
+// cores; the sums over both halves stay in registers); then P to the
+// workspace, T = (I + A)^{-1}.
 template <int DK, typename TIn>
-__global__ void __launch_bounds__(NT, 1) kda_bwd_tables_kernel(BwdParams p) {
+__global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
+    using GS = GateSplit<DK>;
+    using TL = TabLayout<DK>;
+    constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
+    constexpr int LDH = GS::LDH;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    simt::Tables<DK> &tb = *reinterpret_cast<simt::Tables<DK> *>(smem_raw);
+    TabSmem<DK> &sm = *reinterpret_cast<TabSmem<DK> *>(smem_raw);
     const int64_t idx = blockIdx.x;  // the chunk's workspace slot
-    int64_t c;
+    int64_t c0;
     int h, n, L;
     int64_t tok0;
-    cta_chunk(p, idx, c, h);
-    if ((p.status && *p.status) || !chunk_of(p, c, n, tok0, L)) return;
-    simt::gate_tables<DK, TIn>(tb, p.alpha, p.gate, (const TIn *)p.q, (const TIn *)p.k, p.beta, tok0, L,
-                               p.H, h);
-    if (!tb.slow) {
-        ap_products<DK, std::is_same<TIn, float>::value>(tb);  // fp32 inputs: split tf32, fp32 accuracy
-        simt::invert_a<DK>(tb);
+    cta_chunk(p, idx, c0, h);
+    if ((p.status && *p.status) || !chunk_of(p, c0, n, tok0, L)) return;
+    const int H = p.H;
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k;
+    float *dst = p.tabs + idx * TL::FLOATS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int cl = tid % GS::CH, seg = tid / GS::CH;
+    const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
+    if (tid == 0) sm.slow = 0;
+    if (tid < C) sm.beta[tid] = tid < L ? p.beta[(tok0 + tid) * H + h] : 0.f;
+    float accA[4][4], accP[4][4];
+    fzero<4>(accA);
+    fzero<4>(accP);
+    for (int half = 0; half < 2; ++half) {
+        const int c = half * GS::CH + cl;
+        float al[GS::TPS], kk[GS::TPS], qq[GS::TPS];  // every load of the thread in flight at once
+#pragma unroll
+        for (int i = 0; i < GS::TPS; ++i) {
+            const int r = seg * GS::TPS + i;
+            const int64_t th = (tok0 + r) * H + h;
+            const bool in = r < L;
+            al[i] = in ? gate_at(p.alpha, p.gate, th, c, DK) : 1.f;
+            kk[i] = in ? ld_in(k, th * DK + c) : 0.f;
+            qq[i] = in ? ld_in(q, th * DK + c) : 0.f;
+        }
+        float prod = 1.f;
+#pragma unroll
+        for (int i = 0; i < GS::TPS; ++i) prod *= al[i];
+        __syncthreads();  // the previous half's products are done with the tiles
+        sm.part[seg * GS::CH + cl] = prod;
+        __syncthreads();
+        float before = 1.f, after = 1.f, gamma = 1.f;
+#pragma unroll
+        for (int s2 = 0; s2 < GS::SEG; ++s2) {
+            const float pt = sm.part[s2 * GS::CH + cl];
+            if (s2 < seg) before *= pt;
+            if (s2 > seg) after *= pt;
+            gamma *= pt;
+        }
+        if (gamma < simt::kMinGamma) sm.slow = 1;
+        const float mu = sqrtf(gamma), inv_mu = 1.f / mu;
+        if (seg == 0) dst[TL::MU + c] = mu;
+        float suf[GS::TPS];  // exclusive suffix products within the segment, times the later segments
+        float s_acc = after;
+#pragma unroll
+        for (int i = GS::TPS - 1; i >= 0; --i) {
+            suf[i] = s_acc;
+            s_acc *= al[i];
+        }
+        float pre = before;
+#pragma unroll
+        for (int i = 0; i < GS::TPS; ++i) {
+            const int r = seg * GS::TPS + i;
+            pre *= al[i];
+            const float e2 = pre * inv_mu, e3 = suf[i] * inv_mu;
+            const float kr = kk[i] * e2, qr = qq[i] * e2, kc = kk[i] * e3;
+            sm.Kr[r * LDH + cl] = kr;
+            sm.Qr[r * LDH + cl] = qr;
+            sm.Kc[r * LDH + cl] = kc;
+            dst[TL::KR + r * DK + c] = kr;
+            dst[TL::QR + r * DK + c] = qr;
+            dst[TL::KC + r * DK + c] = kc;
+        }
+        __syncthreads();
+        // this half's share of [A; P] = [Kr; Qr] Kc^T (the two share the Kc fragments)
+#pragma unroll 2
+        for (int kx = 0; kx < GS::CH; kx += 8) {
+            uint32_t kh[4], kl[4], qh[4], ql[4];
+            afrag<SPLIT>(sm.Kr, LDH, R0, kx, kh, kl);
+            afrag<SPLIT>(sm.Qr, LDH, R0, kx, qh, ql);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int o = (C0 + 8 * nt + g) * LDH + kx + t4;
+                const BFrag b = bfrag<SPLIT>(sm.Kc[o], sm.Kc[o + 4]);
+                mma_f<SPLIT>(accA[nt], kh, kl, b);
+                mma_f<SPLIT>(accP[nt], qh, ql, b);
+            }
+        }
     }
-    store_tables<DK>(tb, p.tabs + idx * TabLayout<DK>::FLOATS);
+    if (tid < C) dst[TL::BETA + tid] = sm.beta[tid];
+    const int slow = sm.slow;  // (set before the last barrier)
+    if (tid == 0) dst[TL::SLOW] = __int_as_float(slow);
+    if (slow) return;  // the chunk runs token by token: no T or P
+    ffor<4>(accA, R0, C0, [&](int r, int j, float &x) { sm.A[r * LDC + j] = j < r ? sm.beta[r] * x : 0.f; });
+    ffor<4>(accP, R0, C0, [&](int r, int j, float &x) { x = j <= r ? x : 0.f; });
+    gstore<4>(accP, R0, C0, dst + TL::P, C);
+    __syncthreads();
+    simt::invert_unit_lower(simt::TPair{sm.A, sm.T});
+    for (int e = tid; e < C * C / 4; e += NT) {
+        const int r = e / (C / 4), cc = 4 * (e % (C / 4));
+        *reinterpret_cast<float4 *>(dst + TL::T + r * C + cc) = *reinterpret_cast<const float4 *>(&sm.T[r * LDC + cc]);
+    }
 }
 
 // ---------------------------------------------------------------- states
@@ -827,8 +928,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         local_slow<DK, TIn, GATE>(sm.u.slow, p, Sg, Gg, tok0, L, h);
         return;
     }
-    // Kr and Qr are read last, into the pieces' place: pull them into L2 now
+    // Kr and Qr are read last, into the pieces' place, and the gates near the
+    // end: pull them into L2 now
     for (int l = tid; l < 2 * C * DK / 32; l += NT) asm volatile("prefetch.global.L2 [%0];" ::"l"(tab + TL::KR + 32 * l));
+    if (GATE == KDA_GATE_CHANNEL)
+        for (int l = tid; l < L * (DK / 32); l += NT)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.alpha + ((tok0 + l / (DK / 32)) * H + h) * DK + 32 * (l % (DK / 32))));
     // Kc, T, mu, beta, then the first piece
     for (int e = tid; e < C * DK / 4; e += NT) {
         const int r = e / (DK / 4), cc = 4 * (e % (DK / 4));
@@ -1031,7 +1136,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = F.W[1];  // [C][LDK]: spans W[1] and W[2]
     static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
-    simt::gate_factor_table<DK>(sm.part, sm.mu, E2, LDK, p.alpha, GATE, tok0, L, H, h);
+    gate_factor_table<DK>(sm.part, sm.mu, E2, LDK, p.alpha, GATE, tok0, L, H, h);
     sm.part[(tid / DK) * DK + tid % DK] = sm.mu[tid % DK] * sm.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid] + dbr[2 * C + tid];
     float dlogp[NK][4];
@@ -1070,6 +1175,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // per channel: d log mu, then d log alpha by a reverse running sum over the rows
     if (tid < DK) {
         const int cc = tid;
+        float al[C];  // the channel's gates, every load in flight at once
+#pragma unroll
+        for (int r = 0; r < C; ++r) al[r] = r < L ? gate_at(p.alpha, GATE, (tok0 + r) * H + h, cc, DK) : 1.f;
         float s0c = 0.f;
         for (int hp = 0; hp < NT / DK; ++hp) s0c += sm.part[hp * DK + cc];
         float s123c = 0.f;
@@ -1078,13 +1186,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int r = 0; r < L; ++r) colsum += F.Qr[r * LDK + cc];
         const float dlogmu = 2.f * s0c + s123c - colsum;
         float run = 0.5f * dlogmu;
-#pragma unroll 8
-        for (int r = L - 1; r >= 0; --r) {
-            run += F.Qr[r * LDK + cc];
-            const int64_t th = (tok0 + r) * H + h;
-            const float da = run / gate_at(p.alpha, GATE, th, cc, DK);
-            if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + cc] = da;
-            else F.Qr[r * LDK + cc] = da;  // (this thread's own column, read only by itself above)
+#pragma unroll
+        for (int r = C - 1; r >= 0; --r) {
+            if (r < L) {
+                run += F.Qr[r * LDK + cc];
+                const int64_t th = (tok0 + r) * H + h;
+                const float da = run / al[r];
+                if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + cc] = da;
+                else F.Qr[r * LDK + cc] = da;  // (this thread's own column, read only by itself above)
+            }
         }
     }
     if (GATE == KDA_GATE_SCALAR) {  // one gate for every channel: the sum over them, in channel order
@@ -1188,7 +1298,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     const unsigned chunk_ctas = (unsigned)(chunks * b.H);
     if (chunks > 0) {  // 1. every chunk's tables, all chunks at once
         auto tabk = kda_bwd_tables_kernel<DK, TIn>;
-        const size_t st = sizeof(simt::Tables<DK>);
+        const size_t st = sizeof(TabSmem<DK>);
         if ((e = cudaFuncSetAttribute(tabk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st)) != cudaSuccess)
             return e;
         tabk<<<chunk_ctas, NT, st, s>>>(p);

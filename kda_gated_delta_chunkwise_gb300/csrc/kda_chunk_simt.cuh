@@ -1,5 +1,6 @@
-// Per-chunk tables of the chunkwise KDA algebra on CUDA cores (fp32), shared
-// by the fp32 prefill kernel and the backward kernels.
+// Per-chunk tables of the chunkwise KDA algebra on CUDA cores (fp32) for the
+// CUDA-core prefill; the backward shares the constants, the table layout and
+// the inverse.
 //
 // Source: the web page "研究KimiK3，我发现大模型正在学会“管理自己的计算”"
 // (pwwt.cn), the K3 essay: §四 (KDA update), §六.1 (chunks) and §六.2 (the
@@ -115,42 +116,6 @@ __device__ void gate_tables(Tables<DK> &tb, const float *alpha, int gate, const 
     __syncthreads();
 }
 
-// The gate factor p / mu of every row and channel of the chunk (the factor
-// that made Kr and Qr) into E2 ([C][ld] floats), with the same arithmetic as
-// gate_tables, so the same bits. Needs the chunk's mu ([DK], shared memory);
-// uses part ([NT / DK][DK], shared memory) as scratch. Ends with a barrier.
-template <int DK>
-__device__ void gate_factor_table(float *part, const float *mu, float *E2, int ld, const float *alpha, int gate,
-                                  int64_t tok0, int L, int H, int h) {
-    constexpr int SEG = NT / DK;
-    constexpr int TPS = C / SEG;
-    const int tid = threadIdx.x;
-    const int c = tid % DK, seg = tid / DK;
-    float al[TPS];
-    float prod = 1.f;
-#pragma unroll
-    for (int i = 0; i < TPS; ++i) {
-        const int r = seg * TPS + i;
-        al[i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, c, DK) : 1.f;
-        prod *= al[i];
-    }
-    __syncthreads();  // earlier readers of part are done
-    part[seg * DK + c] = prod;
-    __syncthreads();
-    float before = 1.f;
-#pragma unroll
-    for (int s2 = 0; s2 < SEG; ++s2)
-        if (s2 < seg) before *= part[s2 * DK + c];
-    const float inv_mu = 1.f / mu[c];
-    float pre = before;
-#pragma unroll
-    for (int i = 0; i < TPS; ++i) {
-        pre *= al[i];
-        E2[(seg * TPS + i) * ld + c] = pre * inv_mu;
-    }
-    __syncthreads();
-}
-
 // A = beta (Kr Kc^T) strictly lower and P = Qr Kc^T lower incl. diagonal, in
 // fp32 on CUDA cores. Ends with a barrier.
 template <int DK> __device__ void wy_products(Tables<DK> &tb) {
@@ -191,11 +156,14 @@ template <int DK> __device__ void wy_products(Tables<DK> &tb) {
     __syncthreads();
 }
 
-// T = (I + A)^{-1} for the strictly lower A in tb.A (forward substitution on
-// 16 x 16 blocks, then block products). Leaves A's upper triangle
-// overwritten. Ends with a barrier.
-template <int DK> __device__ void invert_a(Tables<DK> &tb) {
-    constexpr int LDC = Tables<DK>::LDC;
+// T = (I + A)^{-1} for a strictly lower A ([C][C + 4] tiles in shared
+// memory; forward substitution on 16 x 16 blocks, then block products).
+// Leaves A's upper triangle overwritten. Ends with a barrier.
+struct TPair {
+    float *A, *T;
+};
+__device__ inline void invert_unit_lower(TPair tb) {
+    constexpr int LDC = C + 4;
     const int tid = threadIdx.x;
     // T = (I + A)^{-1} by blocks of 16 (A strictly lower, so T is unit lower):
     //   the four diagonal blocks by forward substitution, one thread per column;
@@ -264,7 +232,7 @@ template <int DK> __device__ void invert_a(Tables<DK> &tb) {
 // The WY tables of a chunk whose gated tables are in tb: A, P, then T.
 template <int DK> __device__ void wy_tables(Tables<DK> &tb) {
     wy_products<DK>(tb);
-    invert_a<DK>(tb);
+    invert_unit_lower(TPair{tb.A, tb.T});
 }
 
 }  // namespace simt
