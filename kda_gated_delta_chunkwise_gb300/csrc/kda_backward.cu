@@ -147,7 +147,6 @@ template <int DK> struct TabLayout {
     static constexpr int KR = 0, QR = C * DK, KC = 2 * C * DK, T = 3 * C * DK, P = T + C * C, MU = P + C * C,
                          BETA = MU + DK, SLOW = BETA + C, FLOATS = SLOW + 4;
 };
-enum TabPart : unsigned { TAB_KR = 1, TAB_QR = 2, TAB_KC = 4, TAB_T = 8, TAB_P = 16, TAB_ALL = 31 };
 
 // 16 bytes global -> shared without a register round trip (cp.async), so
 // that every thread has all its loads of a table in flight at once.
@@ -182,32 +181,6 @@ __device__ __forceinline__ void prefetch_rows(const TIn *src, int64_t tok0, int 
 }
 // The padded row of such a tile (elements): 16-byte rows, conflict-free reads.
 template <typename TIn> struct RowTile { static constexpr int LD = sizeof(TIn) == 4 ? VS + 4 : VS + 8; };
-
-// Loads the parts `which` (TAB_*) of a chunk's tables, plus mu, beta and the
-// slow flag; T and P only when the chunk is not slow. Ends with a barrier.
-template <int DK> __device__ void load_tables(simt::Tables<DK> &tb, const float *src, unsigned which) {
-    using L = TabLayout<DK>;
-    constexpr int LDK = simt::Tables<DK>::LDK, LDC = simt::Tables<DK>::LDC, Q4 = DK / 4, C4 = C / 4;
-    const int tid = threadIdx.x;
-    const int slow = __float_as_int(src[L::SLOW]);
-    for (int e = tid; e < C * Q4; e += NT) {
-        const int r = e / Q4, c = 4 * (e % Q4);
-        if (which & TAB_KR) cp16(&tb.Kr[r * LDK + c], src + L::KR + r * DK + c);
-        if (which & TAB_QR) cp16(&tb.Qr[r * LDK + c], src + L::QR + r * DK + c);
-        if (which & TAB_KC) cp16(&tb.Kc[r * LDK + c], src + L::KC + r * DK + c);
-    }
-    if (!slow)
-        for (int e = tid; e < C * C4; e += NT) {
-            const int r = e / C4, c = 4 * (e % C4);
-            if (which & TAB_T) cp16(&tb.T[r * LDC + c], src + L::T + r * C + c);
-            if (which & TAB_P) cp16(&tb.P[r * LDC + c], src + L::P + r * C + c);
-        }
-    for (int e = tid; e < DK / 4; e += NT) cp16(&tb.mu[4 * e], src + L::MU + 4 * e);
-    for (int e = tid; e < C / 4; e += NT) cp16(&tb.beta[4 * e], src + L::BETA + 4 * e);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    if (tid == 0) tb.slow = slow;
-    __syncthreads();
-}
 
 // Pulls a chunk's tables into L2 ahead of their use (128-byte lines).
 template <int DK> __device__ __forceinline__ void prefetch_tables(const float *src) {
@@ -500,20 +473,94 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
     }
 }
 
-// ---------------------------------------------------------------- states
-// The forward chain only: one CTA per (sequence, head, value slice) writes the
-// state before every chunk (S_{n+1} = Diag(mu) (Diag(mu) S_n + Kc^T U), U =
-// T Diag(beta) (V - Kr Diag(mu) S_n)) and the chunk's U and V - X, reading the
-// chunk's tables; slow chunks go token by token (the §四 update) and write no
-// U or V - X. Products on the tensor cores (wmm).
-template <int DK> struct StatesSmem {
-    float S[DK * LDC];  // the state slice, rows of LDC
-    simt::Tables<DK> tb;
-    float R[C * LDC];
-    float U[C * LDC];
+// ---------------------------------------------------------------- chains
+// The two serial passes keep every tile in shared memory with a row stride
+// picked for the way the mma fragments read it: = 4 (mod 32) floats for a
+// tile read along its rows (A operands, row-major; B operands stored
+// [n][k]), = 8 (mod 32) for a tile read down its columns (transposed A
+// operands; B operands stored [k][n]; accumulator tiles written two columns
+// at a time). Either way the 32 lanes of a fragment load hit 32 banks.
+constexpr int LR = C + 4;   // a [C][C] tile read along rows
+constexpr int LS = VS + 8;  // a [rows][VS] value tile read down its columns / written as accumulators
+template <int DK> struct Ld {
+    static constexpr int ROW = DK + 4, COL = DK + 8;  // [C][DK] tiles read along rows / down columns
 };
-static_assert(offsetof(StatesSmem<128>, tb) % 16 == 0 && offsetof(StatesSmem<64>, tb) % 16 == 0,
-              "16-byte offsets");
+// dO or v tile (qkv type) read down its columns: 16-byte rows, conflict-free.
+template <typename TIn> struct ColTile { static constexpr int LD = sizeof(TIn) == 4 ? VS + 8 : VS + 16; };
+
+// cp.async of a [rows][cols] fp32 tile (cols a multiple of 4) from rows of
+// sld floats into shared rows of ld floats; not committed.
+__device__ __forceinline__ void cp_tile(float *dst, int ld, const float *src, int sld, int rows, int cols) {
+    const int q4 = cols / 4;
+    for (int e = threadIdx.x; e < rows * q4; e += NT) {
+        const int r = e / q4, c = 4 * (e % q4);
+        cp16(dst + r * ld + c, src + (int64_t)r * sld + c);
+    }
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N> __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// A fragment of a transposed operand: A(m, k) = x[k][m].
+template <bool SPLIT, typename TS>
+__device__ __forceinline__ void afragT(const TS *x, int ld, int r0, int k, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float v[4] = {to_f32(x[(k + t) * ld + r0 + g]), to_f32(x[(k + t) * ld + r0 + g + 8]),
+                        to_f32(x[(k + t + 4) * ld + r0 + g]), to_f32(x[(k + t + 4) * ld + r0 + g + 8])};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (SPLIT) split_tf32(v[u], hi[u], lo[u]);
+        else hi[u] = tf32_bits(v[u]), lo[u] = 0u;
+    }
+}
+// acc[nt] += A B over K for the warp tile at (r0, c0): A from fa(k, hi, lo)
+// (a fragment loader), B(k, n) = x[k][n] times the row factor f[k] (or 1
+// when f is null).
+template <int K, int NT8, bool SPLIT, typename FA, typename TS>
+__device__ __forceinline__ void mm_kn(float (&acc)[NT8][4], FA fa, const TS *x, int ld, const float *f, int r0, int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+    for (int k = 0; k < K; k += 8) {
+        uint32_t ah[4], al[4];
+        fa(k, ah, al);
+        const float f0 = f ? f[k + t] : 1.f, f1 = f ? f[k + t + 4] : 1.f;
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+            const int n = c0 + 8 * nt + g;
+            const BFrag b = bfrag<SPLIT>(f0 * to_f32(x[(k + t) * ld + n]), f1 * to_f32(x[(k + t + 4) * ld + n]));
+            mma_f<SPLIT>(acc[nt], ah, al, b);
+        }
+    }
+}
+// Accumulator tile (r0, c0) into shared rows of ld floats, two columns per store.
+template <int NT8> __device__ __forceinline__ void sstore(const float (&acc)[NT8][4], int r0, int c0, float *dst, int ld) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+        const int c = c0 + 8 * nt + 2 * t;
+        *reinterpret_cast<float2 *>(dst + (r0 + g) * ld + c) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2 *>(dst + (r0 + g + 8) * ld + c) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+}
+// x[r][c] <- mu[r] (mu[r] x[r][c] + acc) for the accumulator tile (r0, c0) of
+// shared rows of ld floats: the state and state-gradient updates.
+template <int NT8>
+__device__ __forceinline__ void state_update(const float (&acc)[NT8][4], int r0, int c0, float *x, int ld, const float *mu) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float m0 = mu[r0 + g], m1 = mu[r0 + g + 8];
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+        const int c = c0 + 8 * nt + 2 * t;
+        float2 *a = reinterpret_cast<float2 *>(x + (r0 + g) * ld + c), *b = reinterpret_cast<float2 *>(x + (r0 + g + 8) * ld + c);
+        float2 va = *a, vb = *b;
+        va.x = m0 * (m0 * va.x + acc[nt][0]);
+        va.y = m0 * (m0 * va.y + acc[nt][1]);
+        vb.x = m1 * (m1 * vb.x + acc[nt][2]);
+        vb.y = m1 * (m1 * vb.y + acc[nt][3]);
+        *a = va;
+        *b = vb;
+    }
+}
 
 // Warp tiles of a DK x 64 product (the state slice): DK = 128 gives each warp
 // 16 rows and all 64 columns, DK = 64 16 rows and 32 columns.
@@ -523,14 +570,60 @@ template <int DK> struct StateTile {
     __device__ static int c0(int warp) { return DK == 128 ? 0 : 32 * (warp >> 2); }
 };
 
+// The per-chunk scalars of a chain step (double-buffered with its token tile).
+template <int DK> struct ChunkScalars {
+    float mu[DK];
+    float beta[C];
+    float flag[4];  // [0]: the slow flag's bits
+};
+// Issues the cp.async of a chunk's mu, beta and slow flag (not committed).
+template <int DK> __device__ __forceinline__ void cp_scalars(ChunkScalars<DK> &d, const float *tab) {
+    using TL = TabLayout<DK>;
+    const int tid = threadIdx.x;
+    if (tid < DK / 4) cp16(&d.mu[4 * tid], tab + TL::MU + 4 * tid);
+    else if (tid < DK / 4 + C / 4) cp16(&d.beta[4 * (tid - DK / 4)], tab + TL::BETA + 4 * (tid - DK / 4));
+    else if (tid == DK / 4 + C / 4) cp16(d.flag, tab + TL::SLOW);
+}
+
+// ---------------------------------------------------------------- states
+// The forward chain only: one CTA per (sequence, head, value slice) writes the
+// state before every chunk (S_{n+1} = Diag(mu) (Diag(mu) S_n + Kc^T U), U =
+// T Diag(beta) (V - Kr Diag(mu) S_n)) and the chunk's U and V - X, reading the
+// chunk's tables; slow chunks go token by token (the §四 update) and write no
+// U or V - X. Products on the tensor cores. Each table of the next chunk is
+// copied in (cp.async) as soon as this chunk is done with it, so the copies
+// run under this chunk's products: Kr after X, T after U, Kc after the state
+// update; mu, beta, the flag and v are double-buffered.
+template <int DK, typename TIn> struct StatesSmem {
+    float S[DK * LS];  // the state slice
+    float Kr[C * Ld<DK>::ROW];
+    float Kc[C * Ld<DK>::COL];
+    float T[C * LR];
+    float R[C * LS];
+    float U[C * LS];
+    TIn V[2][C * ColTile<TIn>::LD];
+    ChunkScalars<DK> sc[2];
+};
+
+// 16-byte offsets for cp.async (every tile and row is a multiple of 16 bytes)
+template <int DK, typename TIn> constexpr bool states_layout_ok() {
+    using S = StatesSmem<DK, TIn>;
+    return offsetof(S, Kr) % 16 == 0 && offsetof(S, Kc) % 16 == 0 && offsetof(S, T) % 16 == 0 &&
+           offsetof(S, R) % 16 == 0 && offsetof(S, U) % 16 == 0 && offsetof(S, V) % 16 == 0 &&
+           offsetof(S, sc) % 16 == 0 && sizeof(ChunkScalars<DK>) % 16 == 0 && (C * ColTile<TIn>::LD * sizeof(TIn)) % 16 == 0;
+}
+static_assert(states_layout_ok<128, float>() && states_layout_ok<128, __nv_bfloat16>() && states_layout_ok<64, float>() &&
+                  states_layout_ok<64, __nv_bfloat16>(),
+              "16-byte offsets");
+
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, const float *s0) {
     constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    StatesSmem<DK> &sm = *reinterpret_cast<StatesSmem<DK> *>(smem_raw);
-    simt::Tables<DK> &tb = sm.tb;
-    constexpr int LDK = simt::Tables<DK>::LDK;
+    using TL = TabLayout<DK>;
     using ST = StateTile<DK>;
+    constexpr int LKR = Ld<DK>::ROW, LKC = Ld<DK>::COL, LV = ColTile<TIn>::LD;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    StatesSmem<DK, TIn> &sm = *reinterpret_cast<StatesSmem<DK, TIn> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int nslices = p.DV / VS;
     const int slice = blockIdx.x % nslices;
@@ -545,99 +638,146 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
     const TIn *k = (const TIn *)p.k, *v = (const TIn *)p.v;
     int64_t wbase, wstride;
     slots_of(p, n, h, cbase, wbase, wstride);
-    float *st = p.states + wbase * DK * DV;                    // chunk i at slot wbase + i wstride
+    float *st = p.states + wbase * DK * DV;  // chunk i at slot wbase + i wstride
     float *wkb = p.work + wbase * 4 * C * DV;
-    const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
-    TIn *Vt = reinterpret_cast<TIn *>(tb.Qr);  // the chunk's v (Qr is not loaded here)
-    constexpr int LDV = RowTile<TIn>::LD;
-    static_assert(C * LDV * sizeof(TIn) <= sizeof(tb.Qr), "the v tile fits in Qr's place");
+    const float *tabs = p.tabs + wbase * TL::FLOATS;
+    auto tab = [&](int i) { return tabs + (int64_t)i * wstride * TL::FLOATS; };
+    auto len = [&](int i) { return (int)((T - (int64_t)i * C) < C ? (T - (int64_t)i * C) : (int64_t)C); };
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
+    // chunk i's copies, in three groups: (scalars, v, Kr), (T), (Kc)
+    auto issue_a = [&](int i) {
+        if (i < NC) {
+            cp_scalars<DK>(sm.sc[i & 1], tab(i));
+            load_rows<TIn>(sm.V[i & 1], LV, v, t_begin + (int64_t)i * C, len(i), H, h, DV, v0);
+            cp_tile(sm.Kr, LKR, tab(i) + TL::KR, DK, C, DK);
+        }
+        cp_commit();
+    };
+    auto issue_b = [&](int i) {
+        if (i < NC) cp_tile(sm.T, LR, tab(i) + TL::T, C, C, C);
+        cp_commit();
+    };
+    auto issue_c = [&](int i) {
+        if (i < NC) cp_tile(sm.Kc, LKC, tab(i) + TL::KC, DK, C, DK);
+        cp_commit();
+    };
     for (int e = tid; e < DK * VS; e += NT)
-        sm.S[(e / VS) * LDC + e % VS] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
-    __syncthreads();
+        sm.S[(e / VS) * LS + e % VS] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    issue_a(0);
+    issue_b(0);
+    issue_c(0);
     for (int ci = 0; ci < NC; ++ci) {
         const int64_t t0 = (int64_t)ci * C, tok0 = t_begin + t0;
-        const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
+        const int L = len(ci);
+        ChunkScalars<DK> &cs = sm.sc[ci & 1];
+        const TIn *Vt = sm.V[ci & 1];
+        cp_wait<1>();  // this chunk's scalars, v, Kr and T (Kc may still be on its way)
+        __syncthreads();
         for (int e = tid; e < DK * VS; e += NT)
-            st[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LDC + e % VS];
-        load_rows<TIn>(Vt, LDV, v, tok0, L, H, h, DV, v0);  // completes with the tables
-        load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_KR | TAB_KC | TAB_T);
-        if (ci + 1 < NC) {
-            prefetch_tables<DK>(tabs + (ci + 1) * wstride * TabLayout<DK>::FLOATS);
-            const int64_t tn = t0 + C;
-            prefetch_rows<TIn>(v, tok0 + C, (int)((T - tn) < C ? (T - tn) : (int64_t)C), H, h, DV, v0);
+            st[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LS + e % VS];
+        if (ci + 2 < NC) {  // two chunks ahead into L2
+            prefetch_tables<DK>(tab(ci + 2));
+            prefetch_rows<TIn>(v, tok0 + 2 * C, len(ci + 2), H, h, DV, v0);
         }
-        if (tb.slow) {
+        if (__float_as_int(cs.flag[0])) {
             const int j = tid % VS, part = tid / VS;
             for (int r = 0; r < L; ++r) {
                 const int64_t tk = (tok0 + r) * H + h;
                 float vh = 0.f;
                 for (int c = part; c < DK; c += NT / VS)
-                    vh += gate_at(p.alpha, p.gate, tk, c, DK) * ld_in(k, tk * DK + c) * sm.S[c * LDC + j];
-                sm.R[part * LDC + j] = vh;
+                    vh += gate_at(p.alpha, p.gate, tk, c, DK) * ld_in(k, tk * DK + c) * sm.S[c * LS + j];
+                sm.R[part * LS + j] = vh;
                 __syncthreads();
                 float vs = 0.f;
 #pragma unroll
-                for (int p2 = 0; p2 < NT / VS; ++p2) vs += sm.R[p2 * LDC + j];
+                for (int p2 = 0; p2 < NT / VS; ++p2) vs += sm.R[p2 * LS + j];
                 const float be = p.beta[tk] * (ld_in(v, tk * DV + v0 + j) - vs);
                 __syncthreads();
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.S[c * LDC + j] = gate_at(p.alpha, p.gate, tk, c, DK) * sm.S[c * LDC + j] + ld_in(k, tk * DK + c) * be;
+                    sm.S[c * LS + j] = gate_at(p.alpha, p.gate, tk, c, DK) * sm.S[c * LS + j] + ld_in(k, tk * DK + c) * be;
                 __syncthreads();
             }
+            cp_wait<0>();  // nothing of this chunk's copies is in flight before the slots are refilled
+            __syncthreads();
+            issue_a(ci + 1);
+            issue_b(ci + 1);
+            issue_c(ci + 1);
             continue;
         }
         float *wk = wkb + ci * wstride * 4 * C * DV + v0;  // this chunk's U, V - X (the slice's columns)
         float acc[4][4];
-        // R = Diag(beta) (V - Kr St); V - X into the workspace
+        // X = Kr St (St = Diag(mu) S); V - X into the workspace; R = Diag(beta) (V - X)
         fzero<4>(acc);
-        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kr[r * LDK + c]; },
-                   [&](int c, int j) { return tb.mu[c] * sm.S[c * LDC + j]; }, R0, C0);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-            x = to_f32(Vt[r * LDV + c]) - x;
-            sm.R[r * LDC + c] = tb.beta[r] * x;
-        });
+        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.Kr, LKR, R0, kx, hi, lo); },
+                            sm.S, LS, cs.mu, R0, C0);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { x = to_f32(Vt[r * LV + c]) - x; });
         gstore<4>(acc, R0, C0, wk + C * DV, DV);
+        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { x *= cs.beta[r]; });
+        sstore<4>(acc, R0, C0, sm.R, LS);
         __syncthreads();
+        issue_a(ci + 1);  // Kr is free
         // U = T R, also into the workspace
         fzero<4>(acc);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[r * LDC + m]; }, [&](int m, int j) { return sm.R[m * LDC + j]; }, R0,
-                  C0);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { sm.U[r * LDC + c] = x; });
+        mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.T, LR, R0, kx, hi, lo); },
+                           sm.R, LS, (const float *)nullptr, R0, C0);
+        sstore<4>(acc, R0, C0, sm.U, LS);
         gstore<4>(acc, R0, C0, wk, DV);
+        cp_wait<1>();  // Kc (the group of the next chunk's scalars, v and Kr may be pending)
         __syncthreads();
+        issue_b(ci + 1);  // T is free
         // S <- Diag(mu) (Diag(mu) S + Kc^T U)
         float acc2[ST::N8][4];
         fzero<ST::N8>(acc2);
-        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Kc[r * LDK + c]; }, [&](int r, int j) { return sm.U[r * LDC + j]; },
-                       SR0, SC0);
-        ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
-            const float m = tb.mu[c];
-            float &sv = sm.S[c * LDC + j];
-            sv = m * (m * sv + x);
-        });
+        mm_kn<C, ST::N8, SPLIT>(acc2, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.Kc, LKC, SR0, kx, hi, lo); },
+                                sm.U, LS, (const float *)nullptr, SR0, SC0);
+        state_update<ST::N8>(acc2, SR0, SC0, sm.S, LS, cs.mu);
         __syncthreads();
+        issue_c(ci + 1);  // Kc is free
     }
+    cp_wait<0>();
 }
 
 // ---------------------------------------------------------------- chain
-template <int DK> struct ChainSmem {
-    float G[DK * LDC];  // dL/dS slice, rows of LDC
-    simt::Tables<DK> tb;
-    float dO[C * LDC];  // holds the chunk's dO tile (qkv type, rows of RowTile::LD)
+// The reverse chain: one CTA per (sequence, head, value slice), chunks last to
+// first; writes dL/dS after every chunk, the chunk's dU and dR, dv, and dS_0.
+// The next chunk's tables are copied in as this chunk frees them: Kc and P
+// after dU, T after dR, Qr and Kr after the state-gradient update; mu, beta
+// and the flag are double-buffered, and so is dO for bf16 inputs (for fp32
+// inputs a second fp32 dO tile does not fit: it comes with Qr and Kr).
+template <typename TIn> struct ChainDo { static constexpr int BUFS = sizeof(TIn) == 4 ? 1 : 2; };
+template <int DK, typename TIn> struct ChainSmem {
+    float G[DK * LS];  // dL/dS slice
+    float Kc[C * Ld<DK>::ROW];
+    float P[C * LS];   // read transposed
+    float T[C * LS];   // read transposed
+    float dU[C * LS];
+    float Qr[C * Ld<DK>::COL];
+    float Kr[C * Ld<DK>::COL];
+    TIn dO[ChainDo<TIn>::BUFS][C * ColTile<TIn>::LD];
+    ChunkScalars<DK> sc[2];
     float red[4 * VS];
 };
-static_assert(offsetof(ChainSmem<128>, tb) % 16 == 0 && offsetof(ChainSmem<64>, tb) % 16 == 0, "16-byte offsets");
+
+template <int DK, typename TIn> constexpr bool chain_layout_ok() {
+    using S = ChainSmem<DK, TIn>;
+    return offsetof(S, Kc) % 16 == 0 && offsetof(S, P) % 16 == 0 && offsetof(S, T) % 16 == 0 &&
+           offsetof(S, dU) % 16 == 0 && offsetof(S, Qr) % 16 == 0 && offsetof(S, Kr) % 16 == 0 &&
+           offsetof(S, dO) % 16 == 0 && offsetof(S, sc) % 16 == 0;
+}
+static_assert(chain_layout_ok<128, float>() && chain_layout_ok<128, __nv_bfloat16>() && chain_layout_ok<64, float>() &&
+                  chain_layout_ok<64, __nv_bfloat16>(),
+              "16-byte offsets");
 
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     constexpr bool SPLIT = std::is_same<TIn, float>::value;  // fp32 inputs: fp32 accuracy
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ChainSmem<DK> &sm = *reinterpret_cast<ChainSmem<DK> *>(smem_raw);
-    simt::Tables<DK> &tb = sm.tb;
-    constexpr int LDK = simt::Tables<DK>::LDK;
+    using TL = TabLayout<DK>;
     using ST = StateTile<DK>;
+    constexpr int LKR = Ld<DK>::ROW, LQK = Ld<DK>::COL, LD = ColTile<TIn>::LD, LP = LS;
+    constexpr bool DB = ChainDo<TIn>::BUFS == 2;  // dO double-buffered
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ChainSmem<DK, TIn> &sm = *reinterpret_cast<ChainSmem<DK, TIn> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int nslices = p.DV / VS;
     const int slice = blockIdx.x % nslices;
@@ -652,41 +792,68 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     const int64_t sh = (int64_t)n * H + h;
     int64_t wbase, wstride;
     slots_of(p, n, h, cbase, wbase, wstride);
-    float *gn = p.gnext + wbase * DK * DV;                     // chunk i at slot wbase + i wstride
+    float *gn = p.gnext + wbase * DK * DV;  // chunk i at slot wbase + i wstride
     float *wkb = p.work + wbase * 4 * C * DV;
-    const float *tabs = p.tabs + wbase * TabLayout<DK>::FLOATS;
-    TIn *dOt = reinterpret_cast<TIn *>(sm.dO);  // the chunk's dO, rows of LDD elements
-    constexpr int LDD = RowTile<TIn>::LD;
-    static_assert(C * LDD * sizeof(TIn) <= sizeof(sm.dO), "the dO tile fits");
+    const float *tabs = p.tabs + wbase * TL::FLOATS;
+    auto tab = [&](int i) { return tabs + (int64_t)i * wstride * TL::FLOATS; };
+    auto len = [&](int i) { return (int)((T - (int64_t)i * C) < C ? (T - (int64_t)i * C) : (int64_t)C); };
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     const int SR0 = ST::r0(warp), SC0 = ST::c0(warp);
+    // chunk i's copies, in three groups: (scalars, dO, Kc, P), (T), (Qr, Kr)
+    // (a single dO tile comes with Qr and Kr)
+    auto issue_a = [&](int i) {
+        if (i >= 0) {
+            cp_scalars<DK>(sm.sc[i & 1], tab(i));
+            if (DB) load_rows<TIn>(sm.dO[i & 1], LD, dO, t_begin + (int64_t)i * C, len(i), H, h, DV, v0);
+            cp_tile(sm.Kc, LKR, tab(i) + TL::KC, DK, C, DK);
+            cp_tile(sm.P, LP, tab(i) + TL::P, C, C, C);
+        }
+        cp_commit();
+    };
+    auto issue_b = [&](int i) {
+        if (i >= 0) cp_tile(sm.T, LS, tab(i) + TL::T, C, C, C);
+        cp_commit();
+    };
+    auto issue_c = [&](int i) {
+        if (i >= 0) {
+            cp_tile(sm.Qr, LQK, tab(i) + TL::QR, DK, C, DK);
+            cp_tile(sm.Kr, LQK, tab(i) + TL::KR, DK, C, DK);
+            if (!DB) load_rows<TIn>(sm.dO[0], LD, dO, t_begin + (int64_t)i * C, len(i), H, h, DV, v0);
+        }
+        cp_commit();
+    };
 
     for (int e = tid; e < DK * VS; e += NT)
-        sm.G[(e / VS) * LDC + e % VS] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
-    __syncthreads();
+        sm.G[(e / VS) * LS + e % VS] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    issue_a(NC - 1);
+    issue_b(NC - 1);
+    issue_c(NC - 1);
 
     for (int ci = NC - 1; ci >= 0; --ci) {
         const int64_t t0 = (int64_t)ci * C;
-        const int L = (int)((T - t0) < C ? (T - t0) : (int64_t)C);
+        const int L = len(ci);
         const int64_t tok0 = t_begin + t0;
+        ChunkScalars<DK> &cs = sm.sc[ci & 1];
+        const TIn *dOt = sm.dO[DB ? (ci & 1) : 0];
+        if (DB) cp_wait<2>();  // this chunk's scalars, dO, Kc and P (T, Qr and Kr may still be on their way)
+        else cp_wait<0>();
+        __syncthreads();
         for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
-            gn[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
-        load_rows<TIn>(dOt, LDD, dO, tok0, L, H, h, DV, v0);  // completes with the tables
-        load_tables<DK>(tb, tabs + ci * wstride * TabLayout<DK>::FLOATS, TAB_ALL);  // (ends with a barrier)
-        if (ci > 0) {
-            prefetch_tables<DK>(tabs + (ci - 1) * wstride * TabLayout<DK>::FLOATS);
-            prefetch_rows<TIn>(dO, tok0 - C, C, H, h, DV, v0);
+            gn[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LS + e % VS];
+        if (ci >= 2) {  // two chunks ahead into L2
+            prefetch_tables<DK>(tab(ci - 2));
+            prefetch_rows<TIn>(dO, tok0 - 2 * C, C, H, h, DV, v0);
         }
-        if (tb.slow) {
+        if (__float_as_int(cs.flag[0])) {
             // token by token, last token first: G += q do^T; w = G^T k; G = Diag(alpha)(G - beta k w^T)
             const int j = tid % VS, part = tid / VS;
             for (int r = L - 1; r >= 0; --r) {
                 const int64_t tk = (tok0 + r) * H + h;
-                const float dj = to_f32(dOt[r * LDD + j]);
+                const float dj = to_f32(dOt[r * LD + j]);
                 float wp = 0.f;
                 for (int c = part; c < DK; c += NT / VS) {
-                    const float g = sm.G[c * LDC + j] + ld_in(q, tk * DK + c) * dj;
-                    sm.G[c * LDC + j] = g;
+                    const float g = sm.G[c * LS + j] + ld_in(q, tk * DK + c) * dj;
+                    sm.G[c * LS + j] = g;
                     wp += ld_in(k, tk * DK + c) * g;
                 }
                 sm.red[part * VS + j] = wp;
@@ -696,50 +863,59 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
                 for (int p2 = 0; p2 < NT / VS; ++p2) w += sm.red[p2 * VS + j];
                 const float bt = p.beta[tk];
                 for (int c = part; c < DK; c += NT / VS)
-                    sm.G[c * LDC + j] = gate_at(p.alpha, p.gate, tk, c, DK) * (sm.G[c * LDC + j] - bt * ld_in(k, tk * DK + c) * w);
+                    sm.G[c * LS + j] = gate_at(p.alpha, p.gate, tk, c, DK) * (sm.G[c * LS + j] - bt * ld_in(k, tk * DK + c) * w);
                 __syncthreads();
             }
+            cp_wait<0>();  // nothing of this chunk's copies is in flight before the slots are refilled
+            __syncthreads();
+            issue_a(ci - 1);
+            issue_b(ci - 1);
+            issue_c(ci - 1);
             continue;
         }
-        float *dU = tb.A;  // a work tile here
         float *wk = wkb + ci * wstride * 4 * C * DV + v0;  // this chunk's dU, dR (the slice's columns)
         float acc[4][4];
-        // dU = Kc Gt + P^T dO, also into the workspace
+        // dU = Kc Gt + P^T dO (Gt = Diag(mu) G), also into the workspace
         fzero<4>(acc);
-        wmm<DK, 4, SPLIT>(acc, [&](int r, int c) { return tb.Kc[r * LDK + c]; },
-                   [&](int c, int j) { return tb.mu[c] * sm.G[c * LDC + j]; }, R0, C0);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.P[m * LDC + r]; },
-                         [&](int m, int j) { return to_f32(dOt[m * LDD + j]); }, R0, C0);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { dU[r * LDC + c] = x; });
+        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.Kc, LKR, R0, kx, hi, lo); },
+                            sm.G, LS, cs.mu, R0, C0);
+        mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.P, LP, R0, kx, hi, lo); },
+                           dOt, LD, (const float *)nullptr, R0, C0);
+        sstore<4>(acc, R0, C0, sm.dU, LS);
         gstore<4>(acc, R0, C0, wk + 2 * C * DV, DV);
+        cp_wait<1>();  // T (the group of Qr and Kr may be pending)
         __syncthreads();
+        issue_a(ci - 1);  // Kc and P are free
         // dR = T^T dU into the workspace; dv = Diag(beta) dR; dX = -Diag(beta) dR (into dU's place)
         fzero<4>(acc);
-        wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return tb.T[m * LDC + r]; }, [&](int m, int j) { return dU[m * LDC + j]; }, R0, C0);
+        mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.T, LS, R0, kx, hi, lo); },
+                           sm.dU, LS, (const float *)nullptr, R0, C0);
         gstore<4>(acc, R0, C0, wk + 3 * C * DV, DV);
-        __syncthreads();
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = tb.beta[r] * x;
-            dU[r * LDC + c] = -tb.beta[r] * x;
+            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = cs.beta[r] * x;
+            x *= -cs.beta[r];
         });
+        cp_wait<1>();  // Qr and Kr (the next chunk's first group may be pending)
+        __syncthreads();  // every read of dU is done; Qr and Kr have landed
+        sstore<4>(acc, R0, C0, sm.dU, LS);
+        issue_b(ci - 1);  // T is free
         __syncthreads();
         // G <- Diag(mu) (Gt + Qr^T dO + Kr^T dX)
         float acc2[ST::N8][4];
         fzero<ST::N8>(acc2);
-        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Qr[r * LDK + c]; },
-                       [&](int r, int j) { return to_f32(dOt[r * LDD + j]); }, SR0, SC0);
-        wmm<C, ST::N8, SPLIT>(acc2, [&](int c, int r) { return tb.Kr[r * LDK + c]; }, [&](int r, int j) { return dU[r * LDC + j]; },
-                       SR0, SC0);
-        ffor<ST::N8>(acc2, SR0, SC0, [&](int c, int j, float &x) {
-            const float m = tb.mu[c];
-            float &gv = sm.G[c * LDC + j];
-            gv = m * (m * gv + x);
-        });
+        mm_kn<C, ST::N8, SPLIT>(acc2, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.Qr, LQK, SR0, kx, hi, lo); },
+                                dOt, LD, (const float *)nullptr, SR0, SC0);
+        mm_kn<C, ST::N8, SPLIT>(acc2, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.Kr, LQK, SR0, kx, hi, lo); },
+                                sm.dU, LS, (const float *)nullptr, SR0, SC0);
+        state_update<ST::N8>(acc2, SR0, SC0, sm.G, LS, cs.mu);
         __syncthreads();
+        issue_c(ci - 1);  // Qr and Kr are free
     }
+    cp_wait<0>();
+    __syncthreads();
     if (p.ds0)
         for (int e = tid; e < DK * VS; e += NT)
-            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LDC + e % VS];
+            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LS + e % VS];
 }
 
 // ---------------------------------------------------------------- local
@@ -1208,7 +1384,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 }
 
 constexpr size_t kMaxSmem = 232448;  // dynamic shared memory one CTA may have
-static_assert(sizeof(StatesSmem<128>) <= kMaxSmem && sizeof(ChainSmem<128>) <= kMaxSmem &&
+static_assert(sizeof(StatesSmem<128, float>) <= kMaxSmem && sizeof(StatesSmem<128, __nv_bfloat16>) <= kMaxSmem &&
+                  sizeof(ChainSmem<128, float>) <= kMaxSmem && sizeof(ChainSmem<128, __nv_bfloat16>) <= kMaxSmem &&
                   sizeof(LocalSmem<128, float>) <= kMaxSmem && sizeof(LocalSmem<128, __nv_bfloat16>) <= kMaxSmem &&
                   sizeof(simt::Tables<128>) <= kMaxSmem,
               "shared memory per CTA");
@@ -1305,7 +1482,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // 2. the state before every chunk
         auto stk = kda_bwd_states_kernel<DK, TIn>;
-        const size_t ss = sizeof(StatesSmem<DK>);
+        const size_t ss = sizeof(StatesSmem<DK, TIn>);
         if ((e = cudaFuncSetAttribute(stk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss)) != cudaSuccess)
             return e;
         stk<<<heads, NT, ss, s>>>(p, b.s0);
@@ -1313,7 +1490,7 @@ cudaError_t launch_t(const BackwardArgs &b, cudaStream_t s) {
     }
     // 3. the reverse state-gradient chain (also for empty sequences: dS_0 = dS_T)
     auto chain = kda_bwd_chain_kernel<DK, TIn>;
-    const size_t sc = sizeof(ChainSmem<DK>);
+    const size_t sc = sizeof(ChainSmem<DK, TIn>);
     if ((e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc)) != cudaSuccess) return e;
     chain<<<heads, NT, sc, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
