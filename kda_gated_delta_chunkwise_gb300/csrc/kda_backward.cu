@@ -387,6 +387,20 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const int cl = tid % GS::CH, seg = tid / GS::CH;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
+    // the chunk's rows of alpha, k and q into L2: the second half of the
+    // channels is read after the first half's products
+    {
+        constexpr int LA = DK * 4 / 128, LK = DK * (int)sizeof(TIn) / 128;  // 128-byte lines per row
+        const int la = p.gate == KDA_GATE_CHANNEL ? LA : 0, per = la + 2 * LK;
+        for (int l = tid; l < L * per; l += NT) {
+            const int r = l / per, u = l % per;
+            const int64_t th = (tok0 + r) * H + h;
+            const void *a = u < la ? (const void *)(p.alpha + th * DK + 32 * u)
+                            : u < la + LK ? (const void *)(k + th * DK + (128 / sizeof(TIn)) * (u - la))
+                                          : (const void *)(q + th * DK + (128 / sizeof(TIn)) * (u - la - LK));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+    }
     if (tid == 0) sm.slow = 0;
     if (tid < C) sm.beta[tid] = tid < L ? p.beta[(tok0 + tid) * H + h] : 0.f;
     float accA[4][4], accP[4][4];
@@ -421,26 +435,28 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
         if (gamma < simt::kMinGamma) sm.slow = 1;
         const float mu = sqrtf(gamma), inv_mu = 1.f / mu;
         if (seg == 0) dst[TL::MU + c] = mu;
-        float suf[GS::TPS];  // exclusive suffix products within the segment, times the later segments
+        // Kc from the exclusive suffix products (within the segment, times the
+        // later segments), last row first; then Kr, Qr from the prefix products
         float s_acc = after;
 #pragma unroll
         for (int i = GS::TPS - 1; i >= 0; --i) {
-            suf[i] = s_acc;
+            const int r = seg * GS::TPS + i;
+            const float kc = kk[i] * (s_acc * inv_mu);
             s_acc *= al[i];
+            sm.Kc[r * LDH + cl] = kc;
+            dst[TL::KC + r * DK + c] = kc;
         }
         float pre = before;
 #pragma unroll
         for (int i = 0; i < GS::TPS; ++i) {
             const int r = seg * GS::TPS + i;
             pre *= al[i];
-            const float e2 = pre * inv_mu, e3 = suf[i] * inv_mu;
-            const float kr = kk[i] * e2, qr = qq[i] * e2, kc = kk[i] * e3;
+            const float e2 = pre * inv_mu;
+            const float kr = kk[i] * e2, qr = qq[i] * e2;
             sm.Kr[r * LDH + cl] = kr;
             sm.Qr[r * LDH + cl] = qr;
-            sm.Kc[r * LDH + cl] = kc;
             dst[TL::KR + r * DK + c] = kr;
             dst[TL::QR + r * DK + c] = qr;
-            dst[TL::KC + r * DK + c] = kc;
         }
         __syncthreads();
         // this half's share of [A; P] = [Kr; Qr] Kc^T (the two share the Kc fragments)
@@ -515,12 +531,15 @@ __device__ __forceinline__ void afragT(const TS *x, int ld, int r0, int k, uint3
 }
 // acc[nt] += A B over K for the warp tile at (r0, c0): A from fa(k, hi, lo)
 // (a fragment loader), B(k, n) = x[k][n] times the row factor f[k] (or 1
-// when f is null).
+// when f is null). Even and odd k-steps go to two accumulator sets (summed at
+// the end), so twice as many products are in flight.
 template <int K, int NT8, bool SPLIT, typename FA, typename TS>
 __device__ __forceinline__ void mm_kn(float (&acc)[NT8][4], FA fa, const TS *x, int ld, const float *f, int r0, int c0) {
+    static_assert(K % 16 == 0, "K in steps of 16");
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
-    for (int k = 0; k < K; k += 8) {
+    float acc2[NT8][4];
+    fzero<NT8>(acc2);
+    auto step = [&](int k, float(&d)[NT8][4]) {
         uint32_t ah[4], al[4];
         fa(k, ah, al);
         const float f0 = f ? f[k + t] : 1.f, f1 = f ? f[k + t + 4] : 1.f;
@@ -528,9 +547,18 @@ __device__ __forceinline__ void mm_kn(float (&acc)[NT8][4], FA fa, const TS *x, 
         for (int nt = 0; nt < NT8; ++nt) {
             const int n = c0 + 8 * nt + g;
             const BFrag b = bfrag<SPLIT>(f0 * to_f32(x[(k + t) * ld + n]), f1 * to_f32(x[(k + t + 4) * ld + n]));
-            mma_f<SPLIT>(acc[nt], ah, al, b);
+            mma_f<SPLIT>(d[nt], ah, al, b);
         }
+    };
+#pragma unroll 1
+    for (int k = 0; k < K; k += 16) {
+        step(k, acc);
+        step(k + 8, acc2);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 }
 // Accumulator tile (r0, c0) into shared rows of ld floats, two columns per store.
 template <int NT8> __device__ __forceinline__ void sstore(const float (&acc)[NT8][4], int r0, int c0, float *dst, int ld) {
