@@ -215,7 +215,7 @@ __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint
 template <int K, int NT8, bool SPLIT = true, typename FA, typename FB>
 __device__ __forceinline__ void wmm(float (&acc)[NT8][4], FA a, FB b, int r0, int c0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
+#pragma unroll 1
     for (int k = 0; k < K; k += 8) {
         uint32_t ah[4], al[4];
         const float av[4] = {a(r0 + g, k + t), a(r0 + g + 8, k + t), a(r0 + g, k + t + 4), a(r0 + g + 8, k + t + 4)};
@@ -1198,7 +1198,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         }
         __syncthreads();
         const LocalPiece<DK, TIn> &P = sm.u.piece[it & 1];
-#pragma unroll 1
+#pragma unroll 2
         for (int k = 0; k < VP; k += 8) {
             uint32_t oh[4], ol[4], rh[4], rl[4], uh[4], ul[4], dh[4], dl[4];
             afrag<SPLIT>(P.dO, DLD, R0, k, oh, ol);
