@@ -965,9 +965,9 @@ template <int DK, typename TIn> struct LocalPiece {
 };
 // What the last part of the local pass reads, in the pieces' place.
 template <int DK> struct LocalFinal {
-    float Kr[C * (DK + 4)];
-    float Qr[C * (DK + 4)];
-    float W[4][C * LDC];  // work tiles
+    float Kr[C * (DK + 8)];
+    float Qr[C * (DK + 8)];
+    float W[4][C * LS];  // work tiles: rows of LDC floats when read along rows, LS when read down columns
 };
 // The token path's buffers (local_slow), in the pieces' place.
 template <int DK> constexpr int slow_floats() { return 2 * DK * 128 + 2 * NT + 2 * 128 + 4 * NT + DK; }
@@ -978,7 +978,7 @@ template <int DK, typename TIn> struct LocalSmem {
         LocalFinal<DK> fin;
         float slow[slow_floats<DK>()];
     } u;
-    float Kc[C * (DK + 4)];
+    float Kc[C * (DK + 8)];
     float T[C * LDC];
     float mu[DK];
     float beta[C];
@@ -1113,7 +1113,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     LocalSmem<DK, TIn> &sm = *reinterpret_cast<LocalSmem<DK, TIn> *>(smem_raw);
     using TL = TabLayout<DK>;
-    constexpr int LDK = DK + 4;
+    constexpr int LDK = DK + 8;  // [C][DK] tables: read down their columns by the chunk-wide products
     constexpr int NK = DK / 16;  // 8-column tiles of a warp's half of a 64 x DK product
     constexpr int DLD = DoRow<TIn>::LD;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
@@ -1273,8 +1273,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
-    float *WA = F.W[0], *WC = F.W[2], *WD = F.W[3];
-    auto store = [&](float (&acc)[4][4], float *W) { ffor<4>(acc, R0, C0, [&](int r, int cc, float &x) { W[r * LDC + cc] = x; }); };
+    // W[0]: dT, then dA (rows of LDC); W[1]: lower(dP), then dA (rows of LS,
+    // for the transposed reads); W[2]: lower(dP) (rows of LDC); W[3]: Z (rows of LS)
+    float *WA = F.W[0], *WP = F.W[1], *WC = F.W[2], *WD = F.W[3];
     float acc[4][4];
     float db[2] = {0.f, 0.f};  // dbeta's second part, rows R0 + g, R0 + g + 8
     // the first parts of d log mu's column sums: Kc (U Gt^T), Qr (dO St^T), Kr (dX St^T)
@@ -1287,25 +1288,29 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             s123[nt][u] = sm.Kc[a0] * dKc[nt][u] + sm.Kc[a1] * dKc[nt][2 + u] + F.Qr[a0] * dQr[nt][u] +
                           F.Qr[a1] * dQr[nt][2 + u] + F.Kr[a0] * dKr[nt][u] + F.Kr[a1] * dKr[nt][2 + u];
         }
-    ffor<4>(dP, R0, C0, [&](int r, int cc, float &x) { WC[r * LDC + cc] = cc <= r ? x : 0.f; });  // lower(dP)
-    store(dT, WA);
+    ffor<4>(dP, R0, C0, [&](int r, int cc, float &x) { x = cc <= r ? x : 0.f; });  // lower(dP)
+    sstore<4>(dP, R0, C0, WC, LDC);
+    sstore<4>(dP, R0, C0, WP, LS);
+    sstore<4>(dT, R0, C0, WA, LDC);
     __syncthreads();
     // dQr += dP Kc;  dKc += dP^T Qr
     wmm<C, NK, SPLIT>(dQr, [&](int r, int m) { return WC[r * LDC + m]; }, [&](int m, int cc) { return sm.Kc[m * LDK + cc]; }, R0,
                       CK);
-    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return WC[m * LDC + r]; }, [&](int m, int cc) { return F.Qr[m * LDK + cc]; }, R0,
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return WP[m * LS + r]; }, [&](int m, int cc) { return F.Qr[m * LDK + cc]; }, R0,
                       CK);
-    // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA
+    // dA = strict-lower(-T^T dT T^T): Z = dT T^T -> WD, then -T^T Z -> WA (and WP)
     fzero<4>(acc);
     wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return WA[r * LDC + m]; }, [&](int m, int cc) { return sm.T[cc * LDC + m]; }, R0,
                      C0);
-    store(acc, WD);
+    sstore<4>(acc, R0, C0, WD, LS);
     __syncthreads();
     fzero<4>(acc);
-    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return sm.T[m * LDC + r]; }, [&](int m, int cc) { return WD[m * LDC + cc]; }, R0,
+    wmm<C, 4, SPLIT>(acc, [&](int r, int m) { return sm.T[m * LDC + r]; }, [&](int m, int cc) { return WD[m * LS + cc]; }, R0,
                      C0);
-    __syncthreads();  // every read of dT in WA is done
-    ffor<4>(acc, R0, C0, [&](int r, int cc, float &x) { WA[r * LDC + cc] = cc < r ? -x : 0.f; });
+    __syncthreads();  // every read of dT in WA and of lower(dP) in WP is done
+    ffor<4>(acc, R0, C0, [&](int r, int cc, float &x) { x = cc < r ? -x : 0.f; });
+    sstore<4>(acc, R0, C0, WA, LDC);
+    sstore<4>(acc, R0, C0, WP, LS);
     __syncthreads();
     // dKr += Diag(beta) dA Kc (and dbeta's second part Kr . (dA Kc));  dKc += (Diag(beta) dA)^T Kr
     {
@@ -1322,7 +1327,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
                 dKr[nt][e] += sm.beta[r] * tmp[nt][e];
             }
     }
-    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return sm.beta[m] * WA[m * LDC + r]; },
+    wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return sm.beta[m] * WP[m * LS + r]; },
                       [&](int m, int cc) { return F.Kr[m * LDK + cc]; }, R0, CK);
     // dbeta's second part: sums over this warp's columns (the 4 lanes of a
     // row), then the two column halves of each row and the first part, in a
@@ -1339,7 +1344,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // the chunk's gate factors p / mu (as in the forward tables) into the free
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = F.W[1];  // [C][LDK]: spans W[1] and W[2]
-    static_assert(C * LDK <= 2 * C * LDC, "E2 fits in two work tiles");
+    static_assert(C * LDK <= 2 * C * LS, "E2 fits in two work tiles");
     gate_factor_table<DK>(sm.part, sm.mu, E2, LDK, p.alpha, GATE, tok0, L, H, h);
     sm.part[(tid / DK) * DK + tid % DK] = sm.mu[tid % DK] * sm.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid] + dbr[2 * C + tid];
