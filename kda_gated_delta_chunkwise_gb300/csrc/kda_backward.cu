@@ -323,13 +323,14 @@ template <int DK> struct TabSmem {
     int slow;
 };
 
-// The gate factor p / mu of every row and channel of the chunk (the factor
-// that made Kr and Qr) into E2 ([C][ld] floats), with the arithmetic of the
-// tables pass, so the same bits. Needs the chunk's mu ([DK], shared memory);
-// uses part ([NT], shared memory) as scratch. Ends with a barrier.
+// The gate factors of every row and channel of the chunk, with the arithmetic
+// of the tables pass, so the same bits: p / mu (the factor that made Kr and
+// Qr) into E2 and mu / p (that of Kc: the later gates over mu) into E3, both
+// [C][ld] floats. Needs the chunk's mu ([DK], shared memory); uses part
+// ([NT], shared memory) as scratch. Ends with a barrier.
 template <int DK>
-__device__ void gate_factor_table(float *part, const float *mu, float *E2, int ld, const float *alpha, int gate,
-                                  int64_t tok0, int L, int H, int h) {
+__device__ void gate_factor_table(float *part, const float *mu, float *E2, float *E3, int ld, const float *alpha,
+                                  int gate, int64_t tok0, int L, int H, int h) {
     using GS = GateSplit<DK>;
     const int tid = threadIdx.x, cl = tid % GS::CH, seg = tid / GS::CH;
     for (int half = 0; half < 2; ++half) {
@@ -345,11 +346,20 @@ __device__ void gate_factor_table(float *part, const float *mu, float *E2, int l
         __syncthreads();  // earlier readers of part are done
         part[seg * GS::CH + cl] = prod;
         __syncthreads();
-        float before = 1.f;
+        float before = 1.f, after = 1.f;
 #pragma unroll
-        for (int s2 = 0; s2 < GS::SEG; ++s2)
-            if (s2 < seg) before *= part[s2 * GS::CH + cl];
+        for (int s2 = 0; s2 < GS::SEG; ++s2) {
+            const float pt = part[s2 * GS::CH + cl];
+            if (s2 < seg) before *= pt;
+            if (s2 > seg) after *= pt;
+        }
         const float inv_mu = 1.f / mu[c];
+        float s_acc = after;
+#pragma unroll
+        for (int i = GS::TPS - 1; i >= 0; --i) {
+            E3[(seg * GS::TPS + i) * ld + c] = s_acc * inv_mu;
+            s_acc *= al[i];
+        }
         float pre = before;
 #pragma unroll
         for (int i = 0; i < GS::TPS; ++i) {
@@ -1343,9 +1353,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     }
     // the chunk's gate factors p / mu (as in the forward tables) into the free
     // work tiles; dq, dk, and d log p into Qr's place
-    float *E2 = F.W[1];  // [C][LDK]: spans W[1] and W[2]
-    static_assert(C * LDK <= 2 * C * LS, "E2 fits in two work tiles");
-    gate_factor_table<DK>(sm.part, sm.mu, E2, LDK, p.alpha, GATE, tok0, L, H, h);
+    float *E2 = F.W[0], *E3 = F.W[2];  // [C][LDK] each: W[0..1] and W[2..3]
+    static_assert(C * LDK <= 2 * C * LS, "E2 and E3 fit in two work tiles each");
+    gate_factor_table<DK>(sm.part, sm.mu, E2, E3, LDK, p.alpha, GATE, tok0, L, H, h);
     sm.part[(tid / DK) * DK + tid % DK] = sm.mu[tid % DK] * sm.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid] + dbr[2 * C + tid];
     float dlogp[NK][4];
@@ -1354,7 +1364,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1), rc = r * LDK + cc;
-            const float e2 = E2[rc], e3 = 1.f / e2;  // p / mu and mu / p
+            const float e2 = E2[rc], e3 = E3[rc];  // p / mu and mu / p
             if (r < L) {
                 const int64_t th = (tok0 + r) * H + h;
                 p.dq[th * DK + cc] = dQr[nt][e] * e2;
@@ -1381,28 +1391,42 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             for (int u = 0; u < 2; ++u) sm.red[(warp & 3) * DK + CK + 8 * nt + 2 * t4 + u] = s123[nt][u];
     ffor<NK>(dlogp, R0, CK, [&](int r, int cc, float &x) { F.Qr[r * LDK + cc] = x; });
     __syncthreads();
-    // per channel: d log mu, then d log alpha by a reverse running sum over the rows
-    if (tid < DK) {
-        const int cc = tid;
-        float al[C];  // the channel's gates, every load in flight at once
+    // per channel: d log mu, then d log alpha by a reverse running sum over
+    // the rows; NT / DK threads per channel, each over a block of RH rows
+    {
+        constexpr int NH = NT / DK, RH = C / NH;
+        const int cc = tid % DK, hp = tid / DK, rb = hp * RH;
+        float al[RH];  // this block's gates, every load in flight at once
 #pragma unroll
-        for (int r = 0; r < C; ++r) al[r] = r < L ? gate_at(p.alpha, GATE, (tok0 + r) * H + h, cc, DK) : 1.f;
-        float s0c = 0.f;
-        for (int hp = 0; hp < NT / DK; ++hp) s0c += sm.part[hp * DK + cc];
+        for (int i = 0; i < RH; ++i)
+            al[i] = rb + i < L ? gate_at(p.alpha, GATE, (tok0 + rb + i) * H + h, cc, DK) : 1.f;
+        float *psum = F.W[0];  // [NH][DK]: d log p summed over each row block (E2 is read no more)
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < RH; ++i)
+            if (rb + i < L) ps += F.Qr[(rb + i) * LDK + cc];
+        psum[hp * DK + cc] = ps;
+        __syncthreads();
+        float s0c = 0.f, colsum = 0.f, later = 0.f;  // (sums in block order)
+        for (int h2 = 0; h2 < NH; ++h2) {
+            s0c += sm.part[h2 * DK + cc];
+            const float x = psum[h2 * DK + cc];
+            colsum += x;
+            if (h2 > hp) later += x;
+        }
         float s123c = 0.f;
         for (int t2 = 0; t2 < 4; ++t2) s123c += sm.red[t2 * DK + cc];
-        float colsum = 0.f;
-        for (int r = 0; r < L; ++r) colsum += F.Qr[r * LDK + cc];
         const float dlogmu = 2.f * s0c + s123c - colsum;
-        float run = 0.5f * dlogmu;
+        float run = 0.5f * dlogmu + later;  // d log p_{L-1} += d log mu / 2, plus the later blocks
 #pragma unroll
-        for (int r = C - 1; r >= 0; --r) {
+        for (int i = RH - 1; i >= 0; --i) {
+            const int r = rb + i;
             if (r < L) {
                 run += F.Qr[r * LDK + cc];
                 const int64_t th = (tok0 + r) * H + h;
-                const float da = run / al[r];
+                const float da = run / al[i];
                 if (GATE == KDA_GATE_CHANNEL) p.dalpha[th * DK + cc] = da;
-                else F.Qr[r * LDK + cc] = da;  // (this thread's own column, read only by itself above)
+                else F.Qr[r * LDK + cc] = da;  // (this thread's own rows and column, read only by itself)
             }
         }
     }
