@@ -600,6 +600,22 @@ __device__ __forceinline__ void state_update(const float (&acc)[NT8][4], int r0,
     }
 }
 
+// A rows x VS fp32 slice from shared rows of LS floats to global rows of DV
+// floats, and back (zeros for a null source); 16-byte moves.
+__device__ __forceinline__ void slice_store(float *g, const float *s, int rows, int DV) {
+    for (int e = threadIdx.x; e < rows * (VS / 4); e += NT) {
+        const int r = e / (VS / 4), c = 4 * (e % (VS / 4));
+        *reinterpret_cast<float4 *>(g + (int64_t)r * DV + c) = *reinterpret_cast<const float4 *>(s + r * LS + c);
+    }
+}
+__device__ __forceinline__ void slice_load(float *s, const float *g, int rows, int DV) {
+    for (int e = threadIdx.x; e < rows * (VS / 4); e += NT) {
+        const int r = e / (VS / 4), c = 4 * (e % (VS / 4));
+        *reinterpret_cast<float4 *>(s + r * LS + c) =
+            g ? *reinterpret_cast<const float4 *>(g + (int64_t)r * DV + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 // Warp tiles of a DK x 64 product (the state slice): DK = 128 gives each warp
 // 16 rows and all 64 columns, DK = 64 16 rows and 32 columns.
 template <int DK> struct StateTile {
@@ -700,8 +716,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         if (i < NC) cp_tile(sm.Kc, LKC, tab(i) + TL::KC, DK, C, DK);
         cp_commit();
     };
-    for (int e = tid; e < DK * VS; e += NT)
-        sm.S[(e / VS) * LS + e % VS] = s0 ? s0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    slice_load(sm.S, s0 ? s0 + sh * DK * DV + v0 : nullptr, DK, DV);
     issue_a(0);
     issue_b(0);
     issue_c(0);
@@ -712,8 +727,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         const TIn *Vt = sm.V[ci & 1];
         cp_wait<1>();  // this chunk's scalars, v, Kr and T (Kc may still be on its way)
         __syncthreads();
-        for (int e = tid; e < DK * VS; e += NT)
-            st[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.S[(e / VS) * LS + e % VS];
+        slice_store(st + ci * wstride * DK * DV + v0, sm.S, DK, DV);
         if (ci + 2 < NC) {  // two chunks ahead into L2
             prefetch_tables<DK>(tab(ci + 2));
             prefetch_rows<TIn>(v, tok0 + 2 * C, len(ci + 2), H, h, DV, v0);
@@ -861,8 +875,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         cp_commit();
     };
 
-    for (int e = tid; e < DK * VS; e += NT)
-        sm.G[(e / VS) * LS + e % VS] = p.dsT ? p.dsT[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] : 0.f;
+    slice_load(sm.G, p.dsT ? p.dsT + sh * DK * DV + v0 : nullptr, DK, DV);
     issue_a(NC - 1);
     issue_b(NC - 1);
     issue_c(NC - 1);
@@ -876,8 +889,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         if (DB) cp_wait<2>();  // this chunk's scalars, dO, Kc and P (T, Qr and Kr may still be on their way)
         else cp_wait<0>();
         __syncthreads();
-        for (int e = tid; e < DK * VS; e += NT)  // dL/dS after this chunk
-            gn[ci * wstride * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LS + e % VS];
+        slice_store(gn + ci * wstride * DK * DV + v0, sm.G, DK, DV);  // dL/dS after this chunk
         if (ci >= 2) {  // two chunks ahead into L2
             prefetch_tables<DK>(tab(ci - 2));
             prefetch_rows<TIn>(dO, tok0 - 2 * C, C, H, h, DV, v0);
@@ -952,8 +964,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
     cp_wait<0>();
     __syncthreads();
     if (p.ds0)
-        for (int e = tid; e < DK * VS; e += NT)
-            p.ds0[sh * DK * DV + (int64_t)(e / VS) * DV + v0 + e % VS] = sm.G[(e / VS) * LS + e % VS];
+        slice_store(p.ds0 + sh * DK * DV + v0, sm.G, DK, DV);
 }
 
 // ---------------------------------------------------------------- local
