@@ -1,6 +1,7 @@
-// KDA chunkwise backward on CUDA cores (fp32 arithmetic): the gradients of
-// L = sum_t <do_t, o_t> + <dS_T, S_T> with respect to q, k, v, alpha, beta
-// and the initial state, for equal-length batches.
+// KDA chunkwise backward (fp32 arithmetic, products on the tensor cores): the
+// gradients of L = sum_t <do_t, o_t> + <dS_T, S_T> with respect to q, k, v,
+// alpha, beta and the initial state, for equal-length or packed batches and
+// every gate kind.
 //
 // Source of the map: the web page "研究KimiK3，我发现大模型正在学会“管理自己的计算”"
 // (pwwt.cn), the K3 essay: §四 (the KDA update), §二.1 (the read-out o = S^T q),
@@ -8,8 +9,8 @@
 // give no gradients; the chain rule applied to the chunk algebra below does.
 //
 // Chunk algebra (as in the forward; C = 64 rows r, j; key channels c; value
-// columns v; St = Diag(mu) S the centred start state; tables from
-// kda_chunk_simt.cuh):
+// columns v; St = Diag(mu) S the centred start state; the tables of
+// kda_chunk_simt.cuh, built here by the tables pass):
 //   X = Kr St,  R = Diag(beta) (V - X),  U = T R,  O = Qr St + P U,
 //   S_next = Diag(mu) (St + Kc^T U).
 // Reverse, with G = dL/dS_next and Gt = Diag(mu) G:
