@@ -636,22 +636,26 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     for (int tu = 0; tu < 4; ++tu) {  // k rows lane, lane + 32, then q rows lane, lane + 32
                         const int t = tu >> 1, r = lane + 32 * (tu & 1);
                         const uint32_t sw = t ? ((tu & 1) ? qsw[1] : qsw[0]) : ((tu & 1) ? ksw[1] : ksw[0]);
-                        uint4 w[4];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            w[c] = *reinterpret_cast<const uint4 *>(ah + 8192 + 4096 * t + r * 64 + 16 * c);
+                        const unsigned char *src = ah + 8192 + 4096 * t + r * 64;
+                        uint4 w0 = *reinterpret_cast<const uint4 *>(src), w1 = *reinterpret_cast<const uint4 *>(src + 16),
+                              w2 = *reinterpret_cast<const uint4 *>(src + 32), w3 = *reinterpret_cast<const uint4 *>(src + 48);
                         __syncwarp();  // q rows 32-63 land on codes other lanes read in this pass
                         unsigned char *dst = ah + 8192 * t + r * 128;
+#pragma unroll 1
+                        for (int c2 = 0; c2 < 4; ++c2) {  // 16 channels: codes 16 c2 .. 16 c2 + 15, in w0
+                            const float sc = e8m0((uint8_t)(sw >> (8 * (2 * (int)rank + (c2 >> 1)))));
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {  // 8 channels: codes 8 c8 .. 8 c8 + 7
-                            const uint4 cw = w[c8 >> 1];
-                            const float sc = e8m0((uint8_t)(sw >> (8 * (2 * (int)rank + (c8 >> 2)))));
-                            float f[4], g[4];
-                            e4m3x4_to_f32((c8 & 1) ? cw.z : cw.x, sc, f);
-                            e4m3x4_to_f32((c8 & 1) ? cw.w : cw.y, sc, g);
-                            *reinterpret_cast<uint4 *>(dst + ((c8 ^ (r & 7)) << 4)) =
-                                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(g[0], g[1]),
-                                           pack_bf16(g[2], g[3]));
+                            for (int hh = 0; hh < 2; ++hh) {
+                                float f[4], g[4];
+                                e4m3x4_to_f32(hh ? w0.z : w0.x, sc, f);
+                                e4m3x4_to_f32(hh ? w0.w : w0.y, sc, g);
+                                *reinterpret_cast<uint4 *>(dst + (((2 * c2 + hh) ^ (r & 7)) << 4)) =
+                                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(g[0], g[1]),
+                                               pack_bf16(g[2], g[3]));
+                            }
+                            w0 = w1;
+                            w1 = w2;
+                            w2 = w3;
                         }
                         __syncwarp();
                     }
@@ -771,6 +775,7 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     const float bt = s.beta(n % NSLOT)[l];
                     const uint64_t bt2 = f2_make(bt, bt);
                     const unsigned char *vt = s.base + SM_V;
+                    if constexpr (FP8) {
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         uint4 vrow[4];  // the v row first: no load waits behind an R store
@@ -809,6 +814,29 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                             }
                             *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                    }
+                    } else {
+#pragma unroll 1
+                        for (int qq = 0; qq < 4; ++qq) {  // 16 columns at a time
+                            uint4 vrow[2];
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                vrow[c2] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 2 * qq + c2));
+                            uint32_t x16[16];
+                            tmem_ld16(tmem + lane_off + TM_XY + 64 * b + 16 * qq, x16);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2) {
+                                const uint32_t vw[4] = {vrow[c2].x, vrow[c2].y, vrow[c2].z, vrow[c2].w};
+                                uint32_t ow[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const uint64_t x2 = (uint64_t)x16[8 * c2 + 2 * e] | ((uint64_t)x16[8 * c2 + 2 * e + 1] << 32);
+                                    ow[e] = f2_to_bf2(f2_mul(f2_sub(bf2_to_f2(vw[e]), x2), bt2));
+                                }
+                                *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 2 * qq + c2)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                            }
                         }
                     }
                     fence_proxy_async();
