@@ -775,68 +775,43 @@ kda_prefill_tc_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_k, cons
                     const float bt = s.beta(n % NSLOT)[l];
                     const uint64_t bt2 = f2_make(bt, bt);
                     const unsigned char *vt = s.base + SM_V;
-                    if constexpr (FP8) {
 #pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint4 vrow[4];  // the v row first: no load waits behind an R store
-                        const float vsc = hf ? vsc2[1] : vsc2[0];
-                        if constexpr (FP8) {  // 32 E4M3 codes: 64-byte rows, 64B swizzle
-                            const int sw = (l >> 1) & 3;
-                            vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 16 * ((2 * hf) ^ sw));
-                            vrow[1] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 16 * ((2 * hf + 1) ^ sw));
+                    for (int qq = 0; qq < 4; ++qq) {  // 16 columns at a time
+                        uint4 vrow[2];  // the v row first: no load waits behind an R store
+                        float vsc = 1.f;
+                        if constexpr (FP8) {  // 16 E4M3 codes of the 64-byte row (64B swizzle) and their scale
+                            vrow[0] = *reinterpret_cast<const uint4 *>(vt + l * 64 + 16 * (qq ^ ((l >> 1) & 3)));
+                            vsc = (qq >> 1) ? vsc2[1] : vsc2[0];
                         } else {
 #pragma unroll
-                            for (int c4 = 0; c4 < 4; ++c4)
-                                vrow[c4] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 4 * hf + c4));
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                vrow[c2] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 2 * qq + c2));
                         }
-                        tmem_ld32(tmem + lane_off + TM_XY + 64 * b + 32 * hf, r32);
+                        uint32_t x16[16];
+                        tmem_ld16(tmem + lane_off + TM_XY + 64 * b + 16 * qq, x16);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
+                        for (int c2 = 0; c2 < 2; ++c2) {
                             uint64_t vp[4];  // 8 values of v as 4 fp32 pairs
                             if constexpr (FP8) {
-                                const uint4 w = vrow[c4 >> 1];
                                 float f[8];
-                                e4m3x4_to_f32((c4 & 1) ? w.z : w.x, vsc, *reinterpret_cast<float (*)[4]>(f));
-                                e4m3x4_to_f32((c4 & 1) ? w.w : w.y, vsc, *reinterpret_cast<float (*)[4]>(f + 4));
+                                e4m3x4_to_f32(c2 ? vrow[0].z : vrow[0].x, vsc, *reinterpret_cast<float (*)[4]>(f));
+                                e4m3x4_to_f32(c2 ? vrow[0].w : vrow[0].y, vsc, *reinterpret_cast<float (*)[4]>(f + 4));
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) vp[e] = f2_make(f[2 * e], f[2 * e + 1]);
                             } else {
-                                const uint32_t vw[4] = {vrow[c4].x, vrow[c4].y, vrow[c4].z, vrow[c4].w};
+                                const uint32_t vw[4] = {vrow[c2].x, vrow[c2].y, vrow[c2].z, vrow[c2].w};
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) vp[e] = bf2_to_f2(vw[e]);
                             }
                             uint32_t ow[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const uint64_t x2 = (uint64_t)r32[8 * c4 + 2 * e] | ((uint64_t)r32[8 * c4 + 2 * e + 1] << 32);
+                                const uint64_t x2 = (uint64_t)x16[8 * c2 + 2 * e] | ((uint64_t)x16[8 * c2 + 2 * e + 1] << 32);
                                 ow[e] = f2_to_bf2(f2_mul(f2_sub(vp[e], x2), bt2));
                             }
-                            *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 4 * hf + c4)) =
+                            *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 2 * qq + c2)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                        }
-                    }
-                    } else {
-#pragma unroll 1
-                        for (int qq = 0; qq < 4; ++qq) {  // 16 columns at a time
-                            uint4 vrow[2];
-#pragma unroll
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                vrow[c2] = *reinterpret_cast<const uint4 *>(vt + row128_chunk(l, 2 * qq + c2));
-                            uint32_t x16[16];
-                            tmem_ld16(tmem + lane_off + TM_XY + 64 * b + 16 * qq, x16);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int c2 = 0; c2 < 2; ++c2) {
-                                const uint32_t vw[4] = {vrow[c2].x, vrow[c2].y, vrow[c2].z, vrow[c2].w};
-                                uint32_t ow[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const uint64_t x2 = (uint64_t)x16[8 * c2 + 2 * e] | ((uint64_t)x16[8 * c2 + 2 * e + 1] << 32);
-                                    ow[e] = f2_to_bf2(f2_mul(f2_sub(bf2_to_f2(vw[e]), x2), bt2));
-                                }
-                                *reinterpret_cast<uint4 *>(ru + row128_chunk(l, 2 * qq + c2)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                            }
                         }
                     }
                     fence_proxy_async();
