@@ -334,16 +334,21 @@ __device__ void gate_factor_table(float *part, const float *mu, float *E2, float
                                   int gate, int64_t tok0, int L, int H, int h) {
     using GS = GateSplit<DK>;
     const int tid = threadIdx.x, cl = tid % GS::CH, seg = tid / GS::CH;
-    for (int half = 0; half < 2; ++half) {
-        const int c = half * GS::CH + cl;
-        float al[GS::TPS];
-        float prod = 1.f;
+    float alh[2][GS::TPS];  // both halves' gates, every load in flight at once
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int i = 0; i < GS::TPS; ++i) {
             const int r = seg * GS::TPS + i;
-            al[i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, c, DK) : 1.f;
-            prod *= al[i];
+            alh[half][i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, half * GS::CH + cl, DK) : 1.f;
         }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int c = half * GS::CH + cl;
+        const float(&al)[GS::TPS] = alh[half];
+        float prod = 1.f;
+#pragma unroll
+        for (int i = 0; i < GS::TPS; ++i) prod *= al[i];
         __syncthreads();  // earlier readers of part are done
         part[seg * GS::CH + cl] = prod;
         __syncthreads();
@@ -1303,13 +1308,16 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // the first parts of d log mu's column sums: Kc (U Gt^T), Qr (dO St^T), Kr (dX St^T)
     float s123[NK][2];
 #pragma unroll
-    for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int cc = CK + 8 * nt + 2 * t4 + u, a0 = (R0 + g) * LDK + cc, a1 = (R0 + g + 8) * LDK + cc;
-            s123[nt][u] = sm.Kc[a0] * dKc[nt][u] + sm.Kc[a1] * dKc[nt][2 + u] + F.Qr[a0] * dQr[nt][u] +
-                          F.Qr[a1] * dQr[nt][2 + u] + F.Kr[a0] * dKr[nt][u] + F.Kr[a1] * dKr[nt][2 + u];
-        }
+    for (int nt = 0; nt < NK; ++nt) {
+        const int cc = CK + 8 * nt + 2 * t4, a0 = (R0 + g) * LDK + cc, a1 = (R0 + g + 8) * LDK + cc;
+        const float2 kc0 = *reinterpret_cast<const float2 *>(sm.Kc + a0), kc1 = *reinterpret_cast<const float2 *>(sm.Kc + a1);
+        const float2 qr0 = *reinterpret_cast<const float2 *>(F.Qr + a0), qr1 = *reinterpret_cast<const float2 *>(F.Qr + a1);
+        const float2 kr0 = *reinterpret_cast<const float2 *>(F.Kr + a0), kr1 = *reinterpret_cast<const float2 *>(F.Kr + a1);
+        s123[nt][0] = kc0.x * dKc[nt][0] + kc1.x * dKc[nt][2] + qr0.x * dQr[nt][0] + qr1.x * dQr[nt][2] +
+                      kr0.x * dKr[nt][0] + kr1.x * dKr[nt][2];
+        s123[nt][1] = kc0.y * dKc[nt][1] + kc1.y * dKc[nt][3] + qr0.y * dQr[nt][1] + qr1.y * dQr[nt][3] +
+                      kr0.y * dKr[nt][1] + kr1.y * dKr[nt][3];
+    }
     ffor<4>(dP, R0, C0, [&](int r, int cc, float &x) { x = cc <= r ? x : 0.f; });  // lower(dP)
     sstore<4>(dP, R0, C0, WC, LDC);
     sstore<4>(dP, R0, C0, WP, LS);
@@ -1343,10 +1351,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1);
-                db[e >> 1] += F.Kr[r * LDK + cc] * tmp[nt][e];
-                dKr[nt][e] += sm.beta[r] * tmp[nt][e];
+            for (int e = 0; e < 4; e += 2) {
+                const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4;
+                const float2 kr = *reinterpret_cast<const float2 *>(F.Kr + r * LDK + cc);
+                const float br = sm.beta[r];
+                db[e >> 1] += kr.x * tmp[nt][e] + kr.y * tmp[nt][e + 1];
+                dKr[nt][e] += br * tmp[nt][e];
+                dKr[nt][e + 1] += br * tmp[nt][e + 1];
             }
     }
     wmm<C, NK, SPLIT>(dKc, [&](int r, int m) { return sm.beta[m] * WP[m * LS + r]; },
@@ -1374,15 +1385,20 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
 #pragma unroll
     for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4 + (e & 1), rc = r * LDK + cc;
-            const float e2 = E2[rc], e3 = E3[rc];  // p / mu and mu / p
+        for (int e = 0; e < 4; e += 2) {  // the two columns of a row together (8-byte accesses)
+            const int r = R0 + g + 8 * (e >> 1), cc = CK + 8 * nt + 2 * t4, rc = r * LDK + cc;
+            const float2 e2 = *reinterpret_cast<const float2 *>(E2 + rc);  // p / mu
+            const float2 e3 = *reinterpret_cast<const float2 *>(E3 + rc);  // mu / p
             if (r < L) {
                 const int64_t th = (tok0 + r) * H + h;
-                p.dq[th * DK + cc] = dQr[nt][e] * e2;
-                p.dk[th * DK + cc] = dKr[nt][e] * e2 + dKc[nt][e] * e3;
+                *reinterpret_cast<float2 *>(p.dq + th * DK + cc) = make_float2(dQr[nt][e] * e2.x, dQr[nt][e + 1] * e2.y);
+                *reinterpret_cast<float2 *>(p.dk + th * DK + cc) =
+                    make_float2(dKr[nt][e] * e2.x + dKc[nt][e] * e3.x, dKr[nt][e + 1] * e2.y + dKc[nt][e + 1] * e3.y);
             }
-            dlogp[nt][e] = dKr[nt][e] * F.Kr[rc] + dQr[nt][e] * F.Qr[rc] - dKc[nt][e] * sm.Kc[rc];
+            const float2 kr = *reinterpret_cast<const float2 *>(F.Kr + rc), qr = *reinterpret_cast<const float2 *>(F.Qr + rc),
+                         kc = *reinterpret_cast<const float2 *>(sm.Kc + rc);
+            dlogp[nt][e] = dKr[nt][e] * kr.x + dQr[nt][e] * qr.x - dKc[nt][e] * kc.x;
+            dlogp[nt][e + 1] = dKr[nt][e + 1] * kr.y + dQr[nt][e + 1] * qr.y - dKc[nt][e + 1] * kc.y;
         }
     // s123: sums over the 16 rows of this warp (lanes with the same t), then by warp row block
 #pragma unroll
