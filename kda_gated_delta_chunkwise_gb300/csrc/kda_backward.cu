@@ -329,12 +329,13 @@ template <int DK> struct TabSmem {
 // Qr) into E2 and mu / p (that of Kc: the later gates over mu) into E3, both
 // [C][ld] floats. Needs the chunk's mu ([DK], shared memory); uses part
 // ([NT], shared memory) as scratch. Ends with a barrier.
+// This thread's gates as gate_factor_table takes them: both halves of the
+// channels, every load in flight at once.
 template <int DK>
-__device__ void gate_factor_table(float *part, const float *mu, float *E2, float *E3, int ld, const float *alpha,
-                                  int gate, int64_t tok0, int L, int H, int h) {
+__device__ __forceinline__ void gate_factor_loads(float (&alh)[2][GateSplit<DK>::TPS], const float *alpha, int gate,
+                                                  int64_t tok0, int L, int H, int h) {
     using GS = GateSplit<DK>;
     const int tid = threadIdx.x, cl = tid % GS::CH, seg = tid / GS::CH;
-    float alh[2][GS::TPS];  // both halves' gates, every load in flight at once
 #pragma unroll
     for (int half = 0; half < 2; ++half)
 #pragma unroll
@@ -342,6 +343,12 @@ __device__ void gate_factor_table(float *part, const float *mu, float *E2, float
             const int r = seg * GS::TPS + i;
             alh[half][i] = r < L ? gate_at(alpha, gate, (tok0 + r) * H + h, half * GS::CH + cl, DK) : 1.f;
         }
+}
+template <int DK>
+__device__ void gate_factor_table(float *part, const float *mu, float *E2, float *E3, int ld,
+                                  const float (&alh)[2][GateSplit<DK>::TPS]) {
+    using GS = GateSplit<DK>;
+    const int tid = threadIdx.x, cl = tid % GS::CH, seg = tid / GS::CH;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int c = half * GS::CH + cl;
@@ -1273,6 +1280,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // dQr = dO St^T, dKr = dX St^T (dX = -Diag(beta) dR), dKc = U Gt^T with
     // St = Diag(mu) S, Gt = Diag(mu) G; dT = dU R^T with R = Diag(beta) (V - X)
     LocalFinal<DK> &F = sm.u.fin;
+    float alh[2][GateSplit<DK>::TPS];  // the gates of the chunk's gate factors, loaded under the products
+    gate_factor_loads<DK>(alh, p.alpha, GATE, tok0, L, H, h);
     for (int e = tid; e < C * DK / 4; e += NT) {
         const int r = e / (DK / 4), cc = 4 * (e % (DK / 4));
         cp16(&F.Kr[r * LDK + cc], tab + TL::KR + r * DK + cc);
@@ -1378,7 +1387,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
     // work tiles; dq, dk, and d log p into Qr's place
     float *E2 = F.W[0], *E3 = F.W[2];  // [C][LDK] each: W[0..1] and W[2..3]
     static_assert(C * LDK <= 2 * C * LS, "E2 and E3 fit in two work tiles each");
-    gate_factor_table<DK>(sm.part, sm.mu, E2, E3, LDK, p.alpha, GATE, tok0, L, H, h);
+    gate_factor_table<DK>(sm.part, sm.mu, E2, E3, LDK, alh);
     sm.part[(tid / DK) * DK + tid % DK] = sm.mu[tid % DK] * sm.mu[tid % DK] * s0;
     if (tid < L) p.dbeta[(tok0 + tid) * H + h] = dbr[tid] + dbr[C + tid] + dbr[2 * C + tid];
     float dlogp[NK][4];
