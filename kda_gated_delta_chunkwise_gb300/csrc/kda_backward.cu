@@ -954,10 +954,23 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.T, LS, R0, kx, hi, lo); },
                            sm.dU, LS, (const float *)nullptr, R0, C0);
         gstore<4>(acc, R0, C0, wk + 3 * C * DV, DV);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) {
-            if (r < L) p.dv[((tok0 + r) * H + h) * DV + v0 + c] = cs.beta[r] * x;
-            x *= -cs.beta[r];
-        });
+        {  // dv = Diag(beta) dR (two columns per store), then dX = -Diag(beta) dR
+            const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = R0 + g + 8 * u;
+                const float br = cs.beta[r];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    float &x0 = acc[nt][2 * u], &x1 = acc[nt][2 * u + 1];
+                    if (r < L)
+                        *reinterpret_cast<float2 *>(p.dv + ((tok0 + r) * H + h) * DV + v0 + C0 + 8 * nt + 2 * t4) =
+                            make_float2(br * x0, br * x1);
+                    x0 *= -br;
+                    x1 *= -br;
+                }
+            }
+        }
         cp_wait<1>();  // Qr and Kr (the next chunk's first group may be pending)
         __syncthreads();  // every read of dU is done; Qr and Kr have landed
         sstore<4>(acc, R0, C0, sm.dU, LS);
