@@ -180,6 +180,11 @@ __device__ __forceinline__ void prefetch_rows(const TIn *src, int64_t tok0, int 
     if ((int)threadIdx.x < L)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(src + ((tok0 + threadIdx.x) * H + h) * DV + v0));
 }
+// Two consecutive elements (the first at an even index) as floats.
+__device__ __forceinline__ float2 ld2(const float *x) { return *reinterpret_cast<const float2 *>(x); }
+__device__ __forceinline__ float2 ld2(const __nv_bfloat16 *x) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(x));
+}
 // The padded row of such a tile (elements): 16-byte rows, conflict-free reads.
 template <typename TIn> struct RowTile { static constexpr int LD = sizeof(TIn) == 4 ? VS + 4 : VS + 8; };
 
@@ -776,7 +781,17 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         fzero<4>(acc);
         mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.Kr, LKR, R0, kx, hi, lo); },
                             sm.S, LS, cs.mu, R0, C0);
-        ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { x = to_f32(Vt[r * LV + c]) - x; });
+        {  // V - X, two columns per load
+            const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float2 vv = ld2(Vt + (R0 + g + 8 * u) * LV + C0 + 8 * nt + 2 * t4);
+                    acc[nt][2 * u] = vv.x - acc[nt][2 * u];
+                    acc[nt][2 * u + 1] = vv.y - acc[nt][2 * u + 1];
+                }
+        }
         gstore<4>(acc, R0, C0, wk + C * DV, DV);
         ffor<4>(acc, R0, C0, [&](int r, int c, float &x) { x *= cs.beta[r]; });
         sstore<4>(acc, R0, C0, sm.R, LS);
@@ -1045,6 +1060,25 @@ static_assert(local_layout_ok<128, float>() && local_layout_ok<128, __nv_bfloat1
                   local_layout_ok<64, __nv_bfloat16>(),
               "16-byte tiles and offsets");
 
+// Four 8 x 8 b16 matrices from shared memory (ldmatrix); this lane's row
+// address is p.
+__device__ __forceinline__ void ldsm_x4(const float *p, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+// A fragment of a row-major fp32 tile through ldmatrix (this lane's row address p).
+template <bool SPLIT> __device__ __forceinline__ void afrag_ldsm(const float *p, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    uint32_t r[4];
+    ldsm_x4(p, r);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float v = __uint_as_float(r[u]);
+        if (SPLIT) split_tf32(v, hi[u], lo[u]);
+        else hi[u] = tf32_bits(v), lo[u] = 0u;
+    }
+}
+
 // The local pass of a chunk that the forward runs token by token (a channel
 // decays past e^-80), in `buf` (slow_floats<DK>() floats of shared memory).
 template <int DK, typename TIn, int GATE>
@@ -1249,25 +1283,41 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
         for (int k = 0; k < VP; k += 8) {
             uint32_t oh[4], ol[4], rh[4], rl[4], uh[4], ul[4], dh[4], dl[4];
             afrag<SPLIT>(P.dO, DLD, R0, k, oh, ol);
-            afrag<SPLIT>(P.dR, LDP, R0, k, rh, rl);
-            afrag<SPLIT>(P.U, LDP, R0, k, uh, ul);
-            afrag<SPLIT>(P.dU, LDP, R0, k, dh, dl);
+            // the fp32 tiles' fragments by ldmatrix: an 8 x 8 b16 matrix is 8 rows of
+            // 4 floats, and lane 4 g + t receives row g, float t of each
+            const int arow = R0 + (lane & 7) + 8 * ((lane >> 3) & 1), acol = k + 4 * (lane >> 4);
+            afrag_ldsm<SPLIT>(P.dR + arow * LDP + acol, rh, rl);
+            afrag_ldsm<SPLIT>(P.U + arow * LDP + acol, uh, ul);
+            afrag_ldsm<SPLIT>(P.dU + arow * LDP + acol, dh, dl);
+            const int brow = (lane & 7) + 8 * (lane >> 4), bcol = k + 4 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int nt = 0; nt < NK; ++nt) {
-                const int o = (CK + 8 * nt + g) * LDP + k + t4;
-                const BFrag bs = bfrag<SPLIT>(P.S[o], P.S[o + 4]);
-                const BFrag bg = bfrag<SPLIT>(P.G[o], P.G[o + 4]);
-                mma_f<SPLIT>(dQr[nt], oh, ol, bs);
-                mma_f<SPLIT>(dKr[nt], rh, rl, bs);
-                mma_f<SPLIT>(dKc[nt], uh, ul, bg);
+            for (int np = 0; np < NK / 2; ++np) {  // two 8-column tiles per load
+                const int o = (CK + 16 * np + brow) * LDP + bcol;
+                uint32_t s4[4], g4[4];
+                ldsm_x4(P.S + o, s4);
+                ldsm_x4(P.G + o, g4);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const BFrag bs = bfrag<SPLIT>(__uint_as_float(s4[2 * u]), __uint_as_float(s4[2 * u + 1]));
+                    const BFrag bg = bfrag<SPLIT>(__uint_as_float(g4[2 * u]), __uint_as_float(g4[2 * u + 1]));
+                    mma_f<SPLIT>(dQr[2 * np + u], oh, ol, bs);
+                    mma_f<SPLIT>(dKr[2 * np + u], rh, rl, bs);
+                    mma_f<SPLIT>(dKc[2 * np + u], uh, ul, bg);
+                }
             }
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int o = (C0 + 8 * nt + g) * LDP + k + t4;
-                const BFrag bu = bfrag<SPLIT>(P.U[o], P.U[o + 4]);
-                const BFrag bv = bfrag<SPLIT>(P.VmX[o], P.VmX[o + 4]);
-                mma_f<SPLIT>(dP[nt], oh, ol, bu);
-                mma_f<SPLIT>(dT[nt], dh, dl, bv);
+            for (int np = 0; np < 2; ++np) {
+                const int o = (C0 + 16 * np + brow) * LDP + bcol;
+                uint32_t u4[4], v4[4];
+                ldsm_x4(P.U + o, u4);
+                ldsm_x4(P.VmX + o, v4);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const BFrag bu = bfrag<SPLIT>(__uint_as_float(u4[2 * u]), __uint_as_float(u4[2 * u + 1]));
+                    const BFrag bv = bfrag<SPLIT>(__uint_as_float(v4[2 * u]), __uint_as_float(v4[2 * u + 1]));
+                    mma_f<SPLIT>(dP[2 * np + u], oh, ol, bu);
+                    mma_f<SPLIT>(dT[2 * np + u], dh, dl, bv);
+                }
             }
         }
         {
