@@ -308,6 +308,33 @@ __device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&ah)[4], co
     mma8(d, ah, b.h0, b.h1);
 }
 
+// Four 8 x 8 b16 matrices from shared memory (ldmatrix); this lane's row
+// address is p.
+__device__ __forceinline__ void ldsm_x4(const float *p, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+// A fragment of a row-major fp32 tile through ldmatrix (this lane's row address p).
+template <bool SPLIT> __device__ __forceinline__ void afrag_ldsm(const float *p, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    uint32_t r[4];
+    ldsm_x4(p, r);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float v = __uint_as_float(r[u]);
+        if (SPLIT) split_tf32(v, hi[u], lo[u]);
+        else hi[u] = tf32_bits(v), lo[u] = 0u;
+    }
+}
+
+// This lane's row and column offsets of the ldmatrix addresses: of an A
+// fragment (rows r0 .. r0 + 15, columns k .. k + 7) and of the B fragments of
+// two 8-column tiles stored [n][k] (rows n0 .. n0 + 15, columns k .. k + 7).
+__device__ __forceinline__ int ldsm_arow() { return (threadIdx.x & 7) + 8 * ((threadIdx.x >> 3) & 1); }
+__device__ __forceinline__ int ldsm_acol() { return 4 * ((threadIdx.x >> 4) & 1); }
+__device__ __forceinline__ int ldsm_brow() { return (threadIdx.x & 7) + 8 * ((threadIdx.x >> 4) & 1); }
+__device__ __forceinline__ int ldsm_bcol() { return 4 * ((threadIdx.x >> 3) & 1); }
+
 // ---------------------------------------------------------------- tables
 // The key channels are taken in two halves of CH = DK / 2, so that the
 // shared memory of a CTA (one half of Kr, Qr, Kc, plus A and T: about 88 KB
@@ -412,7 +439,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
     const int H = p.H;
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k;
     float *dst = p.tabs + idx * TL::FLOATS;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int cl = tid % GS::CH, seg = tid / GS::CH;
     const int R0 = 16 * (warp & 3), C0 = 32 * (warp >> 2);
     // the chunk's rows of alpha, k and q into L2: the second half of the
@@ -491,14 +518,19 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_tables_kernel(BwdParams p) {
 #pragma unroll 2
         for (int kx = 0; kx < GS::CH; kx += 8) {
             uint32_t kh[4], kl[4], qh[4], ql[4];
-            afrag<SPLIT>(sm.Kr, LDH, R0, kx, kh, kl);
-            afrag<SPLIT>(sm.Qr, LDH, R0, kx, qh, ql);
+            const int ao = (R0 + ldsm_arow()) * LDH + kx + ldsm_acol();
+            afrag_ldsm<SPLIT>(sm.Kr + ao, kh, kl);
+            afrag_ldsm<SPLIT>(sm.Qr + ao, qh, ql);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int o = (C0 + 8 * nt + g) * LDH + kx + t4;
-                const BFrag b = bfrag<SPLIT>(sm.Kc[o], sm.Kc[o + 4]);
-                mma_f<SPLIT>(accA[nt], kh, kl, b);
-                mma_f<SPLIT>(accP[nt], qh, ql, b);
+            for (int np = 0; np < 2; ++np) {  // two 8-column tiles of Kc^T per load
+                uint32_t k4[4];
+                ldsm_x4(sm.Kc + (C0 + 16 * np + ldsm_brow()) * LDH + kx + ldsm_bcol(), k4);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const BFrag b = bfrag<SPLIT>(__uint_as_float(k4[2 * u]), __uint_as_float(k4[2 * u + 1]));
+                    mma_f<SPLIT>(accA[2 * np + u], kh, kl, b);
+                    mma_f<SPLIT>(accP[2 * np + u], qh, ql, b);
+                }
             }
         }
     }
@@ -779,7 +811,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         float acc[4][4];
         // X = Kr St (St = Diag(mu) S); V - X into the workspace; R = Diag(beta) (V - X)
         fzero<4>(acc);
-        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.Kr, LKR, R0, kx, hi, lo); },
+        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag_ldsm<SPLIT>(sm.Kr + (R0 + ldsm_arow()) * LKR + kx + ldsm_acol(), hi, lo); },
                             sm.S, LS, cs.mu, R0, C0);
         {  // V - X, two columns per load
             const int lane = tid & 31, g = lane >> 2, t4 = lane & 3;
@@ -799,7 +831,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_states_kernel(BwdParams p, cons
         issue_a(ci + 1);  // Kr is free
         // U = T R, also into the workspace
         fzero<4>(acc);
-        mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.T, LR, R0, kx, hi, lo); },
+        mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag_ldsm<SPLIT>(sm.T + (R0 + ldsm_arow()) * LR + kx + ldsm_acol(), hi, lo); },
                            sm.R, LS, (const float *)nullptr, R0, C0);
         sstore<4>(acc, R0, C0, sm.U, LS);
         gstore<4>(acc, R0, C0, wk, DV);
@@ -955,7 +987,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_chain_kernel(BwdParams p) {
         float acc[4][4];
         // dU = Kc Gt + P^T dO (Gt = Diag(mu) G), also into the workspace
         fzero<4>(acc);
-        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag<SPLIT>(sm.Kc, LKR, R0, kx, hi, lo); },
+        mm_kn<DK, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afrag_ldsm<SPLIT>(sm.Kc + (R0 + ldsm_arow()) * LKR + kx + ldsm_acol(), hi, lo); },
                             sm.G, LS, cs.mu, R0, C0);
         mm_kn<C, 4, SPLIT>(acc, [&](int kx, uint32_t(&hi)[4], uint32_t(&lo)[4]) { afragT<SPLIT>(sm.P, LP, R0, kx, hi, lo); },
                            dOt, LD, (const float *)nullptr, R0, C0);
@@ -1059,25 +1091,6 @@ template <int DK, typename TIn> constexpr bool local_layout_ok() {
 static_assert(local_layout_ok<128, float>() && local_layout_ok<128, __nv_bfloat16>() && local_layout_ok<64, float>() &&
                   local_layout_ok<64, __nv_bfloat16>(),
               "16-byte tiles and offsets");
-
-// Four 8 x 8 b16 matrices from shared memory (ldmatrix); this lane's row
-// address is p.
-__device__ __forceinline__ void ldsm_x4(const float *p, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
-}
-// A fragment of a row-major fp32 tile through ldmatrix (this lane's row address p).
-template <bool SPLIT> __device__ __forceinline__ void afrag_ldsm(const float *p, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
-    uint32_t r[4];
-    ldsm_x4(p, r);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const float v = __uint_as_float(r[u]);
-        if (SPLIT) split_tf32(v, hi[u], lo[u]);
-        else hi[u] = tf32_bits(v), lo[u] = 0u;
-    }
-}
 
 // The local pass of a chunk that the forward runs token by token (a channel
 // decays past e^-80), in `buf` (slow_floats<DK>() floats of shared memory).
@@ -1285,11 +1298,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_local_kernel(BwdParams p) {
             afrag<SPLIT>(P.dO, DLD, R0, k, oh, ol);
             // the fp32 tiles' fragments by ldmatrix: an 8 x 8 b16 matrix is 8 rows of
             // 4 floats, and lane 4 g + t receives row g, float t of each
-            const int arow = R0 + (lane & 7) + 8 * ((lane >> 3) & 1), acol = k + 4 * (lane >> 4);
+            const int arow = R0 + ldsm_arow(), acol = k + ldsm_acol();
             afrag_ldsm<SPLIT>(P.dR + arow * LDP + acol, rh, rl);
             afrag_ldsm<SPLIT>(P.U + arow * LDP + acol, uh, ul);
             afrag_ldsm<SPLIT>(P.dU + arow * LDP + acol, dh, dl);
-            const int brow = (lane & 7) + 8 * (lane >> 4), bcol = k + 4 * ((lane >> 3) & 1);
+            const int brow = ldsm_brow(), bcol = k + ldsm_bcol();
 #pragma unroll
             for (int np = 0; np < NK / 2; ++np) {  // two 8-column tiles per load
                 const int o = (CK + 16 * np + brow) * LDP + bcol;
