@@ -65,6 +65,29 @@ def test_backward_ragged_and_head_sizes(kda, T, dk, dv):
     _check(kda, x, seed=T)
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_backward_bf16_head_sizes(kda, dk, dv):
+    """bf16 inputs with d_k or d_v = 64 (the other template instances of every
+    pass), two full chunks and a ragged tail, with a token-level chunk."""
+    x = W.batched(2, 150, 2, dk, dv, dtype="bf16", alpha_scale=0.2, s0_std=0.05, seed=60 + dk + dv)
+    x.alpha[1, 70:90, 0, 3] = 1e-3  # one channel decays past e^-80 in the second chunk of head 0
+    _check(kda, x, seed=61)
+
+
+def test_varlen_backward_small_heads(kda):
+    """Packed sequences with d_k = d_v = 64 on bf16 inputs against the oracle."""
+    x = W.packed([70, 0, 129, 5], 2, 64, 64, dtype="bf16", s0_std=0.05, seed=62)
+    d_o, dsT = _packed_upstream(x, 63)
+    d = torch.device("cuda")
+    q, k, v, a, b = (t.to(d) for t in x.tensors())
+    g = kda.varlen_prefill_backward(q, k, v, a, b, d_o.to(d), x.cu_seqlens.to(d), x.initial_state.to(d), dsT.to(d))
+    torch.cuda.synchronize()
+    ref = oracle.backward(*x.tensors(), d_o, dsT, cu_seqlens=x.cu_seqlens, initial_state=x.initial_state)
+    for key in KEYS:
+        r = ref[key]
+        assert_close(key, g[key].cpu(), r, dict(rel=5e-3, abs=max(1e-6, 5e-3 * 4 * float(np.abs(r).max()))))
+
+
 def test_backward_without_final_state_gradient_or_initial_state(kda):
     x = W.batched(1, 200, 3, 128, 128, dtype="fp32", alpha_scale=0.1, seed=7)
     assert x.initial_state is None
