@@ -185,8 +185,6 @@ __device__ __forceinline__ float2 ld2(const float *x) { return *reinterpret_cast
 __device__ __forceinline__ float2 ld2(const __nv_bfloat16 *x) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(x));
 }
-// The padded row of such a tile (elements): 16-byte rows, conflict-free reads.
-template <typename TIn> struct RowTile { static constexpr int LD = sizeof(TIn) == 4 ? VS + 4 : VS + 8; };
 
 // Pulls a chunk's tables into L2 ahead of their use (128-byte lines).
 template <int DK> __device__ __forceinline__ void prefetch_tables(const float *src) {
