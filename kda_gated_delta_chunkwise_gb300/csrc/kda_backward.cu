@@ -1555,7 +1555,7 @@ constexpr size_t kMaxSmem = 232448;  // dynamic shared memory one CTA may have
 static_assert(sizeof(StatesSmem<128, float>) <= kMaxSmem && sizeof(StatesSmem<128, __nv_bfloat16>) <= kMaxSmem &&
                   sizeof(ChainSmem<128, float>) <= kMaxSmem && sizeof(ChainSmem<128, __nv_bfloat16>) <= kMaxSmem &&
                   sizeof(LocalSmem<128, float>) <= kMaxSmem && sizeof(LocalSmem<128, __nv_bfloat16>) <= kMaxSmem &&
-                  sizeof(simt::Tables<128>) <= kMaxSmem,
+                  2 * sizeof(TabSmem<128>) + 2048 <= kMaxSmem,  // two tables CTAs per SM
               "shared memory per CTA");
 
 // Packed batches: checks cu_seqlens (starts at 0, never decreases, ends at
