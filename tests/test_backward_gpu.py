@@ -217,3 +217,32 @@ def test_varlen_backward_bad_cu_seqlens_sets_status(kda):
                                 device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == kda.KDA_DEV_BAD_CU_SEQLENS
+
+
+def test_varlen_backward_64seq_full(kda):
+    """The packed workload of 64 lognormal-length sequences (306,055 tokens,
+    16 heads, d = 128, bf16): every gradient element of the packed backward
+    against the oracle, which runs sequence by sequence (host memory stays
+    bounded), with rel-L2 over each whole gradient tensor."""
+    from _parity import ErrAccum
+    x = W.varlen_64seq()
+    d_o, dsT = _packed_upstream(x, 70)
+    d = torch.device("cuda")
+    q, k, v, a, b = (t.to(d) for t in x.tensors())
+    g = kda.varlen_prefill_backward(q, k, v, a, b, d_o.to(d), x.cu_seqlens.to(d), x.initial_state.to(d), dsT.to(d))
+    torch.cuda.synchronize()
+    g = {key: val.cpu() for key, val in g.items()}
+    acc = {key: ErrAccum(key) for key in KEYS}
+    top = dict.fromkeys(KEYS, 0.0)
+    cu = x.cu_seqlens.tolist()
+    for n in range(len(cu) - 1):
+        lo, hi = cu[n], cu[n + 1]
+        ref = oracle.backward(x.q[lo:hi], x.k[lo:hi], x.v[lo:hi], x.alpha[lo:hi], x.beta[lo:hi], d_o[lo:hi],
+                              dsT[n:n + 1], cu_seqlens=np.array([0, hi - lo], dtype=np.int32),
+                              initial_state=x.initial_state[n:n + 1])
+        for key in KEYS:
+            mine = g[key][n:n + 1] if key == "d_initial_state" else g[key][lo:hi]
+            acc[key].add(mine, ref[key])
+            top[key] = max(top[key], float(np.abs(ref[key]).max()) if ref[key].size else 0.0)
+    for key in KEYS:
+        acc[key].check(dict(rel=5e-3, abs=5e-3 * 4 * top[key]))
