@@ -246,3 +246,32 @@ def test_varlen_backward_64seq_full(kda):
             top[key] = max(top[key], float(np.abs(ref[key]).max()) if ref[key].size else 0.0)
     for key in KEYS:
         acc[key].check(dict(rel=5e-3, abs=5e-3 * 4 * top[key]))
+
+
+@pytest.mark.slow
+def test_backward_long_131k_full(kda):
+    """The long-context workload (1 sequence x 32 heads x 131,072 tokens, split
+    decay scales): every gradient element against the oracle, which runs 4
+    heads at a time (host memory stays bounded)."""
+    from _parity import ErrAccum
+    x = W.prefill_long_131k()
+    d_o, dsT = _upstream(x, 71)
+    d = torch.device("cuda")
+    g = kda.prefill_backward(*(t.to(d) for t in x.tensors()), d_o.to(d), initial_state=x.initial_state.to(d),
+                             d_final_state=dsT.to(d))
+    torch.cuda.synchronize()
+    g = {key: val.cpu() for key, val in g.items()}
+    acc = {key: ErrAccum(key) for key in KEYS}
+    top = dict.fromkeys(KEYS, 0.0)
+    qc, kc, vc, ac, bc = x.tensors()
+    for h0 in range(0, x.q.shape[2], 4):
+        hs = slice(h0, h0 + 4)
+        ref = oracle.backward(qc[:, :, hs], kc[:, :, hs], vc[:, :, hs], ac[:, :, hs], bc[:, :, hs], d_o[:, :, hs],
+                              dsT[:, hs], initial_state=x.initial_state[:, hs])
+        for key in KEYS:
+            mine = g[key][:, hs] if key == "d_initial_state" else g[key][:, :, hs]
+            acc[key].add(mine, ref[key])
+            top[key] = max(top[key], float(np.abs(ref[key]).max()))
+        del ref
+    for key in KEYS:
+        acc[key].check(dict(rel=5e-3, abs=5e-3 * 4 * top[key]))
