@@ -14,7 +14,9 @@ Prints ONE JSON line (rank 0). Keys beyond the basic contract:
   e2e           the same metric through the public API with host buffers,
                 host<->device copies inside the timed region
   decode        the decode step on 256 sequences x 32 heads (state GB/s)
-  long_context  prefill of one 131,072-token sequence with 32 heads
+  long_context  prefill of one 131,072-token sequence with 32 heads, cut
+                into segments that run at once (kda_prefill_segmented), with
+                the plain one-cluster-per-head launch beside it
   varlen        packed prefill of 64 lognormal-length sequences (306,055
                 tokens, 16 heads), and varlen_1m: the same lengths scaled to
                 2^20 tokens
@@ -248,21 +250,36 @@ def oracle_tokens_per_s(x, n_tokens_of, sample: str, target_s: float = 4.0, lib=
 def bench_long_context(kda, W, dev, stream, peaks, steps, warmup, with_cpu):
     """One 131,072-token sequence with 32 heads (split decay scales, S0 given):
     the case where a sequence is far longer than the batch is wide, so the
-    per-chunk state chain of each head sets the time."""
+    per-chunk state chain of each head sets the time. Timed through
+    kda_prefill_segmented (segments of the sequence run at once, joined by
+    their transition products) with the plain launch beside it."""
     x = W.prefill_long_131k()
     q, k, v, a, b, s0 = (t.to(dev) for t in (*x.tensors(), x.initial_state))
     Bl, Tl, Hl = 1, x.q.shape[1], x.q.shape[2]
     o = torch_empty_like(v)
     sT = torch_empty_like(s0)
-    ms = time_events(lambda: kda.prefill(q, k, v, a, b, s0, out=o, final_state=sT), steps, warmup, stream)
     nbytes = prefill_bytes(Bl, Tl, Hl, DK, DV, with_s0=True)
+    # the sequence cut into segments that run at once (kda_prefill_segmented,
+    # the library's plan), and the plain one-cluster-per-head launch beside it
+    G, first, seg = kda.segment_plan(Tl, Hl)
+    ws = torch_empty_bytes(kda.prefill_segmented_workspace_bytes(Tl, Hl), dev)
+    ms = time_events(lambda: kda.prefill_segmented(q, k, v, a, b, s0, out=o, final_state=sT, workspace=ws),
+                     steps, warmup, stream)
+    ms_plain = time_events(lambda: kda.prefill(q, k, v, a, b, s0, out=o, final_state=sT), steps, warmup, stream)
     gbs = nbytes / (ms / 1e3) / 1e9
-    res = {"workload": f"kda_prefill B=1 H={Hl} T={Tl} d_k={DK} d_v={DV} chunk={CHUNK}, bf16 q/k/v, "
+    gbs_plain = nbytes / (ms_plain / 1e3) / 1e9
+    res = {"workload": f"kda_prefill_segmented B=1 H={Hl} T={Tl} d_k={DK} d_v={DV} chunk={CHUNK}, bf16 q/k/v, "
                        "alpha scales 1e-4 / 0.2 per half of the key channels, S0 ~ N(0, 0.01^2)",
            "value": Bl * Tl / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
            "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
-           "kernel": "kda_prefill_tc", "clusters": Bl * Hl}
-    del q, k, v, a, b, o, sT
+           "kernels": "kda_prefill_tc (segment 0 from S0 on a high-priority stream; later segments from zero "
+                      "and, with v = 0, from the identity on a second stream), seg_combine, seg_correct",
+           "segments": {"n": G, "first_tokens": first, "tokens_each_later": seg},
+           "workspace_bytes": ws.numel(),
+           "plain": {"kernel": "kda_prefill_tc, one cluster per head", "clusters": Bl * Hl,
+                     "value": Bl * Tl / (ms_plain / 1e3), "ms_per_step": ms_plain, "achieved_gbs": gbs_plain,
+                     "frac": gbs_plain / peaks["hbm_gbs"]}}
+    del q, k, v, a, b, o, sT, ws
     if with_cpu:
         res["cpu_baseline"] = oracle_tokens_per_s(
             x, lambda Ts: ([t[:, :Ts] for t in x.tensors()], {"initial_state": x.initial_state}, Ts),

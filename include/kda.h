@@ -19,8 +19,9 @@
  *    aligned (kda_prefill_host and kda_prefill_fp8_host alone take host
  *    buffers). The caller owns every buffer; the library allocates nothing,
  *    never synchronises the stream, and launches all its work on `stream`
- *    (the two host-buffer calls also use two copy streams of their own,
- *    joined back into `stream`).
+ *    (the two host-buffer calls also use two copy streams of their own, and
+ *    kda_prefill_segmented three streams of its own, all joined back into
+ *    `stream`).
  *  - Layouts: q, k, alpha [.., T, H, d_k]; v, o [.., T, H, d_v]; beta [.., T, H];
  *    states [N, H, d_k, d_v] with d_v fastest. alpha and beta are float32;
  *    q, k, v and o share `qkv_dtype`; states are float32.
@@ -143,6 +144,55 @@ size_t kda_prefill_workspace_bytes(int B, int T, int H, int d_k, int d_v);
 
 /* Workspace bytes kda_varlen_prefill needs for N sequences (0 < result). */
 size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
+
+/*
+ * kda_prefill_segmented - kda_prefill of ONE long sequence (B = 1) with its
+ * token axis cut into segments that run at the same time, for sequences far
+ * longer than the batch is wide (few heads leave most of the GPU idle while
+ * each head walks its chunks in order).
+ *
+ * The update is an affine map of the state, S_t = A_t S_{t-1} + B_t (K3
+ * essay §六), with the transition from token j to t the product A_t..A_{j+1}
+ * (§五). Over a segment, S_end = Phi S_start + b. Segment 0 runs from
+ * initial_state; each later segment runs once from zero (its outputs and b)
+ * and once with v = 0 from the identity (its outputs z_t = Phi_t^T q_t and
+ * Phi), all at once; then S_start of every segment follows in float32 and
+ * o_t += S_start^T z_t corrects the later segments' outputs (bf16 operands,
+ * float32 accumulation). Every segment boundary is a multiple of 64 tokens.
+ *
+ *   q, k, v, alpha, beta, initial_state, o, final_state: as kda_prefill, B = 1
+ *                (final_state may equal initial_state).
+ *   segments     0: the library's plan (no split when it would not pay, e.g.
+ *                more than 38 heads, or a short sequence); 1: no split (a
+ *                plain kda_prefill); >= 2: that many segments (fewer when the
+ *                sequence has too few chunks).
+ *   workspace    device scratch of kda_prefill_segmented_workspace_bytes(...)
+ *                bytes (0 when there is no split; then it may be NULL),
+ *                256-byte aligned; contents on entry do not matter. About
+ *                0.5 KB per token-head of the later segments. Calls sharing a
+ *                workspace must not overlap.
+ * Results agree with kda_prefill within the bf16 tolerance of the tensor-core
+ * path; they are not bitwise equal to it (the later segments' outputs are
+ * rounded to bf16 once before the correction and once after).
+ * A split needs bf16 q/k/v and d_k = d_v = 128 (KDA_ERR_UNSUPPORTED for
+ * segments >= 2 otherwise; segments = 0 then runs kda_prefill). Streams: the
+ * segments run on three streams of the library's own (created once per
+ * device), forked from and joined back into `stream`.
+ */
+kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                   const float *alpha, const float *beta, const float *initial_state, void *o,
+                                   float *final_state, int B, int T, int H, int d_k, int d_v, int segments,
+                                   void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Workspace bytes of kda_prefill_segmented for these arguments. */
+size_t kda_prefill_segmented_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,
+                                             int segments);
+
+/* The split kda_prefill_segmented makes for these arguments: the number of
+ * segments, the tokens of segment 0 and of each later segment (the last one
+ * ends at T). No split: *n_segments = 1, *first_tokens = T. */
+kda_status_t kda_prefill_segment_plan(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype, int segments,
+                                      int *n_segments, int *first_tokens, int *segment_tokens);
 
 /*
  * kda_varlen_prefill_noalloc - kda_varlen_prefill without a workspace, for

@@ -30,6 +30,7 @@ EXPORTS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_gate", "kda_prefill_fp8
            "kda_prefill_host_workspace_bytes", "kda_prefill_fp8_host", "kda_prefill_fp8_host_workspace_bytes",
            "kda_varlen_prefill", "kda_varlen_prefill_slots",
            "kda_varlen_prefill_noalloc", "kda_varlen_workspace_bytes", "kda_prefill_workspace_bytes",
+           "kda_prefill_segmented", "kda_prefill_segmented_workspace_bytes", "kda_prefill_segment_plan",
            "kda_decode_step", "kda_decode_step_slots", "kda_selftest_bounded_wait",
            "kda_prefill_backward", "kda_prefill_backward_gate", "kda_prefill_backward_workspace_bytes",
            "kda_varlen_prefill_backward", "kda_varlen_prefill_backward_workspace_bytes",
@@ -107,6 +108,14 @@ def load(path: str | None = None):
         lib.kda_varlen_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.kda_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.kda_prefill_segmented.restype = i
+        lib.kda_prefill_segmented.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp,
+                                              ctypes.c_size_t, vp]
+        lib.kda_prefill_segmented_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_prefill_segmented_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.kda_prefill_segment_plan.restype = i
+        lib.kda_prefill_segment_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int),
+                                                 ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
         lib.kda_abi_version.restype = ctypes.c_int
@@ -336,6 +345,59 @@ def prefill(q, k, v, alpha, beta, initial_state=None, *, output_final_state: boo
     st = lib.kda_prefill_gate(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate], _ptr(beta),
                               _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
                               ALGOS[algo], _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def segment_plan(T: int, H: int, dk: int = 128, dv: int = 128, dtype=torch.bfloat16, segments: int = 0,
+                 B: int = 1):
+    """The split ``prefill_segmented`` makes: (segments, tokens of segment 0,
+    tokens of each later segment)."""
+    lib = load()
+    g, f, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    _check(lib, lib.kda_prefill_segment_plan(B, T, H, dk, dv, code, segments, ctypes.byref(g), ctypes.byref(f),
+                                             ctypes.byref(n)))
+    return g.value, f.value, n.value
+
+
+def prefill_segmented_workspace_bytes(T: int, H: int, dk: int = 128, dv: int = 128, dtype=torch.bfloat16,
+                                      segments: int = 0, B: int = 1) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(load().kda_prefill_segmented_workspace_bytes(B, T, H, dk, dv, code, segments))
+
+
+def prefill_segmented(q, k, v, alpha, beta, initial_state=None, *, segments: int = 0,
+                      output_final_state: bool = True, out=None, final_state=None, workspace=None, stream=None):
+    """Prefill of one long sequence with its token axis cut into segments that
+    run at the same time (kda_prefill_segmented). Arguments as ``prefill``
+    with B = 1 and the per-channel gate; ``segments`` = 0 lets the library
+    plan the split, 1 runs the plain prefill, >= 2 forces that many."""
+    lib = load()
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(alpha, "alpha", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or alpha.shape != q.shape or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch among q, k, v, alpha, beta")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev)
+        if initial_state.shape != (B, H, dk, dv):
+            raise ValueError(f"initial_state must be {(B, H, dk, dv)}")
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    nbytes = int(lib.kda_prefill_segmented_workspace_bytes(B, T, H, dk, dv, _dtype_code(q), segments))
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_prefill_segmented(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
+                                   _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
+                                   int(segments), _ptr(workspace), wsize, _stream(stream))
     _check(lib, st)
     return out, final_state
 

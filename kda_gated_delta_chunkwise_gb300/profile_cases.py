@@ -10,6 +10,7 @@ CASE is one of:
   decode_256x32       the decode workload (256 sequences x 32 heads, d=128)
   decode_64x32        a quarter of it, for full ncu captures
   long_131k           one 131,072-token sequence with 32 heads (d=128, bf16)
+  long_131k_segmented the same through kda_prefill_segmented (the library's plan)
   varlen_64seq        the packed batch of 64 lognormal-length sequences
   varlen_64seq_1m     the same lengths scaled to 2^20 tokens
   backward_4x16x4096  the gradients of the benchmark workload (kda_prefill_backward)
@@ -77,6 +78,19 @@ def _long(reps: int):
     s = torch.empty_like(s0)
     for _ in range(reps):
         kda.prefill(q, k, v, a, b, s0, out=o, final_state=s)
+    torch.cuda.synchronize()
+
+
+def _long_segmented(reps: int):
+    dev = torch.device("cuda")
+    x = W.prefill_long_131k()
+    q, k, v, a, b, s0 = (t.to(dev) for t in (*x.tensors(), x.initial_state))
+    o = torch.empty_like(v)
+    s = torch.empty_like(s0)
+    T, H = q.shape[1], q.shape[2]
+    ws = torch.empty(kda.prefill_segmented_workspace_bytes(T, H), dtype=torch.uint8, device=dev)
+    for _ in range(reps):
+        kda.prefill_segmented(q, k, v, a, b, s0, out=o, final_state=s, workspace=ws)
     torch.cuda.synchronize()
 
 
@@ -158,6 +172,7 @@ CASES = {
     "decode_256x32": lambda r: _decode(256, r),
     "decode_64x32": lambda r: _decode(64, r),
     "long_131k": _long,
+    "long_131k_segmented": _long_segmented,
     "varlen_64seq": lambda r: _varlen(W.varlen_64seq(), r),
     "varlen_64seq_1m": lambda r: _varlen(W.varlen_64seq_1m(), r),
     "hostlink": _hostlink,

@@ -288,3 +288,70 @@ def test_backward_argument_checks(lib):
     z = list(args)
     z[15] = 0
     assert lib.kda_prefill_backward(*z, None, 0, None) == 0
+
+
+def _plan(lib, B, T, H, dk=128, dv=128, dtype=1, segments=0):
+    g, f, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.kda_prefill_segment_plan(B, T, H, dk, dv, dtype, segments, ctypes.byref(g), ctypes.byref(f),
+                                      ctypes.byref(n))
+    return st, g.value, f.value, n.value
+
+
+def test_segment_plan(lib):
+    # the long-context workload (2048 chunks, 32 heads): segment 0 runs alone
+    # on 32 of the 76 cluster slots while the 4 later segments run twice
+    # (local, then transition) on the other 44, each launch in 3 waves (w = 6)
+    # with a start-up of 16 chunk steps per wave
+    st, G, first, seg = _plan(lib, 1, 131072, 32)
+    assert (st, G) == (0, 5)
+    assert seg == ((2048 + 16 - 6 * 16) // (6 + 4)) * 64 and first == 131072 - 4 * seg
+    # fewer heads leave room for more segments; every plan covers T
+    for T, H in ((131072, 16), (131072, 1), (4096, 16), (100_000, 8), (65 * 64 + 5, 4)):
+        st, G, first, seg = _plan(lib, 1, T, H)
+        assert st == 0 and G >= 1
+        if G > 1:
+            assert first % 64 == 0 and seg % 64 == 0
+            assert first + (G - 2) * seg < T <= first + (G - 1) * seg
+            assert seg >= 8 * 64 and first >= seg
+    # no split where it cannot pay or cannot run
+    assert _plan(lib, 1, 131072, 39)[1] == 1          # more than 38 heads
+    assert _plan(lib, 1, 64 * 9, 32)[1] == 1          # too short
+    assert _plan(lib, 2, 131072, 8)[1] == 1           # a batch
+    assert _plan(lib, 1, 131072, 8, dtype=0)[1] == 1  # fp32 inputs
+    assert _plan(lib, 1, 131072, 8, dk=64)[1] == 1
+    assert _plan(lib, 1, 131072, 8, segments=1)[1:] == (1, 131072, 0)
+    # forced splits
+    assert _plan(lib, 1, 1000, 2, segments=3) == (0, 3, 512, 256)
+    assert _plan(lib, 1, 130, 2, segments=8) == (0, 2, 128, 64)  # three chunks: the last segment has 2 tokens
+    assert _plan(lib, 1, 1000, 2, dtype=0, segments=2)[0] == 2
+    assert _plan(lib, 2, 1000, 2, segments=2)[0] == 2
+
+
+def test_segmented_workspace_and_argument_checks(lib):
+    T, H = 131072, 32
+    _, G, first, seg = _plan(lib, 1, T, H)
+    T1 = T - first
+    mat = 128 * 128
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    want = (up(4 * G) + up(lib.kda_varlen_workspace_bytes(G - 1, H, 128, 128)) + up(4 * H * mat)
+            + 3 * up(4 * (G - 1) * H * mat) + up(2 * (G - 1) * H * mat) + 2 * up(2 * T1 * H * 128))
+    assert lib.kda_prefill_segmented_workspace_bytes(1, T, H, 128, 128, 1, 0) == want
+    assert lib.kda_prefill_segmented_workspace_bytes(1, T, 39, 128, 128, 1, 0) == 0  # no split
+    p = ctypes.c_void_p(0x1000)
+    args = [p, p, p, 1, p, p, None, p, None, 1, 1000, 2, 128, 128, 3]
+    ws = lib.kda_prefill_segmented_workspace_bytes(1, 1000, 2, 128, 128, 1, 3)
+    assert lib.kda_prefill_segmented(*args, None, 0, None) == 5                     # no workspace
+    assert lib.kda_prefill_segmented(*args, ctypes.c_void_p(0x1010), ws, None) == 5  # misaligned
+    assert lib.kda_prefill_segmented(*args, p, ws - 1, None) == 5                    # too small
+    bad = list(args)
+    bad[0] = None
+    assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
+    bad = list(args)
+    bad[5] = ctypes.c_void_p(0x1002)                                                 # beta
+    assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
+    bad = list(args)
+    bad[3] = 0                                                                       # fp32, forced split
+    assert lib.kda_prefill_segmented(*bad, p, ws, None) == 2

@@ -72,14 +72,20 @@ def test_prefill_long_131k_full(kda):
     the key channels), S0 ~ N(0, 0.01^2), in the benchmark's launch (all 32
     heads in one call): every output against the oracle, which runs 16 heads
     at a time; rel-L2 and max-abs over the whole o and the whole final
-    state."""
+    state.
+    The same launch through kda_prefill_segmented (the library's plan: the
+    sequence cut into five segments that run at once) is checked the same way.
+    """
     x = W.prefill_long_131k()
     q, k, v, a, b, s0 = _dev(x)
     o, s = kda.prefill(q, k, v, a, b, s0)
+    o2, s2 = kda.prefill_segmented(q, k, v, a, b, s0)
     torch.cuda.synchronize()
+    assert kda.segment_plan(x.q.shape[1], x.q.shape[2])[0] == 5
     del q, k, v, a, b
-    o, s = o.cpu(), s.cpu()
+    o, s, o2, s2 = o.cpu(), s.cpu(), o2.cpu(), s2.cpu()
     eo, es = ErrAccum("o"), ErrAccum("final_state")
+    eo2, es2 = ErrAccum("o (segmented)"), ErrAccum("final_state (segmented)")
     qc, kc, vc, ac, bc = x.tensors()
     for h0 in range(0, x.q.shape[2], 16):
         hs = slice(h0, h0 + 16)
@@ -87,9 +93,11 @@ def test_prefill_long_131k_full(kda):
                             initial_state=x.initial_state[:, hs])
         eo.add(o[:, :, hs], ro)
         es.add(s[:, hs], rs)
+        eo2.add(o2[:, :, hs], ro)
+        es2.add(s2[:, hs], rs)
         del ro, rs
-    eo.check(tol_for(x.q.dtype))
-    es.check(tol_for(x.q.dtype))
+    for acc in (eo, es, eo2, es2):
+        acc.check(tol_for(x.q.dtype))
 
 
 def test_strong_decay_and_zero_gates(kda):

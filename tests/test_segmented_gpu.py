@@ -1,0 +1,127 @@
+"""GPU parity of kda_prefill_segmented (one long sequence cut into segments
+that run at once, joined through the segments' transition products) against
+the float64 oracle, on every output and the final state."""
+import pytest
+import torch
+
+import oracle
+from kda_gated_delta_chunkwise_gb300 import workloads as W
+from _parity import TOL_BF16, assert_close, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(x: W.Inputs):
+    d = torch.device("cuda")
+    s0 = None if x.initial_state is None else x.initial_state.to(d)
+    return [t.to(d) for t in x.tensors()] + [s0]
+
+
+def _oracle(x: W.Inputs):
+    return oracle.run(*x.tensors(), initial_state=x.initial_state)
+
+
+def _check_split(kda, x: W.Inputs, segments, want_segments=None):
+    q, k, v, a, b, s0 = _dev(x)
+    o, s = kda.prefill_segmented(q, k, v, a, b, s0, segments=segments)
+    torch.cuda.synchronize()
+    assert kda.device_errors() == 0
+    G, first, seg = kda.segment_plan(x.q.shape[1], x.q.shape[2], segments=segments)
+    if want_segments is not None:
+        assert G == want_segments
+    ro, rs = _oracle(x)
+    assert_close("o", o.cpu(), ro, TOL_BF16)
+    assert_close("final_state", s.cpu(), rs, TOL_BF16)
+    # against the unsplit tensor-core prefill: the same bf16 error budget
+    o1, s1 = kda.prefill(q, k, v, a, b, s0, algo="tc")
+    assert_close("o vs prefill", o, o1, TOL_BF16)
+    assert_close("S vs prefill", s, s1, TOL_BF16)
+    return o, s, (G, first, seg), (ro, rs)
+
+
+@pytest.mark.parametrize("T,H,segments,s0", [(1000, 2, 2, True), (1000, 2, 3, False), (4133, 3, 5, True),
+                                             (130, 2, 8, True), (64 * 40, 4, 16, True)])
+def test_forced_splits(kda, T, H, segments, s0):
+    """Forced splits over several chunks and a ragged tail, segments of one
+    chunk included; with and without an initial state."""
+    x = W.batched(1, T, H, dtype="bf16", alpha_scale=0.1, s0_std=0.05 if s0 else None, seed=T + segments)
+    _, _, (G, first, seg), _ = _check_split(kda, x, segments)
+    assert G >= 2 and first + (G - 2) * seg < T <= first + (G - 1) * seg
+
+
+def test_long_memory_carries_across_segments(kda):
+    """Slow gates (alpha ~ 0.999) and weak writes (beta / 20) keep the state of
+    one segment alive through the next ones, so the correction carries most
+    of the later segments' outputs: a later segment run alone from zero is far
+    from the oracle, the split is not."""
+    x = W.batched(1, 3000, 2, dtype="bf16", alpha_scale=1e-3, s0_std=0.5, seed=77)
+    x.beta.mul_(0.05)
+    _, _, (G, first, seg), (ro, _) = _check_split(kda, x, 4, want_segments=4)
+    q, k, v, a, b, _ = _dev(x)
+    sl = slice(first, first + seg)
+    alone, _ = kda.prefill(q[:, sl].contiguous(), k[:, sl].contiguous(), v[:, sl].contiguous(),
+                           a[:, sl].contiguous(), b[:, sl].contiguous(), None)
+    assert rel_l2(alone.cpu(), ro[:, sl]) > 0.2
+
+
+def test_strong_decay_across_segment_boundaries(kda):
+    """Token-by-token chunks (alpha = 0, e^-138 channels, e^-103 chunks) in
+    segment 0, at a segment boundary and inside later segments."""
+    x = W.batched(1, 1500, 2, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=15)
+    G, first, seg = kda.segment_plan(1500, 2, segments=3)
+    x.alpha[0, 10, 0, :] = 0.0
+    x.alpha[0, first - 3:first + 20, 1, 5] = 1e-3
+    x.alpha[0, first + seg:first + seg + 64, 1, :64] = 0.2
+    x.alpha[0, first + seg + 100, :, :] = 0.0
+    _check_split(kda, x, 3, want_segments=3)
+
+
+def test_automatic_plan_1x16x16384(kda):
+    """The library's own plan on a 16-head sequence of 16,384 tokens."""
+    x = W.batched(1, 16384, 16, dtype="bf16", alpha_scale=W.split_scales(128), s0_std=0.01, seed=3)
+    G, _, _ = kda.segment_plan(16384, 16)
+    assert G >= 2
+    _check_split(kda, x, 0, want_segments=G)
+
+
+def test_in_place_state_optional_outputs_and_repeat(kda):
+    x = W.batched(1, 2000, 2, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=31)
+    q, k, v, a, b, s0 = _dev(x)
+    o_ref, s_ref = kda.prefill_segmented(q, k, v, a, b, s0, segments=3)
+    o2, s2 = kda.prefill_segmented(q, k, v, a, b, s0, segments=3)
+    torch.testing.assert_close(o2, o_ref, rtol=0, atol=0)          # two calls, the same bits
+    torch.testing.assert_close(s2, s_ref, rtol=0, atol=0)
+    st = s0.clone()
+    o3, s3 = kda.prefill_segmented(q, k, v, a, b, st, segments=3, final_state=st)
+    assert s3.data_ptr() == st.data_ptr()
+    torch.testing.assert_close(st, s_ref, rtol=0, atol=0)
+    torch.testing.assert_close(o3, o_ref, rtol=0, atol=0)
+    o4, s4 = kda.prefill_segmented(q, k, v, a, b, s0, segments=3, output_final_state=False)
+    assert s4 is None
+    torch.testing.assert_close(o4, o_ref, rtol=0, atol=0)
+    o5, s5 = kda.prefill_segmented(q, k, v, a, b, None, segments=3)
+    o6, s6 = kda.prefill_segmented(q, k, v, a, b, torch.zeros_like(s0), segments=3)
+    torch.testing.assert_close(o5, o6, rtol=0, atol=0)
+    torch.testing.assert_close(s5, s6, rtol=0, atol=0)
+    torch.cuda.synchronize()
+    assert kda.device_errors() == 0
+
+
+def test_no_split_is_the_plain_prefill(kda):
+    """segments = 1, and configurations the split does not take (fp32 inputs,
+    d = 64, more than 38 heads under the automatic plan), are kda_prefill
+    bit for bit."""
+    for x, segs in ((W.batched(1, 700, 2, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=1), 1),
+                    (W.batched(1, 700, 2, dtype="fp32", alpha_scale=0.1, s0_std=0.05, seed=2), 0),
+                    (W.batched(1, 700, 2, 64, 64, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=3), 0),
+                    (W.batched(1, 1024, 40, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=4), 0)):
+        q, k, v, a, b, s0 = _dev(x)
+        assert kda.segment_plan(x.q.shape[1], x.q.shape[2], x.q.shape[3], x.v.shape[3], q.dtype, segs)[0] == 1
+        o, s = kda.prefill_segmented(q, k, v, a, b, s0, segments=segs)
+        o1, s1 = kda.prefill(q, k, v, a, b, s0)
+        torch.testing.assert_close(o, o1, rtol=0, atol=0)
+        torch.testing.assert_close(s, s1, rtol=0, atol=0)
+    with pytest.raises(kda.KdaError):
+        x = W.batched(1, 700, 2, dtype="fp32", alpha_scale=0.1, seed=5)
+        q, k, v, a, b, _ = _dev(x)
+        kda.prefill_segmented(q, k, v, a, b, None, segments=2)
