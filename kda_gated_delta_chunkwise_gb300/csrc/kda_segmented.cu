@@ -206,10 +206,11 @@ seg_combine_kernel(const float *__restrict__ fs0, const float *__restrict__ fs1,
         for (int c = 0; c < 8; ++c) final_state[(size_t)h * mat + (size_t)i * kD + j0 + jh + c] = acc[c];
 }
 
-constexpr int kCorrWarps = 8;
+constexpr int kCorrWarps = 4;
 constexpr int kCorrRows = 512;           // token rows of one segment per CTA
-constexpr int kLd = kD + 8;              // padded bf16 row (272 bytes: ldmatrix rows hit distinct banks)
-constexpr size_t kCorrSmem = (size_t)(kD + kCorrWarps * 2 * 16) * kLd * sizeof(__nv_bfloat16);
+constexpr int kLd = kD + 8;              // padded bf16 row (272 bytes: ldmatrix rows and fragment reads hit distinct banks)
+constexpr int kStrip = 16 * kLd;         // one 16-row strip of z or o in shared memory
+constexpr size_t kCorrSmem = (size_t)(kD * kLd + kCorrWarps * 4 * kStrip) * sizeof(__nv_bfloat16);
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -236,12 +237,14 @@ __device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1
 // o_t += S_start,g^T z_t for the tokens of segments 1..G-1: per head a
 // [rows x 128] x [128 x 128] product. CTA (x, g - 1, h) takes rows
 // [x * kCorrRows, +kCorrRows) of segment g and holds S_start,g^T in shared
-// memory; each warp takes 16-row strips, the next strip's z rows copied in
-// (cp.async) while the current one is multiplied; the products accumulate in
-// float32 onto the strip's o values, rounded to bf16 once at the end. Segments start at multiples of 64 tokens, so a
-// strip never spans two. Rows past the segment are neither copied nor stored
-// (each output row depends on its own z row only).
-__global__ void __launch_bounds__(kCorrWarps * 32, 2)
+// memory; each warp takes 16-row strips. The z and o rows of the next strip
+// are copied in (cp.async, 16 bytes a lane) while the current strip is
+// multiplied; the products accumulate in float32 onto o, are rounded to bf16
+// once, and leave through shared memory as 16-byte stores. Segments start at
+// multiples of 64 tokens, so a strip never spans two. Rows past the segment
+// are neither copied nor stored (each output row depends on its own z row
+// only).
+__global__ void __launch_bounds__(kCorrWarps * 32)
 seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__restrict__ sst,
                    __nv_bfloat16 *__restrict__ o, int H, int len_tokens, int T1) {
     extern __shared__ __align__(16) unsigned char corr_smem[];
@@ -253,8 +256,10 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
     if (row_lo >= seg_hi) return;
     const int row_hi = min(seg_hi, row_lo + kCorrRows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-    __nv_bfloat16 *Zs = Bs + kD * kLd + warp * 2 * 16 * kLd;  // this warp's two 16-row buffers
-    const size_t row_stride = (size_t)H * kD;                 // elements from one token to the next
+    // this warp's buffers: z strips [2], o strips [2]
+    __nv_bfloat16 *Zs = Bs + kD * kLd + warp * 4 * kStrip;
+    __nv_bfloat16 *Os = Zs + 2 * kStrip;
+    const size_t row_stride = (size_t)H * kD;  // elements from one token to the next
     const __nv_bfloat16 *zh = z + (size_t)h * kD;
     __nv_bfloat16 *oh = o + (size_t)h * kD;
 
@@ -265,16 +270,19 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
     }
     cp_commit();
 
-    const int first = row_lo + warp * 16;
     auto issue = [&](int r0, int buf) {
-        __nv_bfloat16 *dst = Zs + buf * 16 * kLd;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int c = lane + 32 * j, r = c >> 4, c8 = (c & 15) * 8;
-            if (r0 + r < row_hi) cp16(dst + r * kLd + c8, zh + (size_t)(r0 + r) * row_stride + c8);
+            if (r0 + r < row_hi) {
+                const size_t at = (size_t)(r0 + r) * row_stride + c8;
+                cp16(Zs + buf * kStrip + r * kLd + c8, zh + at);
+                cp16(Os + buf * kStrip + r * kLd + c8, oh + at);
+            }
         }
         cp_commit();
     };
+    const int first = row_lo + warp * 16;
     if (first < row_hi) issue(first, 0);
     else cp_commit();
     cp_wait1();  // S_start^T landed (this thread's part)
@@ -285,27 +293,22 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
         const int rn = r0 + kCorrWarps * 16;
         if (rn < row_hi) issue(rn, buf ^ 1);
         else cp_commit();
-        const int ra = r0 + gq, rb = ra + 8;
-        const bool va = ra < row_hi, vb = rb < row_hi;
-        // the accumulators start from o (loaded before the products need them)
+        cp_wait1();
+        __syncwarp();
+        __nv_bfloat16 *ob = Os + buf * kStrip;
+        // the accumulators start from o
         float acc[16][4];
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int c = nt * 8 + 2 * tq;
-            const float2 fa = va ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
-                                       oh + (size_t)ra * row_stride + c))
-                                 : make_float2(0.f, 0.f);
-            const float2 fb = vb ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
-                                       oh + (size_t)rb * row_stride + c))
-                                 : make_float2(0.f, 0.f);
+            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + gq * kLd + c));
+            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + (gq + 8) * kLd + c));
             acc[nt][0] = fa.x;
             acc[nt][1] = fa.y;
             acc[nt][2] = fb.x;
             acc[nt][3] = fb.y;
         }
-        cp_wait1();
-        __syncwarp();
-        const __nv_bfloat16 *za = Zs + buf * 16 * kLd + (lane & 15) * kLd + (lane >> 4) * 8;
+        const __nv_bfloat16 *za = Zs + buf * kStrip + (lane & 15) * kLd + (lane >> 4) * 8;
         const __nv_bfloat16 *bb = Bs + ((lane >> 4) * 8 + (lane & 7)) * kLd + ((lane >> 3) & 1) * 8;
 #pragma unroll 1
         for (int ks = 0; ks < kD / 16; ++ks) {
@@ -319,17 +322,22 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
                 mma_bf16_16816(acc[2 * np + 1], a, b[2], b[3]);
             }
         }
-        __syncwarp();  // the buffer is refilled two strips on
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int c = nt * 8 + 2 * tq;
-            if (va)
-                *reinterpret_cast<__nv_bfloat162 *>(oh + (size_t)ra * row_stride + c) =
-                    __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
-            if (vb)
-                *reinterpret_cast<__nv_bfloat162 *>(oh + (size_t)rb * row_stride + c) =
-                    __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
+            *reinterpret_cast<__nv_bfloat162 *>(ob + gq * kLd + c) = __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<__nv_bfloat162 *>(ob + (gq + 8) * kLd + c) =
+                __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
         }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = lane + 32 * j, r = c >> 4, c8 = (c & 15) * 8;
+            if (r0 + r < row_hi)
+                *reinterpret_cast<uint4 *>(oh + (size_t)(r0 + r) * row_stride + c8) =
+                    *reinterpret_cast<const uint4 *>(ob + r * kLd + c8);
+        }
+        __syncwarp();  // both buffers of this strip are refilled two strips on
     }
 }
 
