@@ -20,7 +20,9 @@ Prints ONE JSON line (rank 0). Keys beyond the basic contract:
   varlen        packed prefill of 64 lognormal-length sequences (306,055
                 tokens, 16 heads), and varlen_1m: the same lengths scaled to
                 2^20 tokens
-  backward      gradients of the benchmark workload (kda_prefill_backward)
+  backward      gradients of the benchmark workload (kda_prefill_backward);
+                more_workloads: the long-context sequence and the packed
+                64-sequence batch
   gate_variants the benchmark workload with a scalar gate, no gate, FP8 inputs
   clocks        SM clocks and throttle reasons sampled during the timed region
                 (and during about a second of the same steps just before it)
@@ -351,6 +353,43 @@ def bench_backward(kda, W, dev, stream, peaks, steps, warmup):
     return res
 
 
+def bench_backward_more(kda, W, dev, stream, peaks, steps, warmup):
+    """The backward on the long-context workload (1x32x131072, S0 given) and
+    on the packed 64-sequence batch (306,055 tokens x 16 heads, S0 given), a
+    random d_o each: one call per step, CUDA events."""
+    import torch
+    res = {}
+    for key, x, packed in (("long_context", W.prefill_long_131k(), False),
+                           ("varlen", W.varlen_64seq(), True)):
+        q, k, v, a, b = (t.to(dev) for t in x.tensors())
+        s0 = x.initial_state.to(dev)
+        d_o = torch.randn(v.shape, generator=torch.Generator(device=dev).manual_seed(7), device=dev).to(v.dtype)
+        if packed:
+            cu = x.cu_seqlens.to(dev)
+            N, Tt, H = cu.numel() - 1, q.shape[0], q.shape[1]
+            ws = torch_empty_bytes(kda.load().kda_varlen_prefill_backward_workspace_bytes(N, Tt, H, DK, DV), dev)
+            fn = lambda: kda.varlen_prefill_backward(q, k, v, a, b, d_o, cu, s0, workspace=ws)
+            tokens, n_states = Tt, N * H
+            desc = f"kda_varlen_prefill_backward N={N} sequences, T_total={Tt}, H={H}, d_k={DK} d_v={DV}"
+        else:
+            Bb, Tb, H = q.shape[0], q.shape[1], q.shape[2]
+            ws = torch_empty_bytes(kda.load().kda_prefill_backward_workspace_bytes(Bb, Tb, H, DK, DV), dev)
+            fn = lambda: kda.prefill_backward(q, k, v, a, b, d_o, s0, workspace=ws)
+            tokens, n_states = Bb * Tb, Bb * H
+            desc = f"kda_prefill_backward B={Bb} H={H} T={Tb} d_k={DK} d_v={DV}"
+        ms = time_events(fn, max(3, steps // 4), warmup, stream)
+        # backward_bytes counts one sequence-head state (dS0 written); S0 is read too
+        nbytes = backward_bytes(1, tokens, H, DK, DV) + (n_states - H) * DK * DV * 4 + n_states * DK * DV * 4
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[key] = {"workload": desc + ", bf16 q/k/v/d_o, S0 given, fp32 gradients",
+                    "value": tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": max(3, steps // 4),
+                    "algorithmic_bytes_per_launch": nbytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+                    "workspace_bytes": ws.numel()}
+        del q, k, v, a, b, s0, d_o, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def torch_empty_like(t):
     import torch
     return torch.empty_like(t)
@@ -641,6 +680,9 @@ def main():
     if not args.no_backward:
         torch.cuda.empty_cache()
         backward = bench_backward(kda, W, dev, stream, peaks, args.steps, args.warmup)
+        if not args.no_long:
+            torch.cuda.empty_cache()
+            backward["more_workloads"] = bench_backward_more(kda, W, dev, stream, peaks, args.steps, args.warmup)
     long_ctx = varlen = varlen_1m = None
     with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if not args.no_long:
