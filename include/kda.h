@@ -160,8 +160,9 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * o_t += S_start^T z_t corrects the later segments' outputs (bf16 operands,
  * float32 accumulation). Every segment boundary is a multiple of 64 tokens.
  *
- *   q, k, v, alpha, beta, initial_state, o, final_state: as kda_prefill, B = 1
- *                (final_state may equal initial_state).
+ *   q, k, v, alpha, gate, beta, initial_state, o, final_state: as
+ *                kda_prefill_gate with B = 1 (final_state may equal
+ *                initial_state).
  *   segments     0: the library's plan (no split when it would not pay, e.g.
  *                more than 38 heads, or a short sequence); 1: no split (a
  *                plain kda_prefill); >= 2: that many segments (fewer when the
@@ -180,9 +181,10 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * device), forked from and joined back into `stream`.
  */
 kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                                   const float *alpha, const float *beta, const float *initial_state, void *o,
-                                   float *final_state, int B, int T, int H, int d_k, int d_v, int segments,
-                                   void *workspace, size_t workspace_bytes, kda_stream_t stream);
+                                   const float *alpha, kda_gate_t gate, const float *beta,
+                                   const float *initial_state, void *o, float *final_state, int B, int T, int H,
+                                   int d_k, int d_v, int segments, void *workspace, size_t workspace_bytes,
+                                   kda_stream_t stream);
 
 /* Workspace bytes of kda_prefill_segmented for these arguments. */
 size_t kda_prefill_segmented_workspace_bytes(int B, int T, int H, int d_k, int d_v, kda_dtype_t qkv_dtype,

@@ -109,7 +109,7 @@ def load(path: str | None = None):
         lib.kda_prefill_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.kda_prefill_segmented.restype = i
-        lib.kda_prefill_segmented.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp,
+        lib.kda_prefill_segmented.argtypes = [vp, vp, vp, i, vp, i, vp, vp, vp, vp, i, i, i, i, i, i, vp,
                                               ctypes.c_size_t, vp]
         lib.kda_prefill_segmented_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_prefill_segmented_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
@@ -367,22 +367,22 @@ def prefill_segmented_workspace_bytes(T: int, H: int, dk: int = 128, dv: int = 1
     return int(load().kda_prefill_segmented_workspace_bytes(B, T, H, dk, dv, code, segments))
 
 
-def prefill_segmented(q, k, v, alpha, beta, initial_state=None, *, segments: int = 0,
+def prefill_segmented(q, k, v, alpha, beta, initial_state=None, *, segments: int = 0, gate: str = "channel",
                       output_final_state: bool = True, out=None, final_state=None, workspace=None, stream=None):
     """Prefill of one long sequence with its token axis cut into segments that
     run at the same time (kda_prefill_segmented). Arguments as ``prefill``
-    with B = 1 and the per-channel gate; ``segments`` = 0 lets the library
-    plan the split, 1 runs the plain prefill, >= 2 forces that many."""
+    with B = 1; ``segments`` = 0 lets the library plan the split, 1 runs the
+    plain prefill, >= 2 forces that many."""
     lib = load()
     dev = q.device
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, q.dtype, dev)
-    _need(alpha, "alpha", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape != (B, T, H, dv) or alpha.shape != q.shape or beta.shape != (B, T, H):
-        raise ValueError("shape mismatch among q, k, v, alpha, beta")
+    if k.shape != q.shape or v.shape != (B, T, H, dv) or beta.shape != (B, T, H):
+        raise ValueError("shape mismatch among q, k, v, beta")
+    alpha = _check_gate(gate, alpha, (B, T, H), dk, dev)
     if initial_state is not None:
         _need(initial_state, "initial_state", torch.float32, dev)
         if initial_state.shape != (B, H, dk, dv):
@@ -395,7 +395,7 @@ def prefill_segmented(q, k, v, alpha, beta, initial_state=None, *, segments: int
     if workspace is None and nbytes > 0:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.kda_prefill_segmented(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), _ptr(beta),
+    st = lib.kda_prefill_segmented(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(alpha), GATES[gate], _ptr(beta),
                                    _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, dk, dv,
                                    int(segments), _ptr(workspace), wsize, _stream(stream))
     _check(lib, st)

@@ -265,6 +265,15 @@ kda_status_t varlen_prefill(const void *q, const void *k, const void *v, kda_dty
 
 }  // namespace
 
+kda_status_t kda::varlen_prefill_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                      const float *alpha, int gate, const float *beta, const float *initial_state,
+                                      void *o, float *final_state, const int32_t *cu_seqlens, int N, int T_total,
+                                      int H, int d_k, int d_v, void *workspace, size_t workspace_bytes,
+                                      int32_t *device_status, cudaStream_t s) {
+    return varlen_prefill(q, k, v, qkv_dtype, alpha, gate, beta, initial_state, o, final_state, nullptr, 0,
+                          cu_seqlens, N, T_total, H, d_k, d_v, workspace, workspace_bytes, device_status, s);
+}
+
 extern "C" {
 
 kda_status_t kda_varlen_prefill(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,

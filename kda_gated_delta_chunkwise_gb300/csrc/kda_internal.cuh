@@ -96,6 +96,13 @@ cudaError_t launch_varlen_prep(const int32_t *cu_seqlens, int N, int T_total, in
                                int32_t *counter, int32_t *status, const int32_t *slots, int pool_size,
                                cudaStream_t s);
 
+// kda_varlen_prefill with a gate kind (kda_gate_t) and no slot map.
+kda_status_t varlen_prefill_gate(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
+                                 const float *alpha, int gate, const float *beta, const float *initial_state,
+                                 void *o, float *final_state, const int32_t *cu_seqlens, int N, int T_total, int H,
+                                 int d_k, int d_v, void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                 cudaStream_t s);
+
 // Records `msg` as this thread's last error and returns `st`.
 kda_status_t set_error(kda_status_t st, const char *msg);
 

@@ -394,22 +394,30 @@ size_t kda_prefill_segmented_workspace_bytes(int B, int T, int H, int d_k, int d
 }
 
 kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
-                                   const float *alpha, const float *beta, const float *initial_state, void *o,
-                                   float *final_state, int B, int T, int H, int d_k, int d_v, int segments,
-                                   void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+                                   const float *alpha, kda_gate_t gate, const float *beta,
+                                   const float *initial_state, void *o, float *final_state, int B, int T, int H,
+                                   int d_k, int d_v, int segments, void *workspace, size_t workspace_bytes,
+                                   kda_stream_t stream) {
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_SCALAR && gate != KDA_GATE_NONE)
+        return fail(KDA_ERR_INVALID_ARG, "unknown gate kind %d", (int)gate);
     int G = 1, first = 0, seg = 0;
     kda_status_t st = kda_prefill_segment_plan(B, T, H, d_k, d_v, qkv_dtype, segments, &G, &first, &seg);
     if (st != KDA_OK) return st;
     if (G < 2)
-        return kda_prefill_gate(q, k, v, qkv_dtype, alpha, KDA_GATE_CHANNEL, beta, initial_state, o, final_state,
-                                B, T, H, d_k, d_v, KDA_ALGO_AUTO, stream);
+        return kda_prefill_gate(q, k, v, qkv_dtype, alpha, gate, beta, initial_state, o, final_state, B, T, H, d_k,
+                                d_v, KDA_ALGO_AUTO, stream);
     // the pointer checks of the plain call
-    const void *need16[] = {q, k, v, alpha, o};
-    const char *names[] = {"q", "k", "v", "alpha", "o"};
-    for (int i = 0; i < 5; ++i) {
+    const void *need16[] = {q, k, v, o};
+    const char *names[] = {"q", "k", "v", "o"};
+    for (int i = 0; i < 4; ++i) {
         if (!need16[i]) return fail(KDA_ERR_INVALID_ARG, "%s must not be NULL", names[i]);
         if (reinterpret_cast<uintptr_t>(need16[i]) & 15u)
             return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", names[i]);
+    }
+    if (gate != KDA_GATE_NONE) {
+        if (!alpha) return fail(KDA_ERR_INVALID_ARG, "alpha must not be NULL");
+        if (reinterpret_cast<uintptr_t>(alpha) & (gate == KDA_GATE_CHANNEL ? 15u : 3u))
+            return fail(KDA_ERR_INVALID_ARG, "alpha must be %d-byte aligned", gate == KDA_GATE_CHANNEL ? 16 : 4);
     }
     if (!beta) return fail(KDA_ERR_INVALID_ARG, "beta must not be NULL");
     if (reinterpret_cast<uintptr_t>(beta) & 3u) return fail(KDA_ERR_INVALID_ARG, "beta must be 4-byte aligned");
@@ -446,7 +454,7 @@ kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, 
     const char *k1 = static_cast<const char *>(k) + t1 * row * sizeof(__nv_bfloat16);
     const char *v1 = static_cast<const char *>(v) + t1 * row * sizeof(__nv_bfloat16);
     char *o1 = static_cast<char *>(o) + t1 * row * sizeof(__nv_bfloat16);
-    const float *a1 = alpha + t1 * row;
+    const float *a1 = gate == KDA_GATE_CHANNEL ? alpha + t1 * row : gate == KDA_GATE_SCALAR ? alpha + t1 * H : nullptr;
     const float *b1 = beta + t1 * H;
     const int G1 = G - 1, T1 = (int)L.T1;
 
@@ -464,8 +472,8 @@ kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, 
     if (q_ok(cudaEventRecord(S.fork, s), "event record") && q_ok(cudaStreamWaitEvent(S.hi, S.fork, 0), "wait") &&
         q_ok(cudaStreamWaitEvent(S.a, S.fork, 0), "wait") && q_ok(cudaStreamWaitEvent(S.b, S.fork, 0), "wait")) {
         // segment 0 from the caller's initial state
-        k_ok(kda_prefill_gate(q, k, v, KDA_BF16, alpha, KDA_GATE_CHANNEL, beta, initial_state, o, fs0, 1, first, H,
-                              kD, kD, KDA_ALGO_TC, reinterpret_cast<kda_stream_t>(S.hi)));
+        k_ok(kda_prefill_gate(q, k, v, KDA_BF16, alpha, gate, beta, initial_state, o, fs0, 1, first, H, kD, kD,
+                              KDA_ALGO_TC, reinterpret_cast<kda_stream_t>(S.hi)));
         // the transition runs' v: zeros
         if (st == KDA_OK)
             q_ok(cudaMemsetAsync(zv, 0, (size_t)T1 * row * sizeof(__nv_bfloat16), S.b), "zeroing v");
@@ -481,13 +489,13 @@ kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, 
         void *vlws = ws + L.vlws;
         const size_t vlbytes = kda_varlen_workspace_bytes(G1, H, kD, kD);
         if (st == KDA_OK)
-            k_ok(kda_varlen_prefill(q1, k1, v1, KDA_BF16, a1, b1, nullptr, o1, fs1, cu, G1, T1, H, kD, kD, vlws,
-                                    vlbytes, nullptr, reinterpret_cast<kda_stream_t>(S.a)));
+            k_ok(kda::varlen_prefill_gate(q1, k1, v1, KDA_BF16, a1, gate, b1, nullptr, o1, fs1, cu, G1, T1, H, kD,
+                                          kD, vlws, vlbytes, nullptr, S.a));
         if (st == KDA_OK) q_ok(cudaEventRecord(S.b_done, S.b), "event record");
         if (st == KDA_OK) q_ok(cudaStreamWaitEvent(S.a, S.b_done, 0), "wait");
         if (st == KDA_OK)
-            k_ok(kda_varlen_prefill(q1, k1, zv, KDA_BF16, a1, b1, ident, zz, phi, cu, G1, T1, H, kD, kD, vlws,
-                                    vlbytes, nullptr, reinterpret_cast<kda_stream_t>(S.a)));
+            k_ok(kda::varlen_prefill_gate(q1, k1, zv, KDA_BF16, a1, gate, b1, ident, zz, phi, cu, G1, T1, H, kD,
+                                          kD, vlws, vlbytes, nullptr, S.a));
     }
     // joins (always, so that nothing queued outlives the call's stream order)
     cudaError_t j1 = cudaEventRecord(S.hi_done, S.hi);

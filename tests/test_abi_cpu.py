@@ -341,7 +341,7 @@ def test_segmented_workspace_and_argument_checks(lib):
     assert lib.kda_prefill_segmented_workspace_bytes(1, T, H, 128, 128, 1, 0) == want
     assert lib.kda_prefill_segmented_workspace_bytes(1, T, 39, 128, 128, 1, 0) == 0  # no split
     p = ctypes.c_void_p(0x1000)
-    args = [p, p, p, 1, p, p, None, p, None, 1, 1000, 2, 128, 128, 3]
+    args = [p, p, p, 1, p, 0, p, None, p, None, 1, 1000, 2, 128, 128, 3]
     ws = lib.kda_prefill_segmented_workspace_bytes(1, 1000, 2, 128, 128, 1, 3)
     assert lib.kda_prefill_segmented(*args, None, 0, None) == 5                     # no workspace
     assert lib.kda_prefill_segmented(*args, ctypes.c_void_p(0x1010), ws, None) == 5  # misaligned
@@ -350,8 +350,18 @@ def test_segmented_workspace_and_argument_checks(lib):
     bad[0] = None
     assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
     bad = list(args)
-    bad[5] = ctypes.c_void_p(0x1002)                                                 # beta
+    bad[6] = ctypes.c_void_p(0x1002)                                                 # beta
     assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
     bad = list(args)
     bad[3] = 0                                                                       # fp32, forced split
     assert lib.kda_prefill_segmented(*bad, p, ws, None) == 2
+    bad = list(args)
+    bad[5] = 7                                                                       # gate kind
+    assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
+    bad = list(args)
+    bad[4] = ctypes.c_void_p(0x1004)                                                 # per-channel alpha: 16 bytes
+    assert lib.kda_prefill_segmented(*bad, p, ws, None) == 1
+    bad[5] = 1                                                                       # a scalar gate: 4 bytes do
+    assert lib.kda_prefill_segmented(*bad, None, 0, None) == 5
+    bad[4], bad[5] = None, 2                                                         # no gate: alpha unused
+    assert lib.kda_prefill_segmented(*bad, None, 0, None) == 5

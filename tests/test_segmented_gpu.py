@@ -107,6 +107,26 @@ def test_in_place_state_optional_outputs_and_repeat(kda):
     assert kda.device_errors() == 0
 
 
+@pytest.mark.parametrize("gate", ["scalar", "none"])
+def test_gate_kinds(kda, gate):
+    """A scalar gate (Gated DeltaNet) and no gate (the delta rule) through a
+    forced split: against the oracle on the per-channel gate each stands for,
+    and against the unsplit prefill of the same gate kind."""
+    x = W.batched(1, 2500, 3, dtype="bf16", alpha_scale=0.1, s0_std=0.05, seed=41)
+    lead = tuple(x.beta.shape)
+    a_g = x.alpha[..., 0].contiguous() if gate == "scalar" else None
+    full = torch.from_numpy(oracle.expand_gate(None if a_g is None else a_g.numpy(), gate, lead, 128)).float()
+    ro, rs = oracle.run(x.q, x.k, x.v, full, x.beta, initial_state=x.initial_state)
+    q, k, v, _, b, s0 = _dev(x)
+    ad = None if a_g is None else a_g.cuda()
+    o, s = kda.prefill_segmented(q, k, v, ad, b, s0, segments=4, gate=gate)
+    assert_close("o", o.cpu(), ro, TOL_BF16)
+    assert_close("final_state", s.cpu(), rs, TOL_BF16)
+    o1, s1 = kda.prefill(q, k, v, ad, b, s0, gate=gate, algo="tc")
+    assert_close("o vs prefill", o, o1, TOL_BF16)
+    assert_close("S vs prefill", s, s1, TOL_BF16)
+
+
 def test_no_split_is_the_plain_prefill(kda):
     """segments = 1, and configurations the split does not take (fp32 inputs,
     d = 64, more than 38 heads under the automatic plan), are kda_prefill
