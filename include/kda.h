@@ -165,8 +165,8 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  *                initial_state).
  *   segments     0: the library's plan (no split when it would not pay, e.g.
  *                more than 38 heads, or a short sequence); 1: no split (a
- *                plain kda_prefill); >= 2: that many segments (fewer when the
- *                sequence has too few chunks).
+ *                plain kda_prefill); 2..4096: that many segments (fewer when
+ *                the sequence has too few chunks; H <= 65535).
  *   workspace    device scratch of kda_prefill_segmented_workspace_bytes(...)
  *                bytes (0 when there is no split; then it may be NULL),
  *                256-byte aligned; contents on entry do not matter. About

@@ -42,7 +42,8 @@ namespace {
 constexpr int kC = 64;               // tokens per chunk
 constexpr int kD = 128;              // d_k = d_v of the tensor-core prefill
 constexpr int kResidentClusters = 76; // two-CTA prefill clusters the 152 SMs hold at once
-constexpr int kMaxSegments = 16;
+constexpr int kMaxSegments = 16;     // automatic plans
+constexpr int kMaxForced = 4096;     // a forced count
 constexpr int kMinSegChunks = 8;     // automatic plans: shortest later segment
 // Start-up and drain of one launch wave of the prefill (launch, barrier and
 // TMEM set-up, the first chunk through the gate-solve-chain pipeline, the
@@ -380,6 +381,9 @@ kda_status_t kda_prefill_segment_plan(int B, int T, int H, int d_k, int d_v, kda
         return fail(KDA_ERR_INVALID_ARG, "B, T, segments must be >= 0 and H > 0");
     if (segments > 1 && !splittable(B, d_k, d_v, qkv_dtype))
         return fail(KDA_ERR_UNSUPPORTED, "a split needs B = 1, bf16 q/k/v and d_k = d_v = 128");
+    // (the correction's grid holds the heads in z and the segments in y)
+    if (segments > 1 && (H > 65535 || segments > kMaxForced))
+        return fail(KDA_ERR_UNSUPPORTED, "a split needs H <= 65535 and at most %d segments", kMaxForced);
     const Plan p = make_plan(B, T, H, d_k, d_v, qkv_dtype, segments);
     *n_segments = p.G;
     *first_tokens = p.G > 1 ? p.first * kC : T;

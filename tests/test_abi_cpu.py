@@ -325,6 +325,8 @@ def test_segment_plan(lib):
     assert _plan(lib, 1, 130, 2, segments=8) == (0, 2, 128, 64)  # three chunks: the last segment has 2 tokens
     assert _plan(lib, 1, 1000, 2, dtype=0, segments=2)[0] == 2
     assert _plan(lib, 2, 1000, 2, segments=2)[0] == 2
+    assert _plan(lib, 1, 1000, 2, segments=4097)[0] == 2
+    assert _plan(lib, 1, 1000, 65536, segments=2)[0] == 2
 
 
 def test_segmented_workspace_and_argument_checks(lib):
