@@ -11,6 +11,7 @@ CASE is one of:
   decode_64x32        a quarter of it, for full ncu captures
   long_131k           one 131,072-token sequence with 32 heads (d=128, bf16)
   long_131k_segmented the same through kda_prefill_segmented (the library's plan)
+  long_65k_segmented  half of it (65,536 tokens): small enough for full ncu captures
   varlen_64seq        the packed batch of 64 lognormal-length sequences
   varlen_64seq_1m     the same lengths scaled to 2^20 tokens
   backward_4x16x4096  the gradients of the benchmark workload (kda_prefill_backward)
@@ -81,9 +82,9 @@ def _long(reps: int):
     torch.cuda.synchronize()
 
 
-def _long_segmented(reps: int):
+def _long_segmented(reps: int, T: int = 131072):
     dev = torch.device("cuda")
-    x = W.prefill_long_131k()
+    x = W.prefill_long_131k(T=T)
     q, k, v, a, b, s0 = (t.to(dev) for t in (*x.tensors(), x.initial_state))
     o = torch.empty_like(v)
     s = torch.empty_like(s0)
@@ -173,6 +174,7 @@ CASES = {
     "decode_64x32": lambda r: _decode(64, r),
     "long_131k": _long,
     "long_131k_segmented": _long_segmented,
+    "long_65k_segmented": lambda r: _long_segmented(r, T=65536),
     "varlen_64seq": lambda r: _varlen(W.varlen_64seq(), r),
     "varlen_64seq_1m": lambda r: _varlen(W.varlen_64seq_1m(), r),
     "hostlink": _hostlink,
