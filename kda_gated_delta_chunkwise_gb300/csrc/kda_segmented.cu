@@ -165,53 +165,79 @@ __global__ void seg_setup_kernel(int32_t *__restrict__ cu, int G, int len_tokens
     }
 }
 
-constexpr int kCombCols = 16;            // state columns per combine CTA
 constexpr int kCombThreads = 256;
 constexpr int kPhiLd = kD + 1;           // padded row of Phi in shared memory
-constexpr size_t kCombSmem = (size_t)(kD * kPhiLd + kD * kCombCols) * sizeof(float);
+template <int COLS> constexpr size_t comb_smem() { return (size_t)(2 * kD * kPhiLd + kD * (COLS + 1)) * sizeof(float); }
 
-// Start states of segments 1..G-1 and the final state, 16 state columns of
-// one head per CTA (columns of the state never mix: Phi acts on the left).
-// sst[g - 1][h] receives S_start,g^T in bf16 (row = value column, k fastest):
-// the B operand of the correction's products.
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__device__ __forceinline__ void cp4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+
+// Start states of segments 1..G-1 and the final state, COLS state columns
+// of one head per CTA (columns of the state never mix: Phi acts on the left;
+// 16 columns when that keeps more SMs busy, else 32). Thread (row i, COLS / 2
+// columns); Phi of the next step is copied in (cp.async) while this step
+// multiplies. sst[g - 1][h] receives S_start,g^T in bf16 (row = value
+// column, k fastest): the B operand of the correction's products.
+template <int COLS>
 __global__ void __launch_bounds__(kCombThreads)
 seg_combine_kernel(const float *__restrict__ fs0, const float *__restrict__ fs1, const float *__restrict__ phi,
                    __nv_bfloat16 *__restrict__ sst, float *__restrict__ final_state, int G, int H) {
     extern __shared__ float sm[];
-    float *Ps = sm;                  // [kD][kPhiLd]
-    float *Ss = sm + kD * kPhiLd;    // [kD][kCombCols]
-    const int h = blockIdx.x, j0 = blockIdx.y * kCombCols, tid = threadIdx.x;
-    const int i = tid >> 1, jh = (tid & 1) * 8;  // output row, first of 8 columns
+    float *Ps = sm;                      // [2][kD][kPhiLd]
+    constexpr int NC = COLS / 2, LD = COLS + 1;
+    float *Ss = sm + 2 * kD * kPhiLd;    // [kD][LD]
+    const int h = blockIdx.x, j0 = blockIdx.y * COLS, tid = threadIdx.x;
+    const int i = tid & (kD - 1), jh = (tid >> 7) * NC;  // output row, first of NC columns
     const size_t mat = (size_t)kD * kD;
-    float acc[8];
-    for (int c = 0; c < 8; ++c) acc[c] = fs0[(size_t)h * mat + (size_t)i * kD + j0 + jh + c];
+    auto issue = [&](int g, int buf) {  // Phi of segment g + 1 (phi[g]) into buffer buf
+        const float *src = phi + ((size_t)g * H + h) * mat;
+        float *dst = Ps + buf * kD * kPhiLd;
+        for (int e = tid; e < kD * kD; e += kCombThreads) cp4(dst + (e / kD) * kPhiLd + e % kD, src + e);
+        cp_commit();
+    };
+    float acc[NC];
+    for (int c = 0; c < NC; ++c) acc[c] = fs0[(size_t)h * mat + (size_t)i * kD + j0 + jh + c];
+    if (G > 1) issue(0, 0);
     for (int g = 1; g < G; ++g) {
         const size_t at = ((size_t)(g - 1) * H + h) * mat;
-        // S_start,g: to shared memory (the next product's operand) and, as
-        // bf16, to the correction's operand
-        for (int c = 0; c < 8; ++c) {
-            Ss[i * kCombCols + jh + c] = acc[c];
+        // S_start,g: to shared memory (this step's operand) and, as bf16, to
+        // the correction's operand
+        for (int c = 0; c < NC; ++c) {
+            Ss[i * LD + jh + c] = acc[c];
             sst[at + (size_t)(j0 + jh + c) * kD + i] = __float2bfloat16_rn(acc[c]);
         }
-        for (int e = tid; e < kD * kD; e += kCombThreads) Ps[(e / kD) * kPhiLd + e % kD] = phi[at + e];
+        if (g + 1 < G) issue(g, g & 1);
+        else cp_commit();
+        cp_wait1();  // Phi of this step landed (this thread's part)
         __syncthreads();
-        for (int c = 0; c < 8; ++c) acc[c] = fs1[at + (size_t)i * kD + j0 + jh + c];
+        const float *P = Ps + ((g - 1) & 1) * kD * kPhiLd + i * kPhiLd;
+        for (int c = 0; c < NC; ++c) acc[c] = fs1[at + (size_t)i * kD + j0 + jh + c];
         for (int kk = 0; kk < kD; ++kk) {
-            const float p = Ps[i * kPhiLd + kk];
-            const float *sr = Ss + kk * kCombCols + jh;
-            for (int c = 0; c < 8; ++c) acc[c] = fmaf(p, sr[c], acc[c]);
+            const float p = P[kk];
+            const float *sr = Ss + kk * LD + jh;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[c] = fmaf(p, sr[c], acc[c]);
         }
-        __syncthreads();
+        __syncthreads();  // Ss and this Phi buffer are rewritten next step
     }
     if (final_state)
-        for (int c = 0; c < 8; ++c) final_state[(size_t)h * mat + (size_t)i * kD + j0 + jh + c] = acc[c];
+        for (int c = 0; c < NC; ++c) final_state[(size_t)h * mat + (size_t)i * kD + j0 + jh + c] = acc[c];
 }
 
-constexpr int kCorrWarps = 4;
-constexpr int kCorrRows = 512;           // token rows of one segment per CTA
-constexpr int kLd = kD + 8;              // padded bf16 row (272 bytes: ldmatrix rows and fragment reads hit distinct banks)
-constexpr int kStrip = 16 * kLd;         // one 16-row strip of z or o in shared memory
-constexpr size_t kCorrSmem = (size_t)(kD * kLd + kCorrWarps * 4 * kStrip) * sizeof(__nv_bfloat16);
+constexpr int kCorrWarps = 12;          // one CTA per SM: 12 warps share the S_start tile
+constexpr int kCorrRows = 768;           // token rows of one segment per CTA (4 strips per warp)
+constexpr int kStrip = 16 * kD;          // one 16-row strip of z or o in shared memory (bf16)
+constexpr size_t kCorrSmem = (size_t)(kD * kD + kCorrWarps * 4 * kStrip) * sizeof(__nv_bfloat16);
+
+// Shared-memory tiles of 128 bf16 per row (16 chunks of 16 bytes) store
+// chunk c of row r at chunk c ^ (r & 7): the 8 rows an ldmatrix phase or a
+// fragment read touches then sit in 8 different bank groups.
+__device__ __forceinline__ int swz(int r, int c8) { return r * kD + ((((c8 >> 3) ^ r) & 7) | ((c8 >> 3) & 8)) * 8 + (c8 & 7); }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -232,8 +258,6 @@ __device__ __forceinline__ void cp16(void *dst, const void *src) {
                  "l"(src)
                  : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // o_t += S_start,g^T z_t for the tokens of segments 1..G-1: per head a
 // [rows x 128] x [128 x 128] product. CTA (x, g - 1, h) takes rows
@@ -249,7 +273,7 @@ __global__ void __launch_bounds__(kCorrWarps * 32)
 seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__restrict__ sst,
                    __nv_bfloat16 *__restrict__ o, int H, int len_tokens, int T1) {
     extern __shared__ __align__(16) unsigned char corr_smem[];
-    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(corr_smem);  // [128 value columns][kLd]
+    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(corr_smem);  // [128 value columns][128], swizzled
     const int g1 = blockIdx.y, h = blockIdx.z;
     const int seg_lo = g1 * len_tokens;
     const int seg_hi = min(T1, seg_lo + len_tokens);
@@ -258,7 +282,7 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
     const int row_hi = min(seg_hi, row_lo + kCorrRows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
     // this warp's buffers: z strips [2], o strips [2]
-    __nv_bfloat16 *Zs = Bs + kD * kLd + warp * 4 * kStrip;
+    __nv_bfloat16 *Zs = Bs + kD * kD + warp * 4 * kStrip;
     __nv_bfloat16 *Os = Zs + 2 * kStrip;
     const size_t row_stride = (size_t)H * kD;  // elements from one token to the next
     const __nv_bfloat16 *zh = z + (size_t)h * kD;
@@ -267,7 +291,7 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
     const __nv_bfloat16 *src = sst + ((size_t)g1 * H + h) * kD * kD;
     for (int e = threadIdx.x; e < kD * kD / 8; e += kCorrWarps * 32) {
         const int r = e / (kD / 8), c8 = (e % (kD / 8)) * 8;
-        cp16(&Bs[r * kLd + c8], &src[r * kD + c8]);
+        cp16(&Bs[swz(r, c8)], &src[r * kD + c8]);
     }
     cp_commit();
 
@@ -277,8 +301,8 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
             const int c = lane + 32 * j, r = c >> 4, c8 = (c & 15) * 8;
             if (r0 + r < row_hi) {
                 const size_t at = (size_t)(r0 + r) * row_stride + c8;
-                cp16(Zs + buf * kStrip + r * kLd + c8, zh + at);
-                cp16(Os + buf * kStrip + r * kLd + c8, oh + at);
+                cp16(Zs + buf * kStrip + swz(r, c8), zh + at);
+                cp16(Os + buf * kStrip + swz(r, c8), oh + at);
             }
         }
         cp_commit();
@@ -302,23 +326,24 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int c = nt * 8 + 2 * tq;
-            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + gq * kLd + c));
-            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + (gq + 8) * kLd + c));
+            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + swz(gq, c)));
+            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(ob + swz(gq + 8, c)));
             acc[nt][0] = fa.x;
             acc[nt][1] = fa.y;
             acc[nt][2] = fb.x;
             acc[nt][3] = fb.y;
         }
-        const __nv_bfloat16 *za = Zs + buf * kStrip + (lane & 15) * kLd + (lane >> 4) * 8;
-        const __nv_bfloat16 *bb = Bs + ((lane >> 4) * 8 + (lane & 7)) * kLd + ((lane >> 3) & 1) * 8;
+        const __nv_bfloat16 *zb = Zs + buf * kStrip;
+        const int ar = lane & 15, ak = (lane >> 4) * 8;                         // A: this lane's row, k offset
+        const int br = (lane >> 4) * 8 + (lane & 7), bk = ((lane >> 3) & 1) * 8;  // B: row (value column), k offset
 #pragma unroll 1
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t a[4];
-            ldsm_x4(za + ks * 16, a);
+            ldsm_x4(zb + swz(ar, ks * 16 + ak), a);
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
                 uint32_t b[4];
-                ldsm_x4(bb + np * 16 * kLd + ks * 16, b);
+                ldsm_x4(Bs + swz(np * 16 + br, ks * 16 + bk), b);
                 mma_bf16_16816(acc[2 * np], a, b[0], b[1]);
                 mma_bf16_16816(acc[2 * np + 1], a, b[2], b[3]);
             }
@@ -326,9 +351,8 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int c = nt * 8 + 2 * tq;
-            *reinterpret_cast<__nv_bfloat162 *>(ob + gq * kLd + c) = __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<__nv_bfloat162 *>(ob + (gq + 8) * kLd + c) =
-                __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
+            *reinterpret_cast<__nv_bfloat162 *>(ob + swz(gq, c)) = __floats2bfloat162_rn(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<__nv_bfloat162 *>(ob + swz(gq + 8, c)) = __floats2bfloat162_rn(acc[nt][2], acc[nt][3]);
         }
         __syncwarp();
 #pragma unroll
@@ -336,7 +360,7 @@ seg_correct_kernel(const __nv_bfloat16 *__restrict__ z, const __nv_bfloat16 *__r
             const int c = lane + 32 * j, r = c >> 4, c8 = (c & 15) * 8;
             if (r0 + r < row_hi)
                 *reinterpret_cast<uint4 *>(oh + (size_t)(r0 + r) * row_stride + c8) =
-                    *reinterpret_cast<const uint4 *>(ob + r * kLd + c8);
+                    *reinterpret_cast<const uint4 *>(ob + swz(r, c8));
         }
         __syncwarp();  // both buffers of this strip are refilled two strips on
     }
@@ -513,10 +537,18 @@ kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, 
     q_ok(j3, "join");
     if (st != KDA_OK) return st;
 
-    e = cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
-    if (e != cudaSuccess) return cuda_fail(e, "combine attribute");
-    seg_combine_kernel<<<dim3(H, kD / kCombCols), kCombThreads, kCombSmem, s>>>(fs0, fs1, phi, sst, final_state,
-                                                                                 G, H);
+    {
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "SM count");
+        // one CTA per SM (two Phi buffers): 16 columns per CTA while H x 8 CTAs fit at once
+        const bool narrow = (int64_t)H * (kD / 16) <= sms;
+        auto kern = narrow ? seg_combine_kernel<16> : seg_combine_kernel<32>;
+        const size_t smem = narrow ? comb_smem<16>() : comb_smem<32>();
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e, "combine attribute");
+        kern<<<dim3(H, narrow ? kD / 16 : kD / 32), kCombThreads, smem, s>>>(fs0, fs1, phi, sst, final_state, G, H);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "combine launch");
     e = cudaFuncSetAttribute(seg_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCorrSmem);
     if (e != cudaSuccess) return cuda_fail(e, "correction attribute");
