@@ -178,7 +178,12 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * A split needs bf16 q/k/v and d_k = d_v = 128 (KDA_ERR_UNSUPPORTED for
  * segments >= 2 otherwise; segments = 0 then runs kda_prefill). Streams: the
  * segments run on three streams of the library's own (created once per
- * device), forked from and joined back into `stream`.
+ * device), forked from and joined back into `stream`; the call can be
+ * captured into a CUDA graph. Errors: argument, alignment and workspace
+ * checks return before any launch (KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED,
+ * KDA_ERR_WORKSPACE); if a launch fails midway, `stream` still waits for
+ * everything already queued and the call returns KDA_ERR_CUDA. Calls from
+ * several host threads on one device are serialised while they queue work.
  */
 kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v, kda_dtype_t qkv_dtype,
                                    const float *alpha, kda_gate_t gate, const float *beta,
