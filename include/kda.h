@@ -179,7 +179,8 @@ size_t kda_varlen_workspace_bytes(int N, int H, int d_k, int d_v);
  * segments >= 2 otherwise; segments = 0 then runs kda_prefill). Streams: the
  * segments run on three streams of the library's own (created once per
  * device), forked from and joined back into `stream`; the call can be
- * captured into a CUDA graph. Errors: argument, alignment and workspace
+ * captured into a CUDA graph (make the first split call on a device before
+ * any capture: it creates those streams). Errors: argument, alignment and workspace
  * checks return before any launch (KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED,
  * KDA_ERR_WORKSPACE); if a launch fails midway, `stream` still waits for
  * everything already queued and the call returns KDA_ERR_CUDA. Calls from
